@@ -1,0 +1,123 @@
+"""Seeded synthetic inputs for one layer backward (or a stack of them).
+
+Every tensor comes from its own SplitMix64 stream keyed by
+``(seed, config name, layer, tensor name)``.  The arrays returned are the exact
+values both sides receive: float32 activations, weights in their storage type
+(float32, bfloat16-exact float32, or int8 ternary), float32 scales.
+
+Recipe (distributions follow the workload descriptions):
+  * weights ~ N(0, weight_std^2) (bf16 configs: rounded to bfloat16);
+    ternary weights take 0 with probability 1/3 and +-1 otherwise, with one
+    per-tensor scale ~ U(0.5, 2);
+  * LoRA A ~ N(0, lora_a_std^2), B ~ N(0, lora_b_std^2); AdamW moments zero
+    (first step) or, for the warm case, m ~ N(0, 1e-2^2), v ~ U(0, 1e-4);
+  * RMSNorm gammas ~ U(0.5, 1.5);
+  * cached activations, K/V cache and the upstream gradient ~ N(0, 1);
+  * attention rows: softmax of N(0, attn_logit_std^2) logits over the keys a
+    query may see (key j visible to query i iff j <= L - S + i), zero elsewhere;
+  * the cached SiLU output is silu(gate) and the cached LoRA activations are
+    x @ A^T, both formed in float64 from the values above and then rounded.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .configs import LayerConfig
+from . import rng
+
+
+def _n(seed, cfg, layer, name, shape, std=1.0):
+    n = int(np.prod(shape))
+    return rng.normal(rng.stream_key(seed, cfg.name, layer, name), n, 0.0, std).reshape(shape)
+
+
+def _u(seed, cfg, layer, name, shape, lo, hi):
+    n = int(np.prod(shape))
+    return rng.uniform(rng.stream_key(seed, cfg.name, layer, name), n, lo, hi).reshape(shape)
+
+
+def _weight(seed, cfg, layer, name, shape):
+    """Returns (stored array, scale)."""
+    if cfg.wtype == "ternary":
+        w = rng.ternary(rng.stream_key(seed, cfg.name, layer, name), int(np.prod(shape)))
+        scale = float(np.float32(_u(seed, cfg, layer, name + ".scale", (1,), 0.5, 2.0)[0]))
+        return w.reshape(shape), scale
+    w = _n(seed, cfg, layer, name, shape, cfg.weight_std)
+    if cfg.wtype == "bf16":
+        return rng.round_to_bf16(w), 1.0
+    return w.astype(np.float32), 1.0
+
+
+def attention_rows(seed, cfg: LayerConfig, layer: int) -> np.ndarray:
+    """[n_heads, S, L] float32 rows of a masked softmax of normal logits."""
+    S, L, nh = cfg.seq_len, cfg.cache_len, cfg.n_heads
+    logits = _n(seed, cfg, layer, "attn_logits", (nh, S, L), cfg.attn_logit_std)
+    vis = np.arange(L)[None, :] <= (cfg.pos0 + np.arange(S))[:, None]      # [S, L]
+    logits = np.where(vis[None], logits, -np.inf)
+    logits -= logits.max(axis=-1, keepdims=True)
+    e = np.exp(logits)
+    return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+
+
+def layer_inputs(cfg: LayerConfig, layer: int = 0, seed: int = 0, with_dout: bool = True) -> dict:
+    S, L, H, I = cfg.seq_len, cfg.cache_len, cfg.dim, cfg.ffn_dim
+    qd, kvd, r = cfg.q_dim, cfg.kv_dim, cfg.rank
+    f32 = np.float32
+    d: dict = {}
+    # weights, stored [in, out]
+    d["w_down"], d["s_down"] = _weight(seed, cfg, layer, "w_down", (I, H))
+    d["w_gate"], d["s_gate"] = _weight(seed, cfg, layer, "w_gate", (H, I))
+    d["w_up"], d["s_up"] = _weight(seed, cfg, layer, "w_up", (H, I))
+    d["w_o"], d["s_o"] = _weight(seed, cfg, layer, "w_o", (qd, H))
+    if cfg.sub_norm:
+        d["g_sub_ffn"] = _u(seed, cfg, layer, "g_sub_ffn", (I,), 0.5, 1.5).astype(f32)
+        d["g_sub_attn"] = _u(seed, cfg, layer, "g_sub_attn", (qd,), 0.5, 1.5).astype(f32)
+    if cfg.pre_norm:
+        d["g_ffn"] = _u(seed, cfg, layer, "g_ffn", (H,), 0.5, 1.5).astype(f32)
+    # cached activations
+    d["x"] = _n(seed, cfg, layer, "attn_input", (S, H)).astype(f32)
+    d["gate"] = _n(seed, cfg, layer, "gate", (S, I)).astype(f32)
+    d["up"] = _n(seed, cfg, layer, "up", (S, I)).astype(f32)
+    if cfg.act == "silu_mul" and cfg.use_silu_cache:
+        g = d["gate"].astype(np.float64)
+        d["silu_gate"] = (g / (1.0 + np.exp(-g))).astype(f32)
+    if cfg.sub_norm:
+        d["hidden"] = _n(seed, cfg, layer, "hidden", (S, I)).astype(f32)
+        d["ctx"] = _n(seed, cfg, layer, "context", (S, qd)).astype(f32)
+    if cfg.pre_norm:
+        d["r1"] = _n(seed, cfg, layer, "resid1", (S, H)).astype(f32)
+    kshape = (L, kvd) if cfg.kv_layout == "shd" else (cfg.n_kv_heads, L, cfg.head_dim)
+    d["k"] = _n(seed, cfg, layer, "k_cache", kshape).astype(f32)
+    d["v"] = _n(seed, cfg, layer, "v_cache", kshape).astype(f32)
+    d["attn"] = attention_rows(seed, cfg, layer)
+    # LoRA adapters and their AdamW state
+    d["a_q"] = _n(seed, cfg, layer, "lora_a_q", (r, H), cfg.lora_a_std).astype(f32)
+    d["b_q"] = _n(seed, cfg, layer, "lora_b_q", (qd, r), cfg.lora_b_std).astype(f32)
+    d["a_v"] = _n(seed, cfg, layer, "lora_a_v", (r, H), cfg.lora_a_std).astype(f32)
+    d["b_v"] = _n(seed, cfg, layer, "lora_b_v", (kvd, r), cfg.lora_b_std).astype(f32)
+    for p in ("a_q", "b_q", "a_v", "b_v"):
+        if cfg.adam_state == "warm":
+            d["m_" + p] = _n(seed, cfg, layer, "m_" + p, d[p].shape, 1e-2).astype(f32)
+            d["v_" + p] = _u(seed, cfg, layer, "v_" + p, d[p].shape, 0.0, 1e-4).astype(f32)
+        else:
+            d["m_" + p] = np.zeros_like(d[p])
+            d["v_" + p] = np.zeros_like(d[p])
+    x64 = d["x"].astype(np.float64)
+    d["lora_q_h"] = (x64 @ d["a_q"].astype(np.float64).T).astype(f32)
+    d["lora_v_h"] = (x64 @ d["a_v"].astype(np.float64).T).astype(f32)
+    if with_dout:
+        d["dout"] = _n(seed, cfg, layer, "grad_out", (S, H)).astype(f32)
+    return d
+
+
+def stack_dout(cfg: LayerConfig, seed: int = 0) -> np.ndarray:
+    """Upstream gradient entering the top layer of a stack, [S, H] ~ N(0, 1)."""
+    return _n(seed, cfg, "top", "grad_hidden", (cfg.seq_len, cfg.dim)).astype(np.float32)
+
+
+def vector(seed: int, name: str, n: int, dist: str = "normal") -> np.ndarray:
+    """Float32 vector for standalone kernel cases (``dist``: normal, or 'u01')."""
+    key = rng.stream_key(seed, "vector", name)
+    if dist == "u01":
+        return rng.uniform(key, n).astype(np.float32)
+    return rng.normal(key, n).astype(np.float32)
