@@ -1,0 +1,232 @@
+/*
+ * tlb.h - C ABI of the GB300 (sm_103a) LoRA transformer layer backward.
+ *
+ * One call computes one step (or one whole layer) of the backward pass of a
+ * transformer layer fine-tuned with LoRA adapters on Q and V, and applies the
+ * AdamW step with the LoRA+ learning rate to the adapters.
+ *
+ * Sources of the operations (page and section):
+ *   [FFN] Hesper API, Hesper/Training/FFNBackward ("FFN Backward GPU Kernels"):
+ *         the FFN backward chain, ReLU^2 x Mul backward, executeFFNBackward.
+ *   [ATT] Hesper API, Hesper/Training/AttentionBackward ("Attention Backward GPU
+ *         Kernels"): gradient flow, softmax / score / apply / RoPE / RMSNorm
+ *         backward kernels and their execute* wrappers.
+ *   [RS]  entrenar train/transformer_trainer/wgpu_backward.rs (aprender-train
+ *         0.34.0): cpu_adamw, LayerActivations, backward_through_layers.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers owned by the caller unless stated otherwise;
+ *     tensors are dense, row-major float32 unless stated otherwise.
+ *   - Weights are stored [in, out] (the layout the Rust trainer calls
+ *     "pre-transposed"), so each input gradient is dX = scale * dY @ W^T.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls only enqueue work: they never allocate, free or synchronise (except
+ *     tlb_workspace_status), so a sequence of calls can be captured into a CUDA
+ *     graph.  Scratch memory comes from the caller's workspace `ws` of `ws_bytes`
+ *     bytes (256-byte aligned), sized by tlb_workspace_bytes().
+ *   - Return value: TLB_OK or a negative TLB_E* code; tlb_last_error() gives a
+ *     message (thread-local) for the last failing call of this thread.  Argument
+ *     errors are detected on the host before anything is enqueued.  Errors found
+ *     on the device (a bounded wait that ran out) are recorded in the workspace's
+ *     status word and returned by tlb_workspace_status().
+ *   - Outputs must not alias inputs unless a function says so.
+ */
+#ifndef TLB_H_
+#define TLB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TLB_OK 0
+#define TLB_EINVAL (-1)        /* bad argument: shape, null pointer, alignment */
+#define TLB_EUNSUPPORTED (-2)  /* valid but not implemented (e.g. head_dim > 256) */
+#define TLB_ENONFINITE (-3)    /* reserved: non-finite value detected */
+#define TLB_ETIMEOUT (-4)      /* a device-side bounded wait ran out */
+#define TLB_ECUDA (-5)         /* a CUDA runtime call failed */
+
+/* gated activation of the FFN */
+#define TLB_ACT_RELU2_MUL 0    /* hidden = max(0, gate)^2 * up            [FFN] */
+#define TLB_ACT_SILU_MUL 1     /* hidden = silu(gate) * up (SwiGLU)       [RS]  */
+
+/* weight storage types (all weights of one layer share the type) */
+#define TLB_W_F32 0            /* float32 */
+#define TLB_W_BF16 1           /* bfloat16 (tensor-core path for S > 1) */
+#define TLB_W_TERNARY_I8 2     /* int8 in {-1, 0, +1}; the per-tensor float scale multiplies */
+
+/* composition flags of a layer */
+#define TLB_SUB_NORM 1         /* RMSNorm on the attention context and on the FFN hidden */
+#define TLB_PRE_NORM 2         /* RMSNorm before the FFN; its backward adds into dResidual */
+#define TLB_RESIDUAL 4         /* r1 = x + attn and out = r1 + ffn */
+#define TLB_ROPE 8             /* NeoX split-half rotary embedding on q and k */
+#define TLB_USE_SILU_CACHE 16  /* SwiGLU: read the cached silu(gate) instead of recomputing it */
+#define TLB_CAUSAL 32          /* query row i sees keys j <= L - S + i only; attn is 0 elsewhere */
+
+/* Shapes and constants of one layer. q_dim = n_heads*head_dim, kv_dim = n_kv_heads*head_dim. */
+typedef struct {
+    int32_t dim;          /* hidden size H */
+    int32_t ffn_dim;      /* intermediate size I */
+    int32_t n_heads;
+    int32_t n_kv_heads;   /* divides n_heads; KV head of head h is h / (n_heads / n_kv_heads) */
+    int32_t head_dim;     /* even, <= 256 */
+    int32_t rank;         /* LoRA rank r, 1..64 */
+    float lora_alpha;     /* LoRA scaling s = lora_alpha / rank */
+    float rope_base;      /* theta_d = pos * rope_base^(-2d/head_dim) */
+    float norm_eps;       /* RMSNorm eps: rms = sqrt(mean(x^2) + eps) */
+    float attn_scale;     /* softmax logit scale, normally 1/sqrt(head_dim) */
+    int32_t act;          /* TLB_ACT_* */
+    int32_t wtype;        /* TLB_W_* */
+    int32_t flags;        /* TLB_* flags above */
+} tlb_layer_cfg;
+
+/* One weight matrix stored [in, out] row-major in cfg.wtype, times `scale`. */
+typedef struct {
+    const void *w;
+    float scale;          /* 1 for plain float weights; the BitLinear scale for ternary */
+} tlb_weight;
+
+typedef struct {
+    tlb_weight w_down;              /* [ffn_dim, dim] */
+    tlb_weight w_gate;              /* [dim, ffn_dim] */
+    tlb_weight w_up;                /* [dim, ffn_dim] */
+    tlb_weight w_o;                 /* [q_dim, dim]   */
+    const float *gamma_sub_ffn;     /* [ffn_dim], TLB_SUB_NORM */
+    const float *gamma_ffn;         /* [dim],     TLB_PRE_NORM */
+    const float *gamma_sub_attn;    /* [q_dim],   TLB_SUB_NORM */
+} tlb_layer_weights;
+
+/* Cached forward activations of one layer ([RS] LayerActivations, [FFN]
+ * executeFFNBackward saved buffers).  S query rows sit at positions
+ * L - S .. L - 1 of a cache of L keys. */
+typedef struct {
+    const float *x;          /* attention input (normalised) [S, dim]: LoRA input */
+    const float *gate;       /* [S, ffn_dim] */
+    const float *up;         /* [S, ffn_dim] */
+    const float *silu_gate;  /* [S, ffn_dim], read if TLB_USE_SILU_CACHE */
+    const float *hidden;     /* FFN hidden before the sub-norm [S, ffn_dim], TLB_SUB_NORM */
+    const float *r1;         /* residual stream before the FFN norm [S, dim], TLB_PRE_NORM */
+    const float *ctx;        /* attention context before the sub-norm [S, q_dim], TLB_SUB_NORM */
+    const float *k;          /* K cache (after RoPE): element (kvh, j, d) at        */
+    const float *v;          /*   k[kvh*kv_stride_head + j*kv_stride_pos + d]; V alike */
+    int64_t kv_stride_head;  /* [L, kv_dim] layout: head_dim; [n_kv, L, hd]: L*head_dim */
+    int64_t kv_stride_pos;   /* [L, kv_dim] layout: kv_dim;   [n_kv, L, hd]: head_dim   */
+    const float *attn;       /* softmax weights [n_heads, S, L] */
+    const float *lora_q_h;   /* x @ A_q^T [S, rank] */
+    const float *lora_v_h;   /* x @ A_v^T [S, rank] */
+} tlb_layer_acts;
+
+/* A LoRA adapter (A [rank, in], B [out, rank]) and its AdamW moments, updated in place.
+ * grad_a / grad_b: optional outputs of the gradients (NULL = not written). */
+typedef struct {
+    float *a, *b;
+    float *m_a, *v_a, *m_b, *v_b;
+    float *grad_a, *grad_b;
+} tlb_lora;
+
+/* [RS] cpu_adamw hyperparameters; B of each adapter uses lr * lr_b_mult (LoRA+, 16 on the page). */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay, lr_b_mult;
+    int32_t step;            /* >= 1; bias corrections 1/(1 - beta^step) */
+} tlb_adamw_cfg;
+
+/* ---------------------------------------------------------------- library */
+
+/* Message of the last failing call on this thread ("" if none). Owned by the library. */
+const char *tlb_last_error(void);
+/* Build description (compute capability compiled for, version). Owned by the library. */
+const char *tlb_build_info(void);
+
+/* ---------------------------------------------------------------- standalone steps */
+
+/* [ATT] softmaxBackwardKernel / executeSoftmaxBackward:
+ *   dscores[r, j] = attn[r, j] * (dattn[r, j] - sum_j' attn[r, j'] dattn[r, j'])
+ * rows x len, row-major.  rows >= 0, len >= 0 (empty is a no-op). */
+int tlb_softmax_backward(const float *attn, const float *dattn, float *dscores,
+                         int64_t rows, int64_t len, void *stream);
+
+/* [FFN] reluSqrMulBackwardKernel / executeReluSqrMulBackward (act = TLB_ACT_RELU2_MUL):
+ *   dgate = dh * up * 2 max(0, gate),  dup = dh * max(0, gate)^2
+ * [RS] SiLU backward (act = TLB_ACT_SILU_MUL), sig = 1/(1+e^-g):
+ *   dgate = dh * up * sig (1 + g - g sig),  dup = dh * (silu_gate ? silu_gate : g sig)
+ * n elements; silu_gate may be NULL. */
+int tlb_act_backward(int32_t act, const float *gate, const float *up, const float *silu_gate,
+                     const float *dh, float *dgate, float *dup, int64_t n, void *stream);
+
+/* [ATT] rmsNormBackwardKernel / executeRmsNormBackward, one row of n per row:
+ *   rms = sqrt(mean(x^2) + eps),  dx = (1/rms) (dy*gamma - x dot(dy*gamma, x) / (n rms^2))
+ * accumulate = 0 stores dx, 1 adds it into dx ([FFN] "dResidual +=").  dx may alias dy
+ * when accumulate = 0. */
+int tlb_rmsnorm_backward(const float *x, const float *gamma, const float *dy, float *dx,
+                         int64_t rows, int64_t n, float eps, int32_t accumulate, void *stream);
+
+/* [ATT] ropeBackwardKernel / executeRopeBackward: inverse NeoX rotation R(-theta) of
+ * dy [rows, n_heads, head_dim]; row r is at position pos0 + r, theta_d = pos *
+ * base^(-2d/head_dim), d < head_dim/2.  dx may alias dy.  head_dim even, <= 256. */
+int tlb_rope_backward(const float *dy, float *dx, int64_t rows, int32_t n_heads,
+                      int32_t head_dim, int64_t pos0, float base, void *stream);
+
+/* [RS] cpu_adamw on n parameters with learning rate cfg->lr * lr_mult.
+ * If sumsq != NULL (device double), sum(g^2) is added to *sumsq. */
+int tlb_adamw(float *p, const float *g, float *m, float *v, int64_t n,
+              const tlb_adamw_cfg *cfg, float lr_mult, double *sumsq, void *stream);
+
+/* ---------------------------------------------------------------- layer pieces */
+
+/* Workspace bytes needed by tlb_ffn_backward / tlb_attn_backward /
+ * tlb_lora_grad_adamw / tlb_layer_backward for this layer and S, L. */
+size_t tlb_workspace_bytes(const tlb_layer_cfg *cfg, int64_t S, int64_t L);
+
+/* Device status recorded in a workspace by earlier calls on `stream`: synchronises
+ * the stream, returns TLB_OK or the first device error (TLB_ETIMEOUT), and clears it. */
+int tlb_workspace_status(void *ws, size_t ws_bytes, void *stream);
+
+/* [FFN] executeFFNBackward (sequence form: [RS] backward_through_layers, FFN part).
+ *   dF  = dOut W_down^T;  dh = SUB_NORM ? RMSNorm_bwd(hidden, gamma_sub_ffn, dF) : dF
+ *   dG, dU = activation backward;  dN2 = dG W_gate^T + dU W_up^T
+ *   d_residual = (RESIDUAL ? d_out : 0) + (PRE_NORM ? RMSNorm_bwd(r1, gamma_ffn, dN2) : dN2)
+ * d_out [S, dim]; d_residual [S, dim] output, which may alias d_out (the result is
+ * then dR1, written over dOut). */
+int tlb_ffn_backward(const tlb_layer_cfg *cfg, int64_t S, const float *d_out,
+                     const tlb_layer_weights *w, const tlb_layer_acts *acts,
+                     float *d_residual, void *ws, size_t ws_bytes, void *stream);
+
+/* [ATT] gradient flow from the O projection down to dQpre; [RS] attention block.
+ *   dSub = dR1 W_O^T;  dCtx = SUB_NORM ? RMSNorm_bwd(ctx, gamma_sub_attn, dSub) : dSub
+ *   per head h, kvh = h / (n_heads/n_kv_heads):
+ *     dAttn = dCtx_h V_kvh^T;  dS = attn_h (dAttn - rowsum(attn_h dAttn));  dQ_h = scale dS K_kvh
+ *     dV_kvh += attn_h^T dCtx_h
+ *   d_qpre [S, q_dim] = ROPE ? R(-theta) dQ : dQ   (row i at position L - S + i)
+ *   d_v    [S, kv_dim] = dV rows of the S newest cache positions L - S .. L - 1
+ * d_attn_out = dR1 [S, dim]. */
+int tlb_attn_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const float *d_attn_out,
+                      const tlb_layer_weights *w, const tlb_layer_acts *acts,
+                      float *d_qpre, float *d_v, void *ws, size_t ws_bytes, void *stream);
+
+/* [RS] "LoRA Q backward" / "LoRA V backward" and cpu_adamw, s = alpha / rank:
+ *   dB = s G^T h [out, r];  gh = s G B_old [S, r];  dA = gh^T x [r, in]
+ *   then AdamW on A (lr) and B (lr * lr_b_mult); B is read before it is updated.
+ * G [S, out_dim], h [S, rank], x [S, in_dim].  sumsq (device double[2], may be NULL)
+ * += {sum dA^2, sum dB^2}. */
+int tlb_lora_grad_adamw(int64_t S, int32_t out_dim, int32_t in_dim, int32_t rank, float alpha,
+                        const float *G, const float *h, const float *x, const tlb_lora *lora,
+                        const tlb_adamw_cfg *adam, double *sumsq, void *ws, size_t ws_bytes,
+                        void *stream);
+
+/* One whole layer: FFN backward, attention backward, LoRA Q/V gradients and AdamW.
+ * d_hidden [S, dim] in/out: dOut on entry, the gradient for the layer below (dR1) on
+ * return ([RS] grad_hidden).  sumsq (device double[2]) += {sum dA^2, sum dB^2} over both
+ * adapters; the page's gradient norm over a stack is sqrt(sumsq[0]).  lora_q: A [r, dim],
+ * B [q_dim, r]; lora_v: A [r, dim], B [kv_dim, r]. */
+int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L,
+                       const tlb_layer_weights *w, const tlb_layer_acts *acts,
+                       const tlb_lora *lora_q, const tlb_lora *lora_v,
+                       const tlb_adamw_cfg *adam, float *d_hidden, double *sumsq,
+                       void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TLB_H_ */

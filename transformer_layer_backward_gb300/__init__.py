@@ -1,0 +1,18 @@
+"""GB300 (sm_103a) LoRA transformer layer backward.
+
+The computation lives in the CUDA library ``lib/libtlb.so`` (C ABI declared in
+``include/tlb.h``); this package loads it and marshals torch tensors into it.
+Importing the package does not touch the GPU; ``load()`` fails loudly when the
+library has not been built.
+"""
+from . import _abi
+from ._abi import TlbError, load
+from .api import (act_backward, adamw, adamw_cfg, attn_backward, ffn_backward, layer_acts,
+                  layer_backward, layer_cfg, layer_weights, lora, lora_grad_adamw,
+                  rmsnorm_backward, rope_backward, softmax_backward, workspace, workspace_bytes,
+                  workspace_status)
+
+__all__ = ["TlbError", "load", "act_backward", "adamw", "adamw_cfg", "attn_backward",
+           "ffn_backward", "layer_acts", "layer_backward", "layer_cfg", "layer_weights", "lora",
+           "lora_grad_adamw", "rmsnorm_backward", "rope_backward", "softmax_backward",
+           "workspace", "workspace_bytes", "workspace_status", "_abi"]

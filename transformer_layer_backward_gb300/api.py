@@ -1,0 +1,177 @@
+"""Python binding of the C ABI: one function per entry point, with the same names.
+
+Each function checks devices, dtypes and contiguity of torch tensors, then passes
+raw device pointers to the library.  No arithmetic of the backward pass happens
+here; every step runs in the CUDA kernels of ``lib/libtlb.so``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+
+import torch
+
+from . import _abi as A
+
+_WDTYPE = {A.W_F32: torch.float32, A.W_BF16: torch.bfloat16, A.W_TERNARY_I8: torch.int8}
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _ptr(t, dtype=torch.float32, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be on a CUDA device" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return C.c_void_p(t.data_ptr()) if t.numel() else None
+
+
+# ------------------------------------------------------------------ standalone steps
+
+def softmax_backward(attn, dattn, out=None, stream=None):
+    """dS = attn * (dAttn - rowsum(attn * dAttn)) over the last axis."""
+    out = torch.empty_like(attn) if out is None else out
+    rows = attn.numel() // attn.shape[-1] if attn.dim() and attn.shape[-1] else 0
+    A.call("tlb_softmax_backward", _ptr(attn, name="attn"), _ptr(dattn, name="dattn"),
+           _ptr(out, name="out"), rows, attn.shape[-1] if attn.dim() else 0, _stream(stream))
+    return out
+
+
+def act_backward(act, gate, up, dh, silu_gate=None, dgate=None, dup=None, stream=None):
+    """Gated activation backward; act is 'relu2_mul' or 'silu_mul'."""
+    code = {"relu2_mul": A.ACT_RELU2_MUL, "silu_mul": A.ACT_SILU_MUL}[act]
+    dgate = torch.empty_like(gate) if dgate is None else dgate
+    dup = torch.empty_like(gate) if dup is None else dup
+    A.call("tlb_act_backward", code, _ptr(gate, name="gate"), _ptr(up, name="up"),
+           _ptr(silu_gate, name="silu_gate"), _ptr(dh, name="dh"), _ptr(dgate, name="dgate"),
+           _ptr(dup, name="dup"), gate.numel(), _stream(stream))
+    return dgate, dup
+
+
+def rmsnorm_backward(x, gamma, dy, eps=1e-6, out=None, accumulate=False, stream=None):
+    """Row-wise RMSNorm backward over the last axis; accumulate adds into out."""
+    out = torch.empty_like(x) if out is None else out
+    n = x.shape[-1]
+    rows = x.numel() // n if n else 0
+    A.call("tlb_rmsnorm_backward", _ptr(x, name="x"), _ptr(gamma, name="gamma"),
+           _ptr(dy, name="dy"), _ptr(out, name="out"), rows, n, float(eps),
+           1 if accumulate else 0, _stream(stream))
+    return out
+
+
+def rope_backward(dy, pos0, base=10000.0, out=None, stream=None):
+    """Inverse NeoX rotation of dy [rows, n_heads, head_dim]; row r at position pos0 + r."""
+    out = torch.empty_like(dy) if out is None else out
+    rows, nh, hd = dy.shape
+    A.call("tlb_rope_backward", _ptr(dy, name="dy"), _ptr(out, name="out"), rows, nh, hd,
+           int(pos0), float(base), _stream(stream))
+    return out
+
+
+def adamw_cfg(lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1, lr_b_mult=16.0):
+    return A.AdamwCfg(lr, beta1, beta2, eps, weight_decay, lr_b_mult, int(step))
+
+
+def adamw(p, g, m, v, cfg: A.AdamwCfg, lr_mult=1.0, sumsq=None, stream=None):
+    """One AdamW step in place on p, m, v; sumsq (float64 device scalar) += sum(g^2)."""
+    A.call("tlb_adamw", _ptr(p, name="p"), _ptr(g, name="g"), _ptr(m, name="m"),
+           _ptr(v, name="v"), p.numel(), C.byref(cfg), float(lr_mult),
+           _ptr(sumsq, torch.float64, "sumsq"), _stream(stream))
+
+
+# ------------------------------------------------------------------ layer pieces
+
+def layer_cfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, lora_alpha, act="relu2_mul",
+              wtype="f32", sub_norm=False, pre_norm=False, residual=True, rope=True,
+              use_silu_cache=False, causal=True, rope_base=10000.0, norm_eps=1e-6,
+              attn_scale=None) -> A.LayerCfg:
+    flags = ((A.SUB_NORM if sub_norm else 0) | (A.PRE_NORM if pre_norm else 0) |
+             (A.RESIDUAL if residual else 0) | (A.ROPE if rope else 0) |
+             (A.USE_SILU_CACHE if use_silu_cache else 0) | (A.CAUSAL if causal else 0))
+    return A.LayerCfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, float(lora_alpha),
+                      float(rope_base), float(norm_eps),
+                      float(1.0 / math.sqrt(head_dim) if attn_scale is None else attn_scale),
+                      {"relu2_mul": A.ACT_RELU2_MUL, "silu_mul": A.ACT_SILU_MUL}[act],
+                      {"f32": A.W_F32, "bf16": A.W_BF16, "ternary": A.W_TERNARY_I8}[wtype], flags)
+
+
+def workspace_bytes(cfg: A.LayerCfg, S: int, L: int) -> int:
+    return int(A.load().tlb_workspace_bytes(C.byref(cfg), int(S), int(L)))
+
+
+def workspace(cfg: A.LayerCfg, S: int, L: int, device="cuda"):
+    """A zeroed workspace tensor of the size the library asks for."""
+    return torch.zeros(max(workspace_bytes(cfg, S, L), 256), dtype=torch.uint8, device=device)
+
+
+def workspace_status(ws, stream=None):
+    A.call("tlb_workspace_status", _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+
+
+def layer_weights(cfg: A.LayerCfg, t: dict):
+    """Weights from a dict: w_down/w_gate/w_up/w_o (+ s_* scales), gamma_* optional."""
+    wd = _WDTYPE[cfg.wtype]
+
+    def w(name):
+        return A.Weight(_ptr(t[name], wd, name), float(t.get("s_" + name[2:], 1.0)))
+
+    return A.LayerWeights(w("w_down"), w("w_gate"), w("w_up"), w("w_o"),
+                          _ptr(t.get("g_sub_ffn"), name="g_sub_ffn"),
+                          _ptr(t.get("g_ffn"), name="g_ffn"),
+                          _ptr(t.get("g_sub_attn"), name="g_sub_attn"))
+
+
+def layer_acts(cfg: A.LayerCfg, t: dict, kv_layout: str, L: int):
+    """Cached activations from a dict; kv_layout 'shd' = [L, kv_dim], 'hsd' = [n_kv, L, hd]."""
+    hd = cfg.head_dim
+    if kv_layout == "shd":
+        sh, sp = hd, cfg.n_kv_heads * hd
+    else:
+        sh, sp = L * hd, hd
+    g = lambda k: _ptr(t.get(k), name=k)
+    return A.LayerActs(g("x"), g("gate"), g("up"), g("silu_gate"), g("hidden"), g("r1"),
+                       g("ctx"), g("k"), g("v"), sh, sp, g("attn"), g("lora_q_h"), g("lora_v_h"))
+
+
+def lora(t: dict, tag: str, grads: dict | None = None):
+    g = grads or {}
+    p = lambda k: _ptr(t[k], name=k)
+    return A.Lora(p("a_" + tag), p("b_" + tag), p("m_a_" + tag), p("v_a_" + tag),
+                  p("m_b_" + tag), p("v_b_" + tag),
+                  _ptr(g.get("dA_" + tag), name="dA"), _ptr(g.get("dB_" + tag), name="dB"))
+
+
+def ffn_backward(cfg, S, d_out, weights, acts, d_residual, ws, stream=None):
+    A.call("tlb_ffn_backward", C.byref(cfg), int(S), _ptr(d_out, name="d_out"), C.byref(weights),
+           C.byref(acts), _ptr(d_residual, name="d_residual"), _ptr(ws, torch.uint8, "ws"),
+           ws.numel(), _stream(stream))
+
+
+def attn_backward(cfg, S, L, d_attn_out, weights, acts, d_qpre, d_v, ws, stream=None):
+    A.call("tlb_attn_backward", C.byref(cfg), int(S), int(L), _ptr(d_attn_out, name="d_attn_out"),
+           C.byref(weights), C.byref(acts), _ptr(d_qpre, name="d_qpre"), _ptr(d_v, name="d_v"),
+           _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+
+
+def lora_grad_adamw(S, out_dim, in_dim, rank, alpha, G, h, x, lora_: A.Lora, adam: A.AdamwCfg,
+                    sumsq, ws, stream=None):
+    A.call("tlb_lora_grad_adamw", int(S), int(out_dim), int(in_dim), int(rank), float(alpha),
+           _ptr(G, name="G"), _ptr(h, name="h"), _ptr(x, name="x"), C.byref(lora_), C.byref(adam),
+           _ptr(sumsq, torch.float64, "sumsq"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+           _stream(stream))
+
+
+def layer_backward(cfg, S, L, weights, acts, lora_q, lora_v, adam, d_hidden, sumsq, ws, stream=None):
+    A.call("tlb_layer_backward", C.byref(cfg), int(S), int(L), C.byref(weights), C.byref(acts),
+           C.byref(lora_q), C.byref(lora_v), C.byref(adam), _ptr(d_hidden, name="d_hidden"),
+           _ptr(sumsq, torch.float64, "sumsq"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+           _stream(stream))

@@ -1,0 +1,160 @@
+// extern "C" entry points of the standalone steps, error reporting and the small
+// host-side helpers shared by all translation units.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace tlb {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+}
+
+void clear_error() { g_err[0] = '\0'; }
+
+int check_launch(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("%s: kernel launch failed: %s", what, cudaGetErrorString(e));
+        return TLB_ECUDA;
+    }
+    return TLB_OK;
+}
+
+int num_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+            n = v;
+        else
+            return 148;
+    }
+    return n;
+}
+
+unsigned stream_grid(int64_t work, int block) {
+    const int64_t want = ceil_div(work, block);
+    const int64_t cap = int64_t(num_sms()) * 8;
+    return (unsigned)(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+void rope_freqs(RopeFreqs &f, int head_dim, float base) {
+    for (int d = 0; d < 128; ++d) {
+        double v = 0.0;
+        if (d < head_dim / 2) v = std::pow(double(base), -2.0 * double(d) / double(head_dim));
+        f.hi[d] = float(v);
+        f.lo[d] = float(v - double(f.hi[d]));
+    }
+}
+
+AdamCoef adam_coef(const tlb_adamw_cfg &c, float lr_mult) {
+    AdamCoef k;
+    k.lr = c.lr * lr_mult;
+    k.beta1 = c.beta1;
+    k.beta2 = c.beta2;
+    k.eps = c.eps;
+    k.wd = c.weight_decay;
+    k.bc1 = float(1.0 / (1.0 - std::pow(double(c.beta1), double(c.step))));
+    k.bc2 = float(1.0 / (1.0 - std::pow(double(c.beta2), double(c.step))));
+    return k;
+}
+
+}  // namespace tlb
+
+using namespace tlb;
+
+extern "C" {
+
+const char *tlb_last_error(void) { return g_err; }
+
+const char *tlb_build_info(void) {
+    static char info[128];
+    snprintf(info, sizeof(info), "tlb sm_103a build, CUDA %d.%d", CUDART_VERSION / 1000,
+             (CUDART_VERSION % 1000) / 10);
+    return info;
+}
+
+int tlb_softmax_backward(const float *attn, const float *dattn, float *dscores, int64_t rows,
+                         int64_t len, void *stream) {
+    clear_error();
+    TLB_REQUIRE(rows >= 0 && len >= 0, TLB_EINVAL, "softmax_backward: negative size");
+    if (rows == 0 || len == 0) return TLB_OK;
+    TLB_REQUIRE(attn && dattn && dscores, TLB_EINVAL, "softmax_backward: null pointer");
+    return softmax_backward_launch(attn, dattn, dscores, rows, len, as_stream(stream));
+}
+
+int tlb_act_backward(int32_t act, const float *gate, const float *up, const float *silu_gate,
+                     const float *dh, float *dgate, float *dup, int64_t n, void *stream) {
+    clear_error();
+    TLB_REQUIRE(act == TLB_ACT_RELU2_MUL || act == TLB_ACT_SILU_MUL, TLB_EINVAL,
+                "act_backward: unknown activation %d", act);
+    TLB_REQUIRE(n >= 0, TLB_EINVAL, "act_backward: negative size");
+    if (n == 0) return TLB_OK;
+    TLB_REQUIRE(gate && up && dh && dgate && dup, TLB_EINVAL, "act_backward: null pointer");
+    return act_backward_launch(act, gate, up, silu_gate, dh, dgate, dup, n, as_stream(stream));
+}
+
+int tlb_rmsnorm_backward(const float *x, const float *gamma, const float *dy, float *dx, int64_t rows,
+                         int64_t n, float eps, int32_t accumulate, void *stream) {
+    clear_error();
+    TLB_REQUIRE(rows >= 0 && n >= 0, TLB_EINVAL, "rmsnorm_backward: negative size");
+    if (rows == 0 || n == 0) return TLB_OK;
+    TLB_REQUIRE(x && gamma && dy && dx, TLB_EINVAL, "rmsnorm_backward: null pointer");
+    TLB_REQUIRE(!(accumulate && dx == dy), TLB_EINVAL,
+                "rmsnorm_backward: dx may alias dy only when accumulate = 0");
+    return rmsnorm_backward_launch(x, gamma, dy, dx, rows, n, eps, accumulate ? 1 : 0,
+                                   as_stream(stream));
+}
+
+int tlb_rope_backward(const float *dy, float *dx, int64_t rows, int32_t n_heads, int32_t head_dim,
+                      int64_t pos0, float base, void *stream) {
+    clear_error();
+    TLB_REQUIRE(rows >= 0 && n_heads >= 0 && pos0 >= 0, TLB_EINVAL, "rope_backward: negative size");
+    TLB_REQUIRE(head_dim > 0 && head_dim % 2 == 0, TLB_EINVAL, "rope_backward: head_dim must be even");
+    TLB_REQUIRE(head_dim <= 256, TLB_EUNSUPPORTED, "rope_backward: head_dim > 256");
+    TLB_REQUIRE(pos0 + rows <= (int64_t(1) << 24), TLB_EUNSUPPORTED,
+                "rope_backward: positions >= 2^24");
+    if (rows == 0 || n_heads == 0) return TLB_OK;
+    TLB_REQUIRE(dy && dx, TLB_EINVAL, "rope_backward: null pointer");
+    return rope_backward_launch(dy, dx, rows, n_heads, head_dim, pos0, base, as_stream(stream));
+}
+
+int tlb_adamw(float *p, const float *g, float *m, float *v, int64_t n, const tlb_adamw_cfg *cfg,
+              float lr_mult, double *sumsq, void *stream) {
+    clear_error();
+    TLB_REQUIRE(cfg != nullptr, TLB_EINVAL, "adamw: null cfg");
+    TLB_REQUIRE(cfg->step >= 1, TLB_EINVAL, "adamw: step must be >= 1");
+    TLB_REQUIRE(n >= 0, TLB_EINVAL, "adamw: negative size");
+    if (n == 0) return TLB_OK;
+    TLB_REQUIRE(p && g && m && v, TLB_EINVAL, "adamw: null pointer");
+    return adamw_launch(p, g, m, v, n, *cfg, lr_mult, sumsq, as_stream(stream));
+}
+
+int tlb_workspace_status(void *ws, size_t ws_bytes, void *stream) {
+    clear_error();
+    TLB_REQUIRE(ws != nullptr && ws_bytes >= kStatusBytes, TLB_EINVAL,
+                "workspace_status: workspace too small");
+    uint32_t words[2] = {0, 0};
+    cudaStream_t st = as_stream(stream);
+    TLB_CUDA(cudaMemcpyAsync(words, ws, sizeof(words), cudaMemcpyDeviceToHost, st));
+    TLB_CUDA(cudaStreamSynchronize(st));
+    if (words[kStatusCode] == kDevOk) return TLB_OK;
+    TLB_CUDA(cudaMemsetAsync(ws, 0, sizeof(words), st));
+    TLB_CUDA(cudaStreamSynchronize(st));
+    set_error("device status: a bounded wait ran out (code %u, site %u)", words[kStatusCode],
+              words[kStatusWhere]);
+    return TLB_ETIMEOUT;
+}
+
+}  // extern "C"
