@@ -1,0 +1,332 @@
+"""Throughput of the LoRA layer backward on one GB300 (or N independent replicas).
+
+Workload: the single-token decode layer backward (dim 2560, ffn 6912, 20 heads /
+5 KV heads of 128, cache 1024, ternary int8 weights, ReLU^2 x Mul FFN with
+sub-norms, pre-norm residual, RoPE, LoRA rank 16 on Q and V, AdamW + LoRA+).
+One step = one call of tlb_layer_backward for one token through one layer.
+Steps cycle through NL distinct layers (weights, caches and adapters), so the
+working set (NL x 68 MB) is several times the 129 MB L2 and each step reads its
+inputs from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tlb|reference]
+
+--impl reference times the float64 CPU oracle (the only other implementation of
+this path available here) on the same workload.  Under torchrun every rank runs
+its own replica (the path has no exchange step); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA layer-backward tokens/s"
+UNIT = "tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=2000)
+    p.add_argument("--impl", default="tlb", choices=["tlb", "reference"])
+    p.add_argument("--layers", type=int, default=8)
+    p.add_argument("--e2e-steps", type=int, default=2000)
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-graph", action="store_true")
+    return p.parse_args()
+
+
+def decode_bytes(cfg) -> int:
+    """Algorithmic HBM bytes of one decode layer backward (each input read once)."""
+    H, I, qd, kvd, r, L = cfg.dim, cfg.ffn_dim, cfg.q_dim, cfg.kv_dim, cfg.rank, cfg.cache_len
+    weights = (I * H + 2 * H * I + qd * H) * 1                      # ternary int8
+    kv = 2 * kvd * L * 4
+    attn = cfg.n_heads * L * 4
+    lora = (2 * r * H + qd * r + kvd * r) * 24                      # p, m, v read + write
+    vectors = (H * 2 + I * 3 + H + qd + I + H + qd + 2 * r + H) * 4  # dOut,x,gate,up,hid,r1,ctx,gammas,h,d_in
+    return weights + kv + attn + lora + vectors
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), "--query-gpu=" + self.Q,
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        self.p.wait()
+        rows = [l.split(", ") for l in open(self.f.name).read().strip().splitlines() if l.count(",") >= 8]
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        mhz = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def oracle_step_time(cfg, seconds):
+    """Seconds per decode layer backward of the float64 oracle on the host cores."""
+    from oracle import layer as OL
+    from synth import layer_inputs
+    d = layer_inputs(cfg, layer=0, seed=0)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        OL.layer_backward(cfg, d, d["dout"])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n >= 1000:
+            return el / n, n
+
+
+def host_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        t = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if t:
+            return max(t)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from synth import DECODE
+    cfg = DECODE
+    per = max(args.cpu_seconds / max(args.steps, 1), 0.0)
+    times = []
+    for _ in range(args.warmup if args.warmup < 3 else 1):
+        oracle_step_time(cfg, 0.0)
+    for _ in range(args.steps):
+        t, _ = oracle_step_time(cfg, per)
+        times.append(t)
+    t = statistics.mean(times)
+    v = 1.0 / t
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode layer backward (configs[1]): dim 2560, ffn 6912, 20/5 heads x 128, "
+                                   "cache 1024, ternary, LoRA r16", "global_batch": 1, "seq_len": 1,
+                       "parallelism": "replicas"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
+                             "sample": "one decode layer backward per step, float64 numpy oracle"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    import transformer_layer_backward_gb300 as tlb
+    from synth import DECODE, layer_inputs
+    from tests.helpers import adam_to_abi, cfg_to_abi, lora_dev, to_dev
+
+    torch.cuda.set_device(local)
+    tlb.load()
+    cfg = DECODE
+    NL = args.layers
+    c = cfg_to_abi(tlb, cfg)
+    adam = adam_to_abi(tlb, cfg)
+    layers, host_layers = [], []
+    for l in range(NL):
+        d = layer_inputs(cfg, layer=l, seed=0)
+        t = to_dev(d, cfg.wtype)
+        L = lora_dev(t)
+        layers.append(dict(t=t, L=L, w=tlb.layer_weights(c, t),
+                           a=tlb.layer_acts(c, t, cfg.kv_layout, cfg.cache_len),
+                           lq=tlb.lora(L, "q"), lv=tlb.lora(L, "v")))
+        host_layers.append(d)
+    ws = tlb.workspace(c, 1, cfg.cache_len)
+    dh = torch.empty(1, cfg.dim, device="cuda")
+    ss = torch.zeros(2, dtype=torch.float64, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        ly = layers[i % NL]
+        dh.copy_(ly["t"]["dout"])
+        tlb.layer_backward(c, 1, cfg.cache_len, ly["w"], ly["a"], ly["lq"], ly["lv"], adam, dh, ss, ws)
+
+    # one CUDA graph per layer: the same kernels, launched without per-call host overhead
+    graphs = None
+    if not args.no_graph:
+        for i in range(NL):
+            step(i)
+        torch.cuda.synchronize()
+        graphs = []
+        for i in range(NL):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(i)
+            graphs.append(g)
+        torch.cuda.synchronize()
+
+    def run(i):
+        if graphs is not None:
+            graphs[i % NL].replay()
+        else:
+            step(i)
+
+    launches_per_step = None
+    n0 = tlb.launch_count()
+    step(0)
+    launches_per_step = tlb.launch_count() - n0
+    for i in range(max(args.warmup, 3)):
+        run(i)
+    tlb.workspace_status(ws)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        run(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    tlb.workspace_status(ws)
+    t_local = torch.tensor([ms], device="cuda", dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
+    ms_max = float(t_local.item())
+    tokens = args.steps * world
+    value = tokens / (ms_max / 1e3)
+
+    # dominant kernel: the ternary transposed GEMV (W_gate / W_up / W_down sized), timed live on
+    # this stream over the weight matrices of every layer in turn
+    mats = [(ly["t"][k], cfg.ffn_dim if k == "w_down" else cfg.dim, cfg.dim if k == "w_down" else cfg.ffn_dim)
+            for ly in layers for k in ("w_down", "w_gate", "w_up")]
+    xin = torch.randn(1, cfg.ffn_dim, device="cuda")
+    yout = torch.empty(1, cfg.ffn_dim, device="cuda")
+    for k in range(3):
+        W, rows, cols = mats[k]
+        tlb.linear_backward("ternary", W, xin[:, :cols], out=yout[:, :rows])
+    nk = max(3 * len(mats), 96)
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
+    for k in range(nk):
+        W, rows, cols = mats[k % len(mats)]
+        tlb.linear_backward("ternary", W, xin[:, :cols], out=yout[:, :rows])
+    k1.record(stream)
+    torch.cuda.synchronize()
+    kms = k0.elapsed_time(k1) / nk
+    gemv_bytes = cfg.dim * cfg.ffn_dim + 4 * (cfg.dim + cfg.ffn_dim)
+    pk = peaks()
+    hbm = pk["hbm_gbs"] if pk else 6800.0
+    achieved = gemv_bytes / (kms / 1e3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "gemv_ternary_decode.json")
+    if os.path.exists(prof):
+        traffic = json.load(open(prof)).get("dram_bytes_per_launch")
+
+    # end to end through the public API: per-step activations from pinned host memory,
+    # d_in and the gradient norm read back every step
+    e2e = None
+    if rank == 0 or world > 1:
+        acts = ("x", "gate", "up", "hidden", "r1", "ctx", "k", "v", "attn", "lora_q_h", "lora_v_h", "dout")
+        pinned = [{k: torch.from_numpy(np.ascontiguousarray(host_layers[l][k])).pin_memory() for k in acts}
+                  for l in range(NL)]
+        h2d = sum(pinned[0][k].numel() * 4 for k in acts)
+        res_h = torch.empty(1, cfg.dim, pin_memory=True)
+        ss_h = torch.empty(2, dtype=torch.float64, pin_memory=True)
+        d2h = res_h.numel() * 4 + 16
+        ne = min(args.e2e_steps, max(args.steps, 10))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(ne):
+            ly = layers[i % NL]
+            for k in acts:
+                ly["t"][k].copy_(pinned[i % NL][k], non_blocking=True)
+            dh.copy_(ly["t"]["dout"])
+            tlb.layer_backward(c, 1, cfg.cache_len, ly["w"], ly["a"], ly["lq"], ly["lv"], adam, dh, ss, ws)
+            res_h.copy_(dh, non_blocking=True)
+            ss_h.copy_(ss, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_s = time.perf_counter() - t0
+        e2e = {"value": ne * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        t_or, n_or = oracle_step_time(cfg, args.cpu_seconds)
+        cpu = {"value": 1.0 / t_or, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
+               "sample": "%d decode layer backwards of layer 0 (float64 numpy oracle)" % n_or}
+
+    if rank == 0:
+        step_bytes = decode_bytes(cfg)
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": "decode layer backward (configs[1]): dim 2560, ffn 6912, 20/5 heads "
+                                       "x 128, cache 1024, pos 1023, ternary int8 weights, ReLU^2xMul, "
+                                       "sub-norms, LoRA r16 Q/V, AdamW+LoRA+",
+                           "global_batch": world, "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
+                           "layers_cycled": NL, "l2": "inputs > L2: %d distinct layers x %.1f MB" % (NL, step_bytes / 1e6),
+                           "cuda_graph": graphs is not None},
+                "roofline": {"bound": "hbm", "kernel": "gemv_rows_kernel<ternary> (transposed-weight GEMV)",
+                             "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                             "traffic": traffic, "peak_source": "MEASURED_PEAKS.json hbm_gbs" if pk else "fallback"},
+                "step_roofline": {"bytes_per_step": step_bytes, "achieved": step_bytes / (ms_max / args.steps / 1e3) / 1e9,
+                                  "peak": hbm, "unit": "GB/s",
+                                  "frac": step_bytes / (ms_max / args.steps / 1e3) / 1e9 / hbm},
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+                "clocks": clk}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -138,6 +138,8 @@ typedef struct {
 const char *tlb_last_error(void);
 /* Build description (compute capability compiled for, version). Owned by the library. */
 const char *tlb_build_info(void);
+/* Number of kernels this process has enqueued through the library so far (all threads). */
+uint64_t tlb_launch_count(void);
 
 /* ---------------------------------------------------------------- standalone steps */
 
@@ -167,6 +169,14 @@ int tlb_rmsnorm_backward(const float *x, const float *gamma, const float *dy, fl
  * base^(-2d/head_dim), d < head_dim/2.  dx may alias dy.  head_dim even, <= 256. */
 int tlb_rope_backward(const float *dy, float *dx, int64_t rows, int32_t n_heads,
                       int32_t head_dim, int64_t pos0, float base, void *stream);
+
+/* [ATT] O projection backward ("BitLinear transpose"); [FFN] W_down^T, W_gate^T, W_up^T
+ * products; [RS] gemm_backward_a (C = A B^T with the weight stored pre-transposed):
+ *   dX[S, in_dim] (+)= scale * dY[S, out_dim] . W[in_dim, out_dim]^T
+ * W in storage type wtype (TLB_W_*); accumulate = 1 adds into dX.  S = 1 runs a GEMV;
+ * S > 1 a GEMM (tensor cores for bf16 weights). */
+int tlb_linear_backward(int32_t wtype, const void *W, float scale, const float *dY, int64_t S,
+                        int64_t out_dim, int64_t in_dim, float *dX, int32_t accumulate, void *stream);
 
 /* [RS] cpu_adamw on n parameters with learning rate cfg->lr * lr_mult.
  * If sumsq != NULL (device double), sum(g^2) is added to *sumsq. */

@@ -1,0 +1,172 @@
+"""GPU parity of the layer pieces (ffn_backward, attn_backward, lora_grad_adamw) and
+of the whole layer / stack against the float64 oracle on the same seeded inputs.
+
+Configurations: the tiny fp32 layer (all norms, RoPE, GQA, causal), the
+single-token decode layer with ternary weights, a small bf16 sequence layer with
+a ragged sequence length, and the S = 512 SwiGLU layer.
+"""
+import numpy as np
+import pytest
+
+from oracle import layer as OL
+from oracle import ops
+from synth import DECODE, SEQ512, TINY, layer_inputs
+from tests.helpers import (BF16_REL_L2, adam_to_abi, cfg_to_abi, check, host, lora_dev, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+MINI_SEQ = SEQ512.with_(name="mini_seq", dim=256, ffn_dim=640, n_heads=8, n_kv_heads=2, head_dim=32,
+                        rank=8, lora_alpha=16.0, seq_len=77, cache_len=77)
+TINY_WARM = TINY.with_(name="tiny_warm", adam_state="warm", step=7)
+CASES = {c.name: c for c in (TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512)}
+
+
+def tol(cfg):
+    """(rel_l2, max_abs) of the path this config runs on."""
+    return (BF16_REL_L2, None) if cfg.wtype == "bf16" and _tc_path() else (1e-5, 1e-4)
+
+
+def _tc_path():
+    return False   # bf16 weights currently run through the CUDA-core GEMM (fp32 arithmetic)
+
+
+@pytest.fixture(scope="module", params=sorted(CASES))
+def case(request):
+    cfg = CASES[request.param]
+    d = layer_inputs(cfg, layer=0, seed=0)
+    ref = OL.layer_backward(cfg, d, d["dout"])
+    return cfg, d, ref
+
+
+def kv_layout(cfg):
+    return cfg.kv_layout
+
+
+def test_ffn_backward(lib, case):
+    import torch
+    cfg, d, ref = case
+    t = to_dev(d, cfg.wtype)
+    c = cfg_to_abi(lib, cfg)
+    ws = lib.workspace(c, cfg.seq_len, cfg.cache_len)
+    w = lib.layer_weights(c, t)
+    a = lib.layer_acts(c, t, cfg.kv_layout, cfg.cache_len)
+    out = torch.empty_like(t["dout"])
+    lib.ffn_backward(c, cfg.seq_len, t["dout"], w, a, out, ws)
+    rl, ma = tol(cfg)
+    check("dR1", host(out), ref["dR1"], rl, ma)
+    # in place: d_residual aliases d_out
+    inplace = t["dout"].clone()
+    lib.ffn_backward(c, cfg.seq_len, inplace, w, a, inplace, ws)
+    check("dR1 in place", host(inplace), ref["dR1"], rl, ma)
+
+
+def test_attn_backward(lib, case):
+    import torch
+    cfg, d, ref = case
+    t = to_dev(d, cfg.wtype)
+    c = cfg_to_abi(lib, cfg)
+    ws = lib.workspace(c, cfg.seq_len, cfg.cache_len)
+    w = lib.layer_weights(c, t)
+    a = lib.layer_acts(c, t, cfg.kv_layout, cfg.cache_len)
+    dr1 = torch.from_numpy(ref["dR1"].astype(np.float32)).cuda()
+    dq = torch.empty(cfg.seq_len, cfg.q_dim, device="cuda")
+    dv = torch.empty(cfg.seq_len, cfg.kv_dim, device="cuda")
+    lib.attn_backward(c, cfg.seq_len, cfg.cache_len, dr1, w, a, dq, dv, ws)
+    # the oracle from the same float32 dR1 the GPU received
+    d2 = dict(d)
+    r2 = OL.attn_backward(cfg, d2, dr1.cpu().numpy())
+    rl, ma = tol(cfg)
+    check("dQpre", host(dq), r2["dQpre"], rl, ma)
+    check("dV", host(dv), r2["dV"], rl, ma)
+
+
+def test_lora_grad_adamw(lib, case):
+    import torch
+    cfg, d, ref = case
+    t = to_dev(d, cfg.wtype)
+    c = cfg_to_abi(lib, cfg)
+    adam = adam_to_abi(lib, cfg)
+    ws = lib.workspace(c, cfg.seq_len, cfg.cache_len)
+    for tag, G, out_dim in (("q", ref["dQpre"], cfg.q_dim), ("v", ref["dV"], cfg.kv_dim)):
+        Gf = G.astype(np.float32)
+        L = lora_dev(t)
+        grads = {"dA_" + tag: torch.empty_like(L["a_" + tag]), "dB_" + tag: torch.empty_like(L["b_" + tag])}
+        ss = torch.zeros(2, dtype=torch.float64, device="cuda")
+        lib.lora_grad_adamw(cfg.seq_len, out_dim, cfg.dim, cfg.rank, cfg.lora_alpha,
+                            torch.from_numpy(Gf).cuda(), t["lora_%s_h" % tag], t["x"],
+                            lib.lora(L, tag, grads), adam, ss, ws)
+        da, db, _ = ops.lora_backward(Gf, d["lora_%s_h" % tag], d["x"], d["b_" + tag], cfg.lora_alpha, cfg.rank)
+        check("dA_" + tag, host(grads["dA_" + tag]), da)
+        check("dB_" + tag, host(grads["dB_" + tag]), db)
+        for p, g, lr in (("a_" + tag, da, cfg.lr), ("b_" + tag, db, cfg.lr * cfg.lr_b_mult)):
+            rp, rm, rv = ops.adamw(d[p], g, d["m_" + p], d["v_" + p], lr, cfg.beta1, cfg.beta2,
+                                   cfg.adam_eps, cfg.weight_decay, cfg.step)
+            check(p, host(L[p]), rp)
+            check("m_" + p, host(L["m_" + p[0] + "_" + tag]), rm)
+            check("v_" + p, host(L["v_" + p[0] + "_" + tag]), rv)
+        s = ss.cpu().numpy()
+        assert abs(s[0] - np.sum(da ** 2)) <= 1e-5 * np.sum(da ** 2)
+        assert abs(s[1] - np.sum(db ** 2)) <= 1e-5 * np.sum(db ** 2)
+
+
+def test_layer_backward(lib, case):
+    import torch
+    cfg, d, ref = case
+    t = to_dev(d, cfg.wtype)
+    c = cfg_to_abi(lib, cfg)
+    adam = adam_to_abi(lib, cfg)
+    ws = lib.workspace(c, cfg.seq_len, cfg.cache_len)
+    L = lora_dev(t)
+    grads = {k: torch.empty_like(L[k.replace("dA_", "a_").replace("dB_", "b_")])
+             for k in ("dA_q", "dB_q", "dA_v", "dB_v")}
+    dh = t["dout"].clone()
+    ss = torch.zeros(2, dtype=torch.float64, device="cuda")
+    lib.layer_backward(c, cfg.seq_len, cfg.cache_len, lib.layer_weights(c, t),
+                       lib.layer_acts(c, t, cfg.kv_layout, cfg.cache_len), lib.lora(L, "q", grads),
+                       lib.lora(L, "v", grads), adam, dh, ss, ws)
+    lib.workspace_status(ws)
+    rl, ma = tol(cfg)
+    check("d_in", host(dh), ref["d_in"], rl, ma)
+    for k in ("dA_q", "dB_q", "dA_v", "dB_v"):
+        check(k, host(grads[k]), ref[k], rl, ma)
+    s = ss.cpu().numpy()
+    assert abs(s[0] - ref["sumsq_a"]) <= max(rl, 1e-5) * 2 * ref["sumsq_a"]
+    assert abs(s[1] - ref["sumsq_b"]) <= max(rl, 1e-5) * 2 * ref["sumsq_b"]
+    # parameters: AdamW of the GPU's own gradients must match to float32 accuracy
+    for tag in ("q", "v"):
+        for p, lr in (("a_" + tag, cfg.lr), ("b_" + tag, cfg.lr * cfg.lr_b_mult)):
+            g = host(grads["d" + p[0].upper() + "_" + tag])
+            rp, rm, rv = ops.adamw(d[p], g, d["m_" + p], d["v_" + p], lr, cfg.beta1, cfg.beta2,
+                                   cfg.adam_eps, cfg.weight_decay, cfg.step)
+            check(p, host(L[p]), rp)
+            check("m_" + p, host(L["m_" + p[0] + "_" + tag]), rm)
+            if rl <= 1e-5:
+                check(p + " vs oracle", host(L[p]), ref[p])
+
+
+def test_stack_of_layers(lib):
+    """Three tiny layers in reverse: the gradient of layer l feeds layer l - 1."""
+    import torch
+    cfg = TINY.with_(name="tiny_stack", n_layers=3)
+    layers = [layer_inputs(cfg, layer=l, seed=0, with_dout=(l == cfg.n_layers - 1)) for l in range(3)]
+    dout = layers[-1]["dout"]
+    ref = OL.stack_backward(cfg, layers, dout)
+    c = cfg_to_abi(lib, cfg)
+    adam = adam_to_abi(lib, cfg)
+    ws = lib.workspace(c, cfg.seq_len, cfg.cache_len)
+    dh = torch.from_numpy(dout).cuda()
+    ss = torch.zeros(2, dtype=torch.float64, device="cuda")
+    devs = []
+    for l in reversed(range(3)):
+        t = to_dev(layers[l], cfg.wtype)
+        L = lora_dev(t)
+        devs.append((l, L))
+        lib.layer_backward(c, cfg.seq_len, cfg.cache_len, lib.layer_weights(c, t),
+                           lib.layer_acts(c, t, cfg.kv_layout, cfg.cache_len), lib.lora(L, "q"),
+                           lib.lora(L, "v"), adam, dh, ss, ws)
+    check("stack d_in", host(dh), ref["d_in"])
+    gnorm = float(np.sqrt(ss[0].item()))
+    assert abs(gnorm - ref["gnorm"]) <= 1e-5 * ref["gnorm"]
+    for l, L in devs:
+        for p in ("a_q", "b_q", "a_v", "b_v"):
+            check("layer %d %s" % (l, p), host(L[p]), ref["layers"][l][p])

@@ -1,0 +1,65 @@
+"""CPU-side checks of the C ABI library: it builds for sm_103a, loads, exports every
+symbol the header declares, and rejects bad arguments on the host before any
+device work (no GPU needed: these paths return before the first CUDA call)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from transformer_layer_backward_gb300 import build, _abi
+    build.build()
+    return _abi.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "tlb.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const char \*|int |size_t )(tlb_\w+)\(", text, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("tlb_layer_backward", "tlb_attn_backward", "tlb_ffn_backward", "tlb_rmsnorm_backward",
+              "tlb_rope_backward", "tlb_lora_grad_adamw", "tlb_softmax_backward", "tlb_act_backward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from transformer_layer_backward_gb300 import _abi
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+        assert n in _abi.SIGNATURES, "binding lacks " + n
+
+
+def test_host_side_argument_errors(lib):
+    from transformer_layer_backward_gb300 import _abi as A
+    assert lib.tlb_softmax_backward(None, None, None, -1, 4, None) == A.TLB_EINVAL
+    assert b"negative" in lib.tlb_last_error()
+    assert lib.tlb_softmax_backward(None, None, None, 0, 0, None) == A.TLB_OK    # empty: no-op
+    assert lib.tlb_softmax_backward(None, None, None, 3, 4, None) == A.TLB_EINVAL
+    assert lib.tlb_act_backward(7, None, None, None, None, None, None, 4, None) == A.TLB_EINVAL
+    assert lib.tlb_rope_backward(None, None, 2, 2, 5, 0, 1e4, None) == A.TLB_EINVAL     # odd head_dim
+    assert lib.tlb_rope_backward(None, None, 2, 2, 512, 0, 1e4, None) == A.TLB_EUNSUPPORTED
+    assert lib.tlb_rmsnorm_backward(C.c_void_p(16), C.c_void_p(16), C.c_void_p(32), C.c_void_p(32),
+                                    1, 4, 1e-6, 1, None) == A.TLB_EINVAL                # alias + accumulate
+    bad = A.LayerCfg(64, 256, 4, 3, 16, 4, 8.0, 1e4, 1e-6, 0.25, 0, 0, 0)         # 4 heads, 3 kv heads
+    assert lib.tlb_workspace_bytes(C.byref(bad), 4, 4) > 0
+    assert lib.tlb_layer_backward(C.byref(bad), 4, 4, None, None, None, None, None, None, None, None, 0,
+                                  None) == A.TLB_EINVAL
+    assert b"n_kv_heads" in lib.tlb_last_error()
+    adam = A.AdamwCfg(1e-4, 0.9, 0.999, 1e-8, 0.0, 16.0, 0)
+    assert lib.tlb_adamw(C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), 4, C.byref(adam),
+                         1.0, None, None) == A.TLB_EINVAL                               # step 0
+
+
+def test_workspace_grows_with_rows(lib):
+    from transformer_layer_backward_gb300 import _abi as A
+    cfg = A.LayerCfg(2560, 9728, 32, 8, 128, 16, 32.0, 1e4, 1e-6, 128 ** -0.5, 1, 1, 4 | 8 | 32)
+    sizes = [lib.tlb_workspace_bytes(C.byref(cfg), s, s) for s in (1, 64, 512)]
+    assert sizes[0] < sizes[1] < sizes[2]
+    assert all(s % 256 == 0 for s in sizes)

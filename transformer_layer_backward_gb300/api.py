@@ -77,6 +77,21 @@ def rope_backward(dy, pos0, base=10000.0, out=None, stream=None):
     return out
 
 
+def linear_backward(wtype, W, dY, in_dim=None, scale=1.0, out=None, accumulate=False, stream=None):
+    """dX = scale * dY @ W^T for W stored [in, out] (wtype 'f32', 'bf16' or 'ternary')."""
+    code = {"f32": A.W_F32, "bf16": A.W_BF16, "ternary": A.W_TERNARY_I8}[wtype]
+    in_dim, out_dim = W.shape
+    S = dY.shape[0]
+    out = torch.zeros(S, in_dim, device=dY.device) if out is None else out
+    A.call("tlb_linear_backward", code, _ptr(W, _WDTYPE[code], "W"), float(scale), _ptr(dY, name="dY"),
+           S, out_dim, in_dim, _ptr(out, name="out"), 1 if accumulate else 0, _stream(stream))
+    return out
+
+
+def launch_count() -> int:
+    return int(A.load().tlb_launch_count())
+
+
 def adamw_cfg(lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1, lr_b_mult=16.0):
     return A.AdamwCfg(lr, beta1, beta2, eps, weight_decay, lr_b_mult, int(step))
 

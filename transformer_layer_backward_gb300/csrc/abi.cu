@@ -11,6 +11,7 @@
 namespace tlb {
 
 static thread_local char g_err[512] = "";
+static unsigned long long g_launches = 0;
 
 void set_error(const char *fmt, ...) {
     va_list ap;
@@ -22,6 +23,7 @@ void set_error(const char *fmt, ...) {
 void clear_error() { g_err[0] = '\0'; }
 
 int check_launch(const char *what) {
+    __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("%s: kernel launch failed: %s", what, cudaGetErrorString(e));
@@ -83,6 +85,19 @@ const char *tlb_build_info(void) {
     snprintf(info, sizeof(info), "tlb sm_103a build, CUDA %d.%d", CUDART_VERSION / 1000,
              (CUDART_VERSION % 1000) / 10);
     return info;
+}
+
+uint64_t tlb_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+int tlb_linear_backward(int32_t wtype, const void *W, float scale, const float *dY, int64_t S,
+                        int64_t out_dim, int64_t in_dim, float *dX, int32_t accumulate, void *stream) {
+    clear_error();
+    TLB_REQUIRE(wtype == TLB_W_F32 || wtype == TLB_W_BF16 || wtype == TLB_W_TERNARY_I8, TLB_EINVAL,
+                "linear_backward: unknown weight type %d", wtype);
+    TLB_REQUIRE(S >= 0 && out_dim >= 0 && in_dim >= 0, TLB_EINVAL, "linear_backward: negative size");
+    if (S == 0 || in_dim == 0) return TLB_OK;
+    TLB_REQUIRE(W && dX && (dY || out_dim == 0), TLB_EINVAL, "linear_backward: null pointer");
+    return linear_t_launch(wtype, W, scale, dY, S, out_dim, in_dim, dX, accumulate != 0, as_stream(stream));
 }
 
 int tlb_softmax_backward(const float *attn, const float *dattn, float *dscores, int64_t rows,

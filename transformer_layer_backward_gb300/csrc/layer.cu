@@ -1,0 +1,239 @@
+// Composition of the layer backward and the layer-level extern "C" entry points:
+// FFN backward ([FFN] "Backward (reverse)", executeFFNBackward; [RS] FFN part of
+// backward_through_layers), attention backward ([ATT] "Gradient Flow"; [RS]
+// attention block), LoRA Q/V gradients with AdamW ([RS] LoRA blocks, cpu_adamw).
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace tlb {
+
+namespace {
+
+struct LayerWs {
+    size_t dF, dG, dU, dN2, dSub, dqpre, dv, gh_q, gh_v, total;
+};
+
+LayerWs plan(const tlb_layer_cfg &c, int64_t S) {
+    WsPlan p;
+    LayerWs w;
+    const int64_t I = c.ffn_dim, H = c.dim, qd = int64_t(c.n_heads) * c.head_dim;
+    const int64_t kvd = int64_t(c.n_kv_heads) * c.head_dim;
+    w.dF = p.take(S * I * 4);
+    w.dG = p.take(S * I * 4);
+    w.dU = p.take(S * I * 4);
+    w.dN2 = p.take(S * H * 4);
+    w.dSub = p.take(S * qd * 4);
+    w.dqpre = p.take(S * qd * 4);
+    w.dv = p.take(S * kvd * 4);
+    w.gh_q = p.take(S * c.rank * 4);
+    w.gh_v = p.take(S * c.rank * 4);
+    w.total = p.off;
+    return w;
+}
+
+int validate_cfg(const tlb_layer_cfg *c) {
+    TLB_REQUIRE(c != nullptr, TLB_EINVAL, "layer cfg is NULL");
+    TLB_REQUIRE(c->dim > 0 && c->ffn_dim > 0 && c->n_heads > 0 && c->n_kv_heads > 0 && c->head_dim > 0,
+                TLB_EINVAL, "layer cfg: dimensions must be positive");
+    TLB_REQUIRE(c->n_heads % c->n_kv_heads == 0, TLB_EINVAL,
+                "layer cfg: n_heads (%d) not a multiple of n_kv_heads (%d)", c->n_heads, c->n_kv_heads);
+    TLB_REQUIRE(c->head_dim % 2 == 0, TLB_EINVAL, "layer cfg: head_dim must be even");
+    TLB_REQUIRE(c->head_dim <= 256, TLB_EUNSUPPORTED, "layer cfg: head_dim > 256");
+    TLB_REQUIRE(c->rank >= 1 && c->rank <= 64, TLB_EINVAL, "layer cfg: rank must be in 1..64");
+    TLB_REQUIRE(c->act == TLB_ACT_RELU2_MUL || c->act == TLB_ACT_SILU_MUL, TLB_EINVAL,
+                "layer cfg: unknown activation %d", c->act);
+    TLB_REQUIRE(c->wtype == TLB_W_F32 || c->wtype == TLB_W_BF16 || c->wtype == TLB_W_TERNARY_I8, TLB_EINVAL,
+                "layer cfg: unknown weight type %d", c->wtype);
+    return TLB_OK;
+}
+
+int validate_ws(const tlb_layer_cfg *c, int64_t S, void *ws, size_t ws_bytes) {
+    const size_t need = plan(*c, S).total;
+    TLB_REQUIRE(ws != nullptr && ws_bytes >= need, TLB_EINVAL,
+                "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
+    TLB_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, TLB_EINVAL, "workspace not 256-byte aligned");
+    return TLB_OK;
+}
+
+int ffn_impl(const tlb_layer_cfg &c, int64_t S, const float *d_out, const tlb_layer_weights &w,
+             const tlb_layer_acts &a, float *d_res, void *ws, cudaStream_t st) {
+    const LayerWs p = plan(c, S);
+    const int64_t I = c.ffn_dim, H = c.dim;
+    float *dF = ws_at<float>(ws, p.dF), *dG = ws_at<float>(ws, p.dG), *dU = ws_at<float>(ws, p.dU);
+    // dF = dOut W_down^T
+    TLB_TRY(linear_t_launch(c.wtype, w.w_down.w, w.w_down.scale, d_out, S, H, I, dF, false, st));
+    // dh = RMSNorm_bwd(hidden, gamma, dF) (sub-norm), in place
+    if (c.flags & TLB_SUB_NORM)
+        TLB_TRY(rmsnorm_backward_launch(a.hidden, w.gamma_sub_ffn, dF, dF, S, I, c.norm_eps, 0, st));
+    // dG, dU = activation backward
+    const float *sg = (c.act == TLB_ACT_SILU_MUL && (c.flags & TLB_USE_SILU_CACHE)) ? a.silu_gate : nullptr;
+    TLB_TRY(act_backward_launch(c.act, a.gate, a.up, sg, dF, dG, dU, S * I, st));
+    const bool resid = (c.flags & TLB_RESIDUAL) != 0;
+    if (resid && d_res != d_out)
+        TLB_CUDA(cudaMemcpyAsync(d_res, d_out, size_t(S * H) * 4, cudaMemcpyDeviceToDevice, st));
+    if (c.flags & TLB_PRE_NORM) {
+        float *dN2 = ws_at<float>(ws, p.dN2);
+        TLB_TRY(linear_t_launch(c.wtype, w.w_gate.w, w.w_gate.scale, dG, S, I, H, dN2, false, st));
+        TLB_TRY(linear_t_launch(c.wtype, w.w_up.w, w.w_up.scale, dU, S, I, H, dN2, true, st));
+        // dResidual (+)= RMSNorm_bwd(r1, gamma_ffn, dN2)
+        TLB_TRY(rmsnorm_backward_launch(a.r1, w.gamma_ffn, dN2, d_res, S, H, c.norm_eps, resid ? 1 : 0, st));
+    } else {
+        TLB_TRY(linear_t_launch(c.wtype, w.w_gate.w, w.w_gate.scale, dG, S, I, H, d_res, resid, st));
+        TLB_TRY(linear_t_launch(c.wtype, w.w_up.w, w.w_up.scale, dU, S, I, H, d_res, true, st));
+    }
+    return TLB_OK;
+}
+
+int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, const tlb_layer_weights &w,
+              const tlb_layer_acts &a, float *d_qpre, float *d_v, void *ws, cudaStream_t st) {
+    const LayerWs p = plan(c, S);
+    const int64_t qd = int64_t(c.n_heads) * c.head_dim;
+    float *dSub = ws_at<float>(ws, p.dSub);
+    // dSub = dR1 W_O^T
+    TLB_TRY(linear_t_launch(c.wtype, w.w_o.w, w.w_o.scale, dR1, S, c.dim, qd, dSub, false, st));
+    // dCtx = RMSNorm_bwd(ctx, gamma_sub_attn, dSub) (sub-norm), in place
+    if (c.flags & TLB_SUB_NORM)
+        TLB_TRY(rmsnorm_backward_launch(a.ctx, w.gamma_sub_attn, dSub, dSub, S, qd, c.norm_eps, 0, st));
+    AttnArgs g;
+    g.dctx = dSub;
+    g.k = a.k;
+    g.v = a.v;
+    g.sh = a.kv_stride_head;
+    g.sp = a.kv_stride_pos;
+    g.attn = a.attn;
+    g.dq = d_qpre;
+    g.dv = d_v;
+    g.S = int(S);
+    g.L = int(L);
+    g.nh = c.n_heads;
+    g.nkv = c.n_kv_heads;
+    g.hd = c.head_dim;
+    g.pos0 = int(L - S);
+    g.causal = (c.flags & TLB_CAUSAL) ? 1 : 0;
+    g.rope = (c.flags & TLB_ROPE) ? 1 : 0;
+    g.scale = c.attn_scale;
+    return attn_core_launch(g, c.rope_base, st);
+}
+
+int check_acts_ffn(const tlb_layer_cfg &c, const tlb_layer_weights *w, const tlb_layer_acts *a) {
+    TLB_REQUIRE(w && a, TLB_EINVAL, "weights / activations struct is NULL");
+    TLB_REQUIRE(w->w_down.w && w->w_gate.w && w->w_up.w, TLB_EINVAL, "FFN weight pointer is NULL");
+    TLB_REQUIRE(a->gate && a->up, TLB_EINVAL, "gate / up activation is NULL");
+    if (c.flags & TLB_SUB_NORM)
+        TLB_REQUIRE(a->hidden && w->gamma_sub_ffn, TLB_EINVAL, "SUB_NORM needs hidden and gamma_sub_ffn");
+    if (c.flags & TLB_PRE_NORM)
+        TLB_REQUIRE(a->r1 && w->gamma_ffn, TLB_EINVAL, "PRE_NORM needs r1 and gamma_ffn");
+    if (c.act == TLB_ACT_SILU_MUL && (c.flags & TLB_USE_SILU_CACHE))
+        TLB_REQUIRE(a->silu_gate, TLB_EINVAL, "USE_SILU_CACHE needs silu_gate");
+    return TLB_OK;
+}
+
+int check_acts_attn(const tlb_layer_cfg &c, int64_t S, int64_t L, const tlb_layer_weights *w,
+                    const tlb_layer_acts *a) {
+    TLB_REQUIRE(w && a, TLB_EINVAL, "weights / activations struct is NULL");
+    TLB_REQUIRE(L >= S && S >= 0, TLB_EINVAL, "need 0 <= S <= L (S=%lld, L=%lld)", (long long)S, (long long)L);
+    TLB_REQUIRE(L < (int64_t(1) << 24), TLB_EUNSUPPORTED, "cache length >= 2^24");
+    TLB_REQUIRE(w->w_o.w && a->k && a->v && a->attn, TLB_EINVAL, "W_O / K / V / attn pointer is NULL");
+    TLB_REQUIRE(a->kv_stride_pos >= c.head_dim && a->kv_stride_head >= c.head_dim, TLB_EINVAL,
+                "K/V strides smaller than head_dim");
+    if (c.flags & TLB_SUB_NORM)
+        TLB_REQUIRE(a->ctx && w->gamma_sub_attn, TLB_EINVAL, "SUB_NORM needs ctx and gamma_sub_attn");
+    return TLB_OK;
+}
+
+int check_lora(const tlb_lora *l, const char *tag) {
+    TLB_REQUIRE(l && l->a && l->b && l->m_a && l->v_a && l->m_b && l->v_b, TLB_EINVAL,
+                "LoRA %s adapter: NULL pointer", tag);
+    return TLB_OK;
+}
+
+int check_adam(const tlb_adamw_cfg *a) {
+    TLB_REQUIRE(a != nullptr, TLB_EINVAL, "adamw cfg is NULL");
+    TLB_REQUIRE(a->step >= 1, TLB_EINVAL, "adamw step must be >= 1");
+    return TLB_OK;
+}
+
+}  // namespace
+}  // namespace tlb
+
+using namespace tlb;
+
+extern "C" {
+
+size_t tlb_workspace_bytes(const tlb_layer_cfg *cfg, int64_t S, int64_t L) {
+    (void)L;
+    if (cfg == nullptr || S < 0) return 0;
+    return plan(*cfg, S).total;
+}
+
+int tlb_ffn_backward(const tlb_layer_cfg *cfg, int64_t S, const float *d_out, const tlb_layer_weights *w,
+                     const tlb_layer_acts *acts, float *d_residual, void *ws, size_t ws_bytes, void *stream) {
+    clear_error();
+    TLB_TRY(validate_cfg(cfg));
+    TLB_REQUIRE(S >= 0, TLB_EINVAL, "ffn_backward: negative S");
+    if (S == 0) return TLB_OK;
+    TLB_REQUIRE(d_out && d_residual, TLB_EINVAL, "ffn_backward: NULL gradient pointer");
+    TLB_TRY(check_acts_ffn(*cfg, w, acts));
+    TLB_TRY(validate_ws(cfg, S, ws, ws_bytes));
+    return ffn_impl(*cfg, S, d_out, *w, *acts, d_residual, ws, as_stream(stream));
+}
+
+int tlb_attn_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const float *d_attn_out,
+                      const tlb_layer_weights *w, const tlb_layer_acts *acts, float *d_qpre, float *d_v,
+                      void *ws, size_t ws_bytes, void *stream) {
+    clear_error();
+    TLB_TRY(validate_cfg(cfg));
+    TLB_TRY(check_acts_attn(*cfg, S, L, w, acts));
+    if (S == 0) return TLB_OK;
+    TLB_REQUIRE(d_attn_out && d_qpre && d_v, TLB_EINVAL, "attn_backward: NULL gradient pointer");
+    TLB_TRY(validate_ws(cfg, S, ws, ws_bytes));
+    return attn_impl(*cfg, S, L, d_attn_out, *w, *acts, d_qpre, d_v, ws, as_stream(stream));
+}
+
+int tlb_lora_grad_adamw(int64_t S, int32_t out_dim, int32_t in_dim, int32_t rank, float alpha, const float *G,
+                        const float *h, const float *x, const tlb_lora *lora, const tlb_adamw_cfg *adam,
+                        double *sumsq, void *ws, size_t ws_bytes, void *stream) {
+    clear_error();
+    TLB_REQUIRE(S >= 0 && out_dim > 0 && in_dim > 0, TLB_EINVAL, "lora_grad_adamw: bad sizes");
+    TLB_REQUIRE(rank >= 1 && rank <= 64, TLB_EINVAL, "lora_grad_adamw: rank must be in 1..64");
+    TLB_TRY(check_lora(lora, "(lora_grad_adamw)"));
+    TLB_TRY(check_adam(adam));
+    TLB_REQUIRE(S == 0 || (G && h && x), TLB_EINVAL, "lora_grad_adamw: NULL input");
+    const size_t need = kStatusBytes + ((size_t(S) * rank * 4 + 255) & ~size_t(255));
+    TLB_REQUIRE(ws && ws_bytes >= need, TLB_EINVAL, "lora_grad_adamw: workspace smaller than %zu bytes", need);
+    if (S == 0) {
+        // no rows: zero gradients, AdamW still decays and moves the moments
+    }
+    float *gh = ws_at<float>(ws, kStatusBytes);
+    return lora_launch(S, out_dim, in_dim, rank, alpha, G, h, x, *lora, *adam, sumsq, gh, as_stream(stream));
+}
+
+int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb_layer_weights *w,
+                       const tlb_layer_acts *acts, const tlb_lora *lora_q, const tlb_lora *lora_v,
+                       const tlb_adamw_cfg *adam, float *d_hidden, double *sumsq, void *ws, size_t ws_bytes,
+                       void *stream) {
+    clear_error();
+    TLB_TRY(validate_cfg(cfg));
+    TLB_TRY(check_acts_ffn(*cfg, w, acts));
+    TLB_TRY(check_acts_attn(*cfg, S, L, w, acts));
+    TLB_TRY(check_lora(lora_q, "Q"));
+    TLB_TRY(check_lora(lora_v, "V"));
+    TLB_TRY(check_adam(adam));
+    if (S == 0) return TLB_OK;
+    TLB_REQUIRE(d_hidden && acts->x && acts->lora_q_h && acts->lora_v_h, TLB_EINVAL,
+                "layer_backward: NULL d_hidden / x / lora_q_h / lora_v_h");
+    TLB_TRY(validate_ws(cfg, S, ws, ws_bytes));
+    cudaStream_t st = as_stream(stream);
+    const tlb_layer_cfg &c = *cfg;
+    const LayerWs p = plan(c, S);
+    const int qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
+    float *dqpre = ws_at<float>(ws, p.dqpre), *dv = ws_at<float>(ws, p.dv);
+    TLB_TRY(ffn_impl(c, S, d_hidden, *w, *acts, d_hidden, ws, st));
+    TLB_TRY(attn_impl(c, S, L, d_hidden, *w, *acts, dqpre, dv, ws, st));
+    TLB_TRY(lora_launch(S, qd, c.dim, c.rank, c.lora_alpha, dqpre, acts->lora_q_h, acts->x, *lora_q, *adam,
+                        sumsq, ws_at<float>(ws, p.gh_q), st));
+    return lora_launch(S, kvd, c.dim, c.rank, c.lora_alpha, dv, acts->lora_v_h, acts->x, *lora_v, *adam, sumsq,
+                       ws_at<float>(ws, p.gh_v), st);
+}
+
+}  // extern "C"
