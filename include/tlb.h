@@ -126,9 +126,11 @@ typedef struct {
     float *grad_a, *grad_b;
 } tlb_lora;
 
-/* [RS] cpu_adamw hyperparameters; B of each adapter uses lr * lr_b_mult (LoRA+, 16 on the page). */
+/* [RS] cpu_adamw hyperparameters; B of each adapter uses lr * lr_b_mult (LoRA+, 16 on the page).
+ * Held in double so that 1 - beta and the bias corrections are exact before the kernels
+ * round them to float once (0.999f alone is 1.3e-5 away from 0.999 in 1 - beta2). */
 typedef struct {
-    float lr, beta1, beta2, eps, weight_decay, lr_b_mult;
+    double lr, beta1, beta2, eps, weight_decay, lr_b_mult;
     int32_t step;            /* >= 1; bias corrections 1/(1 - beta^step) */
 } tlb_adamw_cfg;
 

@@ -112,3 +112,28 @@ def test_adamw(lib, n, step):
     check("m", host(tm), rm)
     check("v", host(tv), rv)
     assert abs(float(ss.item()) - float(np.sum(g.astype(np.float64) ** 2))) <= 1e-5 * float(np.sum(g.astype(np.float64) ** 2))
+
+
+@pytest.mark.parametrize("wtype", ["f32", "bf16", "ternary"])
+@pytest.mark.parametrize("S,in_dim,out_dim", [(1, 640, 2560), (1, 37, 50), (3, 100, 64), (130, 96, 272),
+                                              (1, 6912, 2560)])
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_linear_backward(lib, wtype, S, in_dim, out_dim, accumulate):
+    import torch
+    shape = (in_dim, out_dim)
+    if wtype == "ternary":
+        W = rng.ternary(rng.stream_key(0, "steps", "wt", *shape), in_dim * out_dim).reshape(shape)
+        Wt = torch.from_numpy(W).cuda()
+    else:
+        W = normal("w", shape, 0.05)
+        if wtype == "bf16":
+            W = rng.round_to_bf16(W)
+            Wt = torch.from_numpy(W).cuda().to(torch.bfloat16)
+        else:
+            Wt = torch.from_numpy(W).cuda()
+    dY = normal("dy_lin", (S, out_dim))
+    base = normal("base_lin", (S, in_dim))
+    out = dev(base.copy())
+    lib.linear_backward(wtype, Wt, dev(dY), scale=1.25, out=out, accumulate=accumulate)
+    ref = ops.linear_backward(dY, W, 1.25) + (base if accumulate else 0.0)
+    check("dX", host(out), ref)

@@ -46,8 +46,9 @@ class Lora(C.Structure):
 
 
 class AdamwCfg(C.Structure):
-    _fields_ = [("lr", f32), ("beta1", f32), ("beta2", f32), ("eps", f32),
-                ("weight_decay", f32), ("lr_b_mult", f32), ("step", i32)]
+    _fields_ = [("lr", C.c_double), ("beta1", C.c_double), ("beta2", C.c_double),
+                ("eps", C.c_double), ("weight_decay", C.c_double), ("lr_b_mult", C.c_double),
+                ("step", i32)]
 
 
 P = C.POINTER

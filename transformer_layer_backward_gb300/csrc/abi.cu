@@ -62,11 +62,13 @@ void rope_freqs(RopeFreqs &f, int head_dim, float base) {
 
 AdamCoef adam_coef(const tlb_adamw_cfg &c, float lr_mult) {
     AdamCoef k;
-    k.lr = c.lr * lr_mult;
-    k.beta1 = c.beta1;
-    k.beta2 = c.beta2;
-    k.eps = c.eps;
-    k.wd = c.weight_decay;
+    k.lr = float(c.lr * double(lr_mult));
+    k.beta1 = float(c.beta1);
+    k.beta2 = float(c.beta2);
+    k.omb1 = float(1.0 - c.beta1);
+    k.omb2 = float(1.0 - c.beta2);
+    k.eps = float(c.eps);
+    k.wd = float(c.weight_decay);
     k.bc1 = float(1.0 / (1.0 - std::pow(double(c.beta1), double(c.step))));
     k.bc2 = float(1.0 / (1.0 - std::pow(double(c.beta2), double(c.step))));
     return k;

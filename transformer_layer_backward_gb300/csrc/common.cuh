@@ -139,7 +139,7 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) {
 __device__ __forceinline__ void i8x4_to_f32(uint32_t w, float &a, float &b, float &c, float &d) {
     const uint32_t u = w ^ 0x80808080u;
     const float bias = 8388736.0f;   // 2^23 + 128
-    a = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7654)) - bias;
+    a = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - bias;
     b = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - bias;
     c = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - bias;
     d = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - bias;
@@ -190,15 +190,16 @@ struct RopeFreqs {
 };
 void rope_freqs(RopeFreqs &f, int head_dim, float base);
 
-// AdamW constants of one parameter tensor ([RS] cpu_adamw).
+// AdamW constants of one parameter tensor ([RS] cpu_adamw).  1 - beta and the bias
+// corrections are formed in double on the host and rounded once.
 struct AdamCoef {
-    float lr, beta1, beta2, eps, wd, bc1, bc2;
+    float lr, beta1, beta2, omb1, omb2, eps, wd, bc1, bc2;
 };
 AdamCoef adam_coef(const tlb_adamw_cfg &c, float lr_mult);
 
 __device__ __forceinline__ float adam_elem(float p, float g, float &m, float &v, const AdamCoef &k) {
-    m = k.beta1 * m + (1.f - k.beta1) * g;
-    v = k.beta2 * v + (1.f - k.beta2) * g * g;
+    m = k.beta1 * m + k.omb1 * g;
+    v = k.beta2 * v + k.omb2 * g * g;
     const float mh = m * k.bc1, vh = v * k.bc2;
     return p - k.lr * (mh / (sqrtf(vh) + k.eps) + k.wd * p);
 }

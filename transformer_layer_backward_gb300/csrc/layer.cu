@@ -4,16 +4,19 @@
 // attention block), LoRA Q/V gradients with AdamW ([RS] LoRA blocks, cpu_adamw).
 #include "common.cuh"
 #include "kernels.cuh"
+#include "decode.cuh"
 
 namespace tlb {
 
 namespace {
 
 struct LayerWs {
-    size_t dF, dG, dU, dN2, dSub, dqpre, dv, gh_q, gh_v, total;
+    size_t dF, dG, dU, dN2, dSub, dqpre, dv, gh_q, gh_v;
+    size_t dR1, dctx, dattn, Dpart, dqpart, gh2;   // single-token path
+    size_t total;
 };
 
-LayerWs plan(const tlb_layer_cfg &c, int64_t S) {
+LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     WsPlan p;
     LayerWs w;
     const int64_t I = c.ffn_dim, H = c.dim, qd = int64_t(c.n_heads) * c.head_dim;
@@ -27,6 +30,17 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S) {
     w.dv = p.take(S * kvd * 4);
     w.gh_q = p.take(S * c.rank * 4);
     w.gh_v = p.take(S * c.rank * 4);
+    if (S == 1) {
+        const int64_t nchunks = ceil_div(L, kDecodeChunk);
+        w.dR1 = p.take(H * 4);
+        w.dctx = p.take(qd * 4);
+        w.dattn = p.take(int64_t(c.n_heads) * L * 4);
+        w.Dpart = p.take(nchunks * c.n_heads * 4);
+        w.dqpart = p.take(nchunks * qd * 4);
+        w.gh2 = p.take(2 * int64_t(c.rank) * 4);
+    } else {
+        w.dR1 = w.dctx = w.dattn = w.Dpart = w.dqpart = w.gh2 = 0;
+    }
     w.total = p.off;
     return w;
 }
@@ -47,8 +61,8 @@ int validate_cfg(const tlb_layer_cfg *c) {
     return TLB_OK;
 }
 
-int validate_ws(const tlb_layer_cfg *c, int64_t S, void *ws, size_t ws_bytes) {
-    const size_t need = plan(*c, S).total;
+int validate_ws(const tlb_layer_cfg *c, int64_t S, int64_t L, void *ws, size_t ws_bytes) {
+    const size_t need = plan(*c, S, L).total;
     TLB_REQUIRE(ws != nullptr && ws_bytes >= need, TLB_EINVAL,
                 "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
     TLB_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, TLB_EINVAL, "workspace not 256-byte aligned");
@@ -57,7 +71,7 @@ int validate_ws(const tlb_layer_cfg *c, int64_t S, void *ws, size_t ws_bytes) {
 
 int ffn_impl(const tlb_layer_cfg &c, int64_t S, const float *d_out, const tlb_layer_weights &w,
              const tlb_layer_acts &a, float *d_res, void *ws, cudaStream_t st) {
-    const LayerWs p = plan(c, S);
+    const LayerWs p = plan(c, S, S);   // the FFN regions do not depend on L
     const int64_t I = c.ffn_dim, H = c.dim;
     float *dF = ws_at<float>(ws, p.dF), *dG = ws_at<float>(ws, p.dG), *dU = ws_at<float>(ws, p.dU);
     // dF = dOut W_down^T
@@ -86,7 +100,7 @@ int ffn_impl(const tlb_layer_cfg &c, int64_t S, const float *d_out, const tlb_la
 
 int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, const tlb_layer_weights &w,
               const tlb_layer_acts &a, float *d_qpre, float *d_v, void *ws, cudaStream_t st) {
-    const LayerWs p = plan(c, S);
+    const LayerWs p = plan(c, S, L);
     const int64_t qd = int64_t(c.n_heads) * c.head_dim;
     float *dSub = ws_at<float>(ws, p.dSub);
     // dSub = dR1 W_O^T
@@ -161,9 +175,8 @@ using namespace tlb;
 extern "C" {
 
 size_t tlb_workspace_bytes(const tlb_layer_cfg *cfg, int64_t S, int64_t L) {
-    (void)L;
     if (cfg == nullptr || S < 0) return 0;
-    return plan(*cfg, S).total;
+    return plan(*cfg, S, L < S ? S : L).total;
 }
 
 int tlb_ffn_backward(const tlb_layer_cfg *cfg, int64_t S, const float *d_out, const tlb_layer_weights *w,
@@ -174,7 +187,7 @@ int tlb_ffn_backward(const tlb_layer_cfg *cfg, int64_t S, const float *d_out, co
     if (S == 0) return TLB_OK;
     TLB_REQUIRE(d_out && d_residual, TLB_EINVAL, "ffn_backward: NULL gradient pointer");
     TLB_TRY(check_acts_ffn(*cfg, w, acts));
-    TLB_TRY(validate_ws(cfg, S, ws, ws_bytes));
+    TLB_TRY(validate_ws(cfg, S, S, ws, ws_bytes));
     return ffn_impl(*cfg, S, d_out, *w, *acts, d_residual, ws, as_stream(stream));
 }
 
@@ -186,7 +199,7 @@ int tlb_attn_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const floa
     TLB_TRY(check_acts_attn(*cfg, S, L, w, acts));
     if (S == 0) return TLB_OK;
     TLB_REQUIRE(d_attn_out && d_qpre && d_v, TLB_EINVAL, "attn_backward: NULL gradient pointer");
-    TLB_TRY(validate_ws(cfg, S, ws, ws_bytes));
+    TLB_TRY(validate_ws(cfg, S, L, ws, ws_bytes));
     return attn_impl(*cfg, S, L, d_attn_out, *w, *acts, d_qpre, d_v, ws, as_stream(stream));
 }
 
@@ -222,12 +235,77 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
     if (S == 0) return TLB_OK;
     TLB_REQUIRE(d_hidden && acts->x && acts->lora_q_h && acts->lora_v_h, TLB_EINVAL,
                 "layer_backward: NULL d_hidden / x / lora_q_h / lora_v_h");
-    TLB_TRY(validate_ws(cfg, S, ws, ws_bytes));
+    TLB_TRY(validate_ws(cfg, S, L, ws, ws_bytes));
     cudaStream_t st = as_stream(stream);
     const tlb_layer_cfg &c = *cfg;
-    const LayerWs p = plan(c, S);
+    const LayerWs p = plan(c, S, L);
     const int qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
     float *dqpre = ws_at<float>(ws, p.dqpre), *dv = ws_at<float>(ws, p.dv);
+    if (decode_supported(c, S, L) && aligned16(w->w_down.w) && aligned16(w->w_gate.w) &&
+        aligned16(w->w_up.w) && aligned16(w->w_o.w)) {
+        DecodeArgs d;
+        d.H = c.dim;
+        d.I = c.ffn_dim;
+        d.qd = qd;
+        d.kvd = kvd;
+        d.nh = c.n_heads;
+        d.nkv = c.n_kv_heads;
+        d.hd = c.head_dim;
+        d.L = int(L);
+        d.rank = c.rank;
+        d.flags = c.flags;
+        d.act = c.act;
+        d.pos = int(L - 1);
+        d.chunk = kDecodeChunk;
+        d.nchunks = int(ceil_div(L, kDecodeChunk));
+        d.eps = c.norm_eps;
+        d.scale = c.attn_scale;
+        d.lora_scaling = c.lora_alpha / float(c.rank);
+        d.rope_base = c.rope_base;
+        d.w_down = w->w_down.w;
+        d.w_gate = w->w_gate.w;
+        d.w_up = w->w_up.w;
+        d.w_o = w->w_o.w;
+        d.s_down = w->w_down.scale;
+        d.s_gate = w->w_gate.scale;
+        d.s_up = w->w_up.scale;
+        d.s_o = w->w_o.scale;
+        d.g_sub_ffn = w->gamma_sub_ffn;
+        d.g_ffn = w->gamma_ffn;
+        d.g_sub_attn = w->gamma_sub_attn;
+        d.x = acts->x;
+        d.gate = acts->gate;
+        d.up = acts->up;
+        d.silu_gate = acts->silu_gate;
+        d.hidden = acts->hidden;
+        d.r1 = acts->r1;
+        d.ctx = acts->ctx;
+        d.k = acts->k;
+        d.v = acts->v;
+        d.attn = acts->attn;
+        d.hq = acts->lora_q_h;
+        d.hv = acts->lora_v_h;
+        d.sh = acts->kv_stride_head;
+        d.sp = acts->kv_stride_pos;
+        d.d_hidden = d_hidden;
+        d.dF = ws_at<float>(ws, p.dF);
+        d.dN2 = ws_at<float>(ws, p.dN2);
+        d.dR1 = ws_at<float>(ws, p.dR1);
+        d.dSub = ws_at<float>(ws, p.dSub);
+        d.dctx = ws_at<float>(ws, p.dctx);
+        d.dattn = ws_at<float>(ws, p.dattn);
+        d.Dpart = ws_at<float>(ws, p.Dpart);
+        d.dqpart = ws_at<float>(ws, p.dqpart);
+        d.dqpre = dqpre;
+        d.dv = dv;
+        d.gh = ws_at<float>(ws, p.gh2);    // [gh_q | gh_v], 2 * rank floats
+        d.lq = *lora_q;
+        d.lv = *lora_v;
+        d.ka = adam_coef(*adam, 1.0f);
+        d.kb = adam_coef(*adam, float(adam->lr_b_mult));
+        d.sumsq = sumsq;
+        return decode_layer_launch(d, c.wtype, st);
+    }
     TLB_TRY(ffn_impl(c, S, d_hidden, *w, *acts, d_hidden, ws, st));
     TLB_TRY(attn_impl(c, S, L, d_hidden, *w, *acts, dqpre, dv, ws, st));
     TLB_TRY(lora_launch(S, qd, c.dim, c.rank, c.lora_alpha, dqpre, acts->lora_q_h, acts->x, *lora_q, *adam,
