@@ -274,7 +274,7 @@ def main():
     # end to end through the public API: per-step activations from pinned host memory,
     # d_in and the gradient norm read back every step
     e2e = None
-    if rank == 0 or world > 1:
+    if args.e2e_steps > 0:
         acts = ("x", "gate", "up", "hidden", "r1", "ctx", "k", "v", "attn", "lora_q_h", "lora_v_h", "dout")
         pinned = [{k: torch.from_numpy(np.ascontiguousarray(host_layers[l][k])).pin_memory() for k in acts}
                   for l in range(NL)]
