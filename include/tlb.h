@@ -227,6 +227,23 @@ int tlb_lora_grad_adamw(int64_t S, int32_t out_dim, int32_t in_dim, int32_t rank
                         const tlb_adamw_cfg *adam, double *sumsq, void *ws, size_t ws_bytes,
                         void *stream);
 
+/* Same result as tlb_lora_grad_adamw, for callers that cannot allocate device memory
+ * and so have no workspace to pass (for example code running under an allocator it
+ * does not control, or where a cudaMalloc would synchronise the device).  The pages
+ * have no counterpart: it exists only for such callers.  Its one scratch buffer, the
+ * [S, rank] rows gh, is a fixed 65536-float (256 KiB) array inside the library that
+ * every GPU loading the library keeps until the process exits.
+ *   - S * rank must not exceed 65536; larger calls fail with TLB_EINVAL.
+ *   - It allocates and frees nothing.  The first call on each device looks up the
+ *     array's device address with that device current; make that first call before
+ *     any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents (every call
+ *     overwrites the rows it uses before reading them): calls that overlap on the GPU,
+ *     on different streams, race and give wrong results.  Serialise them. */
+int tlb_lora_grad_adamw_noalloc(int64_t S, int32_t out_dim, int32_t in_dim, int32_t rank, float alpha,
+                                const float *G, const float *h, const float *x, const tlb_lora *lora,
+                                const tlb_adamw_cfg *adam, double *sumsq, void *stream);
+
 /* One whole layer: FFN backward, attention backward, LoRA Q/V gradients and AdamW.
  * d_hidden [S, dim] in/out: dOut on entry, the gradient for the layer below (dR1) on
  * return ([RS] grad_hidden).  sumsq (device double[2]) += {sum dA^2, sum dB^2} over both

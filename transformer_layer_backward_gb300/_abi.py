@@ -70,6 +70,8 @@ SIGNATURES = {
                                     vp, vp, sz, vp]),
     "tlb_lora_grad_adamw": (C.c_int, [i64, i32, i32, i32, f32, vp, vp, vp, P(Lora), P(AdamwCfg),
                                       vp, vp, sz, vp]),
+    "tlb_lora_grad_adamw_noalloc": (C.c_int, [i64, i32, i32, i32, f32, vp, vp, vp, P(Lora),
+                                              P(AdamwCfg), vp, vp]),
     "tlb_layer_backward": (C.c_int, [P(LayerCfg), i64, i64, P(LayerWeights), P(LayerActs),
                                      P(Lora), P(Lora), P(AdamwCfg), vp, vp, vp, sz, vp]),
 }

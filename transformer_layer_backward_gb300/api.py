@@ -185,6 +185,16 @@ def lora_grad_adamw(S, out_dim, in_dim, rank, alpha, G, h, x, lora_: A.Lora, ada
            _stream(stream))
 
 
+def lora_grad_adamw_noalloc(S, out_dim, in_dim, rank, alpha, G, h, x, lora_: A.Lora, adam: A.AdamwCfg,
+                            sumsq, stream=None):
+    """lora_grad_adamw without a workspace: for callers that cannot allocate device memory.
+    Its scratch is a fixed array inside the library (S * rank <= 65536); calls sharing it
+    must not overlap on the GPU."""
+    A.call("tlb_lora_grad_adamw_noalloc", int(S), int(out_dim), int(in_dim), int(rank), float(alpha),
+           _ptr(G, name="G"), _ptr(h, name="h"), _ptr(x, name="x"), C.byref(lora_), C.byref(adam),
+           _ptr(sumsq, torch.float64, "sumsq"), _stream(stream))
+
+
 def layer_backward(cfg, S, L, weights, acts, lora_q, lora_v, adam, d_hidden, sumsq, ws, stream=None):
     A.call("tlb_layer_backward", C.byref(cfg), int(S), int(L), C.byref(weights), C.byref(acts),
            C.byref(lora_q), C.byref(lora_v), C.byref(adam), _ptr(d_hidden, name="d_hidden"),
