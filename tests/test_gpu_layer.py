@@ -18,7 +18,17 @@ pytestmark = pytest.mark.gpu
 MINI_SEQ = SEQ512.with_(name="mini_seq", dim=256, ffn_dim=640, n_heads=8, n_kv_heads=2, head_dim=32,
                         rank=8, lora_alpha=16.0, seq_len=77, cache_len=77)
 TINY_WARM = TINY.with_(name="tiny_warm", adam_state="warm", step=7)
-CASES = {c.name: c for c in (TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512)}
+# single-token variants: ragged cache lengths, MHA and 8-head groups, every head size
+DEC_F32 = DECODE.with_(name="dec_f32_hd64", dim=256, ffn_dim=512, n_heads=8, n_kv_heads=2, head_dim=64,
+                       rank=4, lora_alpha=8.0, cache_len=100, wtype="f32", weight_std=0.05)
+DEC_BF16 = DECODE.with_(name="dec_bf16_mha_silu", dim=512, ffn_dim=768, n_heads=4, n_kv_heads=4,
+                        head_dim=128, cache_len=77, wtype="bf16", act="silu_mul", sub_norm=False,
+                        pre_norm=False, kv_layout="shd", adam_state="warm", step=5)
+DEC_G8 = DECODE.with_(name="dec_g8_hd32", dim=256, ffn_dim=256, n_heads=16, n_kv_heads=2, head_dim=32,
+                      rank=8, lora_alpha=16.0, cache_len=40, pre_norm=False)
+DEC_HD256 = DECODE.with_(name="dec_hd256", dim=512, ffn_dim=1024, n_heads=4, n_kv_heads=1, head_dim=256,
+                         cache_len=65, sub_norm=False, rope=True)
+CASES = {c.name: c for c in (TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512, DEC_F32, DEC_BF16, DEC_G8, DEC_HD256)}
 
 
 def tol(cfg):

@@ -129,6 +129,17 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void *p) {
     return r;
 }
 
+// Programmatic dependent launch: let the next kernel of the stream be scheduled
+// (trigger), and wait until the previous kernel has finished and its writes are
+// visible (wait; a no-op when the kernel was launched without the attribute).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Fire-and-forget prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
+__device__ __forceinline__ void l2_prefetch(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
     return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
 }

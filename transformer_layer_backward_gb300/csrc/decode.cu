@@ -9,13 +9,17 @@
 //       dN2  = s_g W_gate dG + s_u W_up dU                        GEMV over H rows
 //   k3  dR1  = dOut + RMSNorm_bwd(r1, g_ffn, dN2) (per block, shared memory), then
 //       dSub = s_o W_O dR1                                        GEMV over q_dim rows
-//   k4  per (KV head, key chunk): dCtx of the group's heads (sub-norm backward),
-//       dAttn[h, j] = dCtx_h . V[j], partial sums of attn * dAttn
-//   k5  per (KV head, key chunk): D_h, dS = scale attn (dAttn - D_h),
-//       partial dQ_h = sum_j dS[h, j] K[j]
-//   k6  per head: dQ = sum of partials, RoPE backward -> dQpre, gh_q += s dQpre_h B_q;
-//       per KV head: dV = sum_group attn[h, pos] dCtx_h, gh_v += s dV B_v
+//   k4  per (KV head, key chunk), one pass over K and V: dCtx of the group's heads
+//       (sub-norm backward), dA = dCtx_h . V[j] and the partial sums
+//       U_h = sum P dA K[j], W_h = sum P K[j], D_h = sum P dA; the chunk holding the
+//       current position also forms dV = sum_group attn[h, pos] dCtx_h and gh_v
+//   k6  per head: dQ = scale (U - D W) over all chunks ([ATT] softmax + score
+//       backward), RoPE backward -> dQpre, gh_q += s dQpre_h B_q
 //   k7  dB = s G h^T and dA = gh x^T for both adapters, AdamW (LoRA+ on B)
+//
+// k1 also issues L2 bulk prefetches of everything the later kernels read (weights of
+// k2/k3, K, V, attention rows, adapter state), so HBM streams the whole step while
+// the dependent chain runs; k2..k7 are launched as programmatic dependents.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "decode.cuh"
@@ -127,9 +131,29 @@ __device__ __forceinline__ float2 rms_sums(const float *x, const float *g, const
 
 // ------------------------------------------------------------------ k1: dF = s_d W_down dOut
 
+// This block's share of the L2 prefetch list (16-byte aligned pieces of <= 32 KiB).
+__device__ void prefetch_share(const DecodeArgs &a, int part, int nparts) {
+    const uint64_t b0 = a.pf_total * part / nparts, b1 = a.pf_total * (part + 1) / nparts;
+    uint64_t base = 0;
+    for (int r = 0; r < a.pf_count; ++r) {
+        const uint64_t n = a.pf_bytes[r];
+        const uint64_t s = b0 > base ? b0 : base, e = b1 < base + n ? b1 : base + n;
+        if (s < e) {
+            const uint64_t o0 = (s - base + 15) & ~uint64_t(15), o1 = (e - base) & ~uint64_t(15);
+            for (uint64_t o = o0; o < o1; o += 32768) {
+                const uint64_t len = o1 - o < 32768 ? o1 - o : 32768;
+                l2_prefetch(a.pf_ptr[r] + o, uint32_t(len));
+            }
+        }
+        base += n;
+    }
+}
+
 template <int WT>
 __global__ void __launch_bounds__(kThreads) dec_k1(DecodeArgs a) {
     extern __shared__ float4 sm4[];
+    pdl_trigger();
+    if (threadIdx.x == 0) prefetch_share(a, blockIdx.x, gridDim.x);
     float *sx = reinterpret_cast<float *>(sm4);
     for (int i = threadIdx.x; i < a.H; i += blockDim.x) sx[i] = a.d_hidden[i];
     if (blockIdx.x == 0 && threadIdx.x < 2 * a.rank) a.gh[threadIdx.x] = 0.f;
@@ -149,6 +173,8 @@ __global__ void __launch_bounds__(kThreads) dec_k2(DecodeArgs a) {
     __shared__ float2 red[32];
     float *sG = reinterpret_cast<float *>(sm4);
     float *sU = sG + a.I;
+    pdl_trigger();
+    pdl_wait();
     float rinv = 1.f, c = 0.f;
     const bool sub = a.flags & TLB_SUB_NORM;
     if (sub) {
@@ -188,6 +214,8 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
     extern __shared__ float4 sm4[];
     __shared__ float2 red[32];
     float *sR = reinterpret_cast<float *>(sm4);
+    pdl_trigger();
+    pdl_wait();
     float rinv = 1.f, c = 0.f;
     const bool pre = a.flags & TLB_PRE_NORM;
     if (pre) {
@@ -212,169 +240,197 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
     if (r0 < a.qd) warp_rows<WT, 1, kR, kU>(W, sc, xs, r0, a.qd, a.H, a.dSub);
 }
 
-// ------------------------------------------------------------------ k4: dCtx, dAttn, partial D
+// ------------------------------------------------------------------ k4: attention, one pass over K and V
 
+// Per (KV head, chunk of keys): dCtx of the group's heads (sub-norm backward), then for
+// every key j of the chunk and head h of the group
+//   dA = dCtx_h . V[j]      U_h += P dA K[j]      W_h += P K[j]      D_h += P dA
+// so that dQ_h = scale (U_h - D_h W_h) summed over chunks equals
+// scale sum_j P (dA - D_h) K[j] without a barrier on the row sum D_h.
+// The chunk holding the current position also forms dV and its LoRA gh_v share.
+template <int VPL, int GM>
 __global__ void __launch_bounds__(kThreads) dec_k4(DecodeArgs a) {
+    constexpr int KPW = kDecodeChunk / kWarps;        // keys per warp
     extern __shared__ float4 sm4[];
-    __shared__ float2 red[32];
-    __shared__ float sD[kWarps][16];
+    __shared__ float2 red2[32];
+    __shared__ float sDp[kWarps][16];
     const int kvh = blockIdx.x, chunk = blockIdx.y;
     const int G = a.nh / a.nkv;
-    float *sC = reinterpret_cast<float *>(sm4);          // [G * hd]
+    const int hd = VPL * 32;
+    float *sC = reinterpret_cast<float *>(sm4);        // [G][hd] dCtx
+    float *sR = sC + G * hd;                           // [kWarps][G][2][hd] reduction
+    pdl_trigger();
+    pdl_wait();
     float rinv = 1.f, c = 0.f;
     const bool sub = a.flags & TLB_SUB_NORM;
     if (sub) {
-        const float2 s = rms_sums(a.ctx, a.g_sub_attn, a.dSub, a.qd, red);
+        const float2 s = rms_sums(a.ctx, a.g_sub_attn, a.dSub, a.qd, red2);
         const float ms = s.x / float(a.qd) + a.eps;
         rinv = rsqrtf(ms);
         c = s.y / float(a.qd) / ms;
     }
-    const int off = kvh * G * a.hd;
-    for (int i = threadIdx.x; i < G * a.hd; i += blockDim.x) {
+    const int off = kvh * G * hd;
+    for (int i = threadIdx.x; i < G * hd; i += blockDim.x) {
         const int q = off + i;
         const float ds = a.dSub[q];
-        const float v = sub ? rinv * (ds * a.g_sub_attn[q] - a.ctx[q] * c) : ds;
-        sC[i] = v;
-        if (chunk == 0) a.dctx[q] = v;
+        sC[i] = sub ? rinv * (ds * a.g_sub_attn[q] - a.ctx[q] * c) : ds;
     }
     if (kvh == 0 && chunk == 0)
         for (int i = threadIdx.x; i < a.H; i += blockDim.x) a.d_hidden[i] = a.dR1[i];
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float dpart[16];
+    const int d0 = lane * VPL;
+    float U[GM][VPL], W[GM][VPL];                      // GM >= heads per KV group
 #pragma unroll
-    for (int g = 0; g < 16; ++g) dpart[g] = 0.f;
-    const int j0 = chunk * a.chunk;
-    const int j1 = min(a.L, j0 + a.chunk);
-    for (int j = j0 + warp; j < j1; j += kWarps) {
-        const float *vr = a.v + int64_t(kvh) * a.sh + int64_t(j) * a.sp;
-        float dots[16];
+    for (int g = 0; g < GM; ++g)
 #pragma unroll
-        for (int g = 0; g < 16; ++g) dots[g] = 0.f;
-        for (int d = lane; d < a.hd; d += 32) {
-            const float vv = vr[d];
+        for (int v = 0; v < VPL; ++v) U[g][v] = W[g][v] = 0.f;
+    float dsum[GM];
 #pragma unroll
-            for (int g = 0; g < 16; ++g)
-                if (g < G) dots[g] = fmaf(sC[g * a.hd + d], vv, dots[g]);
+    for (int g = 0; g < GM; ++g) dsum[g] = 0.f;
+    const int jw = chunk * kDecodeChunk + warp * KPW;
+#pragma unroll
+    for (int k = 0; k < KPW; ++k) {
+        const int j = jw + k;
+        if (j >= a.L) break;
+        float kv[VPL], vv[VPL];
+        const float *kr = a.k + int64_t(kvh) * a.sh + int64_t(j) * a.sp + d0;
+        const float *vr = a.v + int64_t(kvh) * a.sh + int64_t(j) * a.sp + d0;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            kv[v] = kr[v];
+            vv[v] = vr[v];
         }
+        // P of this key for each head of the group (lanes load in parallel)
+        const float pl = lane < G ? a.attn[int64_t(kvh * G + lane) * a.L + j] : 0.f;
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
-            if (g < G) {
-                const float t = warp_sum(dots[g]);
-                const int h = kvh * G + g;
-                if (lane == 0) {
-                    a.dattn[int64_t(h) * a.L + j] = t;
-                    dpart[g] += a.attn[int64_t(h) * a.L + j] * t;
-                }
+        for (int g = 0; g < GM; ++g) {
+            if (g >= G) break;
+            float t = 0.f;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) t = fmaf(sC[g * hd + d0 + v], vv[v], t);
+            const float dA = warp_sum(t);
+            const float P = __shfl_sync(0xffffffffu, pl, g);
+            const float pd = P * dA;
+            dsum[g] += pd;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                U[g][v] = fmaf(pd, kv[v], U[g][v]);
+                W[g][v] = fmaf(P, kv[v], W[g][v]);
             }
         }
     }
-    if (lane == 0)
 #pragma unroll
-        for (int g = 0; g < 16; ++g) sD[warp][g] = dpart[g];
+    for (int g = 0; g < GM; ++g) {
+        if (g >= G) break;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            sR[((warp * G + g) * 2 + 0) * hd + d0 + v] = U[g][v];
+            sR[((warp * G + g) * 2 + 1) * hd + d0 + v] = W[g][v];
+        }
+        if (lane == 0) sDp[warp][g] = dsum[g];
+    }
     __syncthreads();
+    for (int i = threadIdx.x; i < G * 2 * hd; i += blockDim.x) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) t += sR[w * G * 2 * hd + i];
+        const int g = i / (2 * hd), which = (i / hd) & 1, d = i % hd;
+        float *dst = which ? a.Wpart : a.Upart;
+        dst[(int64_t(chunk) * a.nh + kvh * G + g) * hd + d] = t;
+    }
     if (threadIdx.x < G) {
-        float s = 0.f;
-        for (int w = 0; w < kWarps; ++w) s += sD[w][threadIdx.x];
-        a.Dpart[int64_t(chunk) * a.nh + kvh * G + threadIdx.x] = s;
+        float t = 0.f;
+        for (int w = 0; w < kWarps; ++w) t += sDp[w][threadIdx.x];
+        a.Dpart[int64_t(chunk) * a.nh + kvh * G + threadIdx.x] = t;
+    }
+    // dV of the current token: dV[kvh, d] = sum_g attn[h_g, pos] dCtx_h_g[d]; gh_v share
+    if (a.pos / kDecodeChunk == chunk) {
+        __shared__ float sv[256];
+        __shared__ float rr[16][kWarps];
+        for (int d = threadIdx.x; d < hd; d += blockDim.x) {
+            float t = 0.f;
+            for (int g = 0; g < G; ++g) t = fmaf(a.attn[int64_t(kvh * G + g) * a.L + a.pos], sC[g * hd + d], t);
+            sv[d] = t;
+            a.dv[kvh * hd + d] = t;
+        }
+        __syncthreads();
+        float acc[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+        for (int d = threadIdx.x; d < hd; d += blockDim.x) {
+            const float *br = a.lv.b + int64_t(kvh * hd + d) * a.rank;
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                if (r < a.rank) acc[r] = fmaf(sv[d], br[r], acc[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const float t = warp_sum(acc[r]);
+            if (lane == 0) rr[r][warp] = t;
+        }
+        __syncthreads();
+        if (threadIdx.x < a.rank) {
+            float t = 0.f;
+            for (int w = 0; w < kWarps; ++w) t += rr[threadIdx.x][w];
+            atomicAdd(a.gh + a.rank + threadIdx.x, a.lora_scaling * t);
+        }
     }
 }
 
-// ------------------------------------------------------------------ k5: dS, partial dQ
-
-__global__ void __launch_bounds__(kThreads) dec_k5(DecodeArgs a) {
-    extern __shared__ float4 sm4[];
-    const int kvh = blockIdx.x, chunk = blockIdx.y;
-    const int G = a.nh / a.nkv;
-    const int j0 = chunk * a.chunk;
-    const int n = min(a.L, j0 + a.chunk) - j0;
-    float *sS = reinterpret_cast<float *>(sm4);         // [G][chunk]
-    __shared__ float sDh[16];
-    if (threadIdx.x < G) {
-        float s = 0.f;
-        for (int c = 0; c < a.nchunks; ++c) s += a.Dpart[int64_t(c) * a.nh + kvh * G + threadIdx.x];
-        sDh[threadIdx.x] = s;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < G * n; i += blockDim.x) {
-        const int g = i / n, jj = i % n;
-        const int64_t idx = int64_t(kvh * G + g) * a.L + j0 + jj;
-        sS[g * a.chunk + jj] = a.scale * a.attn[idx] * (a.dattn[idx] - sDh[g]);
-    }
-    __syncthreads();
-    for (int o = threadIdx.x; o < G * a.hd; o += blockDim.x) {
-        const int g = o / a.hd, d = o % a.hd;
-        const float *kc = a.k + int64_t(kvh) * a.sh + int64_t(j0) * a.sp + d;
-        float acc = 0.f;
-        for (int jj = 0; jj < n; ++jj) acc = fmaf(sS[g * a.chunk + jj], kc[int64_t(jj) * a.sp], acc);
-        a.dqpart[(int64_t(chunk) * a.nh + kvh * G + g) * a.hd + d] = acc;
-    }
-}
-
-// ------------------------------------------------------------------ k6: dQpre, dV, LoRA gh
+// ------------------------------------------------------------------ k6: dQpre and gh_q per head
 
 __global__ void __launch_bounds__(kThreads) dec_k6(DecodeArgs a, RopeFreqs fr) {
-    __shared__ float sv[256];
+    __shared__ float sq[256];
+    __shared__ float sD;
     __shared__ float red[16][kWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int b = blockIdx.x;
-    float *G;          // gradient row slice this block produces
-    const float *B;    // adapter B rows matching the slice
-    float *gh;
-    int o0;
-    if (b < a.nh) {                      // head b: dQ, RoPE backward
-        const int h = b;
-        for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
-            float s = 0.f;
-            for (int c = 0; c < a.nchunks; ++c) s += a.dqpart[(int64_t(c) * a.nh + h) * a.hd + d];
-            sv[d] = s;
-        }
-        __syncthreads();
-        const int half = a.hd >> 1;
-        for (int d = threadIdx.x; d < half; d += blockDim.x) {
-            float y1 = sv[d], y2 = sv[d + half];
-            if (a.flags & TLB_ROPE) {
-                float cs, sn;
-                rope_cos_sin(float(a.pos), fr.hi[d], fr.lo[d], cs, sn);
-                const float t1 = y1 * cs + y2 * sn, t2 = -y1 * sn + y2 * cs;
-                y1 = t1;
-                y2 = t2;
-            }
-            a.dqpre[h * a.hd + d] = y1;
-            a.dqpre[h * a.hd + d + half] = y2;
-        }
-        __syncthreads();
-        G = a.dqpre;
-        B = a.lq.b;
-        gh = a.gh;
-        o0 = h * a.hd;
-    } else {                             // KV head: dV of the current token
-        const int kvh = b - a.nh;
-        const int grp = a.nh / a.nkv;
-        for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
-            float s = 0.f;
-            for (int g = 0; g < grp; ++g) {
-                const int h = kvh * grp + g;
-                s = fmaf(a.attn[int64_t(h) * a.L + a.pos], a.dctx[h * a.hd + d], s);
-            }
-            a.dv[kvh * a.hd + d] = s;
-        }
-        __syncthreads();
-        G = a.dv;
-        B = a.lv.b;
-        gh = a.gh + a.rank;
-        o0 = kvh * a.hd;
+    const int h = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();
+    if (threadIdx.x < 32) {
+        float t = 0.f;
+        for (int c = lane; c < a.nchunks; c += 32) t += a.Dpart[int64_t(c) * a.nh + h];
+        t = warp_sum(t);
+        if (lane == 0) sD = t;
     }
-    // gh[r] += s * sum_{o in slice} G[o] B[o, r]  (B before its update)
+    __syncthreads();
+    const float D = sD;
+    for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
+        float u = 0.f, w = 0.f;
+        for (int c = 0; c < a.nchunks; ++c) {
+            const int64_t idx = (int64_t(c) * a.nh + h) * a.hd + d;
+            u += a.Upart[idx];
+            w += a.Wpart[idx];
+        }
+        sq[d] = a.scale * (u - D * w);
+    }
+    __syncthreads();
+    const int half = a.hd >> 1;
+    for (int d = threadIdx.x; d < half; d += blockDim.x) {
+        float y1 = sq[d], y2 = sq[d + half];
+        if (a.flags & TLB_ROPE) {
+            float cs, sn;
+            rope_cos_sin(float(a.pos), fr.hi[d], fr.lo[d], cs, sn);
+            const float t1 = y1 * cs + y2 * sn, t2 = -y1 * sn + y2 * cs;
+            y1 = t1;
+            y2 = t2;
+        }
+        a.dqpre[h * a.hd + d] = y1;
+        a.dqpre[h * a.hd + d + half] = y2;
+        sq[d] = y1;
+        sq[d + half] = y2;   // each pair is owned by one thread
+    }
+    __syncthreads();
+    // gh_q[r] += s * sum_{d} dQpre[h, d] B_q[h*hd + d, r]   (B before its update)
     float acc[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) acc[r] = 0.f;
-    for (int o = threadIdx.x; o < a.hd; o += blockDim.x) {
-        const float gv = G[o0 + o];
-        const float *br = B + int64_t(o0 + o) * a.rank;
+    for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
+        const float *br = a.lq.b + int64_t(h * a.hd + d) * a.rank;
 #pragma unroll
         for (int r = 0; r < 16; ++r)
-            if (r < a.rank) acc[r] = fmaf(gv, br[r], acc[r]);
+            if (r < a.rank) acc[r] = fmaf(sq[d], br[r], acc[r]);
     }
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
@@ -383,9 +439,9 @@ __global__ void __launch_bounds__(kThreads) dec_k6(DecodeArgs a, RopeFreqs fr) {
     }
     __syncthreads();
     if (threadIdx.x < a.rank) {
-        float s = 0.f;
-        for (int w = 0; w < kWarps; ++w) s += red[threadIdx.x][w];
-        atomicAdd(gh + threadIdx.x, a.lora_scaling * s);
+        float t = 0.f;
+        for (int w = 0; w < kWarps; ++w) t += red[threadIdx.x][w];
+        atomicAdd(a.gh + threadIdx.x, a.lora_scaling * t);
     }
 }
 
@@ -395,6 +451,8 @@ __global__ void __launch_bounds__(kThreads) dec_k7(DecodeArgs a) {
     __shared__ float red[32];
     const int64_t nbq = int64_t(a.qd) * a.rank, nbv = int64_t(a.kvd) * a.rank, na = int64_t(a.rank) * a.H;
     const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
     float g = 0.f;
     int which = -1;   // 0: sumsq of dA, 1: of dB
     if (e < nbq) {
@@ -442,39 +500,67 @@ __global__ void __launch_bounds__(kThreads) dec_k7(DecodeArgs a) {
     }
 }
 
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, size_t smem, cudaStream_t st, bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <int VPL>
+cudaError_t launch_k4_g(int G, dim3 g4, size_t sm4, cudaStream_t st, const DecodeArgs &a) {
+    if (G <= 1) return launch(dec_k4<VPL, 1>, g4, sm4, st, true, a);
+    if (G <= 2) return launch(dec_k4<VPL, 2>, g4, sm4, st, true, a);
+    if (G <= 4) return launch(dec_k4<VPL, 4>, g4, sm4, st, true, a);
+    if (G <= 8) return launch(dec_k4<VPL, 8>, g4, sm4, st, true, a);
+    if constexpr (VPL <= 4) return launch(dec_k4<VPL, 16>, g4, sm4, st, true, a);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_k4(int G, int hd, dim3 g4, size_t sm4, cudaStream_t st, const DecodeArgs &a) {
+    switch (hd) {
+        case 32: return launch_k4_g<1>(G, g4, sm4, st, a);
+        case 64: return launch_k4_g<2>(G, g4, sm4, st, a);
+        case 128: return launch_k4_g<4>(G, g4, sm4, st, a);
+        default: return launch_k4_g<8>(G, g4, sm4, st, a);
+    }
+}
+
 template <int WT>
 int launch_all(const DecodeArgs &a, cudaStream_t st) {
-    const size_t sm1 = size_t(a.H) * 4, sm2 = size_t(2) * a.I * 4, sm3 = size_t(a.H) * 4;
     const int rows_per_block = kWarps * kR;
-    auto big = [](const void *f, size_t s) -> cudaError_t {
-        return s > 48 * 1024 ? cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, int(s))
-                             : cudaSuccess;
-    };
-    TLB_CUDA(big((const void *)dec_k1<WT>, sm1));
-    dec_k1<WT><<<unsigned(ceil_div(a.I, rows_per_block)), kThreads, sm1, st>>>(a);
+    TLB_CUDA(launch(dec_k1<WT>, dim3(unsigned(ceil_div(a.I, rows_per_block))), size_t(a.H) * 4, st, false, a));
     TLB_TRY(check_launch("decode k1"));
-    if (a.act == TLB_ACT_RELU2_MUL) {
-        TLB_CUDA(big((const void *)dec_k2<WT, TLB_ACT_RELU2_MUL>, sm2));
-        dec_k2<WT, TLB_ACT_RELU2_MUL><<<unsigned(ceil_div(a.H, rows_per_block)), kThreads, sm2, st>>>(a);
-    } else {
-        TLB_CUDA(big((const void *)dec_k2<WT, TLB_ACT_SILU_MUL>, sm2));
-        dec_k2<WT, TLB_ACT_SILU_MUL><<<unsigned(ceil_div(a.H, rows_per_block)), kThreads, sm2, st>>>(a);
-    }
+    const size_t sm2 = size_t(2) * a.I * 4;
+    const dim3 g2(unsigned(ceil_div(a.H, rows_per_block)));
+    if (a.act == TLB_ACT_RELU2_MUL) TLB_CUDA(launch(dec_k2<WT, TLB_ACT_RELU2_MUL>, g2, sm2, st, true, a));
+    else TLB_CUDA(launch(dec_k2<WT, TLB_ACT_SILU_MUL>, g2, sm2, st, true, a));
     TLB_TRY(check_launch("decode k2"));
-    TLB_CUDA(big((const void *)dec_k3<WT>, sm3));
-    dec_k3<WT><<<unsigned(ceil_div(a.qd, rows_per_block)), kThreads, sm3, st>>>(a);
+    TLB_CUDA(launch(dec_k3<WT>, dim3(unsigned(ceil_div(a.qd, rows_per_block))), size_t(a.H) * 4, st, true, a));
     TLB_TRY(check_launch("decode k3"));
     const int G = a.nh / a.nkv;
-    dec_k4<<<dim3(a.nkv, a.nchunks), kThreads, size_t(G) * a.hd * 4, st>>>(a);
+    const dim3 g4(a.nkv, a.nchunks);
+    const size_t sm4 = (size_t(G) * a.hd + size_t(kWarps) * G * 2 * a.hd) * 4;
+    TLB_CUDA(launch_k4(G, a.hd, g4, sm4, st, a));
     TLB_TRY(check_launch("decode k4"));
-    dec_k5<<<dim3(a.nkv, a.nchunks), kThreads, size_t(G) * a.chunk * 4, st>>>(a);
-    TLB_TRY(check_launch("decode k5"));
     RopeFreqs fr;
     rope_freqs(fr, a.hd, a.rope_base);
-    dec_k6<<<a.nh + a.nkv, kThreads, 0, st>>>(a, fr);
+    TLB_CUDA(launch(dec_k6, dim3(a.nh), 0, st, true, a, fr));
     TLB_TRY(check_launch("decode k6"));
     const int64_t n7 = int64_t(a.qd + a.kvd) * a.rank + 2 * int64_t(a.rank) * a.H;
-    dec_k7<<<unsigned(ceil_div(n7, kThreads)), kThreads, 0, st>>>(a);
+    TLB_CUDA(launch(dec_k7, dim3(unsigned(ceil_div(n7, kThreads))), 0, st, true, a));
     return check_launch("decode k7");
 }
 
@@ -483,8 +569,12 @@ int launch_all(const DecodeArgs &a, cudaStream_t st) {
 bool decode_supported(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     const int G = c.n_heads / c.n_kv_heads;
     const int E = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 8 : 16);
-    return S == 1 && G <= 16 && c.rank <= 16 && c.head_dim <= 256 && c.dim % E == 0 && c.ffn_dim % E == 0 &&
-           size_t(2) * c.ffn_dim * 4 <= 200 * 1024 && L >= 1;
+    const int hd = c.head_dim;
+    const int gmax = hd > 128 ? 8 : 16;   // heads per KV group held in registers by k4
+    const size_t sm4 = (size_t(G) * hd + size_t(kWarps) * G * 2 * hd) * 4;
+    return S == 1 && G <= gmax && c.rank <= 16 && (hd == 32 || hd == 64 || hd == 128 || hd == 256) &&
+           c.dim % E == 0 && c.ffn_dim % E == 0 && size_t(2) * c.ffn_dim * 4 <= 200 * 1024 &&
+           sm4 <= 200 * 1024 && L >= 1;
 }
 
 int decode_layer_launch(const DecodeArgs &a, int wtype, cudaStream_t st) {

@@ -15,10 +15,15 @@ struct DecodeArgs {
     int64_t sh, sp;
     float *d_hidden;                                   // [H] in: dOut, out: dR1
     float *dF, *dN2, *dR1, *dSub, *dctx;               // workspace vectors
-    float *dattn, *Dpart, *dqpart, *dqpre, *dv, *gh;   // workspace attention / LoRA
+    float *Upart, *Wpart, *Dpart, *dqpre, *dv, *gh;    // workspace attention / LoRA
     tlb_lora lq, lv;
     AdamCoef ka, kb;
     double *sumsq;
+    // regions read after the first kernel, prefetched into L2 while it runs
+    const char *pf_ptr[24];
+    uint64_t pf_bytes[24];
+    int pf_count;
+    uint64_t pf_total;
 };
 
 constexpr int kDecodeChunk = 32;   // keys per block in the attention passes

@@ -12,7 +12,7 @@ namespace {
 
 struct LayerWs {
     size_t dF, dG, dU, dN2, dSub, dqpre, dv, gh_q, gh_v;
-    size_t dR1, dctx, dattn, Dpart, dqpart, gh2;   // single-token path
+    size_t dR1, Upart, Wpart, Dpart, gh2;   // single-token path
     size_t total;
 };
 
@@ -33,13 +33,12 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     if (S == 1) {
         const int64_t nchunks = ceil_div(L, kDecodeChunk);
         w.dR1 = p.take(H * 4);
-        w.dctx = p.take(qd * 4);
-        w.dattn = p.take(int64_t(c.n_heads) * L * 4);
+        w.Upart = p.take(nchunks * qd * 4);
+        w.Wpart = p.take(nchunks * qd * 4);
         w.Dpart = p.take(nchunks * c.n_heads * 4);
-        w.dqpart = p.take(nchunks * qd * 4);
         w.gh2 = p.take(2 * int64_t(c.rank) * 4);
     } else {
-        w.dR1 = w.dctx = w.dattn = w.Dpart = w.dqpart = w.gh2 = 0;
+        w.dR1 = w.Upart = w.Wpart = w.Dpart = w.gh2 = 0;
     }
     w.total = p.off;
     return w;
@@ -292,10 +291,9 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
         d.dN2 = ws_at<float>(ws, p.dN2);
         d.dR1 = ws_at<float>(ws, p.dR1);
         d.dSub = ws_at<float>(ws, p.dSub);
-        d.dctx = ws_at<float>(ws, p.dctx);
-        d.dattn = ws_at<float>(ws, p.dattn);
+        d.Upart = ws_at<float>(ws, p.Upart);
+        d.Wpart = ws_at<float>(ws, p.Wpart);
         d.Dpart = ws_at<float>(ws, p.Dpart);
-        d.dqpart = ws_at<float>(ws, p.dqpart);
         d.dqpre = dqpre;
         d.dv = dv;
         d.gh = ws_at<float>(ws, p.gh2);    // [gh_q | gh_v], 2 * rank floats
@@ -304,6 +302,35 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
         d.ka = adam_coef(*adam, 1.0f);
         d.kb = adam_coef(*adam, float(adam->lr_b_mult));
         d.sumsq = sumsq;
+        // L2 prefetch list: what k2..k7 read, in the order they read it
+        const size_t es = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 2 : 1);
+        d.pf_count = 0;
+        d.pf_total = 0;
+        auto add = [&](const void *ptr, uint64_t bytes) {
+            if (ptr == nullptr || !aligned16(ptr) || d.pf_count >= 24) return;
+            bytes &= ~uint64_t(15);
+            if (bytes == 0) return;
+            d.pf_ptr[d.pf_count] = static_cast<const char *>(ptr);
+            d.pf_bytes[d.pf_count++] = bytes;
+            d.pf_total += bytes;
+        };
+        const uint64_t kv_span = (uint64_t(c.n_kv_heads - 1) * acts->kv_stride_head +
+                                  uint64_t(L - 1) * acts->kv_stride_pos + c.head_dim) * 4;
+        add(w->w_gate.w, uint64_t(c.dim) * c.ffn_dim * es);
+        add(w->w_up.w, uint64_t(c.dim) * c.ffn_dim * es);
+        add(w->w_o.w, uint64_t(qd) * c.dim * es);
+        add(acts->k, kv_span);
+        add(acts->v, kv_span);
+        add(acts->attn, uint64_t(c.n_heads) * L * 4);
+        for (const tlb_lora *l : {lora_q, lora_v}) {
+            const uint64_t nb = uint64_t(l == lora_q ? qd : kvd) * c.rank * 4, na = uint64_t(c.rank) * c.dim * 4;
+            add(l->b, nb);
+            add(l->m_b, nb);
+            add(l->v_b, nb);
+            add(l->a, na);
+            add(l->m_a, na);
+            add(l->v_a, na);
+        }
         return decode_layer_launch(d, c.wtype, st);
     }
     TLB_TRY(ffn_impl(c, S, d_hidden, *w, *acts, d_hidden, ws, st));
