@@ -17,9 +17,10 @@
 //       backward), RoPE backward -> dQpre, gh_q += s dQpre_h B_q
 //   k7  dB = s G h^T and dA = gh x^T for both adapters, AdamW (LoRA+ on B)
 //
-// k1 also issues L2 bulk prefetches of everything the later kernels read (weights of
-// k2/k3, K, V, attention rows, adapter state), so HBM streams the whole step while
-// the dependent chain runs; k2..k7 are launched as programmatic dependents.
+// The vector a GEMV multiplies sits in shared memory in a swizzled order, so the
+// 16-byte reads of the 32 lanes (each lane owning one 16-byte chunk of a weight row)
+// fall in distinct banks.  The two sums an RMSNorm backward needs over a vector a
+// GEMV produces are accumulated per block by that GEMV and summed by the consumer.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "decode.cuh"
@@ -28,8 +29,10 @@ namespace tlb {
 
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 8;                // GEMV / LoRA kernels
 constexpr int kThreads = kWarps * 32;
+constexpr int kAWarps = 8;               // attention kernel (holds per-head accumulators)
+constexpr int kAThreads = kAWarps * 32;
 
 template <int WT>
 struct EPC {
@@ -63,13 +66,31 @@ __device__ __forceinline__ float chunk_dot(uint4 w, const float *x) {
     }
 }
 
+// Shared-memory position of float4 unit u of a GEMV vector: lane l reads chunk
+// ch = base + l, i.e. units ch*P .. ch*P + P - 1 (P = float4 units per 16-byte weight
+// chunk); XOR-ing the unit index within its chunk with bits of ch puts the 8 lanes of
+// each 128-byte shared-memory phase on 8 different 16-byte bank groups.
+template <int WT>
+__device__ __forceinline__ int xunit(int u) {
+    constexpr int P = EPC<WT>::v / 4;
+    if constexpr (P == 1) {
+        return u;
+    } else {
+        const int ch = u / P, k = u % P;
+        return ch * P + (k ^ ((ch / (8 / P)) % P));
+    }
+}
+
 // Rows [r0, r0 + R) of NM matrices (same shape [rows, cols]), each dotted with its own
-// shared-memory vector, scaled and summed: y[r] = sum_m scale_m W_m[r, :] . x_m.
-// One warp; U chunks of 16 bytes per row and matrix in flight per lane.
+// shared-memory vector (swizzled by xunit), scaled and summed:
+//   y[r] = sum_m scale_m W_m[r, :] . x_m.
+// One warp; U chunks of 16 bytes per row and matrix in flight per lane.  Returns the
+// row values to every lane in out[R] (0 for rows past the end).
 template <int WT, int NM, int R, int U>
 __device__ __forceinline__ void warp_rows(const char *const *W, const float *scale, const float *const *xs,
-                                          int r0, int rows, int cols, float *y) {
+                                          int r0, int rows, int cols, float *y, float *out) {
     constexpr int E = EPC<WT>::v;
+    constexpr int P = E / 4;
     const int lane = threadIdx.x & 31;
     const int nch = cols / E;
     const size_t row_bytes = size_t(cols) * (16 / E);
@@ -97,12 +118,12 @@ __device__ __forceinline__ void warp_rows(const char *const *W, const float *sca
             for (int m = 0; m < NM; ++m) {
                 float xv[E];
 #pragma unroll
-                for (int e = 0; e < E; e += 4) {
-                    const float4 t = *reinterpret_cast<const float4 *>(xs[m] + ch * E + e);
-                    xv[e] = t.x;
-                    xv[e + 1] = t.y;
-                    xv[e + 2] = t.z;
-                    xv[e + 3] = t.w;
+                for (int k = 0; k < P; ++k) {
+                    const float4 t = reinterpret_cast<const float4 *>(xs[m])[xunit<WT>(ch * P + k)];
+                    xv[4 * k] = t.x;
+                    xv[4 * k + 1] = t.y;
+                    xv[4 * k + 2] = t.z;
+                    xv[4 * k + 3] = t.w;
                 }
 #pragma unroll
                 for (int r = 0; r < R; ++r) acc[r] = fmaf(scale[m], chunk_dot<WT>(w[m][r][u], xv), acc[r]);
@@ -112,57 +133,76 @@ __device__ __forceinline__ void warp_rows(const char *const *W, const float *sca
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const float s = warp_sum(acc[r]);
+        out[r] = (r0 + r < rows) ? s : 0.f;
         if (lane == 0 && r0 + r < rows) y[r0 + r] = s;
     }
 }
 
-constexpr int kR = 2, kU = 2;   // rows per warp, chunks in flight per row
+// Copy n floats (n % 4 == 0) from global into shared memory in the GEMV order.
+template <int WT>
+__device__ __forceinline__ void stage_vector(float *sx, const float *x, int n) {
+    const float4 *x4 = reinterpret_cast<const float4 *>(x);
+    float4 *s4 = reinterpret_cast<float4 *>(sx);
+    for (int u = threadIdx.x; u < (n >> 2); u += blockDim.x) s4[xunit<WT>(u)] = x4[u];
+}
 
-// Sum of x^2 and of x * g * dy over n elements (block-wide).
-__device__ __forceinline__ float2 rms_sums(const float *x, const float *g, const float *dy, int n, float2 *red) {
+// Per-block partial sums (sum y g z, sum z^2) over this block's GEMV rows, written to
+// part[blockIdx.x]; the consumer of y adds them up (RMSNorm backward of y with input z).
+template <int R>
+__device__ __forceinline__ void block_partials(const float *vals, int r0, int rows, const float *g,
+                                               const float *z, float2 *part, float2 *red) {
+    float2 acc = make_float2(0.f, 0.f);
+    if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (r0 + r < rows) {
+                const float zz = z[r0 + r];
+                acc.x += vals[r] * g[r0 + r] * zz;
+                acc.y += zz * zz;
+            }
+        }
+    }
+    acc = block_sum2(acc, red);
+    if (threadIdx.x == 0) part[blockIdx.x] = acc;
+}
+
+// Sum of the first n partials (every thread gets the result).
+__device__ __forceinline__ float2 sum_partials(const float2 *part, int n, float2 *red) {
     float2 acc = make_float2(0.f, 0.f);
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const float xv = x[i];
-        acc.x += xv * xv;
-        acc.y += xv * g[i] * dy[i];
+        const float2 p = part[i];
+        acc.x += p.x;
+        acc.y += p.y;
     }
     return block_sum2(acc, red);
 }
 
-// ------------------------------------------------------------------ k1: dF = s_d W_down dOut
-
-// This block's share of the L2 prefetch list (16-byte aligned pieces of <= 32 KiB).
-__device__ void prefetch_share(const DecodeArgs &a, int part, int nparts) {
-    const uint64_t b0 = a.pf_total * part / nparts, b1 = a.pf_total * (part + 1) / nparts;
-    uint64_t base = 0;
-    for (int r = 0; r < a.pf_count; ++r) {
-        const uint64_t n = a.pf_bytes[r];
-        const uint64_t s = b0 > base ? b0 : base, e = b1 < base + n ? b1 : base + n;
-        if (s < e) {
-            const uint64_t o0 = (s - base + 15) & ~uint64_t(15), o1 = (e - base) & ~uint64_t(15);
-            for (uint64_t o = o0; o < o1; o += 32768) {
-                const uint64_t len = o1 - o < 32768 ? o1 - o : 32768;
-                l2_prefetch(a.pf_ptr[r] + o, uint32_t(len));
-            }
-        }
-        base += n;
-    }
+// rinv and c of RMSNorm backward from (sum dy g x, sum x^2): dx = rinv (dy g - x c).
+__device__ __forceinline__ void rms_coef2(float2 s, int n, float eps, float &rinv, float &c) {
+    const float ms = s.y / float(n) + eps;
+    rinv = rsqrtf(ms);
+    c = s.x / float(n) / ms;
 }
+
+constexpr int kR = 2, kU = 2;   // rows per warp, chunks in flight per row and matrix
+
+// ------------------------------------------------------------------ k1: dF = s_d W_down dOut
 
 template <int WT>
 __global__ void __launch_bounds__(kThreads) dec_k1(DecodeArgs a) {
     extern __shared__ float4 sm4[];
-    pdl_trigger();
-    if (threadIdx.x == 0) prefetch_share(a, blockIdx.x, gridDim.x);
+    __shared__ float2 red[32];
     float *sx = reinterpret_cast<float *>(sm4);
-    for (int i = threadIdx.x; i < a.H; i += blockDim.x) sx[i] = a.d_hidden[i];
+    stage_vector<WT>(sx, a.d_hidden, a.H);
     if (blockIdx.x == 0 && threadIdx.x < 2 * a.rank) a.gh[threadIdx.x] = 0.f;
     __syncthreads();
     const char *W[1] = {reinterpret_cast<const char *>(a.w_down)};
     const float sc[1] = {a.s_down};
     const float *xs[1] = {sx};
     const int r0 = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR;
-    if (r0 < a.I) warp_rows<WT, 1, kR, kU>(W, sc, xs, r0, a.I, a.H, a.dF);
+    float vals[kR] = {};
+    if (r0 < a.I) warp_rows<WT, 1, kR, kU>(W, sc, xs, r0, a.I, a.H, a.dF, vals);
+    if (a.flags & TLB_SUB_NORM) block_partials<kR>(vals, r0, a.I, a.g_sub_ffn, a.hidden, a.part1, red);
 }
 
 // ------------------------------------------------------------------ k2: dN2 = W_g dG + W_u dU
@@ -173,30 +213,64 @@ __global__ void __launch_bounds__(kThreads) dec_k2(DecodeArgs a) {
     __shared__ float2 red[32];
     float *sG = reinterpret_cast<float *>(sm4);
     float *sU = sG + a.I;
-    pdl_trigger();
-    pdl_wait();
     float rinv = 1.f, c = 0.f;
     const bool sub = a.flags & TLB_SUB_NORM;
-    if (sub) {
-        const float2 s = rms_sums(a.hidden, a.g_sub_ffn, a.dF, a.I, red);
-        const float ms = s.x / float(a.I) + a.eps;
-        rinv = rsqrtf(ms);
-        c = s.y / float(a.I) / ms;
-    }
+    if (sub) rms_coef2(sum_partials(a.part1, a.n1, red), a.I, a.eps, rinv, c);
     const bool cache = (ACT == TLB_ACT_SILU_MUL) && (a.flags & TLB_USE_SILU_CACHE);
-    for (int i = threadIdx.x; i < a.I; i += blockDim.x) {
-        const float df = a.dF[i];
-        const float dh = sub ? rinv * (df * a.g_sub_ffn[i] - a.hidden[i] * c) : df;
-        const float g = a.gate[i], u = a.up[i];
-        if constexpr (ACT == TLB_ACT_RELU2_MUL) {
-            const float r = fmaxf(g, 0.f);
-            sG[i] = dh * u * 2.f * r;
-            sU[i] = dh * r * r;
-        } else {
-            const float sig = 1.f / (1.f + expf(-g));
-            const float y = g * sig;
-            sG[i] = dh * u * (sig * (1.f + g - y));
-            sU[i] = dh * (cache ? a.silu_gate[i] : y);
+    {
+        // dh (sub-norm backward) and the gated-activation backward, float4 at a time,
+        // two float4 of each of the six inputs in flight per thread
+        constexpr int B = 2;
+        const int n4 = a.I >> 2;
+        const float4 *dF4 = reinterpret_cast<const float4 *>(a.dF);
+        const float4 *hid4 = reinterpret_cast<const float4 *>(a.hidden);
+        const float4 *gam4 = reinterpret_cast<const float4 *>(a.g_sub_ffn);
+        const float4 *gat4 = reinterpret_cast<const float4 *>(a.gate);
+        const float4 *up4 = reinterpret_cast<const float4 *>(a.up);
+        const float4 *sg4 = reinterpret_cast<const float4 *>(a.silu_gate);
+        for (int base = threadIdx.x; base < n4; base += blockDim.x * B) {
+            float4 df[B], hd[B], gm[B], ga[B], uu[B], sl[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int i = base + b * blockDim.x;
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                const bool ok = i < n4;
+                df[b] = ok ? dF4[i] : z;
+                hd[b] = ok && sub ? hid4[i] : z;
+                gm[b] = ok && sub ? gam4[i] : z;
+                ga[b] = ok ? gat4[i] : z;
+                uu[b] = ok ? up4[i] : z;
+                sl[b] = ok && cache ? sg4[i] : z;
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int i = base + b * blockDim.x;
+                if (i >= n4) break;
+                const float dfv[4] = {df[b].x, df[b].y, df[b].z, df[b].w};
+                const float hdv[4] = {hd[b].x, hd[b].y, hd[b].z, hd[b].w};
+                const float gmv[4] = {gm[b].x, gm[b].y, gm[b].z, gm[b].w};
+                const float gav[4] = {ga[b].x, ga[b].y, ga[b].z, ga[b].w};
+                const float uuv[4] = {uu[b].x, uu[b].y, uu[b].z, uu[b].w};
+                const float slv[4] = {sl[b].x, sl[b].y, sl[b].z, sl[b].w};
+                float og[4], ou[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float dh = sub ? rinv * (dfv[e] * gmv[e] - hdv[e] * c) : dfv[e];
+                    const float g = gav[e], u = uuv[e];
+                    if constexpr (ACT == TLB_ACT_RELU2_MUL) {
+                        const float r = fmaxf(g, 0.f);
+                        og[e] = dh * u * 2.f * r;
+                        ou[e] = dh * r * r;
+                    } else {
+                        const float sig = 1.f / (1.f + expf(-g));
+                        const float y = g * sig;
+                        og[e] = dh * u * (sig * (1.f + g - y));
+                        ou[e] = dh * (cache ? slv[e] : y);
+                    }
+                }
+                reinterpret_cast<float4 *>(sG)[xunit<WT>(i)] = make_float4(og[0], og[1], og[2], og[3]);
+                reinterpret_cast<float4 *>(sU)[xunit<WT>(i)] = make_float4(ou[0], ou[1], ou[2], ou[3]);
+            }
         }
     }
     __syncthreads();
@@ -204,7 +278,9 @@ __global__ void __launch_bounds__(kThreads) dec_k2(DecodeArgs a) {
     const float sc[2] = {a.s_gate, a.s_up};
     const float *xs[2] = {sG, sU};
     const int r0 = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR;
-    if (r0 < a.H) warp_rows<WT, 2, kR, kU>(W, sc, xs, r0, a.H, a.I, a.dN2);
+    float vals[kR] = {};
+    if (r0 < a.H) warp_rows<WT, 2, kR, kU>(W, sc, xs, r0, a.H, a.I, a.dN2, vals);
+    if (a.flags & TLB_PRE_NORM) block_partials<kR>(vals, r0, a.H, a.g_ffn, a.r1, a.part2, red);
 }
 
 // ------------------------------------------------------------------ k3: dR1, dSub = s_o W_O dR1
@@ -214,30 +290,34 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
     extern __shared__ float4 sm4[];
     __shared__ float2 red[32];
     float *sR = reinterpret_cast<float *>(sm4);
-    pdl_trigger();
-    pdl_wait();
     float rinv = 1.f, c = 0.f;
     const bool pre = a.flags & TLB_PRE_NORM;
-    if (pre) {
-        const float2 s = rms_sums(a.r1, a.g_ffn, a.dN2, a.H, red);
-        const float ms = s.x / float(a.H) + a.eps;
-        rinv = rsqrtf(ms);
-        c = s.y / float(a.H) / ms;
-    }
+    if (pre) rms_coef2(sum_partials(a.part2, a.n2, red), a.H, a.eps, rinv, c);
     const bool resid = a.flags & TLB_RESIDUAL;
-    for (int i = threadIdx.x; i < a.H; i += blockDim.x) {
-        const float dn = a.dN2[i];
-        float v = pre ? rinv * (dn * a.g_ffn[i] - a.r1[i] * c) : dn;
-        if (resid) v += a.d_hidden[i];
-        sR[i] = v;
-        if (blockIdx.x == 0) a.dR1[i] = v;
+    {
+        const int n4 = a.H >> 2;
+        const float4 *dn4 = reinterpret_cast<const float4 *>(a.dN2), *r14 = reinterpret_cast<const float4 *>(a.r1);
+        const float4 *gf4 = reinterpret_cast<const float4 *>(a.g_ffn), *do4 = reinterpret_cast<const float4 *>(a.d_hidden);
+        for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 dn = dn4[i], r = pre ? r14[i] : z, gm = pre ? gf4[i] : z, dO = resid ? do4[i] : z;
+            float4 v;
+            v.x = (pre ? rinv * (dn.x * gm.x - r.x * c) : dn.x) + dO.x;
+            v.y = (pre ? rinv * (dn.y * gm.y - r.y * c) : dn.y) + dO.y;
+            v.z = (pre ? rinv * (dn.z * gm.z - r.z * c) : dn.z) + dO.z;
+            v.w = (pre ? rinv * (dn.w * gm.w - r.w * c) : dn.w) + dO.w;
+            reinterpret_cast<float4 *>(sR)[xunit<WT>(i)] = v;
+            if (blockIdx.x == 0) reinterpret_cast<float4 *>(a.dR1)[i] = v;
+        }
     }
     __syncthreads();
     const char *W[1] = {reinterpret_cast<const char *>(a.w_o)};
     const float sc[1] = {a.s_o};
     const float *xs[1] = {sR};
     const int r0 = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR;
-    if (r0 < a.qd) warp_rows<WT, 1, kR, kU>(W, sc, xs, r0, a.qd, a.H, a.dSub);
+    float vals[kR] = {};
+    if (r0 < a.qd) warp_rows<WT, 1, kR, kU>(W, sc, xs, r0, a.qd, a.H, a.dSub, vals);
+    if (a.flags & TLB_SUB_NORM) block_partials<kR>(vals, r0, a.qd, a.g_sub_attn, a.ctx, a.part3, red);
 }
 
 // ------------------------------------------------------------------ k4: attention, one pass over K and V
@@ -249,26 +329,19 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
 // scale sum_j P (dA - D_h) K[j] without a barrier on the row sum D_h.
 // The chunk holding the current position also forms dV and its LoRA gh_v share.
 template <int VPL, int GM>
-__global__ void __launch_bounds__(kThreads) dec_k4(DecodeArgs a) {
-    constexpr int KPW = kDecodeChunk / kWarps;        // keys per warp
+__global__ void __launch_bounds__(kAThreads) dec_k4(DecodeArgs a) {
+    constexpr int KPW = kDecodeChunk / kAWarps;        // keys per warp
     extern __shared__ float4 sm4[];
     __shared__ float2 red2[32];
-    __shared__ float sDp[kWarps][16];
+    __shared__ float sDp[kAWarps][16];
     const int kvh = blockIdx.x, chunk = blockIdx.y;
     const int G = a.nh / a.nkv;
     const int hd = VPL * 32;
     float *sC = reinterpret_cast<float *>(sm4);        // [G][hd] dCtx
-    float *sR = sC + G * hd;                           // [kWarps][G][2][hd] reduction
-    pdl_trigger();
-    pdl_wait();
+    float *sR = sC + G * hd;                           // [kAWarps][G][2][hd] reduction
     float rinv = 1.f, c = 0.f;
     const bool sub = a.flags & TLB_SUB_NORM;
-    if (sub) {
-        const float2 s = rms_sums(a.ctx, a.g_sub_attn, a.dSub, a.qd, red2);
-        const float ms = s.x / float(a.qd) + a.eps;
-        rinv = rsqrtf(ms);
-        c = s.y / float(a.qd) / ms;
-    }
+    if (sub) rms_coef2(sum_partials(a.part3, a.n3, red2), a.qd, a.eps, rinv, c);
     const int off = kvh * G * hd;
     for (int i = threadIdx.x; i < G * hd; i += blockDim.x) {
         const int q = off + i;
@@ -334,20 +407,20 @@ __global__ void __launch_bounds__(kThreads) dec_k4(DecodeArgs a) {
     for (int i = threadIdx.x; i < G * 2 * hd; i += blockDim.x) {
         float t = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) t += sR[w * G * 2 * hd + i];
+        for (int w = 0; w < kAWarps; ++w) t += sR[w * G * 2 * hd + i];
         const int g = i / (2 * hd), which = (i / hd) & 1, d = i % hd;
         float *dst = which ? a.Wpart : a.Upart;
         dst[(int64_t(chunk) * a.nh + kvh * G + g) * hd + d] = t;
     }
     if (threadIdx.x < G) {
         float t = 0.f;
-        for (int w = 0; w < kWarps; ++w) t += sDp[w][threadIdx.x];
+        for (int w = 0; w < kAWarps; ++w) t += sDp[w][threadIdx.x];
         a.Dpart[int64_t(chunk) * a.nh + kvh * G + threadIdx.x] = t;
     }
     // dV of the current token: dV[kvh, d] = sum_g attn[h_g, pos] dCtx_h_g[d]; gh_v share
     if (a.pos / kDecodeChunk == chunk) {
         __shared__ float sv[256];
-        __shared__ float rr[16][kWarps];
+        __shared__ float rr[16][kAWarps];
         for (int d = threadIdx.x; d < hd; d += blockDim.x) {
             float t = 0.f;
             for (int g = 0; g < G; ++g) t = fmaf(a.attn[int64_t(kvh * G + g) * a.L + a.pos], sC[g * hd + d], t);
@@ -372,7 +445,7 @@ __global__ void __launch_bounds__(kThreads) dec_k4(DecodeArgs a) {
         __syncthreads();
         if (threadIdx.x < a.rank) {
             float t = 0.f;
-            for (int w = 0; w < kWarps; ++w) t += rr[threadIdx.x][w];
+            for (int w = 0; w < kAWarps; ++w) t += rr[threadIdx.x][w];
             atomicAdd(a.gh + a.rank + threadIdx.x, a.lora_scaling * t);
         }
     }
@@ -386,24 +459,44 @@ __global__ void __launch_bounds__(kThreads) dec_k6(DecodeArgs a, RopeFreqs fr) {
     __shared__ float red[16][kWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int h = blockIdx.x;
-    pdl_trigger();
-    pdl_wait();
+    // blockDim / hd thread groups each sum a slice of the chunks, then combine
+    __shared__ float su[kThreads], sw[kThreads];
+    const int groups = blockDim.x / a.hd;
+    const int grp = threadIdx.x / a.hd, d = threadIdx.x % a.hd;
     if (threadIdx.x < 32) {
         float t = 0.f;
         for (int c = lane; c < a.nchunks; c += 32) t += a.Dpart[int64_t(c) * a.nh + h];
         t = warp_sum(t);
         if (lane == 0) sD = t;
     }
+    if (grp < groups) {
+        float u[4] = {0.f, 0.f, 0.f, 0.f}, w[4] = {0.f, 0.f, 0.f, 0.f};
+        int c = grp;
+        for (; c + 3 * groups < a.nchunks; c += 4 * groups) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int64_t idx = (int64_t(c + k * groups) * a.nh + h) * a.hd + d;
+                u[k] += a.Upart[idx];
+                w[k] += a.Wpart[idx];
+            }
+        }
+        for (; c < a.nchunks; c += groups) {
+            const int64_t idx = (int64_t(c) * a.nh + h) * a.hd + d;
+            u[0] += a.Upart[idx];
+            w[0] += a.Wpart[idx];
+        }
+        su[threadIdx.x] = (u[0] + u[1]) + (u[2] + u[3]);
+        sw[threadIdx.x] = (w[0] + w[1]) + (w[2] + w[3]);
+    }
     __syncthreads();
     const float D = sD;
-    for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
+    for (int dd = threadIdx.x; dd < a.hd; dd += blockDim.x) {
         float u = 0.f, w = 0.f;
-        for (int c = 0; c < a.nchunks; ++c) {
-            const int64_t idx = (int64_t(c) * a.nh + h) * a.hd + d;
-            u += a.Upart[idx];
-            w += a.Wpart[idx];
+        for (int g = 0; g < groups; ++g) {
+            u += su[g * a.hd + dd];
+            w += sw[g * a.hd + dd];
         }
-        sq[d] = a.scale * (u - D * w);
+        sq[dd] = a.scale * (u - D * w);
     }
     __syncthreads();
     const int half = a.hd >> 1;
@@ -451,8 +544,6 @@ __global__ void __launch_bounds__(kThreads) dec_k7(DecodeArgs a) {
     __shared__ float red[32];
     const int64_t nbq = int64_t(a.qd) * a.rank, nbv = int64_t(a.kvd) * a.rank, na = int64_t(a.rank) * a.H;
     const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    pdl_trigger();
-    pdl_wait();
     float g = 0.f;
     int which = -1;   // 0: sumsq of dA, 1: of dB
     if (e < nbq) {
@@ -501,17 +592,18 @@ __global__ void __launch_bounds__(kThreads) dec_k7(DecodeArgs a) {
 }
 
 template <typename... KArgs, typename... Args>
-cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, size_t smem, cudaStream_t st, bool pdl, Args... args) {
+cudaError_t launch_b(void (*kernel)(KArgs...), dim3 grid, int block, size_t smem, cudaStream_t st, bool pdl,
+                     Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = pdl ? 1 : 0;   // callers pass pdl = false: measured slower on this chain
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
@@ -519,13 +611,18 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, size_t smem, cudaStream_
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, size_t smem, cudaStream_t st, bool pdl, Args... args) {
+    return launch_b(kernel, grid, kThreads, smem, st, pdl, args...);
+}
+
 template <int VPL>
 cudaError_t launch_k4_g(int G, dim3 g4, size_t sm4, cudaStream_t st, const DecodeArgs &a) {
-    if (G <= 1) return launch(dec_k4<VPL, 1>, g4, sm4, st, true, a);
-    if (G <= 2) return launch(dec_k4<VPL, 2>, g4, sm4, st, true, a);
-    if (G <= 4) return launch(dec_k4<VPL, 4>, g4, sm4, st, true, a);
-    if (G <= 8) return launch(dec_k4<VPL, 8>, g4, sm4, st, true, a);
-    if constexpr (VPL <= 4) return launch(dec_k4<VPL, 16>, g4, sm4, st, true, a);
+    if (G <= 1) return launch_b(dec_k4<VPL, 1>, g4, kAThreads, sm4, st, false, a);
+    if (G <= 2) return launch_b(dec_k4<VPL, 2>, g4, kAThreads, sm4, st, false, a);
+    if (G <= 4) return launch_b(dec_k4<VPL, 4>, g4, kAThreads, sm4, st, false, a);
+    if (G <= 8) return launch_b(dec_k4<VPL, 8>, g4, kAThreads, sm4, st, false, a);
+    if constexpr (VPL <= 4) return launch_b(dec_k4<VPL, 16>, g4, kAThreads, sm4, st, false, a);
     return cudaErrorInvalidValue;
 }
 
@@ -540,38 +637,39 @@ cudaError_t launch_k4(int G, int hd, dim3 g4, size_t sm4, cudaStream_t st, const
 
 template <int WT>
 int launch_all(const DecodeArgs &a, cudaStream_t st) {
-    const int rows_per_block = kWarps * kR;
-    TLB_CUDA(launch(dec_k1<WT>, dim3(unsigned(ceil_div(a.I, rows_per_block))), size_t(a.H) * 4, st, false, a));
+    TLB_CUDA(launch(dec_k1<WT>, dim3(unsigned(a.n1)), size_t(a.H) * 4, st, false, a));
     TLB_TRY(check_launch("decode k1"));
     const size_t sm2 = size_t(2) * a.I * 4;
-    const dim3 g2(unsigned(ceil_div(a.H, rows_per_block)));
-    if (a.act == TLB_ACT_RELU2_MUL) TLB_CUDA(launch(dec_k2<WT, TLB_ACT_RELU2_MUL>, g2, sm2, st, true, a));
-    else TLB_CUDA(launch(dec_k2<WT, TLB_ACT_SILU_MUL>, g2, sm2, st, true, a));
+    const dim3 g2(unsigned(a.n2));
+    if (a.act == TLB_ACT_RELU2_MUL) TLB_CUDA(launch(dec_k2<WT, TLB_ACT_RELU2_MUL>, g2, sm2, st, false, a));
+    else TLB_CUDA(launch(dec_k2<WT, TLB_ACT_SILU_MUL>, g2, sm2, st, false, a));
     TLB_TRY(check_launch("decode k2"));
-    TLB_CUDA(launch(dec_k3<WT>, dim3(unsigned(ceil_div(a.qd, rows_per_block))), size_t(a.H) * 4, st, true, a));
+    TLB_CUDA(launch(dec_k3<WT>, dim3(unsigned(a.n3)), size_t(a.H) * 4, st, false, a));
     TLB_TRY(check_launch("decode k3"));
     const int G = a.nh / a.nkv;
     const dim3 g4(a.nkv, a.nchunks);
-    const size_t sm4 = (size_t(G) * a.hd + size_t(kWarps) * G * 2 * a.hd) * 4;
+    const size_t sm4 = (size_t(G) * a.hd + size_t(kAWarps) * G * 2 * a.hd) * 4;
     TLB_CUDA(launch_k4(G, a.hd, g4, sm4, st, a));
     TLB_TRY(check_launch("decode k4"));
     RopeFreqs fr;
     rope_freqs(fr, a.hd, a.rope_base);
-    TLB_CUDA(launch(dec_k6, dim3(a.nh), 0, st, true, a, fr));
+    TLB_CUDA(launch(dec_k6, dim3(a.nh), 0, st, false, a, fr));
     TLB_TRY(check_launch("decode k6"));
     const int64_t n7 = int64_t(a.qd + a.kvd) * a.rank + 2 * int64_t(a.rank) * a.H;
-    TLB_CUDA(launch(dec_k7, dim3(unsigned(ceil_div(n7, kThreads))), 0, st, true, a));
+    TLB_CUDA(launch(dec_k7, dim3(unsigned(ceil_div(n7, kThreads))), 0, st, false, a));
     return check_launch("decode k7");
 }
 
 }  // namespace
+
+int decode_rows_per_block() { return kWarps * kR; }
 
 bool decode_supported(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     const int G = c.n_heads / c.n_kv_heads;
     const int E = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 8 : 16);
     const int hd = c.head_dim;
     const int gmax = hd > 128 ? 8 : 16;   // heads per KV group held in registers by k4
-    const size_t sm4 = (size_t(G) * hd + size_t(kWarps) * G * 2 * hd) * 4;
+    const size_t sm4 = (size_t(G) * hd + size_t(kAWarps) * G * 2 * hd) * 4;
     return S == 1 && G <= gmax && c.rank <= 16 && (hd == 32 || hd == 64 || hd == 128 || hd == 256) &&
            c.dim % E == 0 && c.ffn_dim % E == 0 && size_t(2) * c.ffn_dim * 4 <= 200 * 1024 &&
            sm4 <= 200 * 1024 && L >= 1;

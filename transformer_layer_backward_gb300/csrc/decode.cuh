@@ -19,16 +19,16 @@ struct DecodeArgs {
     tlb_lora lq, lv;
     AdamCoef ka, kb;
     double *sumsq;
-    // regions read after the first kernel, prefetched into L2 while it runs
-    const char *pf_ptr[24];
-    uint64_t pf_bytes[24];
-    int pf_count;
-    uint64_t pf_total;
+    // per-block partial sums (sum dy g x, sum x^2) for the RMSNorm backward of the
+    // vector each GEMV produces; n1..n3 = the GEMV grids (blocks of k1, k2, k3)
+    float2 *part1, *part2, *part3;
+    int n1, n2, n3;
 };
 
-constexpr int kDecodeChunk = 32;   // keys per block in the attention passes
+constexpr int kDecodeChunk = 64;   // keys per block in the attention pass
 
 bool decode_supported(const tlb_layer_cfg &c, int64_t S, int64_t L);
+int decode_rows_per_block();
 int decode_layer_launch(const DecodeArgs &a, int wtype, cudaStream_t st);
 
 }  // namespace tlb

@@ -12,7 +12,7 @@ namespace {
 
 struct LayerWs {
     size_t dF, dG, dU, dN2, dSub, dqpre, dv, gh_q, gh_v;
-    size_t dR1, Upart, Wpart, Dpart, gh2;   // single-token path
+    size_t dR1, Upart, Wpart, Dpart, gh2, part1, part2, part3;   // single-token path
     size_t total;
 };
 
@@ -37,8 +37,11 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
         w.Wpart = p.take(nchunks * qd * 4);
         w.Dpart = p.take(nchunks * c.n_heads * 4);
         w.gh2 = p.take(2 * int64_t(c.rank) * 4);
+        w.part1 = p.take(ceil_div(I, 8) * 8);   // one float2 per block of >= 8 rows
+        w.part2 = p.take(ceil_div(H, 8) * 8);
+        w.part3 = p.take(ceil_div(qd, 8) * 8);
     } else {
-        w.dR1 = w.Upart = w.Wpart = w.Dpart = w.gh2 = 0;
+        w.dR1 = w.Upart = w.Wpart = w.Dpart = w.gh2 = w.part1 = w.part2 = w.part3 = 0;
     }
     w.total = p.off;
     return w;
@@ -240,8 +243,14 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
     const LayerWs p = plan(c, S, L);
     const int qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
     float *dqpre = ws_at<float>(ws, p.dqpre), *dv = ws_at<float>(ws, p.dv);
-    if (decode_supported(c, S, L) && aligned16(w->w_down.w) && aligned16(w->w_gate.w) &&
-        aligned16(w->w_up.w) && aligned16(w->w_o.w)) {
+    bool vec_ok = true;   // the single-token kernels read every vector with 16-byte loads
+    for (const void *ptr : {(const void *)w->w_down.w, (const void *)w->w_gate.w, (const void *)w->w_up.w,
+                            (const void *)w->w_o.w, (const void *)w->gamma_sub_ffn, (const void *)w->gamma_ffn,
+                            (const void *)w->gamma_sub_attn, (const void *)acts->gate, (const void *)acts->up,
+                            (const void *)acts->silu_gate, (const void *)acts->hidden, (const void *)acts->r1,
+                            (const void *)acts->ctx, (const void *)d_hidden})
+        vec_ok = vec_ok && (ptr == nullptr || aligned16(ptr));
+    if (decode_supported(c, S, L) && vec_ok) {
         DecodeArgs d;
         d.H = c.dim;
         d.I = c.ffn_dim;
@@ -302,35 +311,13 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
         d.ka = adam_coef(*adam, 1.0f);
         d.kb = adam_coef(*adam, float(adam->lr_b_mult));
         d.sumsq = sumsq;
-        // L2 prefetch list: what k2..k7 read, in the order they read it
-        const size_t es = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 2 : 1);
-        d.pf_count = 0;
-        d.pf_total = 0;
-        auto add = [&](const void *ptr, uint64_t bytes) {
-            if (ptr == nullptr || !aligned16(ptr) || d.pf_count >= 24) return;
-            bytes &= ~uint64_t(15);
-            if (bytes == 0) return;
-            d.pf_ptr[d.pf_count] = static_cast<const char *>(ptr);
-            d.pf_bytes[d.pf_count++] = bytes;
-            d.pf_total += bytes;
-        };
-        const uint64_t kv_span = (uint64_t(c.n_kv_heads - 1) * acts->kv_stride_head +
-                                  uint64_t(L - 1) * acts->kv_stride_pos + c.head_dim) * 4;
-        add(w->w_gate.w, uint64_t(c.dim) * c.ffn_dim * es);
-        add(w->w_up.w, uint64_t(c.dim) * c.ffn_dim * es);
-        add(w->w_o.w, uint64_t(qd) * c.dim * es);
-        add(acts->k, kv_span);
-        add(acts->v, kv_span);
-        add(acts->attn, uint64_t(c.n_heads) * L * 4);
-        for (const tlb_lora *l : {lora_q, lora_v}) {
-            const uint64_t nb = uint64_t(l == lora_q ? qd : kvd) * c.rank * 4, na = uint64_t(c.rank) * c.dim * 4;
-            add(l->b, nb);
-            add(l->m_b, nb);
-            add(l->v_b, nb);
-            add(l->a, na);
-            add(l->m_a, na);
-            add(l->v_a, na);
-        }
+        const int rpb = decode_rows_per_block();
+        d.n1 = int(ceil_div(c.ffn_dim, rpb));
+        d.n2 = int(ceil_div(c.dim, rpb));
+        d.n3 = int(ceil_div(qd, rpb));
+        d.part1 = ws_at<float2>(ws, p.part1);
+        d.part2 = ws_at<float2>(ws, p.part2);
+        d.part3 = ws_at<float2>(ws, p.part3);
         return decode_layer_launch(d, c.wtype, st);
     }
     TLB_TRY(ffn_impl(c, S, d_hidden, *w, *acts, d_hidden, ws, st));
