@@ -23,7 +23,10 @@
  *     Calls only enqueue work: they never allocate, free or synchronise (except
  *     tlb_workspace_status), so a sequence of calls can be captured into a CUDA
  *     graph.  Scratch memory comes from the caller's workspace `ws` of `ws_bytes`
- *     bytes (256-byte aligned), sized by tlb_workspace_bytes().
+ *     bytes (256-byte aligned), sized by tlb_workspace_bytes().  A workspace must be
+ *     zero-filled before its first use (it holds a device status block and grid-barrier
+ *     counters that every call leaves as it found them); calls sharing a workspace must
+ *     not overlap on the GPU.
  *   - Return value: TLB_OK or a negative TLB_E* code; tlb_last_error() gives a
  *     message (thread-local) for the last failing call of this thread.  Argument
  *     errors are detected on the host before anything is enqueued.  Errors found

@@ -34,53 +34,6 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kAWarps = 8;               // attention kernel (holds per-head accumulators)
 constexpr int kAThreads = kAWarps * 32;
 
-template <int WT>
-struct EPC {
-    static constexpr int v = WT == TLB_W_F32 ? 4 : (WT == TLB_W_BF16 ? 8 : 16);
-};
-
-template <int WT>
-__device__ __forceinline__ float chunk_dot(uint4 w, const float *x) {
-    if constexpr (WT == TLB_W_F32) {
-        return __uint_as_float(w.x) * x[0] + __uint_as_float(w.y) * x[1] + __uint_as_float(w.z) * x[2] +
-               __uint_as_float(w.w) * x[3];
-    } else if constexpr (WT == TLB_W_BF16) {
-        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s += bf16_lo(q[i]) * x[2 * i] + bf16_hi(q[i]) * x[2 * i + 1];
-        return s;
-    } else {
-        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float a, b, c, d;
-            i8x4_to_f32(q[i], a, b, c, d);
-            s0 = fmaf(a, x[4 * i], s0);
-            s1 = fmaf(b, x[4 * i + 1], s1);
-            s0 = fmaf(c, x[4 * i + 2], s0);
-            s1 = fmaf(d, x[4 * i + 3], s1);
-        }
-        return s0 + s1;
-    }
-}
-
-// Shared-memory position of float4 unit u of a GEMV vector: lane l reads chunk
-// ch = base + l, i.e. units ch*P .. ch*P + P - 1 (P = float4 units per 16-byte weight
-// chunk); XOR-ing the unit index within its chunk with bits of ch puts the 8 lanes of
-// each 128-byte shared-memory phase on 8 different 16-byte bank groups.
-template <int WT>
-__device__ __forceinline__ int xunit(int u) {
-    constexpr int P = EPC<WT>::v / 4;
-    if constexpr (P == 1) {
-        return u;
-    } else {
-        const int ch = u / P, k = u % P;
-        return ch * P + (k ^ ((ch / (8 / P)) % P));
-    }
-}
-
 // Rows [r0, r0 + R) of NM matrices (same shape [rows, cols]), each dotted with its own
 // shared-memory vector (swizzled by xunit), scaled and summed:
 //   y[r] = sum_m scale_m W_m[r, :] . x_m.

@@ -25,9 +25,66 @@ struct DecodeArgs {
     int n1, n2, n3;
 };
 
+// Weight elements per 16-byte chunk of a row.
+template <int WT>
+struct EPC {
+    static constexpr int v = WT == TLB_W_F32 ? 4 : (WT == TLB_W_BF16 ? 8 : 16);
+};
+
+template <int WT>
+__device__ __forceinline__ float chunk_dot(uint4 w, const float *x) {
+    if constexpr (WT == TLB_W_F32) {
+        return __uint_as_float(w.x) * x[0] + __uint_as_float(w.y) * x[1] + __uint_as_float(w.z) * x[2] +
+               __uint_as_float(w.w) * x[3];
+    } else if constexpr (WT == TLB_W_BF16) {
+        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s += bf16_lo(q[i]) * x[2 * i] + bf16_hi(q[i]) * x[2 * i + 1];
+        return s;
+    } else {
+        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float a, b, c, d;
+            i8x4_to_f32(q[i], a, b, c, d);
+            s0 = fmaf(a, x[4 * i], s0);
+            s1 = fmaf(b, x[4 * i + 1], s1);
+            s0 = fmaf(c, x[4 * i + 2], s0);
+            s1 = fmaf(d, x[4 * i + 3], s1);
+        }
+        return s0 + s1;
+    }
+}
+
+// Shared-memory position of float4 unit u of a GEMV vector: lane l reads chunk
+// ch = base + l, i.e. units ch*P .. ch*P + P - 1 (P = float4 units per 16-byte weight
+// chunk); XOR-ing the unit index within its chunk with bits of ch puts the 8 lanes of
+// each 128-byte shared-memory phase on 8 different 16-byte bank groups.
+template <int WT>
+__device__ __forceinline__ int xunit(int u) {
+    constexpr int P = EPC<WT>::v / 4;
+    if constexpr (P == 1) {
+        return u;
+    } else {
+        const int ch = u / P, k = u % P;
+        return ch * P + (k ^ ((ch / (8 / P)) % P));
+    }
+}
+
+
 constexpr int kDecodeChunk = 64;   // keys per block in the attention pass
 
 bool decode_supported(const tlb_layer_cfg &c, int64_t S, int64_t L);
+
+// Persistent single-kernel version (decode_persistent.cu).  Its workspace needs, besides
+// the DecodeArgs regions, a zero-initialised grid-barrier word pair (off_gbar) and
+// 3 * kMaxPersistentBlocks float2 partial sums (off_pp).
+constexpr int kMaxPersistentBlocks = 1024;
+bool persistent_supported(const tlb_layer_cfg &c, int64_t S, int64_t L);
+int decode_persistent_launch(const DecodeArgs &d, const tlb_layer_cfg &c, int64_t L, void *ws, size_t off_gbar,
+                             size_t off_pp, cudaStream_t st);
 int decode_rows_per_block();
 int decode_layer_launch(const DecodeArgs &a, int wtype, cudaStream_t st);
 
