@@ -6,25 +6,30 @@
 // output, so a multi-kernel version pays a launch, a prologue and a memory latency
 // per step while HBM idles.  Here one block per SM runs all phases, separated by
 // grid barriers, and the weight rows of the three transposed-weight GEMVs stream into
-// shared memory through TMA bulk copies (cp.async.bulk + mbarrier): each warp owns a
-// shared-memory slot and, as soon as it has consumed an item, issues the copy of its
-// next item -- which belongs to the next phase when the current one is done.  So the
-// weights of phase p+1 arrive while the grid barrier and the prologue of phase p+1
-// run, and HBM streams W_down, W_gate | W_up and W_O back to back.
+// shared memory through TMA bulk copies (cp.async.bulk + mbarrier).  Each GEMV warp
+// owns two shared-memory slots: while it computes on one, the copy of its next item
+// lands in the other, and as soon as an item is consumed the warp starts the copy of
+// the item after next -- which belongs to the next phase once the current one is
+// done.  So the weights of phase p+1 arrive while the grid barrier and the prologue
+// of phase p+1 run, and HBM streams W_down, W_gate | W_up and W_O back to back.
 //
 //   phase 1  dF   = s_d W_down dOut                      (+ partial sums for the sub-norm)
 //   phase 2  dG, dU (sub-norm RMSNorm bwd + gated-activation bwd, per block), then
-//            dN2  = s_g W_gate dG + s_u W_up dU           (+ partial sums for the pre-norm)
+//            dN2  = s_g W_gate dG + s_u W_up dU           (rows split in column ranges)
 //   phase 3  dR1  = dOut + RMSNorm_bwd(r1, g_ffn, dN2), then dSub = s_o W_O dR1
 //   phase 4  per (KV head, 32 keys): dCtx (sub-norm bwd), one pass over K and V:
-//            dA = dCtx_h . V[j], U += P dA K[j], W += P K[j], D += P dA; dV and gh_v
-//   phase 5  per head: dQ = scale (U - D W), RoPE bwd -> dQpre, gh_q
-//   phase 6  dB = s G h^T, dA = gh x^T for both adapters, AdamW with LoRA+ on B
+//            dA = dCtx_h . V[j], U += P dA K[j], W += P K[j], D += P dA  (per head),
+//            so that dQ_h = scale (U_h - D_h W_h) over all chunks; the chunk's
+//            RoPE-rotated U and W are also projected on B_q (gh_q is linear in dQ);
+//            the chunk holding the current position forms dV and gh_v
+//   phase 5  dQpre = R(-theta) scale (U - D W); dB = s G h^T, dA = gh x^T for both
+//            adapters, AdamW with LoRA+ on B
 //
-// Waits are bounded: a timed-out mbarrier or grid barrier records TLB_ETIMEOUT in the
-// workspace status block and the kernel winds down (waiting, bounded, for its own
-// copies in flight).  A timed-out call leaves the barrier state of its workspace
-// undefined: zero the workspace before reusing it.
+// Grid barriers count on one monotonic 64-bit word of the workspace (release-add to
+// arrive, acquire-load to wait).  Waits are bounded: a timed-out mbarrier or barrier
+// records TLB_ETIMEOUT in the workspace status block and the kernel winds down
+// (waiting, bounded, for its own copies in flight); the workspace must then be zeroed
+// before it is used again.
 #include "async.cuh"
 #include "common.cuh"
 #include "decode.cuh"
@@ -40,37 +45,48 @@ constexpr int kPW = 16;                 // warps per block
 constexpr int kPT = kPW * 32;
 constexpr int kMaxRowsPerItem = 8;
 constexpr int kKeysPerItem = 32;        // attention keys per (KV head, chunk) item
+constexpr int kBarriers = 4;            // grid barriers per call
+constexpr int kMaxBlockRows = 256;      // phase-2 rows per block held in shared memory
 
 struct PArgs {
     DecodeArgs d;
     uint32_t *status;                   // workspace status block
-    unsigned *gbar;                     // grid barrier: [0] arrivals, [1] generation
+    unsigned long long *gbar;           // grid barrier: monotonic arrival count
     float2 *pp;                         // per-block partial sums, 3 x nblocks
-    int nblocks, nslots, slot_bytes, xbytes;
-    int rpi1, rpi3;                     // rows per item in phases 1 and 3
+    float *Uacc, *Wacc, *Dacc;          // [q_dim], [q_dim], [n_heads]  (zeroed in the call)
+    float *ug, *wg;                     // [n_heads, rank] projections of R(U), R(W) on B_q
+    int nblocks, ngemv, slot_bytes, xbytes;
+    int rpi;                            // rows per item in phases 1 and 3
+    int nsplit;                         // column ranges per phase-2 row
     int achunks;                        // ceil(L / kKeysPerItem)
     RopeFreqs fr;
 };
 
-__device__ __forceinline__ bool grid_sync(const PArgs &p, int site, int *s_abort) {
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Barrier k (1-based) of this call: every block adds 1 to the monotonic counter and
+// waits until it reaches base + k * nblocks.
+__device__ __forceinline__ bool grid_sync(const PArgs &p, int k, unsigned long long base, int *s_abort) {
     __syncthreads();
     if (threadIdx.x == 0 && !*s_abort) {
-        volatile unsigned *gen = p.gbar + 1;
-        const unsigned g = *gen;
         __threadfence();
-        if (atomicAdd(p.gbar, 1u) == unsigned(p.nblocks) - 1u) {
-            atomicExch(p.gbar, 0u);
-            __threadfence();
-            atomicAdd(p.gbar + 1, 1u);
-        } else {
+        red_release_add_u64(p.gbar, 1ull);
+        const unsigned long long target = base + (unsigned long long)k * p.nblocks;
+        if (ld_acquire_u64(p.gbar) < target) {
             const long long t0 = clock64();
-            while (*gen == g) {
+            while (ld_acquire_u64(p.gbar) < target) {
                 if (clock64() - t0 > kWaitLimitCycles) {
-                    report_timeout(p.status, 100u + unsigned(site));
+                    report_timeout(p.status, 100u + unsigned(k));
                     *s_abort = 1;
                     break;
                 }
-                __nanosleep(32);
             }
         }
         __threadfence();
@@ -95,9 +111,9 @@ __device__ __forceinline__ ItemMap item_map(const PArgs &p) {
     block_rows(p.d.I, blockIdx.x, p.nblocks, m.a0, m.a1);
     block_rows(p.d.H, blockIdx.x, p.nblocks, m.b0, m.b1);
     block_rows(p.d.qd, blockIdx.x, p.nblocks, m.c0, m.c1);
-    m.n1 = (m.a1 - m.a0 + p.rpi1 - 1) / p.rpi1;
-    m.n2 = m.b1 - m.b0;
-    m.n3 = (m.c1 - m.c0 + p.rpi3 - 1) / p.rpi3;
+    m.n1 = (m.a1 - m.a0 + p.rpi - 1) / p.rpi;
+    m.n2 = (m.b1 - m.b0) * p.nsplit;
+    m.n3 = (m.c1 - m.c0 + p.rpi - 1) / p.rpi;
     return m;
 }
 
@@ -108,31 +124,34 @@ __device__ __forceinline__ void issue_item(const PArgs &p, const ItemMap &m, int
     const DecodeArgs &d = p.d;
     fence_proxy_async();
     if (g < m.n1) {
-        const int r0 = m.a0 + g * p.rpi1;
-        const int k = min(p.rpi1, m.a1 - r0);
+        const int r0 = m.a0 + g * p.rpi;
+        const int k = min(p.rpi, m.a1 - r0);
         const uint32_t rb = uint32_t(d.H) * ES;
         mbar_arrive_expect_tx(bar, rb * k);
         tma_load_1d(slot, static_cast<const char *>(d.w_down) + size_t(r0) * rb, rb * k, bar);
     } else if (g < m.n1 + m.n2) {
-        const int h = m.b0 + (g - m.n1);
-        const uint32_t rb = uint32_t(d.I) * ES;
-        mbar_arrive_expect_tx(bar, 2 * rb);
-        tma_load_1d(slot, static_cast<const char *>(d.w_gate) + size_t(h) * rb, rb, bar);
-        tma_load_1d(slot + rb, static_cast<const char *>(d.w_up) + size_t(h) * rb, rb, bar);
+        const int j = g - m.n1;
+        const int h = m.b0 + j / p.nsplit, q = j % p.nsplit;
+        const uint32_t rb = uint32_t(d.I) * ES;            // full row bytes
+        const uint32_t pb = rb / p.nsplit;                  // bytes of one column range
+        mbar_arrive_expect_tx(bar, 2 * pb);
+        tma_load_1d(slot, static_cast<const char *>(d.w_gate) + size_t(h) * rb + size_t(q) * pb, pb, bar);
+        tma_load_1d(slot + pb, static_cast<const char *>(d.w_up) + size_t(h) * rb + size_t(q) * pb, pb, bar);
     } else {
-        const int r0 = m.c0 + (g - m.n1 - m.n2) * p.rpi3;
-        const int k = min(p.rpi3, m.c1 - r0);
+        const int r0 = m.c0 + (g - m.n1 - m.n2) * p.rpi;
+        const int k = min(p.rpi, m.c1 - r0);
         const uint32_t rb = uint32_t(d.H) * ES;
         mbar_arrive_expect_tx(bar, rb * k);
         tma_load_1d(slot, static_cast<const char *>(d.w_o) + size_t(r0) * rb, rb * k, bar);
     }
 }
 
-// One warp: k rows of `cols` weights in shared memory (row stride rb bytes) dotted with
-// the swizzled vector x; returns the k sums (times scale) to every lane.
+// One warp: k rows of `cols` weights in shared memory (row stride rb bytes), starting at
+// chunk ch0 of the full vector, dotted with the swizzled vector x; the k sums (times
+// scale) go to every lane.
 template <int WT>
-__device__ __forceinline__ void dot_rows(const char *slot, int k, int cols, uint32_t rb, const float *x, float scale,
-                                         float *out) {
+__device__ __forceinline__ void dot_rows(const char *slot, int k, int cols, uint32_t rb, int ch0, const float *x,
+                                         float scale, float *out) {
     constexpr int E = EPC<WT>::v, P = E / 4;
     const int lane = threadIdx.x & 31;
     const int nch = cols / E;
@@ -143,7 +162,7 @@ __device__ __forceinline__ void dot_rows(const char *slot, int k, int cols, uint
         float xv[E];
 #pragma unroll
         for (int q = 0; q < P; ++q) {
-            const float4 t = reinterpret_cast<const float4 *>(x)[xunit<WT>(c * P + q)];
+            const float4 t = reinterpret_cast<const float4 *>(x)[xunit<WT>((ch0 + c) * P + q)];
             xv[4 * q] = t.x;
             xv[4 * q + 1] = t.y;
             xv[4 * q + 2] = t.z;
@@ -156,8 +175,6 @@ __device__ __forceinline__ void dot_rows(const char *slot, int k, int cols, uint
 #pragma unroll
     for (int r = 0; r < kMaxRowsPerItem; ++r) out[r] = scale * warp_sum(acc[r]);
 }
-
-__device__ __forceinline__ float2 block_sum2_all(float2 v, float2 *red) { return block_sum2(v, red); }
 
 // Sum of nb partials (every thread gets it).
 __device__ __forceinline__ float2 sum_pp(const float2 *pp, int nb, float2 *red) {
@@ -181,29 +198,49 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
     constexpr int GM = 16 / VPL;                 // heads per KV group held in registers
     constexpr int ES = 16 / EPC<WT>::v;
     extern __shared__ float4 smem4[];
-    __shared__ uint64_t mbar[kPW];
+    __shared__ uint64_t mbar[2 * kPW];
     __shared__ float2 red[32];
     __shared__ int s_abort;
+    __shared__ unsigned long long s_base;
     __shared__ float2 s_acc[kPW];
+    __shared__ float racc[kMaxBlockRows];
     const DecodeArgs &d = p.d;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     char *smem = reinterpret_cast<char *>(smem4);
     float *sX = reinterpret_cast<float *>(smem);
     char *slots = smem + p.xbytes;
-    const bool gemv_warp = warp < p.nslots;
-    char *slot = slots + size_t(warp) * p.slot_bytes;
+    const bool gemv_warp = warp < p.ngemv;
 
-    if (threadIdx.x == 0) s_abort = 0;
-    if (lane == 0 && gemv_warp) mbar_init(&mbar[warp], 1);
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        const unsigned long long v = *reinterpret_cast<volatile unsigned long long *>(p.gbar);
+        const unsigned long long per_call = (unsigned long long)kBarriers * p.nblocks;
+        s_base = v - v % per_call;
+    }
+    if (lane == 0 && gemv_warp) {
+        mbar_init(&mbar[2 * warp], 1);
+        mbar_init(&mbar[2 * warp + 1], 1);
+    }
     fence_mbar_init();
     __syncthreads();
+    const unsigned long long base = s_base;
 
     const ItemMap m = item_map(p);
     const int total = m.n1 + m.n2 + m.n3;
-    // first item of each GEMV warp: the weights start streaming right away
-    if (gemv_warp && lane == 0 && warp < total) issue_item<WT>(p, m, warp, slot, &mbar[warp]);
-    if (blockIdx.x == 0 && threadIdx.x < 2 * d.rank) d.gh[threadIdx.x] = 0.f;
-
+    // the first two items of each GEMV warp: the weights start streaming right away
+    if (gemv_warp && lane == 0) {
+        for (int i = 0; i < 2; ++i) {
+            const int g = warp + i * p.ngemv;
+            if (g < total) issue_item<WT>(p, m, g, slots + size_t(2 * warp + i) * p.slot_bytes, &mbar[2 * warp + i]);
+        }
+    }
+    // accumulators of this call (read only after later barriers)
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i < d.qd; i += blockDim.x) p.Uacc[i] = p.Wacc[i] = 0.f;
+        for (int i = threadIdx.x; i < d.nh * d.rank; i += blockDim.x) p.ug[i] = p.wg[i] = 0.f;
+        if (threadIdx.x < d.nh) p.Dacc[threadIdx.x] = 0.f;
+        if (threadIdx.x < 2 * d.rank) d.gh[threadIdx.x] = 0.f;
+    }
     // phase 1 vector: dOut
     {
         const float4 *x4 = reinterpret_cast<const float4 *>(d.d_hidden);
@@ -211,14 +248,13 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
     }
     __syncthreads();
 
-    int g = warp;            // next item of this warp
-    uint32_t parity = 0;
+    int it = 0;              // index of this warp's next item (its global number is warp + it * ngemv)
     bool ok = true;
-    // ---------------------------------------------------------------- phases 1..3
+    // ---------------------------------------------------------------- phases 1..3: GEMVs
     for (int phase = 1; phase <= 3; ++phase) {
         float rinv = 1.f, c = 0.f;
         if (phase == 2) {
-            if (!grid_sync(p, 1, &s_abort)) { ok = false; break; }
+            if (!grid_sync(p, 1, base, &s_abort)) { ok = false; break; }
             const bool sub = d.flags & TLB_SUB_NORM;
             if (sub) coef(sum_pp(p.pp, p.nblocks, red), d.I, d.eps, rinv, c);
             const bool cache = d.act == TLB_ACT_SILU_MUL && (d.flags & TLB_USE_SILU_CACHE);
@@ -254,9 +290,10 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
                 reinterpret_cast<float4 *>(sG)[xunit<WT>(i)] = make_float4(og[0], og[1], og[2], og[3]);
                 reinterpret_cast<float4 *>(sU)[xunit<WT>(i)] = make_float4(ou[0], ou[1], ou[2], ou[3]);
             }
+            for (int i = threadIdx.x; i < m.b1 - m.b0; i += blockDim.x) racc[i] = 0.f;
             __syncthreads();
         } else if (phase == 3) {
-            if (!grid_sync(p, 2, &s_abort)) { ok = false; break; }
+            if (!grid_sync(p, 2, base, &s_abort)) { ok = false; break; }
             const bool pre = d.flags & TLB_PRE_NORM, resid = d.flags & TLB_RESIDUAL;
             if (pre) coef(sum_pp(p.pp + p.nblocks, p.nblocks, red), d.H, d.eps, rinv, c);
             const int n4 = d.H >> 2;
@@ -276,94 +313,121 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
             }
             __syncthreads();
         }
-        // items of this phase owned by this warp
-        const int gbeg = phase == 1 ? 0 : (phase == 2 ? m.n1 : m.n1 + m.n2);
         const int gend = phase == 1 ? m.n1 : (phase == 2 ? m.n1 + m.n2 : total);
-        float2 acc = make_float2(0.f, 0.f);     // (sum y g z, sum z^2), lane 0
+        const int gbeg = phase == 1 ? 0 : (phase == 2 ? m.n1 : m.n1 + m.n2);
+        float2 acc = make_float2(0.f, 0.f);     // (sum y g z, sum z^2) of phases 1 and 3, lane 0
         if (gemv_warp) {
-            for (; g < gend && g >= gbeg; g += p.nslots) {
-                if (!mbar_wait(&mbar[warp], parity, p.status, 1u)) { ok = false; break; }
-                parity ^= 1u;
+            for (int g = warp + it * p.ngemv; g < gend; g = warp + it * p.ngemv) {
+                const int sidx = 2 * warp + (it & 1);
+                char *slot = slots + size_t(sidx) * p.slot_bytes;
+                if (!mbar_wait(&mbar[sidx], (it >> 1) & 1, p.status, 1u)) { ok = false; break; }
                 float out[kMaxRowsPerItem];
-                int row0, k;
+                int row0 = 0, k = 0;
                 if (phase == 2) {
-                    row0 = m.b0 + (g - m.n1);
-                    k = 1;
-                    const uint32_t rb = uint32_t(d.I) * ES;
+                    const int j = g - m.n1;
+                    row0 = m.b0 + j / p.nsplit;
+                    const int q = j % p.nsplit;
+                    const int cols = d.I / p.nsplit;
+                    const uint32_t pb = uint32_t(cols) * ES;
+                    const int ch0 = q * (cols / EPC<WT>::v);
                     float o2[kMaxRowsPerItem];
-                    dot_rows<WT>(slot, 1, d.I, rb, sX, d.s_gate, out);
-                    dot_rows<WT>(slot + rb, 1, d.I, rb, sX + d.I, d.s_up, o2);
+                    dot_rows<WT>(slot, 1, cols, pb, ch0, sX, d.s_gate, out);
+                    dot_rows<WT>(slot + pb, 1, cols, pb, ch0, sX + d.I, d.s_up, o2);
                     out[0] += o2[0];
                 } else {
-                    const int rpi = phase == 1 ? p.rpi1 : p.rpi3;
-                    const int base = phase == 1 ? m.a0 : m.c0;
+                    const int base_r = phase == 1 ? m.a0 : m.c0;
                     const int lim = phase == 1 ? m.a1 : m.c1;
-                    row0 = base + (g - gbeg) * rpi;
-                    k = min(rpi, lim - row0);
-                    dot_rows<WT>(slot, k, d.H, uint32_t(d.H) * ES, sX, phase == 1 ? d.s_down : d.s_o, out);
+                    row0 = base_r + (g - gbeg) * p.rpi;
+                    k = min(p.rpi, lim - row0);
+                    dot_rows<WT>(slot, k, d.H, uint32_t(d.H) * ES, 0, sX, phase == 1 ? d.s_down : d.s_o, out);
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    if (g + p.nslots < total) issue_item<WT>(p, m, g + p.nslots, slot, &mbar[warp]);
-                    float *y = phase == 1 ? d.dF : (phase == 2 ? d.dN2 : d.dSub);
-                    const float *gam = phase == 1 ? d.g_sub_ffn : (phase == 2 ? d.g_ffn : d.g_sub_attn);
-                    const float *z = phase == 1 ? d.hidden : (phase == 2 ? d.r1 : d.ctx);
+                    const int gn = g + 2 * p.ngemv;
+                    if (gn < total) issue_item<WT>(p, m, gn, slot, &mbar[sidx]);
+                    if (phase == 2) {
+                        atomicAdd(&racc[row0 - m.b0], out[0]);
+                    } else {
+                        float *y = phase == 1 ? d.dF : d.dSub;
+                        const float *gam = phase == 1 ? d.g_sub_ffn : d.g_sub_attn;
+                        const float *z = phase == 1 ? d.hidden : d.ctx;
 #pragma unroll
-                    for (int r = 0; r < kMaxRowsPerItem; ++r) {
-                        if (r < k) {
-                            y[row0 + r] = out[r];
-                            if (gam != nullptr) {
-                                const float zz = z[row0 + r];
-                                acc.x += out[r] * gam[row0 + r] * zz;
-                                acc.y += zz * zz;
+                        for (int r = 0; r < kMaxRowsPerItem; ++r) {
+                            if (r < k) {
+                                y[row0 + r] = out[r];
+                                if (gam != nullptr) {
+                                    const float zz = z[row0 + r];
+                                    acc.x += out[r] * gam[row0 + r] * zz;
+                                    acc.y += zz * zz;
+                                }
                             }
                         }
                     }
                 }
+                ++it;
             }
         }
         if (lane == 0) s_acc[warp] = acc;
         __syncthreads();
-        if (threadIdx.x == 0) {
+        if (phase == 2) {
+            // the block's dN2 rows are complete in racc: store them, partial sums for the pre-norm
+            float2 t = make_float2(0.f, 0.f);
+            for (int i = threadIdx.x; i < m.b1 - m.b0; i += blockDim.x) {
+                const float v = racc[i];
+                d.dN2[m.b0 + i] = v;
+                if (d.g_ffn != nullptr) {
+                    const float zz = d.r1[m.b0 + i];
+                    t.x += v * d.g_ffn[m.b0 + i] * zz;
+                    t.y += zz * zz;
+                }
+            }
+            t = block_sum2(t, red);
+            if (threadIdx.x == 0) p.pp[p.nblocks + blockIdx.x] = t;
+        } else if (threadIdx.x == 0) {
             float2 t = make_float2(0.f, 0.f);
             for (int w = 0; w < kPW; ++w) {
                 t.x += s_acc[w].x;
                 t.y += s_acc[w].y;
             }
-            if (phase < 3) p.pp[(phase - 1) * p.nblocks + blockIdx.x] = t;
-            else p.pp[2 * p.nblocks + blockIdx.x] = t;
+            p.pp[(phase == 1 ? 0 : 2) * p.nblocks + blockIdx.x] = t;
         }
-        __syncthreads();
         if (!ok) s_abort = 1;
         __syncthreads();
         if (s_abort) break;
     }
-    if (!ok || s_abort) {
-        // wind down: wait (bounded) for this warp's copy still in flight, then leave
-        if (gemv_warp && g < total) mbar_wait(&mbar[warp], parity, p.status, 2u);
+    if (s_abort) {
+        // wind down: wait (bounded) for this warp's copies still in flight, then leave
+        if (gemv_warp) {
+            for (int i = it; i < it + 2; ++i)
+                if (warp + i * p.ngemv < total) mbar_wait(&mbar[2 * warp + (i & 1)], (i >> 1) & 1, p.status, 2u);
+        }
         return;
     }
     // ---------------------------------------------------------------- phase 4: attention
-    if (!grid_sync(p, 3, &s_abort)) return;
+    if (!grid_sync(p, 3, base, &s_abort)) return;
     {
-        const int G = d.nh / d.nkv, hd = VPL * 32;
+        const int G = d.nh / d.nkv, hd = VPL * 32, half = hd / 2;
         float rinv = 1.f, c = 0.f;
         const bool sub = d.flags & TLB_SUB_NORM;
         if (sub) coef(sum_pp(p.pp + 2 * p.nblocks, p.nblocks, red), d.qd, d.eps, rinv, c);
         if (blockIdx.x == 0)
             for (int i = threadIdx.x; i < d.H; i += blockDim.x) d.d_hidden[i] = __ldcg(d.dR1 + i);
-        float *sC = reinterpret_cast<float *>(smem);            // [G][hd]
-        float *sR = sC + G * hd;                                // [kPW][G][2][hd]
+        float *sC = reinterpret_cast<float *>(smem);            // [G][hd] dCtx
+        float *sR = sC + G * hd;                                // [kPW][G][2][hd] per-warp U, W
+        float *sUW = sR + kPW * G * 2 * hd;                     // [G][2][hd] chunk U, W (rotated in place)
+        float *sB = sUW + G * 2 * hd;                           // [G * hd][rank] rows of B_q
         __shared__ float sDp[kPW][GM];
         const int nitems = d.nkv * p.achunks;
-        for (int it = blockIdx.x; it < nitems; it += p.nblocks) {
-            const int kvh = it / p.achunks, chunk = it % p.achunks;
+        for (int item = blockIdx.x; item < nitems; item += p.nblocks) {
+            const int kvh = item / p.achunks, chunk = item % p.achunks;
             __syncthreads();
             for (int i = threadIdx.x; i < G * hd; i += blockDim.x) {
                 const int q = kvh * G * hd + i;
                 const float ds = __ldcg(d.dSub + q);
                 sC[i] = sub ? rinv * (ds * d.g_sub_attn[q] - d.ctx[q] * c) : ds;
             }
+            for (int i = threadIdx.x; i < G * hd * d.rank; i += blockDim.x)
+                sB[i] = d.lq.b[int64_t(kvh) * G * hd * d.rank + i];
             __syncthreads();
             const int d0 = lane * VPL;
             float U[GM][VPL], W[GM][VPL], dsum[GM];
@@ -415,18 +479,42 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
                 if (lane == 0) sDp[warp][gg] = dsum[gg];
             }
             __syncthreads();
+            // chunk sums over the warps: U, W, D accumulate over chunks in global memory
             for (int i = threadIdx.x; i < G * 2 * hd; i += blockDim.x) {
                 float t = 0.f;
 #pragma unroll
                 for (int w = 0; w < kPW; ++w) t += sR[w * G * 2 * hd + i];
+                sUW[i] = t;
                 const int gg = i / (2 * hd), which = (i / hd) & 1, dd = i % hd;
-                float *dst = which ? d.Wpart : d.Upart;
-                dst[(int64_t(chunk) * d.nh + kvh * G + gg) * hd + dd] = t;
+                atomicAdd((which ? p.Wacc : p.Uacc) + (kvh * G + gg) * hd + dd, t);
             }
             if (threadIdx.x < G) {
                 float t = 0.f;
                 for (int w = 0; w < kPW; ++w) t += sDp[w][threadIdx.x];
-                d.Dpart[int64_t(chunk) * d.nh + kvh * G + threadIdx.x] = t;
+                atomicAdd(p.Dacc + kvh * G + threadIdx.x, t);
+            }
+            __syncthreads();
+            // rotate the chunk's U and W (RoPE backward is linear) ...
+            if (d.flags & TLB_ROPE) {
+                for (int i = threadIdx.x; i < G * 2 * half; i += blockDim.x) {
+                    const int vec = i / half, dd = i % half;            // vec = gg * 2 + which
+                    float cs, sn;
+                    rope_cos_sin(float(d.pos), p.fr.hi[dd], p.fr.lo[dd], cs, sn);
+                    float *v = sUW + vec * hd;
+                    const float y1 = v[dd], y2 = v[dd + half];
+                    v[dd] = y1 * cs + y2 * sn;
+                    v[dd + half] = -y1 * sn + y2 * cs;
+                }
+                __syncthreads();
+            }
+            // ... and project on B_q: ug[h, r] += sum_d R(U)[d] B_q[h*hd + d, r]  (same for W)
+            for (int i = threadIdx.x; i < G * 2 * d.rank; i += blockDim.x) {
+                const int gg = i / (2 * d.rank), which = (i / d.rank) & 1, r = i % d.rank;
+                const float *v = sUW + (gg * 2 + which) * hd;
+                const float *b = sB + gg * hd * d.rank + r;
+                float t = 0.f;
+                for (int dd = 0; dd < hd; ++dd) t = fmaf(v[dd], b[dd * d.rank], t);
+                atomicAdd((which ? p.wg : p.ug) + (kvh * G + gg) * d.rank + r, t);
             }
             // dV of the current token and its share of gh_v
             if (d.pos / kKeysPerItem == chunk) {
@@ -463,91 +551,40 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
             }
         }
     }
-    // ---------------------------------------------------------------- phase 5: dQpre, gh_q
-    if (!grid_sync(p, 4, &s_abort)) return;
-    for (int h = blockIdx.x; h < d.nh; h += p.nblocks) {
-        const int hd = VPL * 32;
-        float *su = reinterpret_cast<float *>(smem);           // [groups][hd] partial U
-        float *sw = su + kPT;                                   // [groups][hd] partial W
-        float *sq = sw + kPT;                                   // [hd]
-        __shared__ float sD;
-        __shared__ float red16[16][kPW];
-        const int groups = kPT / hd;
-        const int grp = threadIdx.x / hd, dd = threadIdx.x % hd;
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            float t = 0.f;
-            for (int c = lane; c < p.achunks; c += 32) t += __ldcg(d.Dpart + int64_t(c) * d.nh + h);
-            t = warp_sum(t);
-            if (lane == 0) sD = t;
-        }
-        {
-            float u = 0.f, w = 0.f;
-            for (int c = grp; c < p.achunks; c += groups) {
-                const int64_t idx = (int64_t(c) * d.nh + h) * hd + dd;
-                u += __ldcg(d.Upart + idx);
-                w += __ldcg(d.Wpart + idx);
-            }
-            su[threadIdx.x] = u;
-            sw[threadIdx.x] = w;
-        }
-        __syncthreads();
-        for (int t = threadIdx.x; t < hd; t += blockDim.x) {
-            float u = 0.f, w = 0.f;
-            for (int q = 0; q < groups; ++q) {
-                u += su[q * hd + t];
-                w += sw[q * hd + t];
-            }
-            sq[t] = d.scale * (u - sD * w);
-        }
-        __syncthreads();
-        const int half = hd >> 1;
-        for (int t = threadIdx.x; t < half; t += blockDim.x) {
-            float y1 = sq[t], y2 = sq[t + half];
-            if (d.flags & TLB_ROPE) {
-                float cs, sn;
-                rope_cos_sin(float(d.pos), p.fr.hi[t], p.fr.lo[t], cs, sn);
-                const float t1 = y1 * cs + y2 * sn, t2 = -y1 * sn + y2 * cs;
-                y1 = t1;
-                y2 = t2;
-            }
-            d.dqpre[h * hd + t] = y1;
-            d.dqpre[h * hd + t + half] = y2;
-            sq[t] = y1;
-            sq[t + half] = y2;
-        }
-        __syncthreads();
-        float ar[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) ar[r] = 0.f;
-        for (int t = threadIdx.x; t < hd; t += blockDim.x) {
-            const float *br = d.lq.b + int64_t(h * hd + t) * d.rank;
-#pragma unroll
-            for (int r = 0; r < 16; ++r)
-                if (r < d.rank) ar[r] = fmaf(sq[t], br[r], ar[r]);
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const float t = warp_sum(ar[r]);
-            if (lane == 0) red16[r][warp] = t;
-        }
-        __syncthreads();
-        if (threadIdx.x < d.rank) {
-            float t = 0.f;
-            for (int w = 0; w < kPW; ++w) t += red16[threadIdx.x][w];
-            atomicAdd(d.gh + threadIdx.x, d.lora_scaling * t);
-        }
-    }
-    // ---------------------------------------------------------------- phase 6: LoRA + AdamW
-    if (!grid_sync(p, 5, &s_abort)) return;
+    // ---------------------------------------------------------------- phase 5: dQpre, LoRA + AdamW
+    if (!grid_sync(p, 4, base, &s_abort)) return;
     {
+        const int hd = VPL * 32, half = hd / 2;
+        __shared__ float ghq[16], ghv[16];
+        if (threadIdx.x < d.rank) {
+            // gh_q = s scale sum_h (ug_h - D_h wg_h)   (B_q before its update)
+            float t = 0.f;
+            for (int h = 0; h < d.nh; ++h)
+                t += __ldcg(p.ug + h * d.rank + threadIdx.x) - __ldcg(p.Dacc + h) * __ldcg(p.wg + h * d.rank + threadIdx.x);
+            ghq[threadIdx.x] = d.lora_scaling * d.scale * t;
+            ghv[threadIdx.x] = __ldcg(d.gh + d.rank + threadIdx.x);
+        }
+        __syncthreads();
         const int64_t nbq = int64_t(d.qd) * d.rank, nbv = int64_t(d.kvd) * d.rank, na = int64_t(d.rank) * d.H;
         const int64_t n = nbq + nbv + 2 * na;
         float sa = 0.f, sb = 0.f;
         for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += int64_t(p.nblocks) * blockDim.x) {
             if (e < nbq) {
                 const int o = int(e / d.rank), r = int(e % d.rank);
-                const float gq = d.lora_scaling * __ldcg(d.dqpre + o) * d.hq[r];
+                // dQpre[o] = R(-theta) scale (U - D W) at row o
+                const int h = o / hd, dd = o % hd, pd = dd < half ? dd : dd - half;
+                const float Dh = __ldcg(p.Dacc + h);
+                const int o1 = h * hd + pd, o2 = o1 + half;
+                const float y1 = d.scale * (__ldcg(p.Uacc + o1) - Dh * __ldcg(p.Wacc + o1));
+                const float y2 = d.scale * (__ldcg(p.Uacc + o2) - Dh * __ldcg(p.Wacc + o2));
+                float q = dd < half ? y1 : y2;
+                if (d.flags & TLB_ROPE) {
+                    float cs, sn;
+                    rope_cos_sin(float(d.pos), p.fr.hi[pd], p.fr.lo[pd], cs, sn);
+                    q = dd < half ? y1 * cs + y2 * sn : -y1 * sn + y2 * cs;
+                }
+                if (r == 0) d.dqpre[o] = q;
+                const float gq = d.lora_scaling * q * d.hq[r];
                 if (d.lq.grad_b) d.lq.grad_b[e] = gq;
                 float mm = d.lq.m_b[e], vv = d.lq.v_b[e];
                 d.lq.b[e] = adam_elem(d.lq.b[e], gq, mm, vv, d.kb);
@@ -570,7 +607,7 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
                 const int64_t f2 = isq ? f : f - na;
                 const int r = int(f2 / d.H), cidx = int(f2 % d.H);
                 const tlb_lora &l = isq ? d.lq : d.lv;
-                const float ga = __ldcg(d.gh + (isq ? 0 : d.rank) + r) * d.x[cidx];
+                const float ga = (isq ? ghq[r] : ghv[r]) * d.x[cidx];
                 if (l.grad_a) l.grad_a[f2] = ga;
                 float mm = l.m_a[f2], vv = l.v_a[f2];
                 l.a[f2] = adam_elem(l.a[f2], ga, mm, vv, d.ka);
@@ -621,27 +658,35 @@ int launch_vpl(const PArgs &p, size_t dyn, cudaStream_t st) {
 }
 
 struct Geometry {
-    int slot_bytes, xbytes, nslots, rpi1, rpi3;
+    int slot_bytes, xbytes, ngemv, rpi, nsplit;
     size_t dyn;
 };
 
 bool geometry(const tlb_layer_cfg &c, Geometry &g) {
     const int es = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 2 : 1);
+    const int E = 16 / es;
     const int hd = c.head_dim, G = c.n_heads / c.n_kv_heads;
     const int64_t rowH = int64_t(c.dim) * es, rowI = int64_t(c.ffn_dim) * es;
-    g.slot_bytes = int(std::max<int64_t>(2 * rowI, rowH));
-    g.rpi1 = g.rpi3 = int(std::min<int64_t>(kMaxRowsPerItem, g.slot_bytes / rowH));
+    // phase-2 items: the two weights' rows cut into nsplit column ranges of whole chunks,
+    // so that an item stays near 8 KiB
+    g.nsplit = 1;
+    for (int n = 1; n <= 8; ++n) {
+        if (c.ffn_dim % (n * E)) continue;
+        g.nsplit = n;
+        if (2 * rowI / n <= 8192) break;
+    }
+    g.slot_bytes = int(std::max<int64_t>(2 * rowI / g.nsplit, rowH));
+    g.rpi = int(std::min<int64_t>(kMaxRowsPerItem, g.slot_bytes / rowH));
     g.xbytes = int(((std::max<int64_t>(c.dim, 2 * int64_t(c.ffn_dim)) * 4) + 127) / 128 * 128);
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return false;
     const int64_t budget = int64_t(optin) - 8 * 1024;     // static shared memory and slack
-    g.nslots = int(std::min<int64_t>(kPW, (budget - g.xbytes) / g.slot_bytes));
-    if (g.nslots < 4) return false;
-    const size_t attn = size_t(33) * G * hd * 4;
-    const size_t fin = size_t(2 * kPT + 256) * 4;
-    g.dyn = std::max({size_t(g.xbytes) + size_t(g.nslots) * g.slot_bytes, attn, fin});
+    g.ngemv = int(std::min<int64_t>(kPW, (budget - g.xbytes) / (2 * int64_t(g.slot_bytes))));
+    if (g.ngemv < 4) return false;
+    const size_t attn = (size_t(G) * hd * (1 + 2 * kPW + 2) + size_t(G) * hd * c.rank) * 4;
+    g.dyn = std::max(size_t(g.xbytes) + size_t(2 * g.ngemv) * g.slot_bytes, attn);
     return int64_t(g.dyn) <= budget;
 }
 
@@ -650,28 +695,36 @@ bool geometry(const tlb_layer_cfg &c, Geometry &g) {
 bool persistent_supported(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     const int hd = c.head_dim, G = c.n_heads / c.n_kv_heads;
     const int E = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 8 : 16);
-    if (S != 1 || L < 1 || c.rank > 16) return false;
+    if (S != 1 || L < 1 || c.rank > 16 || c.n_heads > kPT) return false;
     if (!(hd == 32 || hd == 64 || hd == 128 || hd == 256) || G * (hd / 32) > 16) return false;
     if (c.dim % E || c.ffn_dim % E || c.dim % 4 || c.ffn_dim % 4) return false;
+    if (ceil_div(c.dim, std::min(num_sms(), kMaxPersistentBlocks)) + 1 > kMaxBlockRows) return false;
     Geometry g;
     return geometry(c, g);
 }
 
 int decode_persistent_launch(const DecodeArgs &d, const tlb_layer_cfg &c, int64_t L, void *ws, size_t off_gbar,
-                             size_t off_pp, cudaStream_t st) {
+                             size_t off_pp, size_t off_acc, cudaStream_t st) {
     Geometry g;
     TLB_REQUIRE(geometry(c, g), TLB_EUNSUPPORTED, "decode: no persistent geometry");
     PArgs p;
     p.d = d;
     p.status = ws_at<uint32_t>(ws, 0);
-    p.gbar = ws_at<unsigned>(ws, off_gbar);
+    p.gbar = ws_at<unsigned long long>(ws, off_gbar);
     p.pp = ws_at<float2>(ws, off_pp);
+    const int qd = c.n_heads * c.head_dim;
+    float *acc = ws_at<float>(ws, off_acc);
+    p.Uacc = acc;
+    p.Wacc = acc + qd;
+    p.Dacc = acc + 2 * qd;
+    p.ug = p.Dacc + c.n_heads;
+    p.wg = p.ug + c.n_heads * c.rank;
     p.nblocks = std::min(num_sms(), kMaxPersistentBlocks);
-    p.nslots = g.nslots;
+    p.ngemv = g.ngemv;
     p.slot_bytes = g.slot_bytes;
     p.xbytes = g.xbytes;
-    p.rpi1 = g.rpi1;
-    p.rpi3 = g.rpi3;
+    p.rpi = g.rpi;
+    p.nsplit = g.nsplit;
     p.achunks = int(ceil_div(L, kKeysPerItem));
     rope_freqs(p.fr, c.head_dim, c.rope_base);
     switch (c.wtype) {
