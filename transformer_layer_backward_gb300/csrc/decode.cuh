@@ -80,15 +80,11 @@ bool decode_supported(const tlb_layer_cfg &c, int64_t S, int64_t L);
 
 // Persistent single-kernel version (decode_persistent.cu).  Its workspace needs, besides
 // the DecodeArgs regions, a zero-initialised grid-barrier word pair (off_gbar) and
-// 3 * kMaxPersistentBlocks float2 partial sums (off_pp) and the accumulators (off_acc).
+// 3 * kMaxPersistentBlocks float2 partial sums (off_pp).
 constexpr int kMaxPersistentBlocks = 1024;
 bool persistent_supported(const tlb_layer_cfg &c, int64_t S, int64_t L);
 int decode_persistent_launch(const DecodeArgs &d, const tlb_layer_cfg &c, int64_t L, void *ws, size_t off_gbar,
-                             size_t off_pp, size_t off_acc, cudaStream_t st);
-// floats of the accumulator region: 2 q_dim + n_heads + 2 n_heads rank
-inline int64_t persistent_acc_floats(const tlb_layer_cfg &c) {
-    return 2 * int64_t(c.n_heads) * c.head_dim + c.n_heads + 2 * int64_t(c.n_heads) * c.rank;
-}
+                             size_t off_pp, cudaStream_t st);
 int decode_rows_per_block();
 int decode_layer_launch(const DecodeArgs &a, int wtype, cudaStream_t st);
 

@@ -15,15 +15,18 @@
 //
 //   phase 1  dF   = s_d W_down dOut                      (+ partial sums for the sub-norm)
 //   phase 2  dG, dU (sub-norm RMSNorm bwd + gated-activation bwd, per block), then
-//            dN2  = s_g W_gate dG + s_u W_up dU           (rows split in column ranges)
+//            dN2  = s_g W_gate dG + s_u W_up dU   (items: two rows x one column range)
 //   phase 3  dR1  = dOut + RMSNorm_bwd(r1, g_ffn, dN2), then dSub = s_o W_O dR1
-//   phase 4  per (KV head, 32 keys): dCtx (sub-norm bwd), one pass over K and V:
-//            dA = dCtx_h . V[j], U += P dA K[j], W += P K[j], D += P dA  (per head),
-//            so that dQ_h = scale (U_h - D_h W_h) over all chunks; the chunk's
-//            RoPE-rotated U and W are also projected on B_q (gh_q is linear in dQ);
-//            the chunk holding the current position forms dV and gh_v
-//   phase 5  dQpre = R(-theta) scale (U - D W); dB = s G h^T, dA = gh x^T for both
-//            adapters, AdamW with LoRA+ on B
+//   phase 4  per (KV head, 64 keys): dCtx (sub-norm bwd), one pass over K and V:
+//            dA = dCtx_h . V[j], U += P dA K[j], W += P K[j], D += P dA per head, so
+//            that dQ_h = scale (U_h - D_h W_h) summed over chunks; the chunk holding the
+//            current position also forms dV and gh_v
+//   phase 5  per head: dQ from the chunk sums, RoPE backward -> dQpre, gh_q
+//   phase 6  dB = s G h^T, dA = gh x^T for both adapters, AdamW with LoRA+ on B
+//
+// Every item of the GEMV phases uses each loaded vector chunk for several weight rows
+// (shared-memory bandwidth, not HBM, would otherwise bound the decode), and the dot
+// products run on packed f32x2 FMAs with independent accumulators.
 //
 // Grid barriers count on one monotonic 64-bit word of the workspace (release-add to
 // arrive, acquire-load to wait).  Waits are bounded: a timed-out mbarrier or barrier
@@ -44,20 +47,19 @@ namespace {
 constexpr int kPW = 16;                 // warps per block
 constexpr int kPT = kPW * 32;
 constexpr int kMaxRowsPerItem = 8;
-constexpr int kKeysPerItem = 32;        // attention keys per (KV head, chunk) item
-constexpr int kBarriers = 4;            // grid barriers per call
+constexpr int kKeysPerItem = 64;        // attention keys per (KV head, chunk) item
+constexpr int kBarriers = 5;            // grid barriers per call
 constexpr int kMaxBlockRows = 256;      // phase-2 rows per block held in shared memory
+constexpr int kSlotsPerWarp = 1;        // shared-memory slots (items in flight) per GEMV warp
 
 struct PArgs {
     DecodeArgs d;
     uint32_t *status;                   // workspace status block
     unsigned long long *gbar;           // grid barrier: monotonic arrival count
     float2 *pp;                         // per-block partial sums, 3 x nblocks
-    float *Uacc, *Wacc, *Dacc;          // [q_dim], [q_dim], [n_heads]  (zeroed in the call)
-    float *ug, *wg;                     // [n_heads, rank] projections of R(U), R(W) on B_q
     int nblocks, ngemv, slot_bytes, xbytes;
     int rpi;                            // rows per item in phases 1 and 3
-    int nsplit;                         // column ranges per phase-2 row
+    int nsplit;                         // column ranges of a phase-2 row pair
     int achunks;                        // ceil(L / kKeysPerItem)
     RopeFreqs fr;
 };
@@ -112,7 +114,7 @@ __device__ __forceinline__ ItemMap item_map(const PArgs &p) {
     block_rows(p.d.H, blockIdx.x, p.nblocks, m.b0, m.b1);
     block_rows(p.d.qd, blockIdx.x, p.nblocks, m.c0, m.c1);
     m.n1 = (m.a1 - m.a0 + p.rpi - 1) / p.rpi;
-    m.n2 = (m.b1 - m.b0) * p.nsplit;
+    m.n2 = ((m.b1 - m.b0 + 1) / 2) * p.nsplit;
     m.n3 = (m.c1 - m.c0 + p.rpi - 1) / p.rpi;
     return m;
 }
@@ -130,13 +132,19 @@ __device__ __forceinline__ void issue_item(const PArgs &p, const ItemMap &m, int
         mbar_arrive_expect_tx(bar, rb * k);
         tma_load_1d(slot, static_cast<const char *>(d.w_down) + size_t(r0) * rb, rb * k, bar);
     } else if (g < m.n1 + m.n2) {
+        // rows h, h + 1 (k2 of them) of W_gate then of W_up, column range q of each:
+        // slot = [W_gate row h | W_gate row h+1 | W_up row h | W_up row h+1]
         const int j = g - m.n1;
-        const int h = m.b0 + j / p.nsplit, q = j % p.nsplit;
+        const int h = m.b0 + 2 * (j / p.nsplit), q = j % p.nsplit;
+        const int k2 = min(2, m.b1 - h);
         const uint32_t rb = uint32_t(d.I) * ES;            // full row bytes
         const uint32_t pb = rb / p.nsplit;                  // bytes of one column range
-        mbar_arrive_expect_tx(bar, 2 * pb);
-        tma_load_1d(slot, static_cast<const char *>(d.w_gate) + size_t(h) * rb + size_t(q) * pb, pb, bar);
-        tma_load_1d(slot + pb, static_cast<const char *>(d.w_up) + size_t(h) * rb + size_t(q) * pb, pb, bar);
+        mbar_arrive_expect_tx(bar, 2 * k2 * pb);
+        for (int r = 0; r < k2; ++r) {
+            const size_t off = size_t(h + r) * rb + size_t(q) * pb;
+            tma_load_1d(slot + r * pb, static_cast<const char *>(d.w_gate) + off, pb, bar);
+            tma_load_1d(slot + (2 + r) * pb, static_cast<const char *>(d.w_up) + off, pb, bar);
+        }
     } else {
         const int r0 = m.c0 + (g - m.n1 - m.n2) * p.rpi;
         const int k = min(p.rpi, m.c1 - r0);
@@ -146,34 +154,74 @@ __device__ __forceinline__ void issue_item(const PArgs &p, const ItemMap &m, int
     }
 }
 
-// One warp: k rows of `cols` weights in shared memory (row stride rb bytes), starting at
-// chunk ch0 of the full vector, dotted with the swizzled vector x; the k sums (times
-// scale) go to every lane.
+__device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float f2sum(unsigned long long v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo + hi;
+}
+__device__ __forceinline__ unsigned long long f2fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2add(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Weight pair j (elements 2j, 2j+1) of a 16-byte chunk, as packed floats.
 template <int WT>
-__device__ __forceinline__ void dot_rows(const char *slot, int k, int cols, uint32_t rb, int ch0, const float *x,
+__device__ __forceinline__ unsigned long long wpair(uint4 w, int j) {
+    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+    if constexpr (WT == TLB_W_F32) {
+        return f2pack(__uint_as_float(q[2 * j]), __uint_as_float(q[2 * j + 1]));
+    } else if constexpr (WT == TLB_W_BF16) {
+        return f2pack(bf16_lo(q[j]), bf16_hi(q[j]));
+    } else {
+        // int8 -> float: byte biased into the mantissa of 2^23, then 2^23 + 128 removed (exact)
+        const uint32_t u = q[j >> 1] ^ 0x80808080u;
+        const uint32_t s0 = (j & 1) ? 0x7652u : 0x7650u, s1 = (j & 1) ? 0x7653u : 0x7651u;
+        const unsigned long long raw = f2pack(__uint_as_float(__byte_perm(u, 0x4B000000u, s0)),
+                                              __uint_as_float(__byte_perm(u, 0x4B000000u, s1)));
+        return f2add(raw, 0xCB000080CB000080ull);   // (-8388736, -8388736)
+    }
+}
+
+// One warp: k (<= R) rows of nch 16-byte chunks in shared memory (row stride rb bytes),
+// starting at chunk ch0 of the full vector, dotted with the swizzled vector x; the k
+// sums (times scale) go to every lane.  Each vector chunk is read once for all rows.
+template <int WT, int R>
+__device__ __forceinline__ void dot_rows(const char *slot, int k, int nch, uint32_t rb, int ch0, const float *x,
                                          float scale, float *out) {
     constexpr int E = EPC<WT>::v, P = E / 4;
     const int lane = threadIdx.x & 31;
-    const int nch = cols / E;
-    float acc[kMaxRowsPerItem];
+    unsigned long long acc[R][2];
 #pragma unroll
-    for (int r = 0; r < kMaxRowsPerItem; ++r) acc[r] = 0.f;
+    for (int r = 0; r < R; ++r) acc[r][0] = acc[r][1] = 0ull;
     for (int c = lane; c < nch; c += 32) {
-        float xv[E];
+        ulonglong2 xv[P];
 #pragma unroll
-        for (int q = 0; q < P; ++q) {
-            const float4 t = reinterpret_cast<const float4 *>(x)[xunit<WT>((ch0 + c) * P + q)];
-            xv[4 * q] = t.x;
-            xv[4 * q + 1] = t.y;
-            xv[4 * q + 2] = t.z;
-            xv[4 * q + 3] = t.w;
+        for (int q = 0; q < P; ++q) xv[q] = reinterpret_cast<const ulonglong2 *>(x)[xunit<WT>((ch0 + c) * P + q)];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (r < k) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(slot + r * rb + c * 16);
+#pragma unroll
+                for (int j = 0; j < E / 2; ++j) {
+                    const unsigned long long xp = (j & 1) ? xv[j >> 1].y : xv[j >> 1].x;
+                    acc[r][j & 1] = f2fma(wpair<WT>(w, j), xp, acc[r][j & 1]);
+                }
+            }
         }
-#pragma unroll
-        for (int r = 0; r < kMaxRowsPerItem; ++r)
-            if (r < k) acc[r] += chunk_dot<WT>(*reinterpret_cast<const uint4 *>(slot + r * rb + c * 16), xv);
     }
 #pragma unroll
-    for (int r = 0; r < kMaxRowsPerItem; ++r) out[r] = scale * warp_sum(acc[r]);
+    for (int r = 0; r < R; ++r) out[r] = scale * warp_sum(f2sum(acc[r][0]) + f2sum(acc[r][1]));
 }
 
 // Sum of nb partials (every thread gets it).
@@ -198,7 +246,7 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
     constexpr int GM = 16 / VPL;                 // heads per KV group held in registers
     constexpr int ES = 16 / EPC<WT>::v;
     extern __shared__ float4 smem4[];
-    __shared__ uint64_t mbar[2 * kPW];
+    __shared__ uint64_t mbar[kSlotsPerWarp * kPW];
     __shared__ float2 red[32];
     __shared__ int s_abort;
     __shared__ unsigned long long s_base;
@@ -217,30 +265,23 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
         const unsigned long long per_call = (unsigned long long)kBarriers * p.nblocks;
         s_base = v - v % per_call;
     }
-    if (lane == 0 && gemv_warp) {
-        mbar_init(&mbar[2 * warp], 1);
-        mbar_init(&mbar[2 * warp + 1], 1);
-    }
+    if (lane == 0 && gemv_warp)
+        for (int i = 0; i < kSlotsPerWarp; ++i) mbar_init(&mbar[kSlotsPerWarp * warp + i], 1);
     fence_mbar_init();
     __syncthreads();
     const unsigned long long base = s_base;
 
     const ItemMap m = item_map(p);
     const int total = m.n1 + m.n2 + m.n3;
-    // the first two items of each GEMV warp: the weights start streaming right away
+    // the first items of each GEMV warp: the weights start streaming right away
     if (gemv_warp && lane == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kSlotsPerWarp; ++i) {
             const int g = warp + i * p.ngemv;
-            if (g < total) issue_item<WT>(p, m, g, slots + size_t(2 * warp + i) * p.slot_bytes, &mbar[2 * warp + i]);
+            const int sidx = kSlotsPerWarp * warp + i;
+            if (g < total) issue_item<WT>(p, m, g, slots + size_t(sidx) * p.slot_bytes, &mbar[sidx]);
         }
     }
-    // accumulators of this call (read only after later barriers)
-    if (blockIdx.x == 0) {
-        for (int i = threadIdx.x; i < d.qd; i += blockDim.x) p.Uacc[i] = p.Wacc[i] = 0.f;
-        for (int i = threadIdx.x; i < d.nh * d.rank; i += blockDim.x) p.ug[i] = p.wg[i] = 0.f;
-        if (threadIdx.x < d.nh) p.Dacc[threadIdx.x] = 0.f;
-        if (threadIdx.x < 2 * d.rank) d.gh[threadIdx.x] = 0.f;
-    }
+    if (blockIdx.x == 0 && threadIdx.x < 2 * d.rank) d.gh[threadIdx.x] = 0.f;   // gh_q | gh_v accumulators
     // phase 1 vector: dOut
     {
         const float4 *x4 = reinterpret_cast<const float4 *>(d.d_hidden);
@@ -318,35 +359,39 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
         float2 acc = make_float2(0.f, 0.f);     // (sum y g z, sum z^2) of phases 1 and 3, lane 0
         if (gemv_warp) {
             for (int g = warp + it * p.ngemv; g < gend; g = warp + it * p.ngemv) {
-                const int sidx = 2 * warp + (it & 1);
+                const int sidx = kSlotsPerWarp * warp + (it % kSlotsPerWarp);
                 char *slot = slots + size_t(sidx) * p.slot_bytes;
-                if (!mbar_wait(&mbar[sidx], (it >> 1) & 1, p.status, 1u)) { ok = false; break; }
+                if (!mbar_wait(&mbar[sidx], (it / kSlotsPerWarp) & 1, p.status, 1u)) { ok = false; break; }
                 float out[kMaxRowsPerItem];
                 int row0 = 0, k = 0;
                 if (phase == 2) {
                     const int j = g - m.n1;
-                    row0 = m.b0 + j / p.nsplit;
+                    row0 = m.b0 + 2 * (j / p.nsplit);
+                    k = min(2, m.b1 - row0);
                     const int q = j % p.nsplit;
                     const int cols = d.I / p.nsplit;
                     const uint32_t pb = uint32_t(cols) * ES;
-                    const int ch0 = q * (cols / EPC<WT>::v);
-                    float o2[kMaxRowsPerItem];
-                    dot_rows<WT>(slot, 1, cols, pb, ch0, sX, d.s_gate, out);
-                    dot_rows<WT>(slot + pb, 1, cols, pb, ch0, sX + d.I, d.s_up, o2);
+                    const int nch = cols / EPC<WT>::v;
+                    float o2[2];
+                    dot_rows<WT, 2>(slot, k, nch, pb, q * nch, sX, d.s_gate, out);
+                    dot_rows<WT, 2>(slot + 2 * pb, k, nch, pb, q * nch, sX + d.I, d.s_up, o2);
                     out[0] += o2[0];
+                    out[1] += o2[1];
                 } else {
                     const int base_r = phase == 1 ? m.a0 : m.c0;
                     const int lim = phase == 1 ? m.a1 : m.c1;
                     row0 = base_r + (g - gbeg) * p.rpi;
                     k = min(p.rpi, lim - row0);
-                    dot_rows<WT>(slot, k, d.H, uint32_t(d.H) * ES, 0, sX, phase == 1 ? d.s_down : d.s_o, out);
+                    dot_rows<WT, kMaxRowsPerItem>(slot, k, d.H / EPC<WT>::v, uint32_t(d.H) * ES, 0, sX,
+                                                  phase == 1 ? d.s_down : d.s_o, out);
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    const int gn = g + 2 * p.ngemv;
+                    const int gn = g + kSlotsPerWarp * p.ngemv;
                     if (gn < total) issue_item<WT>(p, m, gn, slot, &mbar[sidx]);
                     if (phase == 2) {
                         atomicAdd(&racc[row0 - m.b0], out[0]);
+                        if (k > 1) atomicAdd(&racc[row0 + 1 - m.b0], out[1]);
                     } else {
                         float *y = phase == 1 ? d.dF : d.dSub;
                         const float *gam = phase == 1 ? d.g_sub_ffn : d.g_sub_attn;
@@ -398,36 +443,33 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
     if (s_abort) {
         // wind down: wait (bounded) for this warp's copies still in flight, then leave
         if (gemv_warp) {
-            for (int i = it; i < it + 2; ++i)
-                if (warp + i * p.ngemv < total) mbar_wait(&mbar[2 * warp + (i & 1)], (i >> 1) & 1, p.status, 2u);
+            for (int i = it; i < it + kSlotsPerWarp; ++i)
+                if (warp + i * p.ngemv < total)
+                    mbar_wait(&mbar[kSlotsPerWarp * warp + (i % kSlotsPerWarp)], (i / kSlotsPerWarp) & 1, p.status, 2u);
         }
         return;
     }
     // ---------------------------------------------------------------- phase 4: attention
     if (!grid_sync(p, 3, base, &s_abort)) return;
     {
-        const int G = d.nh / d.nkv, hd = VPL * 32, half = hd / 2;
+        const int G = d.nh / d.nkv, hd = VPL * 32;
         float rinv = 1.f, c = 0.f;
         const bool sub = d.flags & TLB_SUB_NORM;
         if (sub) coef(sum_pp(p.pp + 2 * p.nblocks, p.nblocks, red), d.qd, d.eps, rinv, c);
         if (blockIdx.x == 0)
             for (int i = threadIdx.x; i < d.H; i += blockDim.x) d.d_hidden[i] = __ldcg(d.dR1 + i);
-        float *sC = reinterpret_cast<float *>(smem);            // [G][hd] dCtx
-        float *sR = sC + G * hd;                                // [kPW][G][2][hd] per-warp U, W
-        float *sUW = sR + kPW * G * 2 * hd;                     // [G][2][hd] chunk U, W (rotated in place)
-        float *sB = sUW + G * 2 * hd;                           // [G * hd][rank] rows of B_q
+        float *sC = reinterpret_cast<float *>(smem);            // [G][hd]
+        float *sR = sC + G * hd;                                // [kPW][G][2][hd]
         __shared__ float sDp[kPW][GM];
         const int nitems = d.nkv * p.achunks;
-        for (int item = blockIdx.x; item < nitems; item += p.nblocks) {
-            const int kvh = item / p.achunks, chunk = item % p.achunks;
+        for (int it = blockIdx.x; it < nitems; it += p.nblocks) {
+            const int kvh = it / p.achunks, chunk = it % p.achunks;
             __syncthreads();
             for (int i = threadIdx.x; i < G * hd; i += blockDim.x) {
                 const int q = kvh * G * hd + i;
                 const float ds = __ldcg(d.dSub + q);
                 sC[i] = sub ? rinv * (ds * d.g_sub_attn[q] - d.ctx[q] * c) : ds;
             }
-            for (int i = threadIdx.x; i < G * hd * d.rank; i += blockDim.x)
-                sB[i] = d.lq.b[int64_t(kvh) * G * hd * d.rank + i];
             __syncthreads();
             const int d0 = lane * VPL;
             float U[GM][VPL], W[GM][VPL], dsum[GM];
@@ -479,42 +521,18 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
                 if (lane == 0) sDp[warp][gg] = dsum[gg];
             }
             __syncthreads();
-            // chunk sums over the warps: U, W, D accumulate over chunks in global memory
             for (int i = threadIdx.x; i < G * 2 * hd; i += blockDim.x) {
                 float t = 0.f;
 #pragma unroll
                 for (int w = 0; w < kPW; ++w) t += sR[w * G * 2 * hd + i];
-                sUW[i] = t;
                 const int gg = i / (2 * hd), which = (i / hd) & 1, dd = i % hd;
-                atomicAdd((which ? p.Wacc : p.Uacc) + (kvh * G + gg) * hd + dd, t);
+                float *dst = which ? d.Wpart : d.Upart;
+                dst[(int64_t(chunk) * d.nh + kvh * G + gg) * hd + dd] = t;
             }
             if (threadIdx.x < G) {
                 float t = 0.f;
                 for (int w = 0; w < kPW; ++w) t += sDp[w][threadIdx.x];
-                atomicAdd(p.Dacc + kvh * G + threadIdx.x, t);
-            }
-            __syncthreads();
-            // rotate the chunk's U and W (RoPE backward is linear) ...
-            if (d.flags & TLB_ROPE) {
-                for (int i = threadIdx.x; i < G * 2 * half; i += blockDim.x) {
-                    const int vec = i / half, dd = i % half;            // vec = gg * 2 + which
-                    float cs, sn;
-                    rope_cos_sin(float(d.pos), p.fr.hi[dd], p.fr.lo[dd], cs, sn);
-                    float *v = sUW + vec * hd;
-                    const float y1 = v[dd], y2 = v[dd + half];
-                    v[dd] = y1 * cs + y2 * sn;
-                    v[dd + half] = -y1 * sn + y2 * cs;
-                }
-                __syncthreads();
-            }
-            // ... and project on B_q: ug[h, r] += sum_d R(U)[d] B_q[h*hd + d, r]  (same for W)
-            for (int i = threadIdx.x; i < G * 2 * d.rank; i += blockDim.x) {
-                const int gg = i / (2 * d.rank), which = (i / d.rank) & 1, r = i % d.rank;
-                const float *v = sUW + (gg * 2 + which) * hd;
-                const float *b = sB + gg * hd * d.rank + r;
-                float t = 0.f;
-                for (int dd = 0; dd < hd; ++dd) t = fmaf(v[dd], b[dd * d.rank], t);
-                atomicAdd((which ? p.wg : p.ug) + (kvh * G + gg) * d.rank + r, t);
+                d.Dpart[int64_t(chunk) * d.nh + kvh * G + threadIdx.x] = t;
             }
             // dV of the current token and its share of gh_v
             if (d.pos / kKeysPerItem == chunk) {
@@ -551,40 +569,91 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
             }
         }
     }
-    // ---------------------------------------------------------------- phase 5: dQpre, LoRA + AdamW
+    // ---------------------------------------------------------------- phase 5: dQpre, gh_q
     if (!grid_sync(p, 4, base, &s_abort)) return;
-    {
-        const int hd = VPL * 32, half = hd / 2;
-        __shared__ float ghq[16], ghv[16];
-        if (threadIdx.x < d.rank) {
-            // gh_q = s scale sum_h (ug_h - D_h wg_h)   (B_q before its update)
+    for (int h = blockIdx.x; h < d.nh; h += p.nblocks) {
+        const int hd = VPL * 32;
+        float *su = reinterpret_cast<float *>(smem);           // [groups][hd] partial U
+        float *sw = su + kPT;                                   // [groups][hd] partial W
+        float *sq = sw + kPT;                                   // [hd]
+        __shared__ float sD;
+        __shared__ float red16[16][kPW];
+        const int groups = kPT / hd;
+        const int grp = threadIdx.x / hd, dd = threadIdx.x % hd;
+        __syncthreads();
+        if (threadIdx.x < 32) {
             float t = 0.f;
-            for (int h = 0; h < d.nh; ++h)
-                t += __ldcg(p.ug + h * d.rank + threadIdx.x) - __ldcg(p.Dacc + h) * __ldcg(p.wg + h * d.rank + threadIdx.x);
-            ghq[threadIdx.x] = d.lora_scaling * d.scale * t;
-            ghv[threadIdx.x] = __ldcg(d.gh + d.rank + threadIdx.x);
+            for (int c = lane; c < p.achunks; c += 32) t += __ldcg(d.Dpart + int64_t(c) * d.nh + h);
+            t = warp_sum(t);
+            if (lane == 0) sD = t;
+        }
+        {
+            float u = 0.f, w = 0.f;
+            for (int c = grp; c < p.achunks; c += groups) {
+                const int64_t idx = (int64_t(c) * d.nh + h) * hd + dd;
+                u += __ldcg(d.Upart + idx);
+                w += __ldcg(d.Wpart + idx);
+            }
+            su[threadIdx.x] = u;
+            sw[threadIdx.x] = w;
         }
         __syncthreads();
+        for (int t = threadIdx.x; t < hd; t += blockDim.x) {
+            float u = 0.f, w = 0.f;
+            for (int q = 0; q < groups; ++q) {
+                u += su[q * hd + t];
+                w += sw[q * hd + t];
+            }
+            sq[t] = d.scale * (u - sD * w);
+        }
+        __syncthreads();
+        const int half = hd >> 1;
+        for (int t = threadIdx.x; t < half; t += blockDim.x) {
+            float y1 = sq[t], y2 = sq[t + half];
+            if (d.flags & TLB_ROPE) {
+                float cs, sn;
+                rope_cos_sin(float(d.pos), p.fr.hi[t], p.fr.lo[t], cs, sn);
+                const float t1 = y1 * cs + y2 * sn, t2 = -y1 * sn + y2 * cs;
+                y1 = t1;
+                y2 = t2;
+            }
+            d.dqpre[h * hd + t] = y1;
+            d.dqpre[h * hd + t + half] = y2;
+            sq[t] = y1;
+            sq[t + half] = y2;
+        }
+        __syncthreads();
+        float ar[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) ar[r] = 0.f;
+        for (int t = threadIdx.x; t < hd; t += blockDim.x) {
+            const float *br = d.lq.b + int64_t(h * hd + t) * d.rank;
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                if (r < d.rank) ar[r] = fmaf(sq[t], br[r], ar[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const float t = warp_sum(ar[r]);
+            if (lane == 0) red16[r][warp] = t;
+        }
+        __syncthreads();
+        if (threadIdx.x < d.rank) {
+            float t = 0.f;
+            for (int w = 0; w < kPW; ++w) t += red16[threadIdx.x][w];
+            atomicAdd(d.gh + threadIdx.x, d.lora_scaling * t);
+        }
+    }
+    // ---------------------------------------------------------------- phase 6: LoRA + AdamW
+    if (!grid_sync(p, 5, base, &s_abort)) return;
+    {
         const int64_t nbq = int64_t(d.qd) * d.rank, nbv = int64_t(d.kvd) * d.rank, na = int64_t(d.rank) * d.H;
         const int64_t n = nbq + nbv + 2 * na;
         float sa = 0.f, sb = 0.f;
         for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += int64_t(p.nblocks) * blockDim.x) {
             if (e < nbq) {
                 const int o = int(e / d.rank), r = int(e % d.rank);
-                // dQpre[o] = R(-theta) scale (U - D W) at row o
-                const int h = o / hd, dd = o % hd, pd = dd < half ? dd : dd - half;
-                const float Dh = __ldcg(p.Dacc + h);
-                const int o1 = h * hd + pd, o2 = o1 + half;
-                const float y1 = d.scale * (__ldcg(p.Uacc + o1) - Dh * __ldcg(p.Wacc + o1));
-                const float y2 = d.scale * (__ldcg(p.Uacc + o2) - Dh * __ldcg(p.Wacc + o2));
-                float q = dd < half ? y1 : y2;
-                if (d.flags & TLB_ROPE) {
-                    float cs, sn;
-                    rope_cos_sin(float(d.pos), p.fr.hi[pd], p.fr.lo[pd], cs, sn);
-                    q = dd < half ? y1 * cs + y2 * sn : -y1 * sn + y2 * cs;
-                }
-                if (r == 0) d.dqpre[o] = q;
-                const float gq = d.lora_scaling * q * d.hq[r];
+                const float gq = d.lora_scaling * __ldcg(d.dqpre + o) * d.hq[r];
                 if (d.lq.grad_b) d.lq.grad_b[e] = gq;
                 float mm = d.lq.m_b[e], vv = d.lq.v_b[e];
                 d.lq.b[e] = adam_elem(d.lq.b[e], gq, mm, vv, d.kb);
@@ -607,7 +676,7 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
                 const int64_t f2 = isq ? f : f - na;
                 const int r = int(f2 / d.H), cidx = int(f2 % d.H);
                 const tlb_lora &l = isq ? d.lq : d.lv;
-                const float ga = (isq ? ghq[r] : ghv[r]) * d.x[cidx];
+                const float ga = __ldcg(d.gh + (isq ? 0 : d.rank) + r) * d.x[cidx];
                 if (l.grad_a) l.grad_a[f2] = ga;
                 float mm = l.m_a[f2], vv = l.v_a[f2];
                 l.a[f2] = adam_elem(l.a[f2], ga, mm, vv, d.ka);
@@ -669,13 +738,15 @@ bool geometry(const tlb_layer_cfg &c, Geometry &g) {
     const int64_t rowH = int64_t(c.dim) * es, rowI = int64_t(c.ffn_dim) * es;
     // phase-2 items: the two weights' rows cut into nsplit column ranges of whole chunks,
     // so that an item stays near 8 KiB
+    // phase-2 items: two rows of W_gate and of W_up, one of nsplit column ranges of whole
+    // chunks, about 14 KiB in all
     g.nsplit = 1;
     for (int n = 1; n <= 8; ++n) {
         if (c.ffn_dim % (n * E)) continue;
         g.nsplit = n;
-        if (2 * rowI / n <= 8192) break;
+        if (4 * rowI / n <= 14336) break;
     }
-    g.slot_bytes = int(std::max<int64_t>(2 * rowI / g.nsplit, rowH));
+    g.slot_bytes = int(std::max<int64_t>(4 * rowI / g.nsplit, rowH));
     g.rpi = int(std::min<int64_t>(kMaxRowsPerItem, g.slot_bytes / rowH));
     g.xbytes = int(((std::max<int64_t>(c.dim, 2 * int64_t(c.ffn_dim)) * 4) + 127) / 128 * 128);
     int dev = 0, optin = 0;
@@ -683,10 +754,11 @@ bool geometry(const tlb_layer_cfg &c, Geometry &g) {
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return false;
     const int64_t budget = int64_t(optin) - 8 * 1024;     // static shared memory and slack
-    g.ngemv = int(std::min<int64_t>(kPW, (budget - g.xbytes) / (2 * int64_t(g.slot_bytes))));
+    g.ngemv = int(std::min<int64_t>(kPW, (budget - g.xbytes) / (kSlotsPerWarp * int64_t(g.slot_bytes))));
     if (g.ngemv < 4) return false;
-    const size_t attn = (size_t(G) * hd * (1 + 2 * kPW + 2) + size_t(G) * hd * c.rank) * 4;
-    g.dyn = std::max(size_t(g.xbytes) + size_t(2 * g.ngemv) * g.slot_bytes, attn);
+    const size_t attn = size_t(1 + 2 * kPW) * G * hd * 4;          // dCtx + per-warp U, W
+    const size_t fin = size_t(2 * kPT + 256) * 4;                   // per-head finalize
+    g.dyn = std::max({size_t(g.xbytes) + size_t(kSlotsPerWarp) * g.ngemv * g.slot_bytes, attn, fin});
     return int64_t(g.dyn) <= budget;
 }
 
@@ -704,7 +776,7 @@ bool persistent_supported(const tlb_layer_cfg &c, int64_t S, int64_t L) {
 }
 
 int decode_persistent_launch(const DecodeArgs &d, const tlb_layer_cfg &c, int64_t L, void *ws, size_t off_gbar,
-                             size_t off_pp, size_t off_acc, cudaStream_t st) {
+                             size_t off_pp, cudaStream_t st) {
     Geometry g;
     TLB_REQUIRE(geometry(c, g), TLB_EUNSUPPORTED, "decode: no persistent geometry");
     PArgs p;
@@ -712,13 +784,6 @@ int decode_persistent_launch(const DecodeArgs &d, const tlb_layer_cfg &c, int64_
     p.status = ws_at<uint32_t>(ws, 0);
     p.gbar = ws_at<unsigned long long>(ws, off_gbar);
     p.pp = ws_at<float2>(ws, off_pp);
-    const int qd = c.n_heads * c.head_dim;
-    float *acc = ws_at<float>(ws, off_acc);
-    p.Uacc = acc;
-    p.Wacc = acc + qd;
-    p.Dacc = acc + 2 * qd;
-    p.ug = p.Dacc + c.n_heads;
-    p.wg = p.ug + c.n_heads * c.rank;
     p.nblocks = std::min(num_sms(), kMaxPersistentBlocks);
     p.ngemv = g.ngemv;
     p.slot_bytes = g.slot_bytes;

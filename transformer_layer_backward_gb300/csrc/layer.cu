@@ -12,7 +12,7 @@ namespace {
 
 struct LayerWs {
     size_t dF, dG, dU, dN2, dSub, dqpre, dv, gh_q, gh_v;
-    size_t dR1, Upart, Wpart, Dpart, gh2, part1, part2, part3, gbar, pp, acc;   // single-token path
+    size_t dR1, Upart, Wpart, Dpart, gh2, part1, part2, part3, gbar, pp;   // single-token path
     size_t total;
 };
 
@@ -42,9 +42,8 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
         w.part3 = p.take(ceil_div(qd, 8) * 8);
         w.gbar = p.take(256);
         w.pp = p.take(3 * int64_t(kMaxPersistentBlocks) * 8);
-        w.acc = p.take(persistent_acc_floats(c) * 4);
     } else {
-        w.dR1 = w.Upart = w.Wpart = w.Dpart = w.gh2 = w.part1 = w.part2 = w.part3 = w.gbar = w.pp = w.acc = 0;
+        w.dR1 = w.Upart = w.Wpart = w.Dpart = w.gh2 = w.part1 = w.part2 = w.part3 = w.gbar = w.pp = 0;
     }
     w.total = p.off;
     return w;
@@ -321,7 +320,7 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
         d.part1 = ws_at<float2>(ws, p.part1);
         d.part2 = ws_at<float2>(ws, p.part2);
         d.part3 = ws_at<float2>(ws, p.part3);
-        if (persistent_supported(c, S, L)) return decode_persistent_launch(d, c, L, ws, p.gbar, p.pp, p.acc, st);
+        if (persistent_supported(c, S, L)) return decode_persistent_launch(d, c, L, ws, p.gbar, p.pp, st);
         return decode_layer_launch(d, c.wtype, st);
     }
     TLB_TRY(ffn_impl(c, S, d_hidden, *w, *acts, d_hidden, ws, st));
