@@ -58,6 +58,21 @@ def decode_bytes(cfg) -> int:
     return weights + kv + attn + lora + vectors
 
 
+# The kernels of one decode layer backward (multi-kernel schedule, launch order) and the
+# bytes each must move at least once (algorithmic traffic; int8 ternary weights).
+def decode_kernel_bytes(cfg):
+    H, I, qd, kvd, r, L, nh = cfg.dim, cfg.ffn_dim, cfg.q_dim, cfg.kv_dim, cfg.rank, cfg.cache_len, cfg.n_heads
+    lora = (2 * r * H + qd * r + kvd * r) * 24 + 2 * H * 4 + 2 * r * 4
+    return [
+        ("dec_k1 dF = W_down dOut", I * H + (H + I + 2 * I) * 4),
+        ("dec_k2 dN2 = W_gate dG + W_up dU", 2 * H * I + (5 * I + 3 * H) * 4),
+        ("dec_k3 dSub = W_O dR1", qd * H + (4 * H + qd + 2 * qd) * 4),
+        ("dec_k4 attention over K, V", 2 * kvd * L * 4 + nh * L * 4 + 3 * qd * 4),
+        ("dec_k6 dQpre, gh_q", 2 * qd * 4 * (L // 64) + qd * r * 4),
+        ("dec_k7 LoRA grads + AdamW", lora),
+    ]
+
+
 def peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -244,32 +259,32 @@ def main():
     tokens = args.steps * world
     value = tokens / (ms_max / 1e3)
 
-    # dominant kernel: the ternary transposed GEMV (W_gate / W_up / W_down sized), timed live on
-    # this stream over the weight matrices of every layer in turn
-    mats = [(ly["t"][k], cfg.ffn_dim if k == "w_down" else cfg.dim, cfg.dim if k == "w_down" else cfg.ffn_dim)
-            for ly in layers for k in ("w_down", "w_gate", "w_up")]
-    xin = torch.randn(1, cfg.ffn_dim, device="cuda")
-    yout = torch.empty(1, cfg.ffn_dim, device="cuda")
-    for k in range(3):
-        W, rows, cols = mats[k]
-        tlb.linear_backward("ternary", W, xin[:, :cols], out=yout[:, :rows])
-    nk = max(3 * len(mats), 96)
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k0.record(stream)
-    for k in range(nk):
-        W, rows, cols = mats[k % len(mats)]
-        tlb.linear_backward("ternary", W, xin[:, :cols], out=yout[:, :rows])
-    k1.record(stream)
-    torch.cuda.synchronize()
-    kms = k0.elapsed_time(k1) / nk
-    gemv_bytes = cfg.dim * cfg.ffn_dim + 4 * (cfg.dim + cfg.ffn_dim)
+    # per-kernel times, live, on this stream: events recorded after every kernel of the step
+    kern = decode_kernel_bytes(cfg)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(kern) + 1)]
+    arr = tlb.profile_events(evs[1:])
+    nk = min(max(args.steps // 10, 50), 500)
+    ktime = [0.0] * len(kern)
+    for i in range(nk):
+        ly = layers[i % NL]
+        dh.copy_(ly["t"]["dout"])
+        evs[0].record(stream)
+        tlb.layer_backward(c, 1, cfg.cache_len, ly["w"], ly["a"], ly["lq"], ly["lv"], adam, dh, ss, ws)
+        torch.cuda.synchronize()
+        for k in range(len(kern)):
+            ktime[k] += evs[k].elapsed_time(evs[k + 1]) / nk
+    tlb.profile_events(None)
+    del arr
     pk = peaks()
     hbm = pk["hbm_gbs"] if pk else 6800.0
-    achieved = gemv_bytes / (kms / 1e3) / 1e9
+    per_kernel = [{"kernel": n, "us": t * 1e3, "bytes": b, "GB/s": b / (t / 1e3) / 1e9}
+                  for (n, b), t in zip(kern, ktime)]
+    dom = max(range(len(kern)), key=lambda k: ktime[k])
+    achieved = per_kernel[dom]["GB/s"]
     traffic = None
-    prof = os.path.join(ROOT, "profiles", "gemv_ternary_decode.json")
+    prof = os.path.join(ROOT, "profiles", "decode_dram_bytes.json")
     if os.path.exists(prof):
-        traffic = json.load(open(prof)).get("dram_bytes_per_launch")
+        traffic = json.load(open(prof)).get(kern[dom][0].split()[0])
 
     # end to end through the public API: per-step activations from pinned host memory,
     # d_in and the gradient norm read back every step
@@ -315,9 +330,11 @@ def main():
                            "global_batch": world, "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
                            "layers_cycled": NL, "l2": "inputs > L2: %d distinct layers x %.1f MB" % (NL, step_bytes / 1e6),
                            "cuda_graph": graphs is not None},
-                "roofline": {"bound": "hbm", "kernel": "gemv_rows_kernel<ternary> (transposed-weight GEMV)",
-                             "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                             "traffic": traffic, "peak_source": "MEASURED_PEAKS.json hbm_gbs" if pk else "fallback"},
+                "roofline": {"bound": "hbm", "kernel": kern[dom][0], "achieved": achieved, "peak": hbm,
+                             "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                             "algorithmic_bytes": kern[dom][1],
+                             "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else "fallback"},
+                "per_kernel": per_kernel,
                 "step_roofline": {"bytes_per_step": step_bytes, "achieved": step_bytes / (ms_max / args.steps / 1e3) / 1e9,
                                   "peak": hbm, "unit": "GB/s",
                                   "frac": step_bytes / (ms_max / args.steps / 1e3) / 1e9 / hbm},

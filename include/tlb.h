@@ -67,6 +67,8 @@ extern "C" {
 #define TLB_ROPE 8             /* NeoX split-half rotary embedding on q and k */
 #define TLB_USE_SILU_CACHE 16  /* SwiGLU: read the cached silu(gate) instead of recomputing it */
 #define TLB_CAUSAL 32          /* query row i sees keys j <= L - S + i only; attn is 0 elsewhere */
+#define TLB_PERSISTENT 64      /* single-token layers: one persistent cooperative kernel (TMA-streamed
+                                  weights, grid barriers) instead of the multi-kernel schedule */
 
 /* Shapes and constants of one layer. q_dim = n_heads*head_dim, kv_dim = n_kv_heads*head_dim. */
 typedef struct {
@@ -145,6 +147,11 @@ const char *tlb_last_error(void);
 const char *tlb_build_info(void);
 /* Number of kernels this process has enqueued through the library so far (all threads). */
 uint64_t tlb_launch_count(void);
+/* Benchmarking aid.  With events != NULL, each later tlb_layer_backward call records
+ * events[i] (cudaEvent_t passed as void*) on its stream right after its i-th kernel
+ * launch, for i < n, so a caller can time the kernels of a layer one by one; NULL turns
+ * it off.  Process-wide setting: do not use while other threads call the library. */
+void tlb_profile_events(void *const *events, int32_t n);
 
 /* ---------------------------------------------------------------- standalone steps */
 

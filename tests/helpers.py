@@ -64,13 +64,14 @@ def check(name, gpu, ref, rel_l2=F32_REL_L2, max_abs=F32_MAX_ABS):
     return rel, mx
 
 
-def cfg_to_abi(tlb, cfg):
+def cfg_to_abi(tlb, cfg, persistent=False):
     """synth LayerConfig -> the C ABI layer struct."""
     return tlb.layer_cfg(cfg.dim, cfg.ffn_dim, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.rank,
                          cfg.lora_alpha, act=cfg.act, wtype=cfg.wtype, sub_norm=cfg.sub_norm,
                          pre_norm=cfg.pre_norm, residual=cfg.residual, rope=cfg.rope,
                          use_silu_cache=(cfg.act == "silu_mul" and cfg.use_silu_cache), causal=True,
-                         rope_base=cfg.rope_base, norm_eps=cfg.norm_eps, attn_scale=cfg.attn_scale)
+                         rope_base=cfg.rope_base, norm_eps=cfg.norm_eps, attn_scale=cfg.attn_scale,
+                         persistent=persistent)
 
 
 def adam_to_abi(tlb, cfg):

@@ -119,11 +119,14 @@ def test_lora_grad_adamw(lib, case):
         assert abs(s[1] - np.sum(db ** 2)) <= 1e-5 * np.sum(db ** 2)
 
 
-def test_layer_backward(lib, case):
+@pytest.mark.parametrize("persistent", [False, True])
+def test_layer_backward(lib, case, persistent):
     import torch
     cfg, d, ref = case
+    if persistent and cfg.seq_len != 1:
+        pytest.skip("the persistent schedule is for single-token layers")
     t = to_dev(d, cfg.wtype)
-    c = cfg_to_abi(lib, cfg)
+    c = cfg_to_abi(lib, cfg, persistent=persistent)
     adam = adam_to_abi(lib, cfg)
     ws = lib.workspace(c, cfg.seq_len, cfg.cache_len)
     L = lora_dev(t)

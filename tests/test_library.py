@@ -19,7 +19,7 @@ def lib():
 
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "tlb.h")).read()
-    return sorted(set(re.findall(r"^\s*(?:const char \*|int |size_t )(tlb_\w+)\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const char \*|int |size_t |void |uint64_t )(tlb_\w+)\(", text, re.M)))
 
 
 def test_header_declares_the_entry_points():

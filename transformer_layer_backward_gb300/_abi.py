@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libt
 TLB_OK, TLB_EINVAL, TLB_EUNSUPPORTED, TLB_ENONFINITE, TLB_ETIMEOUT, TLB_ECUDA = 0, -1, -2, -3, -4, -5
 ACT_RELU2_MUL, ACT_SILU_MUL = 0, 1
 W_F32, W_BF16, W_TERNARY_I8 = 0, 1, 2
-SUB_NORM, PRE_NORM, RESIDUAL, ROPE, USE_SILU_CACHE, CAUSAL = 1, 2, 4, 8, 16, 32
+SUB_NORM, PRE_NORM, RESIDUAL, ROPE, USE_SILU_CACHE, CAUSAL, PERSISTENT = 1, 2, 4, 8, 16, 32, 64
 
 vp, i32, i64, f32, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_size_t
 
@@ -56,6 +56,7 @@ SIGNATURES = {
     "tlb_last_error": (C.c_char_p, []),
     "tlb_build_info": (C.c_char_p, []),
     "tlb_launch_count": (C.c_uint64, []),
+    "tlb_profile_events": (None, [C.POINTER(C.c_void_p), i32]),
     "tlb_linear_backward": (C.c_int, [i32, vp, f32, vp, i64, i64, i64, vp, i32, vp]),
     "tlb_softmax_backward": (C.c_int, [vp, vp, vp, i64, i64, vp]),
     "tlb_act_backward": (C.c_int, [i32, vp, vp, vp, vp, vp, vp, i64, vp]),

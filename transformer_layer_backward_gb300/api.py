@@ -92,6 +92,18 @@ def launch_count() -> int:
     return int(A.load().tlb_launch_count())
 
 
+def profile_events(events):
+    """Record events[i] (torch.cuda.Event) after the i-th kernel of each later layer call;
+    None turns it off.  Returns the ctypes array, which must stay alive while in use."""
+    lib = A.load()
+    if events is None:
+        lib.tlb_profile_events(None, 0)
+        return None
+    arr = (C.c_void_p * len(events))(*[C.c_void_p(e.cuda_event) for e in events])
+    lib.tlb_profile_events(arr, len(events))
+    return arr
+
+
 def adamw_cfg(lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1, lr_b_mult=16.0):
     return A.AdamwCfg(lr, beta1, beta2, eps, weight_decay, lr_b_mult, int(step))
 
@@ -108,10 +120,11 @@ def adamw(p, g, m, v, cfg: A.AdamwCfg, lr_mult=1.0, sumsq=None, stream=None):
 def layer_cfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, lora_alpha, act="relu2_mul",
               wtype="f32", sub_norm=False, pre_norm=False, residual=True, rope=True,
               use_silu_cache=False, causal=True, rope_base=10000.0, norm_eps=1e-6,
-              attn_scale=None) -> A.LayerCfg:
+              attn_scale=None, persistent=False) -> A.LayerCfg:
     flags = ((A.SUB_NORM if sub_norm else 0) | (A.PRE_NORM if pre_norm else 0) |
              (A.RESIDUAL if residual else 0) | (A.ROPE if rope else 0) |
-             (A.USE_SILU_CACHE if use_silu_cache else 0) | (A.CAUSAL if causal else 0))
+             (A.USE_SILU_CACHE if use_silu_cache else 0) | (A.CAUSAL if causal else 0) |
+             (A.PERSISTENT if persistent else 0))
     return A.LayerCfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, float(lora_alpha),
                       float(rope_base), float(norm_eps),
                       float(1.0 / math.sqrt(head_dim) if attn_scale is None else attn_scale),

@@ -12,6 +12,13 @@ namespace tlb {
 
 static thread_local char g_err[512] = "";
 static unsigned long long g_launches = 0;
+static void *const *g_prof_events = nullptr;
+static int g_prof_n = 0;
+
+void profile_mark(int i, cudaStream_t st) {
+    if (g_prof_events != nullptr && i < g_prof_n)
+        cudaEventRecord(reinterpret_cast<cudaEvent_t>(g_prof_events[i]), st);
+}
 
 void set_error(const char *fmt, ...) {
     va_list ap;
@@ -90,6 +97,11 @@ const char *tlb_build_info(void) {
 }
 
 uint64_t tlb_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+void tlb_profile_events(void *const *events, int32_t n) {
+    g_prof_events = events;
+    g_prof_n = events != nullptr && n > 0 ? n : 0;
+}
 
 int tlb_linear_backward(int32_t wtype, const void *W, float scale, const float *dY, int64_t S,
                         int64_t out_dim, int64_t in_dim, float *dX, int32_t accumulate, void *stream) {

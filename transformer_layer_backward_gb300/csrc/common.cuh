@@ -42,6 +42,9 @@ void clear_error();
 // Error of the last launch on this thread (a launch error never enqueues work).
 int check_launch(const char *what);
 
+// Record the i-th profiling event (tlb_profile_events) on st, if profiling is on.
+void profile_mark(int i, cudaStream_t st);
+
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

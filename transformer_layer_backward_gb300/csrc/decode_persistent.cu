@@ -713,7 +713,9 @@ int launch_p(const PArgs &p, size_t dyn, cudaStream_t st) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     TLB_CUDA(cudaLaunchKernelEx(&cfg, k, p));
-    return check_launch("decode persistent");
+    TLB_TRY(check_launch("decode persistent"));
+    profile_mark(0, st);
+    return TLB_OK;
 }
 
 template <int WT>

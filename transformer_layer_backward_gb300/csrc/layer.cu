@@ -320,7 +320,8 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
         d.part1 = ws_at<float2>(ws, p.part1);
         d.part2 = ws_at<float2>(ws, p.part2);
         d.part3 = ws_at<float2>(ws, p.part3);
-        if (persistent_supported(c, S, L)) return decode_persistent_launch(d, c, L, ws, p.gbar, p.pp, st);
+        if ((c.flags & TLB_PERSISTENT) && persistent_supported(c, S, L))
+            return decode_persistent_launch(d, c, L, ws, p.gbar, p.pp, st);
         return decode_layer_launch(d, c.wtype, st);
     }
     TLB_TRY(ffn_impl(c, S, d_hidden, *w, *acts, d_hidden, ws, st));
