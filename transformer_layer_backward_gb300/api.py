@@ -99,6 +99,8 @@ def profile_events(events):
     if events is None:
         lib.tlb_profile_events(None, 0)
         return None
+    for e in events:            # torch creates the CUDA event on its first record
+        e.record()
     arr = (C.c_void_p * len(events))(*[C.c_void_p(e.cuda_event) for e in events])
     lib.tlb_profile_events(arr, len(events))
     return arr
