@@ -259,22 +259,28 @@ def main():
     tokens = args.steps * world
     value = tokens / (ms_max / 1e3)
 
-    # per-kernel times, live, on this stream: events recorded after every kernel of the step
+    # per-kernel times, live, on this stream: events recorded after every kernel of the step.
+    # The steps are queued behind a device-side sleep so that they run back to back on the
+    # GPU (host launch gaps would otherwise show up inside the intervals).
     kern = decode_kernel_bytes(cfg)
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(kern) + 1)]
-    arr = tlb.profile_events(evs[1:])
-    nk = min(max(args.steps // 10, 50), 500)
-    ktime = [0.0] * len(kern)
+    nk = 200
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kern) + 1)] for _ in range(nk)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)
+    keep = []
     for i in range(nk):
         ly = layers[i % NL]
         dh.copy_(ly["t"]["dout"])
-        evs[0].record(stream)
+        evs[i][0].record(stream)
+        keep.append(tlb.profile_events(evs[i][1:]))
         tlb.layer_backward(c, 1, cfg.cache_len, ly["w"], ly["a"], ly["lq"], ly["lv"], adam, dh, ss, ws)
-        torch.cuda.synchronize()
-        for k in range(len(kern)):
-            ktime[k] += evs[k].elapsed_time(evs[k + 1]) / nk
     tlb.profile_events(None)
-    del arr
+    torch.cuda.synchronize()
+    ktime = [sum(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(nk)) / nk for k in range(len(kern))]
+    del keep
     pk = peaks()
     hbm = pk["hbm_gbs"] if pk else 6800.0
     per_kernel = [{"kernel": n, "us": t * 1e3, "bytes": b, "GB/s": b / (t / 1e3) / 1e9}

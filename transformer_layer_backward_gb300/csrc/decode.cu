@@ -39,14 +39,15 @@ constexpr int kAThreads = kAWarps * 32;
 //   y[r] = sum_m scale_m W_m[r, :] . x_m.
 // One warp; U chunks of 16 bytes per row and matrix in flight per lane.  Returns the
 // row values to every lane in out[R] (0 for rows past the end).
-template <int WT, int NM, int R, int U>
+template <int WT, int NM, int R, int U, bool ATOMIC = false>
 __device__ __forceinline__ void warp_rows(const char *const *W, const float *scale, const float *const *xs,
-                                          int r0, int rows, int cols, float *y, float *out) {
+                                          int r0, int rows, int cols, float *y, float *out,
+                                          size_t row_bytes = 0) {
     constexpr int E = EPC<WT>::v;
     constexpr int P = E / 4;
     const int lane = threadIdx.x & 31;
     const int nch = cols / E;
-    const size_t row_bytes = size_t(cols) * (16 / E);
+    if (row_bytes == 0) row_bytes = size_t(cols) * (16 / E);
     float acc[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) acc[r] = 0.f;
@@ -87,7 +88,10 @@ __device__ __forceinline__ void warp_rows(const char *const *W, const float *sca
     for (int r = 0; r < R; ++r) {
         const float s = warp_sum(acc[r]);
         out[r] = (r0 + r < rows) ? s : 0.f;
-        if (lane == 0 && r0 + r < rows) y[r0 + r] = s;
+        if (lane == 0 && r0 + r < rows) {
+            if constexpr (ATOMIC) atomicAdd(y + r0 + r, s);
+            else y[r0 + r] = s;
+        }
     }
 }
 
@@ -139,6 +143,35 @@ __device__ __forceinline__ void rms_coef2(float2 s, int n, float eps, float &rin
 
 constexpr int kR = 2, kU = 2;   // rows per warp, chunks in flight per row and matrix
 
+// Block-wide (sum dy g x, sum x^2) over n elements (n % 4 == 0, 16-byte aligned arrays),
+// every thread issuing all its loads of a batch before using them.
+__device__ __forceinline__ float2 rms_sums_full(const float *x, const float *g, const float *dy, int n, float2 *red) {
+    constexpr int B = 4;
+    const int n4 = n >> 2;
+    const float4 *x4 = reinterpret_cast<const float4 *>(x), *g4 = reinterpret_cast<const float4 *>(g),
+                 *d4 = reinterpret_cast<const float4 *>(dy);
+    float2 acc = make_float2(0.f, 0.f);
+    for (int base = threadIdx.x; base < n4; base += blockDim.x * B) {
+        float4 xv[B], gv[B], dv[B];
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const int i = base + b * blockDim.x;
+            const bool ok = i < n4;
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            xv[b] = ok ? x4[i] : z;
+            gv[b] = ok ? g4[i] : z;
+            dv[b] = ok ? d4[i] : z;
+        }
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            acc.x += xv[b].x * gv[b].x * dv[b].x + xv[b].y * gv[b].y * dv[b].y + xv[b].z * gv[b].z * dv[b].z +
+                     xv[b].w * gv[b].w * dv[b].w;
+            acc.y += dot4(xv[b], xv[b]);
+        }
+    }
+    return block_sum2(acc, red);
+}
+
 // ------------------------------------------------------------------ k1: dF = s_d W_down dOut
 
 template <int WT>
@@ -148,6 +181,9 @@ __global__ void __launch_bounds__(kThreads) dec_k1(DecodeArgs a) {
     float *sx = reinterpret_cast<float *>(sm4);
     stage_vector<WT>(sx, a.d_hidden, a.H);
     if (blockIdx.x == 0 && threadIdx.x < 2 * a.rank) a.gh[threadIdx.x] = 0.f;
+    // dN2 and dSub are sums of per-block column-range products in k2 and k3
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.H + a.qd; i += gridDim.x * blockDim.x)
+        (i < a.H ? a.dN2[i] : a.dSub[i - a.H]) = 0.f;
     __syncthreads();
     const char *W[1] = {reinterpret_cast<const char *>(a.w_down)};
     const float sc[1] = {a.s_down};
@@ -164,8 +200,10 @@ template <int WT, int ACT>
 __global__ void __launch_bounds__(kThreads) dec_k2(DecodeArgs a) {
     extern __shared__ float4 sm4[];
     __shared__ float2 red[32];
+    // this block's column range [c0, c0 + nc) of dG, dU and of the W_gate / W_up rows
+    const int nc = a.I / a.ns2, c0 = blockIdx.y * nc;
     float *sG = reinterpret_cast<float *>(sm4);
-    float *sU = sG + a.I;
+    float *sU = sG + nc;
     float rinv = 1.f, c = 0.f;
     const bool sub = a.flags & TLB_SUB_NORM;
     if (sub) rms_coef2(sum_partials(a.part1, a.n1, red), a.I, a.eps, rinv, c);
@@ -174,13 +212,13 @@ __global__ void __launch_bounds__(kThreads) dec_k2(DecodeArgs a) {
         // dh (sub-norm backward) and the gated-activation backward, float4 at a time,
         // two float4 of each of the six inputs in flight per thread
         constexpr int B = 2;
-        const int n4 = a.I >> 2;
-        const float4 *dF4 = reinterpret_cast<const float4 *>(a.dF);
-        const float4 *hid4 = reinterpret_cast<const float4 *>(a.hidden);
-        const float4 *gam4 = reinterpret_cast<const float4 *>(a.g_sub_ffn);
-        const float4 *gat4 = reinterpret_cast<const float4 *>(a.gate);
-        const float4 *up4 = reinterpret_cast<const float4 *>(a.up);
-        const float4 *sg4 = reinterpret_cast<const float4 *>(a.silu_gate);
+        const int n4 = nc >> 2;
+        const float4 *dF4 = reinterpret_cast<const float4 *>(a.dF + c0);
+        const float4 *hid4 = reinterpret_cast<const float4 *>(a.hidden + c0);
+        const float4 *gam4 = reinterpret_cast<const float4 *>(a.g_sub_ffn + c0);
+        const float4 *gat4 = reinterpret_cast<const float4 *>(a.gate + c0);
+        const float4 *up4 = reinterpret_cast<const float4 *>(a.up + c0);
+        const float4 *sg4 = reinterpret_cast<const float4 *>(a.silu_gate + c0);
         for (int base = threadIdx.x; base < n4; base += blockDim.x * B) {
             float4 df[B], hd[B], gm[B], ga[B], uu[B], sl[B];
 #pragma unroll
@@ -227,13 +265,14 @@ __global__ void __launch_bounds__(kThreads) dec_k2(DecodeArgs a) {
         }
     }
     __syncthreads();
-    const char *W[2] = {reinterpret_cast<const char *>(a.w_gate), reinterpret_cast<const char *>(a.w_up)};
+    constexpr int ES = 16 / EPC<WT>::v;
+    const char *W[2] = {reinterpret_cast<const char *>(a.w_gate) + size_t(c0) * ES,
+                        reinterpret_cast<const char *>(a.w_up) + size_t(c0) * ES};
     const float sc[2] = {a.s_gate, a.s_up};
     const float *xs[2] = {sG, sU};
     const int r0 = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR;
     float vals[kR] = {};
-    if (r0 < a.H) warp_rows<WT, 2, kR, kU>(W, sc, xs, r0, a.H, a.I, a.dN2, vals);
-    if (a.flags & TLB_PRE_NORM) block_partials<kR>(vals, r0, a.H, a.g_ffn, a.r1, a.part2, red);
+    if (r0 < a.H) warp_rows<WT, 2, kR, kU, true>(W, sc, xs, r0, a.H, nc, a.dN2, vals, size_t(a.I) * ES);
 }
 
 // ------------------------------------------------------------------ k3: dR1, dSub = s_o W_O dR1
@@ -242,15 +281,18 @@ template <int WT>
 __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
     extern __shared__ float4 sm4[];
     __shared__ float2 red[32];
+    // this block's column range [c0, c0 + nc) of dR1 and of the W_O rows
+    const int nc = a.H / a.ns3, c0 = blockIdx.y * nc;
     float *sR = reinterpret_cast<float *>(sm4);
     float rinv = 1.f, c = 0.f;
     const bool pre = a.flags & TLB_PRE_NORM;
-    if (pre) rms_coef2(sum_partials(a.part2, a.n2, red), a.H, a.eps, rinv, c);
+    if (pre) rms_coef2(rms_sums_full(a.r1, a.g_ffn, a.dN2, a.H, red), a.H, a.eps, rinv, c);
     const bool resid = a.flags & TLB_RESIDUAL;
     {
-        const int n4 = a.H >> 2;
-        const float4 *dn4 = reinterpret_cast<const float4 *>(a.dN2), *r14 = reinterpret_cast<const float4 *>(a.r1);
-        const float4 *gf4 = reinterpret_cast<const float4 *>(a.g_ffn), *do4 = reinterpret_cast<const float4 *>(a.d_hidden);
+        const int n4 = nc >> 2;
+        const float4 *dn4 = reinterpret_cast<const float4 *>(a.dN2 + c0), *r14 = reinterpret_cast<const float4 *>(a.r1 + c0);
+        const float4 *gf4 = reinterpret_cast<const float4 *>(a.g_ffn + c0),
+                     *do4 = reinterpret_cast<const float4 *>(a.d_hidden + c0);
         for (int i = threadIdx.x; i < n4; i += blockDim.x) {
             const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
             const float4 dn = dn4[i], r = pre ? r14[i] : z, gm = pre ? gf4[i] : z, dO = resid ? do4[i] : z;
@@ -260,17 +302,17 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
             v.z = (pre ? rinv * (dn.z * gm.z - r.z * c) : dn.z) + dO.z;
             v.w = (pre ? rinv * (dn.w * gm.w - r.w * c) : dn.w) + dO.w;
             reinterpret_cast<float4 *>(sR)[xunit<WT>(i)] = v;
-            if (blockIdx.x == 0) reinterpret_cast<float4 *>(a.dR1)[i] = v;
+            if (blockIdx.x == 0) reinterpret_cast<float4 *>(a.dR1 + c0)[i] = v;
         }
     }
     __syncthreads();
-    const char *W[1] = {reinterpret_cast<const char *>(a.w_o)};
+    constexpr int ES = 16 / EPC<WT>::v;
+    const char *W[1] = {reinterpret_cast<const char *>(a.w_o) + size_t(c0) * ES};
     const float sc[1] = {a.s_o};
     const float *xs[1] = {sR};
     const int r0 = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR;
     float vals[kR] = {};
-    if (r0 < a.qd) warp_rows<WT, 1, kR, kU>(W, sc, xs, r0, a.qd, a.H, a.dSub, vals);
-    if (a.flags & TLB_SUB_NORM) block_partials<kR>(vals, r0, a.qd, a.g_sub_attn, a.ctx, a.part3, red);
+    if (r0 < a.qd) warp_rows<WT, 1, kR, kU, true>(W, sc, xs, r0, a.qd, nc, a.dSub, vals, size_t(a.H) * ES);
 }
 
 // ------------------------------------------------------------------ k4: attention, one pass over K and V
@@ -294,7 +336,7 @@ __global__ void __launch_bounds__(kAThreads) dec_k4(DecodeArgs a) {
     float *sR = sC + G * hd;                           // [kAWarps][G][2][hd] reduction
     float rinv = 1.f, c = 0.f;
     const bool sub = a.flags & TLB_SUB_NORM;
-    if (sub) rms_coef2(sum_partials(a.part3, a.n3, red2), a.qd, a.eps, rinv, c);
+    if (sub) rms_coef2(rms_sums_full(a.ctx, a.g_sub_attn, a.dSub, a.qd, red2), a.qd, a.eps, rinv, c);
     const int off = kvh * G * hd;
     for (int i = threadIdx.x; i < G * hd; i += blockDim.x) {
         const int q = off + i;
@@ -593,13 +635,13 @@ int launch_all(const DecodeArgs &a, cudaStream_t st) {
     TLB_CUDA(launch(dec_k1<WT>, dim3(unsigned(a.n1)), size_t(a.H) * 4, st, false, a));
     TLB_TRY(check_launch("decode k1"));
     profile_mark(0, st);
-    const size_t sm2 = size_t(2) * a.I * 4;
-    const dim3 g2(unsigned(a.n2));
+    const size_t sm2 = size_t(2) * (a.I / a.ns2) * 4;
+    const dim3 g2(unsigned(a.n2), unsigned(a.ns2));
     if (a.act == TLB_ACT_RELU2_MUL) TLB_CUDA(launch(dec_k2<WT, TLB_ACT_RELU2_MUL>, g2, sm2, st, false, a));
     else TLB_CUDA(launch(dec_k2<WT, TLB_ACT_SILU_MUL>, g2, sm2, st, false, a));
     TLB_TRY(check_launch("decode k2"));
     profile_mark(1, st);
-    TLB_CUDA(launch(dec_k3<WT>, dim3(unsigned(a.n3)), size_t(a.H) * 4, st, false, a));
+    TLB_CUDA(launch(dec_k3<WT>, dim3(unsigned(a.n3), unsigned(a.ns3)), size_t(a.H / a.ns3) * 4, st, false, a));
     TLB_TRY(check_launch("decode k3"));
     profile_mark(2, st);
     const int G = a.nh / a.nkv;

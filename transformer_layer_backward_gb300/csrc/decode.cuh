@@ -23,6 +23,7 @@ struct DecodeArgs {
     // vector each GEMV produces; n1..n3 = the GEMV grids (blocks of k1, k2, k3)
     float2 *part1, *part2, *part3;
     int n1, n2, n3;
+    int ns2, ns3;   // column ranges (blocks per row block) of the W_gate | W_up and W_O GEMVs
 };
 
 // Weight elements per 16-byte chunk of a row.

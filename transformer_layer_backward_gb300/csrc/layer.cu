@@ -317,6 +317,14 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
         d.n1 = int(ceil_div(c.ffn_dim, rpb));
         d.n2 = int(ceil_div(c.dim, rpb));
         d.n3 = int(ceil_div(qd, rpb));
+        // column ranges: more blocks in flight for the two GEMVs with few rows (whole 16-byte
+        // weight chunks per range, ranges a multiple of 4 floats)
+        const int E = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 8 : 16);
+        d.ns2 = 1;
+        for (int n : {4, 2})
+            if (c.ffn_dim % (n * E) == 0 && (c.ffn_dim / n) % 4 == 0) { d.ns2 = n; break; }
+        d.ns3 = 1;
+        if (c.dim % (2 * E) == 0 && (c.dim / 2) % 4 == 0) d.ns3 = 2;
         d.part1 = ws_at<float2>(ws, p.part1);
         d.part2 = ws_at<float2>(ws, p.part2);
         d.part3 = ws_at<float2>(ws, p.part3);
