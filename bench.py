@@ -259,28 +259,30 @@ def main():
     tokens = args.steps * world
     value = tokens / (ms_max / 1e3)
 
-    # per-kernel times, live, on this stream: events recorded after every kernel of the step.
-    # The steps are queued behind a device-side sleep so that they run back to back on the
-    # GPU (host launch gaps would otherwise show up inside the intervals).
+    # per-kernel times, live, on this stream: events recorded after every kernel of the step,
+    # the steps captured in one CUDA graph like the timed loop (stream launches would add host
+    # dispatch gaps to the intervals).
     kern = decode_kernel_bytes(cfg)
-    nk = 200
+    nk = 64
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kern) + 1)] for _ in range(nk)]
     for row in evs:
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
-    torch.cuda._sleep(200_000_000)
     keep = []
-    for i in range(nk):
-        ly = layers[i % NL]
-        dh.copy_(ly["t"]["dout"])
-        evs[i][0].record(stream)
-        keep.append(tlb.profile_events(evs[i][1:]))
-        tlb.layer_backward(c, 1, cfg.cache_len, ly["w"], ly["a"], ly["lq"], ly["lv"], adam, dh, ss, ws)
-    tlb.profile_events(None)
+    pg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(pg):
+        for i in range(nk):
+            ly = layers[i % NL]
+            dh.copy_(ly["t"]["dout"])
+            evs[i][0].record()
+            keep.append(tlb.profile_events(evs[i][1:]))
+            tlb.layer_backward(c, 1, cfg.cache_len, ly["w"], ly["a"], ly["lq"], ly["lv"], adam, dh, ss, ws)
+        tlb.profile_events(None)
+    pg.replay()
     torch.cuda.synchronize()
     ktime = [sum(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(nk)) / nk for k in range(len(kern))]
-    del keep
+    del keep, pg
     pk = peaks()
     hbm = pk["hbm_gbs"] if pk else 6800.0
     per_kernel = [{"kernel": n, "us": t * 1e3, "bytes": b, "GB/s": b / (t / 1e3) / 1e9}
