@@ -259,9 +259,9 @@ def main():
     tokens = args.steps * world
     value = tokens / (ms_max / 1e3)
 
-    # per-kernel times, live, on this stream: events recorded after every kernel of the step,
-    # the steps captured in one CUDA graph like the timed loop (stream launches would add host
-    # dispatch gaps to the intervals).
+    # per-kernel times, live, on this stream: the library records an event before the first
+    # and after every kernel of the step; the steps are captured in one CUDA graph like the
+    # timed loop (stream launches would add host dispatch gaps to the intervals)
     kern = decode_kernel_bytes(cfg)
     nk = 64
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kern) + 1)] for _ in range(nk)]
@@ -269,20 +269,33 @@ def main():
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
-    keep = []
-    pg = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(pg):
+
+    def profiled_steps():
+        keep = []
         for i in range(nk):
             ly = layers[i % NL]
             dh.copy_(ly["t"]["dout"])
-            evs[i][0].record()
-            keep.append(tlb.profile_events(evs[i][1:]))
+            keep.append(tlb.profile_events(evs[i]))
             tlb.layer_backward(c, 1, cfg.cache_len, ly["w"], ly["a"], ly["lq"], ly["lv"], adam, dh, ss, ws)
         tlb.profile_events(None)
-    pg.replay()
-    torch.cuda.synchronize()
-    ktime = [sum(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(nk)) / nk for k in range(len(kern))]
-    del keep, pg
+        return keep
+
+    try:
+        pg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pg):
+            keep = profiled_steps()
+        pg.replay()
+        torch.cuda.synchronize()
+        ktime = [sum(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(nk)) / nk for k in range(len(kern))]
+        ktiming = "graph"
+    except Exception:
+        torch.cuda.synchronize()
+        torch.cuda._sleep(200_000_000)      # queue the steps so they run back to back
+        keep = profiled_steps()
+        torch.cuda.synchronize()
+        ktime = [sum(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(nk)) / nk for k in range(len(kern))]
+        ktiming = "stream"
+    del keep
     pk = peaks()
     hbm = pk["hbm_gbs"] if pk else 6800.0
     per_kernel = [{"kernel": n, "us": t * 1e3, "bytes": b, "GB/s": b / (t / 1e3) / 1e9}
@@ -342,7 +355,7 @@ def main():
                              "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                              "algorithmic_bytes": kern[dom][1],
                              "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else "fallback"},
-                "per_kernel": per_kernel,
+                "per_kernel": per_kernel, "per_kernel_timing": ktiming,
                 "step_roofline": {"bytes_per_step": step_bytes, "achieved": step_bytes / (ms_max / args.steps / 1e3) / 1e9,
                                   "peak": hbm, "unit": "GB/s",
                                   "frac": step_bytes / (ms_max / args.steps / 1e3) / 1e9 / hbm},

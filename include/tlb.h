@@ -148,9 +148,11 @@ const char *tlb_build_info(void);
 /* Number of kernels this process has enqueued through the library so far (all threads). */
 uint64_t tlb_launch_count(void);
 /* Benchmarking aid.  With events != NULL, each later tlb_layer_backward call records
- * events[i] (cudaEvent_t passed as void*) on its stream right after its i-th kernel
- * launch, for i < n, so a caller can time the kernels of a layer one by one; NULL turns
- * it off.  Process-wide setting: do not use while other threads call the library. */
+ * (cudaEventRecordExternal, so it also works inside stream capture) events[0] on its
+ * stream before its first kernel and events[k + 1] right after its k-th kernel, for
+ * indices < n, so a caller can time the kernels of a layer one by one; NULL turns it off.
+ * Events are cudaEvent_t passed as void*.  Process-wide setting: do not use while other
+ * threads call the library. */
 void tlb_profile_events(void *const *events, int32_t n);
 
 /* ---------------------------------------------------------------- standalone steps */

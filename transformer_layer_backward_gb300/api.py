@@ -93,8 +93,9 @@ def launch_count() -> int:
 
 
 def profile_events(events):
-    """Record events[i] (torch.cuda.Event) after the i-th kernel of each later layer call;
-    None turns it off.  Returns the ctypes array, which must stay alive while in use."""
+    """events[0] (torch.cuda.Event) is recorded at the start of each later layer call and
+    events[k + 1] after its k-th kernel; None turns it off.  Returns the ctypes array,
+    which must stay alive while in use."""
     lib = A.load()
     if events is None:
         lib.tlb_profile_events(None, 0)

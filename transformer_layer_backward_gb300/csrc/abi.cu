@@ -16,8 +16,10 @@ static void *const *g_prof_events = nullptr;
 static int g_prof_n = 0;
 
 void profile_mark(int i, cudaStream_t st) {
-    if (g_prof_events != nullptr && i < g_prof_n)
-        cudaEventRecord(reinterpret_cast<cudaEvent_t>(g_prof_events[i]), st);
+    // external record: inside a stream capture this becomes an event node whose
+    // timestamps remain readable with cudaEventElapsedTime after the graph runs
+    if (g_prof_events != nullptr && i + 1 < g_prof_n && i >= -1)
+        cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(g_prof_events[i + 1]), st, cudaEventRecordExternal);
 }
 
 void set_error(const char *fmt, ...) {

@@ -42,7 +42,8 @@ void clear_error();
 // Error of the last launch on this thread (a launch error never enqueues work).
 int check_launch(const char *what);
 
-// Record the i-th profiling event (tlb_profile_events) on st, if profiling is on.
+// Record profiling event i + 1 (tlb_profile_events) on st, if profiling is on: i = -1 at
+// the start of a layer call, i = k after its k-th kernel.
 void profile_mark(int i, cudaStream_t st);
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
