@@ -188,9 +188,13 @@ int tlb_rope_backward(const float *dy, float *dx, int64_t rows, int32_t n_heads,
  * products; [RS] gemm_backward_a (C = A B^T with the weight stored pre-transposed):
  *   dX[S, in_dim] (+)= scale * dY[S, out_dim] . W[in_dim, out_dim]^T
  * W in storage type wtype (TLB_W_*); accumulate = 1 adds into dX.  S = 1 runs a GEMV;
- * S > 1 a GEMM (tensor cores for bf16 weights). */
+ * S > 1 a GEMM: for bf16 weights on the tcgen05 tensor cores (dY rounded to bf16, fp32
+ * accumulation), otherwise on CUDA cores in fp32.  ws: zero-filled workspace of at least
+ * tlb_linear_workspace_bytes() bytes (bf16 copy of dY and split-K partials). */
+size_t tlb_linear_workspace_bytes(int32_t wtype, int64_t S, int64_t out_dim, int64_t in_dim);
 int tlb_linear_backward(int32_t wtype, const void *W, float scale, const float *dY, int64_t S,
-                        int64_t out_dim, int64_t in_dim, float *dX, int32_t accumulate, void *stream);
+                        int64_t out_dim, int64_t in_dim, float *dX, int32_t accumulate, void *ws,
+                        size_t ws_bytes, void *stream);
 
 /* [RS] cpu_adamw on n parameters with learning rate cfg->lr * lr_mult.
  * If sumsq != NULL (device double), sum(g^2) is added to *sumsq. */

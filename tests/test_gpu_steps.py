@@ -5,7 +5,7 @@ import pytest
 
 from oracle import ops
 from synth import rng
-from tests.helpers import check, host
+from tests.helpers import BF16_REL_L2, check, host
 
 pytestmark = pytest.mark.gpu
 
@@ -116,7 +116,8 @@ def test_adamw(lib, n, step):
 
 @pytest.mark.parametrize("wtype", ["f32", "bf16", "ternary"])
 @pytest.mark.parametrize("S,in_dim,out_dim", [(1, 640, 2560), (1, 37, 50), (3, 100, 64), (130, 96, 272),
-                                              (1, 6912, 2560)])
+                                              (1, 6912, 2560), (256, 768, 1024), (130, 272, 4096),
+                                              (77, 640, 2560), (512, 2560, 9728), (512, 9728, 2560)])
 @pytest.mark.parametrize("accumulate", [False, True])
 def test_linear_backward(lib, wtype, S, in_dim, out_dim, accumulate):
     import torch
@@ -136,4 +137,8 @@ def test_linear_backward(lib, wtype, S, in_dim, out_dim, accumulate):
     out = dev(base.copy())
     lib.linear_backward(wtype, Wt, dev(dY), scale=1.25, out=out, accumulate=accumulate)
     ref = ops.linear_backward(dY, W, 1.25) + (base if accumulate else 0.0)
-    check("dX", host(out), ref)
+    if wtype == "bf16" and S > 1 and out_dim % 8 == 0 and in_dim % 4 == 0:
+        # tcgen05 path: dY rounded to bf16, fp32 accumulation
+        check("dX (tensor cores)", host(out), ref, BF16_REL_L2, None)
+    else:
+        check("dX", host(out), ref)

@@ -77,14 +77,22 @@ def rope_backward(dy, pos0, base=10000.0, out=None, stream=None):
     return out
 
 
-def linear_backward(wtype, W, dY, in_dim=None, scale=1.0, out=None, accumulate=False, stream=None):
+def linear_workspace(wtype, S, out_dim, in_dim, device="cuda"):
+    code = {"f32": A.W_F32, "bf16": A.W_BF16, "ternary": A.W_TERNARY_I8}[wtype]
+    n = int(A.load().tlb_linear_workspace_bytes(code, int(S), int(out_dim), int(in_dim)))
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def linear_backward(wtype, W, dY, scale=1.0, out=None, accumulate=False, ws=None, stream=None):
     """dX = scale * dY @ W^T for W stored [in, out] (wtype 'f32', 'bf16' or 'ternary')."""
     code = {"f32": A.W_F32, "bf16": A.W_BF16, "ternary": A.W_TERNARY_I8}[wtype]
     in_dim, out_dim = W.shape
     S = dY.shape[0]
     out = torch.zeros(S, in_dim, device=dY.device) if out is None else out
+    ws = linear_workspace(wtype, S, out_dim, in_dim, dY.device) if ws is None else ws
     A.call("tlb_linear_backward", code, _ptr(W, _WDTYPE[code], "W"), float(scale), _ptr(dY, name="dY"),
-           S, out_dim, in_dim, _ptr(out, name="out"), 1 if accumulate else 0, _stream(stream))
+           S, out_dim, in_dim, _ptr(out, name="out"), 1 if accumulate else 0,
+           _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
     return out
 
 

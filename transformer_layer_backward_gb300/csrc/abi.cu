@@ -105,15 +105,25 @@ void tlb_profile_events(void *const *events, int32_t n) {
     g_prof_n = events != nullptr && n > 0 ? n : 0;
 }
 
+size_t tlb_linear_workspace_bytes(int32_t wtype, int64_t S, int64_t out_dim, int64_t in_dim) {
+    if (S < 0 || out_dim < 0 || in_dim < 0) return 0;
+    return linear_ws_bytes(wtype, S, out_dim, in_dim);
+}
+
 int tlb_linear_backward(int32_t wtype, const void *W, float scale, const float *dY, int64_t S,
-                        int64_t out_dim, int64_t in_dim, float *dX, int32_t accumulate, void *stream) {
+                        int64_t out_dim, int64_t in_dim, float *dX, int32_t accumulate, void *ws,
+                        size_t ws_bytes, void *stream) {
     clear_error();
     TLB_REQUIRE(wtype == TLB_W_F32 || wtype == TLB_W_BF16 || wtype == TLB_W_TERNARY_I8, TLB_EINVAL,
                 "linear_backward: unknown weight type %d", wtype);
     TLB_REQUIRE(S >= 0 && out_dim >= 0 && in_dim >= 0, TLB_EINVAL, "linear_backward: negative size");
     if (S == 0 || in_dim == 0) return TLB_OK;
     TLB_REQUIRE(W && dX && (dY || out_dim == 0), TLB_EINVAL, "linear_backward: null pointer");
-    return linear_t_launch(wtype, W, scale, dY, S, out_dim, in_dim, dX, accumulate != 0, as_stream(stream));
+    const size_t need = linear_ws_bytes(wtype, S, out_dim, in_dim);
+    TLB_REQUIRE(ws != nullptr && ws_bytes >= need, TLB_EINVAL,
+                "linear_backward: workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
+    return linear_t_launch(wtype, W, scale, dY, S, out_dim, in_dim, dX, accumulate != 0, as_stream(stream), ws,
+                           ws_bytes);
 }
 
 int tlb_softmax_backward(const float *attn, const float *dattn, float *dscores, int64_t rows,

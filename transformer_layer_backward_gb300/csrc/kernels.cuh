@@ -22,12 +22,32 @@ int adamw_launch(float *p, const float *g, float *m, float *v, int64_t n, const 
 namespace tlb {
 
 // dX[S, in] (+)= scale * dY[S, out] . W[in, out]^T  (linear.cu)
+// With a workspace of linear_ws_bytes() (status block first), bf16 weights and S > 1 take
+// the tcgen05 path; otherwise (ws == nullptr allowed) the CUDA-core GEMM / GEMV.
 int linear_t_launch(int wtype, const void *W, float scale, const float *dY, int64_t S, int64_t out_dim,
-                    int64_t in_dim, float *dX, bool accumulate, cudaStream_t st);
-// Tensor-core path of the same product for bf16 weights; TLB_EUNSUPPORTED when the
-// shape or alignment does not fit it (the caller then uses the CUDA-core GEMM).
-int gemm_tc_try(const void *W, float scale, const float *dY, int64_t S, int64_t out_dim, int64_t in_dim,
-                float *dX, bool accumulate, cudaStream_t st);
+                    int64_t in_dim, float *dX, bool accumulate, cudaStream_t st, void *ws = nullptr,
+                    size_t ws_bytes = 0);
+size_t linear_ws_bytes(int wtype, int64_t S, int64_t out_dim, int64_t in_dim);
+// tcgen05 GEMM (gemm_tc.cu): out[M, N] (+)= alpha * sum_seg A_seg[M, K_seg] . B_seg[N, K_seg]^T,
+// A and B bf16 row-major (K-major), 16-byte aligned, K_seg % 8 == 0.
+constexpr int kMaxSplits = 8;
+struct TcOperand {
+    const void *a;   // bf16 [M, K]
+    const void *b;   // bf16 [N, K]
+    int64_t K;
+};
+struct TcPlan {
+    int bn, splits;
+};
+TcPlan tc_plan(int64_t M, int64_t N, int64_t K);
+bool tc_supported(int64_t M, int64_t N, int64_t K);
+size_t tc_partial_bytes(int64_t M, int64_t N, int64_t K);   // split-K scratch for (M, N, K)
+int tc_convert_bf16(const float *x, void *y, int64_t n, cudaStream_t st);
+int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, float *out, bool accumulate,
+            float *partial, uint32_t *status, cudaStream_t st);
+// gated-activation backward writing bf16 dG, dU (rowwise.cu)
+int act_backward_bf16_launch(int act, const float *gate, const float *up, const float *silu_gate, const float *dh,
+                             void *dgate, void *dup, int64_t n, cudaStream_t st);
 
 // Attention backward from dCtx to dQ(pre) and dV (attention.cu).
 struct AttnArgs {

@@ -6,21 +6,40 @@
 #include "kernels.cuh"
 #include "decode.cuh"
 
+#include <algorithm>
+
 namespace tlb {
 
 namespace {
 
 struct LayerWs {
     size_t dF, dG, dU, dN2, dSub, dqpre, dv, gh_q, gh_v;
+    size_t abf, gbf, ubf, part;               // tensor-core path: bf16 A operands, split-K partials
     size_t dR1, Upart, Wpart, Dpart, gh2, part1, part2, part3, gbar, pp;   // single-token path
     size_t total;
 };
+
+// The sequence FFN / O-projection products run on tcgen05 when the weights are bf16.
+bool tc_route(const tlb_layer_cfg &c, int64_t S) {
+    const int64_t I = c.ffn_dim, H = c.dim, qd = int64_t(c.n_heads) * c.head_dim;
+    return c.wtype == TLB_W_BF16 && S > 1 && tc_supported(S, I, H) && tc_supported(S, H, 2 * I) &&
+           tc_supported(S, qd, H) && I % 8 == 0;
+}
 
 LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     WsPlan p;
     LayerWs w;
     const int64_t I = c.ffn_dim, H = c.dim, qd = int64_t(c.n_heads) * c.head_dim;
     const int64_t kvd = int64_t(c.n_kv_heads) * c.head_dim;
+    if (tc_route(c, S)) {
+        w.abf = p.take(S * H * 2);            // dOut, later dR1, in bf16
+        w.gbf = p.take(S * I * 2);            // dG in bf16
+        w.ubf = p.take(S * I * 2);            // dU in bf16
+        w.part = p.take(std::max({tc_partial_bytes(S, I, H), tc_partial_bytes(S, H, 2 * I),
+                                  tc_partial_bytes(S, qd, H), size_t(256)}));
+    } else {
+        w.abf = w.gbf = w.ubf = w.part = 0;
+    }
     w.dF = p.take(S * I * 4);
     w.dG = p.take(S * I * 4);
     w.dU = p.take(S * I * 4);
@@ -78,6 +97,32 @@ int ffn_impl(const tlb_layer_cfg &c, int64_t S, const float *d_out, const tlb_la
     const LayerWs p = plan(c, S, S);   // the FFN regions do not depend on L
     const int64_t I = c.ffn_dim, H = c.dim;
     float *dF = ws_at<float>(ws, p.dF), *dG = ws_at<float>(ws, p.dG), *dU = ws_at<float>(ws, p.dU);
+    if (tc_route(c, S) && w.w_gate.scale == w.w_up.scale) {
+        uint32_t *status = ws_at<uint32_t>(ws, 0);
+        float *part = ws_at<float>(ws, p.part);
+        void *abf = ws_at<void>(ws, p.abf), *gbf = ws_at<void>(ws, p.gbf), *ubf = ws_at<void>(ws, p.ubf);
+        // dF = dOut W_down^T on the tensor cores (dOut rounded to bf16)
+        TLB_TRY(tc_convert_bf16(d_out, abf, S * H, st));
+        const TcOperand down{abf, w.w_down.w, H};
+        TLB_TRY(tc_gemm(&down, 1, S, I, w.w_down.scale, dF, false, part, status, st));
+        if (c.flags & TLB_SUB_NORM)
+            TLB_TRY(rmsnorm_backward_launch(a.hidden, w.gamma_sub_ffn, dF, dF, S, I, c.norm_eps, 0, st));
+        // dG, dU straight to bf16: the A operand of [W_gate | W_up]^T
+        const float *sg = (c.act == TLB_ACT_SILU_MUL && (c.flags & TLB_USE_SILU_CACHE)) ? a.silu_gate : nullptr;
+        TLB_TRY(act_backward_bf16_launch(c.act, a.gate, a.up, sg, dF, gbf, ubf, S * I, st));
+        const TcOperand gu[2] = {{gbf, w.w_gate.w, I}, {ubf, w.w_up.w, I}};
+        const bool resid = (c.flags & TLB_RESIDUAL) != 0;
+        if (c.flags & TLB_PRE_NORM) {
+            float *dN2 = ws_at<float>(ws, p.dN2);
+            TLB_TRY(tc_gemm(gu, 2, S, H, w.w_gate.scale, dN2, false, part, status, st));
+            if (resid && d_res != d_out)
+                TLB_CUDA(cudaMemcpyAsync(d_res, d_out, size_t(S * H) * 4, cudaMemcpyDeviceToDevice, st));
+            return rmsnorm_backward_launch(a.r1, w.gamma_ffn, dN2, d_res, S, H, c.norm_eps, resid ? 1 : 0, st);
+        }
+        if (resid && d_res != d_out)
+            TLB_CUDA(cudaMemcpyAsync(d_res, d_out, size_t(S * H) * 4, cudaMemcpyDeviceToDevice, st));
+        return tc_gemm(gu, 2, S, H, w.w_gate.scale, d_res, resid, part, status, st);
+    }
     // dF = dOut W_down^T
     TLB_TRY(linear_t_launch(c.wtype, w.w_down.w, w.w_down.scale, d_out, S, H, I, dF, false, st));
     // dh = RMSNorm_bwd(hidden, gamma, dF) (sub-norm), in place
@@ -108,7 +153,14 @@ int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, co
     const int64_t qd = int64_t(c.n_heads) * c.head_dim;
     float *dSub = ws_at<float>(ws, p.dSub);
     // dSub = dR1 W_O^T
-    TLB_TRY(linear_t_launch(c.wtype, w.w_o.w, w.w_o.scale, dR1, S, c.dim, qd, dSub, false, st));
+    if (tc_route(c, S)) {
+        void *abf = ws_at<void>(ws, p.abf);
+        TLB_TRY(tc_convert_bf16(dR1, abf, S * c.dim, st));
+        const TcOperand o{abf, w.w_o.w, c.dim};
+        TLB_TRY(tc_gemm(&o, 1, S, qd, w.w_o.scale, dSub, false, ws_at<float>(ws, p.part), ws_at<uint32_t>(ws, 0), st));
+    } else {
+        TLB_TRY(linear_t_launch(c.wtype, w.w_o.w, w.w_o.scale, dR1, S, c.dim, qd, dSub, false, st));
+    }
     // dCtx = RMSNorm_bwd(ctx, gamma_sub_attn, dSub) (sub-norm), in place
     if (c.flags & TLB_SUB_NORM)
         TLB_TRY(rmsnorm_backward_launch(a.ctx, w.gamma_sub_attn, dSub, dSub, S, qd, c.norm_eps, 0, st));

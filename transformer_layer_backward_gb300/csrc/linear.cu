@@ -188,8 +188,14 @@ static int launch_gemm_simt(const float *A, const void *B, float *C, int M, int 
     return check_launch("gemm_nt_simt");
 }
 
+// Workspace of the tensor-core path: [status 256 B][bf16 copy of dY][split-K partials].
+size_t linear_ws_bytes(int wtype, int64_t S, int64_t out_dim, int64_t in_dim) {
+    if (wtype != TLB_W_BF16 || S <= 1 || !tc_supported(S, in_dim, out_dim)) return kStatusBytes;
+    return kStatusBytes + ((size_t(S) * out_dim * 2 + 255) & ~size_t(255)) + tc_partial_bytes(S, in_dim, out_dim);
+}
+
 int linear_t_launch(int wtype, const void *W, float scale, const float *dY, int64_t S, int64_t out_dim,
-                    int64_t in_dim, float *dX, bool accumulate, cudaStream_t st) {
+                    int64_t in_dim, float *dX, bool accumulate, cudaStream_t st, void *ws, size_t ws_bytes) {
     if (S == 0 || in_dim == 0) return TLB_OK;
     TLB_REQUIRE(S < (1 << 30) && out_dim < (1 << 30) && in_dim < (1 << 30), TLB_EUNSUPPORTED,
                 "linear backward: dimension >= 2^30");
@@ -201,9 +207,14 @@ int linear_t_launch(int wtype, const void *W, float scale, const float *dY, int6
             default: return launch_gemv<TLB_W_TERNARY_I8>(W, dY, dX, int(in_dim), int(out_dim), scale, acc, st);
         }
     }
-    if (wtype == TLB_W_BF16) {
-        const int rc = gemm_tc_try(W, scale, dY, S, out_dim, in_dim, dX, accumulate, st);
-        if (rc != TLB_EUNSUPPORTED) return rc;
+    if (wtype == TLB_W_BF16 && ws != nullptr && tc_supported(S, in_dim, out_dim) && aligned16(dY) &&
+        aligned16(W) && aligned16(dX) && ws_bytes >= linear_ws_bytes(wtype, S, out_dim, in_dim)) {
+        char *w = static_cast<char *>(ws);
+        void *a = w + kStatusBytes;
+        float *part = reinterpret_cast<float *>(w + kStatusBytes + ((size_t(S) * out_dim * 2 + 255) & ~size_t(255)));
+        TLB_TRY(tc_convert_bf16(dY, a, S * out_dim, st));
+        const TcOperand op{a, W, out_dim};
+        return tc_gemm(&op, 1, S, in_dim, scale, dX, accumulate, part, reinterpret_cast<uint32_t *>(w), st);
     }
     switch (wtype) {
         case TLB_W_F32:

@@ -359,6 +359,51 @@ int act_backward_launch(int act, const float *gate, const float *up, const float
     return check_launch("act_backward");
 }
 
+// bf16 outputs (the A operands of the [W_gate | W_up]^T tensor-core GEMM)
+__device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    return make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+}
+
+template <int ACT, bool CACHE>
+__global__ void act_bwd_bf16_kernel(const float4 *__restrict__ gate, const float4 *__restrict__ up,
+                                    const float4 *__restrict__ sg, const float4 *__restrict__ dh,
+                                    uint2 *__restrict__ dgate, uint2 *__restrict__ dup, int64_t n4) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const float4 g = ld_stream(gate + i), u = ld_stream(up + i), d = ld_stream(dh + i);
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (CACHE) s = ld_stream(sg + i);
+        float4 og, ou;
+        act_bwd_elem<ACT, CACHE>(g.x, u.x, s.x, d.x, og.x, ou.x);
+        act_bwd_elem<ACT, CACHE>(g.y, u.y, s.y, d.y, og.y, ou.y);
+        act_bwd_elem<ACT, CACHE>(g.z, u.z, s.z, d.z, og.z, ou.z);
+        act_bwd_elem<ACT, CACHE>(g.w, u.w, s.w, d.w, og.w, ou.w);
+        dgate[i] = pack_bf16x4(og.x, og.y, og.z, og.w);
+        dup[i] = pack_bf16x4(ou.x, ou.y, ou.z, ou.w);
+    }
+}
+
+int act_backward_bf16_launch(int act, const float *gate, const float *up, const float *silu_gate, const float *dh,
+                             void *dgate, void *dup, int64_t n, cudaStream_t st) {
+    if (n == 0) return TLB_OK;
+    const bool cache = silu_gate != nullptr && act == TLB_ACT_SILU_MUL;
+    TLB_REQUIRE(n % 4 == 0 && aligned16(gate) && aligned16(up) && aligned16(dh) && aligned16(dgate) &&
+                    aligned16(dup) && (!cache || aligned16(silu_gate)),
+                TLB_EUNSUPPORTED, "act_backward (bf16 out): n %% 4 or alignment");
+    const unsigned grid = stream_grid(n / 4, 256);
+    const float4 *g4 = reinterpret_cast<const float4 *>(gate), *u4 = reinterpret_cast<const float4 *>(up);
+    const float4 *s4 = reinterpret_cast<const float4 *>(silu_gate), *d4 = reinterpret_cast<const float4 *>(dh);
+    uint2 *og = reinterpret_cast<uint2 *>(dgate), *ou = reinterpret_cast<uint2 *>(dup);
+    if (act == TLB_ACT_RELU2_MUL)
+        act_bwd_bf16_kernel<TLB_ACT_RELU2_MUL, false><<<grid, 256, 0, st>>>(g4, u4, nullptr, d4, og, ou, n / 4);
+    else if (cache)
+        act_bwd_bf16_kernel<TLB_ACT_SILU_MUL, true><<<grid, 256, 0, st>>>(g4, u4, s4, d4, og, ou, n / 4);
+    else
+        act_bwd_bf16_kernel<TLB_ACT_SILU_MUL, false><<<grid, 256, 0, st>>>(g4, u4, nullptr, d4, og, ou, n / 4);
+    return check_launch("act_backward_bf16");
+}
+
 // ------------------------------------------------------------------ RoPE backward
 
 // One thread per (row, head, d) with d < head_dim/2: rotates the pair (d, d + half).
