@@ -8,12 +8,12 @@ library has not been built.
 from . import _abi
 from ._abi import TlbError, load
 from .api import (act_backward, adamw, adamw_cfg, attn_backward, ffn_backward, layer_acts,
-                  layer_backward, layer_cfg, layer_weights, launch_count, linear_backward, lora,
+                  layer_backward, layer_cfg, layer_weights, launch_count, linear_backward, linear_workspace, lora,
                   lora_grad_adamw, lora_grad_adamw_noalloc, profile_events,
                   rmsnorm_backward, rope_backward, softmax_backward, workspace, workspace_bytes,
                   workspace_status)
 
 __all__ = ["TlbError", "load", "act_backward", "adamw", "adamw_cfg", "attn_backward",
-           "ffn_backward", "layer_acts", "layer_backward", "layer_cfg", "layer_weights", "launch_count", "linear_backward", "lora",
+           "ffn_backward", "layer_acts", "layer_backward", "layer_cfg", "layer_weights", "launch_count", "linear_backward", "linear_workspace", "lora",
            "lora_grad_adamw", "lora_grad_adamw_noalloc", "profile_events", "rmsnorm_backward", "rope_backward", "softmax_backward",
            "workspace", "workspace_bytes", "workspace_status", "_abi"]
