@@ -2,7 +2,8 @@
 // ([ATT] "Gradient Flow", apply / softmax / score / RoPE backward; [RS]
 // backward_through_layers, attention block).
 //
-// General kernels (any S, L, strides):
+// Sequence kernels (S > 1, head_dim 32/64/128): attn_dq_tiled and attn_dv_tiled below.
+// General kernels (any S, L, strides; decode rows and other head sizes):
 //   attn_rows_kernel  one block per (query row i, head h):
 //       dAttn[j] = dCtx[i,h,:] . V[kvh, j, :]                (apply backward)
 //       D        = sum_j attn[h,i,j] dAttn[j]
@@ -81,10 +82,245 @@ __global__ void attn_dv_kernel(AttnArgs a) {
     }
 }
 
+// ------------------------------------------------------------------ tiled kernels
+
+// Tiled fp32 attention backward (64 x 64 tiles, 256 threads, 4 x 4 register tiles).
+//   attn_dq_tiled: block = (64 query rows, head h).  Pass 1 runs dAttn = dCtx V^T tile by
+//     tile and accumulates the row sums D = sum_j P dAttn; pass 2 recomputes dAttn, forms
+//     dS = scale P (dAttn - D) and accumulates dQ += dS K; RoPE backward in the epilogue.
+//   attn_dv_tiled: block = (64 of the S newest keys, KV head): dV = sum_group P^T dCtx.
+// With TLB_CAUSAL, key tiles past the last visible key of a query tile are skipped and the
+// masked entries inside a diagonal tile are read as zero, as in the per-row kernels.
+constexpr int kT = 64;          // tile edge
+constexpr int kTP = kT + 4;     // padded row of a transposed tile (float4-aligned, 4-way store conflicts)
+
+template <int HD>
+__global__ void __launch_bounds__(256) attn_dq_tiled(AttnArgs a, RopeFreqs fr) {
+    extern __shared__ float4 sm4[];
+    float *sCt = reinterpret_cast<float *>(sm4);        // [HD][kTP]   dCtx tile, transposed
+    float *sVt = sCt + HD * kTP;                        // [HD][kTP]   V tile, transposed
+    float *sK = sVt + HD * kTP;                         // [kT][HD+4]  K tile
+    float *sSt = sK + kT * (HD + 4);                    // [kT][kTP]   dS tile, transposed
+    __shared__ float sD[kT];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int h = blockIdx.y, kvh = h / (a.nh / a.nkv);
+    const int q0 = blockIdx.x * kT;
+    const int q_dim = a.nh * HD;
+    const int jend = a.causal ? min(a.L, a.pos0 + q0 + kT) : a.L;
+    const int nkt = (jend + kT - 1) / kT;
+    const float *Vh = a.v + int64_t(kvh) * a.sh, *Kh = a.k + int64_t(kvh) * a.sh;
+    const float *Ph = a.attn + int64_t(h) * a.S * a.L;
+    // dCtx tile, transposed
+    for (int e = tid; e < kT * HD; e += 256) {
+        const int i = e / HD, d = e % HD;
+        sCt[d * kTP + i] = (q0 + i < a.S) ? a.dctx[int64_t(q0 + i) * q_dim + h * HD + d] : 0.f;
+    }
+    auto load_vt = [&](int j0) {
+        for (int e = tid; e < kT * HD; e += 256) {
+            const int j = e / HD, d = e % HD;
+            sVt[d * kTP + j] = (j0 + j < a.L) ? Vh[int64_t(j0 + j) * a.sp + d] : 0.f;
+        }
+    };
+    // dAttn micro-tile rows 4ty.., cols 4tx.. of the current key tile
+    auto dattn_tile = [&](float (&acc)[4][4]) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+#pragma unroll 4
+        for (int d = 0; d < HD; ++d) {
+            const float4 cv = *reinterpret_cast<const float4 *>(sCt + d * kTP + 4 * ty);
+            const float4 vv = *reinterpret_cast<const float4 *>(sVt + d * kTP + 4 * tx);
+            const float cr[4] = {cv.x, cv.y, cv.z, cv.w}, vc[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(cr[r], vc[c], acc[r][c]);
+        }
+    };
+    auto load_p = [&](int j0, float (&pv)[4][4]) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = q0 + 4 * ty + r;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int j = j0 + 4 * tx + c;
+                const bool vis = i < a.S && j < a.L && (!a.causal || j <= a.pos0 + i);
+                pv[r][c] = vis ? Ph[int64_t(i) * a.L + j] : 0.f;
+            }
+        }
+    };
+    // ---------------- pass 1: D
+    float dp[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int kt = 0; kt < nkt; ++kt) {
+        __syncthreads();
+        load_vt(kt * kT);
+        __syncthreads();
+        float acc[4][4], pv[4][4];
+        dattn_tile(acc);
+        load_p(kt * kT, pv);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) dp[r] = fmaf(pv[r][c], acc[r][c], dp[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        float v = dp[r];
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);   // the 16 tx of this ty
+        if (tx == 0) sD[4 * ty + r] = v;
+    }
+    // ---------------- pass 2: dS and dQ
+    constexpr int CPT = HD / 16;                 // dQ columns per thread
+    float dq[4][CPT];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) dq[r][c] = 0.f;
+    for (int kt = 0; kt < nkt; ++kt) {
+        const int j0 = kt * kT;
+        __syncthreads();
+        load_vt(j0);
+        for (int e = tid; e < kT * HD; e += 256) {
+            const int j = e / HD, d = e % HD;
+            sK[j * (HD + 4) + d] = (j0 + j < a.L) ? Kh[int64_t(j0 + j) * a.sp + d] : 0.f;
+        }
+        __syncthreads();
+        float acc[4][4], pv[4][4];
+        dattn_tile(acc);
+        load_p(j0, pv);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                sSt[(4 * tx + c) * kTP + 4 * ty + r] = a.scale * pv[r][c] * (acc[r][c] - sD[4 * ty + r]);
+        __syncthreads();
+#pragma unroll 4
+        for (int j = 0; j < kT; ++j) {
+            const float4 sv = *reinterpret_cast<const float4 *>(sSt + j * kTP + 4 * ty);
+            const float sr[4] = {sv.x, sv.y, sv.z, sv.w};
+            float kv[CPT];
+#pragma unroll
+            for (int c = 0; c < CPT; c += 2) {
+                const float2 t = *reinterpret_cast<const float2 *>(sK + j * (HD + 4) + tx * CPT + c);
+                kv[c] = t.x;
+                kv[c + 1] = t.y;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < CPT; ++c) dq[r][c] = fmaf(sr[r], kv[c], dq[r][c]);
+        }
+    }
+    // ---------------- epilogue: RoPE backward through shared memory (pairs d, d + HD/2)
+    __syncthreads();
+    float *sQ = sK;                                   // [kT][HD+4]
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) sQ[(4 * ty + r) * (HD + 4) + tx * CPT + c] = dq[r][c];
+    __syncthreads();
+    constexpr int half = HD / 2;
+    for (int e = tid; e < kT * half; e += 256) {
+        const int i = e / half, d = e % half;
+        if (q0 + i >= a.S) continue;
+        float y1 = sQ[i * (HD + 4) + d], y2 = sQ[i * (HD + 4) + d + half];
+        if (a.rope) {
+            float cs, sn;
+            rope_cos_sin(float(a.pos0 + q0 + i), fr.hi[d], fr.lo[d], cs, sn);
+            const float t1 = y1 * cs + y2 * sn, t2 = -y1 * sn + y2 * cs;
+            y1 = t1;
+            y2 = t2;
+        }
+        float *out = a.dq + int64_t(q0 + i) * q_dim + h * HD;
+        out[d] = y1;
+        out[d + half] = y2;
+    }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(256) attn_dv_tiled(AttnArgs a) {
+    extern __shared__ float4 sm4[];
+    float *sP = reinterpret_cast<float *>(sm4);         // [kT][kTP]   P tile [query][key]
+    float *sC = sP + kT * kTP;                          // [kT][HD+4]  dCtx tile
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int kvh = blockIdx.y, G = a.nh / a.nkv;
+    const int k0 = blockIdx.x * kT;                     // among the S newest keys
+    const int q_dim = a.nh * HD;
+    constexpr int CPT = HD / 16;
+    float dv[4][CPT];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) dv[r][c] = 0.f;
+    // query i sees key pos0 + jj iff i >= jj: query tiles from the one holding row k0
+    const int qt0 = a.causal ? k0 / kT : 0;
+    const int nqt = (a.S + kT - 1) / kT;
+    for (int g = 0; g < G; ++g) {
+        const int h = kvh * G + g;
+        const float *Ph = a.attn + int64_t(h) * a.S * a.L + a.pos0;
+        for (int qt = qt0; qt < nqt; ++qt) {
+            const int q0 = qt * kT;
+            __syncthreads();
+            for (int e = tid; e < kT * kT; e += 256) {
+                const int i = e / kT, j = e % kT;
+                const bool vis = q0 + i < a.S && k0 + j < a.S && (!a.causal || q0 + i >= k0 + j);
+                sP[i * kTP + j] = vis ? Ph[int64_t(q0 + i) * a.L + k0 + j] : 0.f;
+            }
+            for (int e = tid; e < kT * HD; e += 256) {
+                const int i = e / HD, d = e % HD;
+                sC[i * (HD + 4) + d] = (q0 + i < a.S) ? a.dctx[int64_t(q0 + i) * q_dim + h * HD + d] : 0.f;
+            }
+            __syncthreads();
+#pragma unroll 4
+            for (int i = 0; i < kT; ++i) {
+                const float4 pv = *reinterpret_cast<const float4 *>(sP + i * kTP + 4 * ty);
+                const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
+                float cv[CPT];
+#pragma unroll
+                for (int c = 0; c < CPT; c += 2) {
+                    const float2 t = *reinterpret_cast<const float2 *>(sC + i * (HD + 4) + tx * CPT + c);
+                    cv[c] = t.x;
+                    cv[c + 1] = t.y;
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < CPT; ++c) dv[r][c] = fmaf(pr[r], cv[c], dv[r][c]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int jj = k0 + 4 * ty + r;
+        if (jj >= a.S) continue;
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) a.dv[int64_t(jj) * a.nkv * HD + kvh * HD + tx * CPT + c] = dv[r][c];
+    }
+}
+
+template <int HD>
+int launch_tiled(const AttnArgs &a, const RopeFreqs &fr, cudaStream_t st) {
+    const size_t smq = (size_t(2) * HD * kTP + size_t(kT) * (HD + 4) + size_t(kT) * kTP) * 4;
+    const size_t smv = (size_t(kT) * kTP + size_t(kT) * (HD + 4)) * 4;
+    if (smq > 48 * 1024) TLB_CUDA(cudaFuncSetAttribute(attn_dq_tiled<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smq)));
+    if (smv > 48 * 1024) TLB_CUDA(cudaFuncSetAttribute(attn_dv_tiled<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smv)));
+    attn_dq_tiled<HD><<<dim3(unsigned(ceil_div(a.S, kT)), unsigned(a.nh)), 256, smq, st>>>(a, fr);
+    TLB_TRY(check_launch("attn_dq_tiled"));
+    attn_dv_tiled<HD><<<dim3(unsigned(ceil_div(a.S, kT)), unsigned(a.nkv)), 256, smv, st>>>(a);
+    return check_launch("attn_dv_tiled");
+}
+
 int attn_core_launch(const AttnArgs &a, float rope_base, cudaStream_t st) {
     if (a.S == 0) return TLB_OK;
     RopeFreqs fr;
     rope_freqs(fr, a.hd, rope_base);
+    if (a.S > 1) {
+        if (a.hd == 128) return launch_tiled<128>(a, fr, st);
+        if (a.hd == 64) return launch_tiled<64>(a, fr, st);
+        if (a.hd == 32) return launch_tiled<32>(a, fr, st);
+    }
     const size_t smem = (size_t(a.L) + 2 * size_t(a.hd)) * sizeof(float);
     TLB_REQUIRE(smem <= 200 * 1024, TLB_EUNSUPPORTED, "attn_backward: cache length %d too long", a.L);
     if (smem > 48 * 1024)
