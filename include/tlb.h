@@ -237,13 +237,16 @@ int tlb_attn_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const floa
  *   dB = s G^T h [out, r];  gh = s G B_old [S, r];  dA = gh^T x [r, in]
  *   then AdamW on A (lr) and B (lr * lr_b_mult); B is read before it is updated.
  * G [S, out_dim], h [S, rank], x [S, in_dim].  sumsq (device double[2], may be NULL)
- * += {sum dA^2, sum dB^2}. */
+ * += {sum dA^2, sum dB^2}.  S = 0 is a no-op (no gradient, no step).  ws: at least
+ * tlb_workspace_bytes of a layer with this rank, dim >= in_dim and q_dim >= out_dim,
+ * 256-byte aligned; it holds partial sums over 64-token tiles. */
 int tlb_lora_grad_adamw(int64_t S, int32_t out_dim, int32_t in_dim, int32_t rank, float alpha,
                         const float *G, const float *h, const float *x, const tlb_lora *lora,
                         const tlb_adamw_cfg *adam, double *sumsq, void *ws, size_t ws_bytes,
                         void *stream);
 
-/* Same result as tlb_lora_grad_adamw, for callers that cannot allocate device memory
+/* Same result as tlb_lora_grad_adamw (up to float rounding: its sums over S run per
+ * element rather than in tiles), for callers that cannot allocate device memory
  * and so have no workspace to pass (for example code running under an allocator it
  * does not control, or where a cudaMalloc would synchronise the device).  The pages
  * have no counterpart: it exists only for such callers.  Its one scratch buffer, the

@@ -67,4 +67,16 @@ int lora_launch(int64_t S, int out_dim, int in_dim, int rank, float alpha, const
                 const float *x, const tlb_lora &l, const tlb_adamw_cfg &adam, double *sumsq, float *gh,
                 cudaStream_t st);
 
+// Tiled LoRA gradients + AdamW (lora.cu) for one or two adapters that share x [S, in_dim].
+// scratch: lora_seq_bytes(S, out_dim, in_dim, rank) bytes per adapter, 256-byte aligned.
+struct LoraJob {
+    const float *G, *h;     // [S, out_dim], [S, rank]
+    int out_dim;
+    tlb_lora l;
+    void *scratch;
+};
+size_t lora_seq_bytes(int64_t S, int out_dim, int in_dim, int rank);
+int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x, const LoraJob *jobs, int njobs,
+                    const tlb_adamw_cfg &adam, double *sumsq, cudaStream_t st);
+
 }  // namespace tlb

@@ -13,7 +13,7 @@ namespace tlb {
 namespace {
 
 struct LayerWs {
-    size_t dF, dG, dU, dN2, dSub, dqpre, dv, gh_q, gh_v;
+    size_t dF, dG, dU, dN2, dSub, dqpre, dv, lora_q, lora_v;   // lora_*: tiled LoRA partial sums
     size_t abf, gbf, ubf, part;               // tensor-core path: bf16 A operands, split-K partials
     size_t dR1, Upart, Wpart, Dpart, gh2, part1, part2, part3, gbar, pp;   // single-token path
     size_t total;
@@ -47,8 +47,8 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     w.dSub = p.take(S * qd * 4);
     w.dqpre = p.take(S * qd * 4);
     w.dv = p.take(S * kvd * 4);
-    w.gh_q = p.take(S * c.rank * 4);
-    w.gh_v = p.take(S * c.rank * 4);
+    w.lora_q = p.take(lora_seq_bytes(S, int(qd), int(H), c.rank));
+    w.lora_v = p.take(lora_seq_bytes(S, int(kvd), int(H), c.rank));
     if (S == 1) {
         const int64_t nchunks = ceil_div(L, 32);   // the finer of the two attention chunkings
         w.dR1 = p.take(H * 4);
@@ -268,13 +268,12 @@ int tlb_lora_grad_adamw(int64_t S, int32_t out_dim, int32_t in_dim, int32_t rank
     TLB_TRY(check_lora(lora, "(lora_grad_adamw)"));
     TLB_TRY(check_adam(adam));
     TLB_REQUIRE(S == 0 || (G && h && x), TLB_EINVAL, "lora_grad_adamw: NULL input");
-    const size_t need = kStatusBytes + ((size_t(S) * rank * 4 + 255) & ~size_t(255));
+    if (S == 0) return TLB_OK;   // no tokens: no gradient and no step, as in tlb_layer_backward
+    const size_t need = kStatusBytes + lora_seq_bytes(S, out_dim, in_dim, rank);
     TLB_REQUIRE(ws && ws_bytes >= need, TLB_EINVAL, "lora_grad_adamw: workspace smaller than %zu bytes", need);
-    if (S == 0) {
-        // no rows: zero gradients, AdamW still decays and moves the moments
-    }
-    float *gh = ws_at<float>(ws, kStatusBytes);
-    return lora_launch(S, out_dim, in_dim, rank, alpha, G, h, x, *lora, *adam, sumsq, gh, as_stream(stream));
+    TLB_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, TLB_EINVAL, "workspace not 256-byte aligned");
+    const LoraJob job{G, h, out_dim, *lora, ws_at<void>(ws, kStatusBytes)};
+    return lora_seq_launch(S, in_dim, rank, alpha, x, &job, 1, *adam, sumsq, as_stream(stream));
 }
 
 int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb_layer_weights *w,
@@ -387,10 +386,9 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
     }
     TLB_TRY(ffn_impl(c, S, d_hidden, *w, *acts, d_hidden, ws, st));
     TLB_TRY(attn_impl(c, S, L, d_hidden, *w, *acts, dqpre, dv, ws, st));
-    TLB_TRY(lora_launch(S, qd, c.dim, c.rank, c.lora_alpha, dqpre, acts->lora_q_h, acts->x, *lora_q, *adam,
-                        sumsq, ws_at<float>(ws, p.gh_q), st));
-    return lora_launch(S, kvd, c.dim, c.rank, c.lora_alpha, dv, acts->lora_v_h, acts->x, *lora_v, *adam, sumsq,
-                       ws_at<float>(ws, p.gh_v), st);
+    const LoraJob jobs[2] = {{dqpre, acts->lora_q_h, qd, *lora_q, ws_at<void>(ws, p.lora_q)},
+                             {dv, acts->lora_v_h, kvd, *lora_v, ws_at<void>(ws, p.lora_v)}};
+    return lora_seq_launch(S, c.dim, c.rank, c.lora_alpha, acts->x, jobs, 2, *adam, sumsq, st);
 }
 
 }  // extern "C"

@@ -5,10 +5,11 @@
 // or a memory pool already fully committed to model state), plugins loaded into a
 // host process that forbids device allocations after start-up, and code running
 // inside a region where a cudaMalloc would synchronise the device and stall other
-// work.  tlb_lora_grad_adamw_noalloc serves them: it computes exactly what
-// tlb_lora_grad_adamw computes, but its only scratch buffer (the [S, rank] rows
-// gh = s G B_old) lives in a fixed array inside this library instead of in a
-// caller workspace.
+// work.  tlb_lora_grad_adamw_noalloc serves them: it computes what
+// tlb_lora_grad_adamw computes (the same sums, reduced per element over S instead
+// of in tiles, so equal up to float rounding), but its only scratch buffer (the
+// [S, rank] rows gh = s G B_old) lives in a fixed array inside this library instead
+// of in a caller workspace.
 #include <mutex>
 
 #include "common.cuh"
