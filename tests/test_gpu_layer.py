@@ -2,8 +2,8 @@
 of the whole layer / stack against the float64 oracle on the same seeded inputs.
 
 Configurations: the tiny fp32 layer (all norms, RoPE, GQA, causal), the
-single-token decode layer with ternary weights, a small bf16 sequence layer with
-a ragged sequence length, and the S = 512 SwiGLU layer.
+single-token decode layer with ternary weights, small bf16 sequence layers with
+ragged sequence and cache lengths, and the S = 512 SwiGLU layer.
 """
 import numpy as np
 import pytest
@@ -28,7 +28,14 @@ DEC_G8 = DECODE.with_(name="dec_g8_hd32", dim=256, ffn_dim=256, n_heads=16, n_kv
                       rank=8, lora_alpha=16.0, cache_len=40, pre_norm=False)
 DEC_HD256 = DECODE.with_(name="dec_hd256", dim=512, ffn_dim=1024, n_heads=4, n_kv_heads=1, head_dim=256,
                          cache_len=65, sub_norm=False, rope=True)
-CASES = {c.name: c for c in (TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512, DEC_F32, DEC_BF16, DEC_G8, DEC_HD256)}
+# bf16 sequence layers on the tensor-core attention: head_dim 64 with S ragged over both
+# tile sizes; a cache longer than the sequence (L not a multiple of 4, 4-head groups)
+SEQ_HD64 = SEQ512.with_(name="seq_hd64", dim=512, ffn_dim=1024, n_heads=8, n_kv_heads=2, head_dim=64,
+                        rank=8, lora_alpha=16.0, seq_len=200, cache_len=200)
+SEQ_CACHE = SEQ512.with_(name="seq_cache", dim=512, ffn_dim=768, n_heads=4, n_kv_heads=1, head_dim=128,
+                         seq_len=96, cache_len=301, adam_state="warm", step=4)
+CASES = {c.name: c for c in (TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512, DEC_F32, DEC_BF16, DEC_G8, DEC_HD256,
+                             SEQ_HD64, SEQ_CACHE)}
 
 
 def tol(cfg):

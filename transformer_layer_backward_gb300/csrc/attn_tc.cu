@@ -1,0 +1,626 @@
+// Tensor-core attention backward for sequences ([ATT] "Gradient Flow": apply, softmax,
+// score and RoPE backward; [RS] backward_through_layers, attention block), with tf32
+// operands and fp32 accumulation in tensor memory.  GQA: kvh = h / (nh / nkv).
+//
+//   attn_tc_prep  tf32-rounded copies laid out for TMA (32 x 32 tile transposes):
+//                   dCr [nh][S][hd]   dCT [nh][hd][S4]   Kt [nkv][hd][L4]   Vr [nkv][L][hd]
+//   attn_tc_dq    CTA = (head h, 128 queries), 6 warps: TMA producer, MMA issuer, and
+//                 4 epilogue warps (one query row per thread = one TMEM lane).  Per tile
+//                 of 64 keys j:
+//                   T  = dCtx_h V_j^T                        tcgen05.mma, T in TMEM
+//                   E  = P (.) T,  D += rowsum(E)            epilogue, fp32
+//                   U += E K_j,    W += P K_j                tcgen05.mma (E, P tf32 in smem)
+//                 then dQ = scale (U - D W), which equals scale sum_j P (T - D) K_j with D
+//                 the literal row sum of P (.) dAttn, and RoPE backward on the way out.
+//   attn_tc_dv    CTA = (KV head, 128 of the S newest keys): over the group's heads and
+//                 64-query tiles, dV += P^T dCtx_h.  The epilogue warps write P^T (tf32,
+//                 K-major) into shared memory; dCtx^T tiles come by TMA.
+// All MMAs: M = 128, K = 8 per instruction, both operands K-major with 128-byte swizzle.
+// Causal: key tiles past a query tile's last visible key are skipped; masked entries of
+// P inside a diagonal tile read as zero.  Every mbarrier wait is bounded.
+#include <cuda.h>
+
+#include <cstring>
+
+#include "async.cuh"
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tc.cuh"
+
+namespace tlb {
+
+namespace {
+
+constexpr int kQM = 128;        // queries per dQ CTA
+constexpr int kQK = 64;         // keys per dQ tile
+constexpr int kVK = 128;        // keys per dV CTA
+constexpr int kVQ = 64;         // queries per dV tile
+constexpr int kAttnThreads = 192;
+
+struct AttnTcParams {
+    CUtensorMap dc;             // dCr  {hd, S, nh},  box {32, 128, 1}
+    CUtensorMap v;              // Vr   {hd, L, nkv}, box {32, 64, 1}
+    CUtensorMap kt;             // Kt   {L, hd, nkv}, box {32, hd, 1}
+    CUtensorMap dct;            // dCT  {S, hd, nh},  box {32, hd, 1}
+    const float *attn;          // [nh, S, L]
+    float *dq;                  // [S, nh * hd]
+    float *dv;                  // [S, nkv * hd]
+    int S, L, nh, nkv, pos0, causal, rope, vecP;
+    float scale;
+    uint32_t *status;
+    RopeFreqs fr;
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint8_t *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// Byte offset of 16-byte chunk `ch` (0..7) of row r in a K-major 128-byte-swizzled box.
+__device__ __forceinline__ uint32_t sw128_off(int r, int ch) { return uint32_t(r) * 128u + (uint32_t(ch ^ (r & 7)) << 4); }
+
+// ------------------------------------------------------------------ prep
+
+// 32 x 32 tiles of three sources: dCtx [S, nh*hd] -> dCr, dCT;  K -> Kt;  V -> Vr.
+__global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dCr, float *dCT, float *Kt, float *Vr,
+                                                           int S4, int L4, int ntc_dc, int ntc_kv) {
+    __shared__ float tile[32][33];
+    const int qd = a.nh * a.hd, kvd = a.nkv * a.hd;
+    int t = blockIdx.x;
+    int job, rows, cols;
+    if (t < ntc_dc * ((a.S + 31) / 32)) {
+        job = 0;
+        rows = a.S;
+        cols = qd;
+    } else {
+        t -= ntc_dc * ((a.S + 31) / 32);
+        job = t / (ntc_kv * ((a.L + 31) / 32)) + 1;   // 1: K, 2: V
+        t %= ntc_kv * ((a.L + 31) / 32);
+        rows = a.L;
+        cols = kvd;
+    }
+    const int nct = cols / 32;
+    const int r0 = (t / nct) * 32, c0 = (t % nct) * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int rr = ty; rr < 32; rr += 8) {
+        const int r = r0 + rr, c = c0 + tx;
+        float v = 0.f;
+        if (r < rows) {
+            if (job == 0) v = a.dctx[int64_t(r) * qd + c];
+            else {
+                const int kvh = c / a.hd, d = c % a.hd;
+                v = (job == 1 ? a.k : a.v)[int64_t(kvh) * a.sh + int64_t(r) * a.sp + d];
+            }
+        }
+        v = __uint_as_float(to_tf32(v));
+        tile[rr][tx] = v;
+        if (r < rows) {
+            const int hh = c / a.hd, d = c % a.hd;
+            if (job == 0) dCr[(int64_t(hh) * a.S + r) * a.hd + d] = v;
+            else if (job == 2) Vr[(int64_t(hh) * a.L + r) * a.hd + d] = v;
+        }
+    }
+    if (job == 2) return;
+    __syncthreads();
+    // transposed: row = column c0 + cc (head, d), column = r0 + tx
+    for (int cc = ty; cc < 32; cc += 8) {
+        const int c = c0 + cc, r = r0 + tx;
+        if (r >= rows) continue;
+        const int hh = c / a.hd, d = c % a.hd;
+        if (job == 0) dCT[(int64_t(hh) * a.hd + d) * S4 + r] = tile[tx][cc];
+        else Kt[(int64_t(hh) * a.hd + d) * L4 + r] = tile[tx][cc];
+    }
+}
+
+// ------------------------------------------------------------------ dQ
+
+template <int HD>
+struct DqLayout {
+    static constexpr int NB = HD / 32;                   // 128-byte boxes along head_dim
+    static constexpr int DC = 0, DC_BYTES = kQM * HD * 4;
+    static constexpr int V0 = DC + DC_BYTES, V_BYTES = kQK * HD * 4;
+    static constexpr int KT = V0 + 2 * V_BYTES, KT_BYTES = HD * kQK * 4;
+    static constexpr int AE = KT + KT_BYTES, A_BYTES = kQM * kQK * 4;
+    static constexpr int AP = AE + A_BYTES;
+    static constexpr int TOTAL = AP + A_BYTES;
+    static constexpr uint32_t COLS = (128 + 2 * HD) <= 256 ? 256 : 512;   // T0 | T1 | U | W
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __grid_constant__ AttnTcParams p) {
+    using Ly = DqLayout<HD>;
+    constexpr int NB = Ly::NB;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    __shared__ uint64_t vfull[2], vempty[2], tfull[2], tempty[2], ktfull, afull, aempty, ufull;
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_abort, s_v_issued, s_v_used, s_kt_issued, s_kt_used;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y, kvh = h / (p.nh / p.nkv);
+    const int q0 = int(gridDim.x - 1 - blockIdx.x) * kQM;       // latest (longest) query tiles first
+    const int kend = p.causal ? min(p.L, p.pos0 + q0 + kQM) : p.L;
+    const int nt = (kend + kQK - 1) / kQK;
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        s_v_issued = s_v_used = s_kt_issued = s_kt_used = 0;
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&vfull[s], 1);
+            mbar_init(&vempty[s], 1);
+            mbar_init(&tfull[s], 1);
+            mbar_init(&tempty[s], 4);
+        }
+        mbar_init(&ktfull, 1);
+        mbar_init(&afull, 4);
+        mbar_init(&aempty, 1);
+        mbar_init(&ufull, 1);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, Ly::COLS);
+        tmem_relinquish();
+    }
+    fence_mbar_init();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    const uint32_t tT0 = tmem, tU = tmem + 128, tW = tmem + 128 + HD;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            auto load_v = [&](int j, int s) {
+                uint8_t *dst = sm + Ly::V0 + s * Ly::V_BYTES;
+                for (int b = 0; b < NB; ++b) tma_load_3d(dst + b * (kQK * 128), &p.v, b * 32, j * kQK, kvh, &vfull[s]);
+            };
+            mbar_arrive_expect_tx(&vfull[0], Ly::DC_BYTES + Ly::V_BYTES);
+            for (int b = 0; b < NB; ++b) tma_load_3d(sm + Ly::DC + b * (kQM * 128), &p.dc, b * 32, q0, h, &vfull[0]);
+            load_v(0, 0);
+            s_v_issued = 1;
+            if (nt > 1) {
+                mbar_arrive_expect_tx(&vfull[1], Ly::V_BYTES);
+                load_v(1, 1);
+                s_v_issued = 2;
+            }
+            for (int j = 0; j < nt; ++j) {
+                // Kt_j once the U / W products of tile j-1 are done with the Kt stage
+                if (j > 0 && !mbar_wait(&aempty, (j - 1) & 1, p.status, 20u)) { s_abort = 1; break; }
+                mbar_arrive_expect_tx(&ktfull, Ly::KT_BYTES);
+                for (int b = 0; b < 2; ++b)
+                    tma_load_3d(sm + Ly::KT + b * (HD * 128), &p.kt, j * kQK + b * 32, 0, kvh, &ktfull);
+                s_kt_issued = j + 1;
+                if (j + 2 < nt) {
+                    const int s = j & 1;
+                    if (!mbar_wait(&vempty[s], (j >> 1) & 1, p.status, 21u)) { s_abort = 1; break; }
+                    mbar_arrive_expect_tx(&vfull[s], Ly::V_BYTES);
+                    load_v(j + 2, s);
+                    s_v_issued = j + 3;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id1 = idesc_tf32(kQM, kQK), id2 = idesc_tf32(kQM, HD);
+            auto mma_t = [&](int j) -> bool {
+                const int s = j & 1;
+                if (!mbar_wait(&vfull[s], (j >> 1) & 1, p.status, 22u)) return false;
+                if (j >= 2 && !mbar_wait(&tempty[s], ((j - 2) >> 1) & 1, p.status, 23u)) return false;
+                tc_fence_after();
+                const uint8_t *a = sm + Ly::DC, *b = sm + Ly::V0 + s * Ly::V_BYTES;
+#pragma unroll
+                for (int kb = 0; kb < NB; ++kb)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_tf32(tT0 + uint32_t(s * kQK), sw128_desc(a + kb * (kQM * 128)) + 2 * k,
+                                 sw128_desc(b + kb * (kQK * 128)) + 2 * k, id1, (kb | k) ? 1u : 0u);
+                mma_commit(&vempty[s]);
+                mma_commit(&tfull[s]);
+                s_v_used = j + 1;
+                return true;
+            };
+            bool ok = mma_t(0);
+            for (int j = 0; ok && j < nt; ++j) {
+                if (j + 1 < nt && !(ok = mma_t(j + 1))) break;
+                if (!mbar_wait(&afull, j & 1, p.status, 24u) || !mbar_wait(&ktfull, j & 1, p.status, 25u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t *ae = sm + Ly::AE, *ap = sm + Ly::AP, *kt = sm + Ly::KT;
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t bd = sw128_desc(kt + kb * (HD * 128)) + 2 * k;
+                        const uint32_t acc = (j > 0 || kb > 0 || k > 0) ? 1u : 0u;
+                        mma_tf32(tU, sw128_desc(ae + kb * (kQM * 128)) + 2 * k, bd, id2, acc);
+                        mma_tf32(tW, sw128_desc(ap + kb * (kQM * 128)) + 2 * k, bd, id2, acc);
+                    }
+                mma_commit(&aempty);
+                s_kt_used = j + 1;
+            }
+            if (!ok) s_abort = 1;
+            mma_commit(&ufull);                     // fires once every MMA issued above is complete
+            mbar_wait(&ufull, 0, nullptr, 0u);
+        }
+    } else {
+        // ------------------------------------------------ epilogue: one query row per thread
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane, i = q0 + r;
+        const bool row_ok = i < p.S;
+        const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+        const float *prow = p.attn + (int64_t(h) * p.S + (row_ok ? i : 0)) * p.L;
+        const int jlast = p.causal ? p.pos0 + i : p.L - 1;      // last visible key
+        float D = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nt && ok; ++j) {
+            const int s = j & 1, k0 = j * kQK;
+            float pv[kQK];
+            if (row_ok && p.vecP) {
+#pragma unroll
+                for (int c = 0; c < kQK; c += 4) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (k0 + c < p.L) v = ld_stream(reinterpret_cast<const float4 *>(prow + k0 + c));
+                    pv[c] = v.x;
+                    pv[c + 1] = v.y;
+                    pv[c + 2] = v.z;
+                    pv[c + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kQK; ++c) pv[c] = (row_ok && k0 + c < p.L) ? prow[k0 + c] : 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < kQK; ++c)
+                if (k0 + c > jlast) pv[c] = 0.f;
+            uint32_t t[kQK];
+            if (!mbar_wait(&tfull[s], (j >> 1) & 1, p.status, 26u)) { ok = false; break; }
+            tc_fence_after();
+            tmem_ld32(tT0 + uint32_t(s * kQK) + lane_off, *reinterpret_cast<uint32_t(*)[32]>(t));
+            tmem_ld32(tT0 + uint32_t(s * kQK + 32) + lane_off, *reinterpret_cast<uint32_t(*)[32]>(t + 32));
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[s]);
+#pragma unroll
+            for (int c = 0; c < kQK; ++c) {
+                const float e = pv[c] * __uint_as_float(t[c]);
+                D += e;
+                t[c] = to_tf32(e);
+            }
+            if (j > 0 && !mbar_wait(&aempty, (j - 1) & 1, p.status, 27u)) { ok = false; break; }
+            uint8_t *ae = sm + Ly::AE, *ap = sm + Ly::AP;
+#pragma unroll
+            for (int c4 = 0; c4 < kQK / 4; ++c4) {
+                const uint32_t off = uint32_t(c4 >> 3) * (kQM * 128) + sw128_off(r, c4 & 7);
+                st_shared_v4(ae + off, t[4 * c4], t[4 * c4 + 1], t[4 * c4 + 2], t[4 * c4 + 3]);
+                st_shared_v4(ap + off, to_tf32(pv[4 * c4]), to_tf32(pv[4 * c4 + 1]), to_tf32(pv[4 * c4 + 2]),
+                             to_tf32(pv[4 * c4 + 3]));
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull);
+        }
+        if (ok && mbar_wait(&ufull, 0, p.status, 28u)) {
+            tc_fence_after();
+            constexpr int half = HD / 2;
+            float *out = p.dq + int64_t(row_ok ? i : 0) * (p.nh * HD) + h * HD;
+            const float pos = float(p.pos0 + i);
+#pragma unroll 1
+            for (int c = 0; c < half; c += 16) {
+                uint32_t u1[16], u2[16], w1[16], w2[16];
+                tmem_ld16(tU + uint32_t(c) + lane_off, u1);
+                tmem_ld16(tU + uint32_t(c + half) + lane_off, u2);
+                tmem_ld16(tW + uint32_t(c) + lane_off, w1);
+                tmem_ld16(tW + uint32_t(c + half) + lane_off, w2);
+                tmem_wait_ld();
+                float y1[16], y2[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    float a1 = p.scale * (__uint_as_float(u1[t]) - D * __uint_as_float(w1[t]));
+                    float a2 = p.scale * (__uint_as_float(u2[t]) - D * __uint_as_float(w2[t]));
+                    if (p.rope) {
+                        float cs, sn;
+                        rope_cos_sin(pos, p.fr.hi[c + t], p.fr.lo[c + t], cs, sn);
+                        const float b1 = a1 * cs + a2 * sn, b2 = -a1 * sn + a2 * cs;
+                        a1 = b1;
+                        a2 = b2;
+                    }
+                    y1[t] = a1;
+                    y2[t] = a2;
+                }
+                if (row_ok) {
+#pragma unroll
+                    for (int t = 0; t < 16; t += 4) {
+                        *reinterpret_cast<float4 *>(out + c + t) = make_float4(y1[t], y1[t + 1], y1[t + 2], y1[t + 3]);
+                        *reinterpret_cast<float4 *>(out + c + half + t) =
+                            make_float4(y2[t], y2[t + 1], y2[t + 2], y2[t + 3]);
+                    }
+                }
+            }
+        }
+        if (!ok) s_abort = 1;
+    }
+    // wind down: the MMA thread waited for its final commit, so no MMA is in flight;
+    // after an abort, wait (bounded) for tile copies that were issued but not consumed
+    tc_fence_before();
+    __syncthreads();
+    if (s_abort && threadIdx.x == 0) {
+        for (int v = s_v_used; v < s_v_issued; ++v) mbar_wait(&vfull[v & 1], (v >> 1) & 1, nullptr, 0u);
+        for (int k = s_kt_used; k < s_kt_issued; ++k) mbar_wait(&ktfull, k & 1, nullptr, 0u);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Ly::COLS);
+    }
+}
+
+// ------------------------------------------------------------------ dV
+
+template <int HD>
+struct DvLayout {
+    static constexpr int A_BYTES = kVK * kVQ * 4;        // P^T [128 keys][64 queries]: 2 boxes
+    static constexpr int B_BYTES = HD * kVQ * 4;         // dCtx^T [HD][64 queries]: 2 boxes
+    static constexpr int A0 = 0, B0 = 2 * A_BYTES, TOTAL = B0 + 2 * B_BYTES;
+    static constexpr uint32_t COLS = HD <= 32 ? 32 : (HD <= 64 ? 64 : (HD <= 128 ? 128 : 256));
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __grid_constant__ AttnTcParams p) {
+    using Ly = DvLayout<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    __shared__ uint64_t bfull[2], bempty[2], afull[2], aempty[2], dfull;
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_abort, s_b_issued, s_b_used;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kvh = blockIdx.y, G = p.nh / p.nkv;
+    const int k0 = int(blockIdx.x) * kVK;                 // among the S newest keys
+    const int t0 = p.causal ? k0 / kVQ : 0;               // first query tile that sees key k0
+    const int nqt = (p.S + kVQ - 1) / kVQ;
+    const int nq = nqt - t0, nw = G * nq;                 // work items (head of group, query tile)
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        s_b_issued = s_b_used = 0;
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bfull[s], 1);
+            mbar_init(&bempty[s], 1);
+            mbar_init(&afull[s], 4);
+            mbar_init(&aempty[s], 1);
+        }
+        mbar_init(&dfull, 1);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, Ly::COLS);
+        tmem_relinquish();
+    }
+    fence_mbar_init();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tD = tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int w = 0; w < nw; ++w) {
+                const int s = w & 1, h = kvh * G + w / nq, qa = (t0 + w % nq) * kVQ;
+                if (w >= 2 && !mbar_wait(&bempty[s], ((w - 2) >> 1) & 1, p.status, 30u)) { s_abort = 1; break; }
+                mbar_arrive_expect_tx(&bfull[s], Ly::B_BYTES);
+                for (int b = 0; b < 2; ++b)
+                    tma_load_3d(sm + Ly::B0 + s * Ly::B_BYTES + b * (HD * 128), &p.dct, qa + b * 32, 0, h, &bfull[s]);
+                s_b_issued = w + 1;
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t id = idesc_tf32(kVK, HD);
+            bool ok = true;
+            for (int w = 0; w < nw; ++w) {
+                const int s = w & 1;
+                if (!mbar_wait(&bfull[s], (w >> 1) & 1, p.status, 31u) ||
+                    !mbar_wait(&afull[s], (w >> 1) & 1, p.status, 32u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t *a = sm + Ly::A0 + s * Ly::A_BYTES, *b = sm + Ly::B0 + s * Ly::B_BYTES;
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_tf32(tD, sw128_desc(a + kb * (kVK * 128)) + 2 * k, sw128_desc(b + kb * (HD * 128)) + 2 * k,
+                                 id, (w > 0 || kb > 0 || k > 0) ? 1u : 0u);
+                mma_commit(&bempty[s]);
+                mma_commit(&aempty[s]);
+                s_b_used = w + 1;
+            }
+            if (!ok) s_abort = 1;
+            mma_commit(&dfull);
+            mbar_wait(&dfull, 0, nullptr, 0u);
+        }
+    } else {
+        // ------------------------------------------------ P^T writers, then the dV epilogue
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane, jj = k0 + r;        // key row of this thread
+        const bool key_ok = jj < p.S;
+        bool ok = true;
+        for (int w = 0; w < nw && ok; ++w) {
+            const int s = w & 1, h = kvh * G + w / nq, qa = (t0 + w % nq) * kVQ;
+            const float *pc = p.attn + int64_t(h) * p.S * p.L + p.pos0 + (key_ok ? jj : 0);
+            float pv[kVQ];
+#pragma unroll
+            for (int qq = 0; qq < kVQ; ++qq) {
+                const int q = qa + qq;
+                const bool vis = key_ok && q < p.S && (!p.causal || q >= jj);
+                pv[qq] = vis ? __ldg(pc + int64_t(q) * p.L) : 0.f;
+            }
+            if (w >= 2 && !mbar_wait(&aempty[s], ((w - 2) >> 1) & 1, p.status, 33u)) { ok = false; break; }
+            uint8_t *a = sm + Ly::A0 + s * Ly::A_BYTES;
+#pragma unroll
+            for (int c4 = 0; c4 < kVQ / 4; ++c4) {
+                const uint32_t off = uint32_t(c4 >> 3) * (kVK * 128) + sw128_off(r, c4 & 7);
+                st_shared_v4(a + off, to_tf32(pv[4 * c4]), to_tf32(pv[4 * c4 + 1]), to_tf32(pv[4 * c4 + 2]),
+                             to_tf32(pv[4 * c4 + 3]));
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[s]);
+        }
+        if (ok && mbar_wait(&dfull, 0, p.status, 34u)) {
+            tc_fence_after();
+            const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+            float *out = p.dv + int64_t(key_ok ? jj : 0) * (p.nkv * HD) + kvh * HD;
+#pragma unroll 1
+            for (int c = 0; c < HD; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tD + uint32_t(c) + lane_off, v);
+                tmem_wait_ld();
+                if (key_ok) {
+#pragma unroll
+                    for (int t = 0; t < 32; t += 4)
+                        *reinterpret_cast<float4 *>(out + c + t) =
+                            make_float4(__uint_as_float(v[t]), __uint_as_float(v[t + 1]), __uint_as_float(v[t + 2]),
+                                        __uint_as_float(v[t + 3]));
+                }
+            }
+        }
+        if (!ok) s_abort = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (s_abort && threadIdx.x == 0) {
+        for (int b = s_b_used; b < s_b_issued; ++b) mbar_wait(&bfull[b & 1], (b >> 1) & 1, nullptr, 0u);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tD, Ly::COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+// fp32 3-D tensor map, 128-byte swizzle, zero fill out of range.  dims / box innermost
+// first; strides in bytes of dims 1 and 2.
+int make_map_f32_3d(CUtensorMap *m, const void *base, const uint64_t dims[3], const uint64_t strides[2],
+                    const uint32_t box[3]) {
+    EncodeTiled enc = encode_fn();
+    TLB_REQUIRE(enc != nullptr, TLB_ECUDA, "attention (tcgen05): cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t st[2] = {strides[0], strides[1]};
+    const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), d, st, bx, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    TLB_REQUIRE(r == CUDA_SUCCESS, TLB_ECUDA, "attention (tcgen05): tensor map encoding failed (%d)", int(r));
+    return TLB_OK;
+}
+
+struct TcAttnWs {
+    size_t dCr, dCT, Kt, Vr, total;
+    int64_t S4, L4;
+};
+
+TcAttnWs tc_attn_layout(int64_t S, int64_t L, int nh, int nkv, int hd) {
+    auto r256 = [](size_t b) { return (b + 255) & ~size_t(255); };
+    TcAttnWs w;
+    w.S4 = (S + 3) & ~int64_t(3);
+    w.L4 = (L + 3) & ~int64_t(3);
+    w.dCr = 0;
+    w.dCT = w.dCr + r256(size_t(nh) * S * hd * 4);
+    w.Kt = w.dCT + r256(size_t(nh) * hd * w.S4 * 4);
+    w.Vr = w.Kt + r256(size_t(nkv) * hd * w.L4 * 4);
+    w.total = w.Vr + r256(size_t(nkv) * L * hd * 4);
+    return w;
+}
+
+template <int HD>
+int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32_t *status, cudaStream_t st) {
+    const TcAttnWs w = tc_attn_layout(a.S, a.L, a.nh, a.nkv, HD);
+    char *base = static_cast<char *>(scratch);
+    float *dCr = reinterpret_cast<float *>(base + w.dCr), *dCT = reinterpret_cast<float *>(base + w.dCT);
+    float *Kt = reinterpret_cast<float *>(base + w.Kt), *Vr = reinterpret_cast<float *>(base + w.Vr);
+    const int ntc_dc = a.nh * HD / 32, ntc_kv = a.nkv * HD / 32;
+    const int64_t nblk = int64_t(ntc_dc) * ceil_div(a.S, 32) + 2 * int64_t(ntc_kv) * ceil_div(a.L, 32);
+    attn_tc_prep_kernel<<<unsigned(nblk), 256, 0, st>>>(a, dCr, dCT, Kt, Vr, int(w.S4), int(w.L4), ntc_dc, ntc_kv);
+    TLB_TRY(check_launch("attn_tc_prep"));
+
+    AttnTcParams p;
+    memset(&p, 0, sizeof(p));
+    {
+        const uint64_t d[3] = {uint64_t(HD), uint64_t(a.S), uint64_t(a.nh)};
+        const uint64_t s[2] = {uint64_t(HD) * 4, uint64_t(a.S) * HD * 4};
+        const uint32_t b[3] = {32, uint32_t(kQM), 1};
+        TLB_TRY(make_map_f32_3d(&p.dc, dCr, d, s, b));
+    }
+    {
+        const uint64_t d[3] = {uint64_t(HD), uint64_t(a.L), uint64_t(a.nkv)};
+        const uint64_t s[2] = {uint64_t(HD) * 4, uint64_t(a.L) * HD * 4};
+        const uint32_t b[3] = {32, uint32_t(kQK), 1};
+        TLB_TRY(make_map_f32_3d(&p.v, Vr, d, s, b));
+    }
+    {
+        const uint64_t d[3] = {uint64_t(a.L), uint64_t(HD), uint64_t(a.nkv)};
+        const uint64_t s[2] = {uint64_t(w.L4) * 4, uint64_t(w.L4) * HD * 4};
+        const uint32_t b[3] = {32, uint32_t(HD), 1};
+        TLB_TRY(make_map_f32_3d(&p.kt, Kt, d, s, b));
+    }
+    {
+        const uint64_t d[3] = {uint64_t(a.S), uint64_t(HD), uint64_t(a.nh)};
+        const uint64_t s[2] = {uint64_t(w.S4) * 4, uint64_t(w.S4) * HD * 4};
+        const uint32_t b[3] = {32, uint32_t(HD), 1};
+        TLB_TRY(make_map_f32_3d(&p.dct, dCT, d, s, b));
+    }
+    p.attn = a.attn;
+    p.dq = a.dq;
+    p.dv = a.dv;
+    p.S = a.S;
+    p.L = a.L;
+    p.nh = a.nh;
+    p.nkv = a.nkv;
+    p.pos0 = a.pos0;
+    p.causal = a.causal;
+    p.rope = a.rope;
+    p.vecP = (a.L % 4 == 0 && aligned16(a.attn)) ? 1 : 0;
+    p.scale = a.scale;
+    p.status = status;
+    p.fr = fr;
+
+    const int smq = DqLayout<HD>::TOTAL + 1024, smv = DvLayout<HD>::TOTAL + 1024;
+    TLB_CUDA(cudaFuncSetAttribute(attn_tc_dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smq));
+    TLB_CUDA(cudaFuncSetAttribute(attn_tc_dv_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smv));
+    attn_tc_dq_kernel<HD><<<dim3(unsigned(ceil_div(a.S, kQM)), unsigned(a.nh)), kAttnThreads, smq, st>>>(p);
+    TLB_TRY(check_launch("attn_tc_dq"));
+    attn_tc_dv_kernel<HD><<<dim3(unsigned(ceil_div(a.S, kVK)), unsigned(a.nkv)), kAttnThreads, smv, st>>>(p);
+    return check_launch("attn_tc_dv");
+}
+
+}  // namespace
+
+bool attn_tc_supported(int64_t S, int64_t L, int nh, int nkv, int hd) {
+    return S > 1 && S <= L && (hd == 64 || hd == 128) && nh <= 65535 && nkv <= 65535 && nh % nkv == 0 &&
+           L < (int64_t(1) << 30);
+}
+
+size_t attn_tc_bytes(int64_t S, int64_t L, int nh, int nkv, int hd) {
+    return tc_attn_layout(S, L, nh, nkv, hd).total;
+}
+
+int attn_tc_launch(const AttnArgs &a, float rope_base, void *scratch, uint32_t *status, cudaStream_t st) {
+    if (a.S == 0) return TLB_OK;
+    TLB_REQUIRE(attn_tc_supported(a.S, a.L, a.nh, a.nkv, a.hd), TLB_EUNSUPPORTED, "attention (tcgen05): shape");
+    TLB_REQUIRE((reinterpret_cast<uintptr_t>(scratch) & 255u) == 0, TLB_EINVAL, "attention (tcgen05): scratch alignment");
+    RopeFreqs fr;
+    rope_freqs(fr, a.hd, rope_base);
+    return a.hd == 128 ? launch_attn_tc<128>(a, fr, scratch, status, st) : launch_attn_tc<64>(a, fr, scratch, status, st);
+}
+
+}  // namespace tlb

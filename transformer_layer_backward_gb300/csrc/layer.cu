@@ -15,6 +15,7 @@ namespace {
 struct LayerWs {
     size_t dF, dG, dU, dN2, dSub, dqpre, dv, lora_q, lora_v;   // lora_*: tiled LoRA partial sums
     size_t abf, gbf, ubf, part;               // tensor-core path: bf16 A operands, split-K partials
+    size_t atc;                               // tensor-core attention: tf32 operand copies
     size_t dR1, Upart, Wpart, Dpart, gh2, part1, part2, part3, gbar, pp;   // single-token path
     size_t total;
 };
@@ -24,6 +25,12 @@ bool tc_route(const tlb_layer_cfg &c, int64_t S) {
     const int64_t I = c.ffn_dim, H = c.dim, qd = int64_t(c.n_heads) * c.head_dim;
     return c.wtype == TLB_W_BF16 && S > 1 && tc_supported(S, I, H) && tc_supported(S, H, 2 * I) &&
            tc_supported(S, qd, H) && I % 8 == 0;
+}
+
+// With bf16 weights the sequence attention contractions run on tcgen05 too (tf32
+// operands); fp32 and ternary layers keep the fp32 CUDA-core kernels.
+bool attn_tc_route(const tlb_layer_cfg &c, int64_t S, int64_t L) {
+    return c.wtype == TLB_W_BF16 && attn_tc_supported(S, L, c.n_heads, c.n_kv_heads, c.head_dim);
 }
 
 LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
@@ -40,6 +47,7 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     } else {
         w.abf = w.gbf = w.ubf = w.part = 0;
     }
+    w.atc = attn_tc_route(c, S, L) ? p.take(attn_tc_bytes(S, L, c.n_heads, c.n_kv_heads, c.head_dim)) : 0;
     w.dF = p.take(S * I * 4);
     w.dG = p.take(S * I * 4);
     w.dU = p.take(S * I * 4);
@@ -182,6 +190,8 @@ int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, co
     g.causal = (c.flags & TLB_CAUSAL) ? 1 : 0;
     g.rope = (c.flags & TLB_ROPE) ? 1 : 0;
     g.scale = c.attn_scale;
+    if (attn_tc_route(c, S, L) && aligned16(d_qpre) && aligned16(d_v))
+        return attn_tc_launch(g, c.rope_base, ws_at<void>(ws, p.atc), ws_at<uint32_t>(ws, 0), st);
     return attn_core_launch(g, c.rope_base, st);
 }
 
