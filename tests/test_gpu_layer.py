@@ -29,13 +29,18 @@ DEC_G8 = DECODE.with_(name="dec_g8_hd32", dim=256, ffn_dim=256, n_heads=16, n_kv
 DEC_HD256 = DECODE.with_(name="dec_hd256", dim=512, ffn_dim=1024, n_heads=4, n_kv_heads=1, head_dim=256,
                          cache_len=65, sub_norm=False, rope=True)
 # bf16 sequence layers on the tensor-core attention: head_dim 64 with S ragged over both
-# tile sizes; a cache longer than the sequence (L not a multiple of 4, 4-head groups)
+# tile sizes; a cache longer than the sequence (4-head groups, MHA).  L = 301 is not a
+# multiple of 4, which the tensor-core attention needs: that layer takes the CUDA-core one.
 SEQ_HD64 = SEQ512.with_(name="seq_hd64", dim=512, ffn_dim=1024, n_heads=8, n_kv_heads=2, head_dim=64,
                         rank=8, lora_alpha=16.0, seq_len=200, cache_len=200)
 SEQ_CACHE = SEQ512.with_(name="seq_cache", dim=512, ffn_dim=768, n_heads=4, n_kv_heads=1, head_dim=128,
-                         seq_len=96, cache_len=301, adam_state="warm", step=4)
+                         seq_len=96, cache_len=300, adam_state="warm", step=4)
+SEQ_MHA = SEQ512.with_(name="seq_mha", dim=256, ffn_dim=512, n_heads=4, n_kv_heads=4, head_dim=64,
+                       rank=4, lora_alpha=8.0, seq_len=130, cache_len=258)
+SEQ_ODD = SEQ512.with_(name="seq_odd_cache", dim=512, ffn_dim=768, n_heads=4, n_kv_heads=1, head_dim=128,
+                       seq_len=45, cache_len=301)
 CASES = {c.name: c for c in (TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512, DEC_F32, DEC_BF16, DEC_G8, DEC_HD256,
-                             SEQ_HD64, SEQ_CACHE)}
+                             SEQ_HD64, SEQ_CACHE, SEQ_MHA, SEQ_ODD)}
 
 
 def tol(cfg):

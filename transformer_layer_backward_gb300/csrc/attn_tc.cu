@@ -6,15 +6,17 @@
 //                   dCr [nh][S][hd]   dCT [nh][hd][S4]   Kt [nkv][hd][L4]   Vr [nkv][L][hd]
 //   attn_tc_dq    CTA = (head h, 128 queries), 6 warps: TMA producer, MMA issuer, and
 //                 4 epilogue warps (one query row per thread = one TMEM lane).  Per tile
-//                 of 64 keys j:
+//                 of 32 keys j (V_j, K_j^T and the P tile arrive by TMA, two tiles ahead):
 //                   T  = dCtx_h V_j^T                        tcgen05.mma, T in TMEM
 //                   E  = P (.) T,  D += rowsum(E)            epilogue, fp32
 //                   U += E K_j,    W += P K_j                tcgen05.mma (E, P tf32 in smem)
 //                 then dQ = scale (U - D W), which equals scale sum_j P (T - D) K_j with D
 //                 the literal row sum of P (.) dAttn, and RoPE backward on the way out.
-//   attn_tc_dv    CTA = (KV head, 128 of the S newest keys): over the group's heads and
-//                 64-query tiles, dV += P^T dCtx_h.  The epilogue warps write P^T (tf32,
-//                 K-major) into shared memory; dCtx^T tiles come by TMA.
+//   attn_tc_dv    CTA = (head h, 128 of the S newest keys): over 64-query tiles,
+//                 dV_h += P_h^T dCtx_h.  P tiles come by TMA and the epilogue warps write
+//                 them transposed (tf32, K-major) for the MMA; dCtx^T tiles by TMA.  With
+//                 several heads per KV head the per-head sums go to a workspace and
+//                 attn_tc_dv_sum adds them in head order.
 // All MMAs: M = 128, K = 8 per instruction, both operands K-major with 128-byte swizzle.
 // Causal: key tiles past a query tile's last visible key are skipped; masked entries of
 // P inside a diagonal tile read as zero.  Every mbarrier wait is bounded.
@@ -32,20 +34,21 @@ namespace tlb {
 namespace {
 
 constexpr int kQM = 128;        // queries per dQ CTA
-constexpr int kQK = 64;         // keys per dQ tile
+constexpr int kQK = 32;         // keys per dQ tile
 constexpr int kVK = 128;        // keys per dV CTA
 constexpr int kVQ = 64;         // queries per dV tile
 constexpr int kAttnThreads = 192;
 
 struct AttnTcParams {
     CUtensorMap dc;             // dCr  {hd, S, nh},  box {32, 128, 1}
-    CUtensorMap v;              // Vr   {hd, L, nkv}, box {32, 64, 1}
+    CUtensorMap v;              // Vr   {hd, L, nkv}, box {32, 32, 1}
     CUtensorMap kt;             // Kt   {L, hd, nkv}, box {32, hd, 1}
     CUtensorMap dct;            // dCT  {S, hd, nh},  box {32, hd, 1}
-    const float *attn;          // [nh, S, L]
+    CUtensorMap pq;             // attn {L, S, nh},   box {32, 128, 1}   (dQ: 128 queries x 32 keys)
+    CUtensorMap pv;             // attn {L, S, nh},   box {32, 64, 1}    (dV: 64 queries x 32 keys)
     float *dq;                  // [S, nh * hd]
-    float *dv;                  // [S, nkv * hd]
-    int S, L, nh, nkv, pos0, causal, rope, vecP;
+    float *dv;                  // [S, nkv * hd], or per-head partial sums [nh / nkv][S, nkv * hd]
+    int S, L, nh, nkv, pos0, causal, rope;
     float scale;
     uint32_t *status;
     RopeFreqs fr;
@@ -122,12 +125,13 @@ template <int HD>
 struct DqLayout {
     static constexpr int NB = HD / 32;                   // 128-byte boxes along head_dim
     static constexpr int DC = 0, DC_BYTES = kQM * HD * 4;
-    static constexpr int V0 = DC + DC_BYTES, V_BYTES = kQK * HD * 4;
-    static constexpr int KT = V0 + 2 * V_BYTES, KT_BYTES = HD * kQK * 4;
-    static constexpr int AE = KT + KT_BYTES, A_BYTES = kQM * kQK * 4;
-    static constexpr int AP = AE + A_BYTES;
-    static constexpr int TOTAL = AP + A_BYTES;
-    static constexpr uint32_t COLS = (128 + 2 * HD) <= 256 ? 256 : 512;   // T0 | T1 | U | W
+    static constexpr int V0 = DC + DC_BYTES, V_BYTES = kQK * HD * 4;          // 2 slots
+    static constexpr int KT0 = V0 + 2 * V_BYTES, KT_BYTES = HD * kQK * 4;     // 2 slots
+    static constexpr int P0 = KT0 + 2 * KT_BYTES, P_BYTES = kQM * kQK * 4;    // 2 slots
+    static constexpr int AE0 = P0 + 2 * P_BYTES, A_BYTES = kQM * kQK * 4;     // 2 slots
+    static constexpr int TOTAL = AE0 + 2 * A_BYTES;
+    static constexpr uint32_t TU = 2 * kQK, TW = 2 * kQK + HD;                // T0 | T1 | U | W
+    static constexpr uint32_t COLS = (2 * kQK + 2 * HD) <= 256 ? 256 : 512;
 };
 
 template <int HD>
@@ -136,9 +140,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
     constexpr int NB = Ly::NB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    __shared__ uint64_t vfull[2], vempty[2], tfull[2], tempty[2], ktfull, afull, aempty, ufull;
+    // vfull/vfree: V ring; kfull/kfree: K^T + P ring; tfull: T in TMEM; afull/afree: E tiles
+    __shared__ uint64_t vfull[2], vfree[2], kfull[2], kfree[2], tfull[2], afull[2], afree[2], ufull;
     __shared__ uint32_t tmem_base;
-    __shared__ int s_abort, s_v_issued, s_v_used, s_kt_issued, s_kt_used;
+    __shared__ int s_abort, s_v_issued, s_v_used, s_k_issued, s_k_used;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y, kvh = h / (p.nh / p.nkv);
     const int q0 = int(gridDim.x - 1 - blockIdx.x) * kQM;       // latest (longest) query tiles first
@@ -147,16 +152,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
 
     if (threadIdx.x == 0) {
         s_abort = 0;
-        s_v_issued = s_v_used = s_kt_issued = s_kt_used = 0;
+        s_v_issued = s_v_used = s_k_issued = s_k_used = 0;
         for (int s = 0; s < 2; ++s) {
             mbar_init(&vfull[s], 1);
-            mbar_init(&vempty[s], 1);
+            mbar_init(&vfree[s], 1);
+            mbar_init(&kfull[s], 1);
+            mbar_init(&kfree[s], 1);
             mbar_init(&tfull[s], 1);
-            mbar_init(&tempty[s], 4);
+            mbar_init(&afull[s], 4);
+            mbar_init(&afree[s], 1);
         }
-        mbar_init(&ktfull, 1);
-        mbar_init(&afull, 4);
-        mbar_init(&aempty, 1);
         mbar_init(&ufull, 1);
     }
     if (warp == 1) {
@@ -168,81 +173,73 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
-    const uint32_t tT0 = tmem, tU = tmem + 128, tW = tmem + 128 + HD;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer (two tiles ahead)
         if (lane == 0) {
-            auto load_v = [&](int j, int s) {
-                uint8_t *dst = sm + Ly::V0 + s * Ly::V_BYTES;
-                for (int b = 0; b < NB; ++b) tma_load_3d(dst + b * (kQK * 128), &p.v, b * 32, j * kQK, kvh, &vfull[s]);
-            };
-            mbar_arrive_expect_tx(&vfull[0], Ly::DC_BYTES + Ly::V_BYTES);
-            for (int b = 0; b < NB; ++b) tma_load_3d(sm + Ly::DC + b * (kQM * 128), &p.dc, b * 32, q0, h, &vfull[0]);
-            load_v(0, 0);
-            s_v_issued = 1;
-            if (nt > 1) {
-                mbar_arrive_expect_tx(&vfull[1], Ly::V_BYTES);
-                load_v(1, 1);
-                s_v_issued = 2;
-            }
             for (int j = 0; j < nt; ++j) {
-                // Kt_j once the U / W products of tile j-1 are done with the Kt stage
-                if (j > 0 && !mbar_wait(&aempty, (j - 1) & 1, p.status, 20u)) { s_abort = 1; break; }
-                mbar_arrive_expect_tx(&ktfull, Ly::KT_BYTES);
-                for (int b = 0; b < 2; ++b)
-                    tma_load_3d(sm + Ly::KT + b * (HD * 128), &p.kt, j * kQK + b * 32, 0, kvh, &ktfull);
-                s_kt_issued = j + 1;
-                if (j + 2 < nt) {
-                    const int s = j & 1;
-                    if (!mbar_wait(&vempty[s], (j >> 1) & 1, p.status, 21u)) { s_abort = 1; break; }
+                const int s = j & 1, k0 = j * kQK;
+                if (j >= 2 && !mbar_wait(&vfree[s], ((j - 2) >> 1) & 1, p.status, 20u)) { s_abort = 1; break; }
+                uint8_t *vd = sm + Ly::V0 + s * Ly::V_BYTES;
+                if (j == 0) {
+                    mbar_arrive_expect_tx(&vfull[0], Ly::DC_BYTES + Ly::V_BYTES);
+                    for (int b = 0; b < NB; ++b)
+                        tma_load_3d(sm + Ly::DC + b * (kQM * 128), &p.dc, b * 32, q0, h, &vfull[0]);
+                } else {
                     mbar_arrive_expect_tx(&vfull[s], Ly::V_BYTES);
-                    load_v(j + 2, s);
-                    s_v_issued = j + 3;
                 }
+                for (int b = 0; b < NB; ++b) tma_load_3d(vd + b * (kQK * 128), &p.v, b * 32, k0, kvh, &vfull[s]);
+                s_v_issued = j + 1;
+                if (j >= 2 && !mbar_wait(&kfree[s], ((j - 2) >> 1) & 1, p.status, 21u)) { s_abort = 1; break; }
+                mbar_arrive_expect_tx(&kfull[s], Ly::KT_BYTES + Ly::P_BYTES);
+                tma_load_3d(sm + Ly::KT0 + s * Ly::KT_BYTES, &p.kt, k0, 0, kvh, &kfull[s]);
+                tma_load_3d(sm + Ly::P0 + s * Ly::P_BYTES, &p.pq, k0, q0, h, &kfull[s]);
+                s_k_issued = j + 1;
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t id1 = idesc_tf32(kQM, kQK), id2 = idesc_tf32(kQM, HD);
-            auto mma_t = [&](int j) -> bool {
+            auto mma_t = [&](int j) -> bool {            // T[j % 2] = dCtx V_j^T
                 const int s = j & 1;
                 if (!mbar_wait(&vfull[s], (j >> 1) & 1, p.status, 22u)) return false;
-                if (j >= 2 && !mbar_wait(&tempty[s], ((j - 2) >> 1) & 1, p.status, 23u)) return false;
                 tc_fence_after();
                 const uint8_t *a = sm + Ly::DC, *b = sm + Ly::V0 + s * Ly::V_BYTES;
 #pragma unroll
                 for (int kb = 0; kb < NB; ++kb)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_tf32(tT0 + uint32_t(s * kQK), sw128_desc(a + kb * (kQM * 128)) + 2 * k,
+                        mma_tf32(tmem + uint32_t(s * kQK), sw128_desc(a + kb * (kQM * 128)) + 2 * k,
                                  sw128_desc(b + kb * (kQK * 128)) + 2 * k, id1, (kb | k) ? 1u : 0u);
-                mma_commit(&vempty[s]);
+                mma_commit(&vfree[s]);
                 mma_commit(&tfull[s]);
                 s_v_used = j + 1;
                 return true;
             };
-            bool ok = mma_t(0);
+            bool ok = mma_t(0) && (nt < 2 || mma_t(1));
             for (int j = 0; ok && j < nt; ++j) {
-                if (j + 1 < nt && !(ok = mma_t(j + 1))) break;
-                if (!mbar_wait(&afull, j & 1, p.status, 24u) || !mbar_wait(&ktfull, j & 1, p.status, 25u)) {
+                const int s = j & 1;
+                if (!mbar_wait(&afull[s], (j >> 1) & 1, p.status, 24u) ||
+                    !mbar_wait(&kfull[s], (j >> 1) & 1, p.status, 25u)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint8_t *ae = sm + Ly::AE, *ap = sm + Ly::AP, *kt = sm + Ly::KT;
+                const uint64_t ad = sw128_desc(sm + Ly::AE0 + s * Ly::A_BYTES);
+                const uint64_t pd = sw128_desc(sm + Ly::P0 + s * Ly::P_BYTES);
+                const uint64_t kd = sw128_desc(sm + Ly::KT0 + s * Ly::KT_BYTES);
 #pragma unroll
-                for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint64_t bd = sw128_desc(kt + kb * (HD * 128)) + 2 * k;
-                        const uint32_t acc = (j > 0 || kb > 0 || k > 0) ? 1u : 0u;
-                        mma_tf32(tU, sw128_desc(ae + kb * (kQM * 128)) + 2 * k, bd, id2, acc);
-                        mma_tf32(tW, sw128_desc(ap + kb * (kQM * 128)) + 2 * k, bd, id2, acc);
-                    }
-                mma_commit(&aempty);
-                s_kt_used = j + 1;
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
+                    mma_tf32(tmem + Ly::TU, ad + 2 * k, kd + 2 * k, id2, acc);
+                    mma_tf32(tmem + Ly::TW, pd + 2 * k, kd + 2 * k, id2, acc);
+                }
+                mma_commit(&afree[s]);
+                mma_commit(&kfree[s]);
+                s_k_used = j + 1;
+                // the epilogue has read T[s] (it arrived on afull after its tensor-memory loads)
+                if (j + 2 < nt && !(ok = mma_t(j + 2))) break;
             }
             if (!ok) s_abort = 1;
             mma_commit(&ufull);                     // fires once every MMA issued above is complete
@@ -254,59 +251,57 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
         const int r = quarter * 32 + lane, i = q0 + r;
         const bool row_ok = i < p.S;
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-        const float *prow = p.attn + (int64_t(h) * p.S + (row_ok ? i : 0)) * p.L;
         const int jlast = p.causal ? p.pos0 + i : p.L - 1;      // last visible key
         float D = 0.f;
         bool ok = true;
-        for (int j = 0; j < nt && ok; ++j) {
+        for (int j = 0; j < nt; ++j) {
             const int s = j & 1, k0 = j * kQK;
-            float pv[kQK];
-            if (row_ok && p.vecP) {
-#pragma unroll
-                for (int c = 0; c < kQK; c += 4) {
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (k0 + c < p.L) v = ld_stream(reinterpret_cast<const float4 *>(prow + k0 + c));
-                    pv[c] = v.x;
-                    pv[c + 1] = v.y;
-                    pv[c + 2] = v.z;
-                    pv[c + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kQK; ++c) pv[c] = (row_ok && k0 + c < p.L) ? prow[k0 + c] : 0.f;
+            if (!mbar_wait(&kfull[s], (j >> 1) & 1, p.status, 26u) ||
+                !mbar_wait(&tfull[s], (j >> 1) & 1, p.status, 27u)) {
+                ok = false;
+                break;
             }
-#pragma unroll
-            for (int c = 0; c < kQK; ++c)
-                if (k0 + c > jlast) pv[c] = 0.f;
-            uint32_t t[kQK];
-            if (!mbar_wait(&tfull[s], (j >> 1) & 1, p.status, 26u)) { ok = false; break; }
             tc_fence_after();
-            tmem_ld32(tT0 + uint32_t(s * kQK) + lane_off, *reinterpret_cast<uint32_t(*)[32]>(t));
-            tmem_ld32(tT0 + uint32_t(s * kQK + 32) + lane_off, *reinterpret_cast<uint32_t(*)[32]>(t + 32));
+            uint32_t t[kQK];
+            tmem_ld32(tmem + uint32_t(s * kQK) + lane_off, t);
+            uint8_t *pt = sm + Ly::P0 + s * Ly::P_BYTES;
+            float pv[kQK];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const float4 v = *reinterpret_cast<const float4 *>(pt + sw128_off(r, ch));
+                pv[4 * ch] = v.x;
+                pv[4 * ch + 1] = v.y;
+                pv[4 * ch + 2] = v.z;
+                pv[4 * ch + 3] = v.w;
+            }
+            if (k0 + kQK - 1 > jlast) {
+#pragma unroll
+                for (int c = 0; c < kQK; ++c)
+                    if (k0 + c > jlast) pv[c] = 0.f;
+            }
             tmem_wait_ld();
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[s]);
 #pragma unroll
             for (int c = 0; c < kQK; ++c) {
                 const float e = pv[c] * __uint_as_float(t[c]);
                 D += e;
                 t[c] = to_tf32(e);
             }
-            if (j > 0 && !mbar_wait(&aempty, (j - 1) & 1, p.status, 27u)) { ok = false; break; }
-            uint8_t *ae = sm + Ly::AE, *ap = sm + Ly::AP;
+            if (j >= 2 && !mbar_wait(&afree[s], ((j - 2) >> 1) & 1, p.status, 28u)) { ok = false; break; }
+            uint8_t *ae = sm + Ly::AE0 + s * Ly::A_BYTES;
 #pragma unroll
-            for (int c4 = 0; c4 < kQK / 4; ++c4) {
-                const uint32_t off = uint32_t(c4 >> 3) * (kQM * 128) + sw128_off(r, c4 & 7);
-                st_shared_v4(ae + off, t[4 * c4], t[4 * c4 + 1], t[4 * c4 + 2], t[4 * c4 + 3]);
-                st_shared_v4(ap + off, to_tf32(pv[4 * c4]), to_tf32(pv[4 * c4 + 1]), to_tf32(pv[4 * c4 + 2]),
-                             to_tf32(pv[4 * c4 + 3]));
+            for (int ch = 0; ch < 8; ++ch) {
+                const uint32_t off = sw128_off(r, ch);
+                st_shared_v4(ae + off, t[4 * ch], t[4 * ch + 1], t[4 * ch + 2], t[4 * ch + 3]);
+                // P in place, rounded and masked: the A operand of W += P K_j
+                st_shared_v4(pt + off, to_tf32(pv[4 * ch]), to_tf32(pv[4 * ch + 1]), to_tf32(pv[4 * ch + 2]),
+                             to_tf32(pv[4 * ch + 3]));
             }
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&afull);
+            if (lane == 0) mbar_arrive(&afull[s]);
         }
-        if (ok && mbar_wait(&ufull, 0, p.status, 28u)) {
+        if (ok && mbar_wait(&ufull, 0, p.status, 29u)) {
             tc_fence_after();
             constexpr int half = HD / 2;
             float *out = p.dq + int64_t(row_ok ? i : 0) * (p.nh * HD) + h * HD;
@@ -314,10 +309,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
 #pragma unroll 1
             for (int c = 0; c < half; c += 16) {
                 uint32_t u1[16], u2[16], w1[16], w2[16];
-                tmem_ld16(tU + uint32_t(c) + lane_off, u1);
-                tmem_ld16(tU + uint32_t(c + half) + lane_off, u2);
-                tmem_ld16(tW + uint32_t(c) + lane_off, w1);
-                tmem_ld16(tW + uint32_t(c + half) + lane_off, w2);
+                tmem_ld16(tmem + Ly::TU + uint32_t(c) + lane_off, u1);
+                tmem_ld16(tmem + Ly::TU + uint32_t(c + half) + lane_off, u2);
+                tmem_ld16(tmem + Ly::TW + uint32_t(c) + lane_off, w1);
+                tmem_ld16(tmem + Ly::TW + uint32_t(c + half) + lane_off, w2);
                 tmem_wait_ld();
                 float y1[16], y2[16];
 #pragma unroll
@@ -352,7 +347,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
     __syncthreads();
     if (s_abort && threadIdx.x == 0) {
         for (int v = s_v_used; v < s_v_issued; ++v) mbar_wait(&vfull[v & 1], (v >> 1) & 1, nullptr, 0u);
-        for (int k = s_kt_used; k < s_kt_issued; ++k) mbar_wait(&ktfull, k & 1, nullptr, 0u);
+        for (int k = s_k_used; k < s_k_issued; ++k) mbar_wait(&kfull[k & 1], (k >> 1) & 1, nullptr, 0u);
     }
     __syncthreads();
     if (warp == 1) {
@@ -367,7 +362,8 @@ template <int HD>
 struct DvLayout {
     static constexpr int A_BYTES = kVK * kVQ * 4;        // P^T [128 keys][64 queries]: 2 boxes
     static constexpr int B_BYTES = HD * kVQ * 4;         // dCtx^T [HD][64 queries]: 2 boxes
-    static constexpr int A0 = 0, B0 = 2 * A_BYTES, TOTAL = B0 + 2 * B_BYTES;
+    static constexpr int S_BYTES = kVQ * kVK * 4;        // P [64 queries][128 keys]: 4 boxes
+    static constexpr int A0 = 0, B0 = 2 * A_BYTES, P0 = B0 + 2 * B_BYTES, TOTAL = P0 + 2 * S_BYTES;
     static constexpr uint32_t COLS = HD <= 32 ? 32 : (HD <= 64 ? 64 : (HD <= 128 ? 128 : 256));
 };
 
@@ -376,24 +372,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
     using Ly = DvLayout<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    __shared__ uint64_t bfull[2], bempty[2], afull[2], aempty[2], dfull;
+    __shared__ uint64_t bfull[2], bfree[2], afull[2], afree[2], dfull;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort, s_b_issued, s_b_used;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kvh = blockIdx.y, G = p.nh / p.nkv;
-    const int k0 = int(blockIdx.x) * kVK;                 // among the S newest keys
+    const int h = blockIdx.x, G = p.nh / p.nkv, kvh = h / G, g = h % G;
+    const int k0 = int(blockIdx.y) * kVK;                 // among the S newest keys (heaviest first)
     const int t0 = p.causal ? k0 / kVQ : 0;               // first query tile that sees key k0
-    const int nqt = (p.S + kVQ - 1) / kVQ;
-    const int nq = nqt - t0, nw = G * nq;                 // work items (head of group, query tile)
+    const int nw = (p.S + kVQ - 1) / kVQ - t0;            // query tiles of this CTA
 
     if (threadIdx.x == 0) {
         s_abort = 0;
         s_b_issued = s_b_used = 0;
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bfull[s], 1);
-            mbar_init(&bempty[s], 1);
+            mbar_init(&bfree[s], 1);
             mbar_init(&afull[s], 4);
-            mbar_init(&aempty[s], 1);
+            mbar_init(&afree[s], 1);
         }
         mbar_init(&dfull, 1);
     }
@@ -410,11 +405,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
     if (warp == 0) {
         if (lane == 0) {
             for (int w = 0; w < nw; ++w) {
-                const int s = w & 1, h = kvh * G + w / nq, qa = (t0 + w % nq) * kVQ;
-                if (w >= 2 && !mbar_wait(&bempty[s], ((w - 2) >> 1) & 1, p.status, 30u)) { s_abort = 1; break; }
-                mbar_arrive_expect_tx(&bfull[s], Ly::B_BYTES);
+                const int s = w & 1, qa = (t0 + w) * kVQ;
+                if (w >= 2 && !mbar_wait(&bfree[s], ((w - 2) >> 1) & 1, p.status, 30u)) { s_abort = 1; break; }
+                mbar_arrive_expect_tx(&bfull[s], Ly::B_BYTES + Ly::S_BYTES);
                 for (int b = 0; b < 2; ++b)
                     tma_load_3d(sm + Ly::B0 + s * Ly::B_BYTES + b * (HD * 128), &p.dct, qa + b * 32, 0, h, &bfull[s]);
+                for (int b = 0; b < kVK / 32; ++b)
+                    tma_load_3d(sm + Ly::P0 + s * Ly::S_BYTES + b * (kVQ * 128), &p.pv, p.pos0 + k0 + b * 32, qa, h,
+                                &bfull[s]);
                 s_b_issued = w + 1;
             }
         }
@@ -424,8 +422,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
             bool ok = true;
             for (int w = 0; w < nw; ++w) {
                 const int s = w & 1;
-                if (!mbar_wait(&bfull[s], (w >> 1) & 1, p.status, 31u) ||
-                    !mbar_wait(&afull[s], (w >> 1) & 1, p.status, 32u)) {
+                if (!mbar_wait(&afull[s], (w >> 1) & 1, p.status, 31u) ||
+                    !mbar_wait(&bfull[s], (w >> 1) & 1, p.status, 32u)) {
                     ok = false;
                     break;
                 }
@@ -437,8 +435,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
                     for (int k = 0; k < 4; ++k)
                         mma_tf32(tD, sw128_desc(a + kb * (kVK * 128)) + 2 * k, sw128_desc(b + kb * (HD * 128)) + 2 * k,
                                  id, (w > 0 || kb > 0 || k > 0) ? 1u : 0u);
-                mma_commit(&bempty[s]);
-                mma_commit(&aempty[s]);
+                mma_commit(&bfree[s]);
+                mma_commit(&afree[s]);
                 s_b_used = w + 1;
             }
             if (!ok) s_abort = 1;
@@ -450,33 +448,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane, jj = k0 + r;        // key row of this thread
         const bool key_ok = jj < p.S;
+        const int box = r >> 5, col = r & 31;
         bool ok = true;
-        for (int w = 0; w < nw && ok; ++w) {
-            const int s = w & 1, h = kvh * G + w / nq, qa = (t0 + w % nq) * kVQ;
-            const float *pc = p.attn + int64_t(h) * p.S * p.L + p.pos0 + (key_ok ? jj : 0);
-            float pv[kVQ];
+        for (int w = 0; w < nw; ++w) {
+            const int s = w & 1, qa = (t0 + w) * kVQ;
+            if (!mbar_wait(&bfull[s], (w >> 1) & 1, p.status, 33u)) { ok = false; break; }
+            const uint8_t *ps = sm + Ly::P0 + s * Ly::S_BYTES + box * (kVQ * 128) + (col & 3) * 4;
+            uint32_t pt[kVQ];
 #pragma unroll
             for (int qq = 0; qq < kVQ; ++qq) {
-                const int q = qa + qq;
-                const bool vis = key_ok && q < p.S && (!p.causal || q >= jj);
-                pv[qq] = vis ? __ldg(pc + int64_t(q) * p.L) : 0.f;
+                const float v = *reinterpret_cast<const float *>(ps + sw128_off(qq, col >> 2));
+                const bool vis = key_ok && (!p.causal || qa + qq >= jj);   // rows past S arrive as zeros
+                pt[qq] = to_tf32(vis ? v : 0.f);
             }
-            if (w >= 2 && !mbar_wait(&aempty[s], ((w - 2) >> 1) & 1, p.status, 33u)) { ok = false; break; }
+            if (w >= 2 && !mbar_wait(&afree[s], ((w - 2) >> 1) & 1, p.status, 34u)) { ok = false; break; }
             uint8_t *a = sm + Ly::A0 + s * Ly::A_BYTES;
 #pragma unroll
             for (int c4 = 0; c4 < kVQ / 4; ++c4) {
                 const uint32_t off = uint32_t(c4 >> 3) * (kVK * 128) + sw128_off(r, c4 & 7);
-                st_shared_v4(a + off, to_tf32(pv[4 * c4]), to_tf32(pv[4 * c4 + 1]), to_tf32(pv[4 * c4 + 2]),
-                             to_tf32(pv[4 * c4 + 3]));
+                st_shared_v4(a + off, pt[4 * c4], pt[4 * c4 + 1], pt[4 * c4 + 2], pt[4 * c4 + 3]);
             }
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(&afull[s]);
         }
-        if (ok && mbar_wait(&dfull, 0, p.status, 34u)) {
+        if (ok && mbar_wait(&dfull, 0, p.status, 35u)) {
             tc_fence_after();
             const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-            float *out = p.dv + int64_t(key_ok ? jj : 0) * (p.nkv * HD) + kvh * HD;
+            const int64_t kvd = int64_t(p.nkv) * HD;
+            float *out = p.dv + (G > 1 ? int64_t(g) * p.S * kvd : 0) + int64_t(key_ok ? jj : 0) * kvd + kvh * HD;
 #pragma unroll 1
             for (int c = 0; c < HD; c += 32) {
                 uint32_t v[32];
@@ -505,6 +505,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
     }
 }
 
+// dV[jj, c] = sum over the group's heads g (in order) of part[g][jj, c]
+__global__ void attn_tc_dv_sum_kernel(const float4 *__restrict__ part, float4 *__restrict__ dv, int64_t n4, int G) {
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n4; e += int64_t(gridDim.x) * blockDim.x) {
+        float4 s = part[e];
+        for (int g = 1; g < G; ++g) {
+            const float4 t = part[int64_t(g) * n4 + e];
+            s.x += t.x;
+            s.y += t.y;
+            s.z += t.z;
+            s.w += t.w;
+        }
+        dv[e] = s;
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 // fp32 3-D tensor map, 128-byte swizzle, zero fill out of range.  dims / box innermost
@@ -525,7 +540,7 @@ int make_map_f32_3d(CUtensorMap *m, const void *base, const uint64_t dims[3], co
 }
 
 struct TcAttnWs {
-    size_t dCr, dCT, Kt, Vr, total;
+    size_t dCr, dCT, Kt, Vr, part, total;
     int64_t S4, L4;
 };
 
@@ -538,7 +553,8 @@ TcAttnWs tc_attn_layout(int64_t S, int64_t L, int nh, int nkv, int hd) {
     w.dCT = w.dCr + r256(size_t(nh) * S * hd * 4);
     w.Kt = w.dCT + r256(size_t(nh) * hd * w.S4 * 4);
     w.Vr = w.Kt + r256(size_t(nkv) * hd * w.L4 * 4);
-    w.total = w.Vr + r256(size_t(nkv) * L * hd * 4);
+    w.part = w.Vr + r256(size_t(nkv) * L * hd * 4);
+    w.total = w.part + (nh > nkv ? r256(size_t(nh) * S * hd * 4) : 0);   // per-head dV sums
     return w;
 }
 
@@ -568,6 +584,13 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
         TLB_TRY(make_map_f32_3d(&p.v, Vr, d, s, b));
     }
     {
+        const uint64_t d[3] = {uint64_t(a.L), uint64_t(a.S), uint64_t(a.nh)};
+        const uint64_t s[2] = {uint64_t(a.L) * 4, uint64_t(a.S) * a.L * 4};
+        const uint32_t bq[3] = {32, uint32_t(kQM), 1}, bv[3] = {32, uint32_t(kVQ), 1};
+        TLB_TRY(make_map_f32_3d(&p.pq, a.attn, d, s, bq));
+        TLB_TRY(make_map_f32_3d(&p.pv, a.attn, d, s, bv));
+    }
+    {
         const uint64_t d[3] = {uint64_t(a.L), uint64_t(HD), uint64_t(a.nkv)};
         const uint64_t s[2] = {uint64_t(w.L4) * 4, uint64_t(w.L4) * HD * 4};
         const uint32_t b[3] = {32, uint32_t(HD), 1};
@@ -579,9 +602,10 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
         const uint32_t b[3] = {32, uint32_t(HD), 1};
         TLB_TRY(make_map_f32_3d(&p.dct, dCT, d, s, b));
     }
-    p.attn = a.attn;
+    const int G = a.nh / a.nkv;
+    float *part = reinterpret_cast<float *>(base + w.part);
     p.dq = a.dq;
-    p.dv = a.dv;
+    p.dv = G > 1 ? part : a.dv;
     p.S = a.S;
     p.L = a.L;
     p.nh = a.nh;
@@ -589,7 +613,6 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     p.pos0 = a.pos0;
     p.causal = a.causal;
     p.rope = a.rope;
-    p.vecP = (a.L % 4 == 0 && aligned16(a.attn)) ? 1 : 0;
     p.scale = a.scale;
     p.status = status;
     p.fr = fr;
@@ -599,15 +622,21 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     TLB_CUDA(cudaFuncSetAttribute(attn_tc_dv_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smv));
     attn_tc_dq_kernel<HD><<<dim3(unsigned(ceil_div(a.S, kQM)), unsigned(a.nh)), kAttnThreads, smq, st>>>(p);
     TLB_TRY(check_launch("attn_tc_dq"));
-    attn_tc_dv_kernel<HD><<<dim3(unsigned(ceil_div(a.S, kVK)), unsigned(a.nkv)), kAttnThreads, smv, st>>>(p);
-    return check_launch("attn_tc_dv");
+    attn_tc_dv_kernel<HD><<<dim3(unsigned(a.nh), unsigned(ceil_div(a.S, kVK))), kAttnThreads, smv, st>>>(p);
+    TLB_TRY(check_launch("attn_tc_dv"));
+    if (G == 1) return TLB_OK;
+    const int64_t n4 = int64_t(a.S) * a.nkv * HD / 4;
+    attn_tc_dv_sum_kernel<<<stream_grid(n4, 256), 256, 0, st>>>(reinterpret_cast<const float4 *>(part),
+                                                                reinterpret_cast<float4 *>(a.dv), n4, G);
+    return check_launch("attn_tc_dv_sum");
 }
 
 }  // namespace
 
 bool attn_tc_supported(int64_t S, int64_t L, int nh, int nkv, int hd) {
-    return S > 1 && S <= L && (hd == 64 || hd == 128) && nh <= 65535 && nkv <= 65535 && nh % nkv == 0 &&
-           L < (int64_t(1) << 30);
+    // TMA reads attn rows from key L - S on: L and L - S multiples of 4 (16-byte starts)
+    return S > 1 && S <= L && L % 4 == 0 && (L - S) % 4 == 0 && (hd == 64 || hd == 128) && nh <= 65535 &&
+           nkv <= 65535 && nh % nkv == 0 && L < (int64_t(1) << 30);
 }
 
 size_t attn_tc_bytes(int64_t S, int64_t L, int nh, int nkv, int hd) {
@@ -618,6 +647,8 @@ int attn_tc_launch(const AttnArgs &a, float rope_base, void *scratch, uint32_t *
     if (a.S == 0) return TLB_OK;
     TLB_REQUIRE(attn_tc_supported(a.S, a.L, a.nh, a.nkv, a.hd), TLB_EUNSUPPORTED, "attention (tcgen05): shape");
     TLB_REQUIRE((reinterpret_cast<uintptr_t>(scratch) & 255u) == 0, TLB_EINVAL, "attention (tcgen05): scratch alignment");
+    TLB_REQUIRE(aligned16(a.attn) && aligned16(a.dq) && aligned16(a.dv), TLB_EUNSUPPORTED,
+                "attention (tcgen05): attn / dq / dv not 16-byte aligned");
     RopeFreqs fr;
     rope_freqs(fr, a.hd, rope_base);
     return a.hd == 128 ? launch_attn_tc<128>(a, fr, scratch, status, st) : launch_attn_tc<64>(a, fr, scratch, status, st);

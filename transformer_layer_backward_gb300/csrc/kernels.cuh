@@ -62,8 +62,8 @@ struct AttnArgs {
 };
 int attn_core_launch(const AttnArgs &a, float rope_base, cudaStream_t st);
 
-// Tensor-core (tf32) attention backward (attn_tc.cu): S > 1, head_dim 64 or 128; dq and
-// dv 16-byte aligned.  scratch: attn_tc_bytes(...) bytes, 256-byte aligned.
+// Tensor-core (tf32) attention backward (attn_tc.cu): S > 1, head_dim 64 or 128, L and
+// L - S multiples of 4; attn, dq and dv 16-byte aligned.  scratch: attn_tc_bytes(...) bytes, 256-byte aligned.
 bool attn_tc_supported(int64_t S, int64_t L, int nh, int nkv, int hd);
 size_t attn_tc_bytes(int64_t S, int64_t L, int nh, int nkv, int hd);
 int attn_tc_launch(const AttnArgs &a, float rope_base, void *scratch, uint32_t *status, cudaStream_t st);

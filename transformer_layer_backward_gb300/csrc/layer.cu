@@ -190,7 +190,7 @@ int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, co
     g.causal = (c.flags & TLB_CAUSAL) ? 1 : 0;
     g.rope = (c.flags & TLB_ROPE) ? 1 : 0;
     g.scale = c.attn_scale;
-    if (attn_tc_route(c, S, L) && aligned16(d_qpre) && aligned16(d_v))
+    if (attn_tc_route(c, S, L) && aligned16(d_qpre) && aligned16(d_v) && aligned16(a.attn))
         return attn_tc_launch(g, c.rope_base, ws_at<void>(ws, p.atc), ws_at<uint32_t>(ws, 0), st);
     return attn_core_launch(g, c.rope_base, st);
 }
