@@ -154,7 +154,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "decode layer backward (configs[1]): dim 2560, ffn 6912, 20/5 heads x 128, "
+            "config": {"workload": "decode layer backward: dim 2560, ffn 6912, 20/5 heads x 128, "
                                    "cache 1024, ternary, LoRA r16", "global_batch": 1, "seq_len": 1,
                        "parallelism": "replicas"},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
@@ -345,7 +345,7 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": {"workload": "decode layer backward (configs[1]): dim 2560, ffn 6912, 20/5 heads "
+                "config": {"workload": "decode layer backward: dim 2560, ffn 6912, 20/5 heads "
                                        "x 128, cache 1024, pos 1023, ternary int8 weights, ReLU^2xMul, "
                                        "sub-norms, LoRA r16 Q/V, AdamW+LoRA+",
                            "global_batch": world, "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
