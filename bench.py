@@ -9,10 +9,17 @@ working set (NL x 68 MB) is several times the 129 MB L2 and each step reads its
 inputs from HBM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tlb|reference]
+                  [--workload decode|seq512|seq2048|stack2048]
 
 --impl reference times the float64 CPU oracle (the only other implementation of
 this path available here) on the same workload.  Under torchrun every rank runs
 its own replica (the path has no exchange step); rank 0 prints one JSON line.
+
+The sequence workloads (bf16 weights, SwiGLU, RoPE, residual, GQA 32/8 x 128, LoRA
+rank 16; the tcgen05 path): seq512 and seq2048 time one layer backward of S tokens
+per step; stack2048 times the 36-layer stack (S = 2048) per step, d_in of each layer
+feeding the next.  Their inputs are drawn on the device with torch's seeded
+generator, with the shapes and distributions of the parity inputs.
 """
 from __future__ import annotations
 
@@ -44,6 +51,7 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=2000)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--workload", default="decode", choices=["decode", "seq512", "seq2048", "stack2048"])
     return p.parse_args()
 
 
@@ -140,6 +148,22 @@ def host_threads():
 def run_reference(args, rank, world):
     if rank != 0:
         return
+    if args.workload != "decode":
+        per = max(args.cpu_seconds / max(args.steps, 1), 0.0)
+        vals = [seq_cpu_baseline(per)["value"] for _ in range(args.steps)]
+        v = statistics.mean(vals)
+        cpu = seq_cpu_baseline(0.0)
+        cpu["value"] = v
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 512 / v * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": "sequence layer backward sample: one S = 512 layer per step "
+                                       "(float64 oracle on the host cores)", "global_batch": 1, "seq_len": 512,
+                           "parallelism": "replicas"},
+                "cpu_baseline": cpu,
+                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
     from synth import DECODE
     cfg = DECODE
     per = max(args.cpu_seconds / max(args.steps, 1), 0.0)
@@ -163,6 +187,259 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- sequence workloads
+
+def seq_config(workload):
+    from synth import SEQ512
+    if workload == "seq512":
+        return SEQ512, 1
+    return SEQ512.with_(name=workload, seq_len=2048, cache_len=2048), (36 if workload == "stack2048" else 1)
+
+
+def device_layer(cfg, layer, seed=0):
+    """One layer's weights, caches, adapters and dOut on the device (bf16 weights),
+    drawn with the distributions of the parity inputs: weights N(0, weight_std^2),
+    activations and caches N(0, 1), attn = causal softmax of N(0, attn_logit_std^2)
+    logits, LoRA A and B N(0, 0.02^2), h = x A^T, AdamW moments zero."""
+    import torch
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1000003 * seed + 7919 * layer + 17)
+    S, L, H, I, qd, kvd, r = cfg.seq_len, cfg.cache_len, cfg.dim, cfg.ffn_dim, cfg.q_dim, cfg.kv_dim, cfg.rank
+    n = lambda *shape, std=1.0: torch.randn(*shape, device="cuda", generator=g) * std
+    t = {}
+    for k, shape in (("w_down", (I, H)), ("w_gate", (H, I)), ("w_up", (H, I)), ("w_o", (qd, H))):
+        t[k] = n(*shape, std=cfg.weight_std).to(torch.bfloat16)
+    for k, shape in (("x", (S, H)), ("gate", (S, I)), ("up", (S, I)), ("dout", (S, H)),
+                     ("k", (L, kvd)), ("v", (L, kvd))):
+        t[k] = n(*shape)
+    t["silu_gate"] = torch.nn.functional.silu(t["gate"])
+    pos0 = L - S
+    attn = torch.empty(cfg.n_heads, S, L, device="cuda")
+    mask = torch.arange(L, device="cuda")[None, :] > (pos0 + torch.arange(S, device="cuda"))[:, None]
+    for h in range(cfg.n_heads):
+        logits = n(S, L, std=cfg.attn_logit_std).masked_fill_(mask, float("-inf"))
+        attn[h] = torch.softmax(logits, dim=-1)
+    t["attn"] = attn
+    for k, shape in (("a_q", (r, H)), ("b_q", (qd, r)), ("a_v", (r, H)), ("b_v", (kvd, r))):
+        t[k] = n(*shape, std=0.02)
+        t["m_" + k] = torch.zeros_like(t[k])
+        t["v_" + k] = torch.zeros_like(t[k])
+    t["lora_q_h"] = t["x"] @ t["a_q"].t()
+    t["lora_v_h"] = t["x"] @ t["a_v"].t()
+    return t
+
+
+def seq_kernel_flops(cfg, names):
+    """Algorithmic flops of each kernel of one sequence layer, by launch order: the
+    three tcgen05 GEMMs are W_down^T, [W_gate | W_up]^T and W_O^T; the attention counts
+    the visible (query, key) pairs; 'tf32' marks the attention contractions."""
+    S, L, H, I, qd = cfg.seq_len, cfg.cache_len, cfg.dim, cfg.ffn_dim, cfg.q_dim
+    pairs = S * (L - S) + S * (S + 1) // 2
+    gemm = [2 * S * I * H, 2 * S * H * 2 * I, 2 * S * qd * H]
+    out, gi = [], 0
+    for nm in names:
+        if nm == "tcgen05 gemm":
+            out.append((gemm[gi] if gi < 3 else 0, "bf16"))
+            gi += 1
+        elif nm == "attn_tc_dq":
+            out.append((3 * 2 * pairs * cfg.head_dim * cfg.n_heads, "tf32"))
+        elif nm == "attn_tc_dv":
+            out.append((2 * pairs * cfg.head_dim * cfg.n_heads, "tf32"))
+        else:
+            out.append((0, None))
+    return out
+
+
+def seq_main(args, rank, world, local, dist):
+    import torch
+    import transformer_layer_backward_gb300 as tlb
+    from tests.helpers import adam_to_abi, cfg_to_abi
+
+    torch.cuda.set_device(local)
+    tlb.load()
+    cfg, depth = seq_config(args.workload)
+    S, L = cfg.seq_len, cfg.cache_len
+    NL = 2 if depth == 1 and S <= 512 else (2 if depth > 1 else 1)
+    c = cfg_to_abi(tlb, cfg)
+    adam = adam_to_abi(tlb, cfg)
+    layers = []
+    for l in range(NL):
+        t = device_layer(cfg, l, seed=rank)
+        layers.append(dict(t=t, w=tlb.layer_weights(c, t), a=tlb.layer_acts(c, t, cfg.kv_layout, L),
+                           lq=tlb.lora(t, "q"), lv=tlb.lora(t, "v")))
+    ws = tlb.workspace(c, S, L)
+    dh = torch.empty(S, cfg.dim, device="cuda")
+    ss = torch.zeros(2, dtype=torch.float64, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def layer_call(j):
+        ly = layers[j % NL]
+        tlb.layer_backward(c, S, L, ly["w"], ly["a"], ly["lq"], ly["lv"], adam, dh, ss, ws)
+
+    def step(i):
+        dh.copy_(layers[i % NL]["t"]["dout"])
+        for j in range(depth):
+            layer_call(i * depth + j)
+
+    graphs = None
+    if not args.no_graph:
+        for i in range(NL):
+            step(i)
+        torch.cuda.synchronize()
+        graphs = []
+        for i in range(NL):
+            gph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gph):
+                step(i)
+            graphs.append(gph)
+        torch.cuda.synchronize()
+
+    def run(i):
+        if graphs is not None:
+            graphs[i % NL].replay()
+        else:
+            step(i)
+
+    n0 = tlb.launch_count()
+    step(0)
+    launches_per_step = tlb.launch_count() - n0
+    for i in range(max(args.warmup, 3)):
+        run(i)
+    tlb.workspace_status(ws)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        run(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    tlb.workspace_status(ws)
+    t_local = torch.tensor([ms], device="cuda", dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
+    ms_max = float(t_local.item())
+    value = args.steps * S * world / (ms_max / 1e3)
+
+    # per-kernel times of one layer, live, inside a CUDA graph of nk layer calls
+    nk, ne = 8, 64
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ne)] for _ in range(nk)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    keep = []
+    pg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(pg):
+        for i in range(nk):
+            dh.copy_(layers[i % NL]["t"]["dout"])
+            keep.append(tlb.profile_events(evs[i]))
+            layer_call(i)
+        lib = tlb._abi.load()
+        names = []
+        while True:
+            nm = lib.tlb_profile_kernel_name(len(names))
+            if nm is None:
+                break
+            names.append(nm.decode())
+        tlb.profile_events(None)
+    pg.replay()
+    torch.cuda.synchronize()
+    nkern = min(len(names), ne - 1)
+    ktime = [sum(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(nk)) / nk for k in range(nkern)]
+    del keep
+    fl = seq_kernel_flops(cfg, names[:nkern])
+    pk = peaks()
+    bf16_peak = pk["bf16_tflops_sustained"] if pk else 1700.0
+    tf32_peak = bf16_peak * 1.1 / 2.25
+    per_kernel = []
+    for nm, t, (f, kind) in zip(names, ktime, fl):
+        e = {"kernel": nm, "us": t * 1e3}
+        if f:
+            e.update({"flop": f, "TFLOP/s": f / (t / 1e3) / 1e12, "operands": kind})
+        per_kernel.append(e)
+    dom = max((k for k in range(nkern) if fl[k][0]), key=lambda k: ktime[k])
+    achieved = fl[dom][0] / (ktime[dom] / 1e3) / 1e12
+    peak = bf16_peak if fl[dom][1] == "bf16" else tf32_peak
+
+    # end to end through the public API: the step's activations and caches from pinned host
+    # memory every step, d_in and the gradient sums read back
+    acts = ("x", "gate", "up", "silu_gate", "k", "v", "attn", "lora_q_h", "lora_v_h", "dout")
+    pinned = [{k: layers[l]["t"][k].cpu().pin_memory() for k in acts} for l in range(NL)]
+    h2d = sum(pinned[0][k].numel() * 4 for k in acts) * depth
+    res_h = torch.empty(S, cfg.dim, pin_memory=True)
+    ss_h = torch.empty(2, dtype=torch.float64, pin_memory=True)
+    d2h = res_h.numel() * 4 + 16
+    n_e2e = max(3, min(args.steps, 20))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        dh.copy_(layers[i % NL]["t"]["dout"])
+        for j in range(depth):
+            ly = layers[(i * depth + j) % NL]
+            for k in acts:
+                ly["t"][k].copy_(pinned[(i * depth + j) % NL][k], non_blocking=True)
+            if j == 0:
+                dh.copy_(ly["t"]["dout"])
+            layer_call(i * depth + j)
+        res_h.copy_(dh, non_blocking=True)
+        ss_h.copy_(ss, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": n_e2e * S * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        cpu = seq_cpu_baseline(args.cpu_seconds)
+
+    if rank == 0:
+        wl = {"seq512": "sequence layer backward S = L = 512",
+              "seq2048": "sequence layer backward S = L = 2048",
+              "stack2048": "36-layer stack backward, S = L = 2048 (one step = 36 layer calls)"}[args.workload]
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (device generator)",
+                "config": {"workload": wl + ": dim 2560, ffn 9728, 32/8 heads x 128, SwiGLU, RoPE, residual, "
+                                       "bf16 weights, LoRA r16 Q/V, AdamW+LoRA+",
+                           "global_batch": world, "seq_len": S, "layers_per_step": depth,
+                           "parallelism": "replicas" if world > 1 else "single",
+                           "layers_cycled": NL, "l2": "inputs > L2 (weights 170 MB and attn %.0f MB per layer)"
+                                                       % (cfg.n_heads * S * L * 4 / 1e6),
+                           "cuda_graph": graphs is not None},
+                "layer_tokens_per_s": value * depth,
+                "roofline": {"bound": "tensor", "kernel": names[dom], "achieved": achieved, "peak": peak,
+                             "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                             "algorithmic_flop": fl[dom][0],
+                             "peak_source": ("MEASURED_PEAKS.json bf16_tflops_sustained (of measured)" if pk else
+                                             "fallback") + ("" if fl[dom][1] == "bf16" else " x 1.1/2.25 for tf32")},
+                "per_kernel": per_kernel, "per_kernel_timing": "graph",
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk}
+        print(json.dumps(line), flush=True)
+
+
+def seq_cpu_baseline(seconds):
+    """The float64 oracle on the S = 512 layer (its own seeded inputs), tokens/s."""
+    from oracle import layer as OL
+    from synth import SEQ512, layer_inputs
+    d = layer_inputs(SEQ512, layer=0, seed=0)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        OL.layer_backward(SEQ512, d, d["dout"])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n >= 100:
+            break
+    return {"value": n * SEQ512.seq_len / el, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
+            "sample": "%d float64 oracle backwards of one S = 512 layer" % n}
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -176,6 +453,12 @@ def main():
         dist.init_process_group("nccl")
     if args.impl == "reference":
         run_reference(args, rank, world)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    if args.workload != "decode":
+        seq_main(args, rank, world, local, dist)
         if dist is not None:
             dist.destroy_process_group()
         return

@@ -154,6 +154,9 @@ uint64_t tlb_launch_count(void);
  * Events are cudaEvent_t passed as void*.  Process-wide setting: do not use while other
  * threads call the library. */
 void tlb_profile_events(void *const *events, int32_t n);
+/* Name of the k-th kernel (from 0) of the last layer call profiled with
+ * tlb_profile_events, or NULL past its last kernel.  Owned by the library. */
+const char *tlb_profile_kernel_name(int32_t k);
 
 /* ---------------------------------------------------------------- standalone steps */
 

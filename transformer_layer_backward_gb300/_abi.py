@@ -57,6 +57,7 @@ SIGNATURES = {
     "tlb_build_info": (C.c_char_p, []),
     "tlb_launch_count": (C.c_uint64, []),
     "tlb_profile_events": (None, [C.POINTER(C.c_void_p), i32]),
+    "tlb_profile_kernel_name": (C.c_char_p, [i32]),
     "tlb_linear_workspace_bytes": (sz, [i32, i64, i64, i64]),
     "tlb_linear_backward": (C.c_int, [i32, vp, f32, vp, i64, i64, i64, vp, i32, vp, sz, vp]),
     "tlb_softmax_backward": (C.c_int, [vp, vp, vp, i64, i64, vp]),

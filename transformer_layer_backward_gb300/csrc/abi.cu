@@ -14,13 +14,28 @@ static thread_local char g_err[512] = "";
 static unsigned long long g_launches = 0;
 static void *const *g_prof_events = nullptr;
 static int g_prof_n = 0;
+// the layer call being profiled: its stream, kernels so far and their names
+static bool g_prof_on = false;
+static cudaStream_t g_prof_stream = nullptr;
+static int g_prof_k = 0;
+static const char *g_prof_names[256];
 
-void profile_mark(int i, cudaStream_t st) {
+static void prof_record(int i, cudaStream_t st) {
     // external record: inside a stream capture this becomes an event node whose
     // timestamps remain readable with cudaEventElapsedTime after the graph runs
-    if (g_prof_events != nullptr && i + 1 < g_prof_n && i >= -1)
-        cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(g_prof_events[i + 1]), st, cudaEventRecordExternal);
+    if (g_prof_events != nullptr && i >= 0 && i < g_prof_n)
+        cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(g_prof_events[i]), st, cudaEventRecordExternal);
 }
+
+ProfileScope::ProfileScope(cudaStream_t st) {
+    if (g_prof_events == nullptr) return;
+    g_prof_on = true;
+    g_prof_stream = st;
+    g_prof_k = 0;
+    prof_record(0, st);
+}
+
+ProfileScope::~ProfileScope() { g_prof_on = false; }
 
 void set_error(const char *fmt, ...) {
     va_list ap;
@@ -37,6 +52,11 @@ int check_launch(const char *what) {
     if (e != cudaSuccess) {
         set_error("%s: kernel launch failed: %s", what, cudaGetErrorString(e));
         return TLB_ECUDA;
+    }
+    if (g_prof_on) {
+        if (g_prof_k < 256) g_prof_names[g_prof_k] = what;
+        ++g_prof_k;
+        prof_record(g_prof_k, g_prof_stream);
     }
     return TLB_OK;
 }
@@ -103,6 +123,11 @@ uint64_t tlb_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_R
 void tlb_profile_events(void *const *events, int32_t n) {
     g_prof_events = events;
     g_prof_n = events != nullptr && n > 0 ? n : 0;
+    g_prof_on = false;
+}
+
+const char *tlb_profile_kernel_name(int32_t k) {
+    return (k >= 0 && k < g_prof_k && k < 256) ? g_prof_names[k] : nullptr;
 }
 
 size_t tlb_linear_workspace_bytes(int32_t wtype, int64_t S, int64_t out_dim, int64_t in_dim) {

@@ -42,9 +42,13 @@ void clear_error();
 // Error of the last launch on this thread (a launch error never enqueues work).
 int check_launch(const char *what);
 
-// Record profiling event i + 1 (tlb_profile_events) on st, if profiling is on: i = -1 at
-// the start of a layer call, i = k after its k-th kernel.
-void profile_mark(int i, cudaStream_t st);
+// Profiling of one layer call (tlb_profile_events): while a ProfileScope lives, event 0
+// is recorded at its start and event k after the k-th kernel launched through
+// check_launch, on the scope's stream, and the kernels' names are kept.
+struct ProfileScope {
+    explicit ProfileScope(cudaStream_t st);
+    ~ProfileScope();
+};
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 

@@ -634,31 +634,25 @@ template <int WT>
 int launch_all(const DecodeArgs &a, cudaStream_t st) {
     TLB_CUDA(launch(dec_k1<WT>, dim3(unsigned(a.n1)), size_t(a.H) * 4, st, false, a));
     TLB_TRY(check_launch("decode k1"));
-    profile_mark(0, st);
     const size_t sm2 = size_t(2) * (a.I / a.ns2) * 4;
     const dim3 g2(unsigned(a.n2), unsigned(a.ns2));
     if (a.act == TLB_ACT_RELU2_MUL) TLB_CUDA(launch(dec_k2<WT, TLB_ACT_RELU2_MUL>, g2, sm2, st, false, a));
     else TLB_CUDA(launch(dec_k2<WT, TLB_ACT_SILU_MUL>, g2, sm2, st, false, a));
     TLB_TRY(check_launch("decode k2"));
-    profile_mark(1, st);
     TLB_CUDA(launch(dec_k3<WT>, dim3(unsigned(a.n3), unsigned(a.ns3)), size_t(a.H / a.ns3) * 4, st, false, a));
     TLB_TRY(check_launch("decode k3"));
-    profile_mark(2, st);
     const int G = a.nh / a.nkv;
     const dim3 g4(a.nkv, a.nchunks);
     const size_t sm4 = (size_t(G) * a.hd + size_t(kAWarps) * G * 2 * a.hd) * 4;
     TLB_CUDA(launch_k4(G, a.hd, g4, sm4, st, a));
     TLB_TRY(check_launch("decode k4"));
-    profile_mark(3, st);
     RopeFreqs fr;
     rope_freqs(fr, a.hd, a.rope_base);
     TLB_CUDA(launch(dec_k6, dim3(a.nh), 0, st, false, a, fr));
     TLB_TRY(check_launch("decode k6"));
-    profile_mark(4, st);
     const int64_t n7 = int64_t(a.qd + a.kvd) * a.rank + 2 * int64_t(a.rank) * a.H;
     TLB_CUDA(launch(dec_k7, dim3(unsigned(ceil_div(n7, kThreads))), 0, st, false, a));
     TLB_TRY(check_launch("decode k7"));
-    profile_mark(5, st);
     return TLB_OK;
 }
 

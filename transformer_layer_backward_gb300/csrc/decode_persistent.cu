@@ -714,7 +714,6 @@ int launch_p(const PArgs &p, size_t dyn, cudaStream_t st) {
     cfg.numAttrs = 1;
     TLB_CUDA(cudaLaunchKernelEx(&cfg, k, p));
     TLB_TRY(check_launch("decode persistent"));
-    profile_mark(0, st);
     return TLB_OK;
 }
 

@@ -305,7 +305,7 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
     const tlb_layer_cfg &c = *cfg;
     const LayerWs p = plan(c, S, L);
     const int qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
-    profile_mark(-1, st);
+    ProfileScope prof(st);
     float *dqpre = ws_at<float>(ws, p.dqpre), *dv = ws_at<float>(ws, p.dv);
     bool vec_ok = true;   // the single-token kernels read every vector with 16-byte loads
     for (const void *ptr : {(const void *)w->w_down.w, (const void *)w->w_gate.w, (const void *)w->w_up.w,
