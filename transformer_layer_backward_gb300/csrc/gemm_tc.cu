@@ -4,20 +4,31 @@
 // (= [N, K], K-major), fp32 accumulation in tensor memory ([FFN] W_down^T, W_gate^T,
 // W_up^T products; [ATT] O-projection backward; [RS] gemm_backward_a).
 //
-// One CTA computes one 128 x BN tile (cta_group::1):
+// Persistent: one CTA per SM walks its share of the work, tile segment by tile segment
+// (cta_group::1):
 //   warp 0      TMA producer: 128x64 (A) and BNx64 (B) bf16 tiles, 128-byte swizzle,
-//               into a STAGES-deep shared-memory ring guarded by mbarriers
-//   warp 1      allocates BN TMEM columns; one thread issues tcgen05.mma.kind::f16
-//               (M = 128, N = BN, K = 16) four times per 64-wide k block, and
-//               tcgen05.commit frees each stage when its MMAs have completed
+//               into a STAGES-deep shared-memory ring guarded by mbarriers; the ring
+//               runs on across units
+//   warp 1      allocates 2 x BN TMEM columns (two accumulators); one thread issues
+//               tcgen05.mma.kind::f16 (M = 128, N = BN, K = 16) four times per 64-wide
+//               k block into the accumulator of the segment's parity; tcgen05.commit
+//               frees each stage and, after a segment's last block, hands the
+//               accumulator over
 //   warps 2..5  epilogue: tcgen05.ld 32x32b.x32 (each warp its 32 TMEM lanes = rows),
-//               scale, optional accumulate into C, fp32 stores
-// K may come from two segments (A0.B0^T + A1.B1^T, e.g. [dG | dU] . [W_gate | W_up]^T)
-// and may be split over gridDim.z CTAs, which then write fp32 partial tiles to a
-// workspace that tc_reduce sums.  Every mbarrier wait is bounded (status + wind-down).
+//               scale, optional accumulate into C, fp32 stores, then release the
+//               accumulator, so one segment's epilogue overlaps the next one's MMAs
+// K may come from two segments (A0.B0^T + A1.B1^T, e.g. [dG | dU] . [W_gate | W_up]^T).
+// Work is balanced stream-K style: the (tile, k block) iterations are split evenly over
+// the CTAs; a tile done by one CTA is written by it, a tile shared by several is summed
+// from their partial tiles by tc_fixup in CTA order.  Every mbarrier wait is bounded
+// (status + wind-down).
 #include <cuda.h>
 
+#include <algorithm>
 #include <cstring>
+#include <vector>
+#include <tuple>
+#include <map>
 #include <mutex>
 
 #include "async.cuh"
@@ -40,11 +51,29 @@ struct TcParams {
     int nseg;
     int M, N;
     float alpha;
-    float *out;                          // [M, N] fp32 when splits == 1
+    float *out;                          // [M, N] fp32
     int accumulate;
-    float *partial;                      // [splits, M, N] fp32 when splits > 1
+    float *partial;                      // [ctas][2][kBM * BN] fp32 partial tiles
+    // schedule over the flattened (tile, k block) iterations, tiles numbered m fastest:
+    // CTA c first runs the whole tiles [c dp, (c + 1) dp), then the stream-K share
+    // [sk_base + sk_work c / ctas, sk_base + sk_work (c + 1) / ctas) of the rest
+    int dp;                              // whole tiles per CTA
+    int ctas;
+    int64_t sk_base, sk_work;
     uint32_t *status;
 };
+
+constexpr int kMaxFix = 256;
+// Tiles shared by several CTAs (stream-K part): tile t is the sum of the partial tiles of
+// CTAs c0..c1, CTA c0's in slot s0 (1 when c0 began in an earlier tile), the others in slot 0.
+struct TcFixup {
+    int n;
+    int4 e[kMaxFix];                     // {tile, c0, c1, s0}
+};
+
+__host__ __device__ __forceinline__ int64_t sk_start(int64_t work, int ctas, int c) {
+    return work * c / ctas;
+}
 
 template <int BN>
 __device__ __forceinline__ uint32_t idesc_bf16() {
@@ -56,15 +85,29 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
     constexpr int A_BYTES = kBM * kBK * 2, B_BYTES = BN * kBK * 2, STAGE = A_BYTES + B_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t full[kStages], empty[kStages], tmem_full;
+    __shared__ uint64_t full[kStages], empty[kStages], accfull[2], accempty[2], done;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort, s_issued, s_consumed;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kBM;
 
-    // k blocks of this CTA (split over gridDim.z)
+    // this CTA's iterations: the whole tiles [c dp, (c + 1) dp), then its stream-K range;
+    // cut at tile boundaries into segments
+    const int tiles_m = (p.M + kBM - 1) / kBM;
     const int KB = p.kb[0] + (p.nseg > 1 ? p.kb[1] : 0);
-    const int kb0 = int(int64_t(KB) * blockIdx.z / gridDim.z), kb1 = int(int64_t(KB) * (blockIdx.z + 1) / gridDim.z);
+    const int64_t a0 = int64_t(blockIdx.x) * p.dp * KB, a1 = a0 + int64_t(p.dp) * KB;
+    const int64_t b0 = p.sk_base + sk_start(p.sk_work, p.ctas, blockIdx.x);
+    const int64_t b1 = p.sk_base + sk_start(p.sk_work, p.ctas, blockIdx.x + 1);
+    const int64_t g0 = a0, g1 = a1 + (b1 - b0);               // local iteration count g1 - g0
+    auto to_global = [&](int64_t g) { return g < a1 ? g : b0 + (g - a1); };
+    // segment starting at local iteration g: tile, rows, columns, k blocks [kb0, kb1)
+    auto segment = [&](int64_t g, int &m0, int &n0, int &kb0, int &kb1) {
+        const int64_t gg = to_global(g), end = g < a1 ? a1 : b1;
+        const int64_t t = gg / KB;
+        kb0 = int(gg - t * KB);
+        kb1 = int(std::min<int64_t>(KB, end - t * KB));
+        m0 = int(t % tiles_m) * kBM;
+        n0 = int(t / tiles_m) * BN;
+    };
 
     if (threadIdx.x == 0) {
         s_abort = 0;
@@ -73,65 +116,114 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(&tmem_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accfull[b], 1);
+            mbar_init(&accempty[b], 4);
+        }
+        mbar_init(&done, 1);
     }
     if (warp == 1) {
-        tmem_alloc(&tmem_base, BN);
+        tmem_alloc(&tmem_base, 2 * BN);
         tmem_relinquish();
     }
     fence_mbar_init();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_d = tmem_base;
+    const uint32_t tmem = tmem_base;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer (ring continues across units)
         if (lane == 0) {
-            for (int kb = kb0; kb < kb1; ++kb) {
-                const int i = kb - kb0, s = i % kStages;
-                if (!mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1, p.status, 10u)) { s_abort = 1; break; }
-                const int seg = kb < p.kb[0] ? 0 : 1;
-                const int kx = (seg == 0 ? kb : kb - p.kb[0]) * kBK;
-                uint8_t *sa = smem + s * STAGE;
-                mbar_arrive_expect_tx(&full[s], STAGE);
-                tma_load_2d(sa, &p.a[seg], kx, m0, &full[s]);
-                tma_load_2d(sa + A_BYTES, &p.b[seg], kx, n0, &full[s]);
-                s_issued = i + 1;
+            int g = 0;
+            bool ok = true;
+            for (int64_t gs = g0; ok && gs < g1;) {
+                int m0, n0, kb0, kb1;
+                segment(gs, m0, n0, kb0, kb1);
+                gs += kb1 - kb0;
+                for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                    const int s = g % kStages;
+                    if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) - 1) & 1, p.status, 10u)) {
+                        ok = false;
+                        break;
+                    }
+                    const int seg = kb < p.kb[0] ? 0 : 1;
+                    const int kx = (seg == 0 ? kb : kb - p.kb[0]) * kBK;
+                    uint8_t *sa = smem + s * STAGE;
+                    mbar_arrive_expect_tx(&full[s], STAGE);
+                    tma_load_2d(sa, &p.a[seg], kx, m0, &full[s]);
+                    tma_load_2d(sa + A_BYTES, &p.b[seg], kx, n0, &full[s]);
+                    s_issued = g + 1;
+                }
             }
+            if (!ok) s_abort = 1;
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+        // ------------------------------------------------ MMA issuer, accumulators alternate
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16<BN>();
-            for (int kb = kb0; kb < kb1; ++kb) {
-                const int i = kb - kb0, s = i % kStages;
-                if (!mbar_wait(&full[s], (i / kStages) & 1, p.status, 11u)) { s_abort = 1; break; }
+            int g = 0, i = 0;
+            bool ok = true;
+            for (int64_t gs = g0; ok && gs < g1; ++i) {
+                int m0, n0, kb0, kb1;
+                segment(gs, m0, n0, kb0, kb1);
+                gs += kb1 - kb0;
+                const int b = i & 1;
+                const uint32_t acc = tmem + uint32_t(b * BN);
+                if (i >= 2 && !mbar_wait(&accempty[b], ((i >> 1) - 1) & 1, p.status, 13u)) { ok = false; break; }
                 tc_fence_after();
-                const uint8_t *sa = smem + s * STAGE;
-                const uint64_t ad = sw128_desc(sa), bd = sw128_desc(sa + A_BYTES);
+                for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                    const int s = g % kStages;
+                    if (!mbar_wait(&full[s], (g / kStages) & 1, p.status, 11u)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint8_t *sa = smem + s * STAGE;
+                    const uint64_t ad = sw128_desc(sa), bd = sw128_desc(sa + A_BYTES);
 #pragma unroll
-                for (int k = 0; k < kBK / 16; ++k)   // 16 bf16 = 32 bytes = 2 descriptor units
-                    mma_bf16(tmem_d, ad + 2 * k, bd + 2 * k, idesc, (i > 0 || k > 0) ? 1u : 0u);
-                mma_commit(&empty[s]);
-                s_consumed = i + 1;
+                    for (int k = 0; k < kBK / 16; ++k)   // 16 bf16 = 32 bytes = 2 descriptor units
+                        mma_bf16(acc, ad + 2 * k, bd + 2 * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                    mma_commit(&empty[s]);
+                    s_consumed = g + 1;
+                }
+                if (ok) mma_commit(&accfull[b]);      // this unit's MMAs done -> epilogue
             }
-            mma_commit(&tmem_full);               // all MMAs of this CTA done -> epilogue
+            if (!ok) s_abort = 1;
+            mma_commit(&done);                        // fires once every MMA issued above is complete
+            mbar_wait(&done, 0, nullptr, 0u);
         }
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;                   // TMEM lane quarter this warp may read
-        const int row = m0 + q * 32 + lane;
-        const bool ok = mbar_wait(&tmem_full, 0, p.status, 12u);
-        tc_fence_after();
-        if (ok && kb1 > kb0) {
+        int i = 0;
+        for (int64_t gs = g0; gs < g1; ++i) {
+            int m0, n0, kb0, kb1;
+            segment(gs, m0, n0, kb0, kb1);
+            const bool whole = kb0 == 0 && kb1 == KB;
+            const int slot = to_global(gs) == b0 ? 0 : 1;   // first or last stream-K segment
+            gs += kb1 - kb0;
+            const int b = i & 1;
+            if (!mbar_wait(&accfull[b], (i >> 1) & 1, p.status, 12u)) {
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const int row = m0 + q * 32 + lane;
             for (int j = 0; j < BN / 32; ++j) {
                 uint32_t v[32];
-                tmem_ld32(tmem_d + (uint32_t(q * 32) << 16) + uint32_t(j * 32), v);
+                tmem_ld32(tmem + uint32_t(b * BN) + (uint32_t(q * 32) << 16) + uint32_t(j * 32), v);
                 tmem_wait_ld();
                 const int col0 = n0 + j * 32;
+                if (!whole) {
+                    // partial tile of this CTA, tile-local [kBM][BN]
+                    float *o = p.partial + ((int64_t(blockIdx.x) * 2 + slot) * kBM + q * 32 + lane) * BN + j * 32;
+#pragma unroll
+                    for (int t = 0; t < 32; t += 4)
+                        *reinterpret_cast<float4 *>(o + t) = make_float4(
+                            __uint_as_float(v[t]), __uint_as_float(v[t + 1]), __uint_as_float(v[t + 2]),
+                            __uint_as_float(v[t + 3]));
+                    continue;
+                }
                 if (row >= p.M || col0 >= p.N) continue;
-                if (gridDim.z == 1) {
+                {
                     float *o = p.out + int64_t(row) * p.N + col0;
                     if (col0 + 32 <= p.N && (p.N & 3) == 0) {
 #pragma unroll
@@ -149,51 +241,60 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                         for (int t = 0; t < 32 && col0 + t < p.N; ++t)
                             o[t] = p.alpha * __uint_as_float(v[t]) + (p.accumulate ? o[t] : 0.f);
                     }
-                } else {
-                    float *o = p.partial + (int64_t(blockIdx.z) * p.M + row) * p.N + col0;
-                    if (col0 + 32 <= p.N && (p.N & 3) == 0) {
-#pragma unroll
-                        for (int t = 0; t < 32; t += 4)
-                            *reinterpret_cast<float4 *>(o + t) = make_float4(
-                                __uint_as_float(v[t]), __uint_as_float(v[t + 1]), __uint_as_float(v[t + 2]),
-                                __uint_as_float(v[t + 3]));
-                    } else {
-                        for (int t = 0; t < 32 && col0 + t < p.N; ++t) o[t] = __uint_as_float(v[t]);
-                    }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accempty[b]);
         }
     }
-    // wind down: every MMA this CTA issued has completed once tmem_full fired (the
-    // epilogue waited for it); after an abort, also wait (bounded) for the tile copies
-    // that were issued but never consumed, so nothing lands in shared memory after exit
+    // wind down: the MMA thread waited for its final commit, so no MMA is in flight;
+    // after an abort, also wait (bounded) for the tile copies that were issued but never
+    // consumed, so nothing lands in shared memory after exit
     tc_fence_before();
     __syncthreads();
     if (s_abort && threadIdx.x == 0) {
-        for (int i = s_consumed; i < s_issued; ++i) mbar_wait(&full[i % kStages], (i / kStages) & 1, nullptr, 0u);
+        for (int g = s_consumed; g < s_issued; ++g) mbar_wait(&full[g % kStages], (g / kStages) & 1, nullptr, 0u);
     }
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_d, BN);
+        tmem_dealloc(tmem, 2 * BN);
     }
 }
 
-// out[m, n] (+)= alpha * sum_z partial[z, m, n]
-__global__ void tc_reduce_kernel(const float4 *__restrict__ part, float4 *out, int64_t mn4, int splits, float alpha,
-                                 int accumulate) {
-    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < mn4; i += int64_t(gridDim.x) * blockDim.x) {
-        float4 s = part[i];
-        for (int z = 1; z < splits; ++z) {
-            const float4 t = part[int64_t(z) * mn4 + i];
-            s.x += t.x; s.y += t.y; s.z += t.z; s.w += t.w;
+// Stream-K fixup: a tile shared by CTAs c0..c1 is the sum, in CTA order, of their partial
+// tiles; out (+)= alpha * sum.  Block (entry, y) does rows [y kBM / gridDim.y, ...) of it.
+template <int BN>
+__global__ void __launch_bounds__(256) tc_fixup_kernel(const __grid_constant__ TcParams p,
+                                                       const __grid_constant__ TcFixup f) {
+    const int4 en = f.e[blockIdx.x];
+    const int tiles_m = (p.M + kBM - 1) / kBM;
+    const int m0 = (en.x % tiles_m) * kBM, n0 = (en.x / tiles_m) * BN;
+    const int rows = kBM / gridDim.y, r0 = blockIdx.y * rows;
+    for (int e = threadIdx.x; e < rows * (BN / 4); e += blockDim.x) {
+        const int r = r0 + e / (BN / 4), c4 = (e % (BN / 4)) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = en.y; c <= en.z; ++c) {
+            const int slot = c == en.y ? en.w : 0;
+            const float4 v =
+                *reinterpret_cast<const float4 *>(p.partial + ((int64_t(c) * 2 + slot) * kBM + r) * BN + c4);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
         }
-        s.x *= alpha; s.y *= alpha; s.z *= alpha; s.w *= alpha;
-        if (accumulate) {
-            const float4 c = out[i];
-            s.x += c.x; s.y += c.y; s.z += c.z; s.w += c.w;
+        const int row = m0 + r, col = n0 + c4;
+        if (row >= p.M || col >= p.N) continue;
+        float *o = p.out + int64_t(row) * p.N + col;
+        if (col + 4 <= p.N) {
+            float4 y = make_float4(p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w);
+            if (p.accumulate) {
+                const float4 c = *reinterpret_cast<const float4 *>(o);
+                y.x += c.x; y.y += c.y; y.z += c.z; y.w += c.w;
+            }
+            *reinterpret_cast<float4 *>(o) = y;
+        } else {
+            const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+            for (int u = 0; u < 4 && col + u < p.N; ++u) o[u] = p.alpha * a4[u] + (p.accumulate ? o[u] : 0.f);
         }
-        out[i] = s;
     }
 }
 
@@ -224,43 +325,83 @@ int make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int b
 }
 
 template <int BN>
-int launch_tc(const TcParams &p, int splits, cudaStream_t st) {
+int launch_tc(const TcParams &p, cudaStream_t st) {
     constexpr int smem = kStages * (kBM * kBK * 2 + BN * kBK * 2) + 1024;
     auto k = tc_gemm_kernel<BN>;
     TLB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    dim3 grid(unsigned(ceil_div(p.N, BN)), unsigned(ceil_div(p.M, kBM)), unsigned(splits));
-    k<<<grid, kThreadsTC, smem, st>>>(p);
-    return check_launch("tcgen05 gemm");
+    k<<<p.ctas, kThreadsTC, smem, st>>>(p);
+    TLB_TRY(check_launch("tcgen05 gemm"));
+    // tiles of the stream-K part that more than one CTA touched
+    const int64_t KB = p.kb[0] + (p.nseg > 1 ? p.kb[1] : 0);
+    TcFixup f;
+    f.n = 0;
+    int c = 0;
+    for (int64_t t = p.sk_base / KB; p.sk_work > 0 && t < (p.sk_base + p.sk_work) / KB; ++t) {
+        const int64_t ta = t * KB - p.sk_base, tb = ta + KB;     // within the stream-K range
+        while (c + 1 < p.ctas && sk_start(p.sk_work, p.ctas, c + 1) <= ta) ++c;
+        int c1 = c;
+        while (c1 + 1 < p.ctas && sk_start(p.sk_work, p.ctas, c1 + 1) < tb) ++c1;
+        if (c1 > c) {
+            TLB_REQUIRE(f.n < kMaxFix, TLB_EUNSUPPORTED, "tcgen05 GEMM: too many shared tiles");
+            f.e[f.n++] = make_int4(int(t), c, c1, sk_start(p.sk_work, p.ctas, c) < ta ? 1 : 0);
+        }
+    }
+    if (f.n == 0) return TLB_OK;
+    tc_fixup_kernel<BN><<<dim3(unsigned(f.n), 16), 256, 0, st>>>(p, f);
+    return check_launch("tcgen05 gemm fixup");
 }
 
 }  // namespace
 
 TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
-    // pick the tile width and K split that minimise (waves x work per CTA): one CTA per
-    // SM fits (the 4-stage ring takes 132-197 KB of shared memory)
+    // 128 x 256 tiles (128 x 128 when N is narrow) on persistent CTAs.  Candidates: `dp`
+    // whole tiles per CTA, the remaining tiles shared stream-K style by the `ctas` CTAs.
+    // Cost: the busiest CTA's k blocks (one 128 x BN x 64 MMA block each), plus the
+    // partial-tile traffic and a fixup launch when tiles are shared.  Plans are cached.
+    static std::mutex mu;
+    static std::map<std::tuple<int64_t, int64_t, int64_t, int>, TcPlan> cache;
     const int nsm = num_sms();
-    const int64_t KB = ceil_div(K, kBK);
-    TcPlan best{256, 1};
-    double best_cost = 1e300;
-    for (int bn : {256, 128}) {
-        const int64_t tiles = ceil_div(N, bn) * ceil_div(M, kBM);
-        for (int sp = 1; sp <= kMaxSplits; ++sp) {
-            if (sp > 1 && KB / sp < 8) break;
-            const int64_t ctas = tiles * sp;
-            const double waves = double(ceil_div(ctas, nsm));
-            const double cost = waves * (double(bn) * double(ceil_div(KB, sp)) + 2048.0) + (sp > 1 ? 64.0 * sp : 0.0);
-            if (cost < best_cost) {
-                best_cost = cost;
-                best = TcPlan{bn, sp};
-            }
-        }
+    const auto key = std::make_tuple(M, N, K, nsm);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
     }
+    const int bn = N > 128 ? 256 : 128;
+    const int64_t tiles = ceil_div(N, bn) * ceil_div(M, kBM), KB = ceil_div(K, kBK);
+    const double t_kb = 2.0 * kBM * bn * kBK / (1.6e15 / nsm);           // s per k block
+    const double tile_io = 2.0 * kBM * bn * 4 / 6.0e12;                    // s per partial tile written + read
+    TcPlan best{bn, int(std::min<int64_t>(tiles, nsm)), 0, 0};
+    double best_cost = 1e300;
+    auto consider = [&](int64_t ctas, int64_t dp) {
+        if (ctas < 1 || ctas > nsm || dp < 0 || dp * ctas > tiles) return;
+        const int64_t skw = (tiles - dp * ctas) * KB;
+        int64_t shared = 0;
+        for (int64_t c = 1; c < ctas && skw > 0; ++c)
+            if (sk_start(skw, int(ctas), int(c)) % KB != 0) ++shared;
+        const double cost = double(dp * KB + ceil_div(skw, ctas)) * t_kb + (shared > 0 ? 2.0 * shared * tile_io + 3e-6 : 0.0);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = TcPlan{bn, int(ctas), int(dp), int(shared)};
+        }
+    };
+    std::vector<int64_t> cand = {nsm};
+    for (int64_t s = 1; s <= 8; ++s) cand.push_back(std::min<int64_t>(tiles * s, nsm));
+    for (int64_t d = 1; d <= 8; ++d) cand.push_back(std::max<int64_t>(1, std::min<int64_t>(nsm, ceil_div(tiles, d))));
+    for (int64_t ctas : cand) {
+        consider(ctas, tiles / ctas);
+        consider(ctas, tiles / ctas - 1);
+        consider(ctas, 0);
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = best;
     return best;
 }
 
 size_t tc_partial_bytes(int64_t M, int64_t N, int64_t K) {
+    // sized for two partial tiles per CTA whatever the split of K into segments
     const TcPlan pl = tc_plan(M, N, K);
-    return pl.splits > 1 ? size_t(pl.splits) * M * N * 4 : 0;
+    return size_t(pl.ctas) * 2 * kBM * pl.bn * 4;
 }
 
 int tc_convert_bf16(const float *x, void *y, int64_t n, cudaStream_t st) {
@@ -281,7 +422,7 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
     TLB_REQUIRE(nseg == 1 || nseg == 2, TLB_EINVAL, "tcgen05 GEMM: 1 or 2 K segments");
     const int64_t K = seg[0].K + (nseg > 1 ? seg[1].K : 0);
     const TcPlan pl = tc_plan(M, N, K);
-    TLB_REQUIRE(pl.splits == 1 || partial != nullptr, TLB_EINVAL, "tcgen05 GEMM: split K needs a partial buffer");
+    TLB_REQUIRE(partial != nullptr, TLB_EINVAL, "tcgen05 GEMM: needs a partial-tile buffer");
     TLB_REQUIRE(aligned16(out), TLB_EUNSUPPORTED, "tcgen05 GEMM: output alignment");
     TcParams p;
     memset(&p, 0, sizeof(p));
@@ -299,16 +440,13 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
     p.out = out;
     p.accumulate = accumulate ? 1 : 0;
     p.partial = partial;
+    const int64_t KB = p.kb[0] + (nseg > 1 ? p.kb[1] : 0), tiles = ceil_div(N, pl.bn) * ceil_div(M, kBM);
+    p.ctas = pl.ctas;
+    p.dp = pl.dp;
+    p.sk_base = int64_t(pl.dp) * pl.ctas * KB;
+    p.sk_work = (tiles - int64_t(pl.dp) * pl.ctas) * KB;
     p.status = status;
-    TLB_TRY(pl.bn == 256 ? launch_tc<256>(p, pl.splits, st) : launch_tc<128>(p, pl.splits, st));
-    if (pl.splits > 1) {
-        const int64_t mn4 = M * N / 4;
-        tc_reduce_kernel<<<stream_grid(mn4, 256), 256, 0, st>>>(reinterpret_cast<const float4 *>(partial),
-                                                                reinterpret_cast<float4 *>(out), mn4, pl.splits,
-                                                                alpha, accumulate ? 1 : 0);
-        TLB_TRY(check_launch("tcgen05 gemm reduce"));
-    }
-    return TLB_OK;
+    return pl.bn == 256 ? launch_tc<256>(p, st) : launch_tc<128>(p, st);
 }
 
 }  // namespace tlb

@@ -30,18 +30,19 @@ int linear_t_launch(int wtype, const void *W, float scale, const float *dY, int6
 size_t linear_ws_bytes(int wtype, int64_t S, int64_t out_dim, int64_t in_dim);
 // tcgen05 GEMM (gemm_tc.cu): out[M, N] (+)= alpha * sum_seg A_seg[M, K_seg] . B_seg[N, K_seg]^T,
 // A and B bf16 row-major (K-major), 16-byte aligned, K_seg % 8 == 0.
-constexpr int kMaxSplits = 8;
 struct TcOperand {
     const void *a;   // bf16 [M, K]
     const void *b;   // bf16 [N, K]
     int64_t K;
 };
 struct TcPlan {
-    int bn, splits;
+    int bn, ctas;    // tile width, persistent CTAs
+    int dp;          // whole tiles per CTA before the stream-K part
+    int shared;      // CTA boundaries that fall inside a stream-K tile (0: no fixup)
 };
 TcPlan tc_plan(int64_t M, int64_t N, int64_t K);
 bool tc_supported(int64_t M, int64_t N, int64_t K);
-size_t tc_partial_bytes(int64_t M, int64_t N, int64_t K);   // split-K scratch for (M, N, K)
+size_t tc_partial_bytes(int64_t M, int64_t N, int64_t K);   // stream-K partial tiles for (M, N, K)
 int tc_convert_bf16(const float *x, void *y, int64_t n, cudaStream_t st);
 int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, float *out, bool accumulate,
             float *partial, uint32_t *status, cudaStream_t st);

@@ -188,7 +188,7 @@ static int launch_gemm_simt(const float *A, const void *B, float *C, int M, int 
     return check_launch("gemm_nt_simt");
 }
 
-// Workspace of the tensor-core path: [status 256 B][bf16 copy of dY][split-K partials].
+// Workspace of the tensor-core path: [status 256 B][bf16 copy of dY][stream-K partial tiles].
 size_t linear_ws_bytes(int wtype, int64_t S, int64_t out_dim, int64_t in_dim) {
     if (wtype != TLB_W_BF16 || S <= 1 || !tc_supported(S, in_dim, out_dim)) return kStatusBytes;
     return kStatusBytes + ((size_t(S) * out_dim * 2 + 255) & ~size_t(255)) + tc_partial_bytes(S, in_dim, out_dim);
