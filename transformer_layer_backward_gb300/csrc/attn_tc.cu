@@ -4,12 +4,14 @@
 //
 //   attn_tc_prep  tf32-rounded copies laid out for TMA (32 x 32 tile transposes):
 //                   dCr [nh][S][hd]   dCT [nh][hd][S4]   Kt [nkv][hd][L4]   Vr [nkv][L][hd]
-//   attn_tc_dq    CTA = (head h, 128 queries), 6 warps: TMA producer, MMA issuer, and
-//                 4 epilogue warps (one query row per thread = one TMEM lane).  Per tile
-//                 of 32 keys j (V_j, K_j^T and the P tile arrive by TMA, two tiles ahead):
+//   attn_tc_dq    CTA = (head h, 128 queries), 10 warps: TMA producer, MMA issuer, and
+//                 8 epilogue warps (one query row = one TMEM lane and half of the key
+//                 columns per thread).  dCtx_h sits in tensor memory as the A operand of T;
+//                 E and P go to tensor memory as the A operands of U and W.  Per tile
+//                 of 32 keys j (V_j, K_j^T and the P tile arrive by TMA, three tiles ahead):
 //                   T  = dCtx_h V_j^T                        tcgen05.mma, T in TMEM
 //                   E  = P (.) T,  D += rowsum(E)            epilogue, fp32
-//                   U += E K_j,    W += P K_j                tcgen05.mma (E, P tf32 in smem)
+//                   U += E K_j,    W += P K_j                tcgen05.mma (E, P tf32 in TMEM)
 //                 then dQ = scale (U - D W), which equals scale sum_j P (T - D) K_j with D
 //                 the literal row sum of P (.) dAttn, and RoPE backward on the way out.
 //   attn_tc_dv    CTA = (head h, 128 of the S newest keys): over 64-query tiles,
@@ -35,17 +37,19 @@ namespace {
 
 constexpr int kQM = 128;        // queries per dQ CTA
 constexpr int kQK = 32;         // keys per dQ tile
+constexpr int kQSlots = 4;      // dQ tiles in flight (V, K^T, P staged up to four tiles ahead)
 constexpr int kVK = 128;        // keys per dV CTA
 constexpr int kVQ = 64;         // queries per dV tile
-constexpr int kAttnThreads = 192;
+constexpr int kAttnThreads = 320;    // producer warp, MMA warp, 8 epilogue warps
+constexpr int kEpiWarps = 8;          // two per TMEM lane quarter, each half of the columns
 
 struct AttnTcParams {
-    CUtensorMap dc;             // dCr  {hd, S, nh},  box {32, 128, 1}
     CUtensorMap v;              // Vr   {hd, L, nkv}, box {32, 32, 1}
     CUtensorMap kt;             // Kt   {L, hd, nkv}, box {32, hd, 1}
     CUtensorMap dct;            // dCT  {S, hd, nh},  box {32, hd, 1}
     CUtensorMap pq;             // attn {L, S, nh},   box {32, 128, 1}   (dQ: 128 queries x 32 keys)
     CUtensorMap pv;             // attn {L, S, nh},   box {32, 64, 1}    (dV: 64 queries x 32 keys)
+    const float *dcr;           // dCr [nh][S][hd] (tf32 values)
     float *dq;                  // [S, nh * hd]
     float *dv;                  // [S, nkv * hd], or per-head partial sums [nh / nkv][S, nkv * hd]
     int S, L, nh, nkv, pos0, causal, rope;
@@ -124,26 +128,29 @@ __global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dC
 template <int HD>
 struct DqLayout {
     static constexpr int NB = HD / 32;                   // 128-byte boxes along head_dim
-    static constexpr int DC = 0, DC_BYTES = kQM * HD * 4;
-    static constexpr int V0 = DC + DC_BYTES, V_BYTES = kQK * HD * 4;          // 2 slots
-    static constexpr int KT0 = V0 + 2 * V_BYTES, KT_BYTES = HD * kQK * 4;     // 2 slots
-    static constexpr int P0 = KT0 + 2 * KT_BYTES, P_BYTES = kQM * kQK * 4;    // 2 slots
-    static constexpr int AE0 = P0 + 2 * P_BYTES, A_BYTES = kQM * kQK * 4;     // 2 slots
-    static constexpr int TOTAL = AE0 + 2 * A_BYTES;
-    static constexpr uint32_t TU = 2 * kQK, TW = 2 * kQK + HD;                // T0 | T1 | U | W
-    static constexpr uint32_t COLS = (2 * kQK + 2 * HD) <= 256 ? 256 : 512;
+    // shared memory: a ring of kQSlots tile slots, each {V_j, K_j^T, P tile}
+    static constexpr int V_BYTES = kQK * HD * 4, KT_BYTES = HD * kQK * 4, P_BYTES = kQM * kQK * 4;
+    static constexpr int SLOT = V_BYTES + KT_BYTES + P_BYTES;
+    static constexpr int TOTAL = kQSlots * SLOT;
+    __host__ __device__ static constexpr int V(int s) { return s * SLOT; }
+    __host__ __device__ static constexpr int KT(int s) { return s * SLOT + V_BYTES; }
+    __host__ __device__ static constexpr int P(int s) { return s * SLOT + V_BYTES + KT_BYTES; }
+    // tensor memory columns: dCtx (A of T), T double buffer, U, W, E and P (A of U and W)
+    static constexpr uint32_t TDC = 0, TT = HD, TU = HD + 2 * kQK, TW = TU + HD, TE = TW + HD, TP = TE + kQK;
+    static constexpr uint32_t COLS = (TP + kQK) <= 256 ? 256 : 512;
 };
 
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __grid_constant__ AttnTcParams p) {
     using Ly = DqLayout<HD>;
     constexpr int NB = Ly::NB;
+    static_assert(Ly::TP + kQK <= 512, "tensor memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    // vfull/vfree: V ring; kfull/kfree: K^T + P ring; tfull: T in TMEM; afull/afree: E tiles
-    __shared__ uint64_t vfull[2], vfree[2], kfull[2], kfree[2], tfull[2], afull[2], afree[2], ufull;
+    // full/sfree: tile slots; dcready: dCtx in TMEM; tfull: T; afull/afree: E and P in TMEM
+    __shared__ uint64_t full[kQSlots], sfree[kQSlots], dcready, tfull[2], afull, afree, ufull;
     __shared__ uint32_t tmem_base;
-    __shared__ int s_abort, s_v_issued, s_v_used, s_k_issued, s_k_used;
+    __shared__ int s_abort, s_issued, s_used;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y, kvh = h / (p.nh / p.nkv);
     const int q0 = int(gridDim.x - 1 - blockIdx.x) * kQM;       // latest (longest) query tiles first
@@ -152,16 +159,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
 
     if (threadIdx.x == 0) {
         s_abort = 0;
-        s_v_issued = s_v_used = s_k_issued = s_k_used = 0;
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&vfull[s], 1);
-            mbar_init(&vfree[s], 1);
-            mbar_init(&kfull[s], 1);
-            mbar_init(&kfree[s], 1);
-            mbar_init(&tfull[s], 1);
-            mbar_init(&afull[s], 4);
-            mbar_init(&afree[s], 1);
+        s_issued = s_used = 0;
+        for (int s = 0; s < kQSlots; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&sfree[s], 1);
         }
+        mbar_init(&dcready, kEpiWarps);
+        mbar_init(&tfull[0], 1);
+        mbar_init(&tfull[1], 1);
+        mbar_init(&afull, kEpiWarps);
+        mbar_init(&afree, 1);
         mbar_init(&ufull, 1);
     }
     if (warp == 1) {
@@ -175,70 +182,62 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
     const uint32_t tmem = tmem_base;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer (two tiles ahead)
+        // ------------------------------------------------ TMA producer (kQSlots tiles ahead)
         if (lane == 0) {
             for (int j = 0; j < nt; ++j) {
-                const int s = j & 1, k0 = j * kQK;
-                if (j >= 2 && !mbar_wait(&vfree[s], ((j - 2) >> 1) & 1, p.status, 20u)) { s_abort = 1; break; }
-                uint8_t *vd = sm + Ly::V0 + s * Ly::V_BYTES;
-                if (j == 0) {
-                    mbar_arrive_expect_tx(&vfull[0], Ly::DC_BYTES + Ly::V_BYTES);
-                    for (int b = 0; b < NB; ++b)
-                        tma_load_3d(sm + Ly::DC + b * (kQM * 128), &p.dc, b * 32, q0, h, &vfull[0]);
-                } else {
-                    mbar_arrive_expect_tx(&vfull[s], Ly::V_BYTES);
+                const int s = j % kQSlots, k0 = j * kQK;
+                // the slot's previous tile (j - kQSlots) is done once its U / W products are
+                if (j >= kQSlots && !mbar_wait(&sfree[s], (j / kQSlots - 1) & 1, p.status, 20u)) {
+                    s_abort = 1;
+                    break;
                 }
-                for (int b = 0; b < NB; ++b) tma_load_3d(vd + b * (kQK * 128), &p.v, b * 32, k0, kvh, &vfull[s]);
-                s_v_issued = j + 1;
-                if (j >= 2 && !mbar_wait(&kfree[s], ((j - 2) >> 1) & 1, p.status, 21u)) { s_abort = 1; break; }
-                mbar_arrive_expect_tx(&kfull[s], Ly::KT_BYTES + Ly::P_BYTES);
-                tma_load_3d(sm + Ly::KT0 + s * Ly::KT_BYTES, &p.kt, k0, 0, kvh, &kfull[s]);
-                tma_load_3d(sm + Ly::P0 + s * Ly::P_BYTES, &p.pq, k0, q0, h, &kfull[s]);
-                s_k_issued = j + 1;
+                mbar_arrive_expect_tx(&full[s], Ly::SLOT);
+                for (int b = 0; b < NB; ++b)
+                    tma_load_3d(sm + Ly::V(s) + b * (kQK * 128), &p.v, b * 32, k0, kvh, &full[s]);
+                tma_load_3d(sm + Ly::KT(s), &p.kt, k0, 0, kvh, &full[s]);
+                tma_load_3d(sm + Ly::P(s), &p.pq, k0, q0, h, &full[s]);
+                s_issued = j + 1;
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t id1 = idesc_tf32(kQM, kQK), id2 = idesc_tf32(kQM, HD);
-            auto mma_t = [&](int j) -> bool {            // T[j % 2] = dCtx V_j^T
-                const int s = j & 1;
-                if (!mbar_wait(&vfull[s], (j >> 1) & 1, p.status, 22u)) return false;
+            auto mma_t = [&](int j) -> bool {            // T[j % 2] = dCtx V_j^T, dCtx from TMEM
+                const int s = j % kQSlots;
+                if (!mbar_wait(&full[s], (j / kQSlots) & 1, p.status, 22u)) return false;
+                s_used = j + 1;
                 tc_fence_after();
-                const uint8_t *a = sm + Ly::DC, *b = sm + Ly::V0 + s * Ly::V_BYTES;
+                const uint8_t *b = sm + Ly::V(s);
 #pragma unroll
                 for (int kb = 0; kb < NB; ++kb)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_tf32(tmem + uint32_t(s * kQK), sw128_desc(a + kb * (kQM * 128)) + 2 * k,
-                                 sw128_desc(b + kb * (kQK * 128)) + 2 * k, id1, (kb | k) ? 1u : 0u);
-                mma_commit(&vfree[s]);
-                mma_commit(&tfull[s]);
-                s_v_used = j + 1;
+                        mma_tf32_ts(tmem + Ly::TT + uint32_t((j & 1) * kQK), tmem + Ly::TDC + uint32_t(kb * 32 + k * 8),
+                                    sw128_desc(b + kb * (kQK * 128)) + 2 * k, id1, (kb | k) ? 1u : 0u);
+                mma_commit(&tfull[j & 1]);
                 return true;
             };
-            bool ok = mma_t(0) && (nt < 2 || mma_t(1));
+            bool ok = mbar_wait(&dcready, 0, p.status, 23u);
+            tc_fence_after();
+            ok = ok && mma_t(0) && (nt < 2 || mma_t(1));
             for (int j = 0; ok && j < nt; ++j) {
-                const int s = j & 1;
-                if (!mbar_wait(&afull[s], (j >> 1) & 1, p.status, 24u) ||
-                    !mbar_wait(&kfull[s], (j >> 1) & 1, p.status, 25u)) {
+                const int s = j % kQSlots;
+                if (!mbar_wait(&afull, j & 1, p.status, 24u)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t ad = sw128_desc(sm + Ly::AE0 + s * Ly::A_BYTES);
-                const uint64_t pd = sw128_desc(sm + Ly::P0 + s * Ly::P_BYTES);
-                const uint64_t kd = sw128_desc(sm + Ly::KT0 + s * Ly::KT_BYTES);
+                const uint64_t kd = sw128_desc(sm + Ly::KT(s));
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
-                    mma_tf32(tmem + Ly::TU, ad + 2 * k, kd + 2 * k, id2, acc);
-                    mma_tf32(tmem + Ly::TW, pd + 2 * k, kd + 2 * k, id2, acc);
+                    mma_tf32_ts(tmem + Ly::TU, tmem + Ly::TE + uint32_t(8 * k), kd + 2 * k, id2, acc);
+                    mma_tf32_ts(tmem + Ly::TW, tmem + Ly::TP + uint32_t(8 * k), kd + 2 * k, id2, acc);
                 }
-                mma_commit(&afree[s]);
-                mma_commit(&kfree[s]);
-                s_k_used = j + 1;
-                // the epilogue has read T[s] (it arrived on afull after its tensor-memory loads)
+                mma_commit(&afree);
+                mma_commit(&sfree[s]);
+                // the epilogue has read T[j % 2] (it arrived on afull after its tensor-memory loads)
                 if (j + 2 < nt && !(ok = mma_t(j + 2))) break;
             }
             if (!ok) s_abort = 1;
@@ -246,68 +245,93 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
             mbar_wait(&ufull, 0, nullptr, 0u);
         }
     } else {
-        // ------------------------------------------------ epilogue: one query row per thread
-        const int quarter = warp & 3;
+        // ------------------------------------------------ epilogue: one query row and half of
+        // the key columns per thread (two warps per TMEM lane quarter)
+        constexpr int HK = kQK / 2;
+        const int quarter = warp & 3, hf = (warp - 2) >> 2;
         const int r = quarter * 32 + lane, i = q0 + r;
         const bool row_ok = i < p.S;
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
         const int jlast = p.causal ? p.pos0 + i : p.L - 1;      // last visible key
+        {   // this row's half of dCtx_h (tf32) into tensor memory: the A operand of T
+            const float *src = p.dcr + (int64_t(h) * p.S + (row_ok ? i : 0)) * HD + hf * (HD / 2);
+#pragma unroll
+            for (int c = 0; c < HD / 2; c += 16) {
+                uint32_t v[16];
+#pragma unroll
+                for (int t = 0; t < 16; t += 4) {
+                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (row_ok) x = *reinterpret_cast<const float4 *>(src + c + t);
+                    v[t] = __float_as_uint(x.x);
+                    v[t + 1] = __float_as_uint(x.y);
+                    v[t + 2] = __float_as_uint(x.z);
+                    v[t + 3] = __float_as_uint(x.w);
+                }
+                tmem_st16(tmem + Ly::TDC + uint32_t(hf * (HD / 2) + c) + lane_off, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dcready);
+        }
         float D = 0.f;
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
-            const int s = j & 1, k0 = j * kQK;
-            if (!mbar_wait(&kfull[s], (j >> 1) & 1, p.status, 26u) ||
-                !mbar_wait(&tfull[s], (j >> 1) & 1, p.status, 27u)) {
+            const int s = j % kQSlots, k0 = j * kQK + hf * HK;
+            if (!mbar_wait(&full[s], (j / kQSlots) & 1, p.status, 26u) ||
+                !mbar_wait(&tfull[j & 1], (j >> 1) & 1, p.status, 27u)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t t[kQK];
-            tmem_ld32(tmem + uint32_t(s * kQK) + lane_off, t);
-            uint8_t *pt = sm + Ly::P0 + s * Ly::P_BYTES;
-            float pv[kQK];
+            uint32_t t[HK];
+            tmem_ld16(tmem + Ly::TT + uint32_t((j & 1) * kQK + hf * HK) + lane_off, t);
+            const uint8_t *pt = sm + Ly::P(s);
+            float pv[HK];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const float4 v = *reinterpret_cast<const float4 *>(pt + sw128_off(r, ch));
+            for (int ch = 0; ch < HK / 4; ++ch) {
+                const float4 v = *reinterpret_cast<const float4 *>(pt + sw128_off(r, hf * (HK / 4) + ch));
                 pv[4 * ch] = v.x;
                 pv[4 * ch + 1] = v.y;
                 pv[4 * ch + 2] = v.z;
                 pv[4 * ch + 3] = v.w;
             }
-            if (k0 + kQK - 1 > jlast) {
+            if (k0 + HK - 1 > jlast) {                          // masked keys in this half row
 #pragma unroll
-                for (int c = 0; c < kQK; ++c)
+                for (int c = 0; c < HK; ++c)
                     if (k0 + c > jlast) pv[c] = 0.f;
             }
             tmem_wait_ld();
-            tc_fence_before();
+            uint32_t pr[HK];
 #pragma unroll
-            for (int c = 0; c < kQK; ++c) {
+            for (int c = 0; c < HK; ++c) {
                 const float e = pv[c] * __uint_as_float(t[c]);
                 D += e;
                 t[c] = to_tf32(e);
+                pr[c] = to_tf32(pv[c]);
             }
-            if (j >= 2 && !mbar_wait(&afree[s], ((j - 2) >> 1) & 1, p.status, 28u)) { ok = false; break; }
-            uint8_t *ae = sm + Ly::AE0 + s * Ly::A_BYTES;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const uint32_t off = sw128_off(r, ch);
-                st_shared_v4(ae + off, t[4 * ch], t[4 * ch + 1], t[4 * ch + 2], t[4 * ch + 3]);
-                // P in place, rounded and masked: the A operand of W += P K_j
-                st_shared_v4(pt + off, to_tf32(pv[4 * ch]), to_tf32(pv[4 * ch + 1]), to_tf32(pv[4 * ch + 2]),
-                             to_tf32(pv[4 * ch + 3]));
-            }
-            fence_proxy_async();
+            // E and P (tf32) into tensor memory once the U / W products of tile j - 1 are done
+            if (j >= 1 && !mbar_wait(&afree, (j - 1) & 1, p.status, 28u)) { ok = false; break; }
+            tc_fence_after();
+            tmem_st16(tmem + Ly::TE + uint32_t(hf * HK) + lane_off, t);
+            tmem_st16(tmem + Ly::TP + uint32_t(hf * HK) + lane_off, pr);
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[s]);
+            if (lane == 0) mbar_arrive(&afull);
         }
+        // D of the row: the two column halves meet in shared memory
+        __shared__ float sD[2][kQM];
+        sD[hf][r] = D;
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+        D = sD[0][r] + sD[1][r];
         if (ok && mbar_wait(&ufull, 0, p.status, 29u)) {
             tc_fence_after();
-            constexpr int half = HD / 2;
+            constexpr int half = HD / 2, q4 = HD / 4;
             float *out = p.dq + int64_t(row_ok ? i : 0) * (p.nh * HD) + h * HD;
             const float pos = float(p.pos0 + i);
 #pragma unroll 1
-            for (int c = 0; c < half; c += 16) {
+            for (int c = hf * q4; c < (hf + 1) * q4; c += 16) {      // pairs (c, c + HD / 2)
                 uint32_t u1[16], u2[16], w1[16], w2[16];
                 tmem_ld16(tmem + Ly::TU + uint32_t(c) + lane_off, u1);
                 tmem_ld16(tmem + Ly::TU + uint32_t(c + half) + lane_off, u2);
@@ -346,8 +370,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
     tc_fence_before();
     __syncthreads();
     if (s_abort && threadIdx.x == 0) {
-        for (int v = s_v_used; v < s_v_issued; ++v) mbar_wait(&vfull[v & 1], (v >> 1) & 1, nullptr, 0u);
-        for (int k = s_k_used; k < s_k_issued; ++k) mbar_wait(&kfull[k & 1], (k >> 1) & 1, nullptr, 0u);
+        for (int j = s_used; j < s_issued; ++j) mbar_wait(&full[j % kQSlots], (j / kQSlots) & 1, nullptr, 0u);
     }
     __syncthreads();
     if (warp == 1) {
@@ -387,7 +410,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bfull[s], 1);
             mbar_init(&bfree[s], 1);
-            mbar_init(&afull[s], 4);
+            mbar_init(&afull[s], kEpiWarps);
             mbar_init(&afree[s], 1);
         }
         mbar_init(&dfull, 1);
@@ -444,28 +467,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
             mbar_wait(&dfull, 0, nullptr, 0u);
         }
     } else {
-        // ------------------------------------------------ P^T writers, then the dV epilogue
-        const int quarter = warp & 3;
+        // ------------------------------------------------ P^T writers, then the dV epilogue:
+        // one key row and half of the queries (later: half of the columns) per thread
+        constexpr int HQ = kVQ / 2;
+        const int quarter = warp & 3, hf = (warp - 2) >> 2;
         const int r = quarter * 32 + lane, jj = k0 + r;        // key row of this thread
         const bool key_ok = jj < p.S;
         const int box = r >> 5, col = r & 31;
         bool ok = true;
         for (int w = 0; w < nw; ++w) {
-            const int s = w & 1, qa = (t0 + w) * kVQ;
+            const int s = w & 1, qa = (t0 + w) * kVQ + hf * HQ;
             if (!mbar_wait(&bfull[s], (w >> 1) & 1, p.status, 33u)) { ok = false; break; }
             const uint8_t *ps = sm + Ly::P0 + s * Ly::S_BYTES + box * (kVQ * 128) + (col & 3) * 4;
-            uint32_t pt[kVQ];
+            uint32_t pt[HQ];
 #pragma unroll
-            for (int qq = 0; qq < kVQ; ++qq) {
-                const float v = *reinterpret_cast<const float *>(ps + sw128_off(qq, col >> 2));
+            for (int qq = 0; qq < HQ; ++qq) {
+                const float v = *reinterpret_cast<const float *>(ps + sw128_off(hf * HQ + qq, col >> 2));
                 const bool vis = key_ok && (!p.causal || qa + qq >= jj);   // rows past S arrive as zeros
                 pt[qq] = to_tf32(vis ? v : 0.f);
             }
             if (w >= 2 && !mbar_wait(&afree[s], ((w - 2) >> 1) & 1, p.status, 34u)) { ok = false; break; }
             uint8_t *a = sm + Ly::A0 + s * Ly::A_BYTES;
 #pragma unroll
-            for (int c4 = 0; c4 < kVQ / 4; ++c4) {
-                const uint32_t off = uint32_t(c4 >> 3) * (kVK * 128) + sw128_off(r, c4 & 7);
+            for (int c4 = 0; c4 < HQ / 4; ++c4) {
+                const int cc = hf * (HQ / 4) + c4;            // 16-byte chunk along the 64 queries
+                const uint32_t off = uint32_t(cc >> 3) * (kVK * 128) + sw128_off(r, cc & 7);
                 st_shared_v4(a + off, pt[4 * c4], pt[4 * c4 + 1], pt[4 * c4 + 2], pt[4 * c4 + 3]);
             }
             fence_proxy_async();
@@ -478,7 +504,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
             const int64_t kvd = int64_t(p.nkv) * HD;
             float *out = p.dv + (G > 1 ? int64_t(g) * p.S * kvd : 0) + int64_t(key_ok ? jj : 0) * kvd + kvh * HD;
 #pragma unroll 1
-            for (int c = 0; c < HD; c += 32) {
+            for (int c = hf * (HD / 2); c < (hf + 1) * (HD / 2); c += 32) {
                 uint32_t v[32];
                 tmem_ld32(tD + uint32_t(c) + lane_off, v);
                 tmem_wait_ld();
@@ -572,12 +598,6 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     AttnTcParams p;
     memset(&p, 0, sizeof(p));
     {
-        const uint64_t d[3] = {uint64_t(HD), uint64_t(a.S), uint64_t(a.nh)};
-        const uint64_t s[2] = {uint64_t(HD) * 4, uint64_t(a.S) * HD * 4};
-        const uint32_t b[3] = {32, uint32_t(kQM), 1};
-        TLB_TRY(make_map_f32_3d(&p.dc, dCr, d, s, b));
-    }
-    {
         const uint64_t d[3] = {uint64_t(HD), uint64_t(a.L), uint64_t(a.nkv)};
         const uint64_t s[2] = {uint64_t(HD) * 4, uint64_t(a.L) * HD * 4};
         const uint32_t b[3] = {32, uint32_t(kQK), 1};
@@ -604,6 +624,7 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     }
     const int G = a.nh / a.nkv;
     float *part = reinterpret_cast<float *>(base + w.part);
+    p.dcr = dCr;
     p.dq = a.dq;
     p.dv = G > 1 ? part : a.dv;
     p.S = a.S;

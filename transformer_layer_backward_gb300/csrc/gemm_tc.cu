@@ -354,8 +354,8 @@ int launch_tc(const TcParams &p, cudaStream_t st) {
 }  // namespace
 
 TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
-    // 128 x 256 tiles (128 x 128 when N is narrow) on persistent CTAs.  Candidates: `dp`
-    // whole tiles per CTA, the remaining tiles shared stream-K style by the `ctas` CTAs.
+    // 128 x 256 or 128 x 128 tiles on persistent CTAs.  Candidates: `dp` whole tiles per
+    // CTA, the remaining tiles shared stream-K style by the `ctas` CTAs.
     // Cost: the busiest CTA's k blocks (one 128 x BN x 64 MMA block each), plus the
     // partial-tile traffic and a fixup launch when tiles are shared.  Plans are cached.
     static std::mutex mu;
@@ -367,31 +367,35 @@ TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    const int bn = N > 128 ? 256 : 128;
-    const int64_t tiles = ceil_div(N, bn) * ceil_div(M, kBM), KB = ceil_div(K, kBK);
-    const double t_kb = 2.0 * kBM * bn * kBK / (1.6e15 / nsm);           // s per k block
-    const double tile_io = 2.0 * kBM * bn * 4 / 6.0e12;                    // s per partial tile written + read
-    TcPlan best{bn, int(std::min<int64_t>(tiles, nsm)), 0, 0};
+    TcPlan best{N > 128 ? 256 : 128, 1, 0, 0};
     double best_cost = 1e300;
-    auto consider = [&](int64_t ctas, int64_t dp) {
-        if (ctas < 1 || ctas > nsm || dp < 0 || dp * ctas > tiles) return;
-        const int64_t skw = (tiles - dp * ctas) * KB;
-        int64_t shared = 0;
-        for (int64_t c = 1; c < ctas && skw > 0; ++c)
-            if (sk_start(skw, int(ctas), int(c)) % KB != 0) ++shared;
-        const double cost = double(dp * KB + ceil_div(skw, ctas)) * t_kb + (shared > 0 ? 2.0 * shared * tile_io + 3e-6 : 0.0);
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = TcPlan{bn, int(ctas), int(dp), int(shared)};
+    for (int bn : {256, 128}) {
+        if (bn == 256 && N <= 128) continue;
+        const int64_t tiles = ceil_div(N, bn) * ceil_div(M, kBM), KB = ceil_div(K, kBK);
+        // s per k block; 128-wide tiles fetch A twice as often per flop
+        const double t_kb = 2.0 * kBM * bn * kBK / (1.6e15 / nsm) * (bn == 128 ? 1.15 : 1.0);
+        const double tile_io = 2.0 * kBM * bn * 4 / 6.0e12;                // s per partial tile written + read
+        auto consider = [&](int64_t ctas, int64_t dp) {
+            if (ctas < 1 || ctas > nsm || dp < 0 || dp * ctas > tiles) return;
+            const int64_t skw = (tiles - dp * ctas) * KB;
+            int64_t shared = 0;
+            for (int64_t c = 1; c < ctas && skw > 0; ++c)
+                if (sk_start(skw, int(ctas), int(c)) % KB != 0) ++shared;
+            const double cost =
+                double(dp * KB + ceil_div(skw, ctas)) * t_kb + (shared > 0 ? 2.0 * shared * tile_io + 3e-6 : 0.0);
+            if (cost < best_cost) {
+                best_cost = cost;
+                best = TcPlan{bn, int(ctas), int(dp), int(shared)};
+            }
+        };
+        std::vector<int64_t> cand = {nsm};
+        for (int64_t s = 1; s <= 8; ++s) cand.push_back(std::min<int64_t>(tiles * s, nsm));
+        for (int64_t d = 1; d <= 8; ++d) cand.push_back(std::max<int64_t>(1, std::min<int64_t>(nsm, ceil_div(tiles, d))));
+        for (int64_t ctas : cand) {
+            consider(ctas, tiles / ctas);
+            consider(ctas, tiles / ctas - 1);
+            consider(ctas, 0);
         }
-    };
-    std::vector<int64_t> cand = {nsm};
-    for (int64_t s = 1; s <= 8; ++s) cand.push_back(std::min<int64_t>(tiles * s, nsm));
-    for (int64_t d = 1; d <= 8; ++d) cand.push_back(std::max<int64_t>(1, std::min<int64_t>(nsm, ceil_div(tiles, d))));
-    for (int64_t ctas : cand) {
-        consider(ctas, tiles / ctas);
-        consider(ctas, tiles / ctas - 1);
-        consider(ctas, 0);
     }
     std::lock_guard<std::mutex> lk(mu);
     cache[key] = best;
