@@ -3,15 +3,17 @@
 // operands and fp32 accumulation in tensor memory.  GQA: kvh = h / (nh / nkv).
 //
 //   attn_tc_prep  tf32-rounded copies laid out for TMA (32 x 32 tile transposes):
-//                   dCr [nh][S][hd]   dCT [nh][hd][S4]   Kt [nkv][hd][L4]   Vr [nkv][L][hd]
+//                   dCT [nh][hd][S4]   Kt [nkv][hd][L4]   Vr [nkv][L][hd]
 //   attn_tc_dq    CTA = (head h, 128 queries), 10 warps: TMA producer, MMA issuer, and
 //                 8 epilogue warps (one query row = one TMEM lane and half of the key
 //                 columns per thread).  dCtx_h sits in tensor memory as the A operand of T;
-//                 E and P go to tensor memory as the A operands of U and W.  Per tile
-//                 of 32 keys j (V_j, K_j^T and the P tile arrive by TMA, three tiles ahead):
+//                 E goes to tensor memory (two buffers) as the A operand of U; the staged P
+//                 tile is the A operand of W.  Per tile
+//                 of 32 keys j (V_j, K_j^T and the P tile arrive by TMA in two rings, four
+//                 tiles deep: V is released when T_j is formed, K^T and P after U and W):
 //                   T  = dCtx_h V_j^T                        tcgen05.mma, T in TMEM
 //                   E  = P (.) T,  D += rowsum(E)            epilogue, fp32
-//                   U += E K_j,    W += P K_j                tcgen05.mma (E, P tf32 in TMEM)
+//                   U += E K_j,    W += P K_j                tcgen05.mma (E tf32 in TMEM, P in smem)
 //                 then dQ = scale (U - D W), which equals scale sum_j P (T - D) K_j with D
 //                 the literal row sum of P (.) dAttn, and RoPE backward on the way out.
 //   attn_tc_dv    CTA = (head h, 128 of the S newest keys): over 64-query tiles,
@@ -49,7 +51,7 @@ struct AttnTcParams {
     CUtensorMap dct;            // dCT  {S, hd, nh},  box {32, hd, 1}
     CUtensorMap pq;             // attn {L, S, nh},   box {32, 128, 1}   (dQ: 128 queries x 32 keys)
     CUtensorMap pv;             // attn {L, S, nh},   box {32, 64, 1}    (dV: 64 queries x 32 keys)
-    const float *dcr;           // dCr [nh][S][hd] (tf32 values)
+    const float *dctx;          // dCtx [S, nh * hd]
     float *dq;                  // [S, nh * hd]
     float *dv;                  // [S, nkv * hd], or per-head partial sums [nh / nkv][S, nkv * hd]
     int S, L, nh, nkv, pos0, causal, rope;
@@ -72,8 +74,8 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int ch) { return uint32_t(r
 
 // ------------------------------------------------------------------ prep
 
-// 32 x 32 tiles of three sources: dCtx [S, nh*hd] -> dCr, dCT;  K -> Kt;  V -> Vr.
-__global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dCr, float *dCT, float *Kt, float *Vr,
+// 32 x 32 tiles of three sources: dCtx [S, nh*hd] -> dCT;  K -> Kt;  V -> Vr.
+__global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dCT, float *Kt, float *Vr,
                                                            int S4, int L4, int ntc_dc, int ntc_kv) {
     __shared__ float tile[32][33];
     const int qd = a.nh * a.hd, kvd = a.nkv * a.hd;
@@ -107,8 +109,7 @@ __global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dC
         tile[rr][tx] = v;
         if (r < rows) {
             const int hh = c / a.hd, d = c % a.hd;
-            if (job == 0) dCr[(int64_t(hh) * a.S + r) * a.hd + d] = v;
-            else if (job == 2) Vr[(int64_t(hh) * a.L + r) * a.hd + d] = v;
+            if (job == 2) Vr[(int64_t(hh) * a.L + r) * a.hd + d] = v;
         }
     }
     if (job == 2) return;
@@ -128,47 +129,56 @@ __global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dC
 template <int HD>
 struct DqLayout {
     static constexpr int NB = HD / 32;                   // 128-byte boxes along head_dim
-    // shared memory: a ring of kQSlots tile slots, each {V_j, K_j^T, P tile}
+    // shared memory: two rings of kQSlots slots each, V_j (freed once T_j is formed) and
+    // {K_j^T, P tile} (freed once U and W have taken tile j)
     static constexpr int V_BYTES = kQK * HD * 4, KT_BYTES = HD * kQK * 4, P_BYTES = kQM * kQK * 4;
-    static constexpr int SLOT = V_BYTES + KT_BYTES + P_BYTES;
-    static constexpr int TOTAL = kQSlots * SLOT;
-    __host__ __device__ static constexpr int V(int s) { return s * SLOT; }
-    __host__ __device__ static constexpr int KT(int s) { return s * SLOT + V_BYTES; }
-    __host__ __device__ static constexpr int P(int s) { return s * SLOT + V_BYTES + KT_BYTES; }
-    // tensor memory columns: dCtx (A of T), T double buffer, U, W, E and P (A of U and W)
-    static constexpr uint32_t TDC = 0, TT = HD, TU = HD + 2 * kQK, TW = TU + HD, TE = TW + HD, TP = TE + kQK;
-    static constexpr uint32_t COLS = (TP + kQK) <= 256 ? 256 : 512;
+    static constexpr int KSLOT = KT_BYTES + P_BYTES;
+    static constexpr int K0 = kQSlots * V_BYTES;
+    static constexpr int TOTAL = K0 + kQSlots * KSLOT;
+    __host__ __device__ static constexpr int V(int s) { return s * V_BYTES; }
+    __host__ __device__ static constexpr int KT(int s) { return K0 + s * KSLOT; }
+    __host__ __device__ static constexpr int P(int s) { return K0 + s * KSLOT + KT_BYTES; }
+    // tensor memory columns: dCtx (A of T), T double buffer, U, W, E double buffer (A of U)
+    static constexpr uint32_t TDC = 0, TT = HD, TU = HD + 2 * kQK, TW = TU + HD, TE = TW + HD;
+    static constexpr uint32_t COLS = (TE + 2 * kQK) <= 256 ? 256 : 512;
 };
 
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __grid_constant__ AttnTcParams p) {
     using Ly = DqLayout<HD>;
     constexpr int NB = Ly::NB;
-    static_assert(Ly::TP + kQK <= 512, "tensor memory");
+    static_assert(Ly::TE + 2 * kQK <= 512, "tensor memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    // full/sfree: tile slots; dcready: dCtx in TMEM; tfull: T; afull/afree: E and P in TMEM
-    __shared__ uint64_t full[kQSlots], sfree[kQSlots], dcready, tfull[2], afull, afree, ufull;
+    // vfull/vfree: V ring; kfull/kfree: K^T + P ring; dcready: dCtx in TMEM; tfull: T;
+    // afull/afree: E in TMEM (and the masked P tile in shared memory), double-buffered
+    __shared__ uint64_t vfull[kQSlots], vfree[kQSlots], kfull[kQSlots], kfree[kQSlots], dcready, tfull[2], afull[2],
+        afree[2], ufull;
     __shared__ uint32_t tmem_base;
-    __shared__ int s_abort, s_issued, s_used;
+    __shared__ int s_abort, s_v_issued, s_v_used, s_k_issued, s_k_used;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.y, kvh = h / (p.nh / p.nkv);
-    const int q0 = int(gridDim.x - 1 - blockIdx.x) * kQM;       // latest (longest) query tiles first
+    // blocks start in x-fastest order: x = head, y = query tile from the last (longest) one,
+    // so every head's longest tiles start first
+    const int h = blockIdx.x, kvh = h / (p.nh / p.nkv);
+    const int q0 = int(gridDim.y - 1 - blockIdx.y) * kQM;
     const int kend = p.causal ? min(p.L, p.pos0 + q0 + kQM) : p.L;
     const int nt = (kend + kQK - 1) / kQK;
 
     if (threadIdx.x == 0) {
         s_abort = 0;
-        s_issued = s_used = 0;
+        s_v_issued = s_v_used = s_k_issued = s_k_used = 0;
         for (int s = 0; s < kQSlots; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&sfree[s], 1);
+            mbar_init(&vfull[s], 1);
+            mbar_init(&vfree[s], 1);
+            mbar_init(&kfull[s], 1);
+            mbar_init(&kfree[s], 1);
         }
         mbar_init(&dcready, kEpiWarps);
-        mbar_init(&tfull[0], 1);
-        mbar_init(&tfull[1], 1);
-        mbar_init(&afull, kEpiWarps);
-        mbar_init(&afree, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&afull[b], kEpiWarps);
+            mbar_init(&afree[b], 1);
+        }
         mbar_init(&ufull, 1);
     }
     if (warp == 1) {
@@ -186,17 +196,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
         if (lane == 0) {
             for (int j = 0; j < nt; ++j) {
                 const int s = j % kQSlots, k0 = j * kQK;
-                // the slot's previous tile (j - kQSlots) is done once its U / W products are
-                if (j >= kQSlots && !mbar_wait(&sfree[s], (j / kQSlots - 1) & 1, p.status, 20u)) {
+                // V slot: tile j - kQSlots has formed its T; K^T + P slot: its U and W are done
+                if (j >= kQSlots && !mbar_wait(&vfree[s], (j / kQSlots - 1) & 1, p.status, 20u)) {
                     s_abort = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], Ly::SLOT);
+                mbar_arrive_expect_tx(&vfull[s], Ly::V_BYTES);
                 for (int b = 0; b < NB; ++b)
-                    tma_load_3d(sm + Ly::V(s) + b * (kQK * 128), &p.v, b * 32, k0, kvh, &full[s]);
-                tma_load_3d(sm + Ly::KT(s), &p.kt, k0, 0, kvh, &full[s]);
-                tma_load_3d(sm + Ly::P(s), &p.pq, k0, q0, h, &full[s]);
-                s_issued = j + 1;
+                    tma_load_3d(sm + Ly::V(s) + b * (kQK * 128), &p.v, b * 32, k0, kvh, &vfull[s]);
+                s_v_issued = j + 1;
+                if (j >= kQSlots && !mbar_wait(&kfree[s], (j / kQSlots - 1) & 1, p.status, 21u)) {
+                    s_abort = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&kfull[s], Ly::KSLOT);
+                tma_load_3d(sm + Ly::KT(s), &p.kt, k0, 0, kvh, &kfull[s]);
+                tma_load_3d(sm + Ly::P(s), &p.pq, k0, q0, h, &kfull[s]);
+                s_k_issued = j + 1;
             }
         }
     } else if (warp == 1) {
@@ -205,8 +221,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
             constexpr uint32_t id1 = idesc_tf32(kQM, kQK), id2 = idesc_tf32(kQM, HD);
             auto mma_t = [&](int j) -> bool {            // T[j % 2] = dCtx V_j^T, dCtx from TMEM
                 const int s = j % kQSlots;
-                if (!mbar_wait(&full[s], (j / kQSlots) & 1, p.status, 22u)) return false;
-                s_used = j + 1;
+                if (!mbar_wait(&vfull[s], (j / kQSlots) & 1, p.status, 22u)) return false;
+                s_v_used = j + 1;
                 tc_fence_after();
                 const uint8_t *b = sm + Ly::V(s);
 #pragma unroll
@@ -215,6 +231,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
                     for (int k = 0; k < 4; ++k)
                         mma_tf32_ts(tmem + Ly::TT + uint32_t((j & 1) * kQK), tmem + Ly::TDC + uint32_t(kb * 32 + k * 8),
                                     sw128_desc(b + kb * (kQK * 128)) + 2 * k, id1, (kb | k) ? 1u : 0u);
+                mma_commit(&vfree[s]);
                 mma_commit(&tfull[j & 1]);
                 return true;
             };
@@ -223,20 +240,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
             ok = ok && mma_t(0) && (nt < 2 || mma_t(1));
             for (int j = 0; ok && j < nt; ++j) {
                 const int s = j % kQSlots;
-                if (!mbar_wait(&afull, j & 1, p.status, 24u)) {
+                if (!mbar_wait(&afull[j & 1], (j >> 1) & 1, p.status, 24u) ||
+                    !mbar_wait(&kfull[s], (j / kQSlots) & 1, p.status, 25u)) {
                     ok = false;
                     break;
                 }
+                s_k_used = j + 1;
                 tc_fence_after();
-                const uint64_t kd = sw128_desc(sm + Ly::KT(s));
+                const uint64_t kd = sw128_desc(sm + Ly::KT(s)), pd = sw128_desc(sm + Ly::P(s));
+                const uint32_t te = tmem + Ly::TE + uint32_t((j & 1) * kQK);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
-                    mma_tf32_ts(tmem + Ly::TU, tmem + Ly::TE + uint32_t(8 * k), kd + 2 * k, id2, acc);
-                    mma_tf32_ts(tmem + Ly::TW, tmem + Ly::TP + uint32_t(8 * k), kd + 2 * k, id2, acc);
+                    mma_tf32_ts(tmem + Ly::TU, te + uint32_t(8 * k), kd + 2 * k, id2, acc);
+                    mma_tf32(tmem + Ly::TW, pd + 2 * k, kd + 2 * k, id2, acc);
                 }
-                mma_commit(&afree);
-                mma_commit(&sfree[s]);
+                mma_commit(&afree[j & 1]);
+                mma_commit(&kfree[s]);
                 // the epilogue has read T[j % 2] (it arrived on afull after its tensor-memory loads)
                 if (j + 2 < nt && !(ok = mma_t(j + 2))) break;
             }
@@ -253,8 +273,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
         const bool row_ok = i < p.S;
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
         const int jlast = p.causal ? p.pos0 + i : p.L - 1;      // last visible key
-        {   // this row's half of dCtx_h (tf32) into tensor memory: the A operand of T
-            const float *src = p.dcr + (int64_t(h) * p.S + (row_ok ? i : 0)) * HD + hf * (HD / 2);
+        {   // this row's half of dCtx_h, rounded to tf32, into tensor memory: the A operand of T
+            const float *src = p.dctx + int64_t(row_ok ? i : 0) * (p.nh * HD) + h * HD + hf * (HD / 2);
 #pragma unroll
             for (int c = 0; c < HD / 2; c += 16) {
                 uint32_t v[16];
@@ -262,10 +282,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
                 for (int t = 0; t < 16; t += 4) {
                     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (row_ok) x = *reinterpret_cast<const float4 *>(src + c + t);
-                    v[t] = __float_as_uint(x.x);
-                    v[t + 1] = __float_as_uint(x.y);
-                    v[t + 2] = __float_as_uint(x.z);
-                    v[t + 3] = __float_as_uint(x.w);
+                    v[t] = to_tf32(x.x);
+                    v[t + 1] = to_tf32(x.y);
+                    v[t + 2] = to_tf32(x.z);
+                    v[t + 3] = to_tf32(x.w);
                 }
                 tmem_st16(tmem + Ly::TDC + uint32_t(hf * (HD / 2) + c) + lane_off, v);
             }
@@ -278,7 +298,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
             const int s = j % kQSlots, k0 = j * kQK + hf * HK;
-            if (!mbar_wait(&full[s], (j / kQSlots) & 1, p.status, 26u) ||
+            if (!mbar_wait(&kfull[s], (j / kQSlots) & 1, p.status, 26u) ||
                 !mbar_wait(&tfull[j & 1], (j >> 1) & 1, p.status, 27u)) {
                 ok = false;
                 break;
@@ -296,29 +316,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
                 pv[4 * ch + 2] = v.z;
                 pv[4 * ch + 3] = v.w;
             }
-            if (k0 + HK - 1 > jlast) {                          // masked keys in this half row
+            const bool diag = k0 + HK - 1 > jlast;              // masked keys in this half row
+            if (diag) {
 #pragma unroll
                 for (int c = 0; c < HK; ++c)
                     if (k0 + c > jlast) pv[c] = 0.f;
             }
             tmem_wait_ld();
-            uint32_t pr[HK];
 #pragma unroll
             for (int c = 0; c < HK; ++c) {
                 const float e = pv[c] * __uint_as_float(t[c]);
                 D += e;
                 t[c] = to_tf32(e);
-                pr[c] = to_tf32(pv[c]);
             }
-            // E and P (tf32) into tensor memory once the U / W products of tile j - 1 are done
-            if (j >= 1 && !mbar_wait(&afree, (j - 1) & 1, p.status, 28u)) { ok = false; break; }
+            // the P tile is the A operand of W += P K_j as staged (the MMA reads tf32); masked
+            // keys of a diagonal tile are zeroed in place
+            if (diag) {
+#pragma unroll
+                for (int ch = 0; ch < HK / 4; ++ch)
+                    st_shared_v4(sm + Ly::P(s) + sw128_off(r, hf * (HK / 4) + ch), __float_as_uint(pv[4 * ch]),
+                                 __float_as_uint(pv[4 * ch + 1]), __float_as_uint(pv[4 * ch + 2]),
+                                 __float_as_uint(pv[4 * ch + 3]));
+                fence_proxy_async();
+            }
+            // E (tf32) into tensor memory once the U product of tile j - 2 is done with the buffer
+            if (j >= 2 && !mbar_wait(&afree[j & 1], ((j - 2) >> 1) & 1, p.status, 28u)) { ok = false; break; }
             tc_fence_after();
-            tmem_st16(tmem + Ly::TE + uint32_t(hf * HK) + lane_off, t);
-            tmem_st16(tmem + Ly::TP + uint32_t(hf * HK) + lane_off, pr);
+            tmem_st16(tmem + Ly::TE + uint32_t((j & 1) * kQK + hf * HK) + lane_off, t);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&afull);
+            if (lane == 0) mbar_arrive(&afull[j & 1]);
         }
         // D of the row: the two column halves meet in shared memory
         __shared__ float sD[2][kQM];
@@ -370,7 +398,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
     tc_fence_before();
     __syncthreads();
     if (s_abort && threadIdx.x == 0) {
-        for (int j = s_used; j < s_issued; ++j) mbar_wait(&full[j % kQSlots], (j / kQSlots) & 1, nullptr, 0u);
+        for (int j = s_v_used; j < s_v_issued; ++j) mbar_wait(&vfull[j % kQSlots], (j / kQSlots) & 1, nullptr, 0u);
+        for (int j = s_k_used; j < s_k_issued; ++j) mbar_wait(&kfull[j % kQSlots], (j / kQSlots) & 1, nullptr, 0u);
     }
     __syncthreads();
     if (warp == 1) {
@@ -566,7 +595,7 @@ int make_map_f32_3d(CUtensorMap *m, const void *base, const uint64_t dims[3], co
 }
 
 struct TcAttnWs {
-    size_t dCr, dCT, Kt, Vr, part, total;
+    size_t dCT, Kt, Vr, part, total;
     int64_t S4, L4;
 };
 
@@ -575,8 +604,7 @@ TcAttnWs tc_attn_layout(int64_t S, int64_t L, int nh, int nkv, int hd) {
     TcAttnWs w;
     w.S4 = (S + 3) & ~int64_t(3);
     w.L4 = (L + 3) & ~int64_t(3);
-    w.dCr = 0;
-    w.dCT = w.dCr + r256(size_t(nh) * S * hd * 4);
+    w.dCT = 0;
     w.Kt = w.dCT + r256(size_t(nh) * hd * w.S4 * 4);
     w.Vr = w.Kt + r256(size_t(nkv) * hd * w.L4 * 4);
     w.part = w.Vr + r256(size_t(nkv) * L * hd * 4);
@@ -588,11 +616,11 @@ template <int HD>
 int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32_t *status, cudaStream_t st) {
     const TcAttnWs w = tc_attn_layout(a.S, a.L, a.nh, a.nkv, HD);
     char *base = static_cast<char *>(scratch);
-    float *dCr = reinterpret_cast<float *>(base + w.dCr), *dCT = reinterpret_cast<float *>(base + w.dCT);
+    float *dCT = reinterpret_cast<float *>(base + w.dCT);
     float *Kt = reinterpret_cast<float *>(base + w.Kt), *Vr = reinterpret_cast<float *>(base + w.Vr);
     const int ntc_dc = a.nh * HD / 32, ntc_kv = a.nkv * HD / 32;
     const int64_t nblk = int64_t(ntc_dc) * ceil_div(a.S, 32) + 2 * int64_t(ntc_kv) * ceil_div(a.L, 32);
-    attn_tc_prep_kernel<<<unsigned(nblk), 256, 0, st>>>(a, dCr, dCT, Kt, Vr, int(w.S4), int(w.L4), ntc_dc, ntc_kv);
+    attn_tc_prep_kernel<<<unsigned(nblk), 256, 0, st>>>(a, dCT, Kt, Vr, int(w.S4), int(w.L4), ntc_dc, ntc_kv);
     TLB_TRY(check_launch("attn_tc_prep"));
 
     AttnTcParams p;
@@ -624,7 +652,7 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     }
     const int G = a.nh / a.nkv;
     float *part = reinterpret_cast<float *>(base + w.part);
-    p.dcr = dCr;
+    p.dctx = a.dctx;
     p.dq = a.dq;
     p.dv = G > 1 ? part : a.dv;
     p.S = a.S;
@@ -641,7 +669,7 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     const int smq = DqLayout<HD>::TOTAL + 1024, smv = DvLayout<HD>::TOTAL + 1024;
     TLB_CUDA(cudaFuncSetAttribute(attn_tc_dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smq));
     TLB_CUDA(cudaFuncSetAttribute(attn_tc_dv_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smv));
-    attn_tc_dq_kernel<HD><<<dim3(unsigned(ceil_div(a.S, kQM)), unsigned(a.nh)), kAttnThreads, smq, st>>>(p);
+    attn_tc_dq_kernel<HD><<<dim3(unsigned(a.nh), unsigned(ceil_div(a.S, kQM))), kAttnThreads, smq, st>>>(p);
     TLB_TRY(check_launch("attn_tc_dq"));
     attn_tc_dv_kernel<HD><<<dim3(unsigned(a.nh), unsigned(ceil_div(a.S, kVK))), kAttnThreads, smv, st>>>(p);
     TLB_TRY(check_launch("attn_tc_dv"));
@@ -668,7 +696,7 @@ int attn_tc_launch(const AttnArgs &a, float rope_base, void *scratch, uint32_t *
     if (a.S == 0) return TLB_OK;
     TLB_REQUIRE(attn_tc_supported(a.S, a.L, a.nh, a.nkv, a.hd), TLB_EUNSUPPORTED, "attention (tcgen05): shape");
     TLB_REQUIRE((reinterpret_cast<uintptr_t>(scratch) & 255u) == 0, TLB_EINVAL, "attention (tcgen05): scratch alignment");
-    TLB_REQUIRE(aligned16(a.attn) && aligned16(a.dq) && aligned16(a.dv), TLB_EUNSUPPORTED,
+    TLB_REQUIRE(aligned16(a.attn) && aligned16(a.dq) && aligned16(a.dv) && aligned16(a.dctx), TLB_EUNSUPPORTED,
                 "attention (tcgen05): attn / dq / dv not 16-byte aligned");
     RopeFreqs fr;
     rope_freqs(fr, a.hd, rope_base);
