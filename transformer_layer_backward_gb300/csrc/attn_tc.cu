@@ -16,9 +16,10 @@
 //                   U += E K_j,    W += P K_j                tcgen05.mma (E tf32 in TMEM, P in smem)
 //                 then dQ = scale (U - D W), which equals scale sum_j P (T - D) K_j with D
 //                 the literal row sum of P (.) dAttn, and RoPE backward on the way out.
-//   attn_tc_dv    CTA = (head h, 128 of the S newest keys): over 64-query tiles,
-//                 dV_h += P_h^T dCtx_h.  P tiles come by TMA and the epilogue warps write
-//                 them transposed (tf32, K-major) for the MMA; dCtx^T tiles by TMA.  With
+//   attn_tc_dv    CTA = (head h, 128 of the S newest keys), two CTAs per SM: over 32-query
+//                 items, dV_h += P_h^T dCtx_h.  P tiles come by TMA and the writer warps
+//                 put them transposed (tf32) into tensor memory as the A operand;
+//                 dCtx^T tiles (B) by TMA; three items in flight.  With
 //                 several heads per KV head the per-head sums go to a workspace and
 //                 attn_tc_dv_sum adds them in head order.
 // All MMAs: M = 128, K = 8 per instruction, both operands K-major with 128-byte swizzle.
@@ -41,7 +42,8 @@ constexpr int kQM = 128;        // queries per dQ CTA
 constexpr int kQK = 32;         // keys per dQ tile
 constexpr int kQSlots = 4;      // dQ tiles in flight (V, K^T, P staged up to four tiles ahead)
 constexpr int kVK = 128;        // keys per dV CTA
-constexpr int kVQ = 64;         // queries per dV tile
+constexpr int kVQ = 32;         // queries per dV item
+constexpr int kVSlots = 3;      // dV items staged ahead (P tile and dCtx^T tile rings)
 constexpr int kAttnThreads = 320;    // producer warp, MMA warp, 8 epilogue warps
 constexpr int kEpiWarps = 8;          // two per TMEM lane quarter, each half of the columns
 
@@ -50,7 +52,7 @@ struct AttnTcParams {
     CUtensorMap kt;             // Kt   {L, hd, nkv}, box {32, hd, 1}
     CUtensorMap dct;            // dCT  {S, hd, nh},  box {32, hd, 1}
     CUtensorMap pq;             // attn {L, S, nh},   box {32, 128, 1}   (dQ: 128 queries x 32 keys)
-    CUtensorMap pv;             // attn {L, S, nh},   box {32, 64, 1}    (dV: 64 queries x 32 keys)
+    CUtensorMap pv;             // attn {L, S, nh},   box {32, 32, 1}    (dV: 32 queries x 32 keys)
     const float *dctx;          // dCtx [S, nh * hd]
     float *dq;                  // [S, nh * hd]
     float *dv;                  // [S, nkv * hd], or per-head partial sums [nh / nkv][S, nkv * hd]
@@ -412,21 +414,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
 
 template <int HD>
 struct DvLayout {
-    static constexpr int A_BYTES = kVK * kVQ * 4;        // P^T [128 keys][64 queries]: 2 boxes
-    static constexpr int B_BYTES = HD * kVQ * 4;         // dCtx^T [HD][64 queries]: 2 boxes
-    static constexpr int S_BYTES = kVQ * kVK * 4;        // P [64 queries][128 keys]: 4 boxes
-    static constexpr int A0 = 0, B0 = 2 * A_BYTES, P0 = B0 + 2 * B_BYTES, TOTAL = P0 + 2 * S_BYTES;
-    static constexpr uint32_t COLS = HD <= 32 ? 32 : (HD <= 64 ? 64 : (HD <= 128 ? 128 : 256));
+    // shared memory: rings of kVSlots slots: P tiles [kVQ queries][128 keys] (4 boxes) and
+    // dCtx^T tiles [HD][kVQ queries] (the B operand)
+    static constexpr int S_BYTES = kVQ * kVK * 4, B_BYTES = HD * kVQ * 4;
+    static constexpr int B0 = kVSlots * S_BYTES, TOTAL = B0 + kVSlots * B_BYTES;
+    // tensor memory: dV accumulator [128 keys][HD], then two P^T buffers [128 keys][kVQ] (A operand)
+    static constexpr uint32_t TA = HD;
+    static constexpr uint32_t COLS = (HD + 2 * kVQ) <= 128 ? 128 : 256;
 };
 
 template <int HD>
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __grid_constant__ AttnTcParams p) {
+__global__ void __launch_bounds__(kAttnThreads, 2) attn_tc_dv_kernel(const __grid_constant__ AttnTcParams p) {
     using Ly = DvLayout<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    __shared__ uint64_t bfull[2], bfree[2], afull[2], afree[2], dfull;
+    // sfull/sfree: P staging ring; bfull/bfree: dCtx^T ring; afull/afree: P^T in TMEM
+    __shared__ uint64_t sfull[kVSlots], sfree[kVSlots], bfull[kVSlots], bfree[kVSlots], afull[2], afree[2], dfull;
     __shared__ uint32_t tmem_base;
-    __shared__ int s_abort, s_b_issued, s_b_used;
+    __shared__ int s_abort, s_s_issued, s_b_issued, s_b_used;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.x, G = p.nh / p.nkv, kvh = h / G, g = h % G;
     const int k0 = int(blockIdx.y) * kVK;                 // among the S newest keys (heaviest first)
@@ -435,12 +440,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
 
     if (threadIdx.x == 0) {
         s_abort = 0;
-        s_b_issued = s_b_used = 0;
-        for (int s = 0; s < 2; ++s) {
+        s_s_issued = s_b_issued = s_b_used = 0;
+        for (int s = 0; s < kVSlots; ++s) {
+            mbar_init(&sfull[s], 1);
+            mbar_init(&sfree[s], kEpiWarps);
             mbar_init(&bfull[s], 1);
             mbar_init(&bfree[s], 1);
-            mbar_init(&afull[s], kEpiWarps);
-            mbar_init(&afree[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&afull[b], kEpiWarps);
+            mbar_init(&afree[b], 1);
         }
         mbar_init(&dfull, 1);
     }
@@ -455,41 +464,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
     const uint32_t tD = tmem_base;
 
     if (warp == 0) {
+        // ------------------------------------------------ TMA producer, kVSlots items ahead
         if (lane == 0) {
             for (int w = 0; w < nw; ++w) {
-                const int s = w & 1, qa = (t0 + w) * kVQ;
-                if (w >= 2 && !mbar_wait(&bfree[s], ((w - 2) >> 1) & 1, p.status, 30u)) { s_abort = 1; break; }
-                mbar_arrive_expect_tx(&bfull[s], Ly::B_BYTES + Ly::S_BYTES);
-                for (int b = 0; b < 2; ++b)
-                    tma_load_3d(sm + Ly::B0 + s * Ly::B_BYTES + b * (HD * 128), &p.dct, qa + b * 32, 0, h, &bfull[s]);
+                const int s = w % kVSlots, qa = (t0 + w) * kVQ;
+                if (w >= kVSlots && !mbar_wait(&sfree[s], (w / kVSlots - 1) & 1, p.status, 30u)) { s_abort = 1; break; }
+                mbar_arrive_expect_tx(&sfull[s], Ly::S_BYTES);
                 for (int b = 0; b < kVK / 32; ++b)
-                    tma_load_3d(sm + Ly::P0 + s * Ly::S_BYTES + b * (kVQ * 128), &p.pv, p.pos0 + k0 + b * 32, qa, h,
-                                &bfull[s]);
+                    tma_load_3d(sm + s * Ly::S_BYTES + b * (kVQ * 128), &p.pv, p.pos0 + k0 + b * 32, qa, h, &sfull[s]);
+                s_s_issued = w + 1;
+                if (w >= kVSlots && !mbar_wait(&bfree[s], (w / kVSlots - 1) & 1, p.status, 36u)) { s_abort = 1; break; }
+                mbar_arrive_expect_tx(&bfull[s], Ly::B_BYTES);
+                tma_load_3d(sm + Ly::B0 + s * Ly::B_BYTES, &p.dct, qa, 0, h, &bfull[s]);
                 s_b_issued = w + 1;
             }
         }
     } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer: dV += P^T (TMEM) dCtx^T^T
         if (lane == 0) {
             constexpr uint32_t id = idesc_tf32(kVK, HD);
             bool ok = true;
             for (int w = 0; w < nw; ++w) {
-                const int s = w & 1;
-                if (!mbar_wait(&afull[s], (w >> 1) & 1, p.status, 31u) ||
-                    !mbar_wait(&bfull[s], (w >> 1) & 1, p.status, 32u)) {
+                const int s = w % kVSlots;
+                if (!mbar_wait(&afull[w & 1], (w >> 1) & 1, p.status, 31u) ||
+                    !mbar_wait(&bfull[s], (w / kVSlots) & 1, p.status, 32u)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const uint8_t *a = sm + Ly::A0 + s * Ly::A_BYTES, *b = sm + Ly::B0 + s * Ly::B_BYTES;
-#pragma unroll
-                for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_tf32(tD, sw128_desc(a + kb * (kVK * 128)) + 2 * k, sw128_desc(b + kb * (HD * 128)) + 2 * k,
-                                 id, (w > 0 || kb > 0 || k > 0) ? 1u : 0u);
-                mma_commit(&bfree[s]);
-                mma_commit(&afree[s]);
                 s_b_used = w + 1;
+                tc_fence_after();
+                const uint64_t bd = sw128_desc(sm + Ly::B0 + s * Ly::B_BYTES);
+                const uint32_t ta = tD + Ly::TA + uint32_t((w & 1) * kVQ);
+#pragma unroll
+                for (int k = 0; k < kVQ / 8; ++k)
+                    mma_tf32_ts(tD, ta + uint32_t(8 * k), bd + 2 * k, id, (w > 0 || k > 0) ? 1u : 0u);
+                mma_commit(&bfree[s]);
+                mma_commit(&afree[w & 1]);
             }
             if (!ok) s_abort = 1;
             mma_commit(&dfull);
@@ -503,11 +513,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
         const int r = quarter * 32 + lane, jj = k0 + r;        // key row of this thread
         const bool key_ok = jj < p.S;
         const int box = r >> 5, col = r & 31;
+        const uint32_t lane_off = uint32_t(quarter * 32) << 16;
         bool ok = true;
         for (int w = 0; w < nw; ++w) {
-            const int s = w & 1, qa = (t0 + w) * kVQ + hf * HQ;
-            if (!mbar_wait(&bfull[s], (w >> 1) & 1, p.status, 33u)) { ok = false; break; }
-            const uint8_t *ps = sm + Ly::P0 + s * Ly::S_BYTES + box * (kVQ * 128) + (col & 3) * 4;
+            const int s = w % kVSlots, qa = (t0 + w) * kVQ + hf * HQ;
+            if (!mbar_wait(&sfull[s], (w / kVSlots) & 1, p.status, 33u)) { ok = false; break; }
+            const uint8_t *ps = sm + s * Ly::S_BYTES + box * (kVQ * 128) + (col & 3) * 4;
+            static_assert(HQ == 16, "one 16-column tensor-memory store per writer");
             uint32_t pt[HQ];
 #pragma unroll
             for (int qq = 0; qq < HQ; ++qq) {
@@ -515,21 +527,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
                 const bool vis = key_ok && (!p.causal || qa + qq >= jj);   // rows past S arrive as zeros
                 pt[qq] = to_tf32(vis ? v : 0.f);
             }
-            if (w >= 2 && !mbar_wait(&afree[s], ((w - 2) >> 1) & 1, p.status, 34u)) { ok = false; break; }
-            uint8_t *a = sm + Ly::A0 + s * Ly::A_BYTES;
-#pragma unroll
-            for (int c4 = 0; c4 < HQ / 4; ++c4) {
-                const int cc = hf * (HQ / 4) + c4;            // 16-byte chunk along the 64 queries
-                const uint32_t off = uint32_t(cc >> 3) * (kVK * 128) + sw128_off(r, cc & 7);
-                st_shared_v4(a + off, pt[4 * c4], pt[4 * c4 + 1], pt[4 * c4 + 2], pt[4 * c4 + 3]);
-            }
-            fence_proxy_async();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[s]);
+            if (lane == 0) mbar_arrive(&sfree[s]);               // staging slot read
+            if (w >= 2 && !mbar_wait(&afree[w & 1], ((w - 2) >> 1) & 1, p.status, 34u)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t ta = tD + Ly::TA + uint32_t((w & 1) * kVQ + hf * HQ) + lane_off;
+            tmem_st16(ta, pt);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[w & 1]);
         }
         if (ok && mbar_wait(&dfull, 0, p.status, 35u)) {
             tc_fence_after();
-            const uint32_t lane_off = uint32_t(quarter * 32) << 16;
             const int64_t kvd = int64_t(p.nkv) * HD;
             float *out = p.dv + (G > 1 ? int64_t(g) * p.S * kvd : 0) + int64_t(key_ok ? jj : 0) * kvd + kvh * HD;
 #pragma unroll 1
@@ -551,7 +561,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_kernel(const __gri
     tc_fence_before();
     __syncthreads();
     if (s_abort && threadIdx.x == 0) {
-        for (int b = s_b_used; b < s_b_issued; ++b) mbar_wait(&bfull[b & 1], (b >> 1) & 1, nullptr, 0u);
+        // at most kVSlots copies per ring are in flight: the last ones issued
+        for (int w = max(s_b_used, s_s_issued - kVSlots); w < s_s_issued; ++w)
+            mbar_wait(&sfull[w % kVSlots], (w / kVSlots) & 1, nullptr, 0u);
+        for (int w = max(s_b_used, s_b_issued - kVSlots); w < s_b_issued; ++w)
+            mbar_wait(&bfull[w % kVSlots], (w / kVSlots) & 1, nullptr, 0u);
     }
     __syncthreads();
     if (warp == 1) {
