@@ -16,6 +16,9 @@
 //       x pass   one read of each x tile gives the dA partials of every adapter;
 //       AdamW    sums the token-tile partials of dA and dB, applies the update.
 //     Every sum runs in a fixed order: the result does not depend on scheduling.
+#include <algorithm>
+
+#include "async.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -136,16 +139,18 @@ struct LoraSide {
     int O, n_ot, blk0, vecG;     // columns, column tiles, first G-pass block, 16-byte loads ok
     float s;
     tlb_lora l;
-    float *part_b;               // [n_rt][O][rank]
+    float *part_b;               // [nrc_b][O][rank] (sized for n_rt)
     float *part_gh;              // [n_ot][S][rank]
     float *gh;                   // [S][rank]
-    float *part_a;               // [n_rt][rank][C]
+    float *part_a;               // [nrc_a][rank][C] (sized for n_rt)
 };
 
 struct LoraSeqArgs {
     LoraSide side[2];
     const float *x;              // [S, C]
-    int nside, S, C, rank, n_rt, vecx;
+    int nside, S, C, rank, n_rt, vecx, vech;
+    int tpc_b, nrc_b;            // G pass: row tiles per chunk, chunks (dB partials)
+    int tpc_a, nrc_a;            // x pass: row tiles per chunk, chunks (dA partials)
 };
 
 // Zero-padded [kLT][kLP] tile of rows r0.. and columns c0.. of src [nrow, ncol] (leading dim ld).
@@ -167,63 +172,242 @@ __device__ __forceinline__ void load_tile(float *dst, const float *__restrict__ 
     }
 }
 
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
+    // 16 bytes global -> shared, zero-filled when !valid (no bytes are read then)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Start copying the [kLT][kLP] tile at rows r0.., columns c0.. of src [nrow, ncol] (leading
+// dim ld) with 16-byte cp.async when `vec`; else load it now.
+__device__ __forceinline__ void issue_tile(float *dst, const float *__restrict__ src, int64_t ld, int nrow, int ncol,
+                                           int r0, int c0, bool vec) {
+    if (!vec) {
+        load_tile(dst, src, ld, nrow, ncol, r0, c0, false);
+        return;
+    }
+    for (int e = threadIdx.x; e < kLT * (kLO / 4); e += blockDim.x) {
+        const int i = e / (kLO / 4), c = (e % (kLO / 4)) * 4;
+        const bool ok = r0 + i < nrow && c0 + c < ncol;
+        cp_async16(dst + i * kLP + c, ok ? src + int64_t(r0 + i) * ld + c0 + c : src, ok);
+    }
+}
+
+// [kLT][RB] rows r0.. of a [nrow, R] matrix, zero-padded to RB columns.
+template <int RB>
+__device__ __forceinline__ void issue_rows(float *dst, const float *__restrict__ src, int nrow, int R, int r0,
+                                           bool vec) {
+    if (vec) {                                   // R == RB, 16-byte aligned rows
+        for (int e = threadIdx.x; e < kLT * (RB / 4); e += blockDim.x) {
+            const int i = e / (RB / 4), c = (e % (RB / 4)) * 4;
+            const bool ok = r0 + i < nrow;
+            cp_async16(dst + i * RB + c, ok ? src + int64_t(r0 + i) * RB + c : src, ok);
+        }
+    } else {
+        for (int e = threadIdx.x; e < kLT * RB; e += blockDim.x) {
+            const int i = e / RB, r = e % RB;
+            dst[e] = (r < R && r0 + i < nrow) ? src[int64_t(r0 + i) * R + r] : 0.f;
+        }
+    }
+}
+
+// Block (column tile of one side, chunk of row tiles): one pass over its G tiles, staged
+// two deep, gives the dB partial of the chunk (kept in registers across its tiles) and
+// the gh partial of each tile.
 template <int RB>
 __global__ void __launch_bounds__(256) lora_gpass_kernel(LoraSeqArgs a) {
     extern __shared__ float4 sm4[];
-    float *sG = reinterpret_cast<float *>(sm4);   // [kLT][kLP]
-    float *sh = sG + kLT * kLP;                   // [kLT][RB]
-    float *sB = sh + kLT * RB;                    // [kLO][RB]
+    float *sG = reinterpret_cast<float *>(sm4);   // 2 x [kLT][kLP]
+    float *sh = sG + 2 * kLT * kLP;               // 2 x [kLT][RB]
+    float *sB = sh + 2 * kLT * RB;                // [kLO][RB]
     const int side = (a.nside > 1 && int(blockIdx.x) >= a.side[1].blk0) ? 1 : 0;
     const LoraSide &p = a.side[side];
-    const int ot = int(blockIdx.x) - p.blk0, rt = blockIdx.y;
-    const int r0 = rt * kLT, o0 = ot * kLO, R = a.rank, tid = threadIdx.x;
-    for (int e = tid; e < kLT * RB; e += 256) {
-        const int i = e / RB, r = e % RB;
-        sh[e] = (r < R && r0 + i < a.S) ? p.h[int64_t(r0 + i) * R + r] : 0.f;
-    }
+    const int ot = int(blockIdx.x) - p.blk0, o0 = ot * kLO, R = a.rank, tid = threadIdx.x;
+    const int rt0 = blockIdx.y * a.tpc_b, rt1 = min(rt0 + a.tpc_b, a.n_rt);
+    const bool vecG = p.vecG != 0, vech = a.vech != 0;
     for (int e = tid; e < kLO * RB; e += 256) {
         const int o = e / RB, r = e % RB;
         sB[e] = (r < R && o0 + o < p.O) ? p.l.b[int64_t(o0 + o) * R + r] : 0.f;
     }
-    load_tile(sG, p.G, p.O, a.S, p.O, r0, o0, p.vecG != 0);
-    __syncthreads();
-    {   // dB partial [128 columns][RB]: thread = (column, half of the ranks)
-        constexpr int NB = RB / 2;
-        const int o = tid % kLO, rb = (tid / kLO) * NB;
-        float acc[NB];
+    issue_tile(sG, p.G, p.O, a.S, p.O, rt0 * kLT, o0, vecG);
+    issue_rows<RB>(sh, p.h, a.S, R, rt0 * kLT, vech);
+    cp_async_commit();
+    constexpr int NB = RB / 2, NG = RB / 4;
+    const int ob = tid % kLO, rbb = (tid / kLO) * NB;          // dB: (column, half of the ranks)
+    const int ig = tid / 4, rbg = (tid % 4) * NG;              // gh: (token, quarter of the ranks)
+    float accb[NB];
 #pragma unroll
-        for (int k = 0; k < NB; ++k) acc[k] = 0.f;
+    for (int k = 0; k < NB; ++k) accb[k] = 0.f;
+    for (int rt = rt0; rt < rt1; ++rt) {
+        const int buf = (rt - rt0) & 1, r0 = rt * kLT;
+        if (rt + 1 < rt1) {
+            issue_tile(sG + (buf ^ 1) * kLT * kLP, p.G, p.O, a.S, p.O, r0 + kLT, o0, vecG);
+            issue_rows<RB>(sh + (buf ^ 1) * kLT * RB, p.h, a.S, R, r0 + kLT, vech);
+            cp_async_commit();
+            cp_async_wait_one();
+        } else {
+            cp_async_wait_all();
+        }
+        __syncthreads();
+        const float *g = sG + buf * kLT * kLP, *hh = sh + buf * kLT * RB;
 #pragma unroll 4
         for (int i = 0; i < kLT; ++i) {
-            const float g = sG[i * kLP + o];
+            const float gv = g[i * kLP + ob];
+            const float4 *h4 = reinterpret_cast<const float4 *>(hh + i * RB + rbb);   // NB % 4 == 0 or NB == 2
+            if constexpr (NB % 4 == 0) {
 #pragma unroll
-            for (int k = 0; k < NB; ++k) acc[k] = fmaf(g, sh[i * RB + rb + k], acc[k]);
+                for (int k = 0; k < NB / 4; ++k) {
+                    const float4 v = h4[k];
+                    accb[4 * k] = fmaf(gv, v.x, accb[4 * k]);
+                    accb[4 * k + 1] = fmaf(gv, v.y, accb[4 * k + 1]);
+                    accb[4 * k + 2] = fmaf(gv, v.z, accb[4 * k + 2]);
+                    accb[4 * k + 3] = fmaf(gv, v.w, accb[4 * k + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < NB; ++k) accb[k] = fmaf(gv, hh[i * RB + rbb + k], accb[k]);
+            }
         }
-        if (o0 + o < p.O) {
-            float *dst = p.part_b + (int64_t(rt) * p.O + o0 + o) * R;
+        float accg[NG];
 #pragma unroll
-            for (int k = 0; k < NB; ++k)
-                if (rb + k < R) dst[rb + k] = acc[k];
-        }
-    }
-    {   // gh partial [64 tokens][RB]: thread = (token, quarter of the ranks)
-        constexpr int NG = RB / 4;
-        const int i = tid / 4, rb = (tid % 4) * NG;
-        float acc[NG];
-#pragma unroll
-        for (int k = 0; k < NG; ++k) acc[k] = 0.f;
+        for (int k = 0; k < NG; ++k) accg[k] = 0.f;
 #pragma unroll 4
         for (int o = 0; o < kLO; ++o) {
-            const float g = sG[i * kLP + o];
+            const float gv = g[ig * kLP + o];
+            if constexpr (NG % 4 == 0) {
 #pragma unroll
-            for (int k = 0; k < NG; ++k) acc[k] = fmaf(g, sB[o * RB + rb + k], acc[k]);
+                for (int k = 0; k < NG / 4; ++k) {
+                    const float4 v = reinterpret_cast<const float4 *>(sB + o * RB + rbg)[k];
+                    accg[4 * k] = fmaf(gv, v.x, accg[4 * k]);
+                    accg[4 * k + 1] = fmaf(gv, v.y, accg[4 * k + 1]);
+                    accg[4 * k + 2] = fmaf(gv, v.z, accg[4 * k + 2]);
+                    accg[4 * k + 3] = fmaf(gv, v.w, accg[4 * k + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < NG; ++k) accg[k] = fmaf(gv, sB[o * RB + rbg + k], accg[k]);
+            }
         }
-        if (r0 + i < a.S) {
-            float *dst = p.part_gh + (int64_t(ot) * a.S + r0 + i) * R;
+        if (r0 + ig < a.S) {
+            float *dst = p.part_gh + (int64_t(ot) * a.S + r0 + ig) * R;
 #pragma unroll
             for (int k = 0; k < NG; ++k)
-                if (rb + k < R) dst[rb + k] = acc[k];
+                if (rbg + k < R) dst[rbg + k] = accg[k];
         }
+        __syncthreads();                           // buffer buf is refilled next iteration
+    }
+    if (o0 + ob < p.O) {
+        float *dst = p.part_b + (int64_t(blockIdx.y) * p.O + o0 + ob) * R;
+#pragma unroll
+        for (int k = 0; k < NB; ++k)
+            if (rbb + k < R) dst[rbb + k] = accb[k];
+    }
+}
+
+// Rank-16 G pass with 4 x 4 register blocks (the layers' rank): per tile, dB as 128
+// columns x 16 ranks = 32 column quads x 4 rank quads x 2 halves of the 64 rows, and
+// gh as 64 rows x 16 ranks = 16 row groups x 4 rank quads x 4 column quarters; every
+// float4 read from shared memory feeds four FMAs.  The halves / quarters meet in shared
+// memory in a fixed order.
+__global__ void __launch_bounds__(256) lora_gpass16_kernel(LoraSeqArgs a) {
+    constexpr int RB = 16;
+    extern __shared__ float4 sm4[];
+    float *sG = reinterpret_cast<float *>(sm4);   // 2 x [kLT][kLP]
+    float *sh = sG + 2 * kLT * kLP;               // 2 x [kLT][RB]
+    float *sB = sh + 2 * kLT * RB;                // [kLO][RB]
+    float *red = sB + kLO * RB;                   // [4][kLT][RB] gh quarters, then [2][kLO][RB] dB halves
+    const int side = (a.nside > 1 && int(blockIdx.x) >= a.side[1].blk0) ? 1 : 0;
+    const LoraSide &p = a.side[side];
+    const int ot = int(blockIdx.x) - p.blk0, o0 = ot * kLO, R = a.rank, tid = threadIdx.x;
+    const int rt0 = blockIdx.y * a.tpc_b, rt1 = min(rt0 + a.tpc_b, a.n_rt);
+    const bool vecG = p.vecG != 0, vech = a.vech != 0;
+    for (int e = tid; e < kLO * RB; e += 256) {
+        const int o = e / RB, r = e % RB;
+        sB[e] = (r < R && o0 + o < p.O) ? p.l.b[int64_t(o0 + o) * R + r] : 0.f;
+    }
+    issue_tile(sG, p.G, p.O, a.S, p.O, rt0 * kLT, o0, vecG);
+    issue_rows<RB>(sh, p.h, a.S, R, rt0 * kLT, vech);
+    cp_async_commit();
+    // dB: column quad cq, rank quad rq, row half ih
+    const int cq = tid & 31, rq = (tid >> 5) & 3, ih = tid >> 7;
+    // gh: rows iq + 16 u (u = 0..3), rank quad gq, column quarter oq
+    const int iq = tid & 15, gq = (tid >> 4) & 3, oq = tid >> 6;
+    float accb[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) accb[u][k] = 0.f;
+    for (int rt = rt0; rt < rt1; ++rt) {
+        const int buf = (rt - rt0) & 1, r0 = rt * kLT;
+        if (rt + 1 < rt1) {
+            issue_tile(sG + (buf ^ 1) * kLT * kLP, p.G, p.O, a.S, p.O, r0 + kLT, o0, vecG);
+            issue_rows<RB>(sh + (buf ^ 1) * kLT * RB, p.h, a.S, R, r0 + kLT, vech);
+            cp_async_commit();
+            cp_async_wait_one();
+        } else {
+            cp_async_wait_all();
+        }
+        __syncthreads();
+        const float *g = sG + buf * kLT * kLP, *hh = sh + buf * kLT * RB;
+#pragma unroll 4
+        for (int i = ih * (kLT / 2); i < (ih + 1) * (kLT / 2); ++i) {
+            const float4 gv = *reinterpret_cast<const float4 *>(g + i * kLP + 4 * cq);
+            const float4 hv = *reinterpret_cast<const float4 *>(hh + i * RB + 4 * rq);
+            const float gc[4] = {gv.x, gv.y, gv.z, gv.w}, hr[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) accb[u][k] = fmaf(gc[u], hr[k], accb[u][k]);
+        }
+        float accg[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) accg[u][k] = 0.f;
+#pragma unroll 2
+        for (int o = oq * (kLO / 4); o < (oq + 1) * (kLO / 4); o += 4) {
+            float gr[4][4], bo[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 v = *reinterpret_cast<const float4 *>(g + (iq + 16 * u) * kLP + o);
+                gr[u][0] = v.x; gr[u][1] = v.y; gr[u][2] = v.z; gr[u][3] = v.w;
+                const float4 w = *reinterpret_cast<const float4 *>(sB + (o + u) * RB + 4 * gq);
+                bo[u][0] = w.x; bo[u][1] = w.y; bo[u][2] = w.z; bo[u][3] = w.w;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) accg[u][k] = fmaf(gr[u][v], bo[v][k], accg[u][k]);
+        }
+        // gh partial of the tile: sum the four column quarters in order
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<float4 *>(red + (oq * kLT + iq + 16 * u) * RB + 4 * gq) =
+                make_float4(accg[u][0], accg[u][1], accg[u][2], accg[u][3]);
+        __syncthreads();
+        for (int e = tid; e < kLT * RB; e += 256) {
+            const int i = e / RB, r = e % RB;
+            const float v = red[e] + red[kLT * RB + e] + red[2 * kLT * RB + e] + red[3 * kLT * RB + e];
+            if (r < R && r0 + i < a.S) p.part_gh[(int64_t(ot) * a.S + r0 + i) * R + r] = v;
+        }
+        __syncthreads();                           // buffer buf and red are reused next iteration
+    }
+    // dB partial of the chunk: sum the two row halves in order
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        *reinterpret_cast<float4 *>(red + (ih * kLO + 4 * cq + u) * RB + 4 * rq) =
+            make_float4(accb[u][0], accb[u][1], accb[u][2], accb[u][3]);
+    __syncthreads();
+    for (int e = tid; e < kLO * RB; e += 256) {
+        const int o = e / RB, r = e % RB;
+        if (r < R && o0 + o < p.O)
+            p.part_b[(int64_t(blockIdx.y) * p.O + o0 + o) * R + r] = red[e] + red[kLO * RB + e];
     }
 }
 
@@ -242,38 +426,144 @@ __global__ void __launch_bounds__(256) lora_gh_sum_kernel(LoraSeqArgs a) {
     p.gh[e] = p.s * acc;
 }
 
+// Block (column tile of x, chunk of row tiles): one pass over its x tiles, staged two
+// deep, gives the dA partials of the chunk for every side (registers across its tiles).
 template <int RB>
 __global__ void __launch_bounds__(256) lora_xpass_kernel(LoraSeqArgs a) {
     extern __shared__ float4 sm4[];
-    float *sx = reinterpret_cast<float *>(sm4);   // [kLT][kLP]
-    float *sg = sx + kLT * kLP;                   // [nside][kLT][RB]
-    const int ct = blockIdx.x, rt = blockIdx.y;
-    const int c0 = ct * kLO, r0 = rt * kLT, R = a.rank, tid = threadIdx.x;
-    for (int sd = 0; sd < a.nside; ++sd)
-        for (int e = tid; e < kLT * RB; e += 256) {
-            const int i = e / RB, r = e % RB;
-            sg[sd * kLT * RB + e] = (r < R && r0 + i < a.S) ? a.side[sd].gh[int64_t(r0 + i) * R + r] : 0.f;
-        }
-    load_tile(sx, a.x, a.C, a.S, a.C, r0, c0, a.vecx != 0);
-    __syncthreads();
+    float *sx = reinterpret_cast<float *>(sm4);   // 2 x [kLT][kLP]
+    float *sg = sx + 2 * kLT * kLP;               // 2 x [nside][kLT][RB]
+    const int c0 = blockIdx.x * kLO, R = a.rank, tid = threadIdx.x;
+    const int rt0 = blockIdx.y * a.tpc_a, rt1 = min(rt0 + a.tpc_a, a.n_rt);
+    const bool vecx = a.vecx != 0, vech = a.vech != 0;
+    auto issue = [&](int rt, int buf) {
+        issue_tile(sx + buf * kLT * kLP, a.x, a.C, a.S, a.C, rt * kLT, c0, vecx);
+        for (int sd = 0; sd < a.nside; ++sd)
+            issue_rows<RB>(sg + (buf * 2 + sd) * kLT * RB, a.side[sd].gh, a.S, R, rt * kLT, vech);
+        cp_async_commit();
+    };
+    issue(rt0, 0);
     constexpr int NB = RB / 2;
     const int c = tid % kLO, rb = (tid / kLO) * NB;
-    for (int sd = 0; sd < a.nside; ++sd) {
-        const float *g = sg + sd * kLT * RB;
-        float acc[NB];
+    float acc[2][NB];
 #pragma unroll
-        for (int k = 0; k < NB; ++k) acc[k] = 0.f;
-#pragma unroll 4
-        for (int i = 0; i < kLT; ++i) {
-            const float xv = sx[i * kLP + c];
+    for (int sd = 0; sd < 2; ++sd)
 #pragma unroll
-            for (int k = 0; k < NB; ++k) acc[k] = fmaf(g[i * RB + rb + k], xv, acc[k]);
+        for (int k = 0; k < NB; ++k) acc[sd][k] = 0.f;
+    for (int rt = rt0; rt < rt1; ++rt) {
+        const int buf = (rt - rt0) & 1;
+        if (rt + 1 < rt1) {
+            issue(rt + 1, buf ^ 1);
+            cp_async_wait_one();
+        } else {
+            cp_async_wait_all();
         }
-        if (c0 + c < a.C) {
-            float *dst = a.side[sd].part_a + int64_t(rt) * R * a.C + c0 + c;
+        __syncthreads();
+        const float *xs = sx + buf * kLT * kLP;
+#pragma unroll
+        for (int sd = 0; sd < 2; ++sd) {
+            if (sd >= a.nside) break;
+            const float *g = sg + (buf * 2 + sd) * kLT * RB;
+#pragma unroll 4
+            for (int i = 0; i < kLT; ++i) {
+                const float xv = xs[i * kLP + c];
+                if constexpr (NB % 4 == 0) {
+#pragma unroll
+                    for (int k = 0; k < NB / 4; ++k) {
+                        const float4 v = reinterpret_cast<const float4 *>(g + i * RB + rb)[k];
+                        acc[sd][4 * k] = fmaf(v.x, xv, acc[sd][4 * k]);
+                        acc[sd][4 * k + 1] = fmaf(v.y, xv, acc[sd][4 * k + 1]);
+                        acc[sd][4 * k + 2] = fmaf(v.z, xv, acc[sd][4 * k + 2]);
+                        acc[sd][4 * k + 3] = fmaf(v.w, xv, acc[sd][4 * k + 3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < NB; ++k) acc[sd][k] = fmaf(g[i * RB + rb + k], xv, acc[sd][k]);
+                }
+            }
+        }
+        __syncthreads();                           // buffer buf is refilled next iteration
+    }
+    if (c0 + c < a.C) {
+#pragma unroll
+        for (int sd = 0; sd < 2; ++sd) {
+            if (sd >= a.nside) break;
+            float *dst = a.side[sd].part_a + int64_t(blockIdx.y) * R * a.C + c0 + c;
 #pragma unroll
             for (int k = 0; k < NB; ++k)
-                if (rb + k < R) dst[int64_t(rb + k) * a.C] = acc[k];
+                if (rb + k < R) dst[int64_t(rb + k) * a.C] = acc[sd][k];
+        }
+    }
+}
+
+// Rank-16 x pass with 4 x 4 register blocks: dA of each side as 16 ranks x 128 columns =
+// 4 rank quads x 32 column quads x 2 halves of the 64 rows; the halves meet in shared
+// memory (in the x buffers, free after the last tile) in a fixed order.
+__global__ void __launch_bounds__(256) lora_xpass16_kernel(LoraSeqArgs a) {
+    constexpr int RB = 16;
+    extern __shared__ float4 sm4[];
+    float *sx = reinterpret_cast<float *>(sm4);   // 2 x [kLT][kLP]
+    float *sg = sx + 2 * kLT * kLP;               // 2 x [nside][kLT][RB]
+    const int c0 = blockIdx.x * kLO, R = a.rank, tid = threadIdx.x;
+    const int rt0 = blockIdx.y * a.tpc_a, rt1 = min(rt0 + a.tpc_a, a.n_rt);
+    const bool vecx = a.vecx != 0, vech = a.vech != 0;
+    auto issue = [&](int rt, int buf) {
+        issue_tile(sx + buf * kLT * kLP, a.x, a.C, a.S, a.C, rt * kLT, c0, vecx);
+        for (int sd = 0; sd < a.nside; ++sd)
+            issue_rows<RB>(sg + (buf * 2 + sd) * kLT * RB, a.side[sd].gh, a.S, R, rt * kLT, vech);
+        cp_async_commit();
+    };
+    issue(rt0, 0);
+    const int cq = tid & 31, rq = (tid >> 5) & 3, ih = tid >> 7;
+    float acc[2][4][4];                            // [side][column][rank]
+#pragma unroll
+    for (int sd = 0; sd < 2; ++sd)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[sd][u][k] = 0.f;
+    for (int rt = rt0; rt < rt1; ++rt) {
+        const int buf = (rt - rt0) & 1;
+        if (rt + 1 < rt1) {
+            issue(rt + 1, buf ^ 1);
+            cp_async_wait_one();
+        } else {
+            cp_async_wait_all();
+        }
+        __syncthreads();
+        const float *xs = sx + buf * kLT * kLP;
+#pragma unroll 2
+        for (int i = ih * (kLT / 2); i < (ih + 1) * (kLT / 2); ++i) {
+            const float4 xv = *reinterpret_cast<const float4 *>(xs + i * kLP + 4 * cq);
+            const float xc[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int sd = 0; sd < 2; ++sd) {
+                if (sd >= a.nside) break;
+                const float4 gv = *reinterpret_cast<const float4 *>(sg + ((buf * 2 + sd) * kLT + i) * RB + 4 * rq);
+                const float gr[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc[sd][u][k] = fmaf(gr[k], xc[u], acc[sd][u][k]);
+            }
+        }
+        __syncthreads();                           // buffer buf is refilled next iteration
+    }
+    // halves in order: red[ih][side][rank][column]
+    float *red = sx;
+#pragma unroll
+    for (int sd = 0; sd < 2; ++sd)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<float4 *>(red + ((ih * 2 + sd) * RB + 4 * rq + k) * kLO + 4 * cq) =
+                make_float4(acc[sd][0][k], acc[sd][1][k], acc[sd][2][k], acc[sd][3][k]);
+    __syncthreads();
+    for (int sd = 0; sd < a.nside; ++sd) {
+        float *dst = a.side[sd].part_a + int64_t(blockIdx.y) * R * a.C;
+        for (int e = tid; e < RB * kLO; e += 256) {
+            const int r = e / kLO, c = e % kLO;
+            if (r < R && c0 + c < a.C)
+                dst[int64_t(r) * a.C + c0 + c] = red[(sd * RB + r) * kLO + c] + red[((2 + sd) * RB + r) * kLO + c];
         }
     }
 }
@@ -290,7 +580,7 @@ __global__ void __launch_bounds__(256) lora_seq_adamw_kernel(LoraSeqArgs a, Adam
         if (e < 0) break;
         if (e < nA) {
             float g = 0.f;
-            for (int rt = 0; rt < a.n_rt; ++rt) g += p.part_a[int64_t(rt) * nA + e];
+            for (int rt = 0; rt < a.nrc_a; ++rt) g += p.part_a[int64_t(rt) * nA + e];
             if (p.l.grad_a) p.l.grad_a[e] = g;
             float m = p.l.m_a[e], v = p.l.v_a[e];
             p.l.a[e] = adam_elem(p.l.a[e], g, m, v, ka);
@@ -301,7 +591,7 @@ __global__ void __launch_bounds__(256) lora_seq_adamw_kernel(LoraSeqArgs a, Adam
         } else if (e < nA + nB) {
             const int64_t f = e - nA;
             float g = 0.f;
-            for (int rt = 0; rt < a.n_rt; ++rt) g += p.part_b[int64_t(rt) * nB + f];
+            for (int rt = 0; rt < a.nrc_b; ++rt) g += p.part_b[int64_t(rt) * nB + f];
             g *= p.s;
             if (p.l.grad_b) p.l.grad_b[f] = g;
             float m = p.l.m_b[f], v = p.l.v_b[f];
@@ -341,20 +631,39 @@ SideBytes side_bytes(int64_t S, int out_dim, int in_dim, int rank) {
 }
 
 template <int RB>
-int lora_seq_run(const LoraSeqArgs &a, int n_ot_total, const AdamCoef &ka, const AdamCoef &kb, double *sumsq,
+int lora_seq_run(LoraSeqArgs a, int n_ot_total, const AdamCoef &ka, const AdamCoef &kb, double *sumsq,
                  cudaStream_t st) {
-    const size_t smg = size_t(kLT * kLP + kLT * RB + kLO * RB) * 4;
-    const size_t smx = size_t(kLT * kLP + 2 * kLT * RB) * 4;
+    // chunks of row tiles per block: at most two blocks per SM in each pass (one wave)
+    const int target = 2 * num_sms();
+    a.nrc_b = int(std::min<int64_t>(a.n_rt, std::max<int64_t>(1, target / n_ot_total)));
+    a.tpc_b = int(ceil_div(a.n_rt, a.nrc_b));
+    a.nrc_b = int(ceil_div(a.n_rt, a.tpc_b));
+    const int n_ct = int(ceil_div(a.C, kLO));
+    a.nrc_a = int(std::min<int64_t>(a.n_rt, std::max<int64_t>(1, target / n_ct)));
+    a.tpc_a = int(ceil_div(a.n_rt, a.nrc_a));
+    a.nrc_a = int(ceil_div(a.n_rt, a.tpc_a));
+    const size_t smg = size_t(2 * kLT * kLP + 2 * kLT * RB + kLO * RB) * 4;
+    const size_t smx = size_t(2 * kLT * kLP + 4 * kLT * RB) * 4;
     if (smg > 48 * 1024)
         TLB_CUDA(cudaFuncSetAttribute(lora_gpass_kernel<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smg)));
-    if (smx > 48 * 1024)
+    if (smx > 48 * 1024) {
         TLB_CUDA(cudaFuncSetAttribute(lora_xpass_kernel<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smx)));
-    lora_gpass_kernel<RB><<<dim3(unsigned(n_ot_total), unsigned(a.n_rt)), 256, smg, st>>>(a);
+        if constexpr (RB == 16)
+            TLB_CUDA(cudaFuncSetAttribute(lora_xpass16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smx)));
+    }
+    if constexpr (RB == 16) {
+        const size_t sm16 = smg + size_t(4 * kLT * RB) * 4;
+        TLB_CUDA(cudaFuncSetAttribute(lora_gpass16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm16)));
+        lora_gpass16_kernel<<<dim3(unsigned(n_ot_total), unsigned(a.nrc_b)), 256, sm16, st>>>(a);
+    } else {
+        lora_gpass_kernel<RB><<<dim3(unsigned(n_ot_total), unsigned(a.nrc_b)), 256, smg, st>>>(a);
+    }
     TLB_TRY(check_launch("lora_gpass"));
     const int64_t ngh = int64_t(a.nside) * a.S * a.rank;
     lora_gh_sum_kernel<<<unsigned(ceil_div(ngh, int64_t(256))), 256, 0, st>>>(a);
     TLB_TRY(check_launch("lora_gh_sum"));
-    lora_xpass_kernel<RB><<<dim3(unsigned(ceil_div(a.C, kLO)), unsigned(a.n_rt)), 256, smx, st>>>(a);
+    if constexpr (RB == 16) lora_xpass16_kernel<<<dim3(unsigned(n_ct), unsigned(a.nrc_a)), 256, smx, st>>>(a);
+    else lora_xpass_kernel<RB><<<dim3(unsigned(n_ct), unsigned(a.nrc_a)), 256, smx, st>>>(a);
     TLB_TRY(check_launch("lora_xpass"));
     int64_t np = 0;
     for (int sd = 0; sd < a.nside; ++sd) np += int64_t(a.rank) * (a.C + a.side[sd].O);
@@ -383,6 +692,9 @@ int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x
     a.rank = rank;
     a.n_rt = int(n_rt);
     a.vecx = (in_dim % 4 == 0 && aligned16(x)) ? 1 : 0;
+    // rows of h and gh stream with 16-byte copies when they are exactly one padded row
+    const int rb = rank <= 4 ? 4 : rank <= 8 ? 8 : rank <= 16 ? 16 : rank <= 32 ? 32 : 64;
+    a.vech = rank == rb ? 1 : 0;
     int blk = 0;
     for (int sd = 0; sd < njobs; ++sd) {
         const LoraJob &j = jobs[sd];
@@ -392,6 +704,7 @@ int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x
         TLB_REQUIRE((reinterpret_cast<uintptr_t>(base) & 255u) == 0, TLB_EINVAL, "lora: scratch not 256-byte aligned");
         p.G = j.G;
         p.h = j.h;
+        if (!aligned16(j.h)) a.vech = 0;
         p.O = j.out_dim;
         p.n_ot = int(ceil_div(int64_t(j.out_dim), int64_t(kLO)));
         p.blk0 = blk;
