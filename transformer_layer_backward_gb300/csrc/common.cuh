@@ -209,6 +209,29 @@ struct RopeFreqs {
 };
 void rope_freqs(RopeFreqs &f, int head_dim, float base);
 
+// Gated-activation backward of one element ([FFN] "ReLU^2 x Mul Backward"; [RS] SwiGLU):
+// hidden = act(g) * u, dh = dL/dhidden -> dg = dL/dg, du = dL/du.  With CACHE, s = silu(g)
+// comes from the forward's cache.
+template <int ACT, bool CACHE>
+__device__ __forceinline__ void act_bwd_elem(float g, float u, float s, float dh, float &dg, float &du) {
+    if constexpr (ACT == TLB_ACT_RELU2_MUL) {
+        const float r = fmaxf(g, 0.f);
+        dg = dh * u * 2.f * r;
+        du = dh * r * r;
+    } else {
+        const float sig = 1.f / (1.f + expf(-g));
+        const float y = g * sig;
+        dg = dh * u * (sig * (1.f + g - y));
+        du = dh * (CACHE ? s : y);
+    }
+}
+
+// bf16 outputs (the A operands of the [W_gate | W_up]^T tensor-core GEMM)
+__device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    return make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+}
+
 // AdamW constants of one parameter tensor ([RS] cpu_adamw).  1 - beta and the bias
 // corrections are formed in double on the host and rounded once.
 struct AdamCoef {

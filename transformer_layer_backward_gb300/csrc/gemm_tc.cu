@@ -14,7 +14,8 @@
 //               k block into the accumulator of the segment's parity; tcgen05.commit
 //               frees each stage and, after a segment's last block, hands the
 //               accumulator over
-//   warps 2..5  epilogue: tcgen05.ld 32x32b.x32 (each warp its 32 TMEM lanes = rows),
+//   warps 2..9  epilogue: tcgen05.ld 32x32b.x32 (two warps per 32 TMEM lanes = rows, each
+//               half of the columns),
 //               scale, optional accumulate into C, fp32 stores, then release the
 //               accumulator, so one segment's epilogue overlaps the next one's MMAs
 // K may come from two segments (A0.B0^T + A1.B1^T, e.g. [dG | dU] . [W_gate | W_up]^T).
@@ -42,7 +43,8 @@ namespace {
 
 constexpr int kBM = 128, kBK = 64;       // tile rows, k block (64 bf16 = 128 bytes)
 constexpr int kStages = 4;
-constexpr int kThreadsTC = 192;          // 6 warps
+constexpr int kThreadsTC = 320;          // 10 warps: producer, MMA, 8 epilogue warps
+constexpr int kEpiWarpsTC = 8;           // two per TMEM lane quarter, each half of the columns
 
 struct TcParams {
     CUtensorMap a[2];                    // bf16 [M, K_seg], box 64 x 128
@@ -54,6 +56,11 @@ struct TcParams {
     float *out;                          // [M, N] fp32
     int accumulate;
     float *partial;                      // [ctas][2][kBM * BN] fp32 partial tiles
+    // epilogue: mode 0 writes out (+)= alpha acc; mode 1 treats alpha acc as dh and writes
+    // the gated-activation backward dG, dU in bf16 ([FFN] ReLU^2 x Mul / [RS] SwiGLU)
+    int mode, act, act_cache;
+    const float *gate, *up, *silu;       // [M, N] fp32 (mode 1)
+    uint2 *dg, *du;                      // [M, N] bf16, four per uint2 (mode 1)
     // schedule over the flattened (tile, k block) iterations, tiles numbered m fastest:
     // CTA c first runs the whole tiles [c dp, (c + 1) dp), then the stream-K share
     // [sk_base + sk_work c / ctas, sk_base + sk_work (c + 1) / ctas) of the rest
@@ -73,6 +80,83 @@ struct TcFixup {
 
 __host__ __device__ __forceinline__ int64_t sk_start(int64_t work, int ctas, int c) {
     return work * c / ctas;
+}
+
+// Epilogue of four columns col..col+3 (< N, col % 4 == 0) of one row; acc before alpha.
+__device__ __forceinline__ void emit4(const TcParams &p, int row, int col, float4 acc) {
+    const int64_t e = int64_t(row) * p.N + col;
+    const float4 d = make_float4(p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w);
+    if (p.mode == 0) {
+        float4 y = d;
+        if (p.accumulate) {
+            const float4 c = *reinterpret_cast<const float4 *>(p.out + e);
+            y.x += c.x; y.y += c.y; y.z += c.z; y.w += c.w;
+        }
+        *reinterpret_cast<float4 *>(p.out + e) = y;
+        return;
+    }
+    const float4 g = ld_stream(reinterpret_cast<const float4 *>(p.gate + e));
+    const float4 u = ld_stream(reinterpret_cast<const float4 *>(p.up + e));
+    float4 og, ou;
+    if (p.act == TLB_ACT_RELU2_MUL) {
+        act_bwd_elem<TLB_ACT_RELU2_MUL, false>(g.x, u.x, 0.f, d.x, og.x, ou.x);
+        act_bwd_elem<TLB_ACT_RELU2_MUL, false>(g.y, u.y, 0.f, d.y, og.y, ou.y);
+        act_bwd_elem<TLB_ACT_RELU2_MUL, false>(g.z, u.z, 0.f, d.z, og.z, ou.z);
+        act_bwd_elem<TLB_ACT_RELU2_MUL, false>(g.w, u.w, 0.f, d.w, og.w, ou.w);
+    } else if (p.act_cache) {
+        const float4 sv = ld_stream(reinterpret_cast<const float4 *>(p.silu + e));
+        act_bwd_elem<TLB_ACT_SILU_MUL, true>(g.x, u.x, sv.x, d.x, og.x, ou.x);
+        act_bwd_elem<TLB_ACT_SILU_MUL, true>(g.y, u.y, sv.y, d.y, og.y, ou.y);
+        act_bwd_elem<TLB_ACT_SILU_MUL, true>(g.z, u.z, sv.z, d.z, og.z, ou.z);
+        act_bwd_elem<TLB_ACT_SILU_MUL, true>(g.w, u.w, sv.w, d.w, og.w, ou.w);
+    } else {
+        act_bwd_elem<TLB_ACT_SILU_MUL, false>(g.x, u.x, 0.f, d.x, og.x, ou.x);
+        act_bwd_elem<TLB_ACT_SILU_MUL, false>(g.y, u.y, 0.f, d.y, og.y, ou.y);
+        act_bwd_elem<TLB_ACT_SILU_MUL, false>(g.z, u.z, 0.f, d.z, og.z, ou.z);
+        act_bwd_elem<TLB_ACT_SILU_MUL, false>(g.w, u.w, 0.f, d.w, og.w, ou.w);
+    }
+    p.dg[e / 4] = pack_bf16x4(og.x, og.y, og.z, og.w);
+    p.du[e / 4] = pack_bf16x4(ou.x, ou.y, ou.z, ou.w);
+}
+
+// Activation epilogue of one 32 x 32 block (rows rbase.., columns col0..) held in shared
+// memory [32][33]: lanes are 8 column quads x 4 rows; every load of the block is issued
+// before the first store, so the memory latency is paid once per block.
+template <int ACT, bool CACHE>
+__device__ __forceinline__ void act_block_t(const TcParams &p, int rbase, int col0, const float *blk, int lane) {
+    const int c4 = (lane & 7) * 4, rl = lane >> 3;
+    float4 g[8], u[8], sv[8];
+    bool ok[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int r = 4 * k + rl;
+        ok[k] = rbase + r < p.M && col0 + c4 < p.N;
+        const int64_t e = ok[k] ? int64_t(rbase + r) * p.N + col0 + c4 : 0;
+        g[k] = ld_stream(reinterpret_cast<const float4 *>(p.gate + e));
+        u[k] = ld_stream(reinterpret_cast<const float4 *>(p.up + e));
+        if constexpr (CACHE) sv[k] = ld_stream(reinterpret_cast<const float4 *>(p.silu + e));
+        else sv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int r = 4 * k + rl;
+        if (!ok[k]) continue;
+        const float *a = blk + r * 33 + c4;
+        float4 og, ou;
+        act_bwd_elem<ACT, CACHE>(g[k].x, u[k].x, sv[k].x, p.alpha * a[0], og.x, ou.x);
+        act_bwd_elem<ACT, CACHE>(g[k].y, u[k].y, sv[k].y, p.alpha * a[1], og.y, ou.y);
+        act_bwd_elem<ACT, CACHE>(g[k].z, u[k].z, sv[k].z, p.alpha * a[2], og.z, ou.z);
+        act_bwd_elem<ACT, CACHE>(g[k].w, u[k].w, sv[k].w, p.alpha * a[3], og.w, ou.w);
+        const int64_t e = int64_t(rbase + r) * p.N + col0 + c4;
+        p.dg[e / 4] = pack_bf16x4(og.x, og.y, og.z, og.w);
+        p.du[e / 4] = pack_bf16x4(ou.x, ou.y, ou.z, ou.w);
+    }
+}
+
+__device__ __forceinline__ void act_block(const TcParams &p, int rbase, int col0, const float *blk, int lane) {
+    if (p.act == TLB_ACT_RELU2_MUL) act_block_t<TLB_ACT_RELU2_MUL, false>(p, rbase, col0, blk, lane);
+    else if (p.act_cache) act_block_t<TLB_ACT_SILU_MUL, true>(p, rbase, col0, blk, lane);
+    else act_block_t<TLB_ACT_SILU_MUL, false>(p, rbase, col0, blk, lane);
 }
 
 template <int BN>
@@ -118,7 +202,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accfull[b], 1);
-            mbar_init(&accempty[b], 4);
+            mbar_init(&accempty[b], kEpiWarpsTC);
         }
         mbar_init(&done, 1);
     }
@@ -191,8 +275,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
             mbar_wait(&done, 0, nullptr, 0u);
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
+        // ------------------------------------------------ epilogue (warps 2..9)
         const int q = warp & 3;                   // TMEM lane quarter this warp may read
+        float *ep = reinterpret_cast<float *>(smem + kStages * STAGE);   // 8 x [32][33] transpose blocks
         int i = 0;
         for (int64_t gs = g0; gs < g1; ++i) {
             int m0, n0, kb0, kb1;
@@ -207,7 +292,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
             }
             tc_fence_after();
             const int row = m0 + q * 32 + lane;
-            for (int j = 0; j < BN / 32; ++j) {
+            const int half = (warp - 2) >> 2;     // this warp's half of the tile's columns
+            for (int j = half * (BN / 64); j < (half + 1) * (BN / 64); ++j) {
                 uint32_t v[32];
                 tmem_ld32(tmem + uint32_t(b * BN) + (uint32_t(q * 32) << 16) + uint32_t(j * 32), v);
                 tmem_wait_ld();
@@ -222,26 +308,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                             __uint_as_float(v[t + 3]));
                     continue;
                 }
-                if (row >= p.M || col0 >= p.N) continue;
-                {
-                    float *o = p.out + int64_t(row) * p.N + col0;
-                    if (col0 + 32 <= p.N && (p.N & 3) == 0) {
+                if (p.mode == 1) {
+                    // activation epilogue: the warp's 32 x 32 block goes through shared memory
+                    // so that lanes run along columns and every global access is coalesced
+                    float *blk = ep + (warp - 2) * 32 * 33;
 #pragma unroll
-                        for (int t = 0; t < 32; t += 4) {
-                            float4 r = make_float4(p.alpha * __uint_as_float(v[t]), p.alpha * __uint_as_float(v[t + 1]),
-                                                   p.alpha * __uint_as_float(v[t + 2]),
-                                                   p.alpha * __uint_as_float(v[t + 3]));
-                            if (p.accumulate) {
-                                const float4 c = *reinterpret_cast<const float4 *>(o + t);
-                                r.x += c.x; r.y += c.y; r.z += c.z; r.w += c.w;
-                            }
-                            *reinterpret_cast<float4 *>(o + t) = r;
-                        }
-                    } else {
-                        for (int t = 0; t < 32 && col0 + t < p.N; ++t)
-                            o[t] = p.alpha * __uint_as_float(v[t]) + (p.accumulate ? o[t] : 0.f);
-                    }
+                    for (int t = 0; t < 32; ++t) blk[lane * 33 + t] = __uint_as_float(v[t]);
+                    __syncwarp();
+                    act_block(p, m0 + q * 32, col0, blk, lane);
+                    __syncwarp();
+                    continue;
                 }
+                if (row >= p.M || col0 >= p.N) continue;
+#pragma unroll
+                for (int t = 0; t < 32; t += 4)                 // N % 4 == 0 (tc_supported)
+                    if (col0 + t < p.N)
+                        emit4(p, row, col0 + t,
+                              make_float4(__uint_as_float(v[t]), __uint_as_float(v[t + 1]),
+                                          __uint_as_float(v[t + 2]), __uint_as_float(v[t + 3])));
             }
             tc_fence_before();
             __syncwarp();
@@ -283,18 +367,7 @@ __global__ void __launch_bounds__(256) tc_fixup_kernel(const __grid_constant__ T
         }
         const int row = m0 + r, col = n0 + c4;
         if (row >= p.M || col >= p.N) continue;
-        float *o = p.out + int64_t(row) * p.N + col;
-        if (col + 4 <= p.N) {
-            float4 y = make_float4(p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w);
-            if (p.accumulate) {
-                const float4 c = *reinterpret_cast<const float4 *>(o);
-                y.x += c.x; y.y += c.y; y.z += c.z; y.w += c.w;
-            }
-            *reinterpret_cast<float4 *>(o) = y;
-        } else {
-            const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-            for (int u = 0; u < 4 && col + u < p.N; ++u) o[u] = p.alpha * a4[u] + (p.accumulate ? o[u] : 0.f);
-        }
+        emit4(p, row, col, acc);
     }
 }
 
@@ -326,7 +399,7 @@ int make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int b
 
 template <int BN>
 int launch_tc(const TcParams &p, cudaStream_t st) {
-    constexpr int smem = kStages * (kBM * kBK * 2 + BN * kBK * 2) + 1024;
+    constexpr int smem = kStages * (kBM * kBK * 2 + BN * kBK * 2) + kEpiWarpsTC * 32 * 33 * 4 + 1024;
     auto k = tc_gemm_kernel<BN>;
     TLB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     k<<<p.ctas, kThreadsTC, smem, st>>>(p);
@@ -422,12 +495,19 @@ bool tc_supported(int64_t M, int64_t N, int64_t K) {
 }
 
 int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, float *out, bool accumulate,
-            float *partial, uint32_t *status, cudaStream_t st) {
+            float *partial, uint32_t *status, cudaStream_t st, const TcActEpilogue *act) {
     TLB_REQUIRE(nseg == 1 || nseg == 2, TLB_EINVAL, "tcgen05 GEMM: 1 or 2 K segments");
     const int64_t K = seg[0].K + (nseg > 1 ? seg[1].K : 0);
     const TcPlan pl = tc_plan(M, N, K);
     TLB_REQUIRE(partial != nullptr, TLB_EINVAL, "tcgen05 GEMM: needs a partial-tile buffer");
-    TLB_REQUIRE(aligned16(out), TLB_EUNSUPPORTED, "tcgen05 GEMM: output alignment");
+    if (act != nullptr) {
+        const bool cache = act->act == TLB_ACT_SILU_MUL && act->silu_gate != nullptr;
+        TLB_REQUIRE(!accumulate && N % 4 == 0 && aligned16(act->gate) && aligned16(act->up) &&
+                        aligned16(act->dgate) && aligned16(act->dup) && (!cache || aligned16(act->silu_gate)),
+                    TLB_EUNSUPPORTED, "tcgen05 GEMM: activation epilogue operands");
+    } else {
+        TLB_REQUIRE(aligned16(out), TLB_EUNSUPPORTED, "tcgen05 GEMM: output alignment");
+    }
     TcParams p;
     memset(&p, 0, sizeof(p));
     for (int i = 0; i < nseg; ++i) {
@@ -444,6 +524,16 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
     p.out = out;
     p.accumulate = accumulate ? 1 : 0;
     p.partial = partial;
+    if (act != nullptr) {
+        p.mode = 1;
+        p.act = act->act;
+        p.act_cache = (act->act == TLB_ACT_SILU_MUL && act->silu_gate != nullptr) ? 1 : 0;
+        p.gate = act->gate;
+        p.up = act->up;
+        p.silu = act->silu_gate;
+        p.dg = static_cast<uint2 *>(act->dgate);
+        p.du = static_cast<uint2 *>(act->dup);
+    }
     const int64_t KB = p.kb[0] + (nseg > 1 ? p.kb[1] : 0), tiles = ceil_div(N, pl.bn) * ceil_div(M, kBM);
     p.ctas = pl.ctas;
     p.dp = pl.dp;

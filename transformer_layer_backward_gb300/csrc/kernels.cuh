@@ -44,8 +44,15 @@ TcPlan tc_plan(int64_t M, int64_t N, int64_t K);
 bool tc_supported(int64_t M, int64_t N, int64_t K);
 size_t tc_partial_bytes(int64_t M, int64_t N, int64_t K);   // stream-K partial tiles for (M, N, K)
 int tc_convert_bf16(const float *x, void *y, int64_t n, cudaStream_t st);
+// Optional epilogue of tc_gemm: alpha * acc is dh, and the gated-activation backward
+// writes dG, dU in bf16 (the A operands of the [W_gate | W_up]^T product) instead of out.
+struct TcActEpilogue {
+    int act;                              // TLB_ACT_*
+    const float *gate, *up, *silu_gate;   // [M, N] fp32; silu_gate may be NULL (recomputed)
+    void *dgate, *dup;                    // [M, N] bf16
+};
 int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, float *out, bool accumulate,
-            float *partial, uint32_t *status, cudaStream_t st);
+            float *partial, uint32_t *status, cudaStream_t st, const TcActEpilogue *act = nullptr);
 // gated-activation backward writing bf16 dG, dU (rowwise.cu)
 int act_backward_bf16_launch(int act, const float *gate, const float *up, const float *silu_gate, const float *dh,
                              void *dgate, void *dup, int64_t n, cudaStream_t st);

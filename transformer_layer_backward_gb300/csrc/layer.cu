@@ -109,15 +109,23 @@ int ffn_impl(const tlb_layer_cfg &c, int64_t S, const float *d_out, const tlb_la
         uint32_t *status = ws_at<uint32_t>(ws, 0);
         float *part = ws_at<float>(ws, p.part);
         void *abf = ws_at<void>(ws, p.abf), *gbf = ws_at<void>(ws, p.gbf), *ubf = ws_at<void>(ws, p.ubf);
-        // dF = dOut W_down^T on the tensor cores (dOut rounded to bf16)
+        // dF = dOut W_down^T on the tensor cores (dOut rounded to bf16); dG, dU in bf16 are
+        // the A operands of [W_gate | W_up]^T
         TLB_TRY(tc_convert_bf16(d_out, abf, S * H, st));
         const TcOperand down{abf, w.w_down.w, H};
-        TLB_TRY(tc_gemm(&down, 1, S, I, w.w_down.scale, dF, false, part, status, st));
-        if (c.flags & TLB_SUB_NORM)
-            TLB_TRY(rmsnorm_backward_launch(a.hidden, w.gamma_sub_ffn, dF, dF, S, I, c.norm_eps, 0, st));
-        // dG, dU straight to bf16: the A operand of [W_gate | W_up]^T
         const float *sg = (c.act == TLB_ACT_SILU_MUL && (c.flags & TLB_USE_SILU_CACHE)) ? a.silu_gate : nullptr;
-        TLB_TRY(act_backward_bf16_launch(c.act, a.gate, a.up, sg, dF, gbf, ubf, S * I, st));
+        const bool fuse = !(c.flags & TLB_SUB_NORM) && aligned16(a.gate) && aligned16(a.up) &&
+                          (sg == nullptr || aligned16(sg));
+        if (!fuse) {
+            TLB_TRY(tc_gemm(&down, 1, S, I, w.w_down.scale, dF, false, part, status, st));
+            if (c.flags & TLB_SUB_NORM)
+                TLB_TRY(rmsnorm_backward_launch(a.hidden, w.gamma_sub_ffn, dF, dF, S, I, c.norm_eps, 0, st));
+            TLB_TRY(act_backward_bf16_launch(c.act, a.gate, a.up, sg, dF, gbf, ubf, S * I, st));
+        } else {
+            // the activation backward runs in the product's epilogue: dF never reaches memory
+            const TcActEpilogue ae{c.act, a.gate, a.up, sg, gbf, ubf};
+            TLB_TRY(tc_gemm(&down, 1, S, I, w.w_down.scale, nullptr, false, part, status, st, &ae));
+        }
         const TcOperand gu[2] = {{gbf, w.w_gate.w, I}, {ubf, w.w_up.w, I}};
         const bool resid = (c.flags & TLB_RESIDUAL) != 0;
         if (c.flags & TLB_PRE_NORM) {

@@ -285,19 +285,6 @@ int rmsnorm_backward_launch(const float *x, const float *gamma, const float *dy,
 
 // ------------------------------------------------------------------ gated activation backward
 
-template <int ACT, bool CACHE>
-__device__ __forceinline__ void act_bwd_elem(float g, float u, float s, float dh, float &dg, float &du) {
-    if constexpr (ACT == TLB_ACT_RELU2_MUL) {
-        const float r = fmaxf(g, 0.f);
-        dg = dh * u * 2.f * r;
-        du = dh * r * r;
-    } else {
-        const float sig = 1.f / (1.f + expf(-g));
-        const float y = g * sig;
-        dg = dh * u * (sig * (1.f + g - y));
-        du = dh * (CACHE ? s : y);
-    }
-}
 
 template <int ACT, bool CACHE>
 __global__ void act_bwd_kernel(const float4 *__restrict__ gate, const float4 *__restrict__ up,
@@ -357,12 +344,6 @@ int act_backward_launch(int act, const float *gate, const float *up, const float
     else
         launch_act<TLB_ACT_SILU_MUL, false>(gate, up, nullptr, dh, dgate, dup, n, vec, st);
     return check_launch("act_backward");
-}
-
-// bf16 outputs (the A operands of the [W_gate | W_up]^T tensor-core GEMM)
-__device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
-    return make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
 }
 
 template <int ACT, bool CACHE>
