@@ -75,7 +75,7 @@ __device__ __forceinline__ int xunit(int u) {
 }
 
 
-constexpr int kDecodeChunk = 64;   // keys per block in the attention pass
+constexpr int kDecodeChunk = 32;   // keys per block in the attention pass
 
 bool decode_supported(const tlb_layer_cfg &c, int64_t S, int64_t L);
 

@@ -58,7 +58,7 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     w.lora_q = p.take(lora_seq_bytes(S, int(qd), int(H), c.rank));
     w.lora_v = p.take(lora_seq_bytes(S, int(kvd), int(H), c.rank));
     if (S == 1) {
-        const int64_t nchunks = ceil_div(L, 32);   // the finer of the two attention chunkings
+        const int64_t nchunks = ceil_div(L, int64_t(std::min(32, kDecodeChunk)));   // the finer chunking
         w.dR1 = p.take(H * 4);
         w.Upart = p.take(nchunks * qd * 4);
         w.Wpart = p.take(nchunks * qd * 4);
