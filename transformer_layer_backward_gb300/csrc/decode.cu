@@ -143,6 +143,15 @@ __device__ __forceinline__ void rms_coef2(float2 s, int n, float eps, float &rin
 
 constexpr int kR = 2, kU = 2;   // rows per warp, chunks in flight per row and matrix
 
+// L2 prefetch of [p, p + bytes) when both are 16-byte multiples (else nothing).  The
+// kernels after k1 start early (programmatic dependent launch), prefetch the weights and
+// caches they will read -- which depend on nothing the chain computes -- and only then
+// wait for the previous kernel's results.
+__device__ __forceinline__ void prefetch_l2(const void *p, size_t bytes) {
+    if (bytes > 0 && bytes < (size_t(1) << 31) && ((reinterpret_cast<uintptr_t>(p) | bytes) & 15) == 0)
+        l2_prefetch(p, uint32_t(bytes));
+}
+
 // Block-wide (sum dy g x, sum x^2) over n elements (n % 4 == 0, 16-byte aligned arrays),
 // every thread issuing all its loads of a batch before using them.
 __device__ __forceinline__ float2 rms_sums_full(const float *x, const float *g, const float *dy, int n, float2 *red) {
@@ -179,6 +188,7 @@ __global__ void __launch_bounds__(kThreads) dec_k1(DecodeArgs a) {
     extern __shared__ float4 sm4[];
     __shared__ float2 red[32];
     float *sx = reinterpret_cast<float *>(sm4);
+    pdl_trigger();
     stage_vector<WT>(sx, a.d_hidden, a.H);
     if (blockIdx.x == 0 && threadIdx.x < 2 * a.rank) a.gh[threadIdx.x] = 0.f;
     // dN2 and dSub are sums of per-block column-range products in k2 and k3
@@ -204,6 +214,15 @@ __global__ void __launch_bounds__(kThreads) dec_k2(DecodeArgs a) {
     const int nc = a.I / a.ns2, c0 = blockIdx.y * nc;
     float *sG = reinterpret_cast<float *>(sm4);
     float *sU = sG + nc;
+    {
+        constexpr int ES = 16 / EPC<WT>::v;
+        const int lane = threadIdx.x & 31, r = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR + (lane % kR);
+        if (lane < 2 * kR && r < a.H)
+            prefetch_l2(reinterpret_cast<const char *>(lane < kR ? a.w_gate : a.w_up) +
+                            (size_t(r) * a.I + c0) * ES, size_t(nc) * ES);
+    }
+    pdl_trigger();
+    pdl_wait();
     float rinv = 1.f, c = 0.f;
     const bool sub = a.flags & TLB_SUB_NORM;
     if (sub) rms_coef2(sum_partials(a.part1, a.n1, red), a.I, a.eps, rinv, c);
@@ -284,6 +303,14 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
     // this block's column range [c0, c0 + nc) of dR1 and of the W_O rows
     const int nc = a.H / a.ns3, c0 = blockIdx.y * nc;
     float *sR = reinterpret_cast<float *>(sm4);
+    {
+        constexpr int ES = 16 / EPC<WT>::v;
+        const int lane = threadIdx.x & 31, r = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR + lane;
+        if (lane < kR && r < a.qd)
+            prefetch_l2(reinterpret_cast<const char *>(a.w_o) + (size_t(r) * a.H + c0) * ES, size_t(nc) * ES);
+    }
+    pdl_trigger();
+    pdl_wait();
     float rinv = 1.f, c = 0.f;
     const bool pre = a.flags & TLB_PRE_NORM;
     if (pre) rms_coef2(rms_sums_full(a.r1, a.g_ffn, a.dN2, a.H, red), a.H, a.eps, rinv, c);
@@ -334,6 +361,19 @@ __global__ void __launch_bounds__(kAThreads) dec_k4(DecodeArgs a) {
     const int hd = VPL * 32;
     float *sC = reinterpret_cast<float *>(sm4);        // [G][hd] dCtx
     float *sR = sC + G * hd;                           // [kAWarps][G][2][hd] reduction
+    {
+        const int j0 = chunk * kDecodeChunk, nj = min(kDecodeChunk, a.L - j0);
+        if (threadIdx.x < 2 * kDecodeChunk) {        // one K or V row per thread
+            const int j = threadIdx.x % kDecodeChunk;
+            const float *base = threadIdx.x < kDecodeChunk ? a.k : a.v;
+            if (j < nj) prefetch_l2(base + int64_t(kvh) * a.sh + int64_t(j0 + j) * a.sp, size_t(hd) * 4);
+        } else if (threadIdx.x < 2 * kDecodeChunk + G) {
+            const int g = threadIdx.x - 2 * kDecodeChunk;
+            prefetch_l2(a.attn + int64_t(kvh * G + g) * a.L + j0, size_t(nj) * 4);
+        }
+    }
+    pdl_trigger();
+    pdl_wait();
     float rinv = 1.f, c = 0.f;
     const bool sub = a.flags & TLB_SUB_NORM;
     if (sub) rms_coef2(rms_sums_full(a.ctx, a.g_sub_attn, a.dSub, a.qd, red2), a.qd, a.eps, rinv, c);
@@ -454,6 +494,9 @@ __global__ void __launch_bounds__(kThreads) dec_k6(DecodeArgs a, RopeFreqs fr) {
     __shared__ float red[16][kWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int h = blockIdx.x;
+    if (threadIdx.x == 0) prefetch_l2(a.lq.b + int64_t(h) * a.hd * a.rank, size_t(a.hd) * a.rank * 4);
+    pdl_trigger();
+    pdl_wait();
     // blockDim / hd thread groups each sum a slice of the chunks, then combine
     __shared__ float su[kThreads], sw[kThreads];
     const int groups = blockDim.x / a.hd;
@@ -537,6 +580,8 @@ __global__ void __launch_bounds__(kThreads) dec_k6(DecodeArgs a, RopeFreqs fr) {
 
 __global__ void __launch_bounds__(kThreads) dec_k7(DecodeArgs a) {
     __shared__ float red[32];
+    pdl_trigger();
+    pdl_wait();
     const int64_t nbq = int64_t(a.qd) * a.rank, nbv = int64_t(a.kvd) * a.rank, na = int64_t(a.rank) * a.H;
     const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     float g = 0.f;
@@ -598,7 +643,7 @@ cudaError_t launch_b(void (*kernel)(KArgs...), dim3 grid, int block, size_t smem
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;   // callers pass pdl = false: measured slower on this chain
+    cfg.numAttrs = pdl ? 1 : 0;   // k2..k7 start early and wait on the kernel before them
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
@@ -613,11 +658,11 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, size_t smem, cudaStream_
 
 template <int VPL>
 cudaError_t launch_k4_g(int G, dim3 g4, size_t sm4, cudaStream_t st, const DecodeArgs &a) {
-    if (G <= 1) return launch_b(dec_k4<VPL, 1>, g4, kAThreads, sm4, st, false, a);
-    if (G <= 2) return launch_b(dec_k4<VPL, 2>, g4, kAThreads, sm4, st, false, a);
-    if (G <= 4) return launch_b(dec_k4<VPL, 4>, g4, kAThreads, sm4, st, false, a);
-    if (G <= 8) return launch_b(dec_k4<VPL, 8>, g4, kAThreads, sm4, st, false, a);
-    if constexpr (VPL <= 4) return launch_b(dec_k4<VPL, 16>, g4, kAThreads, sm4, st, false, a);
+    if (G <= 1) return launch_b(dec_k4<VPL, 1>, g4, kAThreads, sm4, st, true, a);
+    if (G <= 2) return launch_b(dec_k4<VPL, 2>, g4, kAThreads, sm4, st, true, a);
+    if (G <= 4) return launch_b(dec_k4<VPL, 4>, g4, kAThreads, sm4, st, true, a);
+    if (G <= 8) return launch_b(dec_k4<VPL, 8>, g4, kAThreads, sm4, st, true, a);
+    if constexpr (VPL <= 4) return launch_b(dec_k4<VPL, 16>, g4, kAThreads, sm4, st, true, a);
     return cudaErrorInvalidValue;
 }
 
@@ -636,10 +681,10 @@ int launch_all(const DecodeArgs &a, cudaStream_t st) {
     TLB_TRY(check_launch("decode k1"));
     const size_t sm2 = size_t(2) * (a.I / a.ns2) * 4;
     const dim3 g2(unsigned(a.n2), unsigned(a.ns2));
-    if (a.act == TLB_ACT_RELU2_MUL) TLB_CUDA(launch(dec_k2<WT, TLB_ACT_RELU2_MUL>, g2, sm2, st, false, a));
-    else TLB_CUDA(launch(dec_k2<WT, TLB_ACT_SILU_MUL>, g2, sm2, st, false, a));
+    if (a.act == TLB_ACT_RELU2_MUL) TLB_CUDA(launch(dec_k2<WT, TLB_ACT_RELU2_MUL>, g2, sm2, st, true, a));
+    else TLB_CUDA(launch(dec_k2<WT, TLB_ACT_SILU_MUL>, g2, sm2, st, true, a));
     TLB_TRY(check_launch("decode k2"));
-    TLB_CUDA(launch(dec_k3<WT>, dim3(unsigned(a.n3), unsigned(a.ns3)), size_t(a.H / a.ns3) * 4, st, false, a));
+    TLB_CUDA(launch(dec_k3<WT>, dim3(unsigned(a.n3), unsigned(a.ns3)), size_t(a.H / a.ns3) * 4, st, true, a));
     TLB_TRY(check_launch("decode k3"));
     const int G = a.nh / a.nkv;
     const dim3 g4(a.nkv, a.nchunks);
@@ -648,10 +693,10 @@ int launch_all(const DecodeArgs &a, cudaStream_t st) {
     TLB_TRY(check_launch("decode k4"));
     RopeFreqs fr;
     rope_freqs(fr, a.hd, a.rope_base);
-    TLB_CUDA(launch(dec_k6, dim3(a.nh), 0, st, false, a, fr));
+    TLB_CUDA(launch(dec_k6, dim3(a.nh), 0, st, true, a, fr));
     TLB_TRY(check_launch("decode k6"));
     const int64_t n7 = int64_t(a.qd + a.kvd) * a.rank + 2 * int64_t(a.rank) * a.H;
-    TLB_CUDA(launch(dec_k7, dim3(unsigned(ceil_div(n7, kThreads))), 0, st, false, a));
+    TLB_CUDA(launch(dec_k7, dim3(unsigned(ceil_div(n7, kThreads))), 0, st, true, a));
     TLB_TRY(check_launch("decode k7"));
     return TLB_OK;
 }
