@@ -368,6 +368,13 @@ def seq_main(args, rank, world, local, dist):
     dom = max((k for k in range(nkern) if fl[k][0]), key=lambda k: ktime[k])
     achieved = fl[dom][0] / (ktime[dom] / 1e3) / 1e12
     peak = bf16_peak if fl[dom][1] == "bf16" else tf32_peak
+    # DRAM bytes of the dominant kernel from the committed ncu capture of the S = 2048 layer
+    # (per launch; the stack runs the same layer launches)
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "seq2048_dram_bytes.json")
+    if S == 2048 and os.path.exists(prof):
+        key = names[dom] if names[dom] != "tcgen05 gemm" else "tcgen05 gemm #%d" % (names[:dom + 1].count("tcgen05 gemm"))
+        traffic = json.load(open(prof)).get(key)
 
     # end to end through the public API: the step's activations and caches from pinned host
     # memory every step, d_in and the gradient sums read back
@@ -415,7 +422,7 @@ def seq_main(args, rank, world, local, dist):
                            "cuda_graph": graphs is not None},
                 "layer_tokens_per_s": value * depth,
                 "roofline": {"bound": "tensor", "kernel": names[dom], "achieved": achieved, "peak": peak,
-                             "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                             "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                              "algorithmic_flop": fl[dom][0],
                              "peak_source": ("MEASURED_PEAKS.json bf16_tflops_sustained (of measured)" if pk else
                                              "fallback") + ("" if fl[dom][1] == "bf16" else " x 1.1/2.25 for tf32")},
