@@ -9,7 +9,7 @@ working set (NL x 68 MB) is several times the 129 MB L2 and each step reads its
 inputs from HBM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tlb|reference]
-                  [--workload decode|seq512|seq2048|stack2048]
+                  [--workload decode|seq512|seq2048|stack2048|sweep]
 
 --impl reference times the float64 CPU oracle (the only other implementation of
 this path available here) on the same workload.  Under torchrun every rank runs
@@ -20,12 +20,17 @@ rank 16; the tcgen05 path): seq512 and seq2048 time one layer backward of S toke
 per step; stack2048 times the 36-layer stack (S = 2048) per step, d_in of each layer
 feeding the next.  Their inputs are drawn on the device with torch's seeded
 generator, with the shapes and distributions of the parity inputs.
+
+--workload sweep measures the standalone fp32 kernels (softmax, RMSNorm, RoPE, gated
+activations, AdamW) over their size ranges, one case after another, and reports
+per-case GB/s; the headline value is the lowest among the cases above 4 x L2.
 """
 from __future__ import annotations
 
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -51,7 +56,9 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=2000)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-graph", action="store_true")
-    p.add_argument("--workload", default="decode", choices=["decode", "seq512", "seq2048", "stack2048"])
+    p.add_argument("--cases", default=None,
+                   help="sweep: run only the cases whose 'kernel shape' label matches this regex")
+    p.add_argument("--workload", default="decode", choices=["decode", "seq512", "seq2048", "stack2048", "sweep"])
     return p.parse_args()
 
 
@@ -147,6 +154,26 @@ def host_threads():
 
 def run_reference(args, rank, world):
     if rank != 0:
+        return
+    if args.workload == "sweep":
+        per = max(args.cpu_seconds / 8, 0.5)
+        big = {}
+        for kind, shape, bpe in sweep_cases():       # the largest case of each kernel
+            big[kind] = (shape, bpe)
+        res = {k: sweep_oracle_gbs(k, shp, bpe, per) for k, (shp, bpe) in big.items()}
+        worst = min(res, key=lambda k: res[k][0])
+        v = res[worst][0]
+        line = {"impl": "reference", "metric": SWEEP_METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+                "steps": len(res), "warmup": 0, "ms_per_step": per * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": "standalone kernel sweep sample: the float64 oracle on up to 2^22 "
+                                       "elements of the largest case of each kernel",
+                           "parallelism": "replicas"},
+                "sweep": [{"kernel": k, "GB/s": r[0], "sample": r[1]} for k, r in res.items()],
+                "cpu_baseline": {"value": v, "unit": "GB/s", "cores": host_threads(), "kind": "oracle",
+                                 "sample": "%s: %s" % (worst, res[worst][1])},
+                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
         return
     if args.workload != "decode":
         per = max(args.cpu_seconds / max(args.steps, 1), 0.0)
@@ -447,6 +474,220 @@ def seq_cpu_baseline(seconds):
             "sample": "%d float64 oracle backwards of one S = 512 layer" % n}
 
 
+# ---------------------------------------------------------------- bandwidth sweep
+
+SWEEP_METRIC = "standalone-kernel HBM bandwidth (lowest over the kernels)"
+
+
+def sweep_cases():
+    """The standalone fp32 kernels over the stated size ranges: (kernel, shape, bytes per
+    element that must cross HBM once).  Softmax rows [32, len] as stated plus [rows, len]
+    with rows * len = 2^27 (1.6 GB, far above L2); RMSNorm rows of 2560; RoPE [rows, 32,
+    128]; gated activations 2^16 .. 2^28 elements; AdamW 2^12 .. 2^26 parameters."""
+    c = []
+    for n in (128, 512, 2048, 8192, 32768):
+        c.append(("softmax_backward", (32, n), 12))
+        c.append(("softmax_backward", (2 ** 27 // n, n), 12))
+    for rows in (1, 16, 256, 4096, 65536):
+        c.append(("rmsnorm_backward", (rows, 2560), 12))
+    c.append(("rmsnorm_backward +=", (65536, 2560), 16))
+    for rows in (1, 16, 256, 4096, 65536):
+        c.append(("rope_backward", (rows, 32, 128), 8))
+    for e in (16, 20, 24, 28):
+        c.append(("act_backward relu2_mul", (2 ** e,), 20))
+        c.append(("act_backward silu_mul cached", (2 ** e,), 24))
+    c.append(("act_backward silu_mul", (2 ** 24,), 20))
+    c.append(("act_backward silu_mul", (2 ** 28,), 20))
+    for e in (12, 16, 20, 24, 26):
+        c.append(("adamw", (2 ** e,), 28))
+    return c
+
+
+def sweep_setup(tlb, kind, shape, g):
+    """Device inputs of one case (N(0, 1); softmax rows normalised; gammas U(0.5, 1.5))
+    and the call that runs it through the binding."""
+    import torch
+    n = lambda: torch.randn(*shape, device="cuda", generator=g)
+    if kind == "softmax_backward":
+        a, d = torch.softmax(n(), dim=-1), n()
+        o = torch.empty_like(a)
+        return (lambda: tlb.softmax_backward(a, d, out=o)), {"attn": a, "dattn": d}, o
+    if kind.startswith("rmsnorm_backward"):
+        x, dy, o = n(), n(), n()
+        gam = torch.rand(shape[-1], device="cuda", generator=g) + 0.5
+        acc = kind.endswith("+=")
+        return (lambda: tlb.rmsnorm_backward(x, gam, dy, out=o, accumulate=acc)), {"x": x, "dy": dy}, o
+    if kind == "rope_backward":
+        dy = n()
+        o = torch.empty_like(dy)
+        return (lambda: tlb.rope_backward(dy, 0, out=o)), {"dy": dy}, o
+    if kind.startswith("act_backward"):
+        gate, up, dh = n(), n(), n()
+        dg, du = torch.empty_like(gate), torch.empty_like(gate)
+        act = "relu2_mul" if "relu2" in kind else "silu_mul"
+        sg = torch.nn.functional.silu(gate) if kind.endswith("cached") else None
+        ins = {"gate": gate, "up": up, "dh": dh}
+        if sg is not None:
+            ins["silu_gate"] = sg
+        return (lambda: tlb.act_backward(act, gate, up, dh, silu_gate=sg, dgate=dg, dup=du)), ins, dg
+    if kind == "adamw":
+        p, gr = n(), n()
+        m, v = torch.zeros_like(p), torch.zeros_like(p)
+        cfg = tlb.adamw_cfg(1e-4)
+        return (lambda: tlb.adamw(p, gr, m, v, cfg)), {"g": gr}, p
+    raise ValueError(kind)
+
+
+def sweep_oracle_gbs(kind, shape, bpe, seconds):
+    """Algorithmic GB/s of the float64 oracle on a sample of one case (at most 2^22
+    elements of it), on the host cores."""
+    from oracle import ops
+    rng = np.random.default_rng(0)
+    size = int(np.prod(shape))
+    if len(shape) > 1:
+        rows = max(1, min(shape[0], (2 ** 22) // (size // shape[0])))
+        shp = (rows,) + tuple(shape[1:])
+    else:
+        shp = (min(size, 2 ** 22),)
+    a = rng.standard_normal(shp)
+    b = rng.standard_normal(shp)
+    c = rng.standard_normal(shp)
+    if kind == "softmax_backward":
+        e = np.exp(a - a.max(axis=-1, keepdims=True))
+        p = e / e.sum(axis=-1, keepdims=True)
+        fn = lambda: ops.softmax_backward(p, b)
+    elif kind.startswith("rmsnorm_backward"):
+        gam = rng.uniform(0.5, 1.5, shp[-1])
+        fn = lambda: ops.rmsnorm_backward(a, gam, b, 1e-6)
+    elif kind == "rope_backward":
+        pos = np.arange(shp[0])
+        fn = lambda: ops.rope_backward(a, pos, 10000.0)
+    elif kind.startswith("act_backward"):
+        fn = (lambda: ops.relu2_mul_backward(a, b, c)) if "relu2" in kind else (lambda: ops.silu_mul_backward(a, b, c))
+    else:
+        z = np.zeros(shp)
+        fn = lambda: ops.adamw(a.copy(), b, z.copy(), z.copy(), 1e-4, 0.9, 0.999, 1e-8, 0.01, 1)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n >= 1000:
+            break
+    return n * int(np.prod(shp)) * bpe / el / 1e9, "%d oracle calls on %s" % (n, "x".join(map(str, shp)))
+
+
+def sweep_main(args, rank, world, local, dist):
+    """Each case: W untimed launches, then K launches each timed alone with CUDA events on
+    the launching stream (median); L2 is flushed (a 2 x L2 buffer cleared) before every
+    timed launch whose working set is under 4 x L2.  Those small cases are reported but
+    not counted in the lowest-bandwidth figure."""
+    import torch
+    import transformer_layer_backward_gb300 as tlb
+    torch.cuda.set_device(local)
+    tlb.load()
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
+    flush = torch.empty(2 * l2 // 4, device="cuda")
+    pk = peaks()
+    hbm = pk["hbm_gbs"] if pk else 6800.0
+    K, W = max(1, min(args.steps, 20)), max(3, min(args.warmup, 5))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234 + rank)
+    stream = torch.cuda.current_stream()
+    rows, launches = [], 0
+    if dist is not None:
+        dist.barrier()
+    clocks = Clocks(local)
+    t_start = time.perf_counter()
+    cases = [c for c in sweep_cases()
+             if args.cases is None or re.search(args.cases, "%s %s" % (c[0], "x".join(map(str, c[1]))))]
+    for kind, shape, bpe in cases:
+        fn, ins, out = sweep_setup(tlb, kind, shape, g)
+        elems = int(np.prod(shape))
+        nbytes = elems * bpe
+        small = nbytes < 4 * l2
+        for _ in range(W):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        c0 = tlb.launch_count()
+        for e0, e1 in ev:
+            if small:
+                flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        launches += tlb.launch_count() - c0
+        us = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
+        gbs = nbytes / (us * 1e-6) / 1e9
+        rows.append({"kernel": kind, "shape": list(shape), "bytes": nbytes, "us": us, "GB/s": gbs,
+                     "frac": gbs / hbm, "set": "small (< 4 x L2, flushed)" if small else "hbm"})
+        print("%-30s %-18s %10.1f MB %9.2f us %8.0f GB/s %5.1f %%%s" % (
+            kind, "x".join(map(str, shape)), nbytes / 1e6, us, gbs, 100 * gbs / hbm,
+            "  (small)" if small else ""), file=sys.stderr, flush=True)
+        del fn, ins, out
+        torch.cuda.empty_cache()
+    wall = time.perf_counter() - t_start
+    clk = clocks.stop()
+    if dist is not None:
+        dist.barrier()
+    big = [r for r in rows if r["set"] == "hbm"] or rows
+    worst = min(big, key=lambda r: r["GB/s"])
+    value = worst["GB/s"]
+
+    # end to end through the binding for the lowest case: its inputs from pinned host
+    # memory, the call, its output read back
+    fn, ins, out = sweep_setup(tlb, worst["kernel"], tuple(worst["shape"]), g)
+    pinned = {k: v.cpu().pin_memory() for k, v in ins.items()}
+    out_h = torch.empty(out.shape, pin_memory=True)
+    h2d = sum(v.numel() * 4 for v in pinned.values())
+    d2h = out_h.numel() * 4
+    torch.cuda.synchronize()
+    n_e2e = 3
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        for k, v in pinned.items():
+            ins[k].copy_(v, non_blocking=True)
+        fn()
+        out_h.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    e2e = {"value": worst["bytes"] / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "case": worst["kernel"]}
+    del fn, ins, out
+
+    # DRAM bytes per algorithmic byte of the kernel from the committed ncu capture (one
+    # case of 0.3 - 2 GB per kernel; a streaming kernel's traffic grows in proportion to
+    # its elements), times this case's algorithmic bytes
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "sweep_dram_bytes.json")
+    if os.path.exists(prof):
+        caps = json.load(open(prof))
+        r = caps.get("%s %s" % (worst["kernel"], "x".join(map(str, worst["shape"]))))
+        r = r or next((v for v in caps.values() if v["kernel"] == worst["kernel"]), None)
+        traffic = None if r is None else r["traffic_per_algorithmic_byte"] * worst["bytes"]
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        v, sample = sweep_oracle_gbs(worst["kernel"], tuple(worst["shape"]), worst["bytes"] // int(np.prod(worst["shape"])),
+                                     min(args.cpu_seconds, 10.0))
+        cpu = {"value": v, "unit": "GB/s", "cores": host_threads(), "kind": "oracle", "sample": sample}
+    if rank == 0:
+        line = {"metric": SWEEP_METRIC, "value": value * world, "unit": "GB/s", "n_gpus": world, "steps": K,
+                "warmup": W, "ms_per_step": wall * 1e3 / len(rows), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (device generator)",
+                "config": {"workload": "standalone fp32 kernel sweep: softmax, RMSNorm, RoPE, gated "
+                                       "activations, AdamW over the stated sizes",
+                           "cases": len(rows), "l2": "flushed before each timed launch below 4 x L2",
+                           "timing": "median of K launches, each timed alone"},
+                "roofline": {"bound": "hbm", "kernel": "%s %s" % (worst["kernel"], "x".join(map(str, worst["shape"]))),
+                             "achieved": value, "peak": hbm, "unit": "GB/s", "frac": value / hbm,
+                             "traffic": traffic, "algorithmic_bytes": worst["bytes"],
+                             "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else "fallback"},
+                "sweep": rows, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -464,6 +705,11 @@ def main():
             dist.destroy_process_group()
         return
 
+    if args.workload == "sweep":
+        sweep_main(args, rank, world, local, dist)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     if args.workload != "decode":
         seq_main(args, rank, world, local, dist)
         if dist is not None:

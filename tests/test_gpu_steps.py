@@ -81,7 +81,8 @@ def test_rmsnorm_backward(lib, rows, n, accumulate):
 
 
 @pytest.mark.parametrize("rows,nh,hd,pos0", [(1, 20, 128, 1023), (33, 3, 16, 0), (65, 4, 6, 2000),
-                                             (7, 32, 128, 2041), (0, 2, 8, 0)])
+                                             (7, 32, 128, 2041), (0, 2, 8, 0), (100, 5, 8, 60000),
+                                             (20000, 2, 128, 5), (9, 7, 64, 300), (3000, 24, 128, 7)])
 def test_rope_backward(lib, rows, nh, hd, pos0):
     dy = normal("dq", (rows, nh, hd))
     ref = ops.rope_backward(dy, pos0 + np.arange(rows), 10000.0)

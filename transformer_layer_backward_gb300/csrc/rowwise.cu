@@ -407,13 +407,79 @@ __global__ void rope_bwd_kernel(const float *dy, float *dx, int64_t rows, int n_
     }
 }
 
+// The angle depends on the position and the frequency index only, so one thread per
+// (row, group of hpt heads, four frequencies) computes its four cos/sin pairs once and
+// rotates those pairs in each head of its group, with 128-bit loads and stores (HU
+// heads in flight).  hpt is all the heads unless rows are too few to fill the GPU.
+// Needs head_dim/2 a multiple of 4 and 16-byte aligned buffers; dx may alias dy.
+template <int HU>
+__global__ void __launch_bounds__(256)
+rope_bwd_vec_kernel(const float4 *dy, float4 *dx, int64_t rows, int n_heads, int hpt, int half4,
+                    int64_t pos0, RopeFreqs fr) {
+    const int groups = (n_heads + hpt - 1) / hpt;
+    const int64_t total = rows * groups * half4;
+    const int64_t hd4 = 2 * int64_t(half4);
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t rg = i / half4;
+        const int q = int(i - rg * half4);
+        const int64_t row = rg / groups;
+        const int h0 = int(rg - row * groups) * hpt;
+        const int h1 = min(h0 + hpt, n_heads);
+        const float pos = float(pos0 + row);
+        float c[4], s[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) rope_cos_sin(pos, fr.hi[4 * q + k], fr.lo[4 * q + k], c[k], s[k]);
+        const int64_t base = row * n_heads * hd4 + q;
+        for (int h = h0; h < h1; h += HU) {
+            float4 a[HU], b[HU];
+#pragma unroll
+            for (int u = 0; u < HU; ++u) {
+                if (h + u < h1) {
+                    a[u] = __ldcs(dy + base + (h + u) * hd4);
+                    b[u] = __ldcs(dy + base + (h + u) * hd4 + half4);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < HU; ++u) {
+                if (h + u < h1) {
+                    float4 o1, o2;
+                    o1.x = a[u].x * c[0] + b[u].x * s[0];
+                    o2.x = -a[u].x * s[0] + b[u].x * c[0];
+                    o1.y = a[u].y * c[1] + b[u].y * s[1];
+                    o2.y = -a[u].y * s[1] + b[u].y * c[1];
+                    o1.z = a[u].z * c[2] + b[u].z * s[2];
+                    o2.z = -a[u].z * s[2] + b[u].z * c[2];
+                    o1.w = a[u].w * c[3] + b[u].w * s[3];
+                    o2.w = -a[u].w * s[3] + b[u].w * c[3];
+                    __stcs(dx + base + (h + u) * hd4, o1);
+                    __stcs(dx + base + (h + u) * hd4 + half4, o2);
+                }
+            }
+        }
+    }
+}
+
 int rope_backward_launch(const float *dy, float *dx, int64_t rows, int n_heads, int head_dim,
                          int64_t pos0, float base, cudaStream_t st) {
     if (rows == 0 || n_heads == 0) return TLB_OK;
     RopeFreqs fr;
     rope_freqs(fr, head_dim, base);
-    const int64_t total = rows * n_heads * (head_dim / 2);
-    rope_bwd_kernel<<<stream_grid(total, 256), 256, 0, st>>>(dy, dx, rows, n_heads, head_dim, pos0, fr);
+    const int half = head_dim / 2;
+    if (half % 4 == 0 && aligned16(dy) && aligned16(dx)) {
+        // heads per thread: all of them once the (row, frequency) items alone fill
+        // about 1024 threads per SM, fewer (down to one) below that
+        const int64_t items = rows * (half / 4), fill = int64_t(num_sms()) * 1024;
+        const int64_t want = items * n_heads / fill;
+        const int hpt = int(want < 1 ? 1 : (want > n_heads ? n_heads : want));
+        const int64_t total = items * ((n_heads + hpt - 1) / hpt);
+        rope_bwd_vec_kernel<4><<<stream_grid(total, 256), 256, 0, st>>>(
+            reinterpret_cast<const float4 *>(dy), reinterpret_cast<float4 *>(dx), rows, n_heads, hpt,
+            half / 4, pos0, fr);
+    } else {
+        const int64_t total = rows * n_heads * half;
+        rope_bwd_kernel<<<stream_grid(total, 256), 256, 0, st>>>(dy, dx, rows, n_heads, head_dim, pos0, fr);
+    }
     return check_launch("rope_backward");
 }
 
