@@ -277,6 +277,29 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L,
                        const tlb_adamw_cfg *adam, float *d_hidden, double *sumsq,
                        void *ws, size_t ws_bytes, void *stream);
 
+/* [RS] backward_through_layers: a stack of n_layers layers of one configuration, run
+ * from the top (layer n_layers - 1) down to layer 0.  Layer l's d_in becomes layer
+ * l - 1's dOut, its adapters take their AdamW step, and sumsq accumulates over all of
+ * them: the result is that of tlb_layer_backward called for l = n_layers - 1 .. 0 in
+ * turn on the same d_hidden, up to the order of float atomic additions.
+ *   w, acts, lora_q, lora_v: host arrays of n_layers structs, entry l for layer l.
+ *   d_hidden [S, dim] in/out: the top layer's dOut on entry, layer 0's d_in on return.
+ *   ws: tlb_stack_workspace_bytes(cfg, S, L) bytes, 256-byte aligned, zero-filled once.
+ * Single-token layers (S = 1 on the single-token path) overlap: layer l's attention,
+ * LoRA and AdamW kernels run on a second, lower-priority stream of the library beside
+ * layer l - 1's FFN and O-projection kernels, and `stream` joins that stream before the
+ * call's work ends.  The second stream and its events are created on the first such call
+ * on each device, which must therefore not be made inside a stream capture; later calls
+ * may be captured.  Calls that share that device's second stream are serialised on the
+ * host.  Other layers run one after another on `stream`.  Errors as tlb_layer_backward;
+ * n_layers = 0 or S = 0 is a no-op. */
+size_t tlb_stack_workspace_bytes(const tlb_layer_cfg *cfg, int64_t S, int64_t L);
+int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n_layers,
+                       const tlb_layer_weights *w, const tlb_layer_acts *acts,
+                       const tlb_lora *lora_q, const tlb_lora *lora_v,
+                       const tlb_adamw_cfg *adam, float *d_hidden, double *sumsq,
+                       void *ws, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

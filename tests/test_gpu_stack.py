@@ -1,0 +1,109 @@
+"""The stack entry point ([RS] backward_through_layers): layers n-1 .. 0, d_in of layer l
+feeding layer l - 1.  Single-token layers overlap one layer's attention and LoRA kernels
+with the next layer's GEMV chain on a second stream; the results must not depend on
+that, so the stack is checked against the oracle's stack and against the same layers
+called one at a time."""
+import numpy as np
+import pytest
+
+from oracle import layer as OL
+from synth import DECODE, TINY, layer_inputs
+from tests.helpers import adam_to_abi, cfg_to_abi, check, host, lora_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+ADAPTER_KEYS = ("a_q", "b_q", "a_v", "b_v", "m_a_q", "v_a_q", "m_b_q", "v_b_q",
+                "m_a_v", "v_a_v", "m_b_v", "v_b_v")
+
+
+def device_stack(lib, cfg, layers):
+    devs = []
+    for l, d in enumerate(layers):
+        t = to_dev(d, cfg.wtype)
+        L = lora_dev(t)
+        c = cfg_to_abi(lib, cfg)
+        devs.append(dict(t=t, L=L, w=lib.layer_weights(c, t), a=lib.layer_acts(c, t, cfg.kv_layout, cfg.cache_len),
+                         lq=lib.lora(L, "q"), lv=lib.lora(L, "v")))
+    return devs
+
+
+@pytest.mark.parametrize("n_layers", [1, 2, 4])
+def test_decode_stack_against_oracle(lib, n_layers):
+    import torch
+    cfg = DECODE.with_(name="decode_stack", n_layers=n_layers)
+    layers = [layer_inputs(cfg, layer=l, seed=0, with_dout=(l == n_layers - 1)) for l in range(n_layers)]
+    dout = layers[-1]["dout"]
+    ref = OL.stack_backward(cfg, layers, dout)
+    c = cfg_to_abi(lib, cfg)
+    adam = adam_to_abi(lib, cfg)
+    devs = device_stack(lib, cfg, layers)
+    ws = lib.stack_workspace(c, 1, cfg.cache_len)
+    dh = torch.from_numpy(dout).cuda()
+    ss = torch.zeros(2, dtype=torch.float64, device="cuda")
+    lib.stack_backward(c, 1, cfg.cache_len, [d["w"] for d in devs], [d["a"] for d in devs],
+                       [d["lq"] for d in devs], [d["lv"] for d in devs], adam, dh, ss, ws)
+    lib.workspace_status(ws)
+    check("stack d_in", host(dh), ref["d_in"])
+    gnorm = float(np.sqrt(ss[0].item()))
+    assert abs(gnorm - ref["gnorm"]) <= 1e-5 * ref["gnorm"]
+
+
+@pytest.mark.parametrize("n_layers", [2, 5])
+def test_decode_stack_matches_layer_calls(lib, n_layers):
+    """Same layers, same inputs: the overlapped stack and n_layers separate calls."""
+    import torch
+    cfg = DECODE.with_(name="decode_stack", n_layers=n_layers)
+    layers = [layer_inputs(cfg, layer=l, seed=3, with_dout=(l == n_layers - 1)) for l in range(n_layers)]
+    # the gradient grows ~5e3 times per synthetic ternary layer; a small dOut keeps dA^2 of
+    # the lowest of five layers within float range (everything before AdamW is linear in it)
+    dout = (layers[-1]["dout"] * 1e-8).astype(np.float32)
+    c = cfg_to_abi(lib, cfg)
+    adam = adam_to_abi(lib, cfg)
+    a, b = device_stack(lib, cfg, layers), device_stack(lib, cfg, layers)
+    ws_s = lib.stack_workspace(c, 1, cfg.cache_len)
+    ws_l = lib.workspace(c, 1, cfg.cache_len)
+    dh_s = torch.from_numpy(dout).cuda()
+    dh_l = dh_s.clone()
+    ss_s = torch.zeros(2, dtype=torch.float64, device="cuda")
+    ss_l = torch.zeros(2, dtype=torch.float64, device="cuda")
+    dout_dev = torch.from_numpy(dout).cuda()
+    for rep in range(2):      # a second pass starts from the updated adapters and moments
+        dh_s.copy_(dout_dev)
+        dh_l.copy_(dout_dev)
+        lib.stack_backward(c, 1, cfg.cache_len, [d["w"] for d in a], [d["a"] for d in a],
+                           [d["lq"] for d in a], [d["lv"] for d in a], adam, dh_s, ss_s, ws_s)
+        for l in reversed(range(n_layers)):
+            lib.layer_backward(c, 1, cfg.cache_len, b[l]["w"], b[l]["a"], b[l]["lq"], b[l]["lv"], adam, dh_l, ss_l,
+                               ws_l)
+    lib.workspace_status(ws_s)
+    # d_in runs through no atomic sum whose order could change: bit for bit
+    np.testing.assert_array_equal(host(dh_s), host(dh_l))
+    # the adapter gradients sum the heads' shares with float atomics, in either order
+    for l in range(n_layers):
+        for k in ADAPTER_KEYS:
+            check("layer %d %s" % (l, k), host(a[l]["L"][k]), host(b[l]["L"][k]), rel_l2=1e-6, max_abs=None)
+    # sum dA^2 inherits those ~1e-7 differences of dA
+    np.testing.assert_allclose(ss_s.cpu().numpy(), ss_l.cpu().numpy(), rtol=1e-6)
+
+
+def test_sequence_stack_runs_layers_in_turn(lib):
+    """Layers with S > 1 take the plain loop on the caller's stream."""
+    import torch
+    cfg = TINY.with_(name="tiny_stack", n_layers=3)
+    layers = [layer_inputs(cfg, layer=l, seed=0, with_dout=(l == cfg.n_layers - 1)) for l in range(3)]
+    dout = layers[-1]["dout"]
+    ref = OL.stack_backward(cfg, layers, dout)
+    c = cfg_to_abi(lib, cfg)
+    adam = adam_to_abi(lib, cfg)
+    devs = device_stack(lib, cfg, layers)
+    ws = lib.stack_workspace(c, cfg.seq_len, cfg.cache_len)
+    dh = torch.from_numpy(dout).cuda()
+    ss = torch.zeros(2, dtype=torch.float64, device="cuda")
+    lib.stack_backward(c, cfg.seq_len, cfg.cache_len, [d["w"] for d in devs], [d["a"] for d in devs],
+                       [d["lq"] for d in devs], [d["lv"] for d in devs], adam, dh, ss, ws)
+    check("stack d_in", host(dh), ref["d_in"])
+    gnorm = float(np.sqrt(ss[0].item()))
+    assert abs(gnorm - ref["gnorm"]) <= 1e-5 * ref["gnorm"]
+    for l in range(3):
+        for p in ("a_q", "b_q", "a_v", "b_v"):
+            check("layer %d %s" % (l, p), host(devs[l]["L"][p]), ref["layers"][l][p])

@@ -57,6 +57,49 @@ def test_host_side_argument_errors(lib):
                          1.0, None, None) == A.TLB_EINVAL                               # step 0
 
 
+def test_struct_layouts_match_the_header(tmp_path):
+    """The binding passes these structs by pointer and, to tlb_stack_backward, as arrays:
+    their sizes and field offsets must be the C compiler's."""
+    import shutil
+    import subprocess
+    from transformer_layer_backward_gb300 import _abi as A
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    pairs = [("tlb_layer_cfg", A.LayerCfg), ("tlb_weight", A.Weight), ("tlb_layer_weights", A.LayerWeights),
+             ("tlb_layer_acts", A.LayerActs), ("tlb_lora", A.Lora), ("tlb_adamw_cfg", A.AdamwCfg)]
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "tlb.h"', "int main(void) {"]
+    for cname, py in pairs:
+        lines.append('printf("%%s %%zu\\n", "%s", sizeof(%s));' % (cname, cname))
+        for f in py._fields_:
+            lines.append('printf("%%s.%%s %%zu\\n", "%s", "%s", offsetof(%s, %s));' % (cname, f[0], cname, f[0]))
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(l.rsplit(" ", 1) for l in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                          text=True).stdout.split("\n") if l)
+    for cname, py in pairs:
+        assert int(got[cname]) == C.sizeof(py), cname
+        for f in py._fields_:
+            assert int(got["%s.%s" % (cname, f[0])]) == getattr(py, f[0]).offset, (cname, f[0])
+
+
+def test_stack_host_side_errors(lib):
+    from transformer_layer_backward_gb300 import _abi as A
+    cfg = A.LayerCfg(64, 256, 4, 2, 16, 4, 8.0, 1e4, 1e-6, 0.25, 0, 0, 0)
+    adam = A.AdamwCfg(1e-4, 0.9, 0.999, 1e-8, 0.0, 16.0, 1)
+    assert lib.tlb_stack_workspace_bytes(C.byref(cfg), 1, 8) >= 2 * lib.tlb_workspace_bytes(C.byref(cfg), 1, 8)
+    assert lib.tlb_stack_backward(C.byref(cfg), 1, 8, -1, None, None, None, None, C.byref(adam), None, None,
+                                  None, 0, None) == A.TLB_EINVAL
+    assert lib.tlb_stack_backward(C.byref(cfg), 1, 8, 0, None, None, None, None, C.byref(adam), None, None,
+                                  None, 0, None) == A.TLB_OK                          # no layers: no-op
+    assert lib.tlb_stack_backward(C.byref(cfg), 1, 8, 2, None, None, None, None, C.byref(adam), None, None,
+                                  None, 0, None) == A.TLB_EINVAL
+    assert b"NULL layer array" in lib.tlb_last_error()
+
+
 def test_workspace_grows_with_rows(lib):
     from transformer_layer_backward_gb300 import _abi as A
     cfg = A.LayerCfg(2560, 9728, 32, 8, 128, 16, 32.0, 1e4, 1e-6, 128 ** -0.5, 1, 1, 4 | 8 | 32)

@@ -77,6 +77,9 @@ SIGNATURES = {
                                               P(AdamwCfg), vp, vp]),
     "tlb_layer_backward": (C.c_int, [P(LayerCfg), i64, i64, P(LayerWeights), P(LayerActs),
                                      P(Lora), P(Lora), P(AdamwCfg), vp, vp, vp, sz, vp]),
+    "tlb_stack_workspace_bytes": (sz, [P(LayerCfg), i64, i64]),
+    "tlb_stack_backward": (C.c_int, [P(LayerCfg), i64, i64, i32, P(LayerWeights), P(LayerActs),
+                                     P(Lora), P(Lora), P(AdamwCfg), vp, vp, vp, sz, vp]),
 }
 
 _lib = None

@@ -224,3 +224,24 @@ def layer_backward(cfg, S, L, weights, acts, lora_q, lora_v, adam, d_hidden, sum
            C.byref(lora_q), C.byref(lora_v), C.byref(adam), _ptr(d_hidden, name="d_hidden"),
            _ptr(sumsq, torch.float64, "sumsq"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
            _stream(stream))
+
+
+def stack_workspace(cfg: A.LayerCfg, S: int, L: int, device="cuda"):
+    """A zeroed workspace tensor for stack_backward."""
+    n = int(A.load().tlb_stack_workspace_bytes(C.byref(cfg), int(S), int(L)))
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def stack_backward(cfg, S, L, weights, acts, lora_q, lora_v, adam, d_hidden, sumsq, ws, stream=None):
+    """Layers len(weights) - 1 .. 0 of a stack (entry l of each list is layer l); d_hidden
+    holds the top layer's dOut on entry and layer 0's d_in on return."""
+    n = len(weights)
+    if not (len(acts) == len(lora_q) == len(lora_v) == n):
+        raise ValueError("stack_backward: the four layer lists differ in length")
+    W = (A.LayerWeights * max(n, 1))(*weights)
+    X = (A.LayerActs * max(n, 1))(*acts)
+    Q = (A.Lora * max(n, 1))(*lora_q)
+    V = (A.Lora * max(n, 1))(*lora_v)
+    A.call("tlb_stack_backward", C.byref(cfg), int(S), int(L), n, W, X, Q, V, C.byref(adam),
+           _ptr(d_hidden, name="d_hidden"), _ptr(sumsq, torch.float64, "sumsq"), _ptr(ws, torch.uint8, "ws"),
+           ws.numel(), _stream(stream))

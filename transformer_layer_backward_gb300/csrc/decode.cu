@@ -21,6 +21,9 @@
 // 16-byte reads of the 32 lanes (each lane owning one 16-byte chunk of a weight row)
 // fall in distinct banks.  The two sums an RMSNorm backward needs over a vector a
 // GEMV produces are accumulated per block by that GEMV and summed by the consumer.
+#include <mutex>
+#include <unordered_set>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "decode.cuh"
@@ -33,6 +36,8 @@ constexpr int kWarps = 8;                // GEMV / LoRA kernels
 constexpr int kThreads = kWarps * 32;
 constexpr int kAWarps = 8;               // attention kernel (holds per-head accumulators)
 constexpr int kAThreads = kAWarps * 32;
+constexpr int kQWarps = 32;              // k6: thread groups over the chunk partials of one head
+constexpr int kQThreads = kQWarps * 32;
 
 // Rows [r0, r0 + R) of NM matrices (same shape [rows, cols]), each dotted with its own
 // shared-memory vector (swizzled by xunit), scaled and summed:
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(kThreads) dec_k1(DecodeArgs a) {
     __shared__ float2 red[32];
     float *sx = reinterpret_cast<float *>(sm4);
     pdl_trigger();
-    stage_vector<WT>(sx, a.d_hidden, a.H);
+    stage_vector<WT>(sx, a.dout, a.H);
     if (blockIdx.x == 0 && threadIdx.x < 2 * a.rank) a.gh[threadIdx.x] = 0.f;
     // dN2 and dSub are sums of per-block column-range products in k2 and k3
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.H + a.qd; i += gridDim.x * blockDim.x)
@@ -319,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
         const int n4 = nc >> 2;
         const float4 *dn4 = reinterpret_cast<const float4 *>(a.dN2 + c0), *r14 = reinterpret_cast<const float4 *>(a.r1 + c0);
         const float4 *gf4 = reinterpret_cast<const float4 *>(a.g_ffn + c0),
-                     *do4 = reinterpret_cast<const float4 *>(a.d_hidden + c0);
+                     *do4 = reinterpret_cast<const float4 *>(a.dout + c0);
         for (int i = threadIdx.x; i < n4; i += blockDim.x) {
             const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
             const float4 dn = dn4[i], r = pre ? r14[i] : z, gm = pre ? gf4[i] : z, dO = resid ? do4[i] : z;
@@ -383,8 +388,8 @@ __global__ void __launch_bounds__(kAThreads) dec_k4(DecodeArgs a) {
         const float ds = a.dSub[q];
         sC[i] = sub ? rinv * (ds * a.g_sub_attn[q] - a.ctx[q] * c) : ds;
     }
-    if (kvh == 0 && chunk == 0)
-        for (int i = threadIdx.x; i < a.H; i += blockDim.x) a.d_hidden[i] = a.dR1[i];
+    if (kvh == 0 && chunk == 0 && a.dhid_out != nullptr)
+        for (int i = threadIdx.x; i < a.H; i += blockDim.x) a.dhid_out[i] = a.dR1[i];
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int d0 = lane * VPL;
@@ -397,34 +402,39 @@ __global__ void __launch_bounds__(kAThreads) dec_k4(DecodeArgs a) {
 #pragma unroll
     for (int g = 0; g < GM; ++g) dsum[g] = 0.f;
     const int jw = chunk * kDecodeChunk + warp * KPW;
+    // all of this warp's K and V rows and P values are loaded before any is used
+    float kv[KPW][VPL], vv[KPW][VPL], pl[KPW];
 #pragma unroll
     for (int k = 0; k < KPW; ++k) {
         const int j = jw + k;
-        if (j >= a.L) break;
-        float kv[VPL], vv[VPL];
-        const float *kr = a.k + int64_t(kvh) * a.sh + int64_t(j) * a.sp + d0;
-        const float *vr = a.v + int64_t(kvh) * a.sh + int64_t(j) * a.sp + d0;
+        const bool ok = j < a.L;
+        const float *kr = a.k + int64_t(kvh) * a.sh + int64_t(ok ? j : 0) * a.sp + d0;
+        const float *vr = a.v + int64_t(kvh) * a.sh + int64_t(ok ? j : 0) * a.sp + d0;
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-            kv[v] = kr[v];
-            vv[v] = vr[v];
+            kv[k][v] = ok ? kr[v] : 0.f;
+            vv[k][v] = ok ? vr[v] : 0.f;
         }
         // P of this key for each head of the group (lanes load in parallel)
-        const float pl = lane < G ? a.attn[int64_t(kvh * G + lane) * a.L + j] : 0.f;
+        pl[k] = ok && lane < G ? a.attn[int64_t(kvh * G + lane) * a.L + j] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < KPW; ++k) {
+        if (jw + k >= a.L) break;
 #pragma unroll
         for (int g = 0; g < GM; ++g) {
             if (g >= G) break;
             float t = 0.f;
 #pragma unroll
-            for (int v = 0; v < VPL; ++v) t = fmaf(sC[g * hd + d0 + v], vv[v], t);
+            for (int v = 0; v < VPL; ++v) t = fmaf(sC[g * hd + d0 + v], vv[k][v], t);
             const float dA = warp_sum(t);
-            const float P = __shfl_sync(0xffffffffu, pl, g);
+            const float P = __shfl_sync(0xffffffffu, pl[k], g);
             const float pd = P * dA;
             dsum[g] += pd;
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
-                U[g][v] = fmaf(pd, kv[v], U[g][v]);
-                W[g][v] = fmaf(P, kv[v], W[g][v]);
+                U[g][v] = fmaf(pd, kv[k][v], U[g][v]);
+                W[g][v] = fmaf(P, kv[k][v], W[g][v]);
             }
         }
     }
@@ -488,17 +498,18 @@ __global__ void __launch_bounds__(kAThreads) dec_k4(DecodeArgs a) {
 
 // ------------------------------------------------------------------ k6: dQpre and gh_q per head
 
-__global__ void __launch_bounds__(kThreads) dec_k6(DecodeArgs a, RopeFreqs fr) {
+__global__ void __launch_bounds__(kQThreads) dec_k6(DecodeArgs a, RopeFreqs fr) {
     __shared__ float sq[256];
     __shared__ float sD;
-    __shared__ float red[16][kWarps];
+    __shared__ float red[16][kQWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int h = blockIdx.x;
     if (threadIdx.x == 0) prefetch_l2(a.lq.b + int64_t(h) * a.hd * a.rank, size_t(a.hd) * a.rank * 4);
     pdl_trigger();
     pdl_wait();
-    // blockDim / hd thread groups each sum a slice of the chunks, then combine
-    __shared__ float su[kThreads], sw[kThreads];
+    // blockDim / hd thread groups each sum a slice of the chunks (four chunks in flight per
+    // thread), then combine
+    __shared__ float su[kQThreads], sw[kQThreads];
     const int groups = blockDim.x / a.hd;
     const int grp = threadIdx.x / a.hd, d = threadIdx.x % a.hd;
     if (threadIdx.x < 32) {
@@ -571,7 +582,7 @@ __global__ void __launch_bounds__(kThreads) dec_k6(DecodeArgs a, RopeFreqs fr) {
     __syncthreads();
     if (threadIdx.x < a.rank) {
         float t = 0.f;
-        for (int w = 0; w < kWarps; ++w) t += red[threadIdx.x][w];
+        for (int w = 0; w < kQWarps; ++w) t += red[threadIdx.x][w];
         atomicAdd(a.gh + threadIdx.x, a.lora_scaling * t);
     }
 }
@@ -648,6 +659,19 @@ cudaError_t launch_b(void (*kernel)(KArgs...), dim3 grid, int block, size_t smem
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
     }
+    // The largest shared-memory carveout: with the default split an SM hosts only two k2
+    // blocks (28 KB each), and the rest of the grid waits for a second wave.  The weight
+    // streams bypass L1, so the smaller L1 costs nothing.
+    static std::mutex mu;
+    static std::unordered_set<const void *> carved;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (carved.insert(reinterpret_cast<const void *>(kernel)).second) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                 int(cudaSharedmemCarveoutMaxShared));
+            if (e != cudaSuccess) return e;
+        }
+    }
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
@@ -676,7 +700,7 @@ cudaError_t launch_k4(int G, int hd, dim3 g4, size_t sm4, cudaStream_t st, const
 }
 
 template <int WT>
-int launch_all(const DecodeArgs &a, cudaStream_t st) {
+int launch_ffn(const DecodeArgs &a, cudaStream_t st) {
     TLB_CUDA(launch(dec_k1<WT>, dim3(unsigned(a.n1)), size_t(a.H) * 4, st, false, a));
     TLB_TRY(check_launch("decode k1"));
     const size_t sm2 = size_t(2) * (a.I / a.ns2) * 4;
@@ -686,6 +710,10 @@ int launch_all(const DecodeArgs &a, cudaStream_t st) {
     TLB_TRY(check_launch("decode k2"));
     TLB_CUDA(launch(dec_k3<WT>, dim3(unsigned(a.n3), unsigned(a.ns3)), size_t(a.H / a.ns3) * 4, st, true, a));
     TLB_TRY(check_launch("decode k3"));
+    return TLB_OK;
+}
+
+int launch_attn(const DecodeArgs &a, cudaStream_t st) {
     const int G = a.nh / a.nkv;
     const dim3 g4(a.nkv, a.nchunks);
     const size_t sm4 = (size_t(G) * a.hd + size_t(kAWarps) * G * 2 * a.hd) * 4;
@@ -693,7 +721,7 @@ int launch_all(const DecodeArgs &a, cudaStream_t st) {
     TLB_TRY(check_launch("decode k4"));
     RopeFreqs fr;
     rope_freqs(fr, a.hd, a.rope_base);
-    TLB_CUDA(launch(dec_k6, dim3(a.nh), 0, st, true, a, fr));
+    TLB_CUDA(launch_b(dec_k6, dim3(a.nh), kQThreads, 0, st, true, a, fr));
     TLB_TRY(check_launch("decode k6"));
     const int64_t n7 = int64_t(a.qd + a.kvd) * a.rank + 2 * int64_t(a.rank) * a.H;
     TLB_CUDA(launch(dec_k7, dim3(unsigned(ceil_div(n7, kThreads))), 0, st, true, a));
@@ -716,12 +744,19 @@ bool decode_supported(const tlb_layer_cfg &c, int64_t S, int64_t L) {
            sm4 <= 200 * 1024 && L >= 1;
 }
 
-int decode_layer_launch(const DecodeArgs &a, int wtype, cudaStream_t st) {
+int decode_ffn_launch(const DecodeArgs &a, int wtype, cudaStream_t st) {
     switch (wtype) {
-        case TLB_W_F32: return launch_all<TLB_W_F32>(a, st);
-        case TLB_W_BF16: return launch_all<TLB_W_BF16>(a, st);
-        default: return launch_all<TLB_W_TERNARY_I8>(a, st);
+        case TLB_W_F32: return launch_ffn<TLB_W_F32>(a, st);
+        case TLB_W_BF16: return launch_ffn<TLB_W_BF16>(a, st);
+        default: return launch_ffn<TLB_W_TERNARY_I8>(a, st);
     }
+}
+
+int decode_attn_launch(const DecodeArgs &a, cudaStream_t st) { return launch_attn(a, st); }
+
+int decode_layer_launch(const DecodeArgs &a, int wtype, cudaStream_t st) {
+    TLB_TRY(decode_ffn_launch(a, wtype, st));
+    return decode_attn_launch(a, st);
 }
 
 }  // namespace tlb

@@ -13,7 +13,9 @@ struct DecodeArgs {
     const float *g_sub_ffn, *g_ffn, *g_sub_attn;
     const float *x, *gate, *up, *silu_gate, *hidden, *r1, *ctx, *k, *v, *attn, *hq, *hv;
     int64_t sh, sp;
-    float *d_hidden;                                   // [H] in: dOut, out: dR1
+    float *d_hidden;                                   // [H] in: dOut, out: dR1 (single call)
+    const float *dout;                                 // [H] the layer's dOut (k1, k3)
+    float *dhid_out;                                   // [H] receives dR1 (k4), or NULL
     float *dF, *dN2, *dR1, *dSub, *dctx;               // workspace vectors
     float *Upart, *Wpart, *Dpart, *dqpre, *dv, *gh;    // workspace attention / LoRA
     tlb_lora lq, lv;
@@ -88,5 +90,10 @@ int decode_persistent_launch(const DecodeArgs &d, const tlb_layer_cfg &c, int64_
                              size_t off_pp, cudaStream_t st);
 int decode_rows_per_block();
 int decode_layer_launch(const DecodeArgs &a, int wtype, cudaStream_t st);
+// The two halves of the chain: k1 .. k3 (dF, dN2, dR1 and dSub) and k4 .. k7 (attention,
+// dQpre, LoRA and AdamW), for callers that overlap one layer's second half with the next
+// layer's first half on another stream.
+int decode_ffn_launch(const DecodeArgs &a, int wtype, cudaStream_t st);
+int decode_attn_launch(const DecodeArgs &a, cudaStream_t st);
 
 }  // namespace tlb

@@ -7,6 +7,8 @@
 #include "decode.cuh"
 
 #include <algorithm>
+#include <map>
+#include <mutex>
 
 namespace tlb {
 
@@ -241,6 +243,144 @@ int check_adam(const tlb_adamw_cfg *a) {
     return TLB_OK;
 }
 
+// The single-token kernels read every vector with 16-byte loads.
+bool decode_route(const tlb_layer_cfg &c, int64_t S, int64_t L, const tlb_layer_weights *w,
+                  const tlb_layer_acts *acts, const float *d_hidden) {
+    if (!decode_supported(c, S, L)) return false;
+    for (const void *ptr : {(const void *)w->w_down.w, (const void *)w->w_gate.w, (const void *)w->w_up.w,
+                            (const void *)w->w_o.w, (const void *)w->gamma_sub_ffn, (const void *)w->gamma_ffn,
+                            (const void *)w->gamma_sub_attn, (const void *)acts->gate, (const void *)acts->up,
+                            (const void *)acts->silu_gate, (const void *)acts->hidden, (const void *)acts->r1,
+                            (const void *)acts->ctx, (const void *)d_hidden})
+        if (ptr != nullptr && !aligned16(ptr)) return false;
+    return true;
+}
+
+// Arguments of the single-token kernels for one layer; dOut is read from and dR1
+// copied to d_hidden (a stack overrides both).
+void decode_args(const tlb_layer_cfg &c, int64_t L, const tlb_layer_weights *w, const tlb_layer_acts *acts,
+                 const tlb_lora *lora_q, const tlb_lora *lora_v, const tlb_adamw_cfg *adam, float *d_hidden,
+                 double *sumsq, void *ws, const LayerWs &p, DecodeArgs &d) {
+    const int qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
+    float *dqpre = ws_at<float>(ws, p.dqpre), *dv = ws_at<float>(ws, p.dv);
+    d.H = c.dim;
+    d.I = c.ffn_dim;
+    d.qd = qd;
+    d.kvd = kvd;
+    d.nh = c.n_heads;
+    d.nkv = c.n_kv_heads;
+    d.hd = c.head_dim;
+    d.L = int(L);
+    d.rank = c.rank;
+    d.flags = c.flags;
+    d.act = c.act;
+    d.pos = int(L - 1);
+    d.chunk = kDecodeChunk;
+    d.nchunks = int(ceil_div(L, kDecodeChunk));
+    d.eps = c.norm_eps;
+    d.scale = c.attn_scale;
+    d.lora_scaling = c.lora_alpha / float(c.rank);
+    d.rope_base = c.rope_base;
+    d.w_down = w->w_down.w;
+    d.w_gate = w->w_gate.w;
+    d.w_up = w->w_up.w;
+    d.w_o = w->w_o.w;
+    d.s_down = w->w_down.scale;
+    d.s_gate = w->w_gate.scale;
+    d.s_up = w->w_up.scale;
+    d.s_o = w->w_o.scale;
+    d.g_sub_ffn = w->gamma_sub_ffn;
+    d.g_ffn = w->gamma_ffn;
+    d.g_sub_attn = w->gamma_sub_attn;
+    d.x = acts->x;
+    d.gate = acts->gate;
+    d.up = acts->up;
+    d.silu_gate = acts->silu_gate;
+    d.hidden = acts->hidden;
+    d.r1 = acts->r1;
+    d.ctx = acts->ctx;
+    d.k = acts->k;
+    d.v = acts->v;
+    d.attn = acts->attn;
+    d.hq = acts->lora_q_h;
+    d.hv = acts->lora_v_h;
+    d.sh = acts->kv_stride_head;
+    d.sp = acts->kv_stride_pos;
+    d.d_hidden = d_hidden;
+    d.dF = ws_at<float>(ws, p.dF);
+    d.dN2 = ws_at<float>(ws, p.dN2);
+    d.dR1 = ws_at<float>(ws, p.dR1);
+    d.dSub = ws_at<float>(ws, p.dSub);
+    d.Upart = ws_at<float>(ws, p.Upart);
+    d.Wpart = ws_at<float>(ws, p.Wpart);
+    d.Dpart = ws_at<float>(ws, p.Dpart);
+    d.dqpre = dqpre;
+    d.dv = dv;
+    d.gh = ws_at<float>(ws, p.gh2);    // [gh_q | gh_v], 2 * rank floats
+    d.lq = *lora_q;
+    d.lv = *lora_v;
+    d.ka = adam_coef(*adam, 1.0f);
+    d.kb = adam_coef(*adam, float(adam->lr_b_mult));
+    d.sumsq = sumsq;
+    const int rpb = decode_rows_per_block();
+    d.n1 = int(ceil_div(c.ffn_dim, rpb));
+    d.n2 = int(ceil_div(c.dim, rpb));
+    d.n3 = int(ceil_div(qd, rpb));
+    // column ranges: more blocks in flight for the two GEMVs with few rows (whole 16-byte
+    // weight chunks per range, ranges a multiple of 4 floats), as long as k2 stays one
+    // wave of three blocks per SM
+    const int E = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 8 : 16);
+    d.ns2 = 1;
+    for (int n : {4, 2})
+        if (c.ffn_dim % (n * E) == 0 && (c.ffn_dim / n) % 4 == 0 && int64_t(d.n2) * n <= 3 * num_sms()) {
+            d.ns2 = n;
+            break;
+        }
+    d.ns3 = 1;
+    if (c.dim % (2 * E) == 0 && (c.dim / 2) % 4 == 0) d.ns3 = 2;
+    d.part1 = ws_at<float2>(ws, p.part1);
+    d.part2 = ws_at<float2>(ws, p.part2);
+    d.part3 = ws_at<float2>(ws, p.part3);
+    d.dout = d_hidden;
+    d.dhid_out = d_hidden;
+}
+
+// The second stream of a single-token stack: one per device, at the lowest priority, so
+// that the blocks of the next layer's GEMV chain go first; with its events (per layer
+// parity): e3 after a layer's k1 .. k3, e7 after its k4 .. k7.  Created on first use,
+// which must not be inside a stream capture.
+struct SideStream {
+    std::mutex mu;
+    cudaStream_t s = nullptr;
+    cudaEvent_t e3[2] = {nullptr, nullptr}, e7[2] = {nullptr, nullptr};
+};
+
+int side_stream(SideStream *&out) {
+    static std::mutex mu;
+    static std::map<int, SideStream *> all;
+    int dev = 0;
+    TLB_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lock(mu);
+    SideStream *&ss = all[dev];
+    if (ss == nullptr) {
+        auto *n = new SideStream();
+        int least = 0, greatest = 0;
+        TLB_CUDA(cudaDeviceGetStreamPriorityRange(&least, &greatest));
+        TLB_CUDA(cudaStreamCreateWithPriority(&n->s, cudaStreamNonBlocking, least));
+        for (int i = 0; i < 2; ++i) {
+            TLB_CUDA(cudaEventCreateWithFlags(&n->e3[i], cudaEventDisableTiming));
+            TLB_CUDA(cudaEventCreateWithFlags(&n->e7[i], cudaEventDisableTiming));
+        }
+        ss = n;
+    }
+    out = ss;
+    return TLB_OK;
+}
+
+size_t stack_half(const tlb_layer_cfg &c, int64_t S, int64_t L) {
+    return (plan(c, S, L).total + 255) / 256 * 256;
+}
+
 }  // namespace
 }  // namespace tlb
 
@@ -315,89 +455,9 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
     const int qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
     ProfileScope prof(st);
     float *dqpre = ws_at<float>(ws, p.dqpre), *dv = ws_at<float>(ws, p.dv);
-    bool vec_ok = true;   // the single-token kernels read every vector with 16-byte loads
-    for (const void *ptr : {(const void *)w->w_down.w, (const void *)w->w_gate.w, (const void *)w->w_up.w,
-                            (const void *)w->w_o.w, (const void *)w->gamma_sub_ffn, (const void *)w->gamma_ffn,
-                            (const void *)w->gamma_sub_attn, (const void *)acts->gate, (const void *)acts->up,
-                            (const void *)acts->silu_gate, (const void *)acts->hidden, (const void *)acts->r1,
-                            (const void *)acts->ctx, (const void *)d_hidden})
-        vec_ok = vec_ok && (ptr == nullptr || aligned16(ptr));
-    if (decode_supported(c, S, L) && vec_ok) {
+    if (decode_route(c, S, L, w, acts, d_hidden)) {
         DecodeArgs d;
-        d.H = c.dim;
-        d.I = c.ffn_dim;
-        d.qd = qd;
-        d.kvd = kvd;
-        d.nh = c.n_heads;
-        d.nkv = c.n_kv_heads;
-        d.hd = c.head_dim;
-        d.L = int(L);
-        d.rank = c.rank;
-        d.flags = c.flags;
-        d.act = c.act;
-        d.pos = int(L - 1);
-        d.chunk = kDecodeChunk;
-        d.nchunks = int(ceil_div(L, kDecodeChunk));
-        d.eps = c.norm_eps;
-        d.scale = c.attn_scale;
-        d.lora_scaling = c.lora_alpha / float(c.rank);
-        d.rope_base = c.rope_base;
-        d.w_down = w->w_down.w;
-        d.w_gate = w->w_gate.w;
-        d.w_up = w->w_up.w;
-        d.w_o = w->w_o.w;
-        d.s_down = w->w_down.scale;
-        d.s_gate = w->w_gate.scale;
-        d.s_up = w->w_up.scale;
-        d.s_o = w->w_o.scale;
-        d.g_sub_ffn = w->gamma_sub_ffn;
-        d.g_ffn = w->gamma_ffn;
-        d.g_sub_attn = w->gamma_sub_attn;
-        d.x = acts->x;
-        d.gate = acts->gate;
-        d.up = acts->up;
-        d.silu_gate = acts->silu_gate;
-        d.hidden = acts->hidden;
-        d.r1 = acts->r1;
-        d.ctx = acts->ctx;
-        d.k = acts->k;
-        d.v = acts->v;
-        d.attn = acts->attn;
-        d.hq = acts->lora_q_h;
-        d.hv = acts->lora_v_h;
-        d.sh = acts->kv_stride_head;
-        d.sp = acts->kv_stride_pos;
-        d.d_hidden = d_hidden;
-        d.dF = ws_at<float>(ws, p.dF);
-        d.dN2 = ws_at<float>(ws, p.dN2);
-        d.dR1 = ws_at<float>(ws, p.dR1);
-        d.dSub = ws_at<float>(ws, p.dSub);
-        d.Upart = ws_at<float>(ws, p.Upart);
-        d.Wpart = ws_at<float>(ws, p.Wpart);
-        d.Dpart = ws_at<float>(ws, p.Dpart);
-        d.dqpre = dqpre;
-        d.dv = dv;
-        d.gh = ws_at<float>(ws, p.gh2);    // [gh_q | gh_v], 2 * rank floats
-        d.lq = *lora_q;
-        d.lv = *lora_v;
-        d.ka = adam_coef(*adam, 1.0f);
-        d.kb = adam_coef(*adam, float(adam->lr_b_mult));
-        d.sumsq = sumsq;
-        const int rpb = decode_rows_per_block();
-        d.n1 = int(ceil_div(c.ffn_dim, rpb));
-        d.n2 = int(ceil_div(c.dim, rpb));
-        d.n3 = int(ceil_div(qd, rpb));
-        // column ranges: more blocks in flight for the two GEMVs with few rows (whole 16-byte
-        // weight chunks per range, ranges a multiple of 4 floats)
-        const int E = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 8 : 16);
-        d.ns2 = 1;
-        for (int n : {4, 2})
-            if (c.ffn_dim % (n * E) == 0 && (c.ffn_dim / n) % 4 == 0) { d.ns2 = n; break; }
-        d.ns3 = 1;
-        if (c.dim % (2 * E) == 0 && (c.dim / 2) % 4 == 0) d.ns3 = 2;
-        d.part1 = ws_at<float2>(ws, p.part1);
-        d.part2 = ws_at<float2>(ws, p.part2);
-        d.part3 = ws_at<float2>(ws, p.part3);
+        decode_args(c, L, w, acts, lora_q, lora_v, adam, d_hidden, sumsq, ws, p, d);
         if ((c.flags & TLB_PERSISTENT) && persistent_supported(c, S, L))
             return decode_persistent_launch(d, c, L, ws, p.gbar, p.pp, st);
         return decode_layer_launch(d, c.wtype, st);
@@ -407,6 +467,73 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
     const LoraJob jobs[2] = {{dqpre, acts->lora_q_h, qd, *lora_q, ws_at<void>(ws, p.lora_q)},
                              {dv, acts->lora_v_h, kvd, *lora_v, ws_at<void>(ws, p.lora_v)}};
     return lora_seq_launch(S, c.dim, c.rank, c.lora_alpha, acts->x, jobs, 2, *adam, sumsq, st);
+}
+
+
+size_t tlb_stack_workspace_bytes(const tlb_layer_cfg *cfg, int64_t S, int64_t L) {
+    if (cfg == nullptr || S < 0) return 0;
+    return 2 * stack_half(*cfg, S, L < S ? S : L);
+}
+
+int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n_layers,
+                       const tlb_layer_weights *w, const tlb_layer_acts *acts, const tlb_lora *lora_q,
+                       const tlb_lora *lora_v, const tlb_adamw_cfg *adam, float *d_hidden, double *sumsq,
+                       void *ws, size_t ws_bytes, void *stream) {
+    clear_error();
+    TLB_TRY(validate_cfg(cfg));
+    TLB_REQUIRE(n_layers >= 0 && S >= 0, TLB_EINVAL, "stack_backward: negative n_layers or S");
+    if (n_layers == 0 || S == 0) return TLB_OK;
+    TLB_REQUIRE(w && acts && lora_q && lora_v, TLB_EINVAL, "stack_backward: NULL layer array");
+    TLB_REQUIRE(d_hidden, TLB_EINVAL, "stack_backward: NULL d_hidden");
+    TLB_TRY(check_adam(adam));
+    const tlb_layer_cfg &c = *cfg;
+    const size_t half = stack_half(c, S, L);
+    TLB_REQUIRE(ws != nullptr && ws_bytes >= 2 * half, TLB_EINVAL,
+                "stack workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, 2 * half);
+    TLB_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, TLB_EINVAL, "workspace not 256-byte aligned");
+    bool pipelined = S == 1 && !(c.flags & TLB_PERSISTENT);
+    for (int l = 0; l < n_layers; ++l) {
+        TLB_TRY(check_acts_ffn(c, &w[l], &acts[l]));
+        TLB_TRY(check_acts_attn(c, S, L, &w[l], &acts[l]));
+        TLB_TRY(check_lora(&lora_q[l], "Q"));
+        TLB_TRY(check_lora(&lora_v[l], "V"));
+        TLB_REQUIRE(acts[l].x && acts[l].lora_q_h && acts[l].lora_v_h, TLB_EINVAL,
+                    "stack_backward: layer %d: NULL x / lora_q_h / lora_v_h", l);
+        pipelined = pipelined && decode_route(c, S, L, &w[l], &acts[l], d_hidden);
+    }
+    if (!pipelined) {
+        // the layers one after another on the caller's stream ([RS] backward_through_layers)
+        for (int l = n_layers - 1; l >= 0; --l)
+            TLB_TRY(tlb_layer_backward(cfg, S, L, &w[l], &acts[l], &lora_q[l], &lora_v[l], adam, d_hidden, sumsq,
+                                       ws, half, stream));
+        return TLB_OK;
+    }
+    // Single-token layers: layer l's k1 .. k3 (its dR1, the next layer's dOut) on the
+    // caller's stream, its k4 .. k7 on the side stream, so that the attention and LoRA
+    // half of layer l runs beside the GEMV chain of layer l - 1.  Layer l uses workspace
+    // half l % 2; before layer l's first kernel the caller's stream waits for layer l + 2's
+    // side work, the last user of that half.
+    cudaStream_t st = as_stream(stream);
+    SideStream *side = nullptr;
+    TLB_TRY(side_stream(side));
+    std::lock_guard<std::mutex> lock(side->mu);
+    const LayerWs p = plan(c, S, L);
+    void *halves[2] = {ws, static_cast<char *>(ws) + half};
+    for (int l = n_layers - 1; l >= 0; --l) {
+        const int par = l & 1;
+        if (l + 2 <= n_layers - 1) TLB_CUDA(cudaStreamWaitEvent(st, side->e7[par], 0));
+        DecodeArgs d;
+        decode_args(c, L, &w[l], &acts[l], &lora_q[l], &lora_v[l], adam, d_hidden, sumsq, halves[par], p, d);
+        d.dout = l == n_layers - 1 ? d_hidden : ws_at<float>(halves[par ^ 1], p.dR1);
+        d.dhid_out = l == 0 ? d_hidden : nullptr;
+        TLB_TRY(decode_ffn_launch(d, c.wtype, st));
+        TLB_CUDA(cudaEventRecord(side->e3[par], st));
+        TLB_CUDA(cudaStreamWaitEvent(side->s, side->e3[par], 0));
+        TLB_TRY(decode_attn_launch(d, side->s));
+        TLB_CUDA(cudaEventRecord(side->e7[par], side->s));
+    }
+    TLB_CUDA(cudaStreamWaitEvent(st, side->e7[0], 0));   // layer 0 ends the side stream's work
+    return TLB_OK;
 }
 
 }  // extern "C"
