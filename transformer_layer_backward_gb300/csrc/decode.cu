@@ -21,6 +21,7 @@
 // 16-byte reads of the 32 lanes (each lane owning one 16-byte chunk of a weight row)
 // fall in distinct banks.  The two sums an RMSNorm backward needs over a vector a
 // GEMV produces are accumulated per block by that GEMV and summed by the consumer.
+#include <algorithm>
 #include <mutex>
 #include <unordered_set>
 
@@ -157,35 +158,6 @@ __device__ __forceinline__ void prefetch_l2(const void *p, size_t bytes) {
         l2_prefetch(p, uint32_t(bytes));
 }
 
-// Block-wide (sum dy g x, sum x^2) over n elements (n % 4 == 0, 16-byte aligned arrays),
-// every thread issuing all its loads of a batch before using them.
-__device__ __forceinline__ float2 rms_sums_full(const float *x, const float *g, const float *dy, int n, float2 *red) {
-    constexpr int B = 4;
-    const int n4 = n >> 2;
-    const float4 *x4 = reinterpret_cast<const float4 *>(x), *g4 = reinterpret_cast<const float4 *>(g),
-                 *d4 = reinterpret_cast<const float4 *>(dy);
-    float2 acc = make_float2(0.f, 0.f);
-    for (int base = threadIdx.x; base < n4; base += blockDim.x * B) {
-        float4 xv[B], gv[B], dv[B];
-#pragma unroll
-        for (int b = 0; b < B; ++b) {
-            const int i = base + b * blockDim.x;
-            const bool ok = i < n4;
-            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            xv[b] = ok ? x4[i] : z;
-            gv[b] = ok ? g4[i] : z;
-            dv[b] = ok ? d4[i] : z;
-        }
-#pragma unroll
-        for (int b = 0; b < B; ++b) {
-            acc.x += xv[b].x * gv[b].x * dv[b].x + xv[b].y * gv[b].y * dv[b].y + xv[b].z * gv[b].z * dv[b].z +
-                     xv[b].w * gv[b].w * dv[b].w;
-            acc.y += dot4(xv[b], xv[b]);
-        }
-    }
-    return block_sum2(acc, red);
-}
-
 // ------------------------------------------------------------------ k1: dF = s_d W_down dOut
 
 template <int WT>
@@ -193,7 +165,16 @@ __global__ void __launch_bounds__(kThreads) dec_k1(DecodeArgs a) {
     extern __shared__ float4 sm4[];
     __shared__ float2 red[32];
     float *sx = reinterpret_cast<float *>(sm4);
+    {
+        // this block's W_down rows, which depend on nothing before it, go to L2 first
+        constexpr int ES = 16 / EPC<WT>::v;
+        const int rows = kWarps * kR, r0 = blockIdx.x * rows;
+        if (threadIdx.x == 0 && r0 < a.I)
+            prefetch_l2(static_cast<const char *>(a.w_down) + size_t(r0) * a.H * ES,
+                        size_t(min(rows, a.I - r0)) * a.H * ES);
+    }
     pdl_trigger();
+    pdl_wait();
     stage_vector<WT>(sx, a.dout, a.H);
     if (blockIdx.x == 0 && threadIdx.x < 2 * a.rank) a.gh[threadIdx.x] = 0.f;
     // dN2 and dSub are sums of per-block column-range products in k2 and k3
@@ -306,8 +287,10 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
     extern __shared__ float4 sm4[];
     __shared__ float2 red[32];
     // this block's column range [c0, c0 + nc) of dR1 and of the W_O rows
-    const int nc = a.H / a.ns3, c0 = blockIdx.y * nc;
+    const int nc = a.H / a.ns3, c0 = blockIdx.y * nc, n4 = nc >> 2;
+    // [sR (swizzled dR1) | sDo | sGam | sR1] over the range (nc floats each), then sGR over H
     float *sR = reinterpret_cast<float *>(sm4);
+    float4 *sDo = sm4 + n4, *sGam = sm4 + 2 * n4, *sR1 = sm4 + 3 * n4, *sGR = sm4 + 4 * n4;
     {
         constexpr int ES = 16 / EPC<WT>::v;
         const int lane = threadIdx.x & 31, r = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR + lane;
@@ -315,27 +298,60 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
             prefetch_l2(reinterpret_cast<const char *>(a.w_o) + (size_t(r) * a.H + c0) * ES, size_t(nc) * ES);
     }
     pdl_trigger();
-    pdl_wait();
-    float rinv = 1.f, c = 0.f;
-    const bool pre = a.flags & TLB_PRE_NORM;
-    if (pre) rms_coef2(rms_sums_full(a.r1, a.g_ffn, a.dN2, a.H, red), a.H, a.eps, rinv, c);
-    const bool resid = a.flags & TLB_RESIDUAL;
-    {
-        const int n4 = nc >> 2;
-        const float4 *dn4 = reinterpret_cast<const float4 *>(a.dN2 + c0), *r14 = reinterpret_cast<const float4 *>(a.r1 + c0);
-        const float4 *gf4 = reinterpret_cast<const float4 *>(a.g_ffn + c0),
-                     *do4 = reinterpret_cast<const float4 *>(a.dout + c0);
-        for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 dn = dn4[i], r = pre ? r14[i] : z, gm = pre ? gf4[i] : z, dO = resid ? do4[i] : z;
-            float4 v;
-            v.x = (pre ? rinv * (dn.x * gm.x - r.x * c) : dn.x) + dO.x;
-            v.y = (pre ? rinv * (dn.y * gm.y - r.y * c) : dn.y) + dO.y;
-            v.z = (pre ? rinv * (dn.z * gm.z - r.z * c) : dn.z) + dO.z;
-            v.w = (pre ? rinv * (dn.w * gm.w - r.w * c) : dn.w) + dO.w;
-            reinterpret_cast<float4 *>(sR)[xunit<WT>(i)] = v;
-            if (blockIdx.x == 0) reinterpret_cast<float4 *>(a.dR1 + c0)[i] = v;
+    const bool pre = a.flags & TLB_PRE_NORM, resid = a.flags & TLB_RESIDUAL;
+    // Before the wait: gamma_ffn * r1 over all H and sum r1^2 (the pre-norm sums need all
+    // of dim), and dOut, gamma_ffn, r1 over the range.
+    float rr = 0.f;
+    const int h4 = a.H >> 2;
+    if (pre) {
+        const float4 *g4 = reinterpret_cast<const float4 *>(a.g_ffn), *r4 = reinterpret_cast<const float4 *>(a.r1);
+        for (int i = threadIdx.x; i < h4; i += blockDim.x) {
+            const float4 g = g4[i], x = r4[i];
+            sGR[i] = make_float4(g.x * x.x, g.y * x.y, g.z * x.z, g.w * x.w);
+            rr += dot4(x, x);
         }
+    }
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        sDo[i] = resid ? reinterpret_cast<const float4 *>(a.dout + c0)[i] : z;
+        sGam[i] = pre ? reinterpret_cast<const float4 *>(a.g_ffn + c0)[i] : z;
+        sR1[i] = pre ? reinterpret_cast<const float4 *>(a.r1 + c0)[i] : z;
+    }
+    pdl_wait();
+    // After the wait: dN2 (one round of loads), the pre-norm coefficients, dR1 over the range.
+    float rinv = 1.f, c = 0.f;
+    const float4 *dn4 = reinterpret_cast<const float4 *>(a.dN2);
+    if (pre) {
+        constexpr int B = 4;
+        float4 dn[B];
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const int i = threadIdx.x + b * blockDim.x;
+            dn[b] = i < h4 ? __ldcg(dn4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float dot = 0.f;
+        for (int base = threadIdx.x; base < h4; base += blockDim.x * B) {
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int i = base + b * blockDim.x;
+                if (i >= h4) break;
+                const float4 d = base == int(threadIdx.x) ? dn[b] : __ldcg(dn4 + i);
+                dot += dot4(d, sGR[i]);
+                sGR[i] = d;
+            }
+        }
+        rms_coef2(block_sum2(make_float2(dot, rr), red), a.H, a.eps, rinv, c);   // synchronises
+    }
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 dn = pre ? sGR[(c0 >> 2) + i] : __ldcg(dn4 + (c0 >> 2) + i);
+        const float4 gm = sGam[i], r = sR1[i], dO = sDo[i];
+        float4 v;
+        v.x = (pre ? rinv * (dn.x * gm.x - r.x * c) : dn.x) + dO.x;
+        v.y = (pre ? rinv * (dn.y * gm.y - r.y * c) : dn.y) + dO.y;
+        v.z = (pre ? rinv * (dn.z * gm.z - r.z * c) : dn.z) + dO.z;
+        v.w = (pre ? rinv * (dn.w * gm.w - r.w * c) : dn.w) + dO.w;
+        reinterpret_cast<float4 *>(sR)[xunit<WT>(i)] = v;
+        if (blockIdx.x == 0) reinterpret_cast<float4 *>(a.dR1 + c0)[i] = v;
     }
     __syncthreads();
     constexpr int ES = 16 / EPC<WT>::v;
@@ -362,52 +378,36 @@ __global__ void __launch_bounds__(kAThreads) dec_k4(DecodeArgs a) {
     __shared__ float2 red2[32];
     __shared__ float sDp[kAWarps][16];
     const int kvh = blockIdx.x, chunk = blockIdx.y;
+    const bool dv_block = chunk == a.nchunks;          // the extra block of each KV head: dV, gh_v
     const int G = a.nh / a.nkv;
     const int hd = VPL * 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int d0 = lane * VPL;
     float *sC = reinterpret_cast<float *>(sm4);        // [G][hd] dCtx
-    float *sR = sC + G * hd;                           // [kAWarps][G][2][hd] reduction
+    float *sR = sC + G * hd;                           // [kAWarps][G][2][hd] reduction (dV block: B_v rows)
+    float *sGC = sR + kAWarps * G * 2 * hd;            // [qd] gamma * ctx, then dSub
+    const bool sub = a.flags & TLB_SUB_NORM;
     {
-        const int j0 = chunk * kDecodeChunk, nj = min(kDecodeChunk, a.L - j0);
+        const int j0 = chunk * kDecodeChunk, nj = dv_block ? 0 : min(kDecodeChunk, a.L - j0);
         if (threadIdx.x < 2 * kDecodeChunk) {        // one K or V row per thread
             const int j = threadIdx.x % kDecodeChunk;
             const float *base = threadIdx.x < kDecodeChunk ? a.k : a.v;
             if (j < nj) prefetch_l2(base + int64_t(kvh) * a.sh + int64_t(j0 + j) * a.sp, size_t(hd) * 4);
-        } else if (threadIdx.x < 2 * kDecodeChunk + G) {
+        } else if (threadIdx.x < 2 * kDecodeChunk + G && nj > 0) {
             const int g = threadIdx.x - 2 * kDecodeChunk;
             prefetch_l2(a.attn + int64_t(kvh * G + g) * a.L + j0, size_t(nj) * 4);
         }
     }
     pdl_trigger();
-    pdl_wait();
-    float rinv = 1.f, c = 0.f;
-    const bool sub = a.flags & TLB_SUB_NORM;
-    if (sub) rms_coef2(rms_sums_full(a.ctx, a.g_sub_attn, a.dSub, a.qd, red2), a.qd, a.eps, rinv, c);
-    const int off = kvh * G * hd;
-    for (int i = threadIdx.x; i < G * hd; i += blockDim.x) {
-        const int q = off + i;
-        const float ds = a.dSub[q];
-        sC[i] = sub ? rinv * (ds * a.g_sub_attn[q] - a.ctx[q] * c) : ds;
-    }
-    if (kvh == 0 && chunk == 0 && a.dhid_out != nullptr)
-        for (int i = threadIdx.x; i < a.H; i += blockDim.x) a.dhid_out[i] = a.dR1[i];
-    __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int d0 = lane * VPL;
-    float U[GM][VPL], W[GM][VPL];                      // GM >= heads per KV group
-#pragma unroll
-    for (int g = 0; g < GM; ++g)
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) U[g][v] = W[g][v] = 0.f;
-    float dsum[GM];
-#pragma unroll
-    for (int g = 0; g < GM; ++g) dsum[g] = 0.f;
+    // Before the wait: this warp's K and V rows and P values, gamma * ctx over all q_dim
+    // entries and sum ctx^2 (the sub-norm sums need all of them), and for the dV block
+    // the KV head's rows of B_v.
     const int jw = chunk * kDecodeChunk + warp * KPW;
-    // all of this warp's K and V rows and P values are loaded before any is used
     float kv[KPW][VPL], vv[KPW][VPL], pl[KPW];
 #pragma unroll
     for (int k = 0; k < KPW; ++k) {
         const int j = jw + k;
-        const bool ok = j < a.L;
+        const bool ok = !dv_block && j < a.L;
         const float *kr = a.k + int64_t(kvh) * a.sh + int64_t(ok ? j : 0) * a.sp + d0;
         const float *vr = a.v + int64_t(kvh) * a.sh + int64_t(ok ? j : 0) * a.sp + d0;
 #pragma unroll
@@ -418,6 +418,92 @@ __global__ void __launch_bounds__(kAThreads) dec_k4(DecodeArgs a) {
         // P of this key for each head of the group (lanes load in parallel)
         pl[k] = ok && lane < G ? a.attn[int64_t(kvh * G + lane) * a.L + j] : 0.f;
     }
+    float cc = 0.f;
+    if (sub) {
+        const float4 *g4 = reinterpret_cast<const float4 *>(a.g_sub_attn);
+        const float4 *c4 = reinterpret_cast<const float4 *>(a.ctx);
+        for (int i = threadIdx.x; i < (a.qd >> 2); i += blockDim.x) {
+            const float4 g = g4[i], x = c4[i];
+            reinterpret_cast<float4 *>(sGC)[i] = make_float4(g.x * x.x, g.y * x.y, g.z * x.z, g.w * x.w);
+            cc += dot4(x, x);
+        }
+    }
+    if (dv_block)
+        for (int i = threadIdx.x; i < hd * a.rank; i += blockDim.x) sR[i] = a.lv.b[int64_t(kvh) * hd * a.rank + i];
+    pdl_wait();
+    // After the wait: dSub (one round of loads), the sub-norm coefficients, dCtx.
+    float rinv = 1.f, c = 0.f;
+    if (sub) {
+        constexpr int B = 4;
+        const float4 *ds4 = reinterpret_cast<const float4 *>(a.dSub);
+        const int n4 = a.qd >> 2;
+        float4 dsv[B];
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const int i = threadIdx.x + b * blockDim.x;
+            dsv[b] = i < n4 ? __ldcg(ds4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float dot = 0.f;
+        for (int base = threadIdx.x; base < n4; base += blockDim.x * B) {
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int i = base + b * blockDim.x;
+                if (i >= n4) break;
+                const float4 d = base == int(threadIdx.x) ? dsv[b] : __ldcg(ds4 + i);
+                dot += dot4(d, reinterpret_cast<const float4 *>(sGC)[i]);
+                reinterpret_cast<float4 *>(sGC)[i] = d;      // each thread rereads only its own entries
+            }
+        }
+        rms_coef2(block_sum2(make_float2(dot, cc), red2), a.qd, a.eps, rinv, c);
+    }
+    const int off = kvh * G * hd;
+    for (int i = threadIdx.x; i < G * hd; i += blockDim.x) {
+        const int q = off + i;
+        sC[i] = sub ? rinv * (sGC[q] * a.g_sub_attn[q] - a.ctx[q] * c) : __ldcg(a.dSub + q);
+    }
+    if (kvh == 0 && chunk == 0 && a.dhid_out != nullptr)
+        for (int i = threadIdx.x; i < a.H; i += blockDim.x) a.dhid_out[i] = __ldcg(a.dR1 + i);
+    __syncthreads();
+    if (dv_block) {
+        // dV of the current token: dV[kvh, d] = sum_g attn[h_g, pos] dCtx_h_g[d]; gh_v share
+        __shared__ float sv[256];
+        __shared__ float rr[16][kAWarps];
+        for (int d = threadIdx.x; d < hd; d += blockDim.x) {
+            float t = 0.f;
+            for (int g = 0; g < G; ++g) t = fmaf(a.attn[int64_t(kvh * G + g) * a.L + a.pos], sC[g * hd + d], t);
+            sv[d] = t;
+            a.dv[kvh * hd + d] = t;
+        }
+        __syncthreads();
+        float acc[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+        for (int d = threadIdx.x; d < hd; d += blockDim.x) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                if (r < a.rank) acc[r] = fmaf(sv[d], sR[d * a.rank + r], acc[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const float t = warp_sum(acc[r]);
+            if (lane == 0) rr[r][warp] = t;
+        }
+        __syncthreads();
+        if (threadIdx.x < a.rank) {
+            float t = 0.f;
+            for (int w = 0; w < kAWarps; ++w) t += rr[threadIdx.x][w];
+            atomicAdd(a.gh + a.rank + threadIdx.x, a.lora_scaling * t);
+        }
+        return;
+    }
+    float U[GM][VPL], W[GM][VPL];                      // GM >= heads per KV group
+#pragma unroll
+    for (int g = 0; g < GM; ++g)
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) U[g][v] = W[g][v] = 0.f;
+    float dsum[GM];
+#pragma unroll
+    for (int g = 0; g < GM; ++g) dsum[g] = 0.f;
 #pragma unroll
     for (int k = 0; k < KPW; ++k) {
         if (jw + k >= a.L) break;
@@ -462,38 +548,6 @@ __global__ void __launch_bounds__(kAThreads) dec_k4(DecodeArgs a) {
         for (int w = 0; w < kAWarps; ++w) t += sDp[w][threadIdx.x];
         a.Dpart[int64_t(chunk) * a.nh + kvh * G + threadIdx.x] = t;
     }
-    // dV of the current token: dV[kvh, d] = sum_g attn[h_g, pos] dCtx_h_g[d]; gh_v share
-    if (a.pos / kDecodeChunk == chunk) {
-        __shared__ float sv[256];
-        __shared__ float rr[16][kAWarps];
-        for (int d = threadIdx.x; d < hd; d += blockDim.x) {
-            float t = 0.f;
-            for (int g = 0; g < G; ++g) t = fmaf(a.attn[int64_t(kvh * G + g) * a.L + a.pos], sC[g * hd + d], t);
-            sv[d] = t;
-            a.dv[kvh * hd + d] = t;
-        }
-        __syncthreads();
-        float acc[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) acc[r] = 0.f;
-        for (int d = threadIdx.x; d < hd; d += blockDim.x) {
-            const float *br = a.lv.b + int64_t(kvh * hd + d) * a.rank;
-#pragma unroll
-            for (int r = 0; r < 16; ++r)
-                if (r < a.rank) acc[r] = fmaf(sv[d], br[r], acc[r]);
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const float t = warp_sum(acc[r]);
-            if (lane == 0) rr[r][warp] = t;
-        }
-        __syncthreads();
-        if (threadIdx.x < a.rank) {
-            float t = 0.f;
-            for (int w = 0; w < kAWarps; ++w) t += rr[threadIdx.x][w];
-            atomicAdd(a.gh + a.rank + threadIdx.x, a.lora_scaling * t);
-        }
-    }
 }
 
 // ------------------------------------------------------------------ k6: dQpre and gh_q per head
@@ -502,10 +556,17 @@ __global__ void __launch_bounds__(kQThreads) dec_k6(DecodeArgs a, RopeFreqs fr) 
     __shared__ float sq[256];
     __shared__ float sD;
     __shared__ float red[16][kQWarps];
+    __shared__ float sB[256 * 16];
+    __shared__ float sCos[128], sSin[128];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int h = blockIdx.x;
-    if (threadIdx.x == 0) prefetch_l2(a.lq.b + int64_t(h) * a.hd * a.rank, size_t(a.hd) * a.rank * 4);
     pdl_trigger();
+    // Before the wait: this head's rows of B_q (only this layer's k7, later, writes them)
+    // and the rotation angles of the current position.
+    for (int i = threadIdx.x; i < a.hd * a.rank; i += blockDim.x) sB[i] = a.lq.b[int64_t(h) * a.hd * a.rank + i];
+    if (a.flags & TLB_ROPE)
+        for (int d = threadIdx.x; d < (a.hd >> 1); d += blockDim.x)
+            rope_cos_sin(float(a.pos), fr.hi[d], fr.lo[d], sCos[d], sSin[d]);
     pdl_wait();
     // blockDim / hd thread groups each sum a slice of the chunks (four chunks in flight per
     // thread), then combine
@@ -552,8 +613,7 @@ __global__ void __launch_bounds__(kQThreads) dec_k6(DecodeArgs a, RopeFreqs fr) 
     for (int d = threadIdx.x; d < half; d += blockDim.x) {
         float y1 = sq[d], y2 = sq[d + half];
         if (a.flags & TLB_ROPE) {
-            float cs, sn;
-            rope_cos_sin(float(a.pos), fr.hi[d], fr.lo[d], cs, sn);
+            const float cs = sCos[d], sn = sSin[d];
             const float t1 = y1 * cs + y2 * sn, t2 = -y1 * sn + y2 * cs;
             y1 = t1;
             y2 = t2;
@@ -569,10 +629,9 @@ __global__ void __launch_bounds__(kQThreads) dec_k6(DecodeArgs a, RopeFreqs fr) 
 #pragma unroll
     for (int r = 0; r < 16; ++r) acc[r] = 0.f;
     for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
-        const float *br = a.lq.b + int64_t(h * a.hd + d) * a.rank;
 #pragma unroll
         for (int r = 0; r < 16; ++r)
-            if (r < a.rank) acc[r] = fmaf(sq[d], br[r], acc[r]);
+            if (r < a.rank) acc[r] = fmaf(sq[d], sB[d * a.rank + r], acc[r]);
     }
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
@@ -589,55 +648,76 @@ __global__ void __launch_bounds__(kQThreads) dec_k6(DecodeArgs a, RopeFreqs fr) 
 
 // ------------------------------------------------------------------ k7: LoRA gradients + AdamW
 
+// One thread per adapter element.  Before the wait: the element's parameter, moments and
+// the cached factor it multiplies (h or x); after it: the chain's factor (dQpre, dV or
+// gh), the gradient and the AdamW step.
 __global__ void __launch_bounds__(kThreads) dec_k7(DecodeArgs a) {
     __shared__ float red[32];
     pdl_trigger();
-    pdl_wait();
     const int64_t nbq = int64_t(a.qd) * a.rank, nbv = int64_t(a.kvd) * a.rank, na = int64_t(a.rank) * a.H;
+    const int64_t n = nbq + nbv + 2 * na;
     const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    float g = 0.f;
-    int which = -1;   // 0: sumsq of dA, 1: of dB
+    // which: 0 B_q, 1 B_v, 2 A_q, 3 A_v; f: index within it; o, r: its factors' indices
+    int which = -1;
+    int64_t f = 0;
+    int o = 0, r = 0;
     if (e < nbq) {
-        const int o = int(e / a.rank), r = int(e % a.rank);
-        g = a.lora_scaling * a.dqpre[o] * a.hq[r];
-        if (a.lq.grad_b) a.lq.grad_b[e] = g;
-        float m = a.lq.m_b[e], v = a.lq.v_b[e];
-        a.lq.b[e] = adam_elem(a.lq.b[e], g, m, v, a.kb);
-        a.lq.m_b[e] = m;
-        a.lq.v_b[e] = v;
-        which = 1;
-    } else if (e < nbq + nbv) {
-        const int64_t f = e - nbq;
-        const int o = int(f / a.rank), r = int(f % a.rank);
-        g = a.lora_scaling * a.dv[o] * a.hv[r];
-        if (a.lv.grad_b) a.lv.grad_b[f] = g;
-        float m = a.lv.m_b[f], v = a.lv.v_b[f];
-        a.lv.b[f] = adam_elem(a.lv.b[f], g, m, v, a.kb);
-        a.lv.m_b[f] = m;
-        a.lv.v_b[f] = v;
-        which = 1;
-    } else if (e < nbq + nbv + 2 * na) {
-        const int64_t f = e - nbq - nbv;
-        const bool isq = f < na;
-        const int64_t f2 = isq ? f : f - na;
-        const int r = int(f2 / a.H), cidx = int(f2 % a.H);
-        const tlb_lora &l = isq ? a.lq : a.lv;
-        g = a.gh[(isq ? 0 : a.rank) + r] * a.x[cidx];
-        if (l.grad_a) l.grad_a[f2] = g;
-        float m = l.m_a[f2], v = l.v_a[f2];
-        l.a[f2] = adam_elem(l.a[f2], g, m, v, a.ka);
-        l.m_a[f2] = m;
-        l.v_a[f2] = v;
         which = 0;
+        f = e;
+    } else if (e < nbq + nbv) {
+        which = 1;
+        f = e - nbq;
+    } else if (e < n) {
+        f = e - nbq - nbv;
+        which = f < na ? 2 : 3;
+        if (which == 3) f -= na;
+    }
+    const tlb_lora &l = (which == 0 || which == 2) ? a.lq : a.lv;
+    float p = 0.f, m = 0.f, v = 0.f, fac = 0.f;
+    if (which >= 0) {
+        if (which <= 1) {
+            o = int(f / a.rank);
+            r = int(f % a.rank);
+            p = l.b[f];
+            m = l.m_b[f];
+            v = l.v_b[f];
+            fac = (which == 0 ? a.hq : a.hv)[r];
+        } else {
+            r = int(f / a.H);
+            o = int(f % a.H);
+            p = l.a[f];
+            m = l.m_a[f];
+            v = l.v_a[f];
+            fac = a.x[o];
+        }
+    }
+    pdl_wait();
+    float sa = 0.f, sb = 0.f;   // dA^2, dB^2
+    if (which >= 0) {
+        float g;
+        if (which == 0) g = a.lora_scaling * __ldcg(a.dqpre + o) * fac;
+        else if (which == 1) g = a.lora_scaling * __ldcg(a.dv + o) * fac;
+        else g = __ldcg(a.gh + (which == 2 ? 0 : a.rank) + r) * fac;
+        if (which <= 1) {
+            if (l.grad_b) l.grad_b[f] = g;
+            l.b[f] = adam_elem(p, g, m, v, a.kb);
+            l.m_b[f] = m;
+            l.v_b[f] = v;
+            sb = g * g;
+        } else {
+            if (l.grad_a) l.grad_a[f] = g;
+            l.a[f] = adam_elem(p, g, m, v, a.ka);
+            l.m_a[f] = m;
+            l.v_a[f] = v;
+            sa = g * g;
+        }
     }
     if (a.sumsq) {
-        // blocks never straddle the dB / dA boundary when both counts are multiples of the
-        // block size; otherwise the two sums are reduced separately
-        const float sa = block_sum(which == 0 ? g * g : 0.f, red);
-        const float sb = block_sum(which == 1 ? g * g : 0.f, red);
+        const float ta = block_sum(sa, red);
+        const float tb = block_sum(sb, red);
         if (threadIdx.x == 0) {
-            if (sa != 0.f) atomicAdd(a.sumsq, double(sa));
-            if (sb != 0.f) atomicAdd(a.sumsq + 1, double(sb));
+            if (ta != 0.f) atomicAdd(a.sumsq, double(ta));
+            if (tb != 0.f) atomicAdd(a.sumsq + 1, double(tb));
         }
     }
 }
@@ -700,23 +780,24 @@ cudaError_t launch_k4(int G, int hd, dim3 g4, size_t sm4, cudaStream_t st, const
 }
 
 template <int WT>
-int launch_ffn(const DecodeArgs &a, cudaStream_t st) {
-    TLB_CUDA(launch(dec_k1<WT>, dim3(unsigned(a.n1)), size_t(a.H) * 4, st, false, a));
+int launch_ffn(const DecodeArgs &a, cudaStream_t st, bool k1_pdl) {
+    TLB_CUDA(launch(dec_k1<WT>, dim3(unsigned(a.n1)), size_t(a.H) * 4, st, k1_pdl, a));
     TLB_TRY(check_launch("decode k1"));
     const size_t sm2 = size_t(2) * (a.I / a.ns2) * 4;
     const dim3 g2(unsigned(a.n2), unsigned(a.ns2));
     if (a.act == TLB_ACT_RELU2_MUL) TLB_CUDA(launch(dec_k2<WT, TLB_ACT_RELU2_MUL>, g2, sm2, st, true, a));
     else TLB_CUDA(launch(dec_k2<WT, TLB_ACT_SILU_MUL>, g2, sm2, st, true, a));
     TLB_TRY(check_launch("decode k2"));
-    TLB_CUDA(launch(dec_k3<WT>, dim3(unsigned(a.n3), unsigned(a.ns3)), size_t(a.H / a.ns3) * 4, st, true, a));
+    TLB_CUDA(launch(dec_k3<WT>, dim3(unsigned(a.n3), unsigned(a.ns3)), (size_t(4) * (a.H / a.ns3) + a.H) * 4, st,
+                    true, a));
     TLB_TRY(check_launch("decode k3"));
     return TLB_OK;
 }
 
 int launch_attn(const DecodeArgs &a, cudaStream_t st) {
     const int G = a.nh / a.nkv;
-    const dim3 g4(a.nkv, a.nchunks);
-    const size_t sm4 = (size_t(G) * a.hd + size_t(kAWarps) * G * 2 * a.hd) * 4;
+    const dim3 g4(a.nkv, a.nchunks + 1);     // the last block of each KV head forms dV and gh_v
+    const size_t sm4 = (size_t(G) * a.hd + size_t(kAWarps) * G * 2 * a.hd + size_t(a.qd)) * 4;
     TLB_CUDA(launch_k4(G, a.hd, g4, sm4, st, a));
     TLB_TRY(check_launch("decode k4"));
     RopeFreqs fr;
@@ -738,24 +819,24 @@ bool decode_supported(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     const int E = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 8 : 16);
     const int hd = c.head_dim;
     const int gmax = hd > 128 ? 8 : 16;   // heads per KV group held in registers by k4
-    const size_t sm4 = (size_t(G) * hd + size_t(kAWarps) * G * 2 * hd) * 4;
+    const size_t sm4 = (size_t(G) * hd + size_t(kAWarps) * G * 2 * hd + size_t(c.n_heads) * hd) * 4;
     return S == 1 && G <= gmax && c.rank <= 16 && (hd == 32 || hd == 64 || hd == 128 || hd == 256) &&
            c.dim % E == 0 && c.ffn_dim % E == 0 && size_t(2) * c.ffn_dim * 4 <= 200 * 1024 &&
-           sm4 <= 200 * 1024 && L >= 1;
+           sm4 <= 200 * 1024 && size_t(5) * c.dim * 4 <= 200 * 1024 && L >= 1;
 }
 
-int decode_ffn_launch(const DecodeArgs &a, int wtype, cudaStream_t st) {
+int decode_ffn_launch(const DecodeArgs &a, int wtype, cudaStream_t st, bool k1_pdl) {
     switch (wtype) {
-        case TLB_W_F32: return launch_ffn<TLB_W_F32>(a, st);
-        case TLB_W_BF16: return launch_ffn<TLB_W_BF16>(a, st);
-        default: return launch_ffn<TLB_W_TERNARY_I8>(a, st);
+        case TLB_W_F32: return launch_ffn<TLB_W_F32>(a, st, k1_pdl);
+        case TLB_W_BF16: return launch_ffn<TLB_W_BF16>(a, st, k1_pdl);
+        default: return launch_ffn<TLB_W_TERNARY_I8>(a, st, k1_pdl);
     }
 }
 
 int decode_attn_launch(const DecodeArgs &a, cudaStream_t st) { return launch_attn(a, st); }
 
 int decode_layer_launch(const DecodeArgs &a, int wtype, cudaStream_t st) {
-    TLB_TRY(decode_ffn_launch(a, wtype, st));
+    TLB_TRY(decode_ffn_launch(a, wtype, st, false));
     return decode_attn_launch(a, st);
 }
 

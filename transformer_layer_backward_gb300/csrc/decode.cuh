@@ -93,7 +93,9 @@ int decode_layer_launch(const DecodeArgs &a, int wtype, cudaStream_t st);
 // The two halves of the chain: k1 .. k3 (dF, dN2, dR1 and dSub) and k4 .. k7 (attention,
 // dQpre, LoRA and AdamW), for callers that overlap one layer's second half with the next
 // layer's first half on another stream.
-int decode_ffn_launch(const DecodeArgs &a, int wtype, cudaStream_t st);
+// k1_pdl: launch k1 as a programmatic dependent of the kernel before it on `st` (it
+// prefetches its weights into L2, then waits for that kernel).
+int decode_ffn_launch(const DecodeArgs &a, int wtype, cudaStream_t st, bool k1_pdl);
 int decode_attn_launch(const DecodeArgs &a, cudaStream_t st);
 
 }  // namespace tlb

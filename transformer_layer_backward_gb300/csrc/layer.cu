@@ -345,14 +345,17 @@ void decode_args(const tlb_layer_cfg &c, int64_t L, const tlb_layer_weights *w, 
     d.dhid_out = d_hidden;
 }
 
+// Workspace sets of a single-token stack: layer l uses set l % kStackSets.
+constexpr int kStackSets = 4;
+
 // The second stream of a single-token stack: one per device, at the lowest priority, so
-// that the blocks of the next layer's GEMV chain go first; with its events (per layer
-// parity): e3 after a layer's k1 .. k3, e7 after its k4 .. k7.  Created on first use,
+// that the blocks of the next layer's GEMV chain go first; with its events: e3 after a
+// layer's k1 .. k3, e7[l % kStackSets] after layer l's k4 .. k7.  Created on first use,
 // which must not be inside a stream capture.
 struct SideStream {
     std::mutex mu;
     cudaStream_t s = nullptr;
-    cudaEvent_t e3[2] = {nullptr, nullptr}, e7[2] = {nullptr, nullptr};
+    cudaEvent_t e3 = nullptr, e7[kStackSets] = {};
 };
 
 int side_stream(SideStream *&out) {
@@ -367,10 +370,8 @@ int side_stream(SideStream *&out) {
         int least = 0, greatest = 0;
         TLB_CUDA(cudaDeviceGetStreamPriorityRange(&least, &greatest));
         TLB_CUDA(cudaStreamCreateWithPriority(&n->s, cudaStreamNonBlocking, least));
-        for (int i = 0; i < 2; ++i) {
-            TLB_CUDA(cudaEventCreateWithFlags(&n->e3[i], cudaEventDisableTiming));
-            TLB_CUDA(cudaEventCreateWithFlags(&n->e7[i], cudaEventDisableTiming));
-        }
+        TLB_CUDA(cudaEventCreateWithFlags(&n->e3, cudaEventDisableTiming));
+        for (int i = 0; i < kStackSets; ++i) TLB_CUDA(cudaEventCreateWithFlags(&n->e7[i], cudaEventDisableTiming));
         ss = n;
     }
     out = ss;
@@ -472,7 +473,7 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
 
 size_t tlb_stack_workspace_bytes(const tlb_layer_cfg *cfg, int64_t S, int64_t L) {
     if (cfg == nullptr || S < 0) return 0;
-    return 2 * stack_half(*cfg, S, L < S ? S : L);
+    return kStackSets * stack_half(*cfg, S, L < S ? S : L);
 }
 
 int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n_layers,
@@ -488,8 +489,8 @@ int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n
     TLB_TRY(check_adam(adam));
     const tlb_layer_cfg &c = *cfg;
     const size_t half = stack_half(c, S, L);
-    TLB_REQUIRE(ws != nullptr && ws_bytes >= 2 * half, TLB_EINVAL,
-                "stack workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, 2 * half);
+    TLB_REQUIRE(ws != nullptr && ws_bytes >= kStackSets * half, TLB_EINVAL,
+                "stack workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, kStackSets * half);
     TLB_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, TLB_EINVAL, "workspace not 256-byte aligned");
     bool pipelined = S == 1 && !(c.flags & TLB_PERSISTENT);
     for (int l = 0; l < n_layers; ++l) {
@@ -511,26 +512,29 @@ int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n
     // Single-token layers: layer l's k1 .. k3 (its dR1, the next layer's dOut) on the
     // caller's stream, its k4 .. k7 on the side stream, so that the attention and LoRA
     // half of layer l runs beside the GEMV chain of layer l - 1.  Layer l uses workspace
-    // half l % 2; before layer l's first kernel the caller's stream waits for layer l + 2's
-    // side work, the last user of that half.
+    // set l % 4, last used by layer l + 4.  Before the first kernel of each even layer l
+    // the caller's stream waits for layer l + 2's side work; the side stream is in order,
+    // so that also covers every layer above, and with it layer l + 4 for layers l and
+    // l - 1.  The k1 of the other layers starts as a programmatic dependent of the k3
+    // before it.
     cudaStream_t st = as_stream(stream);
     SideStream *side = nullptr;
     TLB_TRY(side_stream(side));
     std::lock_guard<std::mutex> lock(side->mu);
     const LayerWs p = plan(c, S, L);
-    void *halves[2] = {ws, static_cast<char *>(ws) + half};
+    auto set = [&](int l) { return static_cast<void *>(static_cast<char *>(ws) + size_t(l % kStackSets) * half); };
     for (int l = n_layers - 1; l >= 0; --l) {
-        const int par = l & 1;
-        if (l + 2 <= n_layers - 1) TLB_CUDA(cudaStreamWaitEvent(st, side->e7[par], 0));
+        const bool wait = (l % 2 == 0) && l + 2 <= n_layers - 1;
+        if (wait) TLB_CUDA(cudaStreamWaitEvent(st, side->e7[(l + 2) % kStackSets], 0));
         DecodeArgs d;
-        decode_args(c, L, &w[l], &acts[l], &lora_q[l], &lora_v[l], adam, d_hidden, sumsq, halves[par], p, d);
-        d.dout = l == n_layers - 1 ? d_hidden : ws_at<float>(halves[par ^ 1], p.dR1);
+        decode_args(c, L, &w[l], &acts[l], &lora_q[l], &lora_v[l], adam, d_hidden, sumsq, set(l), p, d);
+        d.dout = l == n_layers - 1 ? d_hidden : ws_at<float>(set(l + 1), p.dR1);
         d.dhid_out = l == 0 ? d_hidden : nullptr;
-        TLB_TRY(decode_ffn_launch(d, c.wtype, st));
-        TLB_CUDA(cudaEventRecord(side->e3[par], st));
-        TLB_CUDA(cudaStreamWaitEvent(side->s, side->e3[par], 0));
+        TLB_TRY(decode_ffn_launch(d, c.wtype, st, !wait && l < n_layers - 1));
+        TLB_CUDA(cudaEventRecord(side->e3, st));
+        TLB_CUDA(cudaStreamWaitEvent(side->s, side->e3, 0));
         TLB_TRY(decode_attn_launch(d, side->s));
-        TLB_CUDA(cudaEventRecord(side->e7[par], side->s));
+        TLB_CUDA(cudaEventRecord(side->e7[l % kStackSets], side->s));
     }
     TLB_CUDA(cudaStreamWaitEvent(st, side->e7[0], 0));   // layer 0 ends the side stream's work
     return TLB_OK;
