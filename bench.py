@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=2000)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--stack-layers", type=int, default=36,
+                   help="decode: also time the layer inside a stack of this many layers (0: skip)")
     p.add_argument("--cases", default=None,
                    help="sweep: run only the cases whose 'kernel shape' label matches this regex")
     p.add_argument("--workload", default="decode", choices=["decode", "seq512", "seq2048", "stack2048", "sweep"])
@@ -870,6 +872,50 @@ def main():
         e2e = {"value": ne * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
+    # the same layer inside a stack ([RS] backward_through_layers): args.stack_layers layer
+    # calls (weights and caches cycling the NL sets, adapters of their own) through
+    # tlb_stack_backward, which overlaps each layer's attention / LoRA half with the next
+    # layer's GEMV chain; reported per layer
+    stack = None
+    if args.stack_layers > 0:
+        NS = args.stack_layers
+        sl = []
+        for l in range(NS):
+            src = layers[l % NL]
+            L = lora_dev(src["L"])
+            sl.append(dict(L=L, w=src["w"], a=src["a"], lq=tlb.lora(L, "q"), lv=tlb.lora(L, "v")))
+        sws = tlb.stack_workspace(c, 1, cfg.cache_len)
+        sW, sA = [d["w"] for d in sl], [d["a"] for d in sl]
+        sQ, sV = [d["lq"] for d in sl], [d["lv"] for d in sl]
+        # d_in grows ~5e3 times per synthetic ternary layer: a small dOut keeps the deep
+        # layers' values finite (the work does not depend on the values)
+        sd = (layers[0]["t"]["dout"] * 1e-30).contiguous()
+
+        def sstep():
+            dh.copy_(sd)
+            tlb.stack_backward(c, 1, cfg.cache_len, sW, sA, sQ, sV, adam, dh, ss, sws)
+
+        sstep()                      # creates the library's second stream outside any capture
+        torch.cuda.synchronize()
+        sg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(sg):
+            sstep()
+        for _ in range(3):
+            sg.replay()
+        ns = max(3, min(200, args.steps // NS))
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(ns):
+            sg.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        sms = e0.elapsed_time(e1) / ns
+        tlb.workspace_status(sws)
+        stack = {"value": NS * world / (sms / 1e3), "unit": "layer tokens/s", "layers": NS,
+                 "ms_per_stack": sms, "us_per_layer": sms * 1e3 / NS, "steps": ns,
+                 "note": "one token through %d decode layers per step (tlb_stack_backward, one CUDA graph)" % NS}
+        del sl, sws
+
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         t_or, n_or = oracle_step_time(cfg, args.cpu_seconds)
@@ -896,7 +942,7 @@ def main():
                                   "peak": hbm, "unit": "GB/s",
                                   "frac": step_bytes / (ms_max / args.steps / 1e3) / 1e9 / hbm},
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk}
+                "clocks": clk, "in_stack": stack}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
