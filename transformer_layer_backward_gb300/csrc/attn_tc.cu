@@ -76,53 +76,80 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int ch) { return uint32_t(r
 
 // ------------------------------------------------------------------ prep
 
-// 32 x 32 tiles of three sources: dCtx [S, nh*hd] -> dCT;  K -> Kt;  V -> Vr.
+// 64 x 64 tiles of three sources, every value rounded to tf32:
+//   dCtx [S, nh*hd] -> dCT [nh*hd][S4] (transposed);  K -> Kt [nkv*hd][L4] (transposed);
+//   V -> Vr [nkv][L][hd].
+// Each thread loads four float4 of its tile (16-byte loads of rows of 64 floats); a
+// transposed tile goes out through shared memory, one warp writing 32 consecutive floats
+// of an output row per store, and V is written straight from the registers.  vec_kv:
+// K and V rows allow 16-byte loads (else those two load one float at a time).
+constexpr int kPrepT = 64;
 __global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dCT, float *Kt, float *Vr,
-                                                           int S4, int L4, int ntc_dc, int ntc_kv) {
-    __shared__ float tile[32][33];
+                                                           int S4, int L4, int nt_dc, int nt_kv, int vec_kv) {
+    __shared__ float tile[kPrepT][kPrepT + 1];
     const int qd = a.nh * a.hd, kvd = a.nkv * a.hd;
     int t = blockIdx.x;
     int job, rows, cols;
-    if (t < ntc_dc * ((a.S + 31) / 32)) {
+    if (t < nt_dc) {
         job = 0;
         rows = a.S;
         cols = qd;
     } else {
-        t -= ntc_dc * ((a.S + 31) / 32);
-        job = t / (ntc_kv * ((a.L + 31) / 32)) + 1;   // 1: K, 2: V
-        t %= ntc_kv * ((a.L + 31) / 32);
+        t -= nt_dc;
+        job = t / nt_kv + 1;                       // 1: K, 2: V
+        t %= nt_kv;
         rows = a.L;
         cols = kvd;
     }
-    const int nct = cols / 32;
-    const int r0 = (t / nct) * 32, c0 = (t % nct) * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    for (int rr = ty; rr < 32; rr += 8) {
-        const int r = r0 + rr, c = c0 + tx;
-        float v = 0.f;
+    const int nct = cols / kPrepT;
+    const int r0 = (t / nct) * kPrepT, c0 = (t % nct) * kPrepT;
+    const int tid = threadIdx.x;
+    float4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int e = tid + 256 * k, rr = e >> 4, c = c0 + 4 * (e & 15), r = r0 + rr;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (r < rows) {
-            if (job == 0) v = a.dctx[int64_t(r) * qd + c];
-            else {
+            if (job == 0) {
+                x = *reinterpret_cast<const float4 *>(a.dctx + int64_t(r) * qd + c);
+            } else {
                 const int kvh = c / a.hd, d = c % a.hd;
-                v = (job == 1 ? a.k : a.v)[int64_t(kvh) * a.sh + int64_t(r) * a.sp + d];
+                const float *src = (job == 1 ? a.k : a.v) + int64_t(kvh) * a.sh + int64_t(r) * a.sp + d;
+                if (vec_kv) x = *reinterpret_cast<const float4 *>(src);
+                else x = make_float4(src[0], src[1], src[2], src[3]);
             }
         }
-        v = __uint_as_float(to_tf32(v));
-        tile[rr][tx] = v;
-        if (r < rows) {
-            const int hh = c / a.hd, d = c % a.hd;
-            if (job == 2) Vr[(int64_t(hh) * a.L + r) * a.hd + d] = v;
-        }
+        v[k] = make_float4(__uint_as_float(to_tf32(x.x)), __uint_as_float(to_tf32(x.y)),
+                           __uint_as_float(to_tf32(x.z)), __uint_as_float(to_tf32(x.w)));
     }
-    if (job == 2) return;
+    if (job == 2) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int e = tid + 256 * k, rr = e >> 4, c = c0 + 4 * (e & 15), r = r0 + rr;
+            if (r < rows) {
+                const int hh = c / a.hd, d = c % a.hd;
+                *reinterpret_cast<float4 *>(Vr + (int64_t(hh) * a.L + r) * a.hd + d) = v[k];
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int e = tid + 256 * k, rr = e >> 4, cc = 4 * (e & 15);
+        tile[rr][cc] = v[k].x;
+        tile[rr][cc + 1] = v[k].y;
+        tile[rr][cc + 2] = v[k].z;
+        tile[rr][cc + 3] = v[k].w;
+    }
     __syncthreads();
-    // transposed: row = column c0 + cc (head, d), column = r0 + tx
-    for (int cc = ty; cc < 32; cc += 8) {
-        const int c = c0 + cc, r = r0 + tx;
-        if (r >= rows) continue;
-        const int hh = c / a.hd, d = c % a.hd;
-        if (job == 0) dCT[(int64_t(hh) * a.hd + d) * S4 + r] = tile[tx][cc];
-        else Kt[(int64_t(hh) * a.hd + d) * L4 + r] = tile[tx][cc];
+    // transposed: output row c0 + cc (head, d), columns r0 + 0 .. 63; lane = column
+    float *dst = job == 0 ? dCT : Kt;
+    const int ld = job == 0 ? S4 : L4;
+    const int lane = tid & 31, w = tid >> 5;
+#pragma unroll 4
+    for (int k = 0; k < (kPrepT * kPrepT) / 256; ++k) {
+        const int cc = w + 8 * (k >> 1), rr = lane + 32 * (k & 1), r = r0 + rr;
+        if (r < rows) dst[int64_t(c0 + cc) * ld + r] = tile[rr][cc];
     }
 }
 
@@ -632,9 +659,11 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     char *base = static_cast<char *>(scratch);
     float *dCT = reinterpret_cast<float *>(base + w.dCT);
     float *Kt = reinterpret_cast<float *>(base + w.Kt), *Vr = reinterpret_cast<float *>(base + w.Vr);
-    const int ntc_dc = a.nh * HD / 32, ntc_kv = a.nkv * HD / 32;
-    const int64_t nblk = int64_t(ntc_dc) * ceil_div(a.S, 32) + 2 * int64_t(ntc_kv) * ceil_div(a.L, 32);
-    attn_tc_prep_kernel<<<unsigned(nblk), 256, 0, st>>>(a, dCT, Kt, Vr, int(w.S4), int(w.L4), ntc_dc, ntc_kv);
+    const int nt_dc = int(ceil_div(a.S, kPrepT)) * (a.nh * HD / kPrepT);
+    const int nt_kv = int(ceil_div(a.L, kPrepT)) * (a.nkv * HD / kPrepT);
+    const int vec_kv = aligned16(a.k) && aligned16(a.v) && a.sh % 4 == 0 && a.sp % 4 == 0;
+    attn_tc_prep_kernel<<<unsigned(nt_dc + 2 * nt_kv), 256, 0, st>>>(a, dCT, Kt, Vr, int(w.S4), int(w.L4), nt_dc,
+                                                                    nt_kv, vec_kv);
     TLB_TRY(check_launch("attn_tc_prep"));
 
     AttnTcParams p;
