@@ -18,6 +18,8 @@
 //     Every sum runs in a fixed order: the result does not depend on scheduling.
 #include <algorithm>
 
+#include <mutex>
+
 #include "async.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
@@ -411,6 +413,21 @@ __global__ void __launch_bounds__(256) lora_gpass16_kernel(LoraSeqArgs a) {
     }
 }
 
+// sum_{k < n} p[k * stride] in index order, eight loads in flight at a time.
+__device__ __forceinline__ float ordered_sum(const float *p, int n, int64_t stride) {
+    float acc = 0.f;
+    int k = 0;
+    for (; k + 8 <= n; k += 8) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = p[int64_t(k + j) * stride];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc += v[j];
+    }
+    for (; k < n; ++k) acc += p[int64_t(k) * stride];
+    return acc;
+}
+
 __global__ void __launch_bounds__(256) lora_gh_sum_kernel(LoraSeqArgs a) {
     const int64_t n = int64_t(a.S) * a.rank;
     int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -421,9 +438,7 @@ __global__ void __launch_bounds__(256) lora_gh_sum_kernel(LoraSeqArgs a) {
     }
     if (side >= a.nside || e >= n) return;
     const LoraSide &p = a.side[side];
-    float acc = 0.f;
-    for (int ot = 0; ot < p.n_ot; ++ot) acc += p.part_gh[int64_t(ot) * n + e];
-    p.gh[e] = p.s * acc;
+    p.gh[e] = p.s * ordered_sum(p.part_gh + e, p.n_ot, n);
 }
 
 // Block (column tile of x, chunk of row tiles): one pass over its x tiles, staged two
@@ -579,8 +594,7 @@ __global__ void __launch_bounds__(256) lora_seq_adamw_kernel(LoraSeqArgs a, Adam
         const int64_t nA = int64_t(a.rank) * a.C, nB = int64_t(p.O) * a.rank;
         if (e < 0) break;
         if (e < nA) {
-            float g = 0.f;
-            for (int rt = 0; rt < a.nrc_a; ++rt) g += p.part_a[int64_t(rt) * nA + e];
+            const float g = ordered_sum(p.part_a + e, a.nrc_a, nA);
             if (p.l.grad_a) p.l.grad_a[e] = g;
             float m = p.l.m_a[e], v = p.l.v_a[e];
             p.l.a[e] = adam_elem(p.l.a[e], g, m, v, ka);
@@ -590,9 +604,7 @@ __global__ void __launch_bounds__(256) lora_seq_adamw_kernel(LoraSeqArgs a, Adam
             e = -1;
         } else if (e < nA + nB) {
             const int64_t f = e - nA;
-            float g = 0.f;
-            for (int rt = 0; rt < a.nrc_b; ++rt) g += p.part_b[int64_t(rt) * nB + f];
-            g *= p.s;
+            const float g = p.s * ordered_sum(p.part_b + f, a.nrc_b, nB);
             if (p.l.grad_b) p.l.grad_b[f] = g;
             float m = p.l.m_b[f], v = p.l.v_b[f];
             p.l.b[f] = adam_elem(p.l.b[f], g, m, v, kb);
@@ -644,6 +656,32 @@ int lora_seq_run(LoraSeqArgs a, int n_ot_total, const AdamCoef &ka, const AdamCo
     a.nrc_a = int(ceil_div(a.n_rt, a.tpc_a));
     const size_t smg = size_t(2 * kLT * kLP + 2 * kLT * RB + kLO * RB) * 4;
     const size_t smx = size_t(2 * kLT * kLP + 4 * kLT * RB) * 4;
+    // two blocks per SM need the largest shared-memory carveout (the default split may
+    // leave room for one, which turns each pass into two waves)
+    {
+        static std::once_flag once;
+        cudaError_t err = cudaSuccess;
+        std::call_once(once, [&] {
+            const void *ks[] = {reinterpret_cast<const void *>(lora_gpass_kernel<4>),
+                                reinterpret_cast<const void *>(lora_gpass_kernel<8>),
+                                reinterpret_cast<const void *>(lora_gpass_kernel<16>),
+                                reinterpret_cast<const void *>(lora_gpass_kernel<32>),
+                                reinterpret_cast<const void *>(lora_gpass_kernel<64>),
+                                reinterpret_cast<const void *>(lora_xpass_kernel<4>),
+                                reinterpret_cast<const void *>(lora_xpass_kernel<8>),
+                                reinterpret_cast<const void *>(lora_xpass_kernel<16>),
+                                reinterpret_cast<const void *>(lora_xpass_kernel<32>),
+                                reinterpret_cast<const void *>(lora_xpass_kernel<64>),
+                                reinterpret_cast<const void *>(lora_gpass16_kernel),
+                                reinterpret_cast<const void *>(lora_xpass16_kernel)};
+            for (const void *k : ks) {
+                const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                           int(cudaSharedmemCarveoutMaxShared));
+                if (e != cudaSuccess && err == cudaSuccess) err = e;
+            }
+        });
+        TLB_CUDA(err);
+    }
     if (smg > 48 * 1024)
         TLB_CUDA(cudaFuncSetAttribute(lora_gpass_kernel<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smg)));
     if (smx > 48 * 1024) {
