@@ -429,8 +429,12 @@ int launch_tc(const TcParams &p, cudaStream_t st) {
 TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
     // 128 x 256 or 128 x 128 tiles on persistent CTAs.  Candidates: `dp` whole tiles per
     // CTA, the remaining tiles shared stream-K style by the `ctas` CTAs.
-    // Cost: the busiest CTA's k blocks (one 128 x BN x 64 MMA block each), plus the
-    // partial-tile traffic and a fixup launch when tiles are shared.  Plans are cached.
+    // Cost: the busiest CTA's k blocks (one 128 x BN x 64 MMA block each, at the rate
+    // these kernels reach: 128-wide tiles about 1.4 times slower per flop), plus 8 us
+    // per stream-K segment of the busiest CTA (each ends in a TMEM drain into a partial
+    // tile), the partial-tile traffic and a fixup launch when tiles are shared.  The
+    // constants are fitted to measured plans of the S = 512 and S = 2048 layer products:
+    // an even split (every CTA inside one tile) beats a finer uneven one.  Plans are cached.
     static std::mutex mu;
     static std::map<std::tuple<int64_t, int64_t, int64_t, int>, TcPlan> cache;
     const int nsm = num_sms();
@@ -446,7 +450,7 @@ TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
         if (bn == 256 && N <= 128) continue;
         const int64_t tiles = ceil_div(N, bn) * ceil_div(M, kBM), KB = ceil_div(K, kBK);
         // s per k block; 128-wide tiles fetch A twice as often per flop
-        const double t_kb = 2.0 * kBM * bn * kBK / (1.6e15 / nsm) * (bn == 128 ? 1.15 : 1.0);
+        const double t_kb = 2.0 * kBM * bn * kBK / (1.3e15 / nsm) * (bn == 128 ? 1.4 : 1.0);
         const double tile_io = 2.0 * kBM * bn * 4 / 6.0e12;                // s per partial tile written + read
         auto consider = [&](int64_t ctas, int64_t dp) {
             if (ctas < 1 || ctas > nsm || dp < 0 || dp * ctas > tiles) return;
@@ -454,8 +458,13 @@ TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
             int64_t shared = 0;
             for (int64_t c = 1; c < ctas && skw > 0; ++c)
                 if (sk_start(skw, int(ctas), int(c)) % KB != 0) ++shared;
-            const double cost =
-                double(dp * KB + ceil_div(skw, ctas)) * t_kb + (shared > 0 ? 2.0 * shared * tile_io + 3e-6 : 0.0);
+            int64_t segs = 0;   // stream-K segments of the busiest CTA
+            for (int64_t c = 0; c < ctas && skw > 0; ++c) {
+                const int64_t a = sk_start(skw, int(ctas), int(c)), b = sk_start(skw, int(ctas), int(c + 1));
+                if (b > a) segs = std::max<int64_t>(segs, (b - 1) / KB - a / KB + 1);
+            }
+            const double cost = double(dp * KB + ceil_div(skw, ctas)) * t_kb + double(segs) * 8e-6 +
+                                (shared > 0 ? 2.0 * shared * tile_io + 3e-6 : 0.0);
             if (cost < best_cost) {
                 best_cost = cost;
                 best = TcPlan{bn, int(ctas), int(dp), int(shared)};
