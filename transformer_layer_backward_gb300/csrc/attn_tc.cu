@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
         mbar_init(&dcready, kEpiWarps);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&afull[b], kEpiWarps);
+            mbar_init(&afull[b], kEpiWarps / 2);    // the four warps of the group that forms E_j
             mbar_init(&afree[b], 1);
         }
         mbar_init(&ufull, 1);
@@ -294,9 +294,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
             mbar_wait(&ufull, 0, nullptr, 0u);
         }
     } else {
-        // ------------------------------------------------ epilogue: one query row and half of
-        // the key columns per thread (two warps per TMEM lane quarter)
-        constexpr int HK = kQK / 2;
+        // ------------------------------------------------ epilogue: two groups of four warps (one
+        // per TMEM lane quarter), one query row per thread
         const int quarter = warp & 3, hf = (warp - 2) >> 2;
         const int r = quarter * 32 + lane, i = q0 + r;
         const bool row_ok = i < p.S;
@@ -323,37 +322,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
             __syncwarp();
             if (lane == 0) mbar_arrive(&dcready);
         }
+        // Key tiles alternate between the two groups of four warps (group hf takes the tiles
+        // j = hf mod 2 and with them T / E buffer hf), each thread one query row and all of
+        // the tile's columns, so that one group forms E_j while the other forms E_j+1.
         float D = 0.f;
         bool ok = true;
-        for (int j = 0; j < nt; ++j) {
-            const int s = j % kQSlots, k0 = j * kQK + hf * HK;
+        for (int j = hf; j < nt; j += 2) {
+            const int s = j % kQSlots, k0 = j * kQK;
             if (!mbar_wait(&kfull[s], (j / kQSlots) & 1, p.status, 26u) ||
                 !mbar_wait(&tfull[j & 1], (j >> 1) & 1, p.status, 27u)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t t[HK];
-            tmem_ld16(tmem + Ly::TT + uint32_t((j & 1) * kQK + hf * HK) + lane_off, t);
+            uint32_t t[kQK];
+            tmem_ld32(tmem + Ly::TT + uint32_t((j & 1) * kQK) + lane_off, t);
             const uint8_t *pt = sm + Ly::P(s);
-            float pv[HK];
+            float pv[kQK];
 #pragma unroll
-            for (int ch = 0; ch < HK / 4; ++ch) {
-                const float4 v = *reinterpret_cast<const float4 *>(pt + sw128_off(r, hf * (HK / 4) + ch));
+            for (int ch = 0; ch < kQK / 4; ++ch) {
+                const float4 v = *reinterpret_cast<const float4 *>(pt + sw128_off(r, ch));
                 pv[4 * ch] = v.x;
                 pv[4 * ch + 1] = v.y;
                 pv[4 * ch + 2] = v.z;
                 pv[4 * ch + 3] = v.w;
             }
-            const bool diag = k0 + HK - 1 > jlast;              // masked keys in this half row
+            const bool diag = k0 + kQK - 1 > jlast;             // masked keys in this row of the tile
             if (diag) {
 #pragma unroll
-                for (int c = 0; c < HK; ++c)
+                for (int c = 0; c < kQK; ++c)
                     if (k0 + c > jlast) pv[c] = 0.f;
             }
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < HK; ++c) {
+            for (int c = 0; c < kQK; ++c) {
                 const float e = pv[c] * __uint_as_float(t[c]);
                 D += e;
                 t[c] = to_tf32(e);
@@ -362,8 +364,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
             // keys of a diagonal tile are zeroed in place
             if (diag) {
 #pragma unroll
-                for (int ch = 0; ch < HK / 4; ++ch)
-                    st_shared_v4(sm + Ly::P(s) + sw128_off(r, hf * (HK / 4) + ch), __float_as_uint(pv[4 * ch]),
+                for (int ch = 0; ch < kQK / 4; ++ch)
+                    st_shared_v4(sm + Ly::P(s) + sw128_off(r, ch), __float_as_uint(pv[4 * ch]),
                                  __float_as_uint(pv[4 * ch + 1]), __float_as_uint(pv[4 * ch + 2]),
                                  __float_as_uint(pv[4 * ch + 3]));
                 fence_proxy_async();
@@ -371,13 +373,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
             // E (tf32) into tensor memory once the U product of tile j - 2 is done with the buffer
             if (j >= 2 && !mbar_wait(&afree[j & 1], ((j - 2) >> 1) & 1, p.status, 28u)) { ok = false; break; }
             tc_fence_after();
-            tmem_st16(tmem + Ly::TE + uint32_t((j & 1) * kQK + hf * HK) + lane_off, t);
+            tmem_st32(tmem + Ly::TE + uint32_t((j & 1) * kQK) + lane_off, t);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&afull[j & 1]);
         }
-        // D of the row: the two column halves meet in shared memory
+        // D of the row: the two groups' shares meet in shared memory
         __shared__ float sD[2][kQM];
         sD[hf][r] = D;
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
