@@ -291,12 +291,6 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
     // [sR (swizzled dR1) | sDo | sGam | sR1] over the range (nc floats each), then sGR over H
     float *sR = reinterpret_cast<float *>(sm4);
     float4 *sDo = sm4 + n4, *sGam = sm4 + 2 * n4, *sR1 = sm4 + 3 * n4, *sGR = sm4 + 4 * n4;
-    {
-        constexpr int ES = 16 / EPC<WT>::v;
-        const int lane = threadIdx.x & 31, r = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR + lane;
-        if (lane < kR && r < a.qd)
-            prefetch_l2(reinterpret_cast<const char *>(a.w_o) + (size_t(r) * a.H + c0) * ES, size_t(nc) * ES);
-    }
     pdl_trigger();
     const bool pre = a.flags & TLB_PRE_NORM, resid = a.flags & TLB_RESIDUAL;
     // Before the wait: gamma_ffn * r1 over all H and sum r1^2 (the pre-norm sums need all
@@ -316,6 +310,13 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
         sDo[i] = resid ? reinterpret_cast<const float4 *>(a.dout + c0)[i] : z;
         sGam[i] = pre ? reinterpret_cast<const float4 *>(a.g_ffn + c0)[i] : z;
         sR1[i] = pre ? reinterpret_cast<const float4 *>(a.r1 + c0)[i] : z;
+    }
+    {   // this block's W_O rows into L2, after the staging loads above (so they do not queue
+        // behind this prefetch while the previous kernel still streams its weights)
+        constexpr int ES = 16 / EPC<WT>::v;
+        const int lane = threadIdx.x & 31, r = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR + lane;
+        if (lane < kR && r < a.qd)
+            prefetch_l2(reinterpret_cast<const char *>(a.w_o) + (size_t(r) * a.H + c0) * ES, size_t(nc) * ES);
     }
     pdl_wait();
     // After the wait: dN2 (one round of loads), the pre-norm coefficients, dR1 over the range.
@@ -836,7 +837,9 @@ int decode_ffn_launch(const DecodeArgs &a, int wtype, cudaStream_t st, bool k1_p
 int decode_attn_launch(const DecodeArgs &a, cudaStream_t st) { return launch_attn(a, st); }
 
 int decode_layer_launch(const DecodeArgs &a, int wtype, cudaStream_t st) {
-    TLB_TRY(decode_ffn_launch(a, wtype, st, false));
+    // k1 too starts as a programmatic dependent of whatever kernel precedes the call: before
+    // its wait it only prefetches its W_down rows into L2
+    TLB_TRY(decode_ffn_launch(a, wtype, st, true));
     return decode_attn_launch(a, st);
 }
 
