@@ -65,7 +65,9 @@ extern "C" {
 #define TLB_PRE_NORM 2         /* RMSNorm before the FFN; its backward adds into dResidual */
 #define TLB_RESIDUAL 4         /* r1 = x + attn and out = r1 + ffn */
 #define TLB_ROPE 8             /* NeoX split-half rotary embedding on q and k */
-#define TLB_USE_SILU_CACHE 16  /* SwiGLU: read the cached silu(gate) instead of recomputing it */
+#define TLB_USE_SILU_CACHE 16  /* SwiGLU: silu_gate holds silu(gate) and may be read instead of
+                                  recomputing it (the fused tensor-core W_down^T epilogue, bound
+                                  by its loads, recomputes it all the same) */
 #define TLB_CAUSAL 32          /* query row i sees keys j <= L - S + i only; attn is 0 elsewhere */
 #define TLB_PERSISTENT 64      /* single-token layers: one persistent cooperative kernel (TMA-streamed
                                   weights, grid barriers) instead of the multi-kernel schedule */
@@ -110,7 +112,7 @@ typedef struct {
     const float *x;          /* attention input (normalised) [S, dim]: LoRA input */
     const float *gate;       /* [S, ffn_dim] */
     const float *up;         /* [S, ffn_dim] */
-    const float *silu_gate;  /* [S, ffn_dim], read if TLB_USE_SILU_CACHE */
+    const float *silu_gate;  /* [S, ffn_dim] = silu(gate), may be read if TLB_USE_SILU_CACHE */
     const float *hidden;     /* FFN hidden before the sub-norm [S, ffn_dim], TLB_SUB_NORM */
     const float *r1;         /* residual stream before the FFN norm [S, dim], TLB_PRE_NORM */
     const float *ctx;        /* attention context before the sub-norm [S, q_dim], TLB_SUB_NORM */
