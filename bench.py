@@ -305,10 +305,17 @@ def seq_main(args, rank, world, local, dist):
         ly = layers[j % NL]
         tlb.layer_backward(c, S, L, ly["w"], ly["a"], ly["lq"], ly["lv"], adam, dh, ss, ws)
 
+    if depth > 1:
+        # the stack entry point, layer l of the stack being distinct layer l % NL
+        sws = tlb.stack_workspace(c, S, L)
+        sW, sA, sQ, sV = ([layers[l % NL][k] for l in range(depth)] for k in ("w", "a", "lq", "lv"))
+
     def step(i):
         dh.copy_(layers[i % NL]["t"]["dout"])
-        for j in range(depth):
-            layer_call(i * depth + j)
+        if depth > 1:
+            tlb.stack_backward(c, S, L, sW, sA, sQ, sV, adam, dh, ss, sws)
+        else:
+            layer_call(i)
 
     graphs = None
     if not args.no_graph:
@@ -438,7 +445,8 @@ def seq_main(args, rank, world, local, dist):
     if rank == 0:
         wl = {"seq512": "sequence layer backward S = L = 512",
               "seq2048": "sequence layer backward S = L = 2048",
-              "stack2048": "36-layer stack backward, S = L = 2048 (one step = 36 layer calls)"}[args.workload]
+              "stack2048": "36-layer stack backward, S = L = 2048 (one step = one tlb_stack_backward call "
+                           "over 36 layers)"}[args.workload]
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (device generator)",

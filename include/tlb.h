@@ -286,14 +286,17 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L,
  * turn on the same d_hidden, up to the order of float atomic additions.
  *   w, acts, lora_q, lora_v: host arrays of n_layers structs, entry l for layer l.
  *   d_hidden [S, dim] in/out: the top layer's dOut on entry, layer 0's d_in on return.
- *   ws: tlb_stack_workspace_bytes(cfg, S, L) bytes, 256-byte aligned, zero-filled once.
+ *   ws: tlb_stack_workspace_bytes(cfg, S, L) bytes, 256-byte aligned, zero-filled once
+ *   (four layer workspaces for S = 1, one for S > 1).
  * Single-token layers (S = 1 on the single-token path) overlap: layer l's attention,
  * LoRA and AdamW kernels run on a second, lower-priority stream of the library beside
  * layer l - 1's FFN and O-projection kernels, and `stream` joins that stream before the
  * call's work ends.  The second stream and its events are created on the first such call
  * on each device, which must therefore not be made inside a stream capture; later calls
  * may be captured.  Calls that share that device's second stream are serialised on the
- * host.  Other layers run one after another on `stream`.  Errors as tlb_layer_backward;
+ * host.  Other layers run one after another on `stream`; with bf16 weights and S > 1 each
+ * layer's first product reads the bf16 copy of d_in that the layer above left in the
+ * workspace instead of converting d_hidden again.  Errors as tlb_layer_backward;
  * n_layers = 0 or S = 0 is a no-op. */
 size_t tlb_stack_workspace_bytes(const tlb_layer_cfg *cfg, int64_t S, int64_t L);
 int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n_layers,

@@ -8,7 +8,7 @@ import pytest
 
 from oracle import layer as OL
 from synth import DECODE, TINY, layer_inputs
-from tests.helpers import adam_to_abi, cfg_to_abi, check, host, lora_dev, to_dev
+from tests.helpers import BF16_REL_L2, adam_to_abi, cfg_to_abi, check, host, lora_dev, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -107,3 +107,44 @@ def test_sequence_stack_runs_layers_in_turn(lib):
     for l in range(3):
         for p in ("a_q", "b_q", "a_v", "b_v"):
             check("layer %d %s" % (l, p), host(devs[l]["L"][p]), ref["layers"][l][p])
+
+
+def test_sequence_tensor_core_stack(lib):
+    """bf16 layers with S > 1: each layer's first product takes the bf16 copy of d_in that
+    the layer above left in the workspace.  Against the oracle's stack, and bit for bit
+    against the same layers called one at a time (which convert d_hidden themselves)."""
+    import torch
+    from synth import SEQ512
+    n_layers = 3
+    cfg = SEQ512.with_(name="seq_stack", dim=512, ffn_dim=1024, n_heads=8, n_kv_heads=2, head_dim=64, rank=8,
+                       lora_alpha=16.0, seq_len=200, cache_len=200, n_layers=n_layers)
+    layers = [layer_inputs(cfg, layer=l, seed=4, with_dout=(l == n_layers - 1)) for l in range(n_layers)]
+    dout = layers[-1]["dout"]
+    ref = OL.stack_backward(cfg, layers, dout)
+    c = cfg_to_abi(lib, cfg)
+    adam = adam_to_abi(lib, cfg)
+    a, b = device_stack(lib, cfg, layers), device_stack(lib, cfg, layers)
+    S, L = cfg.seq_len, cfg.cache_len
+    ws_s = lib.stack_workspace(c, S, L)
+    ws_l = lib.workspace(c, S, L)
+    dh_s = torch.from_numpy(dout).cuda()
+    dh_l = dh_s.clone()
+    ss_s = torch.zeros(2, dtype=torch.float64, device="cuda")
+    ss_l = torch.zeros(2, dtype=torch.float64, device="cuda")
+    lib.stack_backward(c, S, L, [d["w"] for d in a], [d["a"] for d in a], [d["lq"] for d in a],
+                       [d["lv"] for d in a], adam, dh_s, ss_s, ws_s)
+    for l in reversed(range(n_layers)):
+        lib.layer_backward(c, S, L, b[l]["w"], b[l]["a"], b[l]["lq"], b[l]["lv"], adam, dh_l, ss_l, ws_l)
+    lib.workspace_status(ws_s)
+    lib.workspace_status(ws_l)
+    np.testing.assert_array_equal(host(dh_s), host(dh_l))
+    for l in range(n_layers):
+        for k in ("a_q", "b_q", "a_v", "b_v"):
+            np.testing.assert_array_equal(host(a[l]["L"][k]), host(b[l]["L"][k]))
+    tol = BF16_REL_L2 * np.sqrt(n_layers)
+    check("stack d_in", host(dh_s), ref["d_in"], tol, None)
+    for l in range(n_layers):
+        for p in ("a_q", "b_q", "a_v", "b_v"):
+            check("layer %d %s" % (l, p), host(a[l]["L"][p]), ref["layers"][l][p], tol, None)
+    gnorm = float(np.sqrt(ss_s[0].item()))
+    assert abs(gnorm - ref["gnorm"]) <= 2 * tol * ref["gnorm"]

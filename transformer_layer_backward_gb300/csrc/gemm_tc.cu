@@ -15,9 +15,10 @@
 //               frees each stage and, after a segment's last block, hands the
 //               accumulator over
 //   warps 2..9  epilogue: tcgen05.ld 32x32b.x32 (two warps per 32 TMEM lanes = rows, each
-//               half of the columns),
-//               scale, optional accumulate into C, fp32 stores, then release the
-//               accumulator, so one segment's epilogue overlaps the next one's MMAs
+//               half of the columns); each 32 x 32 block turns in shared memory so that
+//               lanes run along columns; scale, optional accumulate into C, coalesced fp32
+//               (and optional bf16) stores, then release the accumulator, so one segment's
+//               epilogue overlaps the next one's MMAs
 // K may come from two segments (A0.B0^T + A1.B1^T, e.g. [dG | dU] . [W_gate | W_up]^T).
 // Work is balanced stream-K style: the (tile, k block) iterations are split evenly over
 // the CTAs; a tile done by one CTA is written by it, a tile shared by several is summed
@@ -54,6 +55,7 @@ struct TcParams {
     int M, N;
     float alpha;
     float *out;                          // [M, N] fp32
+    uint2 *obf;                          // mode 0: [M, N] bf16 copy of out (four per uint2), or null
     int accumulate;
     float *partial;                      // [ctas][2][kBM * BN] fp32 partial tiles
     // epilogue: mode 0 writes out (+)= alpha acc; mode 1 treats alpha acc as dh and writes
@@ -93,6 +95,7 @@ __device__ __forceinline__ void emit4(const TcParams &p, int row, int col, float
             y.x += c.x; y.y += c.y; y.z += c.z; y.w += c.w;
         }
         *reinterpret_cast<float4 *>(p.out + e) = y;
+        if (p.obf != nullptr) p.obf[e / 4] = pack_bf16x4(y.x, y.y, y.z, y.w);
         return;
     }
     const float4 g = ld_stream(reinterpret_cast<const float4 *>(p.gate + e));
@@ -157,6 +160,49 @@ __device__ __forceinline__ void act_block(const TcParams &p, int rbase, int col0
     if (p.act == TLB_ACT_RELU2_MUL) act_block_t<TLB_ACT_RELU2_MUL, false>(p, rbase, col0, blk, lane);
     else if (p.act_cache) act_block_t<TLB_ACT_SILU_MUL, true>(p, rbase, col0, blk, lane);
     else act_block_t<TLB_ACT_SILU_MUL, false>(p, rbase, col0, blk, lane);
+}
+
+// Plain epilogue of a warp's 32 x 32 block staged in shared memory (blk[r * 33 + c], before
+// alpha): out (+)= alpha acc and the optional bf16 copy, with lanes along the columns
+// (8 column quads x 4 rows per access), so every load and store is coalesced.
+__device__ __forceinline__ void out_block(const TcParams &p, int rbase, int col0, const float *blk, int lane) {
+    const int c4 = (lane & 7) * 4, rl = lane >> 3;
+    const bool col_ok = col0 + c4 < p.N;                  // N % 4 == 0: the quad is whole
+#pragma unroll 1
+    for (int k0 = 0; k0 < 8; k0 += 4) {                   // four loads of C in flight
+        float4 c[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = 4 * (k0 + k) + rl;
+            c[k] = (p.accumulate && col_ok && rbase + r < p.M)
+                       ? *reinterpret_cast<const float4 *>(p.out + int64_t(rbase + r) * p.N + col0 + c4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = 4 * (k0 + k) + rl;
+            if (!col_ok || rbase + r >= p.M) continue;
+            const float *a = blk + r * 33 + c4;
+            float4 y = make_float4(p.alpha * a[0], p.alpha * a[1], p.alpha * a[2], p.alpha * a[3]);
+            if (p.accumulate) {
+                y.x += c[k].x; y.y += c[k].y; y.z += c[k].z; y.w += c[k].w;
+            }
+            const int64_t e = int64_t(rbase + r) * p.N + col0 + c4;
+            *reinterpret_cast<float4 *>(p.out + e) = y;
+            if (p.obf != nullptr) p.obf[e / 4] = pack_bf16x4(y.x, y.y, y.z, y.w);
+        }
+    }
+}
+
+// A warp's 32 x 32 block of a partial tile (rows of BN floats), from shared memory, coalesced.
+__device__ __forceinline__ void partial_block(float *o, int ld, const float *blk, int lane) {
+    const int c4 = (lane & 7) * 4, rl = lane >> 3;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int r = 4 * k + rl;
+        const float *a = blk + r * 33 + c4;
+        *reinterpret_cast<float4 *>(o + int64_t(r) * ld + c4) = make_float4(a[0], a[1], a[2], a[3]);
+    }
 }
 
 template <int BN>
@@ -291,41 +337,26 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                 break;
             }
             tc_fence_after();
-            const int row = m0 + q * 32 + lane;
             const int half = (warp - 2) >> 2;     // this warp's half of the tile's columns
             for (int j = half * (BN / 64); j < (half + 1) * (BN / 64); ++j) {
                 uint32_t v[32];
                 tmem_ld32(tmem + uint32_t(b * BN) + (uint32_t(q * 32) << 16) + uint32_t(j * 32), v);
                 tmem_wait_ld();
                 const int col0 = n0 + j * 32;
-                if (!whole) {
-                    // partial tile of this CTA, tile-local [kBM][BN]
-                    float *o = p.partial + ((int64_t(blockIdx.x) * 2 + slot) * kBM + q * 32 + lane) * BN + j * 32;
+                // the warp's 32 x 32 block (one row per lane) goes through shared memory so
+                // that lanes run along columns and every global access is coalesced
+                float *blk = ep + (warp - 2) * 32 * 33;
 #pragma unroll
-                    for (int t = 0; t < 32; t += 4)
-                        *reinterpret_cast<float4 *>(o + t) = make_float4(
-                            __uint_as_float(v[t]), __uint_as_float(v[t + 1]), __uint_as_float(v[t + 2]),
-                            __uint_as_float(v[t + 3]));
-                    continue;
-                }
-                if (p.mode == 1) {
-                    // activation epilogue: the warp's 32 x 32 block goes through shared memory
-                    // so that lanes run along columns and every global access is coalesced
-                    float *blk = ep + (warp - 2) * 32 * 33;
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) blk[lane * 33 + t] = __uint_as_float(v[t]);
-                    __syncwarp();
+                for (int t = 0; t < 32; ++t) blk[lane * 33 + t] = __uint_as_float(v[t]);
+                __syncwarp();
+                if (!whole)         // partial tile of this CTA, tile-local [kBM][BN]
+                    partial_block(p.partial + ((int64_t(blockIdx.x) * 2 + slot) * kBM + q * 32) * BN + j * 32, BN,
+                                  blk, lane);
+                else if (p.mode == 1)
                     act_block(p, m0 + q * 32, col0, blk, lane);
-                    __syncwarp();
-                    continue;
-                }
-                if (row >= p.M || col0 >= p.N) continue;
-#pragma unroll
-                for (int t = 0; t < 32; t += 4)                 // N % 4 == 0 (tc_supported)
-                    if (col0 + t < p.N)
-                        emit4(p, row, col0 + t,
-                              make_float4(__uint_as_float(v[t]), __uint_as_float(v[t + 1]),
-                                          __uint_as_float(v[t + 2]), __uint_as_float(v[t + 3])));
+                else
+                    out_block(p, m0 + q * 32, col0, blk, lane);
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
@@ -504,7 +535,7 @@ bool tc_supported(int64_t M, int64_t N, int64_t K) {
 }
 
 int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, float *out, bool accumulate,
-            float *partial, uint32_t *status, cudaStream_t st, const TcActEpilogue *act) {
+            float *partial, uint32_t *status, cudaStream_t st, const TcActEpilogue *act, void *out_bf16) {
     TLB_REQUIRE(nseg == 1 || nseg == 2, TLB_EINVAL, "tcgen05 GEMM: 1 or 2 K segments");
     const int64_t K = seg[0].K + (nseg > 1 ? seg[1].K : 0);
     const TcPlan pl = tc_plan(M, N, K);
@@ -515,8 +546,10 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
                         aligned16(act->dgate) && aligned16(act->dup) && (!cache || aligned16(act->silu_gate)),
                     TLB_EUNSUPPORTED, "tcgen05 GEMM: activation epilogue operands");
     } else {
-        TLB_REQUIRE(aligned16(out), TLB_EUNSUPPORTED, "tcgen05 GEMM: output alignment");
+        TLB_REQUIRE(aligned16(out) && (out_bf16 == nullptr || aligned16(out_bf16)), TLB_EUNSUPPORTED,
+                    "tcgen05 GEMM: output alignment");
     }
+    TLB_REQUIRE(act == nullptr || out_bf16 == nullptr, TLB_EINVAL, "tcgen05 GEMM: bf16 copy of an activation epilogue");
     TcParams p;
     memset(&p, 0, sizeof(p));
     for (int i = 0; i < nseg; ++i) {
@@ -531,6 +564,7 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
     p.N = int(N);
     p.alpha = alpha;
     p.out = out;
+    p.obf = static_cast<uint2 *>(out_bf16);
     p.accumulate = accumulate ? 1 : 0;
     p.partial = partial;
     if (act != nullptr) {

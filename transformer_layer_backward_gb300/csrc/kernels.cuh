@@ -51,8 +51,10 @@ struct TcActEpilogue {
     const float *gate, *up, *silu_gate;   // [M, N] fp32; silu_gate may be NULL (recomputed)
     void *dgate, *dup;                    // [M, N] bf16
 };
+// out_bf16 (optional, no activation epilogue): [M, N] bf16 copy of every value stored to out.
 int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, float *out, bool accumulate,
-            float *partial, uint32_t *status, cudaStream_t st, const TcActEpilogue *act = nullptr);
+            float *partial, uint32_t *status, cudaStream_t st, const TcActEpilogue *act = nullptr,
+            void *out_bf16 = nullptr);
 // gated-activation backward writing bf16 dG, dU (rowwise.cu)
 int act_backward_bf16_launch(int act, const float *gate, const float *up, const float *silu_gate, const float *dh,
                              void *dgate, void *dup, int64_t n, cudaStream_t st);

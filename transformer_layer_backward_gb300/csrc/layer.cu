@@ -102,8 +102,13 @@ int validate_ws(const tlb_layer_cfg *c, int64_t S, int64_t L, void *ws, size_t w
     return TLB_OK;
 }
 
+// abf_dout: the workspace's bf16 operand buffer already holds dOut in bf16 (a stack's layer
+// above left it there).  *abf_dres (optional) is set when the buffer ends up holding the
+// finished d_res in bf16, the A operand of the O-projection product.
 int ffn_impl(const tlb_layer_cfg &c, int64_t S, const float *d_out, const tlb_layer_weights &w,
-             const tlb_layer_acts &a, float *d_res, void *ws, cudaStream_t st) {
+             const tlb_layer_acts &a, float *d_res, void *ws, cudaStream_t st, bool abf_dout = false,
+             bool *abf_dres = nullptr) {
+    if (abf_dres != nullptr) *abf_dres = false;
     const LayerWs p = plan(c, S, S);   // the FFN regions do not depend on L
     const int64_t I = c.ffn_dim, H = c.dim;
     float *dF = ws_at<float>(ws, p.dF), *dG = ws_at<float>(ws, p.dG), *dU = ws_at<float>(ws, p.dU);
@@ -113,7 +118,7 @@ int ffn_impl(const tlb_layer_cfg &c, int64_t S, const float *d_out, const tlb_la
         void *abf = ws_at<void>(ws, p.abf), *gbf = ws_at<void>(ws, p.gbf), *ubf = ws_at<void>(ws, p.ubf);
         // dF = dOut W_down^T on the tensor cores (dOut rounded to bf16); dG, dU in bf16 are
         // the A operands of [W_gate | W_up]^T
-        TLB_TRY(tc_convert_bf16(d_out, abf, S * H, st));
+        if (!abf_dout) TLB_TRY(tc_convert_bf16(d_out, abf, S * H, st));
         const TcOperand down{abf, w.w_down.w, H};
         const float *sg = (c.act == TLB_ACT_SILU_MUL && (c.flags & TLB_USE_SILU_CACHE)) ? a.silu_gate : nullptr;
         const bool fuse = !(c.flags & TLB_SUB_NORM) && aligned16(a.gate) && aligned16(a.up) &&
@@ -141,7 +146,10 @@ int ffn_impl(const tlb_layer_cfg &c, int64_t S, const float *d_out, const tlb_la
         }
         if (resid && d_res != d_out)
             TLB_CUDA(cudaMemcpyAsync(d_res, d_out, size_t(S * H) * 4, cudaMemcpyDeviceToDevice, st));
-        return tc_gemm(gu, 2, S, H, w.w_gate.scale, d_res, resid, part, status, st);
+        // the epilogue also leaves d_res in bf16 where dOut was (the W_down^T product is done with it)
+        TLB_TRY(tc_gemm(gu, 2, S, H, w.w_gate.scale, d_res, resid, part, status, st, nullptr, abf));
+        if (abf_dres != nullptr) *abf_dres = true;
+        return TLB_OK;
     }
     // dF = dOut W_down^T
     TLB_TRY(linear_t_launch(c.wtype, w.w_down.w, w.w_down.scale, d_out, S, H, I, dF, false, st));
@@ -167,15 +175,16 @@ int ffn_impl(const tlb_layer_cfg &c, int64_t S, const float *d_out, const tlb_la
     return TLB_OK;
 }
 
+// abf_dr1: the workspace's bf16 operand buffer already holds dR1 in bf16.
 int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, const tlb_layer_weights &w,
-              const tlb_layer_acts &a, float *d_qpre, float *d_v, void *ws, cudaStream_t st) {
+              const tlb_layer_acts &a, float *d_qpre, float *d_v, void *ws, cudaStream_t st, bool abf_dr1 = false) {
     const LayerWs p = plan(c, S, L);
     const int64_t qd = int64_t(c.n_heads) * c.head_dim;
     float *dSub = ws_at<float>(ws, p.dSub);
     // dSub = dR1 W_O^T
     if (tc_route(c, S)) {
         void *abf = ws_at<void>(ws, p.abf);
-        TLB_TRY(tc_convert_bf16(dR1, abf, S * c.dim, st));
+        if (!abf_dr1) TLB_TRY(tc_convert_bf16(dR1, abf, S * c.dim, st));
         const TcOperand o{abf, w.w_o.w, c.dim};
         TLB_TRY(tc_gemm(&o, 1, S, qd, w.w_o.scale, dSub, false, ws_at<float>(ws, p.part), ws_at<uint32_t>(ws, 0), st));
     } else {
@@ -389,6 +398,44 @@ size_t stack_half(const tlb_layer_cfg &c, int64_t S, int64_t L) {
 
 using namespace tlb;
 
+// One layer.  abf_dout: the workspace's bf16 operand buffer already holds d_hidden in bf16
+// (the stack's layer above ran with the same workspace and ended with its dR1 = d_in there).
+static int layer_backward_impl(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb_layer_weights *w,
+                               const tlb_layer_acts *acts, const tlb_lora *lora_q, const tlb_lora *lora_v,
+                               const tlb_adamw_cfg *adam, float *d_hidden, double *sumsq, void *ws,
+                               size_t ws_bytes, void *stream, bool abf_dout) {
+    clear_error();
+    TLB_TRY(validate_cfg(cfg));
+    TLB_TRY(check_acts_ffn(*cfg, w, acts));
+    TLB_TRY(check_acts_attn(*cfg, S, L, w, acts));
+    TLB_TRY(check_lora(lora_q, "Q"));
+    TLB_TRY(check_lora(lora_v, "V"));
+    TLB_TRY(check_adam(adam));
+    if (S == 0) return TLB_OK;
+    TLB_REQUIRE(d_hidden && acts->x && acts->lora_q_h && acts->lora_v_h, TLB_EINVAL,
+                "layer_backward: NULL d_hidden / x / lora_q_h / lora_v_h");
+    TLB_TRY(validate_ws(cfg, S, L, ws, ws_bytes));
+    cudaStream_t st = as_stream(stream);
+    const tlb_layer_cfg &c = *cfg;
+    const LayerWs p = plan(c, S, L);
+    const int qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
+    ProfileScope prof(st);
+    float *dqpre = ws_at<float>(ws, p.dqpre), *dv = ws_at<float>(ws, p.dv);
+    if (decode_route(c, S, L, w, acts, d_hidden)) {
+        DecodeArgs d;
+        decode_args(c, L, w, acts, lora_q, lora_v, adam, d_hidden, sumsq, ws, p, d);
+        if ((c.flags & TLB_PERSISTENT) && persistent_supported(c, S, L))
+            return decode_persistent_launch(d, c, L, ws, p.gbar, p.pp, st);
+        return decode_layer_launch(d, c.wtype, st);
+    }
+    bool abf_dr1 = false;
+    TLB_TRY(ffn_impl(c, S, d_hidden, *w, *acts, d_hidden, ws, st, abf_dout && tc_route(c, S), &abf_dr1));
+    TLB_TRY(attn_impl(c, S, L, d_hidden, *w, *acts, dqpre, dv, ws, st, abf_dr1));
+    const LoraJob jobs[2] = {{dqpre, acts->lora_q_h, qd, *lora_q, ws_at<void>(ws, p.lora_q)},
+                             {dv, acts->lora_v_h, kvd, *lora_v, ws_at<void>(ws, p.lora_v)}};
+    return lora_seq_launch(S, c.dim, c.rank, c.lora_alpha, acts->x, jobs, 2, *adam, sumsq, st);
+}
+
 extern "C" {
 
 size_t tlb_workspace_bytes(const tlb_layer_cfg *cfg, int64_t S, int64_t L) {
@@ -441,41 +488,14 @@ int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, const tlb
                        const tlb_layer_acts *acts, const tlb_lora *lora_q, const tlb_lora *lora_v,
                        const tlb_adamw_cfg *adam, float *d_hidden, double *sumsq, void *ws, size_t ws_bytes,
                        void *stream) {
-    clear_error();
-    TLB_TRY(validate_cfg(cfg));
-    TLB_TRY(check_acts_ffn(*cfg, w, acts));
-    TLB_TRY(check_acts_attn(*cfg, S, L, w, acts));
-    TLB_TRY(check_lora(lora_q, "Q"));
-    TLB_TRY(check_lora(lora_v, "V"));
-    TLB_TRY(check_adam(adam));
-    if (S == 0) return TLB_OK;
-    TLB_REQUIRE(d_hidden && acts->x && acts->lora_q_h && acts->lora_v_h, TLB_EINVAL,
-                "layer_backward: NULL d_hidden / x / lora_q_h / lora_v_h");
-    TLB_TRY(validate_ws(cfg, S, L, ws, ws_bytes));
-    cudaStream_t st = as_stream(stream);
-    const tlb_layer_cfg &c = *cfg;
-    const LayerWs p = plan(c, S, L);
-    const int qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
-    ProfileScope prof(st);
-    float *dqpre = ws_at<float>(ws, p.dqpre), *dv = ws_at<float>(ws, p.dv);
-    if (decode_route(c, S, L, w, acts, d_hidden)) {
-        DecodeArgs d;
-        decode_args(c, L, w, acts, lora_q, lora_v, adam, d_hidden, sumsq, ws, p, d);
-        if ((c.flags & TLB_PERSISTENT) && persistent_supported(c, S, L))
-            return decode_persistent_launch(d, c, L, ws, p.gbar, p.pp, st);
-        return decode_layer_launch(d, c.wtype, st);
-    }
-    TLB_TRY(ffn_impl(c, S, d_hidden, *w, *acts, d_hidden, ws, st));
-    TLB_TRY(attn_impl(c, S, L, d_hidden, *w, *acts, dqpre, dv, ws, st));
-    const LoraJob jobs[2] = {{dqpre, acts->lora_q_h, qd, *lora_q, ws_at<void>(ws, p.lora_q)},
-                             {dv, acts->lora_v_h, kvd, *lora_v, ws_at<void>(ws, p.lora_v)}};
-    return lora_seq_launch(S, c.dim, c.rank, c.lora_alpha, acts->x, jobs, 2, *adam, sumsq, st);
+    return layer_backward_impl(cfg, S, L, w, acts, lora_q, lora_v, adam, d_hidden, sumsq, ws, ws_bytes, stream,
+                               false);
 }
-
 
 size_t tlb_stack_workspace_bytes(const tlb_layer_cfg *cfg, int64_t S, int64_t L) {
     if (cfg == nullptr || S < 0) return 0;
-    return kStackSets * stack_half(*cfg, S, L < S ? S : L);
+    // single-token layers rotate over kStackSets workspace sets; longer ones share one
+    return (S == 1 ? kStackSets : 1) * stack_half(*cfg, S, L < S ? S : L);
 }
 
 int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n_layers,
@@ -490,9 +510,9 @@ int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n
     TLB_REQUIRE(d_hidden, TLB_EINVAL, "stack_backward: NULL d_hidden");
     TLB_TRY(check_adam(adam));
     const tlb_layer_cfg &c = *cfg;
-    const size_t half = stack_half(c, S, L);
-    TLB_REQUIRE(ws != nullptr && ws_bytes >= kStackSets * half, TLB_EINVAL,
-                "stack workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, kStackSets * half);
+    const size_t half = stack_half(c, S, L), need = (S == 1 ? kStackSets : 1) * half;
+    TLB_REQUIRE(ws != nullptr && ws_bytes >= need, TLB_EINVAL,
+                "stack workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
     TLB_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, TLB_EINVAL, "workspace not 256-byte aligned");
     bool pipelined = S == 1 && !(c.flags & TLB_PERSISTENT);
     for (int l = 0; l < n_layers; ++l) {
@@ -505,10 +525,12 @@ int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n
         pipelined = pipelined && decode_route(c, S, L, &w[l], &acts[l], d_hidden);
     }
     if (!pipelined) {
-        // the layers one after another on the caller's stream ([RS] backward_through_layers)
+        // the layers one after another on the caller's stream ([RS] backward_through_layers),
+        // all in the first workspace set: on the tensor-core route each layer leaves its d_in
+        // in bf16 in the set's operand buffer, where the next layer's first product reads it
         for (int l = n_layers - 1; l >= 0; --l)
-            TLB_TRY(tlb_layer_backward(cfg, S, L, &w[l], &acts[l], &lora_q[l], &lora_v[l], adam, d_hidden, sumsq,
-                                       ws, half, stream));
+            TLB_TRY(layer_backward_impl(cfg, S, L, &w[l], &acts[l], &lora_q[l], &lora_v[l], adam, d_hidden, sumsq,
+                                        ws, half, stream, l < n_layers - 1));
         return TLB_OK;
     }
     // Single-token layers: layer l's k1 .. k3 (its dR1, the next layer's dOut) on the
