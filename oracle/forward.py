@@ -5,8 +5,11 @@ assembles the forward the pages describe ([FFN] "Forward"; [ATT] "Gradient
 Flow", read in forward order; [RS] LayerActivations) for S query rows at
 positions L - S .. L - 1 over a cache of L keys:
 
-  h_q = n1 A_q^T             q = RoPE(n1 W_Q + s h_q B_q^T)      s = alpha / rank
-  k   = RoPE(n1 W_K)         h_v = n1 A_v^T      v = n1 W_V + s h_v B_v^T
+  h_q = n1 A_q^T             q = RoPE([QKNorm](n1 W_Q + s h_q B_q^T))      s = alpha / rank
+  k   = RoPE([QKNorm](n1 W_K))                h_v = n1 A_v^T      v = n1 W_V + s h_v B_v^T
+      (QKNorm: RMSNorm of each head's head_dim values, gains g_q and g_k of length
+       head_dim shared by the heads, when the QK-norm is on; [RS] LayerActivations caches
+       q and k after it and RoPE)
   P   = softmax(scale q k^T) over keys j <= position(i)          ctx = P v (per head, GQA)
   a   = [RMSNorm(ctx; g_sub_attn)] (s_o W_O)                     r1 = [x +] a
   n2  = [RMSNorm(r1; g_ffn)]   gate = n2 s_g W_g   up = n2 s_u W_u   hid = act(gate) up
@@ -65,6 +68,9 @@ def layer_forward(cfg, p, n1, x_in, k_prev, v_prev, r1_delta=None):
     hq = n1 @ f64(p["a_q"]).T
     q = (n1 @ f64(p["w_q"]) + s * hq @ f64(p["b_q"]).T).reshape(S, nh, hd)
     k = (n1 @ f64(p["w_k"])).reshape(S, nkv, hd)
+    q_raw = q.reshape(S, nh * hd)
+    if cfg.qk_norm:
+        q, k = rmsnorm(q, p["g_q"], cfg.norm_eps), rmsnorm(k, p["g_k"], cfg.norm_eps)
     if cfg.rope:
         q, k = rope(q, pos, cfg.rope_base), rope(k, pos, cfg.rope_base)
     hv = n1 @ f64(p["a_v"]).T
@@ -102,5 +108,6 @@ def layer_forward(cfg, p, n1, x_in, k_prev, v_prev, r1_delta=None):
         kc = K.transpose(1, 0, 2).reshape(L, nkv * hd)
         vc = V.transpose(1, 0, 2).reshape(L, nkv * hd)
     cache = dict(x=n1, gate=gate, up=up, silu_gate=f64(gate) / (1.0 + np.exp(-f64(gate))),
-                 hidden=hid, r1=r1, ctx=ctx, k=kc, v=vc, attn=P, lora_q_h=hq, lora_v_h=hv)
+                 hidden=hid, r1=r1, ctx=ctx, k=kc, v=vc, attn=P, lora_q_h=hq, lora_v_h=hv,
+                 q_raw=q_raw)
     return out, cache

@@ -21,6 +21,9 @@ state of one layer as float arrays.  Order of the steps:
       dAttn = dCtx_h V^T;  dS = softmax_bwd(attn_h, dAttn);  dQ_h = scale dS K
       dV   += attn_h^T dCtx_h
     dQpre = RoPE_bwd(dQ) at positions L - S + i  (if RoPE is on)
+    dQpre = RMSNorm_bwd(q_raw_h, g_q, dQpre_h) per head over head_dim  (if the QK-norm is
+            on: [RS] LayerActivations caches q after a QK-norm and RoPE; q_raw is the Q
+            projection output before the norm)
     dV rows kept: the S newest cache positions (the tokens of this call)
   LoRA ([RS] "LoRA Q backward", "LoRA V backward"; LoRA+ learning rate on B)
     Q adapter from dQpre, V adapter from dV, both with x = attn_input
@@ -80,6 +83,8 @@ def attn_backward(cfg, d, dR1) -> dict:
         dV_all[kvh] += value_backward(attn[h], dctx_h)
     pos = cfg.pos0 + np.arange(S)
     dQpre = rope_backward(dQ, pos, cfg.rope_base) if cfg.rope else dQ
+    if getattr(cfg, "qk_norm", False):
+        dQpre = rmsnorm_backward(f64(d["q_raw"]).reshape(S, nh, hd), d["g_q"], dQpre, cfg.norm_eps)
     dV = dV_all[:, cfg.pos0:, :].transpose(1, 0, 2).reshape(S, nkv * hd)
     return dict(dSub=dSub, dCtx=dCtx, dS=dS_all, dQ=dQ.reshape(S, nh * hd),
                 dQpre=dQpre.reshape(S, nh * hd), dV=dV)

@@ -31,6 +31,7 @@ class LayerConfig:
     pre_norm: bool = False   # RMSNorm before the FFN (backward adds into the residual)
     residual: bool = True    # out = r1 + f and r1 = x + a
     rope: bool = True        # NeoX split-half rotary embedding on q and k
+    qk_norm: bool = False    # per-head RMSNorm of q and k over head_dim, before RoPE
     kv_layout: str = "shd"   # "shd": [L, n_kv*hd]   "hsd": [n_kv, L, hd]
     rope_base: float = 10000.0
     norm_eps: float = 1e-6

@@ -16,7 +16,8 @@ Recipe (distributions follow the workload descriptions):
   * attention rows: softmax of N(0, attn_logit_std^2) logits over the keys a
     query may see (key j visible to query i iff j <= L - S + i), zero elsewhere;
   * the cached SiLU output is silu(gate) and the cached LoRA activations are
-    x @ A^T, both formed in float64 from the values above and then rounded.
+    x @ A^T, both formed in float64 from the values above and then rounded;
+  * with the QK-norm, the Q projection before it ~ N(0, 1) and its gain ~ U(0.5, 1.5).
 """
 from __future__ import annotations
 
@@ -90,6 +91,9 @@ def layer_inputs(cfg: LayerConfig, layer: int = 0, seed: int = 0, with_dout: boo
     d["k"] = _n(seed, cfg, layer, "k_cache", kshape).astype(f32)
     d["v"] = _n(seed, cfg, layer, "v_cache", kshape).astype(f32)
     d["attn"] = attention_rows(seed, cfg, layer)
+    if cfg.qk_norm:
+        d["q_raw"] = _n(seed, cfg, layer, "q_raw", (S, qd)).astype(f32)
+        d["g_q"] = _u(seed, cfg, layer, "g_q", (cfg.head_dim,), 0.5, 1.5).astype(f32)
     # LoRA adapters and their AdamW state
     d["a_q"] = _n(seed, cfg, layer, "lora_a_q", (r, H), cfg.lora_a_std).astype(f32)
     d["b_q"] = _n(seed, cfg, layer, "lora_b_q", (qd, r), cfg.lora_b_std).astype(f32)

@@ -54,13 +54,14 @@ def make_problem(cfg, seed=1):
     k_prev = rs.normal(size=(nkv, L - S, hd))
     v_prev = rs.normal(size=(nkv, L - S, hd))
     dout = rs.normal(size=(S, H))
+    p["g_q"], p["g_k"] = rs.uniform(0.5, 1.5, hd), rs.uniform(0.5, 1.5, hd)
     return p, n1, x_in, k_prev, v_prev, dout
 
 
 def backward_inputs(cfg, p, cache):
     d = dict(cache)
     for k in ("w_o", "w_gate", "w_up", "w_down", "s_o", "s_gate", "s_up", "s_down",
-              "g_sub_attn", "g_ffn", "g_sub_ffn", "a_q", "b_q", "a_v", "b_v"):
+              "g_sub_attn", "g_ffn", "g_sub_ffn", "g_q", "a_q", "b_q", "a_v", "b_v"):
         d[k] = p[k]
     for k in ("a_q", "b_q", "a_v", "b_v"):
         d["m_" + k] = np.zeros_like(p[k])
@@ -77,6 +78,9 @@ FD_CASES = {
                                      residual=False, rope=False, seq_len=3, cache_len=3),
     "prenorm_only_mha": small_cfg(n_kv_heads=4, sub_norm=False, residual=False, rope=False,
                                   seq_len=2, cache_len=4),
+    "qk_norm_gqa": small_cfg(qk_norm=True),
+    "qk_norm_decode_swiglu": small_cfg(qk_norm=True, act="silu_mul", sub_norm=False, seq_len=1,
+                                       cache_len=6, kv_layout="hsd"),
 }
 
 
