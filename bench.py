@@ -61,6 +61,8 @@ def parse():
     p.add_argument("--cases", default=None,
                    help="sweep: run only the cases whose 'kernel shape' label matches this regex")
     p.add_argument("--workload", default="decode", choices=["decode", "seq512", "seq2048", "stack2048", "sweep"])
+    p.add_argument("--qk-norm", action="store_true",
+                   help="layers with the per-head QK-norm on q (decode and sequence workloads)")
     return p.parse_args()
 
 
@@ -194,7 +196,7 @@ def run_reference(args, rank, world):
         print(json.dumps(line), flush=True)
         return
     from synth import DECODE
-    cfg = DECODE
+    cfg = DECODE.with_(qk_norm=True) if args.qk_norm else DECODE
     per = max(args.cpu_seconds / max(args.steps, 1), 0.0)
     times = []
     for _ in range(args.warmup if args.warmup < 3 else 1):
@@ -208,7 +210,8 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "decode layer backward: dim 2560, ffn 6912, 20/5 heads x 128, "
-                                   "cache 1024, ternary, LoRA r16", "global_batch": 1, "seq_len": 1,
+                                   "cache 1024, ternary, " + ("QK-norm on q, " if cfg.qk_norm else "") +
+                                   "LoRA r16", "global_batch": 1, "seq_len": 1,
                        "parallelism": "replicas"},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
                              "sample": "one decode layer backward per step, float64 numpy oracle"},
@@ -255,6 +258,9 @@ def device_layer(cfg, layer, seed=0):
         t["v_" + k] = torch.zeros_like(t[k])
     t["lora_q_h"] = t["x"] @ t["a_q"].t()
     t["lora_v_h"] = t["x"] @ t["a_v"].t()
+    if cfg.qk_norm:                       # Q projection before the per-head norm, the norm's gain
+        t["q_raw"] = n(S, qd)
+        t["g_q"] = torch.rand(cfg.head_dim, device="cuda", generator=g) + 0.5
     return t
 
 
@@ -287,6 +293,8 @@ def seq_main(args, rank, world, local, dist):
     torch.cuda.set_device(local)
     tlb.load()
     cfg, depth = seq_config(args.workload)
+    if args.qk_norm:
+        cfg = cfg.with_(qk_norm=True)
     S, L = cfg.seq_len, cfg.cache_len
     NL = 2 if depth == 1 and S <= 512 else (2 if depth > 1 else 1)
     c = cfg_to_abi(tlb, cfg)
@@ -414,7 +422,8 @@ def seq_main(args, rank, world, local, dist):
 
     # end to end through the public API: the step's activations and caches from pinned host
     # memory every step, d_in and the gradient sums read back
-    acts = ("x", "gate", "up", "silu_gate", "k", "v", "attn", "lora_q_h", "lora_v_h", "dout")
+    acts = ("x", "gate", "up", "silu_gate", "k", "v", "attn", "lora_q_h", "lora_v_h", "dout") + \
+        (("q_raw",) if cfg.qk_norm else ())
     pinned = [{k: layers[l]["t"][k].cpu().pin_memory() for k in acts} for l in range(NL)]
     h2d = sum(pinned[0][k].numel() * 4 for k in acts) * depth
     res_h = torch.empty(S, cfg.dim, pin_memory=True)
@@ -451,6 +460,7 @@ def seq_main(args, rank, world, local, dist):
                 "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (device generator)",
                 "config": {"workload": wl + ": dim 2560, ffn 9728, 32/8 heads x 128, SwiGLU, RoPE, residual, "
+                                       + ("QK-norm on q, " if cfg.qk_norm else "") +
                                        "bf16 weights, LoRA r16 Q/V, AdamW+LoRA+",
                            "global_batch": world, "seq_len": S, "layers_per_step": depth,
                            "parallelism": "replicas" if world > 1 else "single",
@@ -732,7 +742,7 @@ def main():
 
     torch.cuda.set_device(local)
     tlb.load()
-    cfg = DECODE
+    cfg = DECODE.with_(qk_norm=True) if args.qk_norm else DECODE
     NL = args.layers
     c = cfg_to_abi(tlb, cfg)
     adam = adam_to_abi(tlb, cfg)
@@ -946,7 +956,8 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": {"workload": "decode layer backward: dim 2560, ffn 6912, 20/5 heads "
                                        "x 128, cache 1024, pos 1023, ternary int8 weights, ReLU^2xMul, "
-                                       "sub-norms, LoRA r16 Q/V, AdamW+LoRA+",
+                                       "sub-norms, " + ("QK-norm on q, " if cfg.qk_norm else "") +
+                                       "LoRA r16 Q/V, AdamW+LoRA+",
                            "global_batch": world, "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
                            "layers_cycled": NL, "l2": "inputs > L2: %d distinct layers x %.1f MB" % (NL, step_bytes / 1e6),
                            "cuda_graph": "one graph per cycle of %d layer calls" % NL if cycle is not None else False},

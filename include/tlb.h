@@ -71,6 +71,10 @@ extern "C" {
 #define TLB_CAUSAL 32          /* query row i sees keys j <= L - S + i only; attn is 0 elsewhere */
 #define TLB_PERSISTENT 64      /* single-token layers: one persistent cooperative kernel (TMA-streamed
                                   weights, grid barriers) instead of the multi-kernel schedule */
+#define TLB_QK_NORM 128        /* q (and k) pass a per-head RMSNorm over head_dim before RoPE ([RS]
+                                  LayerActivations caches them after a QK-norm and RoPE): dQ is
+                                  taken back through it, which needs q_raw and gamma_q.  Not with
+                                  TLB_PERSISTENT (such layers take the multi-kernel schedule) */
 
 /* Shapes and constants of one layer. q_dim = n_heads*head_dim, kv_dim = n_kv_heads*head_dim. */
 typedef struct {
@@ -103,6 +107,7 @@ typedef struct {
     const float *gamma_sub_ffn;     /* [ffn_dim], TLB_SUB_NORM */
     const float *gamma_ffn;         /* [dim],     TLB_PRE_NORM */
     const float *gamma_sub_attn;    /* [q_dim],   TLB_SUB_NORM */
+    const float *gamma_q;           /* [head_dim], TLB_QK_NORM: the per-head norm's gain (all heads) */
 } tlb_layer_weights;
 
 /* Cached forward activations of one layer ([RS] LayerActivations, [FFN]
@@ -123,6 +128,7 @@ typedef struct {
     const float *attn;       /* softmax weights [n_heads, S, L] */
     const float *lora_q_h;   /* x @ A_q^T [S, rank] */
     const float *lora_v_h;   /* x @ A_v^T [S, rank] */
+    const float *q_raw;      /* Q projection output before the per-head norm [S, q_dim], TLB_QK_NORM */
 } tlb_layer_acts;
 
 /* A LoRA adapter (A [rank, in], B [out, rank]) and its AdamW moments, updated in place.

@@ -71,7 +71,7 @@ def cfg_to_abi(tlb, cfg, persistent=False):
                          pre_norm=cfg.pre_norm, residual=cfg.residual, rope=cfg.rope,
                          use_silu_cache=(cfg.act == "silu_mul" and cfg.use_silu_cache), causal=True,
                          rope_base=cfg.rope_base, norm_eps=cfg.norm_eps, attn_scale=cfg.attn_scale,
-                         persistent=persistent)
+                         persistent=persistent, qk_norm=cfg.qk_norm)
 
 
 def adam_to_abi(tlb, cfg):

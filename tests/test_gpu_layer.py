@@ -3,7 +3,8 @@ of the whole layer / stack against the float64 oracle on the same seeded inputs.
 
 Configurations: the tiny fp32 layer (all norms, RoPE, GQA, causal), the
 single-token decode layer with ternary weights, small bf16 sequence layers with
-ragged sequence and cache lengths, and the S = 512 SwiGLU layer.
+ragged sequence and cache lengths, the S = 512 SwiGLU layer, and layers with the
+per-head QK-norm on q.
 """
 import numpy as np
 import pytest
@@ -39,8 +40,13 @@ SEQ_MHA = SEQ512.with_(name="seq_mha", dim=256, ffn_dim=512, n_heads=4, n_kv_hea
                        rank=4, lora_alpha=8.0, seq_len=130, cache_len=258)
 SEQ_ODD = SEQ512.with_(name="seq_odd_cache", dim=512, ffn_dim=768, n_heads=4, n_kv_heads=1, head_dim=128,
                        seq_len=45, cache_len=301)
+# QK-norm on q before RoPE: the CUDA-core sequence path, the single-token chain (its
+# persistent variant falls back to the chain) and the tensor-core sequence path
+TINY_QK = TINY.with_(name="tiny_qknorm", qk_norm=True)
+DEC_QK = DEC_F32.with_(name="dec_qknorm", qk_norm=True, cache_len=65)
+SEQ_QK = SEQ_HD64.with_(name="seq_qknorm", qk_norm=True, seq_len=148, cache_len=180)
 CASES = {c.name: c for c in (TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512, DEC_F32, DEC_BF16, DEC_G8, DEC_HD256,
-                             SEQ_HD64, SEQ_CACHE, SEQ_MHA, SEQ_ODD)}
+                             SEQ_HD64, SEQ_CACHE, SEQ_MHA, SEQ_ODD, TINY_QK, DEC_QK, SEQ_QK)}
 
 
 def tol(cfg):

@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libt
 TLB_OK, TLB_EINVAL, TLB_EUNSUPPORTED, TLB_ENONFINITE, TLB_ETIMEOUT, TLB_ECUDA = 0, -1, -2, -3, -4, -5
 ACT_RELU2_MUL, ACT_SILU_MUL = 0, 1
 W_F32, W_BF16, W_TERNARY_I8 = 0, 1, 2
-SUB_NORM, PRE_NORM, RESIDUAL, ROPE, USE_SILU_CACHE, CAUSAL, PERSISTENT = 1, 2, 4, 8, 16, 32, 64
+SUB_NORM, PRE_NORM, RESIDUAL, ROPE, USE_SILU_CACHE, CAUSAL, PERSISTENT, QK_NORM = 1, 2, 4, 8, 16, 32, 64, 128
 
 vp, i32, i64, f32, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_size_t
 
@@ -31,13 +31,14 @@ class Weight(C.Structure):
 
 class LayerWeights(C.Structure):
     _fields_ = [("w_down", Weight), ("w_gate", Weight), ("w_up", Weight), ("w_o", Weight),
-                ("gamma_sub_ffn", vp), ("gamma_ffn", vp), ("gamma_sub_attn", vp)]
+                ("gamma_sub_ffn", vp), ("gamma_ffn", vp), ("gamma_sub_attn", vp), ("gamma_q", vp)]
 
 
 class LayerActs(C.Structure):
     _fields_ = [("x", vp), ("gate", vp), ("up", vp), ("silu_gate", vp), ("hidden", vp),
                 ("r1", vp), ("ctx", vp), ("k", vp), ("v", vp), ("kv_stride_head", i64),
-                ("kv_stride_pos", i64), ("attn", vp), ("lora_q_h", vp), ("lora_v_h", vp)]
+                ("kv_stride_pos", i64), ("attn", vp), ("lora_q_h", vp), ("lora_v_h", vp),
+                ("q_raw", vp)]
 
 
 class Lora(C.Structure):

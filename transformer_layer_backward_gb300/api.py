@@ -131,11 +131,11 @@ def adamw(p, g, m, v, cfg: A.AdamwCfg, lr_mult=1.0, sumsq=None, stream=None):
 def layer_cfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, lora_alpha, act="relu2_mul",
               wtype="f32", sub_norm=False, pre_norm=False, residual=True, rope=True,
               use_silu_cache=False, causal=True, rope_base=10000.0, norm_eps=1e-6,
-              attn_scale=None, persistent=False) -> A.LayerCfg:
+              attn_scale=None, persistent=False, qk_norm=False) -> A.LayerCfg:
     flags = ((A.SUB_NORM if sub_norm else 0) | (A.PRE_NORM if pre_norm else 0) |
              (A.RESIDUAL if residual else 0) | (A.ROPE if rope else 0) |
              (A.USE_SILU_CACHE if use_silu_cache else 0) | (A.CAUSAL if causal else 0) |
-             (A.PERSISTENT if persistent else 0))
+             (A.PERSISTENT if persistent else 0) | (A.QK_NORM if qk_norm else 0))
     return A.LayerCfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, float(lora_alpha),
                       float(rope_base), float(norm_eps),
                       float(1.0 / math.sqrt(head_dim) if attn_scale is None else attn_scale),
@@ -157,7 +157,8 @@ def workspace_status(ws, stream=None):
 
 
 def layer_weights(cfg: A.LayerCfg, t: dict):
-    """Weights from a dict: w_down/w_gate/w_up/w_o (+ s_* scales), gamma_* optional."""
+    """Weights from a dict: w_down/w_gate/w_up/w_o (+ s_* scales); the gains g_sub_ffn,
+    g_ffn, g_sub_attn, g_q are optional."""
     wd = _WDTYPE[cfg.wtype]
 
     def w(name):
@@ -166,7 +167,8 @@ def layer_weights(cfg: A.LayerCfg, t: dict):
     return A.LayerWeights(w("w_down"), w("w_gate"), w("w_up"), w("w_o"),
                           _ptr(t.get("g_sub_ffn"), name="g_sub_ffn"),
                           _ptr(t.get("g_ffn"), name="g_ffn"),
-                          _ptr(t.get("g_sub_attn"), name="g_sub_attn"))
+                          _ptr(t.get("g_sub_attn"), name="g_sub_attn"),
+                          _ptr(t.get("g_q"), name="g_q"))
 
 
 def layer_acts(cfg: A.LayerCfg, t: dict, kv_layout: str, L: int):
@@ -178,7 +180,8 @@ def layer_acts(cfg: A.LayerCfg, t: dict, kv_layout: str, L: int):
         sh, sp = L * hd, hd
     g = lambda k: _ptr(t.get(k), name=k)
     return A.LayerActs(g("x"), g("gate"), g("up"), g("silu_gate"), g("hidden"), g("r1"),
-                       g("ctx"), g("k"), g("v"), sh, sp, g("attn"), g("lora_q_h"), g("lora_v_h"))
+                       g("ctx"), g("k"), g("v"), sh, sp, g("attn"), g("lora_q_h"), g("lora_v_h"),
+                       g("q_raw"))
 
 
 def lora(t: dict, tag: str, grads: dict | None = None):

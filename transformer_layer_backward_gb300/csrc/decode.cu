@@ -559,8 +559,10 @@ __global__ void __launch_bounds__(kQThreads) dec_k6(DecodeArgs a, RopeFreqs fr) 
     __shared__ float red[16][kQWarps];
     __shared__ float sB[256 * 16];
     __shared__ float sCos[128], sSin[128];
+    __shared__ float sQx[256], sGq[256], sNorm[2];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int h = blockIdx.x;
+    const bool qkn = (a.flags & TLB_QK_NORM) != 0;
     pdl_trigger();
     // Before the wait: this head's rows of B_q (only this layer's k7, later, writes them)
     // and the rotation angles of the current position.
@@ -568,6 +570,11 @@ __global__ void __launch_bounds__(kQThreads) dec_k6(DecodeArgs a, RopeFreqs fr) 
     if (a.flags & TLB_ROPE)
         for (int d = threadIdx.x; d < (a.hd >> 1); d += blockDim.x)
             rope_cos_sin(float(a.pos), fr.hi[d], fr.lo[d], sCos[d], sSin[d]);
+    if (qkn)                    // this head's pre-norm q and the norm's gain
+        for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
+            sQx[d] = a.q_raw[int64_t(h) * a.hd + d];
+            sGq[d] = a.g_q[d];
+        }
     pdl_wait();
     // blockDim / hd thread groups each sum a slice of the chunks (four chunks in flight per
     // thread), then combine
@@ -619,12 +626,32 @@ __global__ void __launch_bounds__(kQThreads) dec_k6(DecodeArgs a, RopeFreqs fr) 
             y1 = t1;
             y2 = t2;
         }
-        a.dqpre[h * a.hd + d] = y1;
-        a.dqpre[h * a.hd + d + half] = y2;
         sq[d] = y1;
         sq[d + half] = y2;   // each pair is owned by one thread
     }
     __syncthreads();
+    if (qkn) {
+        // QK-norm backward over the head (rms = sqrt(mean(x^2) + eps) of the pre-norm q x):
+        // dx = (g dy - x sum(g dy x) / (hd rms^2)) / rms
+        if (warp == 0) {
+            float xx = 0.f, gx = 0.f;
+            for (int d = lane; d < a.hd; d += 32) {
+                xx += sQx[d] * sQx[d];
+                gx += sGq[d] * sq[d] * sQx[d];
+            }
+            xx = warp_sum(xx);
+            gx = warp_sum(gx);
+            if (lane == 0) {
+                sNorm[0] = xx;
+                sNorm[1] = gx;
+            }
+        }
+        __syncthreads();
+        const float rms = sqrtf(sNorm[0] / float(a.hd) + a.eps), c = sNorm[1] / (float(a.hd) * rms * rms);
+        for (int d = threadIdx.x; d < a.hd; d += blockDim.x) sq[d] = (sGq[d] * sq[d] - sQx[d] * c) / rms;
+        __syncthreads();
+    }
+    for (int d = threadIdx.x; d < a.hd; d += blockDim.x) a.dqpre[h * a.hd + d] = sq[d];
     // gh_q[r] += s * sum_{d} dQpre[h, d] B_q[h*hd + d, r]   (B before its update)
     float acc[16];
 #pragma unroll

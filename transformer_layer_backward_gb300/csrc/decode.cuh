@@ -12,6 +12,7 @@ struct DecodeArgs {
     float s_down, s_gate, s_up, s_o;
     const float *g_sub_ffn, *g_ffn, *g_sub_attn;
     const float *x, *gate, *up, *silu_gate, *hidden, *r1, *ctx, *k, *v, *attn, *hq, *hv;
+    const float *q_raw, *g_q;                          // QK-norm: pre-norm q [qd], gain [hd]
     int64_t sh, sp;
     float *d_hidden;                                   // [H] in: dOut, out: dR1 (single call)
     const float *dout;                                 // [H] the layer's dOut (k1, k3)

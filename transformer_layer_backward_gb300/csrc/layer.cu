@@ -212,8 +212,14 @@ int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, co
     g.rope = (c.flags & TLB_ROPE) ? 1 : 0;
     g.scale = c.attn_scale;
     if (attn_tc_route(c, S, L) && aligned16(d_qpre) && aligned16(d_v) && aligned16(a.attn))
-        return attn_tc_launch(g, c.rope_base, ws_at<void>(ws, p.atc), ws_at<uint32_t>(ws, 0), st);
-    return attn_core_launch(g, c.rope_base, st);
+        TLB_TRY(attn_tc_launch(g, c.rope_base, ws_at<void>(ws, p.atc), ws_at<uint32_t>(ws, 0), st));
+    else
+        TLB_TRY(attn_core_launch(g, c.rope_base, st));
+    // QK-norm: dQpre of each (row, head) back through the per-head RMSNorm, in place
+    if (c.flags & TLB_QK_NORM)
+        return rmsnorm_backward_launch(a.q_raw, w.gamma_q, d_qpre, d_qpre, S * c.n_heads, c.head_dim, c.norm_eps,
+                                       0, st);
+    return TLB_OK;
 }
 
 int check_acts_ffn(const tlb_layer_cfg &c, const tlb_layer_weights *w, const tlb_layer_acts *a) {
@@ -239,6 +245,8 @@ int check_acts_attn(const tlb_layer_cfg &c, int64_t S, int64_t L, const tlb_laye
                 "K/V strides smaller than head_dim");
     if (c.flags & TLB_SUB_NORM)
         TLB_REQUIRE(a->ctx && w->gamma_sub_attn, TLB_EINVAL, "SUB_NORM needs ctx and gamma_sub_attn");
+    if (c.flags & TLB_QK_NORM)
+        TLB_REQUIRE(a->q_raw && w->gamma_q, TLB_EINVAL, "QK_NORM needs q_raw and gamma_q");
     return TLB_OK;
 }
 
@@ -315,6 +323,8 @@ void decode_args(const tlb_layer_cfg &c, int64_t L, const tlb_layer_weights *w, 
     d.attn = acts->attn;
     d.hq = acts->lora_q_h;
     d.hv = acts->lora_v_h;
+    d.q_raw = acts->q_raw;
+    d.g_q = w->gamma_q;
     d.sh = acts->kv_stride_head;
     d.sp = acts->kv_stride_pos;
     d.d_hidden = d_hidden;
