@@ -387,9 +387,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
         if (ok && mbar_wait(&ufull, 0, p.status, 29u)) {
             tc_fence_after();
             constexpr int half = HD / 2, q4 = HD / 4;
-            float *out = p.dq + int64_t(row_ok ? i : 0) * (p.nh * HD) + h * HD;
+            float *out0 = p.dq + h * HD;
             const float pos = float(p.pos0 + i);
 #pragma unroll 1
+            // the rings are idle (every copy consumed, every MMA done): each warp turns its
+            // 32-row blocks there so that the stores coalesce
+            float *blk = reinterpret_cast<float *>(sm) + (warp - 2) * 32 * 33;
+            const int c4 = (lane & 7) * 4, rl = lane >> 3;
             for (int c = hf * q4; c < (hf + 1) * q4; c += 16) {      // pairs (c, c + HD / 2)
                 uint32_t u1[16], u2[16], w1[16], w2[16];
                 tmem_ld16(tmem + Ly::TU + uint32_t(c) + lane_off, u1);
@@ -412,14 +416,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
                     y1[t] = a1;
                     y2[t] = a2;
                 }
-                if (row_ok) {
 #pragma unroll
-                    for (int t = 0; t < 16; t += 4) {
-                        *reinterpret_cast<float4 *>(out + c + t) = make_float4(y1[t], y1[t + 1], y1[t + 2], y1[t + 3]);
-                        *reinterpret_cast<float4 *>(out + c + half + t) =
-                            make_float4(y2[t], y2[t + 1], y2[t + 2], y2[t + 3]);
-                    }
+                for (int t = 0; t < 16; ++t) {
+                    blk[lane * 33 + t] = y1[t];
+                    blk[lane * 33 + 16 + t] = y2[t];
                 }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {           // block column c4 is head column c + c4, or
+                    const int rr = 4 * k + rl, ii = q0 + quarter * 32 + rr;   // c + half + c4 - 16
+                    const float *a = blk + rr * 33 + c4;
+                    if (ii < p.S)
+                        *reinterpret_cast<float4 *>(out0 + int64_t(ii) * (p.nh * HD) + (c4 < 16 ? c + c4 : c + half + c4 - 16)) =
+                            make_float4(a[0], a[1], a[2], a[3]);
+                }
+                __syncwarp();
             }
         }
         if (!ok) s_abort = 1;
@@ -569,20 +580,29 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_tc_dv_kernel(const __gri
         }
         if (ok && mbar_wait(&dfull, 0, p.status, 35u)) {
             tc_fence_after();
+            // Every copy into the staging ring has been consumed by now, so each warp turns
+            // its 32 x 32 blocks there: lanes then run along columns and the stores coalesce.
+            float *blk = reinterpret_cast<float *>(sm) + (warp - 2) * 32 * 33;
             const int64_t kvd = int64_t(p.nkv) * HD;
-            float *out = p.dv + (G > 1 ? int64_t(g) * p.S * kvd : 0) + int64_t(key_ok ? jj : 0) * kvd + kvh * HD;
+            float *out = p.dv + (G > 1 ? int64_t(g) * p.S * kvd : 0) + kvh * HD;
+            const int c4 = (lane & 7) * 4, rl = lane >> 3;
 #pragma unroll 1
             for (int c = hf * (HD / 2); c < (hf + 1) * (HD / 2); c += 32) {
                 uint32_t v[32];
                 tmem_ld32(tD + uint32_t(c) + lane_off, v);
                 tmem_wait_ld();
-                if (key_ok) {
 #pragma unroll
-                    for (int t = 0; t < 32; t += 4)
-                        *reinterpret_cast<float4 *>(out + c + t) =
-                            make_float4(__uint_as_float(v[t]), __uint_as_float(v[t + 1]), __uint_as_float(v[t + 2]),
-                                        __uint_as_float(v[t + 3]));
+                for (int t = 0; t < 32; ++t) blk[lane * 33 + t] = __uint_as_float(v[t]);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int rr = 4 * k + rl, key = k0 + quarter * 32 + rr;
+                    const float *a = blk + rr * 33 + c4;
+                    if (key < p.S)
+                        *reinterpret_cast<float4 *>(out + int64_t(key) * kvd + c + c4) =
+                            make_float4(a[0], a[1], a[2], a[3]);
                 }
+                __syncwarp();
             }
         }
         if (!ok) s_abort = 1;
