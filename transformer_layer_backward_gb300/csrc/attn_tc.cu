@@ -625,16 +625,18 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_tc_dv_kernel(const __gri
 
 // dV[jj, c] = sum over the group's heads g (in order) of part[g][jj, c]
 __global__ void attn_tc_dv_sum_kernel(const float4 *__restrict__ part, float4 *__restrict__ dv, int64_t n4, int G) {
-    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n4; e += int64_t(gridDim.x) * blockDim.x) {
-        float4 s = part[e];
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n4; e += 2 * stride) {
+        const bool two = e + stride < n4;                 // two elements' loads in flight
+        float4 s0 = part[e], s1 = two ? part[e + stride] : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int g = 1; g < G; ++g) {
-            const float4 t = part[int64_t(g) * n4 + e];
-            s.x += t.x;
-            s.y += t.y;
-            s.z += t.z;
-            s.w += t.w;
+            const float4 t0 = part[int64_t(g) * n4 + e];
+            const float4 t1 = two ? part[int64_t(g) * n4 + e + stride] : make_float4(0.f, 0.f, 0.f, 0.f);
+            s0.x += t0.x; s0.y += t0.y; s0.z += t0.z; s0.w += t0.w;
+            s1.x += t1.x; s1.y += t1.y; s1.z += t1.z; s1.w += t1.w;
         }
-        dv[e] = s;
+        dv[e] = s0;
+        if (two) dv[e + stride] = s1;
     }
 }
 

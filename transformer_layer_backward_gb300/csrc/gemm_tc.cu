@@ -389,11 +389,24 @@ __global__ void __launch_bounds__(256) tc_fixup_kernel(const __grid_constant__ T
     const int rows = kBM / gridDim.y, r0 = blockIdx.y * rows;
     for (int e = threadIdx.x; e < rows * (BN / 4); e += blockDim.x) {
         const int r = r0 + e / (BN / 4), c4 = (e % (BN / 4)) * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = en.y; c <= en.z; ++c) {
+        auto part = [&](int c) {
             const int slot = c == en.y ? en.w : 0;
-            const float4 v =
-                *reinterpret_cast<const float4 *>(p.partial + ((int64_t(c) * 2 + slot) * kBM + r) * BN + c4);
+            return *reinterpret_cast<const float4 *>(p.partial + ((int64_t(c) * 2 + slot) * kBM + r) * BN + c4);
+        };
+        // CTA order, four partial tiles' loads in flight at a time
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int c = en.y;
+        for (; c + 3 <= en.z; c += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = part(c + u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
+            }
+        }
+        for (; c <= en.z; ++c) {
+            const float4 v = part(c);
             acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
         }
         const int row = m0 + r, col = n0 + c4;
@@ -404,10 +417,18 @@ __global__ void __launch_bounds__(256) tc_fixup_kernel(const __grid_constant__ T
 
 // fp32 [rows, cols] -> bf16 (round to nearest even), 4 at a time
 __global__ void to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict__ y, int64_t n4) {
-    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n4; i += 4 * stride) {          // four loads in flight per thread
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = x[i + u * stride];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) y[i + u * stride] = pack_bf16x4(v[u].x, v[u].y, v[u].z, v[u].w);
+    }
+    for (; i < n4; i += stride) {
         const float4 v = x[i];
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-        y[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+        y[i] = pack_bf16x4(v.x, v.y, v.z, v.w);
     }
 }
 
@@ -451,7 +472,7 @@ int launch_tc(const TcParams &p, cudaStream_t st) {
         }
     }
     if (f.n == 0) return TLB_OK;
-    tc_fixup_kernel<BN><<<dim3(unsigned(f.n), 16), 256, 0, st>>>(p, f);
+    tc_fixup_kernel<BN><<<dim3(unsigned(f.n), 32), 256, 0, st>>>(p, f);
     return check_launch("tcgen05 gemm fixup");
 }
 
