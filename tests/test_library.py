@@ -106,3 +106,24 @@ def test_workspace_grows_with_rows(lib):
     sizes = [lib.tlb_workspace_bytes(C.byref(cfg), s, s) for s in (1, 64, 512)]
     assert sizes[0] < sizes[1] < sizes[2]
     assert all(s % 256 == 0 for s in sizes)
+
+
+def test_qk_norm_needs_its_inputs(lib):
+    """TLB_QK_NORM without q_raw or gamma_q is refused before any device work; with them
+    the call gets past the input checks to the workspace check."""
+    from transformer_layer_backward_gb300 import _abi as A
+    cfg = A.LayerCfg(64, 256, 4, 2, 16, 4, 8.0, 1e4, 1e-6, 0.25, 0, 0, A.QK_NORM | A.CAUSAL)
+    adam = A.AdamwCfg(1e-4, 0.9, 0.999, 1e-8, 0.0, 16.0, 1)
+    fake = C.c_void_p(256)                       # never dereferenced: the checks fail first
+    w = A.LayerWeights(A.Weight(fake, 1.0), A.Weight(fake, 1.0), A.Weight(fake, 1.0), A.Weight(fake, 1.0),
+                       None, None, None, None)
+    acts = A.LayerActs(fake, fake, fake, None, None, None, None, fake, fake, 16, 32, fake, fake, fake, None)
+    lq = A.Lora(fake, fake, fake, fake, fake, fake, None, None)
+    args = (C.byref(cfg), 8, 8, C.byref(w), C.byref(acts), C.byref(lq), C.byref(lq), C.byref(adam), fake, fake,
+            None, 0, None)
+    assert lib.tlb_layer_backward(*args) == A.TLB_EINVAL
+    assert b"QK_NORM needs q_raw and gamma_q" in lib.tlb_last_error()
+    w.gamma_q = fake
+    acts.q_raw = fake
+    assert lib.tlb_layer_backward(*args) == A.TLB_EINVAL
+    assert b"workspace" in lib.tlb_last_error()
