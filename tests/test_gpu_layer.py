@@ -45,8 +45,16 @@ SEQ_ODD = SEQ512.with_(name="seq_odd_cache", dim=512, ffn_dim=768, n_heads=4, n_
 TINY_QK = TINY.with_(name="tiny_qknorm", qk_norm=True)
 DEC_QK = DEC_F32.with_(name="dec_qknorm", qk_norm=True, cache_len=65)
 SEQ_QK = SEQ_HD64.with_(name="seq_qknorm", qk_norm=True, seq_len=148, cache_len=180)
+# the other compositions on the tensor-core route: pre-norm (dR1 from the RMSNorm kernel,
+# converted for the O-projection product) with ReLU^2 x Mul in the fused epilogue;
+# no residual (the [W_gate | W_up]^T product overwrites d_res and writes its bf16 copy);
+# both norms (the unfused W_down^T product, sub-norm and activation kernels)
+SEQ_PRENORM = SEQ_MHA.with_(name="seq_prenorm", pre_norm=True, act="relu2_mul")
+SEQ_NORESID = SEQ_HD64.with_(name="seq_noresid", residual=False, seq_len=96, cache_len=96)
+SEQ_NORMS = SEQ_HD64.with_(name="seq_norms", sub_norm=True, pre_norm=True, seq_len=64, cache_len=96)
 CASES = {c.name: c for c in (TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512, DEC_F32, DEC_BF16, DEC_G8, DEC_HD256,
-                             SEQ_HD64, SEQ_CACHE, SEQ_MHA, SEQ_ODD, TINY_QK, DEC_QK, SEQ_QK)}
+                             SEQ_HD64, SEQ_CACHE, SEQ_MHA, SEQ_ODD, TINY_QK, DEC_QK, SEQ_QK, SEQ_PRENORM,
+                             SEQ_NORESID, SEQ_NORMS)}
 
 
 def tol(cfg):

@@ -109,15 +109,19 @@ def test_sequence_stack_runs_layers_in_turn(lib):
             check("layer %d %s" % (l, p), host(devs[l]["L"][p]), ref["layers"][l][p])
 
 
-def test_sequence_tensor_core_stack(lib):
+@pytest.mark.parametrize("variant", ["residual", "prenorm"])
+def test_sequence_tensor_core_stack(lib, variant):
     """bf16 layers with S > 1: each layer's first product takes the bf16 copy of d_in that
-    the layer above left in the workspace.  Against the oracle's stack, and bit for bit
-    against the same layers called one at a time (which convert d_hidden themselves)."""
+    the layer above left in the workspace (written by the [W_gate | W_up]^T epilogue, or,
+    with the pre-norm, by the O-projection's conversion).  Against the oracle's stack, and
+    bit for bit against the same layers called one at a time (which convert d_hidden
+    themselves)."""
     import torch
     from synth import SEQ512
     n_layers = 3
     cfg = SEQ512.with_(name="seq_stack", dim=512, ffn_dim=1024, n_heads=8, n_kv_heads=2, head_dim=64, rank=8,
-                       lora_alpha=16.0, seq_len=200, cache_len=200, n_layers=n_layers)
+                       lora_alpha=16.0, seq_len=200, cache_len=200, n_layers=n_layers,
+                       pre_norm=(variant == "prenorm"))
     layers = [layer_inputs(cfg, layer=l, seed=4, with_dout=(l == n_layers - 1)) for l in range(n_layers)]
     dout = layers[-1]["dout"]
     ref = OL.stack_backward(cfg, layers, dout)
