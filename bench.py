@@ -46,7 +46,7 @@ METRIC = "LoRA layer-backward tokens/s"
 UNIT = "tokens/s"
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20000)
@@ -63,7 +63,7 @@ def parse():
     p.add_argument("--workload", default="decode", choices=["decode", "seq512", "seq2048", "stack2048", "sweep"])
     p.add_argument("--qk-norm", action="store_true",
                    help="layers with the per-head QK-norm on q (decode and sequence workloads)")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def decode_bytes(cfg) -> int:
@@ -90,6 +90,15 @@ def decode_kernel_bytes(cfg):
         ("dec_k6 dQpre, gh_q", 2 * qd * 4 * (L // 64) + qd * r * 4),
         ("dec_k7 LoRA grads + AdamW", lora),
     ]
+
+
+def slowest_rank_ms(ms, dist, device="cuda"):
+    """The job's time: the slowest rank's, the same on every rank (a max all-reduce)."""
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def peaks():
@@ -366,10 +375,7 @@ def seq_main(args, rank, world, local, dist):
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
     tlb.workspace_status(ws)
-    t_local = torch.tensor([ms], device="cuda", dtype=torch.float64)
-    if dist is not None:
-        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
-    ms_max = float(t_local.item())
+    ms_max = slowest_rank_ms(ms, dist)
     value = args.steps * S * world / (ms_max / 1e3)
 
     # per-kernel times of one layer, live, inside a CUDA graph of nk layer calls
@@ -817,10 +823,7 @@ def main():
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
     tlb.workspace_status(ws)
-    t_local = torch.tensor([ms], device="cuda", dtype=torch.float64)
-    if dist is not None:
-        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
-    ms_max = float(t_local.item())
+    ms_max = slowest_rank_ms(ms, dist)
     tokens = args.steps * world
     value = tokens / (ms_max / 1e3)
 
