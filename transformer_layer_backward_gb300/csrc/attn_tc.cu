@@ -5,11 +5,11 @@
 //   attn_tc_prep  tf32-rounded copies laid out for TMA (32 x 32 tile transposes):
 //                   dCT [nh][hd][S4]   Kt [nkv][hd][L4]   Vr [nkv][L][hd]
 //   attn_tc_dq    CTA = (head h, 128 queries), 10 warps: TMA producer, MMA issuer, and
-//                 8 epilogue warps (one query row = one TMEM lane and half of the key
-//                 columns per thread).  dCtx_h sits in tensor memory as the A operand of T;
-//                 E goes to tensor memory (two buffers) as the A operand of U; the staged P
-//                 tile is the A operand of W.  Per tile
-//                 of 32 keys j (V_j, K_j^T and the P tile arrive by TMA in two rings, four
+//                 8 epilogue warps in two groups that take alternate key tiles (one query
+//                 row = one TMEM lane per thread).  dCtx_h sits in tensor memory as the A
+//                 operand of T; E replaces T in its tensor-memory buffer (two buffers) and
+//                 is the A operand of U; the staged P tile is the A operand of W.  Per tile
+//                 of 64 keys j (V_j, K_j^T and the P tile arrive by TMA in two rings, two
 //                 tiles deep: V is released when T_j is formed, K^T and P after U and W):
 //                   T  = dCtx_h V_j^T                        tcgen05.mma, T in TMEM
 //                   E  = P (.) T,  D += rowsum(E)            epilogue, fp32
@@ -39,8 +39,8 @@ namespace tlb {
 namespace {
 
 constexpr int kQM = 128;        // queries per dQ CTA
-constexpr int kQK = 32;         // keys per dQ tile
-constexpr int kQSlots = 4;      // dQ tiles in flight (V, K^T, P staged up to four tiles ahead)
+constexpr int kQK = 64;         // keys per dQ tile (two 32-key swizzle atoms)
+constexpr int kQSlots = 2;      // dQ tiles in flight (V, K^T, P staged up to two tiles ahead)
 constexpr int kVK = 128;        // keys per dV CTA
 constexpr int kVQ = 32;         // queries per dV item
 constexpr int kVSlots = 3;      // dV items staged ahead (P tile and dCtx^T tile rings)
@@ -158,25 +158,29 @@ __global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dC
 template <int HD>
 struct DqLayout {
     static constexpr int NB = HD / 32;                   // 128-byte boxes along head_dim
+    static constexpr int NA = kQK / 32;                  // 32-key swizzle atoms of a tile
     // shared memory: two rings of kQSlots slots each, V_j (freed once T_j is formed) and
-    // {K_j^T, P tile} (freed once U and W have taken tile j)
+    // {K_j^T, P tile} (freed once U and W have taken tile j).  K^T and P are NA atoms of
+    // 32 keys each (rows of 128 bytes), side by side.
     static constexpr int V_BYTES = kQK * HD * 4, KT_BYTES = HD * kQK * 4, P_BYTES = kQM * kQK * 4;
+    static constexpr int KT_ATOM = HD * 128, P_ATOM = kQM * 128;
     static constexpr int KSLOT = KT_BYTES + P_BYTES;
     static constexpr int K0 = kQSlots * V_BYTES;
     static constexpr int TOTAL = K0 + kQSlots * KSLOT;
     __host__ __device__ static constexpr int V(int s) { return s * V_BYTES; }
     __host__ __device__ static constexpr int KT(int s) { return K0 + s * KSLOT; }
     __host__ __device__ static constexpr int P(int s) { return K0 + s * KSLOT + KT_BYTES; }
-    // tensor memory columns: dCtx (A of T), T double buffer, U, W, E double buffer (A of U)
-    static constexpr uint32_t TDC = 0, TT = HD, TU = HD + 2 * kQK, TW = TU + HD, TE = TW + HD;
-    static constexpr uint32_t COLS = (TE + 2 * kQK) <= 256 ? 256 : 512;
+    // tensor memory columns: dCtx (A of T), the T double buffer, U, W.  E_j replaces T_j
+    // in its buffer and is the A operand of U; T_j+2 goes there once U_j has completed.
+    static constexpr uint32_t TDC = 0, TT = HD, TU = HD + 2 * kQK, TW = TU + HD;
+    static constexpr uint32_t COLS = (TW + HD) <= 256 ? 256 : 512;
 };
 
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __grid_constant__ AttnTcParams p) {
     using Ly = DqLayout<HD>;
     constexpr int NB = Ly::NB;
-    static_assert(Ly::TE + 2 * kQK <= 512, "tensor memory");
+    static_assert(Ly::TW + HD <= 512 && kQK % 32 == 0, "tensor memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     // vfull/vfree: V ring; kfull/kfree: K^T + P ring; dcready: dCtx in TMEM; tfull: T;
@@ -239,8 +243,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
                     break;
                 }
                 mbar_arrive_expect_tx(&kfull[s], Ly::KSLOT);
-                tma_load_3d(sm + Ly::KT(s), &p.kt, k0, 0, kvh, &kfull[s]);
-                tma_load_3d(sm + Ly::P(s), &p.pq, k0, q0, h, &kfull[s]);
+                for (int a = 0; a < Ly::NA; ++a) {
+                    tma_load_3d(sm + Ly::KT(s) + a * Ly::KT_ATOM, &p.kt, k0 + 32 * a, 0, kvh, &kfull[s]);
+                    tma_load_3d(sm + Ly::P(s) + a * Ly::P_ATOM, &p.pq, k0 + 32 * a, q0, h, &kfull[s]);
+                }
                 s_k_issued = j + 1;
             }
         }
@@ -276,18 +282,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
                 }
                 s_k_used = j + 1;
                 tc_fence_after();
-                const uint64_t kd = sw128_desc(sm + Ly::KT(s)), pd = sw128_desc(sm + Ly::P(s));
-                const uint32_t te = tmem + Ly::TE + uint32_t((j & 1) * kQK);
+                const uint32_t te = tmem + Ly::TT + uint32_t((j & 1) * kQK);    // E_j, where T_j was
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
-                    mma_tf32_ts(tmem + Ly::TU, te + uint32_t(8 * k), kd + 2 * k, id2, acc);
-                    mma_tf32(tmem + Ly::TW, pd + 2 * k, kd + 2 * k, id2, acc);
+                for (int a = 0; a < Ly::NA; ++a) {
+                    const uint64_t kd = sw128_desc(sm + Ly::KT(s) + a * Ly::KT_ATOM);
+                    const uint64_t pd = sw128_desc(sm + Ly::P(s) + a * Ly::P_ATOM);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t acc = (j > 0 || a > 0 || k > 0) ? 1u : 0u;
+                        mma_tf32_ts(tmem + Ly::TU, te + uint32_t(32 * a + 8 * k), kd + 2 * k, id2, acc);
+                        mma_tf32(tmem + Ly::TW, pd + 2 * k, kd + 2 * k, id2, acc);
+                    }
                 }
                 mma_commit(&afree[j & 1]);
                 mma_commit(&kfree[s]);
-                // the epilogue has read T[j % 2] (it arrived on afull after its tensor-memory loads)
-                if (j + 2 < nt && !(ok = mma_t(j + 2))) break;
+                // T_j+2 overwrites E_j: issue it once U_j has read E_j
+                if (j + 2 < nt) {
+                    if (!mbar_wait(&afree[j & 1], (j >> 1) & 1, p.status, 28u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (!(ok = mma_t(j + 2))) break;
+                }
             }
             if (!ok) s_abort = 1;
             mma_commit(&ufull);                     // fires once every MMA issued above is complete
@@ -335,45 +352,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
                 break;
             }
             tc_fence_after();
-            uint32_t t[kQK];
-            tmem_ld32(tmem + Ly::TT + uint32_t((j & 1) * kQK) + lane_off, t);
-            const uint8_t *pt = sm + Ly::P(s);
-            float pv[kQK];
+            // T_j -> E_j in place, one 32-key atom at a time.  The buffer is free: T_j was
+            // issued only after U_j-2 had read E_j-2 from it.
+            const uint32_t tb = tmem + Ly::TT + uint32_t((j & 1) * kQK) + lane_off;
+#pragma unroll 1
+            for (int a = 0; a < Ly::NA; ++a) {
+                uint32_t t[32];
+                tmem_ld32(tb + uint32_t(32 * a), t);
+                uint8_t *pt = sm + Ly::P(s) + a * Ly::P_ATOM;
+                float pv[32];
 #pragma unroll
-            for (int ch = 0; ch < kQK / 4; ++ch) {
-                const float4 v = *reinterpret_cast<const float4 *>(pt + sw128_off(r, ch));
-                pv[4 * ch] = v.x;
-                pv[4 * ch + 1] = v.y;
-                pv[4 * ch + 2] = v.z;
-                pv[4 * ch + 3] = v.w;
-            }
-            const bool diag = k0 + kQK - 1 > jlast;             // masked keys in this row of the tile
-            if (diag) {
+                for (int ch = 0; ch < 8; ++ch) {
+                    const float4 v = *reinterpret_cast<const float4 *>(pt + sw128_off(r, ch));
+                    pv[4 * ch] = v.x;
+                    pv[4 * ch + 1] = v.y;
+                    pv[4 * ch + 2] = v.z;
+                    pv[4 * ch + 3] = v.w;
+                }
+                const int ka = k0 + 32 * a;
+                const bool diag = ka + 31 > jlast;               // masked keys in this row of the atom
+                if (diag) {
 #pragma unroll
-                for (int c = 0; c < kQK; ++c)
-                    if (k0 + c > jlast) pv[c] = 0.f;
-            }
-            tmem_wait_ld();
+                    for (int c = 0; c < 32; ++c)
+                        if (ka + c > jlast) pv[c] = 0.f;
+                }
+                tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < kQK; ++c) {
-                const float e = pv[c] * __uint_as_float(t[c]);
-                D += e;
-                t[c] = to_tf32(e);
-            }
-            // the P tile is the A operand of W += P K_j as staged (the MMA reads tf32); masked
-            // keys of a diagonal tile are zeroed in place
-            if (diag) {
+                for (int c = 0; c < 32; ++c) {
+                    const float e = pv[c] * __uint_as_float(t[c]);
+                    D += e;
+                    t[c] = to_tf32(e);
+                }
+                // the P tile is the A operand of W += P K_j as staged (the MMA reads tf32);
+                // masked keys of a diagonal tile are zeroed in place
+                if (diag) {
 #pragma unroll
-                for (int ch = 0; ch < kQK / 4; ++ch)
-                    st_shared_v4(sm + Ly::P(s) + sw128_off(r, ch), __float_as_uint(pv[4 * ch]),
-                                 __float_as_uint(pv[4 * ch + 1]), __float_as_uint(pv[4 * ch + 2]),
-                                 __float_as_uint(pv[4 * ch + 3]));
-                fence_proxy_async();
+                    for (int ch = 0; ch < 8; ++ch)
+                        st_shared_v4(pt + sw128_off(r, ch), __float_as_uint(pv[4 * ch]),
+                                     __float_as_uint(pv[4 * ch + 1]), __float_as_uint(pv[4 * ch + 2]),
+                                     __float_as_uint(pv[4 * ch + 3]));
+                    fence_proxy_async();
+                }
+                tmem_st32(tb + uint32_t(32 * a), t);
             }
-            // E (tf32) into tensor memory once the U product of tile j - 2 is done with the buffer
-            if (j >= 2 && !mbar_wait(&afree[j & 1], ((j - 2) >> 1) & 1, p.status, 28u)) { ok = false; break; }
-            tc_fence_after();
-            tmem_st32(tmem + Ly::TE + uint32_t((j & 1) * kQK) + lane_off, t);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -389,11 +410,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
             constexpr int half = HD / 2, q4 = HD / 4;
             float *out0 = p.dq + h * HD;
             const float pos = float(p.pos0 + i);
-#pragma unroll 1
             // the rings are idle (every copy consumed, every MMA done): each warp turns its
             // 32-row blocks there so that the stores coalesce
             float *blk = reinterpret_cast<float *>(sm) + (warp - 2) * 32 * 33;
             const int c4 = (lane & 7) * 4, rl = lane >> 3;
+#pragma unroll 1
             for (int c = hf * q4; c < (hf + 1) * q4; c += 16) {      // pairs (c, c + HD / 2)
                 uint32_t u1[16], u2[16], w1[16], w2[16];
                 tmem_ld16(tmem + Ly::TU + uint32_t(c) + lane_off, u1);
