@@ -18,7 +18,9 @@ positions L - S .. L - 1 over a cache of L keys:
 n1 (the normalised attention input) is an independent input here: the pages stop
 the gradient at the Q/V projection outputs, so the backward treats n1 as a
 constant.  ``r1_delta`` adds a perturbation to r1 so that finite differences can
-reach the gradient the backward hands to the layer below.
+reach the gradient the backward hands to the layer below.  With ``cfg.exact_din``
+n1 = [RMSNorm(x_in; g_attn)] instead, so that finite differences in x_in reach the
+exact layer-input gradient (cached k for the S new positions depends on x_in too).
 """
 from __future__ import annotations
 
@@ -64,17 +66,21 @@ def layer_forward(cfg, p, n1, x_in, k_prev, v_prev, r1_delta=None):
     nh, nkv, hd = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
     pos = cfg.pos0 + np.arange(S)
     s = cfg.lora_alpha / cfg.rank
+    exact = getattr(cfg, "exact_din", False)
+    if exact:
+        n1 = rmsnorm(x_in, p["g_attn"], cfg.norm_eps) if cfg.pre_norm else f64(x_in)
     n1 = f64(n1)
     hq = n1 @ f64(p["a_q"]).T
-    q = (n1 @ f64(p["w_q"]) + s * hq @ f64(p["b_q"]).T).reshape(S, nh, hd)
-    k = (n1 @ f64(p["w_k"])).reshape(S, nkv, hd)
+    q = (n1 @ (p.get("s_q", 1.0) * f64(p["w_q"])) + s * hq @ f64(p["b_q"]).T).reshape(S, nh, hd)
+    k = (n1 @ (p.get("s_k", 1.0) * f64(p["w_k"]))).reshape(S, nkv, hd)
     q_raw = q.reshape(S, nh * hd)
+    k_raw = k.reshape(S, nkv * hd)
     if cfg.qk_norm:
         q, k = rmsnorm(q, p["g_q"], cfg.norm_eps), rmsnorm(k, p["g_k"], cfg.norm_eps)
     if cfg.rope:
         q, k = rope(q, pos, cfg.rope_base), rope(k, pos, cfg.rope_base)
     hv = n1 @ f64(p["a_v"]).T
-    v = (n1 @ f64(p["w_v"]) + s * hv @ f64(p["b_v"]).T).reshape(S, nkv, hd)
+    v = (n1 @ (p.get("s_v", 1.0) * f64(p["w_v"])) + s * hv @ f64(p["b_v"]).T).reshape(S, nkv, hd)
     K = np.concatenate([f64(k_prev), k.transpose(1, 0, 2)], axis=1)       # [nkv, L, hd]
     V = np.concatenate([f64(v_prev), v.transpose(1, 0, 2)], axis=1)
     L = K.shape[1]
@@ -109,5 +115,5 @@ def layer_forward(cfg, p, n1, x_in, k_prev, v_prev, r1_delta=None):
         vc = V.transpose(1, 0, 2).reshape(L, nkv * hd)
     cache = dict(x=n1, gate=gate, up=up, silu_gate=f64(gate) / (1.0 + np.exp(-f64(gate))),
                  hidden=hid, r1=r1, ctx=ctx, k=kc, v=vc, attn=P, lora_q_h=hq, lora_v_h=hv,
-                 q_raw=q_raw)
+                 q_raw=q_raw, k_raw=k_raw, q=q.reshape(S, nh * hd), x_in=f64(x_in))
     return out, cache

@@ -29,14 +29,22 @@ state of one layer as float arrays.  Order of the steps:
     Q adapter from dQpre, V adapter from dV, both with x = attn_input
     AdamW on A (lr) and B (lr * lr_b_mult); B is read before its update.
   d_in = dR1 (the gradient handed to the next layer down).
+
+With ``cfg.exact_din`` (beyond the pages, which stop at the projection outputs) d_in
+is the exact gradient of the layer input x_in, n1 = [RMSNorm(x_in; g_attn)]:
+    dK_h  = scale dS_h^T Q_h summed over the group, rows of the S new positions, then
+            RoPE_bwd and, with the QK-norm, RMSNorm_bwd(k_raw, g_k, .) per head
+    dn1   = s_q dQpre W_Q^T + s_k dK W_K^T + s_v dV W_V^T + gh_q A_q + gh_v A_v
+            (gh = s G B with B and A before their update: the LoRA-A paths)
+    d_in  = [dR1] + [RMSNorm_bwd(x_in, g_attn, dn1)]        (residual, pre-norm)
 """
 from __future__ import annotations
 
 import numpy as np
 
 from .ops import (adamw, apply_backward, f64, linear_backward, lora_backward,
-                  relu2_mul_backward, rmsnorm_backward, rope_backward, score_backward_q,
-                  silu_mul_backward, softmax_backward, value_backward)
+                  relu2_mul_backward, rmsnorm_backward, rope_backward, score_backward_k,
+                  score_backward_q, silu_mul_backward, softmax_backward, value_backward)
 
 
 def kv_heads_first(a, cfg) -> np.ndarray:
@@ -86,8 +94,32 @@ def attn_backward(cfg, d, dR1) -> dict:
     if getattr(cfg, "qk_norm", False):
         dQpre = rmsnorm_backward(f64(d["q_raw"]).reshape(S, nh, hd), d["g_q"], dQpre, cfg.norm_eps)
     dV = dV_all[:, cfg.pos0:, :].transpose(1, 0, 2).reshape(S, nkv * hd)
-    return dict(dSub=dSub, dCtx=dCtx, dS=dS_all, dQ=dQ.reshape(S, nh * hd),
-                dQpre=dQpre.reshape(S, nh * hd), dV=dV)
+    out = dict(dSub=dSub, dCtx=dCtx, dS=dS_all, dQ=dQ.reshape(S, nh * hd),
+               dQpre=dQpre.reshape(S, nh * hd), dV=dV)
+    if getattr(cfg, "exact_din", False):
+        # key gradient of the S new cache rows (the older rows are constants)
+        Q = f64(d["q"]).reshape(S, nh, hd)
+        dK_all = np.zeros((nkv, L, hd))
+        for h in range(nh):
+            dK_all[h // group] += score_backward_k(dS_all[h], Q[:, h, :], cfg.attn_scale)
+        dK = dK_all[:, cfg.pos0:, :].transpose(1, 0, 2)                 # [S, nkv, hd]
+        dKpre = rope_backward(dK, pos, cfg.rope_base) if cfg.rope else dK
+        if getattr(cfg, "qk_norm", False):
+            dKpre = rmsnorm_backward(f64(d["k_raw"]).reshape(S, nkv, hd), d["g_k"], dKpre, cfg.norm_eps)
+        out["dKpre"] = dKpre.reshape(S, nkv * hd)
+    return out
+
+
+def input_backward(cfg, d, r) -> np.ndarray:
+    """Exact layer-input gradient (``cfg.exact_din``): the attention input n1 feeds the
+    Q, K and V projections and both LoRA A products; x_in reaches r1 through the
+    residual and n1 through the attention pre-norm."""
+    dn1 = (linear_backward(r["dQpre"], d["w_q"], d.get("s_q", 1.0)) +
+           linear_backward(r["dKpre"], d["w_k"], d.get("s_k", 1.0)) +
+           linear_backward(r["dV"], d["w_v"], d.get("s_v", 1.0)) +
+           r["gh_q"] @ f64(d["a_q"]) + r["gh_v"] @ f64(d["a_v"]))
+    dx = rmsnorm_backward(d["x_in"], d["g_attn"], dn1, cfg.norm_eps) if cfg.pre_norm else dn1
+    return r["dR1"] + dx if cfg.residual else dx
 
 
 def lora_adamw(cfg, d, dQpre, dV) -> dict:
@@ -109,7 +141,7 @@ def layer_backward(cfg, d, dout) -> dict:
     r = ffn_backward(cfg, d, dout)
     r.update(attn_backward(cfg, d, r["dR1"]))
     r.update(lora_adamw(cfg, d, r["dQpre"], r["dV"]))
-    r["d_in"] = r["dR1"]
+    r["d_in"] = input_backward(cfg, d, r) if getattr(cfg, "exact_din", False) else r["dR1"]
     return r
 
 

@@ -82,6 +82,15 @@ def score_backward_q(dscores_h, k_h, scale: float) -> np.ndarray:
     return float(scale) * (f64(dscores_h) @ f64(k_h))
 
 
+def score_backward_k(dscores_h, q_h, scale: float) -> np.ndarray:
+    """Key gradient of scores = scale * q k^T (one head): dK[s] = scale * sum_q dScores[q, s] q[q].
+
+    The pages stop the backward at the Q / V projection outputs and print no key
+    gradient; this is the plain derivative, used only for the exact layer-input gradient.
+    """
+    return float(scale) * (f64(dscores_h).T @ f64(q_h))
+
+
 def value_backward(attn_h, dctx_h) -> np.ndarray:
     """[RS] attention block: grad_v[k] += attn[q, k] * grad_context[q], summed over queries q."""
     return f64(attn_h).T @ f64(dctx_h)

@@ -32,6 +32,9 @@ class LayerConfig:
     residual: bool = True    # out = r1 + f and r1 = x + a
     rope: bool = True        # NeoX split-half rotary embedding on q and k
     qk_norm: bool = False    # per-head RMSNorm of q and k over head_dim, before RoPE
+    exact_din: bool = False  # the layer-input gradient also through the Q/K/V projections,
+                             # their LoRA paths and the attention pre-norm (the pages stop
+                             # at the projection outputs); oracle only
     kv_layout: str = "shd"   # "shd": [L, n_kv*hd]   "hsd": [n_kv, L, hd]
     rope_base: float = 10000.0
     norm_eps: float = 1e-6

@@ -17,7 +17,10 @@ Recipe (distributions follow the workload descriptions):
     query may see (key j visible to query i iff j <= L - S + i), zero elsewhere;
   * the cached SiLU output is silu(gate) and the cached LoRA activations are
     x @ A^T, both formed in float64 from the values above and then rounded;
-  * with the QK-norm, the Q projection before it ~ N(0, 1) and its gain ~ U(0.5, 1.5).
+  * with the QK-norm, the Q projection before it ~ N(0, 1) and its gain ~ U(0.5, 1.5);
+  * for the exact layer-input gradient: W_Q, W_K, W_V like the other weights, the layer
+    input, the cached (rotated) q and, with the QK-norm, the new rows of k before it
+    ~ N(0, 1), and the attention pre-norm and k-norm gains ~ U(0.5, 1.5).
 """
 from __future__ import annotations
 
@@ -94,6 +97,17 @@ def layer_inputs(cfg: LayerConfig, layer: int = 0, seed: int = 0, with_dout: boo
     if cfg.qk_norm:
         d["q_raw"] = _n(seed, cfg, layer, "q_raw", (S, qd)).astype(f32)
         d["g_q"] = _u(seed, cfg, layer, "g_q", (cfg.head_dim,), 0.5, 1.5).astype(f32)
+    if cfg.exact_din:
+        d["w_q"], d["s_q"] = _weight(seed, cfg, layer, "w_q", (H, qd))
+        d["w_k"], d["s_k"] = _weight(seed, cfg, layer, "w_k", (H, kvd))
+        d["w_v"], d["s_v"] = _weight(seed, cfg, layer, "w_v", (H, kvd))
+        d["x_in"] = _n(seed, cfg, layer, "layer_input", (S, H)).astype(f32)
+        d["q"] = _n(seed, cfg, layer, "q_cache", (S, qd)).astype(f32)
+        if cfg.pre_norm:
+            d["g_attn"] = _u(seed, cfg, layer, "g_attn", (H,), 0.5, 1.5).astype(f32)
+        if cfg.qk_norm:
+            d["k_raw"] = _n(seed, cfg, layer, "k_raw", (S, kvd)).astype(f32)
+            d["g_k"] = _u(seed, cfg, layer, "g_k", (cfg.head_dim,), 0.5, 1.5).astype(f32)
     # LoRA adapters and their AdamW state
     d["a_q"] = _n(seed, cfg, layer, "lora_a_q", (r, H), cfg.lora_a_std).astype(f32)
     d["b_q"] = _n(seed, cfg, layer, "lora_b_q", (qd, r), cfg.lora_b_std).astype(f32)

@@ -55,13 +55,15 @@ def make_problem(cfg, seed=1):
     v_prev = rs.normal(size=(nkv, L - S, hd))
     dout = rs.normal(size=(S, H))
     p["g_q"], p["g_k"] = rs.uniform(0.5, 1.5, hd), rs.uniform(0.5, 1.5, hd)
+    p["g_attn"] = rs.uniform(0.5, 1.5, H)
     return p, n1, x_in, k_prev, v_prev, dout
 
 
 def backward_inputs(cfg, p, cache):
     d = dict(cache)
     for k in ("w_o", "w_gate", "w_up", "w_down", "s_o", "s_gate", "s_up", "s_down",
-              "g_sub_attn", "g_ffn", "g_sub_ffn", "g_q", "a_q", "b_q", "a_v", "b_v"):
+              "g_sub_attn", "g_ffn", "g_sub_ffn", "g_q", "g_k", "g_attn", "w_q", "w_k", "w_v",
+              "a_q", "b_q", "a_v", "b_v"):
         d[k] = p[k]
     for k in ("a_q", "b_q", "a_v", "b_v"):
         d["m_" + k] = np.zeros_like(p[k])
@@ -117,6 +119,42 @@ def test_layer_backward_matches_finite_differences(case):
         dl[idx] = h
         fd[idx] = (loss(p, dl) - loss(p, -dl)) / (2 * h)
     assert np.max(np.abs(fd - r["d_in"])) <= 1e-6 * max(1.0, np.max(np.abs(r["d_in"]))), case
+
+
+EXACT_CASES = {
+    "exact_all_norms_gqa": small_cfg(exact_din=True),
+    "exact_qk_norm_swiglu": small_cfg(exact_din=True, qk_norm=True, act="silu_mul", sub_norm=False),
+    "exact_decode_hsd": small_cfg(exact_din=True, seq_len=1, cache_len=6, kv_layout="hsd"),
+    "exact_no_residual_no_prenorm_mha": small_cfg(exact_din=True, n_kv_heads=4, pre_norm=False,
+                                                  residual=False, seq_len=4, cache_len=4),
+}
+
+
+@pytest.mark.parametrize("case", sorted(EXACT_CASES))
+def test_exact_input_gradient_matches_finite_differences(case):
+    """The exact layer-input gradient (through Q, K, V, their LoRA paths and the
+    attention pre-norm, beyond the pages' truncation) against central differences in the
+    layer input x_in of a forward where n1 = [RMSNorm(x_in)]."""
+    cfg = EXACT_CASES[case]
+    p, n1, x_in, k_prev, v_prev, dout = make_problem(cfg)
+    out, cache = F.layer_forward(cfg, p, n1, x_in, k_prev, v_prev)
+    r = Lyr.layer_backward(cfg, backward_inputs(cfg, p, cache), dout)
+
+    def loss(xx):
+        o, _ = F.layer_forward(cfg, p, n1, xx, k_prev, v_prev)
+        return float(np.sum(dout * o))
+
+    h = 1e-6
+    fd = np.zeros_like(x_in)
+    for idx in np.ndindex(*x_in.shape):
+        xp, xm = x_in.copy(), x_in.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fd[idx] = (loss(xp) - loss(xm)) / (2 * h)
+    an = r["d_in"]
+    assert np.max(np.abs(fd - an)) <= 1e-6 * max(1.0, np.max(np.abs(an))), case
+    # the truncated reading differs from it by the Q / K / V paths, which are not small here
+    assert np.max(np.abs(an - r["dR1"] * (1.0 if cfg.residual else 0.0))) > 1e-2, case
 
 
 def test_linear_backward_is_the_adjoint():
