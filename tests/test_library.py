@@ -100,6 +100,15 @@ def test_stack_host_side_errors(lib):
     assert b"NULL layer array" in lib.tlb_last_error()
 
 
+def test_stack_workspace_sets(lib):
+    """Single-token stacks rotate four layer workspaces; longer layers share one."""
+    from transformer_layer_backward_gb300 import _abi as A
+    cfg = A.LayerCfg(256, 512, 8, 2, 64, 4, 8.0, 1e4, 1e-6, 0.125, 1, 1, 4 | 8 | 32)
+    one = lambda S, L: (lib.tlb_workspace_bytes(C.byref(cfg), S, L) + 255) // 256 * 256
+    assert lib.tlb_stack_workspace_bytes(C.byref(cfg), 1, 40) == 4 * one(1, 40)
+    assert lib.tlb_stack_workspace_bytes(C.byref(cfg), 64, 96) == one(64, 96)
+
+
 def test_workspace_grows_with_rows(lib):
     from transformer_layer_backward_gb300 import _abi as A
     cfg = A.LayerCfg(2560, 9728, 32, 8, 128, 16, 32.0, 1e4, 1e-6, 128 ** -0.5, 1, 1, 4 | 8 | 32)
