@@ -44,3 +44,22 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     import bench
     bench.run_reference(bench.parse(["--impl", "reference"]), rank=1, world=2)     # a non-zero rank returns without work
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_json_line():
+    """bench.py --impl reference (the float64 oracle on the host cores) prints one JSON
+    line with the keys the contract fixes."""
+    import json
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(here, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "1", "--cpu-seconds", "0.5"], capture_output=True, text=True, timeout=600,
+                         cwd=here, check=True).stdout.strip().splitlines()
+    line = json.loads(out[-1])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["value"] > 0 and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
