@@ -183,8 +183,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
     static_assert(Ly::TW + HD <= 512 && kQK % 32 == 0, "tensor memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    // vfull/vfree: V ring; kfull/kfree: K^T + P ring; dcready: dCtx in TMEM; tfull: T;
-    // afull/afree: E in TMEM (and the masked P tile in shared memory), double-buffered
+    // vfull/vfree: V ring; kfull/kfree: K^T + P ring; dcready: dCtx in TMEM; tfull: T_j in
+    // its buffer; afull: E_j written over it (and the masked P tile in shared memory);
+    // afree: U_j has read E_j, so T_j+2 may take the buffer.  Per buffer, double-buffered.
     __shared__ uint64_t vfull[kQSlots], vfree[kQSlots], kfull[kQSlots], kfree[kQSlots], dcready, tfull[2], afull[2],
         afree[2], ufull;
     __shared__ uint32_t tmem_base;
