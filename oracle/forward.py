@@ -117,3 +117,17 @@ def layer_forward(cfg, p, n1, x_in, k_prev, v_prev, r1_delta=None):
                  hidden=hid, r1=r1, ctx=ctx, k=kc, v=vc, attn=P, lora_q_h=hq, lora_v_h=hv,
                  q_raw=q_raw, k_raw=k_raw, q=q.reshape(S, nh * hd), x_in=f64(x_in))
     return out, cache
+
+
+def stack_forward(cfg, params, n1s, x_in, k_prevs, v_prevs):
+    """Layers 0 .. n-1 applied in order ([RS] backward_through_layers runs them in reverse):
+    layer l's output is layer l+1's input x_in (its residual input and, with
+    ``cfg.exact_din``, the input of its attention pre-norm).  Without ``exact_din`` each
+    layer's n1 is its own independent input, as in ``layer_forward``.
+    Returns (output of the last layer, [cache of each layer])."""
+    x = f64(x_in)
+    caches = []
+    for l in range(len(params)):
+        x, c = layer_forward(cfg, params[l], n1s[l], x, k_prevs[l], v_prevs[l])
+        caches.append(c)
+    return x, caches

@@ -157,6 +157,77 @@ def test_exact_input_gradient_matches_finite_differences(case):
     assert np.max(np.abs(an - r["dR1"] * (1.0 if cfg.residual else 0.0))) > 1e-2, case
 
 
+STACK_CASES = {
+    "stack_truncated_all_norms_gqa": small_cfg(),
+    "stack_truncated_swiglu_residual": small_cfg(act="silu_mul", sub_norm=False, pre_norm=False,
+                                                 seq_len=4, cache_len=4),
+    "stack_exact_prenorm_qk_norm": small_cfg(exact_din=True, qk_norm=True, sub_norm=False),
+}
+
+
+@pytest.mark.parametrize("case", sorted(STACK_CASES))
+def test_stack_backward_matches_finite_differences(case):
+    """The layer loop ([RS] backward_through_layers: layers in reverse, layer l's input
+    gradient is layer l-1's output gradient, gnorm = sqrt of the sum over every layer of
+    ||dA_q||^2 + ||dA_v||^2 with dB left out) against central differences of <dOut, out>
+    of two composed layers with weights of their own, in both layers' adapters and in the
+    stack input.  Also shows that the plausible mistakes (forward order, dOut handed to
+    every layer, dB counted in the gnorm) would change the result by far more than the
+    tolerance."""
+    cfg = STACK_CASES[case]
+    probs = [make_problem(cfg, seed=21 + l) for l in range(2)]
+    params = [pr[0] for pr in probs]
+    n1s = [pr[1] for pr in probs]
+    x0 = probs[0][2]
+    kps, vps = [pr[3] for pr in probs], [pr[4] for pr in probs]
+    dout = probs[1][5]
+    out, caches = F.stack_forward(cfg, params, n1s, x0, kps, vps)
+    layers = [backward_inputs(cfg, params[l], caches[l]) for l in range(2)]
+    res = Lyr.stack_backward(cfg, layers, dout)
+
+    def loss(ps, x=x0):
+        o, _ = F.stack_forward(cfg, ps, n1s, x, kps, vps)
+        return float(np.sum(dout * o))
+
+    h = 1e-6
+    fd_sa = fd_sb = 0.0
+    for l in range(2):
+        for pname, gname in (("a_q", "dA_q"), ("b_q", "dB_q"), ("a_v", "dA_v"), ("b_v", "dB_v")):
+            fd = np.zeros_like(params[l][pname])
+            for idx in np.ndindex(*fd.shape):
+                vals = []
+                for sgn in (1.0, -1.0):
+                    ps = [dict(p) for p in params]
+                    w = params[l][pname].copy()
+                    w[idx] += sgn * h
+                    ps[l][pname] = w
+                    vals.append(loss(ps))
+                fd[idx] = (vals[0] - vals[1]) / (2 * h)
+            an = res["layers"][l][gname]
+            assert np.max(np.abs(fd - an)) <= 1e-6 * max(1.0, np.max(np.abs(an))), (case, l, gname)
+            assert np.max(np.abs(an)) > 1e-3, (case, l, gname, "gradient unexpectedly tiny")
+            if gname.startswith("dA"):
+                fd_sa += float(np.sum(fd * fd))
+            else:
+                fd_sb += float(np.sum(fd * fd))
+    fdx = np.zeros_like(x0)
+    for idx in np.ndindex(*x0.shape):
+        xp, xm = x0.copy(), x0.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fdx[idx] = (loss(params, xp) - loss(params, xm)) / (2 * h)
+    assert np.max(np.abs(fdx - res["d_in"])) <= 1e-6 * max(1.0, np.max(np.abs(res["d_in"]))), case
+    # the reported norms against the finite-difference gradients themselves
+    assert abs(res["gnorm"] - math.sqrt(fd_sa)) <= 1e-6 * math.sqrt(fd_sa), case
+    assert abs(res["gnorm_full"] - math.sqrt(fd_sa + fd_sb)) <= 1e-6 * math.sqrt(fd_sa + fd_sb), case
+    # the mistakes the pins must catch move the results well past the tolerance
+    assert fd_sb > 1e-2 * fd_sa, (case, "dB too small to tell the gnorm readings apart")
+    wrong = Lyr.layer_backward(cfg, layers[0], dout)          # layer 0 fed dOut, not d_in of layer 1
+    assert np.max(np.abs(wrong["dA_q"] - res["layers"][0]["dA_q"])) > 1e-3 * np.max(np.abs(wrong["dA_q"])), case
+    fwd = Lyr.layer_backward(cfg, layers[1], wrong["d_in"])    # forward order
+    assert np.max(np.abs(fwd["dA_v"] - res["layers"][1]["dA_v"])) > 1e-3 * np.max(np.abs(fwd["dA_v"])), case
+
+
 def test_linear_backward_is_the_adjoint():
     rs = np.random.default_rng(2)
     x, w, dy = rs.normal(size=(5, 7)), rs.normal(size=(7, 3)), rs.normal(size=(5, 3))
