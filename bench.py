@@ -1,29 +1,27 @@
 """Throughput of the LoRA layer backward on one GB300 (or N independent replicas).
 
-Workload: the single-token decode layer backward (dim 2560, ffn 6912, 20 heads /
-5 KV heads of 128, cache 1024, ternary int8 weights, ReLU^2 x Mul FFN with
-sub-norms, pre-norm residual, RoPE, LoRA rank 16 on Q and V, AdamW + LoRA+).
-One step = one call of tlb_layer_backward for one token through one layer.
-Steps cycle through NL distinct layers (weights, caches and adapters), so the
-working set (NL x 68 MB) is several times the 129 MB L2 and each step reads its
-inputs from HBM.
+Default workload (stack2048): the 36-layer stack backward at S = L = 2048 (dim 2560,
+ffn 9728, 32/8 heads x 128, SwiGLU FFN, RoPE, residual, bf16 weights, LoRA rank 16 on Q
+and V, AdamW + LoRA+).  One step = one tlb_stack_backward call: grad_hidden [2048, 2560]
+through 36 distinct layers (weights, caches and adapters of their own, ~1 GB each), in
+reverse, every layer's adapters updated.  tokens/s = 2048 / step time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tlb|reference]
-                  [--workload decode|seq512|seq2048|stack2048|sweep]
+                  [--workload stack2048|seq2048|seq512|decode|sweep]
 
---impl reference times the float64 CPU oracle (the only other implementation of
-this path available here) on the same workload.  Under torchrun every rank runs
-its own replica (the path has no exchange step); rank 0 prints one JSON line.
+--impl reference times the float64 CPU oracle (the only other implementation of this
+path available here) on the same workload: each step one 512-row causal slice of an
+S = L = 2048 layer (the four slices in turn hold the layer's whole work), extrapolated
+to the 36 layers of a step.  Under torchrun every rank runs its own replica (the path
+has no exchange step); rank 0 prints one JSON line.
 
-The sequence workloads (bf16 weights, SwiGLU, RoPE, residual, GQA 32/8 x 128, LoRA
-rank 16; the tcgen05 path): seq512 and seq2048 time one layer backward of S tokens
-per step; stack2048 times the 36-layer stack (S = 2048) per step, d_in of each layer
-feeding the next.  Their inputs are drawn on the device with torch's seeded
-generator, with the shapes and distributions of the parity inputs.
-
---workload sweep measures the standalone fp32 kernels (softmax, RMSNorm, RoPE, gated
-activations, AdamW) over their size ranges, one case after another, and reports
-per-case GB/s; the headline value is the lowest among the cases above 4 x L2.
+Other workloads: seq512 / seq2048 time one sequence layer backward of S tokens per
+step; decode the single-token layer backward (dim 2560, ffn 6912, 20 / 5 heads of 128,
+cache 1024, ternary int8 weights, ReLU^2 x Mul with sub-norms and pre-norm); sweep the
+standalone fp32 kernels (softmax, RMSNorm, RoPE, gated activations, AdamW) over their
+size ranges, per-case GB/s, the headline the lowest among the cases above 4 x L2.
+The sequence inputs are drawn on the device with torch's seeded generator, with the
+shapes and distributions of the parity inputs.
 """
 from __future__ import annotations
 
@@ -49,10 +47,11 @@ UNIT = "tokens/s"
 def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20000)
-    p.add_argument("--warmup", type=int, default=2000)
+    p.add_argument("--steps", type=int, default=None, help="timed steps (default: decode 20000, stack2048 30, others 200)")
+    p.add_argument("--warmup", type=int, default=None, help="untimed steps (default: decode 2000, others 5)")
     p.add_argument("--impl", default="tlb", choices=["tlb", "reference"])
-    p.add_argument("--layers", type=int, default=8)
+    p.add_argument("--layers", type=int, default=None,
+                   help="distinct layers (weights, caches, adapters) cycled: decode 8, stack the depth, layers 2")
     p.add_argument("--e2e-steps", type=int, default=2000)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-graph", action="store_true")
@@ -60,10 +59,15 @@ def parse(argv=None):
                    help="decode: also time the layer inside a stack of this many layers (0: skip)")
     p.add_argument("--cases", default=None,
                    help="sweep: run only the cases whose 'kernel shape' label matches this regex")
-    p.add_argument("--workload", default="decode", choices=["decode", "seq512", "seq2048", "stack2048", "sweep"])
+    p.add_argument("--workload", default="stack2048", choices=["decode", "seq512", "seq2048", "stack2048", "sweep", "tf32peak"])
     p.add_argument("--qk-norm", action="store_true",
                    help="layers with the per-head QK-norm on q (decode and sequence workloads)")
-    return p.parse_args(argv)
+    a = p.parse_args(argv)
+    if a.steps is None:
+        a.steps = {"decode": 20000, "stack2048": 30}.get(a.workload, 200)
+    if a.warmup is None:
+        a.warmup = 2000 if a.workload == "decode" else 5
+    return a
 
 
 def decode_bytes(cfg) -> int:
@@ -189,18 +193,25 @@ def run_reference(args, rank, world):
         print(json.dumps(line), flush=True)
         return
     if args.workload != "decode":
-        per = max(args.cpu_seconds / max(args.steps, 1), 0.0)
-        vals = [seq_cpu_baseline(per)["value"] for _ in range(args.steps)]
-        v = statistics.mean(vals)
-        cpu = seq_cpu_baseline(0.0)
-        cpu["value"] = v
+        # one step = one row slice of the full-size layer (the slices in turn cover the
+        # layer's work), extrapolated to the step's depth
+        cfg, depth = seq_config(args.workload)
+        if args.qk_norm:
+            cfg = cfg.with_(qk_norm=True)
+        slices = seq_cpu_sample(cfg)
+        for k in range(min(args.warmup, 1)):
+            seq_cpu_time(slices[k])
+        times = [seq_cpu_time(slices[k % SLICES]) for k in range(args.steps)]
+        tok = cfg.seq_len // SLICES
+        v = args.steps * tok / (sum(times) * depth)
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 512 / v * 1e3, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": "sequence layer backward sample: one S = 512 layer per step "
-                                       "(float64 oracle on the host cores)", "global_batch": 1, "seq_len": 512,
-                           "parallelism": "replicas"},
-                "cpu_baseline": cpu,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": sum(times) * depth / args.steps * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (host generator)", "config": seq_workload_config(cfg, depth, world),
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
+                                 "sample": "each step: the float64 numpy oracle on one %d-row causal slice of an "
+                                           "S = L = %d layer (slices 0..%d in turn, together the layer's whole "
+                                           "work), x %d layers" % (tok, cfg.seq_len, SLICES - 1, depth)},
                 "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -237,46 +248,12 @@ def seq_config(workload):
     return SEQ512.with_(name=workload, seq_len=2048, cache_len=2048), (36 if workload == "stack2048" else 1)
 
 
-def device_layer(cfg, layer, seed=0):
-    """One layer's weights, caches, adapters and dOut on the device (bf16 weights),
-    drawn with the distributions of the parity inputs: weights N(0, weight_std^2),
-    activations and caches N(0, 1), attn = causal softmax of N(0, attn_logit_std^2)
-    logits, LoRA A and B N(0, 0.02^2), h = x A^T, AdamW moments zero."""
-    import torch
-    g = torch.Generator(device="cuda")
-    g.manual_seed(1000003 * seed + 7919 * layer + 17)
-    S, L, H, I, qd, kvd, r = cfg.seq_len, cfg.cache_len, cfg.dim, cfg.ffn_dim, cfg.q_dim, cfg.kv_dim, cfg.rank
-    n = lambda *shape, std=1.0: torch.randn(*shape, device="cuda", generator=g) * std
-    t = {}
-    for k, shape in (("w_down", (I, H)), ("w_gate", (H, I)), ("w_up", (H, I)), ("w_o", (qd, H))):
-        t[k] = n(*shape, std=cfg.weight_std).to(torch.bfloat16)
-    for k, shape in (("x", (S, H)), ("gate", (S, I)), ("up", (S, I)), ("dout", (S, H)),
-                     ("k", (L, kvd)), ("v", (L, kvd))):
-        t[k] = n(*shape)
-    t["silu_gate"] = torch.nn.functional.silu(t["gate"])
-    pos0 = L - S
-    attn = torch.empty(cfg.n_heads, S, L, device="cuda")
-    mask = torch.arange(L, device="cuda")[None, :] > (pos0 + torch.arange(S, device="cuda"))[:, None]
-    for h in range(cfg.n_heads):
-        logits = n(S, L, std=cfg.attn_logit_std).masked_fill_(mask, float("-inf"))
-        attn[h] = torch.softmax(logits, dim=-1)
-    t["attn"] = attn
-    for k, shape in (("a_q", (r, H)), ("b_q", (qd, r)), ("a_v", (r, H)), ("b_v", (kvd, r))):
-        t[k] = n(*shape, std=0.02)
-        t["m_" + k] = torch.zeros_like(t[k])
-        t["v_" + k] = torch.zeros_like(t[k])
-    t["lora_q_h"] = t["x"] @ t["a_q"].t()
-    t["lora_v_h"] = t["x"] @ t["a_v"].t()
-    if cfg.qk_norm:                       # Q projection before the per-head norm, the norm's gain
-        t["q_raw"] = n(S, qd)
-        t["g_q"] = torch.rand(cfg.head_dim, device="cuda", generator=g) + 0.5
-    return t
-
-
 def seq_kernel_flops(cfg, names):
     """Algorithmic flops of each kernel of one sequence layer, by launch order: the
     three tcgen05 GEMMs are W_down^T, [W_gate | W_up]^T and W_O^T; the attention counts
-    the visible (query, key) pairs; 'tf32' marks the attention contractions."""
+    the visible (query, key) pairs of the contractions the method needs (dAttn and dQ in
+    the dQ kernel, dV in the dV kernel), not the extra P K product of its U - D W split;
+    'tf32' marks the attention contractions."""
     S, L, H, I, qd = cfg.seq_len, cfg.cache_len, cfg.dim, cfg.ffn_dim, cfg.q_dim
     pairs = S * (L - S) + S * (S + 1) // 2
     gemm = [2 * S * I * H, 2 * S * H * 2 * I, 2 * S * qd * H]
@@ -285,8 +262,8 @@ def seq_kernel_flops(cfg, names):
         if nm == "tcgen05 gemm":
             out.append((gemm[gi] if gi < 3 else 0, "bf16"))
             gi += 1
-        elif nm == "attn_tc_dq":
-            out.append((3 * 2 * pairs * cfg.head_dim * cfg.n_heads, "tf32"))
+        elif nm == "attn_tc_dq":            # dAttn = dCtx V^T and dQ = dS K
+            out.append((2 * 2 * pairs * cfg.head_dim * cfg.n_heads, "tf32"))
         elif nm == "attn_tc_dv":
             out.append((2 * pairs * cfg.head_dim * cfg.n_heads, "tf32"))
         else:
@@ -294,10 +271,31 @@ def seq_kernel_flops(cfg, names):
     return out
 
 
+def seq_workload_config(cfg, depth, world):
+    """The config dict of a sequence workload: the same for both arms."""
+    name = ("%d-layer stack backward, S = L = %d" % (depth, cfg.seq_len) if depth > 1 else
+            "sequence layer backward, S = L = %d" % cfg.seq_len)
+    return {"workload": name + ": dim 2560, ffn 9728, 32/8 heads x 128, SwiGLU, RoPE, residual, " +
+                        ("QK-norm on q, " if cfg.qk_norm else "") + "bf16 weights, LoRA r16 Q/V, AdamW+LoRA+",
+            "global_batch": world, "seq_len": cfg.seq_len, "layers_per_step": depth,
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "inputs > L2 (each layer: weights 170 MB, attn %.0f MB)" % (cfg.n_heads * cfg.seq_len * cfg.cache_len * 4 / 1e6)}
+
+
+def tf32_peak(bf16_sustained):
+    """(TF/s, source) of the dense tf32 peak: the committed measurement of a cuBLAS tf32
+    GEMM (the method of the bf16 figures), else the bf16 figure x the nominal 1.1/2.25."""
+    prof = os.path.join(ROOT, "profiles", "tf32_peak.json")
+    if os.path.exists(prof):
+        m = json.load(open(prof))
+        return m["tf32_tflops_sustained"], "profiles/tf32_peak.json tf32_tflops_sustained (of measured)"
+    return bf16_sustained * 1.1 / 2.25, "bf16 sustained x nominal 1.1/2.25 (derived)"
+
+
 def seq_main(args, rank, world, local, dist):
     import torch
     import transformer_layer_backward_gb300 as tlb
-    from tests.helpers import adam_to_abi, cfg_to_abi
+    from synth.device import device_layer
 
     torch.cuda.set_device(local)
     tlb.load()
@@ -305,9 +303,9 @@ def seq_main(args, rank, world, local, dist):
     if args.qk_norm:
         cfg = cfg.with_(qk_norm=True)
     S, L = cfg.seq_len, cfg.cache_len
-    NL = 2 if depth == 1 and S <= 512 else (2 if depth > 1 else 1)
-    c = cfg_to_abi(tlb, cfg)
-    adam = adam_to_abi(tlb, cfg)
+    NL = args.layers or (depth if depth > 1 else 2)     # distinct layers (weights, caches, adapters)
+    c = tlb.layer_cfg_of(cfg)
+    adam = tlb.adamw_cfg_of(cfg)
     layers = []
     for l in range(NL):
         t = device_layer(cfg, l, seed=rank)
@@ -323,12 +321,13 @@ def seq_main(args, rank, world, local, dist):
         tlb.layer_backward(c, S, L, ly["w"], ly["a"], ly["lq"], ly["lv"], adam, dh, ss, ws)
 
     if depth > 1:
-        # the stack entry point, layer l of the stack being distinct layer l % NL
+        # the stack entry point; layer l of the stack is distinct layer l % NL
         sws = tlb.stack_workspace(c, S, L)
         sW, sA, sQ, sV = ([layers[l % NL][k] for l in range(depth)] for k in ("w", "a", "lq", "lv"))
+    ng = 1 if depth > 1 else NL             # graphs: one per distinct step
 
     def step(i):
-        dh.copy_(layers[i % NL]["t"]["dout"])
+        dh.copy_(layers[(i * depth + depth - 1) % NL]["t"]["dout"])
         if depth > 1:
             tlb.stack_backward(c, S, L, sW, sA, sQ, sV, adam, dh, ss, sws)
         else:
@@ -336,11 +335,11 @@ def seq_main(args, rank, world, local, dist):
 
     graphs = None
     if not args.no_graph:
-        for i in range(NL):
+        for i in range(ng):
             step(i)
         torch.cuda.synchronize()
         graphs = []
-        for i in range(NL):
+        for i in range(ng):
             gph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gph):
                 step(i)
@@ -349,7 +348,7 @@ def seq_main(args, rank, world, local, dist):
 
     def run(i):
         if graphs is not None:
-            graphs[i % NL].replay()
+            graphs[i % ng].replay()
         else:
             step(i)
 
@@ -358,7 +357,7 @@ def seq_main(args, rank, world, local, dist):
     launches_per_step = tlb.launch_count() - n0
     for i in range(max(args.warmup, 3)):
         run(i)
-    tlb.workspace_status(ws)
+    tlb.workspace_status(sws if depth > 1 else ws)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -374,11 +373,12 @@ def seq_main(args, rank, world, local, dist):
         dist.barrier()
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
-    tlb.workspace_status(ws)
+    tlb.workspace_status(sws if depth > 1 else ws)
     ms_max = slowest_rank_ms(ms, dist)
     value = args.steps * S * world / (ms_max / 1e3)
 
-    # per-kernel times of one layer, live, inside a CUDA graph of nk layer calls
+    # per-kernel times of one layer, live, inside a CUDA graph of nk layer calls; the
+    # library records an event before the first and after every kernel of each call
     nk, ne = 8, 64
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ne)] for _ in range(nk)]
     for row in evs:
@@ -408,96 +408,140 @@ def seq_main(args, rank, world, local, dist):
     fl = seq_kernel_flops(cfg, names[:nkern])
     pk = peaks()
     bf16_peak = pk["bf16_tflops_sustained"] if pk else 1700.0
-    tf32_peak = bf16_peak * 1.1 / 2.25
+    tf32, tf32_src = tf32_peak(bf16_peak)
     per_kernel = []
     for nm, t, (f, kind) in zip(names, ktime, fl):
         e = {"kernel": nm, "us": t * 1e3}
         if f:
-            e.update({"flop": f, "TFLOP/s": f / (t / 1e3) / 1e12, "operands": kind})
+            pkk = bf16_peak if kind == "bf16" else tf32
+            e.update({"flop": f, "TFLOP/s": f / (t / 1e3) / 1e12, "operands": kind,
+                      "frac": f / (t / 1e3) / 1e12 / pkk})
         per_kernel.append(e)
     dom = max((k for k in range(nkern) if fl[k][0]), key=lambda k: ktime[k])
     achieved = fl[dom][0] / (ktime[dom] / 1e3) / 1e12
-    peak = bf16_peak if fl[dom][1] == "bf16" else tf32_peak
+    peak = bf16_peak if fl[dom][1] == "bf16" else tf32
     # DRAM bytes of the dominant kernel from the committed ncu capture of the S = 2048 layer
-    # (per launch; the stack runs the same layer launches)
+    # (per launch; the stack runs the same launches per layer)
     traffic = None
     prof = os.path.join(ROOT, "profiles", "seq2048_dram_bytes.json")
     if S == 2048 and os.path.exists(prof):
         key = names[dom] if names[dom] != "tcgen05 gemm" else "tcgen05 gemm #%d" % (names[:dom + 1].count("tcgen05 gemm"))
         traffic = json.load(open(prof)).get(key)
+    layer_flop = seq_layer_flops(cfg)
+    step_s = ms_max / args.steps / 1e3
+    step_roofline = {"bound": "tensor", "flop_per_step": layer_flop * depth,
+                     "achieved": layer_flop * depth / step_s / 1e12, "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": layer_flop * depth / step_s / 1e12 / bf16_peak,
+                     "note": "all algorithmic flops of a step (weight products bf16, attention tf32, "
+                             "LoRA fp32) against the sustained bf16 peak"}
 
-    # end to end through the public API: the step's activations and caches from pinned host
-    # memory every step, d_in and the gradient sums read back
-    acts = ("x", "gate", "up", "silu_gate", "k", "v", "attn", "lora_q_h", "lora_v_h", "dout") + \
+    # end to end through the public API: every layer's activations and caches copied from
+    # pinned host memory on a copy stream (the next layer's copy overlapping this layer's
+    # kernels), one tlb_layer_backward call per layer from the top of the stack down, and
+    # d_in and the gradient sums read back at the end of each step
+    acts = ("x", "gate", "up", "silu_gate", "k", "v", "attn", "lora_q_h", "lora_v_h") + \
         (("q_raw",) if cfg.qk_norm else ())
-    pinned = [{k: layers[l]["t"][k].cpu().pin_memory() for k in acts} for l in range(NL)]
-    h2d = sum(pinned[0][k].numel() * 4 for k in acts) * depth
+    NP = min(NL, 2)
+    pinned = [{k: layers[l]["t"][k].cpu().pin_memory() for k in acts} for l in range(NP)]
+    dout_h = layers[0]["t"]["dout"].cpu().pin_memory()
+    h2d = sum(pinned[0][k].numel() * 4 for k in acts) * depth + dout_h.numel() * 4
     res_h = torch.empty(S, cfg.dim, pin_memory=True)
     ss_h = torch.empty(2, dtype=torch.float64, pin_memory=True)
     d2h = res_h.numel() * 4 + 16
-    n_e2e = max(3, min(args.steps, 20))
+    n_e2e = max(2, min(args.steps, 5 if depth > 1 else 20))
+    cs = torch.cuda.Stream()
+    copied = [torch.cuda.Event() for _ in range(NL)]
+    used = [torch.cuda.Event() for _ in range(NL)]
+    for ev in used:
+        ev.record(stream)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(n_e2e):
-        dh.copy_(layers[i % NL]["t"]["dout"])
-        for j in range(depth):
-            ly = layers[(i * depth + j) % NL]
-            for k in acts:
-                ly["t"][k].copy_(pinned[(i * depth + j) % NL][k], non_blocking=True)
-            if j == 0:
-                dh.copy_(ly["t"]["dout"])
-            layer_call(i * depth + j)
+        for j in reversed(range(depth)):
+            li = (i * depth + j) % NL
+            ly = layers[li]
+            with torch.cuda.stream(cs):
+                cs.wait_event(used[li])                  # the previous user of these buffers is done
+                for k in acts:
+                    ly["t"][k].copy_(pinned[li % NP][k], non_blocking=True)
+                copied[li].record(cs)
+            stream.wait_event(copied[li])
+            if j == depth - 1:
+                dh.copy_(dout_h, non_blocking=True)
+            tlb.layer_backward(c, S, L, ly["w"], ly["a"], ly["lq"], ly["lv"], adam, dh, ss, ws)
+            used[li].record(stream)
         res_h.copy_(dh, non_blocking=True)
         ss_h.copy_(ss, non_blocking=True)
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
-    e2e = {"value": n_e2e * S * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    e2e = {"value": n_e2e * S * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": n_e2e}
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        cpu = seq_cpu_baseline(args.cpu_seconds)
+        cpu = seq_cpu_baseline(cfg, depth)
 
     if rank == 0:
-        wl = {"seq512": "sequence layer backward S = L = 512",
-              "seq2048": "sequence layer backward S = L = 2048",
-              "stack2048": "36-layer stack backward, S = L = 2048 (one step = one tlb_stack_backward call "
-                           "over 36 layers)"}[args.workload]
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (device generator)",
-                "config": {"workload": wl + ": dim 2560, ffn 9728, 32/8 heads x 128, SwiGLU, RoPE, residual, "
-                                       + ("QK-norm on q, " if cfg.qk_norm else "") +
-                                       "bf16 weights, LoRA r16 Q/V, AdamW+LoRA+",
-                           "global_batch": world, "seq_len": S, "layers_per_step": depth,
-                           "parallelism": "replicas" if world > 1 else "single",
-                           "layers_cycled": NL, "l2": "inputs > L2 (weights 170 MB and attn %.0f MB per layer)"
-                                                       % (cfg.n_heads * S * L * 4 / 1e6),
-                           "cuda_graph": graphs is not None},
+                "config": seq_workload_config(cfg, depth, world),
+                "harness": {"layers_distinct": NL, "cuda_graph": graphs is not None,
+                            "step": ("one tlb_stack_backward call over %d layers" % depth) if depth > 1 else
+                                    "one tlb_layer_backward call"},
                 "layer_tokens_per_s": value * depth,
                 "roofline": {"bound": "tensor", "kernel": names[dom], "achieved": achieved, "peak": peak,
                              "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                              "algorithmic_flop": fl[dom][0],
                              "peak_source": ("MEASURED_PEAKS.json bf16_tflops_sustained (of measured)" if pk else
-                                             "fallback") + ("" if fl[dom][1] == "bf16" else " x 1.1/2.25 for tf32")},
+                                             "fallback") if fl[dom][1] == "bf16" else tf32_src},
+                "step_roofline": step_roofline,
                 "per_kernel": per_kernel, "per_kernel_timing": "graph",
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk}
         print(json.dumps(line), flush=True)
 
 
-def seq_cpu_baseline(seconds):
-    """The float64 oracle on the S = 512 layer (its own seeded inputs), tokens/s."""
+def seq_layer_flops(cfg):
+    """Algorithmic flops of one sequence layer backward: the three weight products, the
+    attention's dAttn, dQ and dV contractions over the visible (query, key) pairs, and the
+    LoRA products (dB, gh, dA of both adapters)."""
+    S, L, H, I, qd, kvd, r = cfg.seq_len, cfg.cache_len, cfg.dim, cfg.ffn_dim, cfg.q_dim, cfg.kv_dim, cfg.rank
+    pairs = S * (L - S) + S * (S + 1) // 2
+    gemm = 2 * S * I * H + 2 * S * H * 2 * I + 2 * S * qd * H
+    attn = 3 * 2 * pairs * cfg.head_dim * cfg.n_heads
+    lora = sum(3 * 2 * S * od * r for od in (qd, kvd)) + 2 * 2 * S * r * H
+    return gemm + attn + lora
+
+
+SLICES = 4
+
+
+def seq_cpu_sample(cfg, seed=0):
+    """The host problem of one S = L layer and its SLICES row slices (S / SLICES rows each
+    over the keys they may see): together the slices hold exactly the layer's work."""
+    from synth import layer_inputs_sample, row_slice
+    d = layer_inputs_sample(cfg, seed)
+    n = cfg.seq_len // SLICES
+    return [row_slice(cfg, d, k * n, (k + 1) * n) for k in range(SLICES)]
+
+
+def seq_cpu_time(sl):
+    """Seconds of one float64 oracle layer backward of a slice."""
     from oracle import layer as OL
-    from synth import SEQ512, layer_inputs
-    d = layer_inputs(SEQ512, layer=0, seed=0)
-    n, t0 = 0, time.perf_counter()
-    while True:
-        OL.layer_backward(SEQ512, d, d["dout"])
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or n >= 100:
-            break
-    return {"value": n * SEQ512.seq_len / el, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
-            "sample": "%d float64 oracle backwards of one S = 512 layer" % n}
+    sub, d = sl
+    t0 = time.perf_counter()
+    OL.layer_backward(sub, d, d["dout"])
+    return time.perf_counter() - t0
+
+
+def seq_cpu_baseline(cfg, depth):
+    """The float64 oracle on every row slice of one full-size layer (its whole work),
+    extrapolated to the depth of the step, tokens/s."""
+    slices = seq_cpu_sample(cfg)
+    t = sum(seq_cpu_time(sl) for sl in slices)
+    return {"value": cfg.seq_len / (t * depth), "unit": UNIT, "cores": host_threads(), "kind": "oracle",
+            "sample": "the float64 numpy oracle on one S = L = %d layer, run as its %d causal row slices of "
+                      "%d rows (%.1f s), x %d layers" % (cfg.seq_len, SLICES, cfg.seq_len // SLICES, t, depth)}
 
 
 # ---------------------------------------------------------------- bandwidth sweep
@@ -714,6 +758,50 @@ def sweep_main(args, rank, world, local, dist):
         print(json.dumps(line), flush=True)
 
 
+def tf32peak_main(args, local):
+    """Dense tf32 tensor-core peak, measured like the bf16 figures of the peaks file: a
+    cuBLAS tf32 GEMM of 8192^3 (2 N^3 flops), best of 10 (burst) and back to back for
+    4 s (sustained), CUDA events on the launching stream, clocks sampled meanwhile."""
+    import torch
+    torch.cuda.set_device(local)
+    torch.backends.cuda.matmul.allow_tf32 = True
+    n = 8192
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    a = torch.randn(n, n, device="cuda", generator=g)
+    b = torch.randn(n, n, device="cuda", generator=g)
+    c = torch.empty(n, n, device="cuda")
+    for _ in range(5):
+        torch.matmul(a, b, out=c)
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    best = 1e30
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b, out=c)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    reps, t0 = 0, time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    while time.perf_counter() - t0 < 4.0:
+        for _ in range(20):
+            torch.matmul(a, b, out=c)
+        reps += 20
+        torch.cuda.synchronize()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    flop = 2.0 * n ** 3
+    print(json.dumps({"tf32_tflops": flop / (best / 1e3) / 1e12,
+                      "tf32_tflops_sustained": flop * reps / (e0.elapsed_time(e1) / 1e3) / 1e12,
+                      "how": "torch.matmul fp32 with allow_tf32 (cuBLAS) %d^3, 2 N^3 flops: best of 10 (burst) and "
+                             "%d back to back (sustained), CUDA events" % (n, reps),
+                      "gpu": torch.cuda.get_device_name(local), "torch": torch.__version__, "clocks": clk}), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -731,6 +819,9 @@ def main():
             dist.destroy_process_group()
         return
 
+    if args.workload == "tf32peak":
+        tf32peak_main(args, local)
+        return
     if args.workload == "sweep":
         sweep_main(args, rank, world, local, dist)
         if dist is not None:
@@ -744,14 +835,14 @@ def main():
 
     import transformer_layer_backward_gb300 as tlb
     from synth import DECODE, layer_inputs
-    from tests.helpers import adam_to_abi, cfg_to_abi, lora_dev, to_dev
+    from synth.device import lora_dev, to_dev
 
     torch.cuda.set_device(local)
     tlb.load()
     cfg = DECODE.with_(qk_norm=True) if args.qk_norm else DECODE
-    NL = args.layers
-    c = cfg_to_abi(tlb, cfg)
-    adam = adam_to_abi(tlb, cfg)
+    NL = args.layers or 8
+    c = tlb.layer_cfg_of(cfg)
+    adam = tlb.adamw_cfg_of(cfg)
     layers, host_layers = [], []
     for l in range(NL):
         d = layer_inputs(cfg, layer=l, seed=0)

@@ -155,6 +155,12 @@ const char *tlb_last_error(void);
 const char *tlb_build_info(void);
 /* Number of kernels this process has enqueued through the library so far (all threads). */
 uint64_t tlb_launch_count(void);
+/* Name of launch number i (0 = the first launch counted by tlb_launch_count), kept for
+ * the last 4096 launches; NULL for an index not yet reached or no longer kept.  Lets a
+ * caller see which kernels a call ran: the launches numbered from tlb_launch_count()
+ * before the call to tlb_launch_count() after it.  Owned by the library; while other
+ * threads call the library an entry may already be overwritten. */
+const char *tlb_launch_name(uint64_t i);
 /* Benchmarking aid.  With events != NULL, each later tlb_layer_backward call records
  * (cudaEventRecordExternal, so it also works inside stream capture) events[0] on its
  * stream before its first kernel and events[k + 1] right after its k-th kernel, for

@@ -5,7 +5,7 @@ activations, weights and adapter states of a layer; it computes no gradient.
 """
 from . import rng
 from .configs import CONFIGS, DECODE, SEQ512, STACK2048, TINY, LayerConfig
-from .inputs import attention_rows, layer_inputs, stack_dout, vector
+from .inputs import attention_rows, layer_inputs, layer_inputs_sample, row_slice, stack_dout, vector
 
 __all__ = ["rng", "CONFIGS", "DECODE", "SEQ512", "STACK2048", "TINY", "LayerConfig",
-           "attention_rows", "layer_inputs", "stack_dout", "vector"]
+           "attention_rows", "layer_inputs", "layer_inputs_sample", "row_slice", "stack_dout", "vector"]

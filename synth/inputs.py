@@ -128,6 +128,68 @@ def layer_inputs(cfg: LayerConfig, layer: int = 0, seed: int = 0, with_dout: boo
     return d
 
 
+def layer_inputs_sample(cfg: LayerConfig, seed: int = 0) -> dict:
+    """A full-size draw for CPU timing samples only: the tensors of ``layer_inputs`` with
+    the same shapes and distributions, drawn with numpy's PCG64 (``layer_inputs`` takes
+    minutes at S = 2048 on the host).  The values differ from ``layer_inputs``; no parity
+    check reads them."""
+    S, L, H, I = cfg.seq_len, cfg.cache_len, cfg.dim, cfg.ffn_dim
+    qd, kvd, r = cfg.q_dim, cfg.kv_dim, cfg.rank
+    g = np.random.default_rng(seed)
+    f32 = np.float32
+    n = lambda shape, std=1.0: (g.standard_normal(shape, dtype=f32) * f32(std))
+    d: dict = {}
+    for k, shape in (("w_down", (I, H)), ("w_gate", (H, I)), ("w_up", (H, I)), ("w_o", (qd, H))):
+        w = n(shape, cfg.weight_std)
+        if cfg.wtype == "bf16":                 # round to nearest bfloat16 (finite values)
+            b = w.view(np.uint32)
+            b += np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))
+            b &= np.uint32(0xFFFF0000)
+        d[k] = w
+        d["s_" + k[2:]] = 1.0
+    for k, shape in (("x", (S, H)), ("gate", (S, I)), ("up", (S, I)), ("dout", (S, H))):
+        d[k] = n(shape)
+    d["silu_gate"] = (d["gate"] / (1.0 + np.exp(-d["gate"]))).astype(f32)
+    kshape = (L, kvd) if cfg.kv_layout == "shd" else (cfg.n_kv_heads, L, cfg.head_dim)
+    d["k"], d["v"] = n(kshape), n(kshape)
+    vis = np.arange(L)[None, :] <= (cfg.pos0 + np.arange(S))[:, None]
+    attn = np.empty((cfg.n_heads, S, L), dtype=f32)
+    for h in range(cfg.n_heads):
+        lg = np.where(vis, n((S, L), cfg.attn_logit_std), -np.inf)
+        lg -= lg.max(axis=-1, keepdims=True)
+        np.exp(lg, out=lg)
+        attn[h] = lg / lg.sum(axis=-1, keepdims=True)
+    d["attn"] = attn
+    for p, shape in (("a_q", (r, H)), ("b_q", (qd, r)), ("a_v", (r, H)), ("b_v", (kvd, r))):
+        d[p] = n(shape, 0.02)
+        d["m_" + p] = np.zeros_like(d[p])
+        d["v_" + p] = np.zeros_like(d[p])
+    d["lora_q_h"] = d["x"] @ d["a_q"].T
+    d["lora_v_h"] = d["x"] @ d["a_v"].T
+    return d
+
+
+def row_slice(cfg: LayerConfig, d: dict, r0: int, r1: int):
+    """Query rows r0 .. r1-1 of a layer problem as a problem of their own: S = r1 - r0
+    rows over the first L = pos0 + r1 cache entries (the keys those rows may see).  The
+    slices of a partition of the rows together hold exactly the layer's work."""
+    L = cfg.pos0 + r1
+    sub = cfg.with_(seq_len=r1 - r0, cache_len=L)
+    rows = ("x", "gate", "up", "silu_gate", "dout", "lora_q_h", "lora_v_h", "hidden", "r1", "ctx",
+            "q_raw")
+    out = {}
+    for k, v in d.items():
+        if k in rows:
+            out[k] = v[r0:r1]
+        elif k in ("k", "v"):
+            out[k] = v[:L] if cfg.kv_layout == "shd" else v[:, :L]
+        elif k == "attn":
+            out[k] = v[:, r0:r1, :L]
+        else:
+            out[k] = v
+    return sub, out
+
+
 def stack_dout(cfg: LayerConfig, seed: int = 0) -> np.ndarray:
     """Upstream gradient entering the top layer of a stack, [S, H] ~ N(0, 1)."""
     return _n(seed, cfg, "top", "grad_hidden", (cfg.seq_len, cfg.dim)).astype(np.float32)

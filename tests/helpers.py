@@ -16,27 +16,7 @@ F32_REL_L2 = 1e-5
 F32_MAX_ABS = 1e-4
 BF16_REL_L2 = 5e-3
 
-WEIGHTS = ("w_down", "w_gate", "w_up", "w_o")
-
-
-def to_dev(d: dict, wtype: str):
-    """numpy inputs -> torch CUDA tensors (weights in their storage dtype)."""
-    import torch
-    out = {}
-    for k, v in d.items():
-        if not isinstance(v, np.ndarray):
-            out[k] = v
-            continue
-        if k in WEIGHTS:
-            if wtype == "bf16":
-                out[k] = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to("cuda").to(torch.bfloat16)
-            elif wtype == "ternary":
-                out[k] = torch.from_numpy(np.ascontiguousarray(v, dtype=np.int8)).to("cuda")
-            else:
-                out[k] = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to("cuda")
-        else:
-            out[k] = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to("cuda")
-    return out
+from synth.device import lora_dev, to_dev  # noqa: F401  (re-exported for the tests)
 
 
 def host(t) -> np.ndarray:
@@ -66,27 +46,31 @@ def check(name, gpu, ref, rel_l2=F32_REL_L2, max_abs=F32_MAX_ABS):
 
 def cfg_to_abi(tlb, cfg, persistent=False):
     """synth LayerConfig -> the C ABI layer struct."""
-    return tlb.layer_cfg(cfg.dim, cfg.ffn_dim, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.rank,
-                         cfg.lora_alpha, act=cfg.act, wtype=cfg.wtype, sub_norm=cfg.sub_norm,
-                         pre_norm=cfg.pre_norm, residual=cfg.residual, rope=cfg.rope,
-                         use_silu_cache=(cfg.act == "silu_mul" and cfg.use_silu_cache), causal=True,
-                         rope_base=cfg.rope_base, norm_eps=cfg.norm_eps, attn_scale=cfg.attn_scale,
-                         persistent=persistent, qk_norm=cfg.qk_norm)
+    return tlb.layer_cfg_of(cfg, persistent=persistent)
 
 
 def adam_to_abi(tlb, cfg):
-    return tlb.adamw_cfg(cfg.lr, cfg.beta1, cfg.beta2, cfg.adam_eps, cfg.weight_decay, cfg.step,
-                         cfg.lr_b_mult)
+    return tlb.adamw_cfg_of(cfg)
 
 
-def lora_dev(t: dict):
-    """Adapter tensors keyed the way the binding's lora() expects."""
-    out = {}
-    for tag in ("q", "v"):
-        out["a_" + tag] = t["a_" + tag].clone()
-        out["b_" + tag] = t["b_" + tag].clone()
-        out["m_a_" + tag] = t["m_a_" + tag].clone()
-        out["v_a_" + tag] = t["v_a_" + tag].clone()
-        out["m_b_" + tag] = t["m_b_" + tag].clone()
-        out["v_b_" + tag] = t["v_b_" + tag].clone()
-    return out
+def tc_attention_shape(cfg) -> bool:
+    """The shapes the tensor-core attention takes (bf16 layers with S > 1): head_dim 64 or
+    128, L and L - S multiples of 4 (16-byte starts of the attention rows)."""
+    S, L = cfg.seq_len, cfg.cache_len
+    return (cfg.wtype == "bf16" and S > 1 and L % 4 == 0 and (L - S) % 4 == 0 and cfg.head_dim in (64, 128)
+            and cfg.n_heads % cfg.n_kv_heads == 0)
+
+
+def assert_route(cfg, names):
+    """bf16 layers with S > 1 must run their weight products on the tcgen05 GEMM and, where
+    the shape allows, their attention on the tcgen05 kernels: a silent fall-back to the
+    CUDA-core kernels would still pass the bf16 tolerance."""
+    if cfg.wtype != "bf16" or cfg.seq_len <= 1:
+        return
+    assert "tcgen05 gemm" in names, ("tcgen05 GEMM did not run", names)
+    assert "gemm_nt_simt" not in names, ("CUDA-core GEMM ran on a bf16 sequence layer", names)
+    if tc_attention_shape(cfg):
+        for k in ("attn_tc_dq", "attn_tc_dv"):
+            assert k in names, ("%s did not run" % k, names)
+        for k in ("attn_dq_tiled", "attn_rows"):
+            assert k not in names, ("CUDA-core attention ran", names)

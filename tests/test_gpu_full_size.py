@@ -14,7 +14,7 @@ import pytest
 
 from oracle import layer as OL
 from synth import STACK2048, layer_inputs
-from tests.helpers import BF16_REL_L2, adam_to_abi, cfg_to_abi, check, host, lora_dev, to_dev
+from tests.helpers import BF16_REL_L2, adam_to_abi, assert_route, cfg_to_abi, check, host, lora_dev, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -35,9 +35,11 @@ def test_full_size_layer_against_oracle(lib):
              for k in ("dA_q", "dB_q", "dA_v", "dB_v")}
     dh = t["dout"].clone()
     ss = torch.zeros(2, dtype=torch.float64, device="cuda")
+    n0 = lib.launch_count()
     lib.layer_backward(c, cfg.seq_len, cfg.cache_len, lib.layer_weights(c, t),
                        lib.layer_acts(c, t, cfg.kv_layout, cfg.cache_len), lib.lora(L, "q", grads),
                        lib.lora(L, "v", grads), adam, dh, ss, ws)
+    assert_route(cfg, lib.launch_names(n0))
     lib.workspace_status(ws)
     rel = {"d_in": check("d_in", host(dh), ref["d_in"], BF16_REL_L2, None)[0]}
     for k in ("dA_q", "dB_q", "dA_v", "dB_v"):
@@ -50,14 +52,14 @@ def test_full_size_layer_against_oracle(lib):
 
 def test_full_stack_is_linear_in_dout(lib):
     import torch
-    import bench
+    from synth.device import device_layer
     cfg = STACK2048
     S, L, depth = cfg.seq_len, cfg.cache_len, cfg.n_layers
     c = cfg_to_abi(lib, cfg)
     adam = adam_to_abi(lib, cfg)
     layers = []
     for l in range(2):                      # two distinct layers, alternating through the stack
-        t = bench.device_layer(cfg, l, seed=11)
+        t = device_layer(cfg, l, seed=11)
         # the dict keeps the tensors alive: the ABI structs hold raw device pointers
         layers.append(dict(t=t, w=lib.layer_weights(c, t), a=lib.layer_acts(c, t, cfg.kv_layout, L),
                            lq=lib.lora(t, "q"), lv=lib.lora(t, "v")))
@@ -69,12 +71,17 @@ def test_full_stack_is_linear_in_dout(lib):
     w = torch.randn(S, cfg.dim, device="cuda", generator=g)
     a_, b_ = 0.75, -1.25
 
+    sws = lib.stack_workspace(c, S, L)
+    sW, sA, sQ, sV = ([layers[j % 2][k] for j in range(depth)] for k in ("w", "a", "lq", "lv"))
+
     def stack(dout):
         dh = dout.clone()
-        for j in range(depth):
-            ly = layers[j % 2]
-            lib.layer_backward(c, S, L, ly["w"], ly["a"], ly["lq"], ly["lv"], adam, dh, ss, ws)
-        lib.workspace_status(ws)
+        n0 = lib.launch_count()
+        lib.stack_backward(c, S, L, sW, sA, sQ, sV, adam, dh, ss, sws)
+        names = lib.launch_names(n0)
+        assert_route(cfg, names)
+        assert names.count("attn_tc_dq") == depth
+        lib.workspace_status(sws)
         return host(dh)
 
     yu, yw, yc = stack(u), stack(w), stack(a_ * u + b_ * w)

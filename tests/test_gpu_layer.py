@@ -12,7 +12,8 @@ import pytest
 from oracle import layer as OL
 from oracle import ops
 from synth import DECODE, SEQ512, TINY, layer_inputs
-from tests.helpers import (BF16_REL_L2, adam_to_abi, cfg_to_abi, check, host, lora_dev, to_dev)
+from tests.helpers import (BF16_REL_L2, adam_to_abi, assert_route, cfg_to_abi, check, host, lora_dev,
+                           to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -87,7 +88,10 @@ def test_ffn_backward(lib, case):
     w = lib.layer_weights(c, t)
     a = lib.layer_acts(c, t, cfg.kv_layout, cfg.cache_len)
     out = torch.empty_like(t["dout"])
+    n0 = lib.launch_count()
     lib.ffn_backward(c, cfg.seq_len, t["dout"], w, a, out, ws)
+    if cfg.wtype == "bf16" and cfg.seq_len > 1:
+        assert "tcgen05 gemm" in lib.launch_names(n0)
     rl, ma = tol(cfg)
     check("dR1", host(out), ref["dR1"], rl, ma)
     # in place: d_residual aliases d_out
@@ -160,9 +164,11 @@ def test_layer_backward(lib, case, persistent):
              for k in ("dA_q", "dB_q", "dA_v", "dB_v")}
     dh = t["dout"].clone()
     ss = torch.zeros(2, dtype=torch.float64, device="cuda")
+    n0 = lib.launch_count()
     lib.layer_backward(c, cfg.seq_len, cfg.cache_len, lib.layer_weights(c, t),
                        lib.layer_acts(c, t, cfg.kv_layout, cfg.cache_len), lib.lora(L, "q", grads),
                        lib.lora(L, "v", grads), adam, dh, ss, ws)
+    assert_route(cfg, lib.launch_names(n0))
     lib.workspace_status(ws)
     rl, ma = tol(cfg)
     check("d_in", host(dh), ref["d_in"], rl, ma)

@@ -8,7 +8,8 @@ import pytest
 
 from oracle import layer as OL
 from synth import DECODE, TINY, layer_inputs
-from tests.helpers import BF16_REL_L2, adam_to_abi, cfg_to_abi, check, host, lora_dev, to_dev
+from oracle import ops
+from tests.helpers import BF16_REL_L2, adam_to_abi, assert_route, cfg_to_abi, check, host, lora_dev, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -16,14 +17,19 @@ ADAPTER_KEYS = ("a_q", "b_q", "a_v", "b_v", "m_a_q", "v_a_q", "m_b_q", "v_b_q",
                 "m_a_v", "v_a_v", "m_b_v", "v_b_v")
 
 
-def device_stack(lib, cfg, layers):
+def device_stack(lib, cfg, layers, with_grads=False):
+    """Each layer's inputs on the device; with_grads adds buffers the layer writes its
+    adapter gradients into."""
+    import torch
     devs = []
     for l, d in enumerate(layers):
         t = to_dev(d, cfg.wtype)
         L = lora_dev(t)
         c = cfg_to_abi(lib, cfg)
-        devs.append(dict(t=t, L=L, w=lib.layer_weights(c, t), a=lib.layer_acts(c, t, cfg.kv_layout, cfg.cache_len),
-                         lq=lib.lora(L, "q"), lv=lib.lora(L, "v")))
+        g = ({k: torch.empty_like(L[k.replace("dA_", "a_").replace("dB_", "b_")])
+              for k in ("dA_q", "dB_q", "dA_v", "dB_v")} if with_grads else None)
+        devs.append(dict(t=t, L=L, g=g, w=lib.layer_weights(c, t), a=lib.layer_acts(c, t, cfg.kv_layout, cfg.cache_len),
+                         lq=lib.lora(L, "q", g), lv=lib.lora(L, "v", g)))
     return devs
 
 
@@ -127,7 +133,7 @@ def test_sequence_tensor_core_stack(lib, variant):
     ref = OL.stack_backward(cfg, layers, dout)
     c = cfg_to_abi(lib, cfg)
     adam = adam_to_abi(lib, cfg)
-    a, b = device_stack(lib, cfg, layers), device_stack(lib, cfg, layers)
+    a, b = device_stack(lib, cfg, layers, with_grads=True), device_stack(lib, cfg, layers)
     S, L = cfg.seq_len, cfg.cache_len
     ws_s = lib.stack_workspace(c, S, L)
     ws_l = lib.workspace(c, S, L)
@@ -135,8 +141,12 @@ def test_sequence_tensor_core_stack(lib, variant):
     dh_l = dh_s.clone()
     ss_s = torch.zeros(2, dtype=torch.float64, device="cuda")
     ss_l = torch.zeros(2, dtype=torch.float64, device="cuda")
+    n0 = lib.launch_count()
     lib.stack_backward(c, S, L, [d["w"] for d in a], [d["a"] for d in a], [d["lq"] for d in a],
                        [d["lv"] for d in a], adam, dh_s, ss_s, ws_s)
+    names = lib.launch_names(n0)
+    assert_route(cfg, names)
+    assert names.count("attn_tc_dq") == n_layers, names
     for l in reversed(range(n_layers)):
         lib.layer_backward(c, S, L, b[l]["w"], b[l]["a"], b[l]["lq"], b[l]["lv"], adam, dh_l, ss_l, ws_l)
     lib.workspace_status(ws_s)
@@ -145,10 +155,21 @@ def test_sequence_tensor_core_stack(lib, variant):
     for l in range(n_layers):
         for k in ("a_q", "b_q", "a_v", "b_v"):
             np.testing.assert_array_equal(host(a[l]["L"][k]), host(b[l]["L"][k]))
-    tol = BF16_REL_L2 * np.sqrt(n_layers)
-    check("stack d_in", host(dh_s), ref["d_in"], tol, None)
+    # the stated bf16 tensor-core bar on d_in and on every layer's adapter gradients
+    rel = {"d_in": check("stack d_in", host(dh_s), ref["d_in"], BF16_REL_L2, None)[0]}
     for l in range(n_layers):
-        for p in ("a_q", "b_q", "a_v", "b_v"):
-            check("layer %d %s" % (l, p), host(a[l]["L"][p]), ref["layers"][l][p], tol, None)
+        for k in ("dA_q", "dB_q", "dA_v", "dB_v"):
+            rel["layer %d %s" % (l, k)] = check("layer %d %s" % (l, k), host(a[l]["g"][k]), ref["layers"][l][k],
+                                               BF16_REL_L2, None)[0]
+    print("bf16 %d-layer stack (%s), relative L2:" % (n_layers, variant), {k: "%.2e" % v for k, v in rel.items()})
+    # parameters: AdamW of the GPU's own gradients, to float32 accuracy
+    for l in range(n_layers):
+        for tag in ("q", "v"):
+            for p, lr in (("a_" + tag, cfg.lr), ("b_" + tag, cfg.lr * cfg.lr_b_mult)):
+                g = host(a[l]["g"]["d" + p[0].upper() + "_" + tag])
+                d = layers[l]
+                rp, _, _ = ops.adamw(d[p], g, d["m_" + p], d["v_" + p], lr, cfg.beta1, cfg.beta2, cfg.adam_eps,
+                                     cfg.weight_decay, cfg.step)
+                check("layer %d %s" % (l, p), host(a[l]["L"][p]), rp)
     gnorm = float(np.sqrt(ss_s[0].item()))
-    assert abs(gnorm - ref["gnorm"]) <= 2 * tol * ref["gnorm"]
+    assert abs(gnorm - ref["gnorm"]) <= BF16_REL_L2 * ref["gnorm"]

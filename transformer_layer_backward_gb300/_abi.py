@@ -57,6 +57,7 @@ SIGNATURES = {
     "tlb_last_error": (C.c_char_p, []),
     "tlb_build_info": (C.c_char_p, []),
     "tlb_launch_count": (C.c_uint64, []),
+    "tlb_launch_name": (C.c_char_p, [C.c_uint64]),
     "tlb_profile_events": (None, [C.POINTER(C.c_void_p), i32]),
     "tlb_profile_kernel_name": (C.c_char_p, [i32]),
     "tlb_linear_workspace_bytes": (sz, [i32, i64, i64, i64]),

@@ -100,6 +100,18 @@ def launch_count() -> int:
     return int(A.load().tlb_launch_count())
 
 
+def launch_names(first: int, last: int | None = None):
+    """Names of the library's launches numbered first .. last - 1 (launch_count() values
+    taken before and after a call); None where the log no longer holds one."""
+    lib = A.load()
+    last = launch_count() if last is None else last
+    out = []
+    for i in range(first, last):
+        nm = lib.tlb_launch_name(i)
+        out.append(nm.decode() if nm is not None else None)
+    return out
+
+
 def profile_events(events):
     """events[0] (torch.cuda.Event) is recorded at the start of each later layer call and
     events[k + 1] after its k-th kernel; None turns it off.  Returns the ctypes array,
@@ -141,6 +153,25 @@ def layer_cfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, lora_alpha, act
                       float(1.0 / math.sqrt(head_dim) if attn_scale is None else attn_scale),
                       {"relu2_mul": A.ACT_RELU2_MUL, "silu_mul": A.ACT_SILU_MUL}[act],
                       {"f32": A.W_F32, "bf16": A.W_BF16, "ternary": A.W_TERNARY_I8}[wtype], flags)
+
+
+def layer_cfg_of(c, persistent=False) -> A.LayerCfg:
+    """The layer struct for any object with the attributes of a layer configuration
+    (dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, lora_alpha, act, wtype, sub_norm,
+    pre_norm, residual, rope, use_silu_cache, rope_base, norm_eps, attn_scale, qk_norm);
+    the attention is causal."""
+    return layer_cfg(c.dim, c.ffn_dim, c.n_heads, c.n_kv_heads, c.head_dim, c.rank, c.lora_alpha,
+                     act=c.act, wtype=c.wtype, sub_norm=c.sub_norm, pre_norm=c.pre_norm,
+                     residual=c.residual, rope=c.rope,
+                     use_silu_cache=(c.act == "silu_mul" and c.use_silu_cache), causal=True,
+                     rope_base=c.rope_base, norm_eps=c.norm_eps, attn_scale=c.attn_scale,
+                     persistent=persistent, qk_norm=c.qk_norm)
+
+
+def adamw_cfg_of(c) -> A.AdamwCfg:
+    """The AdamW struct for an object with lr, beta1, beta2, adam_eps, weight_decay, step
+    and lr_b_mult attributes."""
+    return adamw_cfg(c.lr, c.beta1, c.beta2, c.adam_eps, c.weight_decay, c.step, c.lr_b_mult)
 
 
 def workspace_bytes(cfg: A.LayerCfg, S: int, L: int) -> int:

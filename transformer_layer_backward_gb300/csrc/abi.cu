@@ -19,6 +19,9 @@ static bool g_prof_on = false;
 static cudaStream_t g_prof_stream = nullptr;
 static int g_prof_k = 0;
 static const char *g_prof_names[256];
+// names of the most recent launches, indexed by launch number modulo kLaunchLog
+constexpr unsigned long long kLaunchLog = 4096;
+static const char *g_launch_names[kLaunchLog];
 
 static void prof_record(int i, cudaStream_t st) {
     // external record: inside a stream capture this becomes an event node whose
@@ -47,7 +50,8 @@ void set_error(const char *fmt, ...) {
 void clear_error() { g_err[0] = '\0'; }
 
 int check_launch(const char *what) {
-    __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+    const unsigned long long n = __atomic_fetch_add(&g_launches, 1ull, __ATOMIC_RELAXED);
+    g_launch_names[n % kLaunchLog] = what;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("%s: kernel launch failed: %s", what, cudaGetErrorString(e));
@@ -124,6 +128,11 @@ void tlb_profile_events(void *const *events, int32_t n) {
     g_prof_events = events;
     g_prof_n = events != nullptr && n > 0 ? n : 0;
     g_prof_on = false;
+}
+
+const char *tlb_launch_name(uint64_t i) {
+    const unsigned long long n = __atomic_load_n(&g_launches, __ATOMIC_RELAXED);
+    return (i < n && n - i <= kLaunchLog) ? g_launch_names[i % kLaunchLog] : nullptr;
 }
 
 const char *tlb_profile_kernel_name(int32_t k) {
