@@ -47,7 +47,7 @@ extern "C" {
 #define TLB_OK 0
 #define TLB_EINVAL (-1)        /* bad argument: shape, null pointer, alignment */
 #define TLB_EUNSUPPORTED (-2)  /* valid but not implemented (e.g. head_dim > 256) */
-#define TLB_ENONFINITE (-3)    /* reserved: non-finite value detected */
+#define TLB_ENONFINITE (-3)    /* a non-finite gradient was found (TLB_CHECK_FINITE) */
 #define TLB_ETIMEOUT (-4)      /* a device-side bounded wait ran out */
 #define TLB_ECUDA (-5)         /* a CUDA runtime call failed */
 
@@ -75,6 +75,15 @@ extern "C" {
                                   LayerActivations caches them after a QK-norm and RoPE): dQ is
                                   taken back through it, which needs q_raw and gamma_q.  Not with
                                   TLB_PERSISTENT (such layers take the multi-kernel schedule) */
+#define TLB_CHECK_FINITE 256   /* [RS] backward_through_layers contract C-WGPU-TRAIN-007 (grad_hidden
+                                  finite): the dOut entering a layer (or the top of a stack) and each
+                                  layer's dR1 (the gradient it hands down) are checked before any
+                                  adapter gradient is formed from them.  A non-finite value is
+                                  recorded in the workspace status block (tlb_workspace_status then
+                                  returns TLB_ENONFINITE) and every later AdamW step of the call
+                                  leaves its adapter and moments unchanged; gradient outputs and
+                                  sumsq are still written.  Not with TLB_PERSISTENT (such layers take
+                                  the multi-kernel schedule) */
 
 /* Shapes and constants of one layer. q_dim = n_heads*head_dim, kv_dim = n_kv_heads*head_dim. */
 typedef struct {
@@ -168,6 +177,13 @@ const char *tlb_launch_name(uint64_t i);
  * Events are cudaEvent_t passed as void*.  Process-wide setting: do not use while other
  * threads call the library. */
 void tlb_profile_events(void *const *events, int32_t n);
+/* Test hook of the device-side timeout path: the next single-token layer call with
+ * TLB_PERSISTENT has block `block` (of its one cooperative kernel) skip its arrival at
+ * the kernel's third global-memory grid barrier, a point where no block has a bulk copy
+ * in flight.  Every block's bounded wait there runs out (about a second), each records
+ * TLB_ETIMEOUT in the workspace status block and leaves; the context stays usable.  The
+ * hook then clears itself; block < 0 clears it.  Process-wide: for tests only. */
+int tlb_debug_skip_barrier_arrival(int32_t block);
 /* Name of the k-th kernel (from 0) of the last layer call profiled with
  * tlb_profile_events, or NULL past its last kernel.  Owned by the library. */
 const char *tlb_profile_kernel_name(int32_t k);
@@ -225,7 +241,11 @@ int tlb_adamw(float *p, const float *g, float *m, float *v, int64_t n,
 size_t tlb_workspace_bytes(const tlb_layer_cfg *cfg, int64_t S, int64_t L);
 
 /* Device status recorded in a workspace by earlier calls on `stream`: synchronises
- * the stream, returns TLB_OK or the first device error (TLB_ETIMEOUT), and clears it. */
+ * the stream, returns TLB_OK or the first device error (TLB_ETIMEOUT or, with
+ * TLB_CHECK_FINITE, TLB_ENONFINITE), and clears it.  After TLB_ETIMEOUT the outputs of
+ * the call that timed out are undefined; the workspace needs nothing more than this call
+ * to be used again (grid-barrier counters are reset by the kernel that used them, on
+ * every path out of it). */
 int tlb_workspace_status(void *ws, size_t ws_bytes, void *stream);
 
 /* [FFN] executeFFNBackward (sequence form: [RS] backward_through_layers, FFN part).

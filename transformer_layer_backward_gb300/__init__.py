@@ -7,13 +7,13 @@ library has not been built.
 """
 from . import _abi
 from ._abi import TlbError, load
-from .api import (act_backward, adamw, adamw_cfg, adamw_cfg_of, attn_backward, ffn_backward, layer_acts,
+from .api import (act_backward, adamw, adamw_cfg, adamw_cfg_of, attn_backward, debug_skip_barrier_arrival, ffn_backward, layer_acts,
                   layer_backward, layer_cfg, layer_cfg_of, layer_weights, launch_count, launch_names, linear_backward, linear_workspace, lora,
                   lora_grad_adamw, lora_grad_adamw_noalloc, profile_events,
                   rmsnorm_backward, rope_backward, softmax_backward, stack_backward, stack_workspace,
                   workspace, workspace_bytes, workspace_status)
 
-__all__ = ["TlbError", "load", "act_backward", "adamw", "adamw_cfg", "adamw_cfg_of", "attn_backward",
+__all__ = ["TlbError", "load", "act_backward", "adamw", "adamw_cfg", "adamw_cfg_of", "attn_backward", "debug_skip_barrier_arrival",
            "ffn_backward", "layer_acts", "layer_backward", "layer_cfg", "layer_cfg_of", "layer_weights", "launch_count", "launch_names", "linear_backward", "linear_workspace", "lora",
            "lora_grad_adamw", "lora_grad_adamw_noalloc", "profile_events", "rmsnorm_backward", "rope_backward", "softmax_backward",
            "stack_backward", "stack_workspace", "workspace", "workspace_bytes", "workspace_status", "_abi"]

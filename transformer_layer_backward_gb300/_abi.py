@@ -14,6 +14,7 @@ TLB_OK, TLB_EINVAL, TLB_EUNSUPPORTED, TLB_ENONFINITE, TLB_ETIMEOUT, TLB_ECUDA = 
 ACT_RELU2_MUL, ACT_SILU_MUL = 0, 1
 W_F32, W_BF16, W_TERNARY_I8 = 0, 1, 2
 SUB_NORM, PRE_NORM, RESIDUAL, ROPE, USE_SILU_CACHE, CAUSAL, PERSISTENT, QK_NORM = 1, 2, 4, 8, 16, 32, 64, 128
+CHECK_FINITE = 256
 
 vp, i32, i64, f32, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_size_t
 
@@ -58,6 +59,7 @@ SIGNATURES = {
     "tlb_build_info": (C.c_char_p, []),
     "tlb_launch_count": (C.c_uint64, []),
     "tlb_launch_name": (C.c_char_p, [C.c_uint64]),
+    "tlb_debug_skip_barrier_arrival": (C.c_int, [i32]),
     "tlb_profile_events": (None, [C.POINTER(C.c_void_p), i32]),
     "tlb_profile_kernel_name": (C.c_char_p, [i32]),
     "tlb_linear_workspace_bytes": (sz, [i32, i64, i64, i64]),

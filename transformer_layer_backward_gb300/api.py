@@ -143,11 +143,12 @@ def adamw(p, g, m, v, cfg: A.AdamwCfg, lr_mult=1.0, sumsq=None, stream=None):
 def layer_cfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, lora_alpha, act="relu2_mul",
               wtype="f32", sub_norm=False, pre_norm=False, residual=True, rope=True,
               use_silu_cache=False, causal=True, rope_base=10000.0, norm_eps=1e-6,
-              attn_scale=None, persistent=False, qk_norm=False) -> A.LayerCfg:
+              attn_scale=None, persistent=False, qk_norm=False, check_finite=False) -> A.LayerCfg:
     flags = ((A.SUB_NORM if sub_norm else 0) | (A.PRE_NORM if pre_norm else 0) |
              (A.RESIDUAL if residual else 0) | (A.ROPE if rope else 0) |
              (A.USE_SILU_CACHE if use_silu_cache else 0) | (A.CAUSAL if causal else 0) |
-             (A.PERSISTENT if persistent else 0) | (A.QK_NORM if qk_norm else 0))
+             (A.PERSISTENT if persistent else 0) | (A.QK_NORM if qk_norm else 0) |
+             (A.CHECK_FINITE if check_finite else 0))
     return A.LayerCfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, float(lora_alpha),
                       float(rope_base), float(norm_eps),
                       float(1.0 / math.sqrt(head_dim) if attn_scale is None else attn_scale),
@@ -155,7 +156,7 @@ def layer_cfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, lora_alpha, act
                       {"f32": A.W_F32, "bf16": A.W_BF16, "ternary": A.W_TERNARY_I8}[wtype], flags)
 
 
-def layer_cfg_of(c, persistent=False) -> A.LayerCfg:
+def layer_cfg_of(c, persistent=False, check_finite=False) -> A.LayerCfg:
     """The layer struct for any object with the attributes of a layer configuration
     (dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, lora_alpha, act, wtype, sub_norm,
     pre_norm, residual, rope, use_silu_cache, rope_base, norm_eps, attn_scale, qk_norm);
@@ -165,7 +166,7 @@ def layer_cfg_of(c, persistent=False) -> A.LayerCfg:
                      residual=c.residual, rope=c.rope,
                      use_silu_cache=(c.act == "silu_mul" and c.use_silu_cache), causal=True,
                      rope_base=c.rope_base, norm_eps=c.norm_eps, attn_scale=c.attn_scale,
-                     persistent=persistent, qk_norm=c.qk_norm)
+                     persistent=persistent, qk_norm=c.qk_norm, check_finite=check_finite)
 
 
 def adamw_cfg_of(c) -> A.AdamwCfg:
@@ -181,6 +182,11 @@ def workspace_bytes(cfg: A.LayerCfg, S: int, L: int) -> int:
 def workspace(cfg: A.LayerCfg, S: int, L: int, device="cuda"):
     """A zeroed workspace tensor of the size the library asks for."""
     return torch.zeros(max(workspace_bytes(cfg, S, L), 256), dtype=torch.uint8, device=device)
+
+
+def debug_skip_barrier_arrival(block: int):
+    """Test hook of the device-side timeout path (see tlb_debug_skip_barrier_arrival)."""
+    A.call("tlb_debug_skip_barrier_arrival", int(block))
 
 
 def workspace_status(ws, stream=None):

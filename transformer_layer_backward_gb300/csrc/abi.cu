@@ -227,6 +227,11 @@ int tlb_workspace_status(void *ws, size_t ws_bytes, void *stream) {
     if (words[kStatusCode] == kDevOk) return TLB_OK;
     TLB_CUDA(cudaMemsetAsync(ws, 0, sizeof(words), st));
     TLB_CUDA(cudaStreamSynchronize(st));
+    if (words[kStatusCode] == kDevNonFinite) {
+        set_error("device status: non-finite gradient (%s); the adapters were not stepped",
+                  words[kStatusWhere] == 1 ? "the dOut entering a layer" : "a layer's dR1");
+        return TLB_ENONFINITE;
+    }
     set_error("device status: a bounded wait ran out (code %u, site %u)", words[kStatusCode],
               words[kStatusWhere]);
     return TLB_ETIMEOUT;

@@ -79,8 +79,10 @@ inline T *ws_at(void *ws, size_t off) {
 }
 
 // Device status block (uint32 words at the start of a workspace).
-enum StatusWord { kStatusCode = 0, kStatusWhere = 1 };
-enum DeviceError { kDevOk = 0, kDevTimeout = 1 };
+// kStatusGate: with TLB_CHECK_FINITE, 1 if a non-finite gradient was seen by the checks
+// ordered before the AdamW kernels that read it (written after each layer's last check).
+enum StatusWord { kStatusCode = 0, kStatusWhere = 1, kStatusGate = 2 };
+enum DeviceError { kDevOk = 0, kDevTimeout = 1, kDevNonFinite = 2 };
 
 // ------------------------------------------------------------------ device side
 

@@ -721,6 +721,7 @@ __global__ void __launch_bounds__(kThreads) dec_k7(DecodeArgs a) {
     }
     pdl_wait();
     float sa = 0.f, sb = 0.f;   // dA^2, dB^2
+    const bool step = a.status == nullptr || __ldcg(a.status + kStatusGate) == 0u;
     if (which >= 0) {
         float g;
         if (which == 0) g = a.lora_scaling * __ldcg(a.dqpre + o) * fac;
@@ -728,15 +729,19 @@ __global__ void __launch_bounds__(kThreads) dec_k7(DecodeArgs a) {
         else g = __ldcg(a.gh + (which == 2 ? 0 : a.rank) + r) * fac;
         if (which <= 1) {
             if (l.grad_b) l.grad_b[f] = g;
-            l.b[f] = adam_elem(p, g, m, v, a.kb);
-            l.m_b[f] = m;
-            l.v_b[f] = v;
+            if (step) {
+                l.b[f] = adam_elem(p, g, m, v, a.kb);
+                l.m_b[f] = m;
+                l.v_b[f] = v;
+            }
             sb = g * g;
         } else {
             if (l.grad_a) l.grad_a[f] = g;
-            l.a[f] = adam_elem(p, g, m, v, a.ka);
-            l.m_a[f] = m;
-            l.v_a[f] = v;
+            if (step) {
+                l.a[f] = adam_elem(p, g, m, v, a.ka);
+                l.m_a[f] = m;
+                l.v_a[f] = v;
+            }
             sa = g * g;
         }
     }

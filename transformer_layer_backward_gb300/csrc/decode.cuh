@@ -22,6 +22,7 @@ struct DecodeArgs {
     tlb_lora lq, lv;
     AdamCoef ka, kb;
     double *sumsq;
+    const uint32_t *status;   // status block (optional): its step gate set skips AdamW (k7)
     // per-block partial sums (sum dy g x, sum x^2) for the RMSNorm backward of the
     // vector each GEMV produces; n1..n3 = the GEMV grids (blocks of k1, k2, k3)
     float2 *part1, *part2, *part3;

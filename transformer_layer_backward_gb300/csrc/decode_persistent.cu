@@ -39,8 +39,13 @@
 #include "kernels.cuh"
 
 #include <algorithm>
+#include <atomic>
 
 namespace tlb {
+
+// Test hook (tlb_debug_skip_barrier_arrival): the block of the next persistent call that
+// skips its arrival at the third grid barrier, or -1.
+static std::atomic<int> g_skip_arrival{-1};
 
 namespace {
 
@@ -48,14 +53,15 @@ constexpr int kPW = 16;                 // warps per block
 constexpr int kPT = kPW * 32;
 constexpr int kMaxRowsPerItem = 8;
 constexpr int kKeysPerItem = 64;        // attention keys per (KV head, chunk) item
-constexpr int kBarriers = 5;            // grid barriers per call
 constexpr int kMaxBlockRows = 256;      // phase-2 rows per block held in shared memory
 constexpr int kSlotsPerWarp = 1;        // shared-memory slots (items in flight) per GEMV warp
 
 struct PArgs {
     DecodeArgs d;
     uint32_t *status;                   // workspace status block
-    unsigned long long *gbar;           // grid barrier: monotonic arrival count
+    unsigned long long *gbar;           // [0] grid-barrier arrivals of this call, [1] blocks done;
+                                        // the last block done puts both back to zero
+    int skip_block;                     // test hook: this block skips its arrival at barrier 3 (-1: none)
     float2 *pp;                         // per-block partial sums, 3 x nblocks
     int nblocks, ngemv, slot_bytes, xbytes;
     int rpi;                            // rows per item in phases 1 and 3
@@ -79,7 +85,7 @@ __device__ __forceinline__ bool grid_sync(const PArgs &p, int k, unsigned long l
     __syncthreads();
     if (threadIdx.x == 0 && !*s_abort) {
         __threadfence();
-        red_release_add_u64(p.gbar, 1ull);
+        if (!(k == 3 && int(blockIdx.x) == p.skip_block)) red_release_add_u64(p.gbar, 1ull);
         const unsigned long long target = base + (unsigned long long)k * p.nblocks;
         if (ld_acquire_u64(p.gbar) < target) {
             const long long t0 = clock64();
@@ -242,7 +248,7 @@ __device__ __forceinline__ void coef(float2 s, int n, float eps, float &rinv, fl
 }
 
 template <int WT, int VPL>
-__global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
+__device__ __forceinline__ void persistent_body(const PArgs &p) {
     constexpr int GM = 16 / VPL;                 // heads per KV group held in registers
     constexpr int ES = 16 / EPC<WT>::v;
     extern __shared__ float4 smem4[];
@@ -261,9 +267,7 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
 
     if (threadIdx.x == 0) {
         s_abort = 0;
-        const unsigned long long v = *reinterpret_cast<volatile unsigned long long *>(p.gbar);
-        const unsigned long long per_call = (unsigned long long)kBarriers * p.nblocks;
-        s_base = v - v % per_call;
+        s_base = 0;   // every call finds the counter at zero (the last block of the previous one reset it)
     }
     if (lane == 0 && gemv_warp)
         for (int i = 0; i < kSlotsPerWarp; ++i) mbar_init(&mbar[kSlotsPerWarp * warp + i], 1);
@@ -695,6 +699,23 @@ __global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
     }
 }
 
+// Every block, on every path out of the body (including a wind-down after a bounded wait
+// ran out), counts itself done; the last one resets the barrier counter, so that each call
+// starts from zero whatever the previous call on this workspace went through.
+template <int WT, int VPL>
+__global__ void __launch_bounds__(kPT, 1) dec_persistent(PArgs p) {
+    persistent_body<WT, VPL>(p);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.gbar + 1, 1ull) == (unsigned long long)(p.nblocks - 1)) {
+            atomicExch(p.gbar, 0ull);
+            atomicExch(p.gbar + 1, 0ull);
+            __threadfence();
+        }
+    }
+}
+
 template <int WT, int VPL>
 int launch_p(const PArgs &p, size_t dyn, cudaStream_t st) {
     auto k = dec_persistent<WT, VPL>;
@@ -782,6 +803,7 @@ int decode_persistent_launch(const DecodeArgs &d, const tlb_layer_cfg &c, int64_
     TLB_REQUIRE(geometry(c, g), TLB_EUNSUPPORTED, "decode: no persistent geometry");
     PArgs p;
     p.d = d;
+    p.skip_block = g_skip_arrival.exchange(-1);
     p.status = ws_at<uint32_t>(ws, 0);
     p.gbar = ws_at<unsigned long long>(ws, off_gbar);
     p.pp = ws_at<float2>(ws, off_pp);
@@ -801,3 +823,8 @@ int decode_persistent_launch(const DecodeArgs &d, const tlb_layer_cfg &c, int64_
 }
 
 }  // namespace tlb
+
+extern "C" int tlb_debug_skip_barrier_arrival(int32_t block) {
+    tlb::g_skip_arrival.store(block < 0 ? -1 : int(block));
+    return TLB_OK;
+}

@@ -16,6 +16,11 @@ int rope_backward_launch(const float *dy, float *dx, int64_t rows, int n_heads, 
                          int64_t pos0, float base, cudaStream_t st);
 int adamw_launch(float *p, const float *g, float *m, float *v, int64_t n, const tlb_adamw_cfg &cfg,
                  float lr_mult, double *sumsq, cudaStream_t st);
+// Records kDevNonFinite with `site` in the status block if any of x[0, n) is not finite.
+int finite_check_launch(const float *x, int64_t n, uint32_t *status, uint32_t site, cudaStream_t st);
+// gate_block[kStatusGate] = (a non-finite value is recorded in status): the step gate the
+// AdamW kernels that come after it read.
+int finite_gate_launch(const uint32_t *status, uint32_t *gate_block, cudaStream_t st);
 
 }  // namespace tlb
 
@@ -92,7 +97,9 @@ struct LoraJob {
     void *scratch;
 };
 size_t lora_seq_bytes(int64_t S, int out_dim, int in_dim, int rank);
+// status (optional): a status block whose step gate (kStatusGate) is 1 skips the AdamW
+// steps (the gradients are still written and summed).
 int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x, const LoraJob *jobs, int njobs,
-                    const tlb_adamw_cfg &adam, double *sumsq, cudaStream_t st);
+                    const tlb_adamw_cfg &adam, double *sumsq, cudaStream_t st, const uint32_t *status = nullptr);
 
 }  // namespace tlb

@@ -343,6 +343,7 @@ void decode_args(const tlb_layer_cfg &c, int64_t L, const tlb_layer_weights *w, 
     d.ka = adam_coef(*adam, 1.0f);
     d.kb = adam_coef(*adam, float(adam->lr_b_mult));
     d.sumsq = sumsq;
+    d.status = nullptr;
     const int rpb = decode_rows_per_block();
     d.n1 = int(ceil_div(c.ffn_dim, rpb));
     d.n2 = int(ceil_div(c.dim, rpb));
@@ -365,6 +366,10 @@ void decode_args(const tlb_layer_cfg &c, int64_t L, const tlb_layer_weights *w, 
     d.dout = d_hidden;
     d.dhid_out = d_hidden;
 }
+
+// Sites of the finiteness checks, recorded beside kDevNonFinite in the status block.
+constexpr uint32_t kSiteDOut = 1;   // the gradient entering a layer call (or the top of a stack)
+constexpr uint32_t kSiteDR1 = 2;    // a layer's dR1: the gradient it hands to the layer below
 
 // Workspace sets of a single-token stack: layer l uses set l % kStackSets.
 constexpr int kStackSets = 4;
@@ -431,19 +436,38 @@ static int layer_backward_impl(const tlb_layer_cfg *cfg, int64_t S, int64_t L, c
     const int qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
     ProfileScope prof(st);
     float *dqpre = ws_at<float>(ws, p.dqpre), *dv = ws_at<float>(ws, p.dv);
+    // TLB_CHECK_FINITE ([RS] contract of backward_through_layers: grad_hidden finite): the
+    // dOut that enters and the dR1 that leaves the FFN half are checked before any adapter
+    // gradient is formed from them; a non-finite value is recorded in the status block,
+    // whose AdamW kernels then leave the adapters and their moments unchanged
+    const bool chk = (c.flags & TLB_CHECK_FINITE) != 0;
+    uint32_t *status = ws_at<uint32_t>(ws, 0);
+    if (chk) TLB_TRY(finite_check_launch(d_hidden, S * c.dim, status, kSiteDOut, st));
     if (decode_route(c, S, L, w, acts, d_hidden)) {
         DecodeArgs d;
         decode_args(c, L, w, acts, lora_q, lora_v, adam, d_hidden, sumsq, ws, p, d);
+        if (chk) {
+            d.status = status;
+            TLB_TRY(decode_ffn_launch(d, c.wtype, st, false));
+            TLB_TRY(finite_check_launch(d.dR1, c.dim, status, kSiteDR1, st));
+            TLB_TRY(finite_gate_launch(status, status, st));
+            return decode_attn_launch(d, st);
+        }
         if ((c.flags & TLB_PERSISTENT) && persistent_supported(c, S, L))
             return decode_persistent_launch(d, c, L, ws, p.gbar, p.pp, st);
         return decode_layer_launch(d, c.wtype, st);
     }
     bool abf_dr1 = false;
     TLB_TRY(ffn_impl(c, S, d_hidden, *w, *acts, d_hidden, ws, st, abf_dout && tc_route(c, S), &abf_dr1));
+    if (chk) {
+        TLB_TRY(finite_check_launch(d_hidden, S * c.dim, status, kSiteDR1, st));
+        TLB_TRY(finite_gate_launch(status, status, st));
+    }
     TLB_TRY(attn_impl(c, S, L, d_hidden, *w, *acts, dqpre, dv, ws, st, abf_dr1));
     const LoraJob jobs[2] = {{dqpre, acts->lora_q_h, qd, *lora_q, ws_at<void>(ws, p.lora_q)},
                              {dv, acts->lora_v_h, kvd, *lora_v, ws_at<void>(ws, p.lora_v)}};
-    return lora_seq_launch(S, c.dim, c.rank, c.lora_alpha, acts->x, jobs, 2, *adam, sumsq, st);
+    return lora_seq_launch(S, c.dim, c.rank, c.lora_alpha, acts->x, jobs, 2, *adam, sumsq, st,
+                           chk ? status : nullptr);
 }
 
 extern "C" {
@@ -525,6 +549,7 @@ int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n
                 "stack workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
     TLB_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, TLB_EINVAL, "workspace not 256-byte aligned");
     bool pipelined = S == 1 && !(c.flags & TLB_PERSISTENT);
+    const bool chk = (c.flags & TLB_CHECK_FINITE) != 0;
     for (int l = 0; l < n_layers; ++l) {
         TLB_TRY(check_acts_ffn(c, &w[l], &acts[l]));
         TLB_TRY(check_acts_attn(c, S, L, &w[l], &acts[l]));
@@ -557,6 +582,11 @@ int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n
     std::lock_guard<std::mutex> lock(side->mu);
     const LayerWs p = plan(c, S, L);
     auto set = [&](int l) { return static_cast<void *>(static_cast<char *>(ws) + size_t(l % kStackSets) * half); };
+    // with TLB_CHECK_FINITE every check reports into the first set's status block, the
+    // one tlb_workspace_status reads: the top dOut, then each layer's dR1 (the next layer's
+    // dOut) before the layer's attention and LoRA half is released to the side stream
+    uint32_t *status = ws_at<uint32_t>(ws, 0);
+    if (chk) TLB_TRY(finite_check_launch(d_hidden, c.dim, status, kSiteDOut, st));
     for (int l = n_layers - 1; l >= 0; --l) {
         const bool wait = (l % 2 == 0) && l + 2 <= n_layers - 1;
         if (wait) TLB_CUDA(cudaStreamWaitEvent(st, side->e7[(l + 2) % kStackSets], 0));
@@ -564,7 +594,14 @@ int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n
         decode_args(c, L, &w[l], &acts[l], &lora_q[l], &lora_v[l], adam, d_hidden, sumsq, set(l), p, d);
         d.dout = l == n_layers - 1 ? d_hidden : ws_at<float>(set(l + 1), p.dR1);
         d.dhid_out = l == 0 ? d_hidden : nullptr;
-        TLB_TRY(decode_ffn_launch(d, c.wtype, st, !wait && l < n_layers - 1));
+        // layer l's AdamW (k7, on the side stream) reads the step gate of its own set,
+        // written after its dR1 check: it sees exactly the checks of layers n-1 .. l
+        if (chk) d.status = ws_at<uint32_t>(set(l), 0);
+        TLB_TRY(decode_ffn_launch(d, c.wtype, st, !chk && !wait && l < n_layers - 1));
+        if (chk) {
+            TLB_TRY(finite_check_launch(d.dR1, c.dim, status, kSiteDR1, st));
+            TLB_TRY(finite_gate_launch(status, ws_at<uint32_t>(set(l), 0), st));
+        }
         TLB_CUDA(cudaEventRecord(side->e3, st));
         TLB_CUDA(cudaStreamWaitEvent(side->s, side->e3, 0));
         TLB_TRY(decode_attn_launch(d, side->s));

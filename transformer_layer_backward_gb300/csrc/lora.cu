@@ -150,6 +150,7 @@ struct LoraSide {
 struct LoraSeqArgs {
     LoraSide side[2];
     const float *x;              // [S, C]
+    const uint32_t *status;      // status block (optional): its step gate set skips AdamW
     int nside, S, C, rank, n_rt, vecx, vech;
     int tpc_b, nrc_b;            // G pass: row tiles per chunk, chunks (dB partials)
     int tpc_a, nrc_a;            // x pass: row tiles per chunk, chunks (dA partials)
@@ -589,6 +590,7 @@ __global__ void __launch_bounds__(256) lora_seq_adamw_kernel(LoraSeqArgs a, Adam
     __shared__ float red[32];
     int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     float ssa = 0.f, ssb = 0.f;
+    const bool step = a.status == nullptr || __ldcg(a.status + kStatusGate) == 0u;
     for (int sd = 0; sd < a.nside; ++sd) {
         const LoraSide &p = a.side[sd];
         const int64_t nA = int64_t(a.rank) * a.C, nB = int64_t(p.O) * a.rank;
@@ -596,20 +598,24 @@ __global__ void __launch_bounds__(256) lora_seq_adamw_kernel(LoraSeqArgs a, Adam
         if (e < nA) {
             const float g = ordered_sum(p.part_a + e, a.nrc_a, nA);
             if (p.l.grad_a) p.l.grad_a[e] = g;
-            float m = p.l.m_a[e], v = p.l.v_a[e];
-            p.l.a[e] = adam_elem(p.l.a[e], g, m, v, ka);
-            p.l.m_a[e] = m;
-            p.l.v_a[e] = v;
+            if (step) {
+                float m = p.l.m_a[e], v = p.l.v_a[e];
+                p.l.a[e] = adam_elem(p.l.a[e], g, m, v, ka);
+                p.l.m_a[e] = m;
+                p.l.v_a[e] = v;
+            }
             ssa = g * g;
             e = -1;
         } else if (e < nA + nB) {
             const int64_t f = e - nA;
             const float g = p.s * ordered_sum(p.part_b + f, a.nrc_b, nB);
             if (p.l.grad_b) p.l.grad_b[f] = g;
-            float m = p.l.m_b[f], v = p.l.v_b[f];
-            p.l.b[f] = adam_elem(p.l.b[f], g, m, v, kb);
-            p.l.m_b[f] = m;
-            p.l.v_b[f] = v;
+            if (step) {
+                float m = p.l.m_b[f], v = p.l.v_b[f];
+                p.l.b[f] = adam_elem(p.l.b[f], g, m, v, kb);
+                p.l.m_b[f] = m;
+                p.l.v_b[f] = v;
+            }
             ssb = g * g;
             e = -1;
         } else {
@@ -716,7 +722,7 @@ size_t lora_seq_bytes(int64_t S, int out_dim, int in_dim, int rank) {
 }
 
 int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x, const LoraJob *jobs, int njobs,
-                    const tlb_adamw_cfg &adam, double *sumsq, cudaStream_t st) {
+                    const tlb_adamw_cfg &adam, double *sumsq, cudaStream_t st, const uint32_t *status) {
     if (S == 0 || njobs == 0) return TLB_OK;
     TLB_REQUIRE(njobs <= 2, TLB_EINVAL, "lora: at most two adapters per call");
     TLB_REQUIRE(rank >= 1 && rank <= 64, TLB_EINVAL, "lora: rank must be in 1..64");
@@ -724,6 +730,7 @@ int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x
     TLB_REQUIRE(n_rt <= 65535, TLB_EUNSUPPORTED, "lora: S = %lld too long", (long long)S);
     LoraSeqArgs a{};
     a.x = x;
+    a.status = status;
     a.nside = njobs;
     a.S = int(S);
     a.C = in_dim;

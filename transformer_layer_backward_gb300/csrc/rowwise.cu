@@ -541,4 +541,44 @@ int adamw_launch(float *p, const float *g, float *m, float *v, int64_t n, const 
     return check_launch("adamw");
 }
 
+
+// ------------------------------------------------------------------ finiteness check
+
+// Any non-finite element of x[0, n) records kDevNonFinite (first device error wins) and
+// the site in the workspace status block.
+__global__ void finite_check_kernel(const float *__restrict__ x, int64_t n, uint32_t *status, uint32_t site,
+                                    int vec) {
+    bool bad = false;
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (vec) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(x);
+        for (; i < n / 4; i += stride) {
+            const float4 v = ld_stream(x4 + i);
+            bad |= !(isfinite(v.x) && isfinite(v.y) && isfinite(v.z) && isfinite(v.w));
+        }
+        i = n / 4 * 4 + int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    }
+    for (; i < n; i += stride) bad |= !isfinite(x[i]);
+    if (__syncthreads_or(bad) && threadIdx.x == 0 &&
+        atomicCAS(status + kStatusCode, 0u, uint32_t(kDevNonFinite)) == 0u)
+        atomicExch(status + kStatusWhere, site);
+}
+
+__global__ void finite_gate_kernel(const uint32_t *status, uint32_t *gate_block) {
+    gate_block[kStatusGate] = __ldcg(status + kStatusCode) == uint32_t(kDevNonFinite) ? 1u : 0u;
+}
+
+int finite_gate_launch(const uint32_t *status, uint32_t *gate_block, cudaStream_t st) {
+    finite_gate_kernel<<<1, 1, 0, st>>>(status, gate_block);
+    return check_launch("finite_gate");
+}
+
+int finite_check_launch(const float *x, int64_t n, uint32_t *status, uint32_t site, cudaStream_t st) {
+    if (n == 0) return TLB_OK;
+    const int vec = aligned16(x) ? 1 : 0;
+    finite_check_kernel<<<stream_grid(vec ? n / 4 + 1 : n, 256), 256, 0, st>>>(x, n, status, site, vec);
+    return check_launch("finite_check");
+}
+
 }  // namespace tlb
