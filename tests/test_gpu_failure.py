@@ -49,7 +49,9 @@ def test_check_finite_changes_nothing_on_finite_input(lib, name):
     b = run_layer(lib, cfg, d, check_finite=True)
     lib.workspace_status(a[3])
     lib.workspace_status(b[3])          # TLB_OK: raises otherwise
-    np.testing.assert_array_equal(host(a[0]), host(b[0]))
+    # the same kernels (float atomics may sum in another order: the single-token chain
+    # combines column ranges that way)
+    check("d_in", host(b[0]), host(a[0]), rel_l2=1e-6, max_abs=None)
     for k in ADAPTERS:
         check(k, host(b[1][k]), host(a[1][k]), rel_l2=1e-6, max_abs=None)
 
