@@ -73,15 +73,16 @@ def test_nan_in_dout_is_reported_and_skips_adamw(lib, name):
 
 
 def test_nan_inside_a_stack_stops_the_steps_below(lib):
-    """A NaN in layer 1's cached gate makes layer 1's dR1 non-finite: layers 3 and 2 (run
-    before it) take their steps as in a clean run, layers 1 and 0 take none."""
+    """A NaN in layer 1's cached up projection makes layer 1's dR1 non-finite (a NaN in
+    the ReLU^2 gate would not: max(0, NaN) is 0 there): layers 3 and 2 (run before it)
+    take their steps as in a clean run, layers 1 and 0 take none."""
     import torch
     n = 4
     cfg = DEC_SMALL.with_(name="dec_small_stack", n_layers=n)
     layers = [layer_inputs(cfg, layer=l, seed=2, with_dout=(l == n - 1)) for l in range(n)]
     bad = [dict(x) for x in layers]
-    bad[1]["gate"] = bad[1]["gate"].copy()
-    bad[1]["gate"][0, 5] = np.nan
+    bad[1]["up"] = bad[1]["up"].copy()
+    bad[1]["up"][0, 5] = np.nan
 
     def run(src, chk):
         c = lib.layer_cfg_of(cfg, check_finite=chk)
