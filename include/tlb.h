@@ -84,6 +84,22 @@ extern "C" {
                                   leaves its adapter and moments unchanged; gradient outputs and
                                   sumsq are still written.  Not with TLB_PERSISTENT (such layers take
                                   the multi-kernel schedule) */
+#define TLB_EXACT_DIN 512      /* d_hidden returns the exact gradient of the layer input x_in instead of
+                                  dR1.  The pages stop the backward at the Q / V projection outputs
+                                  ([ATT] "Gradient Flow"; [RS] backward_through_layers); this is the
+                                  plain derivative of the same forward with n1 = [RMSNorm(x_in;
+                                  gamma_attn)] feeding the Q, K and V projections ([RS] LayerActivations
+                                  caches q and k) and both LoRA A products:
+                                    dK = scale sum_group dS^T q on the S new cache rows, then RoPE
+                                         backward and, with TLB_QK_NORM, the k-side per-head RMSNorm
+                                         backward (gamma_k, k_raw);
+                                    dn1 = s_q dQpre W_Q^T + s_k dK W_K^T + s_v dV W_V^T
+                                          + s (dQpre B_q) A_q + s (dV B_v) A_v   (A, B before AdamW);
+                                    d_in = [RESIDUAL: dR1 +] [PRE_NORM: RMSNorm_bwd(x_in, gamma_attn,
+                                           dn1), else dn1].
+                                  Needs w_q, w_k, w_v and acts->q; with PRE_NORM x_in and gamma_attn;
+                                  with TLB_QK_NORM k_raw and gamma_k.  Not with TLB_PERSISTENT, and a
+                                  single-token stack runs its layers one after another */
 
 /* Shapes and constants of one layer. q_dim = n_heads*head_dim, kv_dim = n_kv_heads*head_dim. */
 typedef struct {
@@ -117,6 +133,12 @@ typedef struct {
     const float *gamma_ffn;         /* [dim],     TLB_PRE_NORM */
     const float *gamma_sub_attn;    /* [q_dim],   TLB_SUB_NORM */
     const float *gamma_q;           /* [head_dim], TLB_QK_NORM: the per-head norm's gain (all heads) */
+    /* TLB_EXACT_DIN only (NULL otherwise): */
+    tlb_weight w_q;                 /* [dim, q_dim]  */
+    tlb_weight w_k;                 /* [dim, kv_dim] */
+    tlb_weight w_v;                 /* [dim, kv_dim] */
+    const float *gamma_attn;        /* [dim], with TLB_PRE_NORM: the attention pre-norm's gain */
+    const float *gamma_k;           /* [head_dim], with TLB_QK_NORM: the k-side per-head norm's gain */
 } tlb_layer_weights;
 
 /* Cached forward activations of one layer ([RS] LayerActivations, [FFN]
@@ -138,6 +160,10 @@ typedef struct {
     const float *lora_q_h;   /* x @ A_q^T [S, rank] */
     const float *lora_v_h;   /* x @ A_v^T [S, rank] */
     const float *q_raw;      /* Q projection output before the per-head norm [S, q_dim], TLB_QK_NORM */
+    /* TLB_EXACT_DIN only (NULL otherwise): */
+    const float *x_in;       /* layer input before the attention pre-norm [S, dim], with TLB_PRE_NORM */
+    const float *q;          /* queries after RoPE (and the QK-norm) [S, q_dim] */
+    const float *k_raw;      /* K projection output of the S new rows before the norm [S, kv_dim], with TLB_QK_NORM */
 } tlb_layer_acts;
 
 /* A LoRA adapter (A [rank, in], B [out, rank]) and its AdamW moments, updated in place.
@@ -301,8 +327,8 @@ int tlb_lora_grad_adamw_noalloc(int64_t S, int32_t out_dim, int32_t in_dim, int3
                                 const tlb_adamw_cfg *adam, double *sumsq, void *stream);
 
 /* One whole layer: FFN backward, attention backward, LoRA Q/V gradients and AdamW.
- * d_hidden [S, dim] in/out: dOut on entry, the gradient for the layer below (dR1) on
- * return ([RS] grad_hidden).  sumsq (device double[2]) += {sum dA^2, sum dB^2} over both
+ * d_hidden [S, dim] in/out: dOut on entry, the gradient for the layer below on return
+ * ([RS] grad_hidden): dR1, or with TLB_EXACT_DIN the exact gradient of the layer input.  sumsq (device double[2]) += {sum dA^2, sum dB^2} over both
  * adapters; the page's gradient norm over a stack is sqrt(sumsq[0]).  lora_q: A [r, dim],
  * B [q_dim, r]; lora_v: A [r, dim], B [kv_dim, r]. */
 int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L,

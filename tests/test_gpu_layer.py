@@ -53,9 +53,23 @@ SEQ_QK = SEQ_HD64.with_(name="seq_qknorm", qk_norm=True, seq_len=148, cache_len=
 SEQ_PRENORM = SEQ_MHA.with_(name="seq_prenorm", pre_norm=True, act="relu2_mul")
 SEQ_NORESID = SEQ_HD64.with_(name="seq_noresid", residual=False, seq_len=96, cache_len=96)
 SEQ_NORMS = SEQ_HD64.with_(name="seq_norms", sub_norm=True, pre_norm=True, seq_len=64, cache_len=96)
+# the exact layer-input gradient (through W_Q, W_K, W_V, the LoRA A paths and the
+# attention pre-norm) on every route: row kernels (tiny, head_dim 16), the single-token
+# chain (fp32 and ternary), CUDA-core tiled attention (bf16, head_dim 32), tensor-core
+# attention with the three-segment tcgen05 product (with and without the pre-norm, with
+# the QK-norm on q and k, a cache longer than the sequence) and S = 512
+TINY_EXACT = TINY.with_(name="tiny_exact", exact_din=True)
+TINY_EXACT_QK = TINY.with_(name="tiny_exact_qknorm", exact_din=True, qk_norm=True, adam_state="warm", step=3)
+DEC_EXACT = DEC_F32.with_(name="dec_exact", exact_din=True)
+DECODE_EXACT = DECODE.with_(name="decode_exact", exact_din=True)
+MINI_SEQ_EXACT = MINI_SEQ.with_(name="mini_seq_exact", exact_din=True)
+SEQ_EXACT = SEQ_HD64.with_(name="seq_exact", exact_din=True)
+SEQ_EXACT_PN = SEQ_MHA.with_(name="seq_exact_prenorm_qknorm", exact_din=True, pre_norm=True, qk_norm=True)
+SEQ512_EXACT = SEQ512.with_(name="seq512_exact", exact_din=True)
 CASES = {c.name: c for c in (TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512, DEC_F32, DEC_BF16, DEC_G8, DEC_HD256,
                              SEQ_HD64, SEQ_CACHE, SEQ_MHA, SEQ_ODD, TINY_QK, DEC_QK, SEQ_QK, SEQ_PRENORM,
-                             SEQ_NORESID, SEQ_NORMS)}
+                             SEQ_NORESID, SEQ_NORMS, TINY_EXACT, TINY_EXACT_QK, DEC_EXACT, DECODE_EXACT,
+                             MINI_SEQ_EXACT, SEQ_EXACT, SEQ_EXACT_PN, SEQ512_EXACT)}
 
 
 def tol(cfg):
@@ -171,7 +185,9 @@ def test_layer_backward(lib, case, persistent):
     assert_route(cfg, lib.launch_names(n0))
     lib.workspace_status(ws)
     rl, ma = tol(cfg)
-    check("d_in", host(dh), ref["d_in"], rl, ma)
+    rel = check("d_in", host(dh), ref["d_in"], rl, ma)[0]
+    if cfg.exact_din:
+        print("%s: exact d_in relative L2 %.2e" % (cfg.name, rel))
     for k in ("dA_q", "dB_q", "dA_v", "dB_v"):
         check(k, host(grads[k]), ref[k], rl, ma)
     s = ss.cpu().numpy()

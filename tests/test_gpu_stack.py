@@ -173,3 +173,40 @@ def test_sequence_tensor_core_stack(lib, variant):
                 check("layer %d %s" % (l, p), host(a[l]["L"][p]), rp)
     gnorm = float(np.sqrt(ss_s[0].item()))
     assert abs(gnorm - ref["gnorm"]) <= BF16_REL_L2 * ref["gnorm"]
+
+
+@pytest.mark.parametrize("name", ["decode", "bf16_seq"])
+def test_exact_input_gradient_stack_against_oracle(lib, name):
+    """The exact layer-input gradient through a stack: each layer's d_in (through Q, K, V,
+    the LoRA A paths and the pre-norm) is the dOut of the layer below; single-token layers
+    run one after another (the overlap would hand dR1 down too early)."""
+    import torch
+    from synth import SEQ512
+    if name == "decode":
+        cfg = DECODE.with_(name="decode_exact_stack", dim=256, ffn_dim=512, n_heads=8, n_kv_heads=2, head_dim=64,
+                           rank=4, lora_alpha=8.0, cache_len=100, wtype="f32", weight_std=0.05, n_layers=3,
+                           exact_din=True)
+        tol = (1e-5, 1e-4)
+    else:
+        cfg = SEQ512.with_(name="seq_exact_stack", dim=512, ffn_dim=1024, n_heads=8, n_kv_heads=2, head_dim=64,
+                           rank=8, lora_alpha=16.0, seq_len=128, cache_len=160, n_layers=3, pre_norm=True,
+                           exact_din=True)
+        tol = (BF16_REL_L2, None)
+    n = cfg.n_layers
+    layers = [layer_inputs(cfg, layer=l, seed=6, with_dout=(l == n - 1)) for l in range(n)]
+    dout = layers[-1]["dout"]
+    ref = OL.stack_backward(cfg, layers, dout)
+    c = cfg_to_abi(lib, cfg)
+    devs = device_stack(lib, cfg, layers, with_grads=True)
+    ws = lib.stack_workspace(c, cfg.seq_len, cfg.cache_len)
+    dh = torch.from_numpy(dout).cuda()
+    ss = torch.zeros(2, dtype=torch.float64, device="cuda")
+    lib.stack_backward(c, cfg.seq_len, cfg.cache_len, [d["w"] for d in devs], [d["a"] for d in devs],
+                       [d["lq"] for d in devs], [d["lv"] for d in devs], adam_to_abi(lib, cfg), dh, ss, ws)
+    lib.workspace_status(ws)
+    rel = {"d_in": check("stack d_in", host(dh), ref["d_in"], *tol)[0]}
+    for l in range(n):
+        for k in ("dA_q", "dB_q", "dA_v", "dB_v"):
+            rel["layer %d %s" % (l, k)] = check("layer %d %s" % (l, k), host(devs[l]["g"][k]), ref["layers"][l][k],
+                                               *tol)[0]
+    print("exact %s stack, relative L2:" % name, {k: "%.2e" % v for k, v in rel.items()})

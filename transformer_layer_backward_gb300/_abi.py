@@ -14,7 +14,7 @@ TLB_OK, TLB_EINVAL, TLB_EUNSUPPORTED, TLB_ENONFINITE, TLB_ETIMEOUT, TLB_ECUDA = 
 ACT_RELU2_MUL, ACT_SILU_MUL = 0, 1
 W_F32, W_BF16, W_TERNARY_I8 = 0, 1, 2
 SUB_NORM, PRE_NORM, RESIDUAL, ROPE, USE_SILU_CACHE, CAUSAL, PERSISTENT, QK_NORM = 1, 2, 4, 8, 16, 32, 64, 128
-CHECK_FINITE = 256
+CHECK_FINITE, EXACT_DIN = 256, 512
 
 vp, i32, i64, f32, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_size_t
 
@@ -32,14 +32,15 @@ class Weight(C.Structure):
 
 class LayerWeights(C.Structure):
     _fields_ = [("w_down", Weight), ("w_gate", Weight), ("w_up", Weight), ("w_o", Weight),
-                ("gamma_sub_ffn", vp), ("gamma_ffn", vp), ("gamma_sub_attn", vp), ("gamma_q", vp)]
+                ("gamma_sub_ffn", vp), ("gamma_ffn", vp), ("gamma_sub_attn", vp), ("gamma_q", vp),
+                ("w_q", Weight), ("w_k", Weight), ("w_v", Weight), ("gamma_attn", vp), ("gamma_k", vp)]
 
 
 class LayerActs(C.Structure):
     _fields_ = [("x", vp), ("gate", vp), ("up", vp), ("silu_gate", vp), ("hidden", vp),
                 ("r1", vp), ("ctx", vp), ("k", vp), ("v", vp), ("kv_stride_head", i64),
                 ("kv_stride_pos", i64), ("attn", vp), ("lora_q_h", vp), ("lora_v_h", vp),
-                ("q_raw", vp)]
+                ("q_raw", vp), ("x_in", vp), ("q", vp), ("k_raw", vp)]
 
 
 class Lora(C.Structure):

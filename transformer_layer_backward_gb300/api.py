@@ -143,12 +143,13 @@ def adamw(p, g, m, v, cfg: A.AdamwCfg, lr_mult=1.0, sumsq=None, stream=None):
 def layer_cfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, lora_alpha, act="relu2_mul",
               wtype="f32", sub_norm=False, pre_norm=False, residual=True, rope=True,
               use_silu_cache=False, causal=True, rope_base=10000.0, norm_eps=1e-6,
-              attn_scale=None, persistent=False, qk_norm=False, check_finite=False) -> A.LayerCfg:
+              attn_scale=None, persistent=False, qk_norm=False, check_finite=False,
+              exact_din=False) -> A.LayerCfg:
     flags = ((A.SUB_NORM if sub_norm else 0) | (A.PRE_NORM if pre_norm else 0) |
              (A.RESIDUAL if residual else 0) | (A.ROPE if rope else 0) |
              (A.USE_SILU_CACHE if use_silu_cache else 0) | (A.CAUSAL if causal else 0) |
              (A.PERSISTENT if persistent else 0) | (A.QK_NORM if qk_norm else 0) |
-             (A.CHECK_FINITE if check_finite else 0))
+             (A.CHECK_FINITE if check_finite else 0) | (A.EXACT_DIN if exact_din else 0))
     return A.LayerCfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, float(lora_alpha),
                       float(rope_base), float(norm_eps),
                       float(1.0 / math.sqrt(head_dim) if attn_scale is None else attn_scale),
@@ -166,7 +167,8 @@ def layer_cfg_of(c, persistent=False, check_finite=False) -> A.LayerCfg:
                      residual=c.residual, rope=c.rope,
                      use_silu_cache=(c.act == "silu_mul" and c.use_silu_cache), causal=True,
                      rope_base=c.rope_base, norm_eps=c.norm_eps, attn_scale=c.attn_scale,
-                     persistent=persistent, qk_norm=c.qk_norm, check_finite=check_finite)
+                     persistent=persistent, qk_norm=c.qk_norm, check_finite=check_finite,
+                     exact_din=getattr(c, "exact_din", False))
 
 
 def adamw_cfg_of(c) -> A.AdamwCfg:
@@ -195,17 +197,22 @@ def workspace_status(ws, stream=None):
 
 def layer_weights(cfg: A.LayerCfg, t: dict):
     """Weights from a dict: w_down/w_gate/w_up/w_o (+ s_* scales); the gains g_sub_ffn,
-    g_ffn, g_sub_attn, g_q are optional."""
+    g_ffn, g_sub_attn, g_q are optional, and so are w_q/w_k/w_v, g_attn, g_k (the exact
+    layer-input gradient)."""
     wd = _WDTYPE[cfg.wtype]
 
     def w(name):
+        if name not in t:
+            return A.Weight(None, 1.0)
         return A.Weight(_ptr(t[name], wd, name), float(t.get("s_" + name[2:], 1.0)))
 
     return A.LayerWeights(w("w_down"), w("w_gate"), w("w_up"), w("w_o"),
                           _ptr(t.get("g_sub_ffn"), name="g_sub_ffn"),
                           _ptr(t.get("g_ffn"), name="g_ffn"),
                           _ptr(t.get("g_sub_attn"), name="g_sub_attn"),
-                          _ptr(t.get("g_q"), name="g_q"))
+                          _ptr(t.get("g_q"), name="g_q"),
+                          w("w_q"), w("w_k"), w("w_v"),
+                          _ptr(t.get("g_attn"), name="g_attn"), _ptr(t.get("g_k"), name="g_k"))
 
 
 def layer_acts(cfg: A.LayerCfg, t: dict, kv_layout: str, L: int):
@@ -218,7 +225,7 @@ def layer_acts(cfg: A.LayerCfg, t: dict, kv_layout: str, L: int):
     g = lambda k: _ptr(t.get(k), name=k)
     return A.LayerActs(g("x"), g("gate"), g("up"), g("silu_gate"), g("hidden"), g("r1"),
                        g("ctx"), g("k"), g("v"), sh, sp, g("attn"), g("lora_q_h"), g("lora_v_h"),
-                       g("q_raw"))
+                       g("q_raw"), g("x_in"), g("q"), g("k_raw"))
 
 
 def lora(t: dict, tag: str, grads: dict | None = None):

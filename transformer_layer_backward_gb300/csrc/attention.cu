@@ -41,6 +41,7 @@ __global__ void attn_rows_kernel(AttnArgs a, RopeFreqs fr) {
     float part = 0.f;
     for (int j = threadIdx.x; j < jmax; j += blockDim.x) part += P[j] * sS[j];
     const float D = block_sum(part, red);
+    if (a.D != nullptr && threadIdx.x == 0) a.D[int64_t(h) * a.S + i] = D;
     for (int j = threadIdx.x; j < jmax; j += blockDim.x) sS[j] = a.scale * P[j] * (sS[j] - D);
     __syncthreads();
     for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
@@ -169,7 +170,10 @@ __global__ void __launch_bounds__(256) attn_dq_tiled(AttnArgs a, RopeFreqs fr) {
         float v = dp[r];
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);   // the 16 tx of this ty
-        if (tx == 0) sD[4 * ty + r] = v;
+        if (tx == 0) {
+            sD[4 * ty + r] = v;
+            if (a.D != nullptr && q0 + 4 * ty + r < a.S) a.D[int64_t(h) * a.S + q0 + 4 * ty + r] = v;
+        }
     }
     // ---------------- pass 2: dS and dQ
     constexpr int CPT = HD / 16;                 // dQ columns per thread
@@ -330,6 +334,181 @@ int attn_core_launch(const AttnArgs &a, float rope_base, cudaStream_t st) {
     TLB_TRY(check_launch("attn_rows"));
     attn_dv_kernel<<<dim3(a.S, a.nkv), a.hd < 128 ? a.hd : 128, 0, st>>>(a);
     return check_launch("attn_dv");
+}
+
+
+// ------------------------------------------------------------------ key gradient (exact d_in)
+
+// Any shape: one block per (new key jj, KV head).  The dS values of up to blockDim (head,
+// query) pairs at a time are formed one pair per thread (a dot over head_dim), then every
+// thread adds their share into the head_dim columns it owns.
+__global__ void attn_dk_rows_kernel(AttnArgs a, const float *__restrict__ q, const float *__restrict__ Dv,
+                                    float *dk) {
+    extern __shared__ float4 smem4[];
+    float *sV = reinterpret_cast<float *>(smem4);      // [hd] V row of the key
+    float *sDs = sV + a.hd;                            // [blockDim] dS of the current pairs
+    const int jj = blockIdx.x, kvh = blockIdx.y, G = a.nh / a.nkv;
+    const int j = a.pos0 + jj, q_dim = a.nh * a.hd;
+    const int i0 = a.causal ? jj : 0;                   // query i sees key pos0 + jj iff i >= jj
+    const int nq = a.S - i0, npairs = G * nq;
+    const float *Vj = a.v + int64_t(kvh) * a.sh + int64_t(j) * a.sp;
+    for (int d = threadIdx.x; d < a.hd; d += blockDim.x) sV[d] = Vj[d];
+    constexpr int kMaxCols = 2;                         // head_dim <= 256, blockDim >= 128
+    float acc[kMaxCols] = {0.f, 0.f};
+    __syncthreads();
+    for (int p0 = 0; p0 < npairs; p0 += blockDim.x) {
+        const int pp = p0 + threadIdx.x;
+        float ds = 0.f;
+        if (pp < npairs) {
+            const int h = kvh * G + pp / nq, i = i0 + pp % nq;
+            const float P = a.attn[(int64_t(h) * a.S + i) * a.L + j];
+            const float *dc = a.dctx + int64_t(i) * q_dim + h * a.hd;
+            float t = 0.f;
+            for (int d = 0; d < a.hd; ++d) t = fmaf(dc[d], sV[d], t);
+            ds = P * (t - Dv[int64_t(h) * a.S + i]);
+        }
+        sDs[threadIdx.x] = ds;
+        __syncthreads();
+        const int n = min(int(blockDim.x), npairs - p0);
+        for (int t = 0; t < n; ++t) {
+            const int pt = p0 + t;
+            const int h = kvh * G + pt / nq, i = i0 + pt % nq;
+            const float *qr = q + int64_t(i) * q_dim + h * a.hd;
+            const float s = sDs[t];
+#pragma unroll
+            for (int k = 0; k < kMaxCols; ++k) {
+                const int d = threadIdx.x + k * blockDim.x;
+                if (d < a.hd) acc[k] = fmaf(s, qr[d], acc[k]);
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxCols; ++k) {
+        const int d = threadIdx.x + k * blockDim.x;
+        if (d < a.hd) dk[int64_t(jj) * a.nkv * a.hd + kvh * a.hd + d] = a.scale * acc[k];
+    }
+}
+
+// S > 1, head_dim 32 / 64 / 128: block = (64 new keys, KV head), 256 threads.  For every
+// head of the group and query tile: T = dCtx V^T on the tile (4 x 4 per thread), dS = P (T
+// - D) in shared memory, then dK += dS^T q (4 keys x HD/16 columns per thread).
+template <int HD>
+__global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__restrict__ q,
+                                                     const float *__restrict__ Dv, float *dk) {
+    extern __shared__ float4 sm4[];
+    float *sV = reinterpret_cast<float *>(sm4);         // [kT][HD+4]  V rows of the key tile
+    float *sC = sV + kT * (HD + 4);                     // [kT][HD+4]  dCtx tile [query][d]
+    float *sQ = sC + kT * (HD + 4);                     // [kT][HD+4]  q tile [query][d]
+    float *sS = sQ + kT * (HD + 4);                     // [kT][kTP]   dS tile [query][key]
+    __shared__ float sDq[kT];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int kvh = blockIdx.y, G = a.nh / a.nkv;
+    const int k0 = blockIdx.x * kT;                     // among the S newest keys
+    const int q_dim = a.nh * HD;
+    constexpr int CPT = HD / 16;
+    for (int e = tid; e < kT * HD; e += 256) {
+        const int j = e / HD, d = e % HD;
+        sV[j * (HD + 4) + d] =
+            (k0 + j < a.S) ? a.v[int64_t(kvh) * a.sh + int64_t(a.pos0 + k0 + j) * a.sp + d] : 0.f;
+    }
+    float acc[4][CPT];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) acc[r][c] = 0.f;
+    const int qt0 = a.causal ? k0 / kT : 0;
+    const int nqt = (a.S + kT - 1) / kT;
+    for (int g = 0; g < G; ++g) {
+        const int h = kvh * G + g;
+        const float *Ph = a.attn + int64_t(h) * a.S * a.L + a.pos0;
+        for (int qt = qt0; qt < nqt; ++qt) {
+            const int q0 = qt * kT;
+            __syncthreads();
+            for (int e = tid; e < kT * HD; e += 256) {
+                const int i = e / HD, d = e % HD;
+                const bool in = q0 + i < a.S;
+                sC[i * (HD + 4) + d] = in ? a.dctx[int64_t(q0 + i) * q_dim + h * HD + d] : 0.f;
+                sQ[i * (HD + 4) + d] = in ? q[int64_t(q0 + i) * q_dim + h * HD + d] : 0.f;
+            }
+            if (tid < kT) sDq[tid] = q0 + tid < a.S ? Dv[int64_t(h) * a.S + q0 + tid] : 0.f;
+            __syncthreads();
+            // T[i][j] for query rows 4 ty + r and keys 4 tx + c
+            float t[4][4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) t[r][c] = 0.f;
+#pragma unroll 4
+            for (int d = 0; d < HD; ++d) {
+                float cq[4], vk[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) cq[r] = sC[(4 * ty + r) * (HD + 4) + d];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) vk[c] = sV[(4 * tx + c) * (HD + 4) + d];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) t[r][c] = fmaf(cq[r], vk[c], t[r][c]);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = q0 + 4 * ty + r;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int jk = k0 + 4 * tx + c;
+                    const bool vis = i < a.S && jk < a.S && (!a.causal || i >= jk);
+                    const float P = vis ? Ph[int64_t(i) * a.L + jk] : 0.f;
+                    sS[(4 * ty + r) * kTP + 4 * tx + c] = P * (t[r][c] - sDq[4 * ty + r]);
+                }
+            }
+            __syncthreads();
+#pragma unroll 4
+            for (int i = 0; i < kT; ++i) {
+                const float4 sv = *reinterpret_cast<const float4 *>(sS + i * kTP + 4 * ty);
+                const float sr[4] = {sv.x, sv.y, sv.z, sv.w};
+                float qv[CPT];
+#pragma unroll
+                for (int c = 0; c < CPT; c += 2) {
+                    const float2 u = *reinterpret_cast<const float2 *>(sQ + i * (HD + 4) + tx * CPT + c);
+                    qv[c] = u.x;
+                    qv[c + 1] = u.y;
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < CPT; ++c) acc[r][c] = fmaf(sr[r], qv[c], acc[r][c]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int jj = k0 + 4 * ty + r;
+        if (jj >= a.S) continue;
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) dk[int64_t(jj) * a.nkv * HD + kvh * HD + tx * CPT + c] = a.scale * acc[r][c];
+    }
+}
+
+template <int HD>
+int launch_dk_tiled(const AttnArgs &a, const float *q, const float *D, float *dk, cudaStream_t st) {
+    const size_t sm = (size_t(3) * kT * (HD + 4) + size_t(kT) * kTP) * 4;
+    if (sm > 48 * 1024) TLB_CUDA(cudaFuncSetAttribute(attn_dk_tiled<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)));
+    attn_dk_tiled<HD><<<dim3(unsigned(ceil_div(a.S, kT)), unsigned(a.nkv)), 256, sm, st>>>(a, q, D, dk);
+    return check_launch("attn_dk_tiled");
+}
+
+int attn_dk_launch(const AttnArgs &a, const float *q, const float *D, float *dk, cudaStream_t st) {
+    if (a.S == 0) return TLB_OK;
+    if (a.S > 1) {
+        if (a.hd == 128) return launch_dk_tiled<128>(a, q, D, dk, st);
+        if (a.hd == 64) return launch_dk_tiled<64>(a, q, D, dk, st);
+        if (a.hd == 32) return launch_dk_tiled<32>(a, q, D, dk, st);
+    }
+    const int threads = 128;
+    attn_dk_rows_kernel<<<dim3(unsigned(a.S), unsigned(a.nkv)), threads, (size_t(a.hd) + threads) * 4, st>>>(
+        a, q, D, dk);
+    return check_launch("attn_dk_rows");
 }
 
 }  // namespace tlb

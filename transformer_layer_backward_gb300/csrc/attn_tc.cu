@@ -59,6 +59,7 @@ struct AttnTcParams {
     int S, L, nh, nkv, pos0, causal, rope;
     float scale;
     uint32_t *status;
+    float *D;                   // [nh, S] row sums D (optional)
     RopeFreqs fr;
 };
 
@@ -406,6 +407,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
         sD[hf][r] = D;
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
         D = sD[0][r] + sD[1][r];
+        if (p.D != nullptr && hf == 0 && i < p.S) p.D[int64_t(h) * p.S + i] = D;
         if (ok && mbar_wait(&ufull, 0, p.status, 29u)) {
             tc_fence_after();
             constexpr int half = HD / 2, q4 = HD / 4;
@@ -753,6 +755,7 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     p.rope = a.rope;
     p.scale = a.scale;
     p.status = status;
+    p.D = a.D;
     p.fr = fr;
 
     const int smq = DqLayout<HD>::TOTAL + 1024, smv = DvLayout<HD>::TOTAL + 1024;

@@ -608,6 +608,7 @@ __global__ void __launch_bounds__(kQThreads) dec_k6(DecodeArgs a, RopeFreqs fr) 
     }
     __syncthreads();
     const float D = sD;
+    if (a.Dout != nullptr && threadIdx.x == 0) a.Dout[h] = D;
     for (int dd = threadIdx.x; dd < a.hd; dd += blockDim.x) {
         float u = 0.f, w = 0.f;
         for (int g = 0; g < groups; ++g) {
@@ -827,7 +828,13 @@ int launch_ffn(const DecodeArgs &a, cudaStream_t st, bool k1_pdl) {
     return TLB_OK;
 }
 
-int launch_attn(const DecodeArgs &a, cudaStream_t st) {
+int launch_k7(const DecodeArgs &a, cudaStream_t st) {
+    const int64_t n7 = int64_t(a.qd + a.kvd) * a.rank + 2 * int64_t(a.rank) * a.H;
+    TLB_CUDA(launch(dec_k7, dim3(unsigned(ceil_div(n7, kThreads))), 0, st, true, a));
+    return check_launch("decode k7");
+}
+
+int launch_attn(const DecodeArgs &a, cudaStream_t st, bool with_k7) {
     const int G = a.nh / a.nkv;
     const dim3 g4(a.nkv, a.nchunks + 1);     // the last block of each KV head forms dV and gh_v
     const size_t sm4 = (size_t(G) * a.hd + size_t(kAWarps) * G * 2 * a.hd + size_t(a.qd)) * 4;
@@ -837,10 +844,7 @@ int launch_attn(const DecodeArgs &a, cudaStream_t st) {
     rope_freqs(fr, a.hd, a.rope_base);
     TLB_CUDA(launch_b(dec_k6, dim3(a.nh), kQThreads, 0, st, true, a, fr));
     TLB_TRY(check_launch("decode k6"));
-    const int64_t n7 = int64_t(a.qd + a.kvd) * a.rank + 2 * int64_t(a.rank) * a.H;
-    TLB_CUDA(launch(dec_k7, dim3(unsigned(ceil_div(n7, kThreads))), 0, st, true, a));
-    TLB_TRY(check_launch("decode k7"));
-    return TLB_OK;
+    return with_k7 ? launch_k7(a, st) : TLB_OK;
 }
 
 }  // namespace
@@ -866,7 +870,9 @@ int decode_ffn_launch(const DecodeArgs &a, int wtype, cudaStream_t st, bool k1_p
     }
 }
 
-int decode_attn_launch(const DecodeArgs &a, cudaStream_t st) { return launch_attn(a, st); }
+int decode_attn_launch(const DecodeArgs &a, cudaStream_t st, bool with_k7) { return launch_attn(a, st, with_k7); }
+
+int decode_lora_launch(const DecodeArgs &a, cudaStream_t st) { return launch_k7(a, st); }
 
 int decode_layer_launch(const DecodeArgs &a, int wtype, cudaStream_t st) {
     // k1 too starts as a programmatic dependent of whatever kernel precedes the call: before

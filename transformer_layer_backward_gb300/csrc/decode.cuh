@@ -23,6 +23,7 @@ struct DecodeArgs {
     AdamCoef ka, kb;
     double *sumsq;
     const uint32_t *status;   // status block (optional): its step gate set skips AdamW (k7)
+    float *Dout;              // [nh] (optional): k6 writes each head's D = sum_j attn dAttn
     // per-block partial sums (sum dy g x, sum x^2) for the RMSNorm backward of the
     // vector each GEMV produces; n1..n3 = the GEMV grids (blocks of k1, k2, k3)
     float2 *part1, *part2, *part3;
@@ -98,6 +99,8 @@ int decode_layer_launch(const DecodeArgs &a, int wtype, cudaStream_t st);
 // k1_pdl: launch k1 as a programmatic dependent of the kernel before it on `st` (it
 // prefetches its weights into L2, then waits for that kernel).
 int decode_ffn_launch(const DecodeArgs &a, int wtype, cudaStream_t st, bool k1_pdl);
-int decode_attn_launch(const DecodeArgs &a, cudaStream_t st);
+// k4, k6 and (with_k7) k7; without it k7 comes later through decode_lora_launch.
+int decode_attn_launch(const DecodeArgs &a, cudaStream_t st, bool with_k7 = true);
+int decode_lora_launch(const DecodeArgs &a, cudaStream_t st);
 
 }  // namespace tlb

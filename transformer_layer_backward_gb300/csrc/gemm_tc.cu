@@ -46,11 +46,12 @@ constexpr int kBM = 128, kBK = 64;       // tile rows, k block (64 bf16 = 128 by
 constexpr int kStages = 4;
 constexpr int kThreadsTC = 320;          // 10 warps: producer, MMA, 8 epilogue warps
 constexpr int kEpiWarpsTC = 8;           // two per TMEM lane quarter, each half of the columns
+constexpr int kMaxSeg = 3;               // K segments of one product
 
 struct TcParams {
-    CUtensorMap a[2];                    // bf16 [M, K_seg], box 64 x 128
-    CUtensorMap b[2];                    // bf16 [N, K_seg], box 64 x BN
-    int kb[2];                           // k blocks of each segment
+    CUtensorMap a[kMaxSeg];              // bf16 [M, K_seg], box 64 x 128
+    CUtensorMap b[kMaxSeg];              // bf16 [N, K_seg], box 64 x BN
+    int kb[kMaxSeg];                     // k blocks of each segment
     int nseg;
     int M, N;
     float alpha;
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
     // this CTA's iterations: the whole tiles [c dp, (c + 1) dp), then its stream-K range;
     // cut at tile boundaries into segments
     const int tiles_m = (p.M + kBM - 1) / kBM;
-    const int KB = p.kb[0] + (p.nseg > 1 ? p.kb[1] : 0);
+    const int KB = p.kb[0] + (p.nseg > 1 ? p.kb[1] : 0) + (p.nseg > 2 ? p.kb[2] : 0);
     const int64_t a0 = int64_t(blockIdx.x) * p.dp * KB, a1 = a0 + int64_t(p.dp) * KB;
     const int64_t b0 = p.sk_base + sk_start(p.sk_work, p.ctas, blockIdx.x);
     const int64_t b1 = p.sk_base + sk_start(p.sk_work, p.ctas, blockIdx.x + 1);
@@ -277,8 +278,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                         ok = false;
                         break;
                     }
-                    const int seg = kb < p.kb[0] ? 0 : 1;
-                    const int kx = (seg == 0 ? kb : kb - p.kb[0]) * kBK;
+                    const int seg = kb < p.kb[0] ? 0 : (kb < p.kb[0] + p.kb[1] ? 1 : 2);
+                    const int kx = (kb - (seg > 0 ? p.kb[0] : 0) - (seg > 1 ? p.kb[1] : 0)) * kBK;
                     uint8_t *sa = smem + s * STAGE;
                     mbar_arrive_expect_tx(&full[s], STAGE);
                     tma_load_2d(sa, &p.a[seg], kx, m0, &full[s]);
@@ -457,7 +458,7 @@ int launch_tc(const TcParams &p, cudaStream_t st) {
     k<<<p.ctas, kThreadsTC, smem, st>>>(p);
     TLB_TRY(check_launch("tcgen05 gemm"));
     // tiles of the stream-K part that more than one CTA touched
-    const int64_t KB = p.kb[0] + (p.nseg > 1 ? p.kb[1] : 0);
+    const int64_t KB = p.kb[0] + (p.nseg > 1 ? p.kb[1] : 0) + (p.nseg > 2 ? p.kb[2] : 0);
     TcFixup f;
     f.n = 0;
     int c = 0;
@@ -557,8 +558,9 @@ bool tc_supported(int64_t M, int64_t N, int64_t K) {
 
 int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, float *out, bool accumulate,
             float *partial, uint32_t *status, cudaStream_t st, const TcActEpilogue *act, void *out_bf16) {
-    TLB_REQUIRE(nseg == 1 || nseg == 2, TLB_EINVAL, "tcgen05 GEMM: 1 or 2 K segments");
-    const int64_t K = seg[0].K + (nseg > 1 ? seg[1].K : 0);
+    TLB_REQUIRE(nseg >= 1 && nseg <= kMaxSeg, TLB_EINVAL, "tcgen05 GEMM: 1 to 3 K segments");
+    int64_t K = 0;
+    for (int i = 0; i < nseg; ++i) K += seg[i].K;
     const TcPlan pl = tc_plan(M, N, K);
     TLB_REQUIRE(partial != nullptr, TLB_EINVAL, "tcgen05 GEMM: needs a partial-tile buffer");
     if (act != nullptr) {
@@ -598,7 +600,7 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
         p.dg = static_cast<uint2 *>(act->dgate);
         p.du = static_cast<uint2 *>(act->dup);
     }
-    const int64_t KB = p.kb[0] + (nseg > 1 ? p.kb[1] : 0), tiles = ceil_div(N, pl.bn) * ceil_div(M, kBM);
+    const int64_t KB = p.kb[0] + (nseg > 1 ? p.kb[1] : 0) + (nseg > 2 ? p.kb[2] : 0), tiles = ceil_div(N, pl.bn) * ceil_div(M, kBM);
     p.ctas = pl.ctas;
     p.dp = pl.dp;
     p.sk_base = int64_t(pl.dp) * pl.ctas * KB;

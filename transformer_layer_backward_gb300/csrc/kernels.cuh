@@ -74,8 +74,15 @@ struct AttnArgs {
     float *dv;               // [S, kv_dim]: rows of keys L - S .. L - 1
     int S, L, nh, nkv, hd, pos0, causal, rope;
     float scale;
+    float *D = nullptr;      // [nh, S] (optional): D[h, i] = sum_j attn[h,i,j] dAttn[h,i,j]
 };
 int attn_core_launch(const AttnArgs &a, float rope_base, cudaStream_t st);
+// Key gradient of the S newest cache rows (the keys of the call's own tokens), for the
+// exact layer-input gradient:
+//   dK[jj, kvh, :] = scale sum_{h in group} sum_i attn[h,i,j] (dCtx[i,h,:] . V[j,kvh,:] - D[h,i]) q[i,h,:]
+// with j = L - S + jj, q [S, q_dim] the cached queries (after RoPE), D from the attention
+// kernels; dk [S, kv_dim] (before RoPE backward).
+int attn_dk_launch(const AttnArgs &a, const float *q, const float *D, float *dk, cudaStream_t st);
 
 // Tensor-core (tf32) attention backward (attn_tc.cu): S > 1, head_dim 64 or 128, L and
 // L - S multiples of 4; attn, dq and dv 16-byte aligned.  scratch: attn_tc_bytes(...) bytes, 256-byte aligned.
@@ -97,6 +104,15 @@ struct LoraJob {
     void *scratch;
 };
 size_t lora_seq_bytes(int64_t S, int out_dim, int in_dim, int rank);
+// The LoRA-A paths of the exact layer-input gradient: dn1[S, in_dim] += sum over the jobs
+// of s (G B) A, with B [out_dim, rank] and A [rank, in_dim] taken before their update.
+struct LoraDinJob {
+    const float *G;          // [S, out_dim]
+    int out_dim;
+    const float *B, *A;
+};
+int lora_din_launch(int64_t S, int in_dim, int rank, float s, const LoraDinJob *jobs, int njobs, float *dn1,
+                    cudaStream_t st);
 // status (optional): a status block whose step gate (kStatusGate) is 1 skips the AdamW
 // steps (the gradients are still written and summed).
 int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x, const LoraJob *jobs, int njobs,

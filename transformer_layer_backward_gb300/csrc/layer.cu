@@ -19,6 +19,7 @@ struct LayerWs {
     size_t abf, gbf, ubf, part;               // tensor-core path: bf16 A operands, split-K partials
     size_t atc;                               // tensor-core attention: tf32 operand copies
     size_t dR1, Upart, Wpart, Dpart, gh2, part1, part2, part3, gbar, pp;   // single-token path
+    size_t dk, Dh, dn1, dctx, xbf;            // exact layer-input gradient (TLB_EXACT_DIN)
     size_t total;
 };
 
@@ -40,12 +41,16 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     LayerWs w;
     const int64_t I = c.ffn_dim, H = c.dim, qd = int64_t(c.n_heads) * c.head_dim;
     const int64_t kvd = int64_t(c.n_kv_heads) * c.head_dim;
+    const bool exact = (c.flags & TLB_EXACT_DIN) != 0;
     if (tc_route(c, S)) {
         w.abf = p.take(S * H * 2);            // dOut, later dR1, in bf16
         w.gbf = p.take(S * I * 2);            // dG in bf16
         w.ubf = p.take(S * I * 2);            // dU in bf16
-        w.part = p.take(std::max({tc_partial_bytes(S, I, H), tc_partial_bytes(S, H, 2 * I),
-                                  tc_partial_bytes(S, qd, H), size_t(256)}));
+        size_t part = std::max({tc_partial_bytes(S, I, H), tc_partial_bytes(S, H, 2 * I),
+                                tc_partial_bytes(S, qd, H), size_t(256)});
+        if (exact) part = std::max({part, tc_partial_bytes(S, H, qd + 2 * kvd), tc_partial_bytes(S, H, qd),
+                                    tc_partial_bytes(S, H, kvd)});
+        w.part = p.take(part);
     } else {
         w.abf = w.gbf = w.ubf = w.part = 0;
     }
@@ -73,6 +78,19 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
         w.pp = p.take(3 * int64_t(kMaxPersistentBlocks) * 8);
     } else {
         w.dR1 = w.Upart = w.Wpart = w.Dpart = w.gh2 = w.part1 = w.part2 = w.part3 = w.gbar = w.pp = 0;
+    }
+    if (exact) {
+        w.dk = p.take(S * kvd * 4);
+        w.Dh = p.take(int64_t(c.n_heads) * S * 4);
+        w.dn1 = p.take(S * H * 4);
+        w.dctx = p.take(S * qd * 4);
+        // [dQpre | dK | dV] in bf16, the A operands of the three-segment tcgen05 product
+        // (q_dim, kv_dim multiples of 8: every operand 16-byte aligned, whole float4 groups)
+        const bool tcx = tc_route(c, S) && qd % 8 == 0 && kvd % 8 == 0 && tc_supported(S, H, qd) &&
+                         tc_supported(S, H, kvd);
+        w.xbf = tcx ? p.take(S * (qd + 2 * kvd) * 2) : 0;
+    } else {
+        w.dk = w.Dh = w.dn1 = w.dctx = w.xbf = 0;
     }
     w.total = p.off;
     return w;
@@ -175,26 +193,10 @@ int ffn_impl(const tlb_layer_cfg &c, int64_t S, const float *d_out, const tlb_la
     return TLB_OK;
 }
 
-// abf_dr1: the workspace's bf16 operand buffer already holds dR1 in bf16.
-int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, const tlb_layer_weights &w,
-              const tlb_layer_acts &a, float *d_qpre, float *d_v, void *ws, cudaStream_t st, bool abf_dr1 = false) {
-    const LayerWs p = plan(c, S, L);
-    const int64_t qd = int64_t(c.n_heads) * c.head_dim;
-    float *dSub = ws_at<float>(ws, p.dSub);
-    // dSub = dR1 W_O^T
-    if (tc_route(c, S)) {
-        void *abf = ws_at<void>(ws, p.abf);
-        if (!abf_dr1) TLB_TRY(tc_convert_bf16(dR1, abf, S * c.dim, st));
-        const TcOperand o{abf, w.w_o.w, c.dim};
-        TLB_TRY(tc_gemm(&o, 1, S, qd, w.w_o.scale, dSub, false, ws_at<float>(ws, p.part), ws_at<uint32_t>(ws, 0), st));
-    } else {
-        TLB_TRY(linear_t_launch(c.wtype, w.w_o.w, w.w_o.scale, dR1, S, c.dim, qd, dSub, false, st));
-    }
-    // dCtx = RMSNorm_bwd(ctx, gamma_sub_attn, dSub) (sub-norm), in place
-    if (c.flags & TLB_SUB_NORM)
-        TLB_TRY(rmsnorm_backward_launch(a.ctx, w.gamma_sub_attn, dSub, dSub, S, qd, c.norm_eps, 0, st));
+AttnArgs attn_args(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dctx, const tlb_layer_acts &a,
+                   float *d_qpre, float *d_v) {
     AttnArgs g;
-    g.dctx = dSub;
+    g.dctx = dctx;
     g.k = a.k;
     g.v = a.v;
     g.sh = a.kv_stride_head;
@@ -211,6 +213,32 @@ int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, co
     g.causal = (c.flags & TLB_CAUSAL) ? 1 : 0;
     g.rope = (c.flags & TLB_ROPE) ? 1 : 0;
     g.scale = c.attn_scale;
+    g.D = nullptr;
+    return g;
+}
+
+// abf_dr1: the workspace's bf16 operand buffer already holds dR1 in bf16.  D (optional):
+// receives the attention's row sums D[h, i].
+int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, const tlb_layer_weights &w,
+              const tlb_layer_acts &a, float *d_qpre, float *d_v, void *ws, cudaStream_t st, bool abf_dr1 = false,
+              float *D = nullptr) {
+    const LayerWs p = plan(c, S, L);
+    const int64_t qd = int64_t(c.n_heads) * c.head_dim;
+    float *dSub = ws_at<float>(ws, p.dSub);
+    // dSub = dR1 W_O^T
+    if (tc_route(c, S)) {
+        void *abf = ws_at<void>(ws, p.abf);
+        if (!abf_dr1) TLB_TRY(tc_convert_bf16(dR1, abf, S * c.dim, st));
+        const TcOperand o{abf, w.w_o.w, c.dim};
+        TLB_TRY(tc_gemm(&o, 1, S, qd, w.w_o.scale, dSub, false, ws_at<float>(ws, p.part), ws_at<uint32_t>(ws, 0), st));
+    } else {
+        TLB_TRY(linear_t_launch(c.wtype, w.w_o.w, w.w_o.scale, dR1, S, c.dim, qd, dSub, false, st));
+    }
+    // dCtx = RMSNorm_bwd(ctx, gamma_sub_attn, dSub) (sub-norm), in place
+    if (c.flags & TLB_SUB_NORM)
+        TLB_TRY(rmsnorm_backward_launch(a.ctx, w.gamma_sub_attn, dSub, dSub, S, qd, c.norm_eps, 0, st));
+    AttnArgs g = attn_args(c, S, L, dSub, a, d_qpre, d_v);
+    g.D = D;
     if (attn_tc_route(c, S, L) && aligned16(d_qpre) && aligned16(d_v) && aligned16(a.attn))
         TLB_TRY(attn_tc_launch(g, c.rope_base, ws_at<void>(ws, p.atc), ws_at<uint32_t>(ws, 0), st));
     else
@@ -219,6 +247,73 @@ int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, co
     if (c.flags & TLB_QK_NORM)
         return rmsnorm_backward_launch(a.q_raw, w.gamma_q, d_qpre, d_qpre, S * c.n_heads, c.head_dim, c.norm_eps,
                                        0, st);
+    return TLB_OK;
+}
+
+// TLB_EXACT_DIN: the gradient of the layer input x_in beyond the pages' truncation
+// (they stop at the Q / V projection outputs), the plain derivative of the stated forward
+// with n1 = [RMSNorm(x_in; gamma_attn)] feeding the Q, K and V projections and both LoRA
+// A products:
+//   dK    = scale sum_group dS^T q on the S new cache rows, then RoPE backward and, with the
+//           QK-norm, the per-head RMSNorm backward with gamma_k;
+//   dn1   = s_q dQpre W_Q^T + s_k dK W_K^T + s_v dV W_V^T + s (dQpre B_q) A_q + s (dV B_v) A_v
+//           (A and B before their AdamW step: this runs before the LoRA kernels);
+//   d_in  = [dR1] + [RMSNorm_bwd(x_in, gamma_attn, dn1)]   (residual, pre-norm).
+// d_hidden holds dR1 on entry (already consumed by the O-projection product) and d_in on
+// return.  dctx: the attention's dCtx; D: its row sums.
+int exact_din_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const tlb_layer_weights &w,
+                   const tlb_layer_acts &a, const tlb_lora &lq, const tlb_lora &lv, const float *dqpre,
+                   const float *dv, const float *dctx, const float *D, float *d_hidden, void *ws, const LayerWs &p,
+                   cudaStream_t st) {
+    const int64_t H = c.dim, qd = int64_t(c.n_heads) * c.head_dim, kvd = int64_t(c.n_kv_heads) * c.head_dim;
+    float *dk = ws_at<float>(ws, p.dk);
+    const AttnArgs g = attn_args(c, S, L, dctx, a, nullptr, nullptr);
+    TLB_TRY(attn_dk_launch(g, a.q, D, dk, st));
+    if (c.flags & TLB_ROPE)
+        TLB_TRY(rope_backward_launch(dk, dk, S, c.n_kv_heads, c.head_dim, L - S, c.rope_base, st));
+    if (c.flags & TLB_QK_NORM)
+        TLB_TRY(rmsnorm_backward_launch(a.k_raw, w.gamma_k, dk, dk, S * c.n_kv_heads, c.head_dim, c.norm_eps, 0, st));
+    const bool pre = (c.flags & TLB_PRE_NORM) != 0, resid = (c.flags & TLB_RESIDUAL) != 0;
+    // the projections' input gradient goes to dn1 (the pre-norm backward then adds it into
+    // d_hidden) or, without the pre-norm, straight onto d_hidden (added to dR1 with the
+    // residual, over it without)
+    float *dst = pre ? ws_at<float>(ws, p.dn1) : d_hidden;
+    const bool acc0 = !pre && resid;
+    if (p.xbf != 0) {
+        uint32_t *status = ws_at<uint32_t>(ws, 0);
+        float *part = ws_at<float>(ws, p.part);
+        char *xb = ws_at<char>(ws, p.xbf);
+        void *qb = xb, *kb = xb + S * qd * 2, *vb = xb + S * (qd + kvd) * 2;
+        TLB_TRY(tc_convert_bf16(dqpre, qb, S * qd, st));
+        TLB_TRY(tc_convert_bf16(dk, kb, S * kvd, st));
+        TLB_TRY(tc_convert_bf16(dv, vb, S * kvd, st));
+        const TcOperand seg[3] = {{qb, w.w_q.w, qd}, {kb, w.w_k.w, kvd}, {vb, w.w_v.w, kvd}};
+        if (w.w_q.scale == w.w_k.scale && w.w_q.scale == w.w_v.scale) {
+            TLB_TRY(tc_gemm(seg, 3, S, H, w.w_q.scale, dst, acc0, part, status, st));
+        } else {
+            TLB_TRY(tc_gemm(&seg[0], 1, S, H, w.w_q.scale, dst, acc0, part, status, st));
+            TLB_TRY(tc_gemm(&seg[1], 1, S, H, w.w_k.scale, dst, true, part, status, st));
+            TLB_TRY(tc_gemm(&seg[2], 1, S, H, w.w_v.scale, dst, true, part, status, st));
+        }
+    } else {
+        TLB_TRY(linear_t_launch(c.wtype, w.w_q.w, w.w_q.scale, dqpre, S, qd, H, dst, acc0, st));
+        TLB_TRY(linear_t_launch(c.wtype, w.w_k.w, w.w_k.scale, dk, S, kvd, H, dst, true, st));
+        TLB_TRY(linear_t_launch(c.wtype, w.w_v.w, w.w_v.scale, dv, S, kvd, H, dst, true, st));
+    }
+    const LoraDinJob jobs[2] = {{dqpre, int(qd), lq.b, lq.a}, {dv, int(kvd), lv.b, lv.a}};
+    TLB_TRY(lora_din_launch(S, int(H), c.rank, c.lora_alpha / float(c.rank), jobs, 2, dst, st));
+    if (pre) TLB_TRY(rmsnorm_backward_launch(a.x_in, w.gamma_attn, dst, d_hidden, S, H, c.norm_eps, resid ? 1 : 0, st));
+    return TLB_OK;
+}
+
+int check_acts_exact(const tlb_layer_cfg &c, const tlb_layer_weights *w, const tlb_layer_acts *a) {
+    if (!(c.flags & TLB_EXACT_DIN)) return TLB_OK;
+    TLB_REQUIRE(w->w_q.w && w->w_k.w && w->w_v.w, TLB_EINVAL, "EXACT_DIN needs w_q, w_k and w_v");
+    TLB_REQUIRE(a->q, TLB_EINVAL, "EXACT_DIN needs q (the cached queries after RoPE)");
+    if (c.flags & TLB_PRE_NORM)
+        TLB_REQUIRE(a->x_in && w->gamma_attn, TLB_EINVAL, "EXACT_DIN with PRE_NORM needs x_in and gamma_attn");
+    if (c.flags & TLB_QK_NORM)
+        TLB_REQUIRE(a->k_raw && w->gamma_k, TLB_EINVAL, "EXACT_DIN with QK_NORM needs k_raw and gamma_k");
     return TLB_OK;
 }
 
@@ -344,6 +439,7 @@ void decode_args(const tlb_layer_cfg &c, int64_t L, const tlb_layer_weights *w, 
     d.kb = adam_coef(*adam, float(adam->lr_b_mult));
     d.sumsq = sumsq;
     d.status = nullptr;
+    d.Dout = nullptr;
     const int rpb = decode_rows_per_block();
     d.n1 = int(ceil_div(c.ffn_dim, rpb));
     d.n2 = int(ceil_div(c.dim, rpb));
@@ -423,6 +519,7 @@ static int layer_backward_impl(const tlb_layer_cfg *cfg, int64_t S, int64_t L, c
     TLB_TRY(validate_cfg(cfg));
     TLB_TRY(check_acts_ffn(*cfg, w, acts));
     TLB_TRY(check_acts_attn(*cfg, S, L, w, acts));
+    TLB_TRY(check_acts_exact(*cfg, w, acts));
     TLB_TRY(check_lora(lora_q, "Q"));
     TLB_TRY(check_lora(lora_v, "V"));
     TLB_TRY(check_adam(adam));
@@ -443,15 +540,30 @@ static int layer_backward_impl(const tlb_layer_cfg *cfg, int64_t S, int64_t L, c
     const bool chk = (c.flags & TLB_CHECK_FINITE) != 0;
     uint32_t *status = ws_at<uint32_t>(ws, 0);
     if (chk) TLB_TRY(finite_check_launch(d_hidden, S * c.dim, status, kSiteDOut, st));
+    const bool exact = (c.flags & TLB_EXACT_DIN) != 0;
+    float *Dh = exact ? ws_at<float>(ws, p.Dh) : nullptr;
     if (decode_route(c, S, L, w, acts, d_hidden)) {
         DecodeArgs d;
         decode_args(c, L, w, acts, lora_q, lora_v, adam, d_hidden, sumsq, ws, p, d);
-        if (chk) {
-            d.status = status;
+        if (chk || exact) {
+            if (chk) d.status = status;
+            d.Dout = Dh;
             TLB_TRY(decode_ffn_launch(d, c.wtype, st, false));
-            TLB_TRY(finite_check_launch(d.dR1, c.dim, status, kSiteDR1, st));
-            TLB_TRY(finite_gate_launch(status, status, st));
-            return decode_attn_launch(d, st);
+            if (chk) {
+                TLB_TRY(finite_check_launch(d.dR1, c.dim, status, kSiteDR1, st));
+                TLB_TRY(finite_gate_launch(status, status, st));
+            }
+            if (!exact) return decode_attn_launch(d, st);
+            // the exact input gradient needs A and B before k7's AdamW step
+            TLB_TRY(decode_attn_launch(d, st, false));
+            const float *dctx = d.dSub;
+            if (c.flags & TLB_SUB_NORM) {
+                float *t = ws_at<float>(ws, p.dctx);
+                TLB_TRY(rmsnorm_backward_launch(acts->ctx, w->gamma_sub_attn, d.dSub, t, 1, qd, c.norm_eps, 0, st));
+                dctx = t;
+            }
+            TLB_TRY(exact_din_impl(c, S, L, *w, *acts, *lora_q, *lora_v, dqpre, dv, dctx, Dh, d_hidden, ws, p, st));
+            return decode_lora_launch(d, st);
         }
         if ((c.flags & TLB_PERSISTENT) && persistent_supported(c, S, L))
             return decode_persistent_launch(d, c, L, ws, p.gbar, p.pp, st);
@@ -463,7 +575,10 @@ static int layer_backward_impl(const tlb_layer_cfg *cfg, int64_t S, int64_t L, c
         TLB_TRY(finite_check_launch(d_hidden, S * c.dim, status, kSiteDR1, st));
         TLB_TRY(finite_gate_launch(status, status, st));
     }
-    TLB_TRY(attn_impl(c, S, L, d_hidden, *w, *acts, dqpre, dv, ws, st, abf_dr1));
+    TLB_TRY(attn_impl(c, S, L, d_hidden, *w, *acts, dqpre, dv, ws, st, abf_dr1, Dh));
+    if (exact)   // attn_impl left dCtx in the dSub region
+        TLB_TRY(exact_din_impl(c, S, L, *w, *acts, *lora_q, *lora_v, dqpre, dv, ws_at<float>(ws, p.dSub), Dh,
+                               d_hidden, ws, p, st));
     const LoraJob jobs[2] = {{dqpre, acts->lora_q_h, qd, *lora_q, ws_at<void>(ws, p.lora_q)},
                              {dv, acts->lora_v_h, kvd, *lora_v, ws_at<void>(ws, p.lora_v)}};
     return lora_seq_launch(S, c.dim, c.rank, c.lora_alpha, acts->x, jobs, 2, *adam, sumsq, st,
@@ -548,11 +663,15 @@ int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n
     TLB_REQUIRE(ws != nullptr && ws_bytes >= need, TLB_EINVAL,
                 "stack workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
     TLB_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, TLB_EINVAL, "workspace not 256-byte aligned");
-    bool pipelined = S == 1 && !(c.flags & TLB_PERSISTENT);
+    // the overlap of a single-token stack hands dR1 down before the layer's attention half
+    // has run, which the exact input gradient needs
+    const bool exact = (c.flags & TLB_EXACT_DIN) != 0;
+    bool pipelined = S == 1 && !(c.flags & TLB_PERSISTENT) && !exact;
     const bool chk = (c.flags & TLB_CHECK_FINITE) != 0;
     for (int l = 0; l < n_layers; ++l) {
         TLB_TRY(check_acts_ffn(c, &w[l], &acts[l]));
         TLB_TRY(check_acts_attn(c, S, L, &w[l], &acts[l]));
+        TLB_TRY(check_acts_exact(c, &w[l], &acts[l]));
         TLB_TRY(check_lora(&lora_q[l], "Q"));
         TLB_TRY(check_lora(&lora_v[l], "V"));
         TLB_REQUIRE(acts[l].x && acts[l].lora_q_h && acts[l].lora_v_h, TLB_EINVAL,
@@ -565,7 +684,7 @@ int tlb_stack_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L, int32_t n
         // in bf16 in the set's operand buffer, where the next layer's first product reads it
         for (int l = n_layers - 1; l >= 0; --l)
             TLB_TRY(layer_backward_impl(cfg, S, L, &w[l], &acts[l], &lora_q[l], &lora_v[l], adam, d_hidden, sumsq,
-                                        ws, half, stream, l < n_layers - 1));
+                                        ws, half, stream, l < n_layers - 1 && !exact));
         return TLB_OK;
     }
     // Single-token layers: layer l's k1 .. k3 (its dR1, the next layer's dOut) on the

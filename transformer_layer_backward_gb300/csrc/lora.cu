@@ -771,4 +771,89 @@ int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x
     return lora_seq_run<64>(a, blk, ka, kb, sumsq, st);
 }
 
+
+// ------------------------------------------------------------------ LoRA-A paths of d_in
+
+namespace {
+
+constexpr int kDinRows = 16;
+
+struct LoraDinArgs {
+    LoraDinJob job[2];
+    int njobs, S, C, rank;
+    float s;
+    float *dn1;                  // [S, C], added into
+};
+
+// Block = 16 rows, 256 threads.  First gh[row][t][r] = s sum_o G_t[row, o] B_t[o, r]: one
+// (row, adapter) pair per warp at a time, the lanes over o, ranks 16 at a time in
+// registers; then dn1[row, c] += sum_t sum_r gh[row][t][r] A_t[r, c], every A value read
+// once per block and used for its 16 rows.
+__global__ void __launch_bounds__(256) lora_din_kernel(LoraDinArgs a) {
+    extern __shared__ float sgh[];                  // [kDinRows][njobs][rank]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = blockIdx.x * kDinRows;
+    const int nrows = min(kDinRows, a.S - r0);
+    for (int pr = warp; pr < kDinRows * a.njobs; pr += 8) {
+        const int row = pr / a.njobs, t = pr % a.njobs;
+        const float *G = a.job[t].G, *B = a.job[t].B;
+        const int O = a.job[t].out_dim;
+        for (int rc = 0; rc < a.rank; rc += 16) {
+            float acc[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+            if (row < nrows) {
+                const float *g = G + int64_t(r0 + row) * O;
+                for (int o = lane; o < O; o += 32) {
+                    const float gv = g[o];
+                    const float *b = B + int64_t(o) * a.rank + rc;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        if (rc + k < a.rank) acc[k] = fmaf(gv, b[k], acc[k]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float v = warp_sum(acc[k]);
+                if (lane == 0 && rc + k < a.rank) sgh[(row * a.njobs + t) * a.rank + rc + k] = a.s * v;
+            }
+        }
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < a.C; c += blockDim.x) {
+        float acc[kDinRows];
+#pragma unroll
+        for (int row = 0; row < kDinRows; ++row) acc[row] = 0.f;
+        for (int t = 0; t < a.njobs; ++t) {
+            const float *A = a.job[t].A;
+            for (int r = 0; r < a.rank; ++r) {
+                const float av = A[int64_t(r) * a.C + c];
+#pragma unroll
+                for (int row = 0; row < kDinRows; ++row)
+                    acc[row] = fmaf(sgh[(row * a.njobs + t) * a.rank + r], av, acc[row]);
+            }
+        }
+        for (int row = 0; row < nrows; ++row) a.dn1[int64_t(r0 + row) * a.C + c] += acc[row];
+    }
+}
+
+}  // namespace
+
+int lora_din_launch(int64_t S, int in_dim, int rank, float s, const LoraDinJob *jobs, int njobs, float *dn1,
+                    cudaStream_t st) {
+    if (S == 0 || njobs == 0) return TLB_OK;
+    TLB_REQUIRE(njobs <= 2 && rank >= 1 && rank <= 64, TLB_EINVAL, "lora d_in: bad adapter count or rank");
+    LoraDinArgs a{};
+    for (int t = 0; t < njobs; ++t) a.job[t] = jobs[t];
+    a.njobs = njobs;
+    a.S = int(S);
+    a.C = in_dim;
+    a.rank = rank;
+    a.s = s;
+    a.dn1 = dn1;
+    const size_t sm = size_t(kDinRows) * njobs * rank * 4;
+    lora_din_kernel<<<unsigned(ceil_div(S, int64_t(kDinRows))), 256, sm, st>>>(a);
+    return check_launch("lora_din");
+}
+
 }  // namespace tlb
