@@ -62,6 +62,9 @@ def parse(argv=None):
     p.add_argument("--workload", default="stack2048", choices=["decode", "seq512", "seq2048", "stack2048", "sweep", "tf32peak"])
     p.add_argument("--qk-norm", action="store_true",
                    help="layers with the per-head QK-norm on q (decode and sequence workloads)")
+    p.add_argument("--exact-din", action="store_true",
+                   help="sequence workloads: the exact layer-input gradient (through W_Q, W_K, W_V, the "
+                        "LoRA A paths and the attention pre-norm) instead of the pages' truncated one")
     a = p.parse_args(argv)
     if a.steps is None:
         a.steps = {"decode": 20000, "stack2048": 30}.get(a.workload, 200)
@@ -198,6 +201,8 @@ def run_reference(args, rank, world):
         cfg, depth = seq_config(args.workload)
         if args.qk_norm:
             cfg = cfg.with_(qk_norm=True)
+        if args.exact_din:
+            cfg = cfg.with_(exact_din=True)
         slices = seq_cpu_sample(cfg)
         for k in range(min(args.warmup, 1)):
             seq_cpu_time(slices[k])
@@ -256,16 +261,19 @@ def seq_kernel_flops(cfg, names):
     'tf32' marks the attention contractions."""
     S, L, H, I, qd = cfg.seq_len, cfg.cache_len, cfg.dim, cfg.ffn_dim, cfg.q_dim
     pairs = S * (L - S) + S * (S + 1) // 2
-    gemm = [2 * S * I * H, 2 * S * H * 2 * I, 2 * S * qd * H]
+    kvd = cfg.kv_dim
+    gemm = [2 * S * I * H, 2 * S * H * 2 * I, 2 * S * qd * H, 2 * S * H * (qd + 2 * kvd)]
     out, gi = [], 0
     for nm in names:
         if nm == "tcgen05 gemm":
-            out.append((gemm[gi] if gi < 3 else 0, "bf16"))
+            out.append((gemm[gi] if gi < 4 else 0, "bf16"))
             gi += 1
         elif nm == "attn_tc_dq":            # dAttn = dCtx V^T and dQ = dS K
             out.append((2 * 2 * pairs * cfg.head_dim * cfg.n_heads, "tf32"))
         elif nm == "attn_tc_dv":
             out.append((2 * pairs * cfg.head_dim * cfg.n_heads, "tf32"))
+        elif nm in ("attn_dk_tiled", "attn_dk_tc"):     # dAttn recomputed and dK = dS^T q
+            out.append((2 * 2 * pairs * cfg.head_dim * cfg.n_heads, "fp32" if nm == "attn_dk_tiled" else "tf32"))
         else:
             out.append((0, None))
     return out
@@ -276,7 +284,9 @@ def seq_workload_config(cfg, depth, world):
     name = ("%d-layer stack backward, S = L = %d" % (depth, cfg.seq_len) if depth > 1 else
             "sequence layer backward, S = L = %d" % cfg.seq_len)
     return {"workload": name + ": dim 2560, ffn 9728, 32/8 heads x 128, SwiGLU, RoPE, residual, " +
-                        ("QK-norm on q, " if cfg.qk_norm else "") + "bf16 weights, LoRA r16 Q/V, AdamW+LoRA+",
+                        ("QK-norm on q, " if cfg.qk_norm else "") +
+                        ("exact layer-input gradient, " if cfg.exact_din else "") +
+                        "bf16 weights, LoRA r16 Q/V, AdamW+LoRA+",
             "global_batch": world, "seq_len": cfg.seq_len, "layers_per_step": depth,
             "parallelism": "replicas" if world > 1 else "single",
             "l2": "inputs > L2 (each layer: weights 170 MB, attn %.0f MB)" % (cfg.n_heads * cfg.seq_len * cfg.cache_len * 4 / 1e6)}
@@ -302,6 +312,8 @@ def seq_main(args, rank, world, local, dist):
     cfg, depth = seq_config(args.workload)
     if args.qk_norm:
         cfg = cfg.with_(qk_norm=True)
+    if args.exact_din:
+        cfg = cfg.with_(exact_din=True)
     S, L = cfg.seq_len, cfg.cache_len
     NL = args.layers or (depth if depth > 1 else 2)     # distinct layers (weights, caches, adapters)
     c = tlb.layer_cfg_of(cfg)
@@ -440,7 +452,8 @@ def seq_main(args, rank, world, local, dist):
     # kernels), one tlb_layer_backward call per layer from the top of the stack down, and
     # d_in and the gradient sums read back at the end of each step
     acts = ("x", "gate", "up", "silu_gate", "k", "v", "attn", "lora_q_h", "lora_v_h") + \
-        (("q_raw",) if cfg.qk_norm else ())
+        (("q_raw",) if cfg.qk_norm else ()) + (("q",) if cfg.exact_din else ()) + \
+        (("k_raw",) if cfg.exact_din and cfg.qk_norm else ())
     NP = min(NL, 2)
     pinned = [{k: layers[l]["t"][k].cpu().pin_memory() for k in acts} for l in range(NP)]
     dout_h = layers[0]["t"]["dout"].cpu().pin_memory()
@@ -510,6 +523,10 @@ def seq_layer_flops(cfg):
     gemm = 2 * S * I * H + 2 * S * H * 2 * I + 2 * S * qd * H
     attn = 3 * 2 * pairs * cfg.head_dim * cfg.n_heads
     lora = sum(3 * 2 * S * od * r for od in (qd, kvd)) + 2 * 2 * S * r * H
+    if cfg.exact_din:       # dK = dS^T q, the [dQpre | dK | dV] W^T product, the LoRA A paths
+        gemm += 2 * S * H * (qd + 2 * kvd)
+        attn += 2 * pairs * cfg.head_dim * cfg.n_heads
+        lora += 2 * 2 * S * r * H
     return gemm + attn + lora
 
 

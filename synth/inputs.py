@@ -166,6 +166,12 @@ def layer_inputs_sample(cfg: LayerConfig, seed: int = 0) -> dict:
         d["v_" + p] = np.zeros_like(d[p])
     d["lora_q_h"] = d["x"] @ d["a_q"].T
     d["lora_v_h"] = d["x"] @ d["a_v"].T
+    if cfg.exact_din:
+        for k, shape in (("w_q", (H, qd)), ("w_k", (H, kvd)), ("w_v", (H, kvd))):
+            d[k], d["s_" + k[2:]] = n(shape, cfg.weight_std), 1.0
+        d["x_in"], d["q"] = n((S, H)), n((S, qd))
+        if cfg.pre_norm:
+            d["g_attn"] = g.uniform(0.5, 1.5, H).astype(f32)
     return d
 
 
@@ -176,7 +182,7 @@ def row_slice(cfg: LayerConfig, d: dict, r0: int, r1: int):
     L = cfg.pos0 + r1
     sub = cfg.with_(seq_len=r1 - r0, cache_len=L)
     rows = ("x", "gate", "up", "silu_gate", "dout", "lora_q_h", "lora_v_h", "hidden", "r1", "ctx",
-            "q_raw")
+            "q_raw", "x_in", "q", "k_raw")
     out = {}
     for k, v in d.items():
         if k in rows:
