@@ -104,18 +104,16 @@ struct LoraJob {
     void *scratch;
 };
 size_t lora_seq_bytes(int64_t S, int out_dim, int in_dim, int rank);
-// The LoRA-A paths of the exact layer-input gradient: dn1[S, in_dim] += sum over the jobs
-// of s (G B) A, with B [out_dim, rank] and A [rank, in_dim] taken before their update.
-struct LoraDinJob {
-    const float *G;          // [S, out_dim]
-    int out_dim;
-    const float *B, *A;
-};
-int lora_din_launch(int64_t S, int in_dim, int rank, float s, const LoraDinJob *jobs, int njobs, float *dn1,
-                    cudaStream_t st);
+// The LoRA-A paths of the exact layer-input gradient: dn1[S, in_dim] += sum over the
+// adapters of gh A, gh [S, rank] = s G B and A [rank, in_dim] both from before the update.
+int lora_din_launch(int64_t S, int in_dim, int rank, const float *const *gh, const float *const *A, int njobs,
+                    float *dn1, cudaStream_t st);
 // status (optional): a status block whose step gate (kStatusGate) is 1 skips the AdamW
 // steps (the gradients are still written and summed).
+// din (optional): dn1 of the exact input gradient; gh A of every adapter is added into it
+// between the gh sums and AdamW.
 int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x, const LoraJob *jobs, int njobs,
-                    const tlb_adamw_cfg &adam, double *sumsq, cudaStream_t st, const uint32_t *status = nullptr);
+                    const tlb_adamw_cfg &adam, double *sumsq, cudaStream_t st, const uint32_t *status = nullptr,
+                    float *din = nullptr);
 
 }  // namespace tlb

@@ -250,21 +250,26 @@ int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, co
     return TLB_OK;
 }
 
-// TLB_EXACT_DIN: the gradient of the layer input x_in beyond the pages' truncation
+// Where exact_din_impl left the projections' input gradient (the LoRA A paths go there too).
+float *exact_dst(const tlb_layer_cfg &c, float *d_hidden, void *ws, const LayerWs &p) {
+    return (c.flags & TLB_PRE_NORM) ? ws_at<float>(ws, p.dn1) : d_hidden;
+}
+
+// TLB_EXACT_DIN (first part): the gradient of the layer input x_in beyond the pages' truncation
 // (they stop at the Q / V projection outputs), the plain derivative of the stated forward
 // with n1 = [RMSNorm(x_in; gamma_attn)] feeding the Q, K and V projections and both LoRA
 // A products:
 //   dK    = scale sum_group dS^T q on the S new cache rows, then RoPE backward and, with the
 //           QK-norm, the per-head RMSNorm backward with gamma_k;
 //   dn1   = s_q dQpre W_Q^T + s_k dK W_K^T + s_v dV W_V^T + s (dQpre B_q) A_q + s (dV B_v) A_v
-//           (A and B before their AdamW step: this runs before the LoRA kernels);
-//   d_in  = [dR1] + [RMSNorm_bwd(x_in, gamma_attn, dn1)]   (residual, pre-norm).
-// d_hidden holds dR1 on entry (already consumed by the O-projection product) and d_in on
-// return.  dctx: the attention's dCtx; D: its row sums.
+//           (the last two, with A and B from before their AdamW step, are added by the LoRA
+//           kernels, which form gh = s G B anyway);
+//   d_in  = [dR1] + [RMSNorm_bwd(x_in, gamma_attn, dn1)]   (residual, pre-norm: exact_din_finish).
+// d_hidden holds dR1 on entry (already consumed by the O-projection product); without the
+// pre-norm dn1 is formed on d_hidden itself.  dctx: the attention's dCtx; D: its row sums.
 int exact_din_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const tlb_layer_weights &w,
-                   const tlb_layer_acts &a, const tlb_lora &lq, const tlb_lora &lv, const float *dqpre,
-                   const float *dv, const float *dctx, const float *D, float *d_hidden, void *ws, const LayerWs &p,
-                   cudaStream_t st) {
+                   const tlb_layer_acts &a, const float *dqpre, const float *dv, const float *dctx, const float *D,
+                   float *d_hidden, void *ws, const LayerWs &p, cudaStream_t st) {
     const int64_t H = c.dim, qd = int64_t(c.n_heads) * c.head_dim, kvd = int64_t(c.n_kv_heads) * c.head_dim;
     float *dk = ws_at<float>(ws, p.dk);
     const AttnArgs g = attn_args(c, S, L, dctx, a, nullptr, nullptr);
@@ -277,7 +282,7 @@ int exact_din_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const tlb_layer
     // the projections' input gradient goes to dn1 (the pre-norm backward then adds it into
     // d_hidden) or, without the pre-norm, straight onto d_hidden (added to dR1 with the
     // residual, over it without)
-    float *dst = pre ? ws_at<float>(ws, p.dn1) : d_hidden;
+    float *dst = exact_dst(c, d_hidden, ws, p);
     const bool acc0 = !pre && resid;
     if (p.xbf != 0) {
         uint32_t *status = ws_at<uint32_t>(ws, 0);
@@ -300,10 +305,15 @@ int exact_din_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const tlb_layer
         TLB_TRY(linear_t_launch(c.wtype, w.w_k.w, w.w_k.scale, dk, S, kvd, H, dst, true, st));
         TLB_TRY(linear_t_launch(c.wtype, w.w_v.w, w.w_v.scale, dv, S, kvd, H, dst, true, st));
     }
-    const LoraDinJob jobs[2] = {{dqpre, int(qd), lq.b, lq.a}, {dv, int(kvd), lv.b, lv.a}};
-    TLB_TRY(lora_din_launch(S, int(H), c.rank, c.lora_alpha / float(c.rank), jobs, 2, dst, st));
-    if (pre) TLB_TRY(rmsnorm_backward_launch(a.x_in, w.gamma_attn, dst, d_hidden, S, H, c.norm_eps, resid ? 1 : 0, st));
     return TLB_OK;
+}
+
+// The last step of the exact input gradient, after the LoRA A paths were added into dn1.
+int exact_din_finish(const tlb_layer_cfg &c, int64_t S, const tlb_layer_weights &w, const tlb_layer_acts &a,
+                     float *d_hidden, void *ws, const LayerWs &p, cudaStream_t st) {
+    if (!(c.flags & TLB_PRE_NORM)) return TLB_OK;
+    return rmsnorm_backward_launch(a.x_in, w.gamma_attn, ws_at<float>(ws, p.dn1), d_hidden, S, c.dim, c.norm_eps,
+                                   (c.flags & TLB_RESIDUAL) ? 1 : 0, st);
 }
 
 int check_acts_exact(const tlb_layer_cfg &c, const tlb_layer_weights *w, const tlb_layer_acts *a) {
@@ -562,7 +572,12 @@ static int layer_backward_impl(const tlb_layer_cfg *cfg, int64_t S, int64_t L, c
                 TLB_TRY(rmsnorm_backward_launch(acts->ctx, w->gamma_sub_attn, d.dSub, t, 1, qd, c.norm_eps, 0, st));
                 dctx = t;
             }
-            TLB_TRY(exact_din_impl(c, S, L, *w, *acts, *lora_q, *lora_v, dqpre, dv, dctx, Dh, d_hidden, ws, p, st));
+            TLB_TRY(exact_din_impl(c, S, L, *w, *acts, dqpre, dv, dctx, Dh, d_hidden, ws, p, st));
+            // gh = [gh_q | gh_v] from k4 / k6 (B before k7's step)
+            const float *gh[2] = {d.gh, d.gh + c.rank};
+            const float *A[2] = {lora_q->a, lora_v->a};
+            TLB_TRY(lora_din_launch(1, c.dim, c.rank, gh, A, 2, exact_dst(c, d_hidden, ws, p), st));
+            TLB_TRY(exact_din_finish(c, S, *w, *acts, d_hidden, ws, p, st));
             return decode_lora_launch(d, st);
         }
         if ((c.flags & TLB_PERSISTENT) && persistent_supported(c, S, L))
@@ -577,12 +592,12 @@ static int layer_backward_impl(const tlb_layer_cfg *cfg, int64_t S, int64_t L, c
     }
     TLB_TRY(attn_impl(c, S, L, d_hidden, *w, *acts, dqpre, dv, ws, st, abf_dr1, Dh));
     if (exact)   // attn_impl left dCtx in the dSub region
-        TLB_TRY(exact_din_impl(c, S, L, *w, *acts, *lora_q, *lora_v, dqpre, dv, ws_at<float>(ws, p.dSub), Dh,
-                               d_hidden, ws, p, st));
+        TLB_TRY(exact_din_impl(c, S, L, *w, *acts, dqpre, dv, ws_at<float>(ws, p.dSub), Dh, d_hidden, ws, p, st));
     const LoraJob jobs[2] = {{dqpre, acts->lora_q_h, qd, *lora_q, ws_at<void>(ws, p.lora_q)},
                              {dv, acts->lora_v_h, kvd, *lora_v, ws_at<void>(ws, p.lora_v)}};
-    return lora_seq_launch(S, c.dim, c.rank, c.lora_alpha, acts->x, jobs, 2, *adam, sumsq, st,
-                           chk ? status : nullptr);
+    TLB_TRY(lora_seq_launch(S, c.dim, c.rank, c.lora_alpha, acts->x, jobs, 2, *adam, sumsq, st,
+                            chk ? status : nullptr, exact ? exact_dst(c, d_hidden, ws, p) : nullptr));
+    return exact ? exact_din_finish(c, S, *w, *acts, d_hidden, ws, p, st) : TLB_OK;
 }
 
 extern "C" {

@@ -650,7 +650,7 @@ SideBytes side_bytes(int64_t S, int out_dim, int in_dim, int rank) {
 
 template <int RB>
 int lora_seq_run(LoraSeqArgs a, int n_ot_total, const AdamCoef &ka, const AdamCoef &kb, double *sumsq,
-                 cudaStream_t st) {
+                 cudaStream_t st, float *din) {
     // chunks of row tiles per block: at most two blocks per SM in each pass (one wave)
     const int target = 2 * num_sms();
     a.nrc_b = int(std::min<int64_t>(a.n_rt, std::max<int64_t>(1, target / n_ot_total)));
@@ -706,6 +706,11 @@ int lora_seq_run(LoraSeqArgs a, int n_ot_total, const AdamCoef &ka, const AdamCo
     const int64_t ngh = int64_t(a.nside) * a.S * a.rank;
     lora_gh_sum_kernel<<<unsigned(ceil_div(ngh, int64_t(256))), 256, 0, st>>>(a);
     TLB_TRY(check_launch("lora_gh_sum"));
+    if (din != nullptr) {      // the LoRA A paths of the exact input gradient, before AdamW moves A
+        const float *gh[2] = {a.side[0].gh, a.side[1].gh};
+        const float *A[2] = {a.side[0].l.a, a.side[1].l.a};
+        TLB_TRY(lora_din_launch(a.S, a.C, a.rank, gh, A, a.nside, din, st));
+    }
     if constexpr (RB == 16) lora_xpass16_kernel<<<dim3(unsigned(n_ct), unsigned(a.nrc_a)), 256, smx, st>>>(a);
     else lora_xpass_kernel<RB><<<dim3(unsigned(n_ct), unsigned(a.nrc_a)), 256, smx, st>>>(a);
     TLB_TRY(check_launch("lora_xpass"));
@@ -722,7 +727,8 @@ size_t lora_seq_bytes(int64_t S, int out_dim, int in_dim, int rank) {
 }
 
 int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x, const LoraJob *jobs, int njobs,
-                    const tlb_adamw_cfg &adam, double *sumsq, cudaStream_t st, const uint32_t *status) {
+                    const tlb_adamw_cfg &adam, double *sumsq, cudaStream_t st, const uint32_t *status,
+                    float *din) {
     if (S == 0 || njobs == 0) return TLB_OK;
     TLB_REQUIRE(njobs <= 2, TLB_EINVAL, "lora: at most two adapters per call");
     TLB_REQUIRE(rank >= 1 && rank <= 64, TLB_EINVAL, "lora: rank must be in 1..64");
@@ -764,11 +770,11 @@ int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x
     }
     const AdamCoef kb = adam_coef(adam, adam.lr_b_mult);
     const AdamCoef ka = adam_coef(adam, 1.0f);
-    if (rank <= 4) return lora_seq_run<4>(a, blk, ka, kb, sumsq, st);
-    if (rank <= 8) return lora_seq_run<8>(a, blk, ka, kb, sumsq, st);
-    if (rank <= 16) return lora_seq_run<16>(a, blk, ka, kb, sumsq, st);
-    if (rank <= 32) return lora_seq_run<32>(a, blk, ka, kb, sumsq, st);
-    return lora_seq_run<64>(a, blk, ka, kb, sumsq, st);
+    if (rank <= 4) return lora_seq_run<4>(a, blk, ka, kb, sumsq, st, din);
+    if (rank <= 8) return lora_seq_run<8>(a, blk, ka, kb, sumsq, st, din);
+    if (rank <= 16) return lora_seq_run<16>(a, blk, ka, kb, sumsq, st, din);
+    if (rank <= 32) return lora_seq_run<32>(a, blk, ka, kb, sumsq, st, din);
+    return lora_seq_run<64>(a, blk, ka, kb, sumsq, st, din);
 }
 
 
@@ -779,45 +785,23 @@ namespace {
 constexpr int kDinRows = 16;
 
 struct LoraDinArgs {
-    LoraDinJob job[2];
+    const float *gh[2];          // [S, rank] each: s G B with B before its update
+    const float *A[2];           // [rank, C] each, before its update
     int njobs, S, C, rank;
-    float s;
     float *dn1;                  // [S, C], added into
 };
 
-// Block = 16 rows, 256 threads.  First gh[row][t][r] = s sum_o G_t[row, o] B_t[o, r]: one
-// (row, adapter) pair per warp at a time, the lanes over o, ranks 16 at a time in
-// registers; then dn1[row, c] += sum_t sum_r gh[row][t][r] A_t[r, c], every A value read
-// once per block and used for its 16 rows.
+// Block = 16 rows, 256 threads: the rows' gh values of both adapters in shared memory, then
+// dn1[row, c] += sum_t sum_r gh_t[row, r] A_t[r, c], each A value read once per block and
+// used for its 16 rows.
 __global__ void __launch_bounds__(256) lora_din_kernel(LoraDinArgs a) {
     extern __shared__ float sgh[];                  // [kDinRows][njobs][rank]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r0 = blockIdx.x * kDinRows;
     const int nrows = min(kDinRows, a.S - r0);
-    for (int pr = warp; pr < kDinRows * a.njobs; pr += 8) {
-        const int row = pr / a.njobs, t = pr % a.njobs;
-        const float *G = a.job[t].G, *B = a.job[t].B;
-        const int O = a.job[t].out_dim;
-        for (int rc = 0; rc < a.rank; rc += 16) {
-            float acc[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-            if (row < nrows) {
-                const float *g = G + int64_t(r0 + row) * O;
-                for (int o = lane; o < O; o += 32) {
-                    const float gv = g[o];
-                    const float *b = B + int64_t(o) * a.rank + rc;
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        if (rc + k < a.rank) acc[k] = fmaf(gv, b[k], acc[k]);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float v = warp_sum(acc[k]);
-                if (lane == 0 && rc + k < a.rank) sgh[(row * a.njobs + t) * a.rank + rc + k] = a.s * v;
-            }
-        }
+    const int per = a.njobs * a.rank;
+    for (int e = threadIdx.x; e < kDinRows * per; e += blockDim.x) {
+        const int row = e / per, t = (e % per) / a.rank, r = e % a.rank;
+        sgh[e] = row < nrows ? (t == 0 ? a.gh[0] : a.gh[1])[int64_t(r0 + row) * a.rank + r] : 0.f;
     }
     __syncthreads();
     for (int c = threadIdx.x; c < a.C; c += blockDim.x) {
@@ -825,12 +809,11 @@ __global__ void __launch_bounds__(256) lora_din_kernel(LoraDinArgs a) {
 #pragma unroll
         for (int row = 0; row < kDinRows; ++row) acc[row] = 0.f;
         for (int t = 0; t < a.njobs; ++t) {
-            const float *A = a.job[t].A;
+            const float *A = t == 0 ? a.A[0] : a.A[1];
             for (int r = 0; r < a.rank; ++r) {
                 const float av = A[int64_t(r) * a.C + c];
 #pragma unroll
-                for (int row = 0; row < kDinRows; ++row)
-                    acc[row] = fmaf(sgh[(row * a.njobs + t) * a.rank + r], av, acc[row]);
+                for (int row = 0; row < kDinRows; ++row) acc[row] = fmaf(sgh[row * per + t * a.rank + r], av, acc[row]);
             }
         }
         for (int row = 0; row < nrows; ++row) a.dn1[int64_t(r0 + row) * a.C + c] += acc[row];
@@ -839,17 +822,19 @@ __global__ void __launch_bounds__(256) lora_din_kernel(LoraDinArgs a) {
 
 }  // namespace
 
-int lora_din_launch(int64_t S, int in_dim, int rank, float s, const LoraDinJob *jobs, int njobs, float *dn1,
-                    cudaStream_t st) {
+int lora_din_launch(int64_t S, int in_dim, int rank, const float *const *gh, const float *const *A, int njobs,
+                    float *dn1, cudaStream_t st) {
     if (S == 0 || njobs == 0) return TLB_OK;
     TLB_REQUIRE(njobs <= 2 && rank >= 1 && rank <= 64, TLB_EINVAL, "lora d_in: bad adapter count or rank");
     LoraDinArgs a{};
-    for (int t = 0; t < njobs; ++t) a.job[t] = jobs[t];
+    for (int t = 0; t < njobs; ++t) {
+        a.gh[t] = gh[t];
+        a.A[t] = A[t];
+    }
     a.njobs = njobs;
     a.S = int(S);
     a.C = in_dim;
     a.rank = rank;
-    a.s = s;
     a.dn1 = dn1;
     const size_t sm = size_t(kDinRows) * njobs * rank * 4;
     lora_din_kernel<<<unsigned(ceil_div(S, int64_t(kDinRows))), 256, sm, st>>>(a);
