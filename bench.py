@@ -62,6 +62,8 @@ def parse(argv=None):
     p.add_argument("--workload", default="stack2048", choices=["decode", "seq512", "seq2048", "stack2048", "sweep", "tf32peak"])
     p.add_argument("--qk-norm", action="store_true",
                    help="layers with the per-head QK-norm on q (decode and sequence workloads)")
+    p.add_argument("--wtype", default="ternary", choices=["ternary", "ternary2"],
+                   help="decode: int8 ternary weights, or the same values packed four 2-bit codes to a byte")
     p.add_argument("--exact-din", action="store_true",
                    help="sequence workloads: the exact layer-input gradient (through W_Q, W_K, W_V, the "
                         "LoRA A paths and the attention pre-norm) instead of the pages' truncated one")
@@ -73,10 +75,15 @@ def parse(argv=None):
     return a
 
 
+def wbytes(cfg) -> float:
+    """Bytes per stored weight: int8 ternary 1, packed ternary 1/4."""
+    return 0.25 if cfg.wtype == "ternary2" else 1.0
+
+
 def decode_bytes(cfg) -> int:
     """Algorithmic HBM bytes of one decode layer backward (each input read once)."""
     H, I, qd, kvd, r, L = cfg.dim, cfg.ffn_dim, cfg.q_dim, cfg.kv_dim, cfg.rank, cfg.cache_len
-    weights = (I * H + 2 * H * I + qd * H) * 1                      # ternary int8
+    weights = int((I * H + 2 * H * I + qd * H) * wbytes(cfg))       # ternary int8 or packed
     kv = 2 * kvd * L * 4
     attn = cfg.n_heads * L * 4
     lora = (2 * r * H + qd * r + kvd * r) * 24                      # p, m, v read + write
@@ -89,10 +96,11 @@ def decode_bytes(cfg) -> int:
 def decode_kernel_bytes(cfg):
     H, I, qd, kvd, r, L, nh = cfg.dim, cfg.ffn_dim, cfg.q_dim, cfg.kv_dim, cfg.rank, cfg.cache_len, cfg.n_heads
     lora = (2 * r * H + qd * r + kvd * r) * 24 + 2 * H * 4 + 2 * r * 4
+    wb = wbytes(cfg)
     return [
-        ("dec_k1 dF = W_down dOut", I * H + (H + I + 2 * I) * 4),
-        ("dec_k2 dN2 = W_gate dG + W_up dU", 2 * H * I + (5 * I + 3 * H) * 4),
-        ("dec_k3 dSub = W_O dR1", qd * H + (4 * H + qd + 2 * qd) * 4),
+        ("dec_k1 dF = W_down dOut", int(I * H * wb) + (H + I + 2 * I) * 4),
+        ("dec_k2 dN2 = W_gate dG + W_up dU", int(2 * H * I * wb) + (5 * I + 3 * H) * 4),
+        ("dec_k3 dSub = W_O dR1", int(qd * H * wb) + (4 * H + qd + 2 * qd) * 4),
         ("dec_k4 attention over K, V", 2 * kvd * L * 4 + nh * L * 4 + 3 * qd * 4),
         ("dec_k6 dQpre, gh_q", 2 * qd * 4 * (L // 64) + qd * r * 4),
         ("dec_k7 LoRA grads + AdamW", lora),
@@ -222,6 +230,8 @@ def run_reference(args, rank, world):
         return
     from synth import DECODE
     cfg = DECODE.with_(qk_norm=True) if args.qk_norm else DECODE
+    if args.wtype == "ternary2":
+        cfg = cfg.with_(name="decode_t2", wtype="ternary2")
     per = max(args.cpu_seconds / max(args.steps, 1), 0.0)
     times = []
     for _ in range(args.warmup if args.warmup < 3 else 1):
@@ -857,6 +867,8 @@ def main():
     torch.cuda.set_device(local)
     tlb.load()
     cfg = DECODE.with_(qk_norm=True) if args.qk_norm else DECODE
+    if args.wtype == "ternary2":
+        cfg = cfg.with_(name="decode_t2", wtype="ternary2")
     NL = args.layers or 8
     c = tlb.layer_cfg_of(cfg)
     adam = tlb.adamw_cfg_of(cfg)
@@ -980,7 +992,7 @@ def main():
     achieved = per_kernel[dom]["GB/s"]
     traffic = None
     prof = os.path.join(ROOT, "profiles", "decode_dram_bytes.json")
-    if os.path.exists(prof):
+    if os.path.exists(prof) and cfg.wtype == "ternary":          # captured with int8 weights
         traffic = json.load(open(prof)).get(kern[dom][0].split()[0])
 
     # end to end through the public API: per-step activations from pinned host memory,
@@ -1066,7 +1078,9 @@ def main():
                 "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": {"workload": "decode layer backward: dim 2560, ffn 6912, 20/5 heads "
-                                       "x 128, cache 1024, pos 1023, ternary int8 weights, ReLU^2xMul, "
+                                       "x 128, cache 1024, pos 1023, " +
+                                       ("packed 2-bit" if cfg.wtype == "ternary2" else "int8") +
+                                       " ternary weights, ReLU^2xMul, "
                                        "sub-norms, " + ("QK-norm on q, " if cfg.qk_norm else "") +
                                        "LoRA r16 Q/V, AdamW+LoRA+",
                            "global_batch": world, "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",

@@ -44,7 +44,14 @@ import numpy as np
 
 from .ops import (adamw, apply_backward, f64, linear_backward, lora_backward,
                   relu2_mul_backward, rmsnorm_backward, rope_backward, score_backward_k,
-                  score_backward_q, silu_mul_backward, softmax_backward, value_backward)
+                  score_backward_q, silu_mul_backward, softmax_backward, unpack_ternary2,
+                  value_backward)
+
+
+def W(cfg, d, name) -> np.ndarray:
+    """A weight matrix [in, out] as values (packed ternary storage decoded)."""
+    w = d[name]
+    return unpack_ternary2(w) if getattr(cfg, "wtype", "") == "ternary2" else w
 
 
 def kv_heads_first(a, cfg) -> np.ndarray:
@@ -58,14 +65,14 @@ def kv_heads_first(a, cfg) -> np.ndarray:
 def ffn_backward(cfg, d, dout) -> dict:
     eps = cfg.norm_eps
     dout = f64(dout)
-    dF = linear_backward(dout, d["w_down"], d["s_down"])
+    dF = linear_backward(dout, W(cfg, d, "w_down"), d["s_down"])
     dh = rmsnorm_backward(d["hidden"], d["g_sub_ffn"], dF, eps) if cfg.sub_norm else dF
     if cfg.act == "relu2_mul":
         dG, dU = relu2_mul_backward(d["gate"], d["up"], dh)
     else:
         sg = d.get("silu_gate") if cfg.use_silu_cache else None
         dG, dU = silu_mul_backward(d["gate"], d["up"], dh, sg)
-    dN2 = linear_backward(dG, d["w_gate"], d["s_gate"]) + linear_backward(dU, d["w_up"], d["s_up"])
+    dN2 = linear_backward(dG, W(cfg, d, "w_gate"), d["s_gate"]) + linear_backward(dU, W(cfg, d, "w_up"), d["s_up"])
     dN2r = rmsnorm_backward(d["r1"], d["g_ffn"], dN2, eps) if cfg.pre_norm else dN2
     dR1 = dout + dN2r if cfg.residual else dN2r
     return dict(dF=dF, dh=dh, dG=dG, dU=dU, dN2=dN2, dR1=dR1)
@@ -73,7 +80,7 @@ def ffn_backward(cfg, d, dout) -> dict:
 
 def attn_backward(cfg, d, dR1) -> dict:
     S, L, nh, nkv, hd = cfg.seq_len, cfg.cache_len, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
-    dSub = linear_backward(dR1, d["w_o"], d["s_o"])
+    dSub = linear_backward(dR1, W(cfg, d, "w_o"), d["s_o"])
     dCtx = rmsnorm_backward(d["ctx"], d["g_sub_attn"], dSub, cfg.norm_eps) if cfg.sub_norm else dSub
     K, V = kv_heads_first(d["k"], cfg), kv_heads_first(d["v"], cfg)
     attn = f64(d["attn"])
@@ -114,9 +121,9 @@ def input_backward(cfg, d, r) -> np.ndarray:
     """Exact layer-input gradient (``cfg.exact_din``): the attention input n1 feeds the
     Q, K and V projections and both LoRA A products; x_in reaches r1 through the
     residual and n1 through the attention pre-norm."""
-    dn1 = (linear_backward(r["dQpre"], d["w_q"], d.get("s_q", 1.0)) +
-           linear_backward(r["dKpre"], d["w_k"], d.get("s_k", 1.0)) +
-           linear_backward(r["dV"], d["w_v"], d.get("s_v", 1.0)) +
+    dn1 = (linear_backward(r["dQpre"], W(cfg, d, "w_q"), d.get("s_q", 1.0)) +
+           linear_backward(r["dKpre"], W(cfg, d, "w_k"), d.get("s_k", 1.0)) +
+           linear_backward(r["dV"], W(cfg, d, "w_v"), d.get("s_v", 1.0)) +
            r["gh_q"] @ f64(d["a_q"]) + r["gh_v"] @ f64(d["a_v"]))
     dx = rmsnorm_backward(d["x_in"], d["g_attn"], dn1, cfg.norm_eps) if cfg.pre_norm else dn1
     return r["dR1"] + dx if cfg.residual else dx

@@ -26,7 +26,8 @@ class LayerConfig:
     cache_len: int           # L: keys visible to the last query row
     n_layers: int = 1
     act: str = "relu2_mul"   # "relu2_mul" (ReLU^2 x Mul) or "silu_mul" (SwiGLU)
-    wtype: str = "f32"       # "f32", "bf16" or "ternary" (int8 {-1,0,1} + scale)
+    wtype: str = "f32"       # "f32", "bf16", "ternary" (int8 {-1,0,1} + scale) or "ternary2"
+                             # (the same values packed four 2-bit codes to a byte)
     sub_norm: bool = False   # RMSNorm after attention context and after the FFN hidden
     pre_norm: bool = False   # RMSNorm before the FFN (backward adds into the residual)
     residual: bool = True    # out = r1 + f and r1 = x + a

@@ -29,6 +29,8 @@ def to_dev(d: dict, wtype: str):
                 out[k] = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to("cuda").to(torch.bfloat16)
             elif wtype == "ternary":
                 out[k] = torch.from_numpy(np.ascontiguousarray(v, dtype=np.int8)).to("cuda")
+            elif wtype == "ternary2":
+                out[k] = torch.from_numpy(np.ascontiguousarray(v, dtype=np.uint8)).to("cuda")
             else:
                 out[k] = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to("cuda")
         else:

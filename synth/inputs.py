@@ -40,12 +40,24 @@ def _u(seed, cfg, layer, name, shape, lo, hi):
     return rng.uniform(rng.stream_key(seed, cfg.name, layer, name), n, lo, hi).reshape(shape)
 
 
+def pack_ternary2(w: np.ndarray) -> np.ndarray:
+    """Packed storage of a ternary [in, out] int8 matrix (out a multiple of 4): uint8 [in,
+    out / 4], weight 4k + i of a row in bits 2i, 2i + 1 of byte k, code 0 for 0, 1 for +1,
+    2 for -1."""
+    w = np.asarray(w)
+    assert w.shape[-1] % 4 == 0 and np.all(np.abs(w) <= 1)
+    code = np.where(w > 0, 1, np.where(w < 0, 2, 0)).astype(np.uint8)
+    c = code.reshape(w.shape[:-1] + (w.shape[-1] // 4, 4))
+    return (c[..., 0] | (c[..., 1] << 2) | (c[..., 2] << 4) | (c[..., 3] << 6)).astype(np.uint8)
+
+
 def _weight(seed, cfg, layer, name, shape):
     """Returns (stored array, scale)."""
-    if cfg.wtype == "ternary":
+    if cfg.wtype in ("ternary", "ternary2"):
         w = rng.ternary(rng.stream_key(seed, cfg.name, layer, name), int(np.prod(shape)))
         scale = float(np.float32(_u(seed, cfg, layer, name + ".scale", (1,), 0.5, 2.0)[0]))
-        return w.reshape(shape), scale
+        w = w.reshape(shape)
+        return (pack_ternary2(w) if cfg.wtype == "ternary2" else w), scale
     w = _n(seed, cfg, layer, name, shape, cfg.weight_std)
     if cfg.wtype == "bf16":
         return rng.round_to_bf16(w), 1.0

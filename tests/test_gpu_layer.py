@@ -66,7 +66,13 @@ MINI_SEQ_EXACT = MINI_SEQ.with_(name="mini_seq_exact", exact_din=True)
 SEQ_EXACT = SEQ_HD64.with_(name="seq_exact", exact_din=True)
 SEQ_EXACT_PN = SEQ_MHA.with_(name="seq_exact_prenorm_qknorm", exact_din=True, pre_norm=True, qk_norm=True)
 SEQ512_EXACT = SEQ512.with_(name="seq512_exact", exact_din=True)
-CASES = {c.name: c for c in (TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512, DEC_F32, DEC_BF16, DEC_G8, DEC_HD256,
+# packed 2-bit ternary weights ([FFN] BitLinear, four to a byte): the full single-token
+# layer, a small one with 8-head groups, and its exact input gradient
+DECODE_T2 = DECODE.with_(name="decode_t2", wtype="ternary2")
+DEC_T2 = DEC_G8.with_(name="dec_t2_g8", wtype="ternary2")
+DEC_T2_EXACT = DEC_T2.with_(name="dec_t2_exact", exact_din=True, pre_norm=True)
+CASES = {c.name: c for c in (DECODE_T2, DEC_T2, DEC_T2_EXACT,
+                             TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512, DEC_F32, DEC_BF16, DEC_G8, DEC_HD256,
                              SEQ_HD64, SEQ_CACHE, SEQ_MHA, SEQ_ODD, TINY_QK, DEC_QK, SEQ_QK, SEQ_PRENORM,
                              SEQ_NORESID, SEQ_NORMS, TINY_EXACT, TINY_EXACT_QK, DEC_EXACT, DECODE_EXACT,
                              MINI_SEQ_EXACT, SEQ_EXACT, SEQ_EXACT_PN, SEQ512_EXACT)}

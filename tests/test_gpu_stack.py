@@ -33,10 +33,11 @@ def device_stack(lib, cfg, layers, with_grads=False):
     return devs
 
 
-@pytest.mark.parametrize("n_layers", [1, 2, 4])
-def test_decode_stack_against_oracle(lib, n_layers):
+@pytest.mark.parametrize("n_layers,wtype", [(1, "ternary"), (2, "ternary"), (4, "ternary"), (2, "ternary2")])
+def test_decode_stack_against_oracle(lib, n_layers, wtype):
     import torch
-    cfg = DECODE.with_(name="decode_stack", n_layers=n_layers)
+    cfg = DECODE.with_(name="decode_stack" if wtype == "ternary" else "decode_stack_t2", n_layers=n_layers,
+                       wtype=wtype)
     layers = [layer_inputs(cfg, layer=l, seed=0, with_dout=(l == n_layers - 1)) for l in range(n_layers)]
     dout = layers[-1]["dout"]
     ref = OL.stack_backward(cfg, layers, dout)

@@ -228,6 +228,35 @@ def test_stack_backward_matches_finite_differences(case):
     assert np.max(np.abs(fwd["dA_v"] - res["layers"][1]["dA_v"])) > 1e-3 * np.max(np.abs(fwd["dA_v"])), case
 
 
+def test_packed_ternary_worked_bytes():
+    """The 2-bit storage read by its definition: byte 0x91 = 10 01 00 01 holds, from the
+    lowest bits up, codes 1, 0, 1, 2 = +1, 0, +1, -1; 0x55 is four +1, 0xAA four -1;
+    code 3 is refused."""
+    got = ops.unpack_ternary2(np.array([[0x91, 0x00, 0x55, 0xAA]], dtype=np.uint8))
+    assert got.tolist() == [[1, 0, 1, -1, 0, 0, 0, 0, 1, 1, 1, 1, -1, -1, -1, -1]]
+    with pytest.raises(ValueError):
+        ops.unpack_ternary2(np.array([[0x03]], dtype=np.uint8))
+
+
+def test_packed_ternary_round_trip_and_layer():
+    """The generator's packer and the oracle's unpacker are written apart: a round trip
+    gives the ternary values back, and a layer with packed weights is the int8 layer."""
+    from synth import DECODE, layer_inputs
+    from synth.inputs import pack_ternary2
+    w = np.random.default_rng(3).integers(-1, 2, size=(7, 64)).astype(np.int8)
+    np.testing.assert_array_equal(ops.unpack_ternary2(pack_ternary2(w)), w)
+    cfg = DECODE.with_(name="t2pin", dim=64, ffn_dim=128, n_heads=4, n_kv_heads=2, head_dim=16, rank=2,
+                       lora_alpha=4.0, cache_len=9)
+    d = layer_inputs(cfg)
+    d2 = dict(d)
+    for k in ("w_down", "w_gate", "w_up", "w_o"):
+        d2[k] = pack_ternary2(d[k])
+    a = Lyr.layer_backward(cfg, d, d["dout"])
+    b = Lyr.layer_backward(cfg.with_(wtype="ternary2"), d2, d["dout"])
+    for k in ("d_in", "dA_q", "dB_q", "dA_v", "dB_v"):
+        np.testing.assert_array_equal(a[k], b[k])
+
+
 def test_linear_backward_is_the_adjoint():
     rs = np.random.default_rng(2)
     x, w, dy = rs.normal(size=(5, 7)), rs.normal(size=(7, 3)), rs.normal(size=(5, 3))

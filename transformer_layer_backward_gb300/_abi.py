@@ -12,7 +12,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libt
 
 TLB_OK, TLB_EINVAL, TLB_EUNSUPPORTED, TLB_ENONFINITE, TLB_ETIMEOUT, TLB_ECUDA = 0, -1, -2, -3, -4, -5
 ACT_RELU2_MUL, ACT_SILU_MUL = 0, 1
-W_F32, W_BF16, W_TERNARY_I8 = 0, 1, 2
+W_F32, W_BF16, W_TERNARY_I8, W_TERNARY_2B = 0, 1, 2, 3
 SUB_NORM, PRE_NORM, RESIDUAL, ROPE, USE_SILU_CACHE, CAUSAL, PERSISTENT, QK_NORM = 1, 2, 4, 8, 16, 32, 64, 128
 CHECK_FINITE, EXACT_DIN = 256, 512
 

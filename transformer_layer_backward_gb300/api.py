@@ -13,7 +13,9 @@ import torch
 
 from . import _abi as A
 
-_WDTYPE = {A.W_F32: torch.float32, A.W_BF16: torch.bfloat16, A.W_TERNARY_I8: torch.int8}
+_WDTYPE = {A.W_F32: torch.float32, A.W_BF16: torch.bfloat16, A.W_TERNARY_I8: torch.int8,
+           A.W_TERNARY_2B: torch.uint8}
+_WCODE = {"f32": A.W_F32, "bf16": A.W_BF16, "ternary": A.W_TERNARY_I8, "ternary2": A.W_TERNARY_2B}
 
 
 def _stream(stream):
@@ -78,15 +80,18 @@ def rope_backward(dy, pos0, base=10000.0, out=None, stream=None):
 
 
 def linear_workspace(wtype, S, out_dim, in_dim, device="cuda"):
-    code = {"f32": A.W_F32, "bf16": A.W_BF16, "ternary": A.W_TERNARY_I8}[wtype]
+    code = _WCODE[wtype]
     n = int(A.load().tlb_linear_workspace_bytes(code, int(S), int(out_dim), int(in_dim)))
     return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
 
 
 def linear_backward(wtype, W, dY, scale=1.0, out=None, accumulate=False, ws=None, stream=None):
-    """dX = scale * dY @ W^T for W stored [in, out] (wtype 'f32', 'bf16' or 'ternary')."""
-    code = {"f32": A.W_F32, "bf16": A.W_BF16, "ternary": A.W_TERNARY_I8}[wtype]
+    """dX = scale * dY @ W^T for W stored [in, out] (wtype 'f32', 'bf16', 'ternary', or
+    'ternary2': uint8 [in, out / 4], four 2-bit codes per byte)."""
+    code = _WCODE[wtype]
     in_dim, out_dim = W.shape
+    if code == A.W_TERNARY_2B:
+        out_dim *= 4
     S = dY.shape[0]
     out = torch.zeros(S, in_dim, device=dY.device) if out is None else out
     ws = linear_workspace(wtype, S, out_dim, in_dim, dY.device) if ws is None else ws
@@ -154,7 +159,7 @@ def layer_cfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, lora_alpha, act
                       float(rope_base), float(norm_eps),
                       float(1.0 / math.sqrt(head_dim) if attn_scale is None else attn_scale),
                       {"relu2_mul": A.ACT_RELU2_MUL, "silu_mul": A.ACT_SILU_MUL}[act],
-                      {"f32": A.W_F32, "bf16": A.W_BF16, "ternary": A.W_TERNARY_I8}[wtype], flags)
+                      _WCODE[wtype], flags)
 
 
 def layer_cfg_of(c, persistent=False, check_finite=False) -> A.LayerCfg:

@@ -148,8 +148,10 @@ int tlb_linear_backward(int32_t wtype, const void *W, float scale, const float *
                         int64_t out_dim, int64_t in_dim, float *dX, int32_t accumulate, void *ws,
                         size_t ws_bytes, void *stream) {
     clear_error();
-    TLB_REQUIRE(wtype == TLB_W_F32 || wtype == TLB_W_BF16 || wtype == TLB_W_TERNARY_I8, TLB_EINVAL,
-                "linear_backward: unknown weight type %d", wtype);
+    TLB_REQUIRE(wtype == TLB_W_F32 || wtype == TLB_W_BF16 || wtype == TLB_W_TERNARY_I8 || wtype == TLB_W_TERNARY_2B,
+                TLB_EINVAL, "linear_backward: unknown weight type %d", wtype);
+    TLB_REQUIRE(wtype != TLB_W_TERNARY_2B || out_dim % 4 == 0, TLB_EINVAL,
+                "linear_backward: packed ternary rows need out_dim %% 4 == 0");
     TLB_REQUIRE(S >= 0 && out_dim >= 0 && in_dim >= 0, TLB_EINVAL, "linear_backward: negative size");
     if (S == 0 || in_dim == 0) return TLB_OK;
     TLB_REQUIRE(W && dX && (dY || out_dim == 0), TLB_EINVAL, "linear_backward: null pointer");

@@ -391,15 +391,16 @@ __global__ void attn_dk_rows_kernel(AttnArgs a, const float *__restrict__ q, con
 }
 
 // S > 1, head_dim 32 / 64 / 128: block = (64 new keys, KV head), 256 threads.  For every
-// head of the group and query tile: T = dCtx V^T on the tile (4 x 4 per thread), dS = P (T
-// - D) in shared memory, then dK += dS^T q (4 keys x HD/16 columns per thread).
+// head of the group and query tile: T = dCtx V^T on the tile (4 x 4 per thread, from
+// transposed tiles so that each step is two 16-byte shared loads), dS = P (T - D) in
+// shared memory, then dK += dS^T q (4 keys x HD/16 columns per thread).
 template <int HD>
 __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__restrict__ q,
                                                      const float *__restrict__ Dv, float *dk) {
     extern __shared__ float4 sm4[];
-    float *sV = reinterpret_cast<float *>(sm4);         // [kT][HD+4]  V rows of the key tile
-    float *sC = sV + kT * (HD + 4);                     // [kT][HD+4]  dCtx tile [query][d]
-    float *sQ = sC + kT * (HD + 4);                     // [kT][HD+4]  q tile [query][d]
+    float *sVt = reinterpret_cast<float *>(sm4);        // [HD][kTP]   V rows of the key tile, transposed
+    float *sCt = sVt + HD * kTP;                        // [HD][kTP]   dCtx tile, transposed
+    float *sQ = sCt + HD * kTP;                         // [kT][HD+4]  q tile [query][d]
     float *sS = sQ + kT * (HD + 4);                     // [kT][kTP]   dS tile [query][key]
     __shared__ float sDq[kT];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__
     constexpr int CPT = HD / 16;
     for (int e = tid; e < kT * HD; e += 256) {
         const int j = e / HD, d = e % HD;
-        sV[j * (HD + 4) + d] =
+        sVt[d * kTP + j] =
             (k0 + j < a.S) ? a.v[int64_t(kvh) * a.sh + int64_t(a.pos0 + k0 + j) * a.sp + d] : 0.f;
     }
     float acc[4][CPT];
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__
             for (int e = tid; e < kT * HD; e += 256) {
                 const int i = e / HD, d = e % HD;
                 const bool in = q0 + i < a.S;
-                sC[i * (HD + 4) + d] = in ? a.dctx[int64_t(q0 + i) * q_dim + h * HD + d] : 0.f;
+                sCt[d * kTP + i] = in ? a.dctx[int64_t(q0 + i) * q_dim + h * HD + d] : 0.f;
                 sQ[i * (HD + 4) + d] = in ? q[int64_t(q0 + i) * q_dim + h * HD + d] : 0.f;
             }
             if (tid < kT) sDq[tid] = q0 + tid < a.S ? Dv[int64_t(h) * a.S + q0 + tid] : 0.f;
@@ -439,17 +440,15 @@ __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__
             for (int r = 0; r < 4; ++r)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) t[r][c] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
             for (int d = 0; d < HD; ++d) {
-                float cq[4], vk[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) cq[r] = sC[(4 * ty + r) * (HD + 4) + d];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) vk[c] = sV[(4 * tx + c) * (HD + 4) + d];
+                const float4 cq = *reinterpret_cast<const float4 *>(sCt + d * kTP + 4 * ty);
+                const float4 vk = *reinterpret_cast<const float4 *>(sVt + d * kTP + 4 * tx);
+                const float cr[4] = {cq.x, cq.y, cq.z, cq.w}, vc[4] = {vk.x, vk.y, vk.z, vk.w};
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) t[r][c] = fmaf(cq[r], vk[c], t[r][c]);
+                    for (int c = 0; c < 4; ++c) t[r][c] = fmaf(cr[r], vc[c], t[r][c]);
             }
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -492,7 +491,7 @@ __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__
 
 template <int HD>
 int launch_dk_tiled(const AttnArgs &a, const float *q, const float *D, float *dk, cudaStream_t st) {
-    const size_t sm = (size_t(3) * kT * (HD + 4) + size_t(kT) * kTP) * 4;
+    const size_t sm = (size_t(2) * HD * kTP + size_t(kT) * (HD + 4) + size_t(kT) * kTP) * 4;
     if (sm > 48 * 1024) TLB_CUDA(cudaFuncSetAttribute(attn_dk_tiled<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)));
     attn_dk_tiled<HD><<<dim3(unsigned(ceil_div(a.S, kT)), unsigned(a.nkv)), 256, sm, st>>>(a, q, D, dk);
     return check_launch("attn_dk_tiled");

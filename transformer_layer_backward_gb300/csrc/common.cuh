@@ -177,9 +177,26 @@ __device__ __forceinline__ float weight_at(const void *w, int64_t idx) {
     } else if constexpr (WT == TLB_W_BF16) {
         unsigned short b = __ldg(reinterpret_cast<const unsigned short *>(w) + idx);
         return __uint_as_float(uint32_t(b) << 16);
-    } else {
+    } else if constexpr (WT == TLB_W_TERNARY_I8) {
         return float(__ldg(reinterpret_cast<const signed char *>(w) + idx));
+    } else {
+        const uint32_t b = __ldg(reinterpret_cast<const unsigned char *>(w) + (idx >> 2));
+        const uint32_t c = (b >> (2 * uint32_t(idx & 3))) & 3u;
+        return c == 1u ? 1.f : (c == 2u ? -1.f : 0.f);
     }
+}
+
+// sum_i w_i x_i over the four 2-bit ternary codes of byte b (lowest bits first; 0: 0,
+// 1: +1, 2: -1, 3: read as 0) and the four floats of x.
+__device__ __forceinline__ float t2_dot4(uint32_t b, float4 x) {
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t c = (b >> (2 * i)) & 3u;
+        s += c == 1u ? xs[i] : (c == 2u ? -xs[i] : 0.f);
+    }
+    return s;
 }
 
 // cos and sin of theta = pos * f with f = f_hi + f_lo (a float pair carrying the

@@ -53,7 +53,7 @@ __device__ __forceinline__ void warp_rows(const char *const *W, const float *sca
     constexpr int P = E / 4;
     const int lane = threadIdx.x & 31;
     const int nch = cols / E;
-    if (row_bytes == 0) row_bytes = size_t(cols) * (16 / E);
+    if (row_bytes == 0) row_bytes = wbytes<WT>(size_t(cols));
     float acc[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) acc[r] = 0.f;
@@ -74,6 +74,28 @@ __device__ __forceinline__ void warp_rows(const char *const *W, const float *sca
         for (int u = 0; u < U; ++u) {
             const int ch = base + u * 32 + lane;
             if (ch >= nch) break;
+            if constexpr (WT == TLB_W_TERNARY_2B) {
+                // 64 packed weights per chunk: byte k of the chunk against float4 unit k
+#pragma unroll
+                for (int m = 0; m < NM; ++m) {
+                    float part[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) part[r] = 0.f;
+#pragma unroll
+                    for (int k = 0; k < P; ++k) {
+                        const float4 t = reinterpret_cast<const float4 *>(xs[m])[xunit<WT>(ch * P + k)];
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint4 &q = w[m][r][u];
+                            const uint32_t word = k < 4 ? q.x : (k < 8 ? q.y : (k < 12 ? q.z : q.w));
+                            part[r] += t2_dot4((word >> (8 * (k & 3))) & 0xFFu, t);
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < R; ++r) acc[r] = fmaf(scale[m], part[r], acc[r]);
+                }
+                continue;
+            }
 #pragma unroll
             for (int m = 0; m < NM; ++m) {
                 float xv[E];
@@ -167,11 +189,10 @@ __global__ void __launch_bounds__(kThreads) dec_k1(DecodeArgs a) {
     float *sx = reinterpret_cast<float *>(sm4);
     {
         // this block's W_down rows, which depend on nothing before it, go to L2 first
-        constexpr int ES = 16 / EPC<WT>::v;
         const int rows = kWarps * kR, r0 = blockIdx.x * rows;
         if (threadIdx.x == 0 && r0 < a.I)
-            prefetch_l2(static_cast<const char *>(a.w_down) + size_t(r0) * a.H * ES,
-                        size_t(min(rows, a.I - r0)) * a.H * ES);
+            prefetch_l2(static_cast<const char *>(a.w_down) + wbytes<WT>(size_t(r0) * a.H),
+                        wbytes<WT>(size_t(min(rows, a.I - r0)) * a.H));
     }
     pdl_trigger();
     pdl_wait();
@@ -201,11 +222,10 @@ __global__ void __launch_bounds__(kThreads) dec_k2(DecodeArgs a) {
     float *sG = reinterpret_cast<float *>(sm4);
     float *sU = sG + nc;
     {
-        constexpr int ES = 16 / EPC<WT>::v;
         const int lane = threadIdx.x & 31, r = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR + (lane % kR);
         if (lane < 2 * kR && r < a.H)
             prefetch_l2(reinterpret_cast<const char *>(lane < kR ? a.w_gate : a.w_up) +
-                            (size_t(r) * a.I + c0) * ES, size_t(nc) * ES);
+                            wbytes<WT>(size_t(r) * a.I + c0), wbytes<WT>(size_t(nc)));
     }
     pdl_trigger();
     pdl_wait();
@@ -270,14 +290,13 @@ __global__ void __launch_bounds__(kThreads) dec_k2(DecodeArgs a) {
         }
     }
     __syncthreads();
-    constexpr int ES = 16 / EPC<WT>::v;
-    const char *W[2] = {reinterpret_cast<const char *>(a.w_gate) + size_t(c0) * ES,
-                        reinterpret_cast<const char *>(a.w_up) + size_t(c0) * ES};
+    const char *W[2] = {reinterpret_cast<const char *>(a.w_gate) + wbytes<WT>(size_t(c0)),
+                        reinterpret_cast<const char *>(a.w_up) + wbytes<WT>(size_t(c0))};
     const float sc[2] = {a.s_gate, a.s_up};
     const float *xs[2] = {sG, sU};
     const int r0 = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR;
     float vals[kR] = {};
-    if (r0 < a.H) warp_rows<WT, 2, kR, kU, true>(W, sc, xs, r0, a.H, nc, a.dN2, vals, size_t(a.I) * ES);
+    if (r0 < a.H) warp_rows<WT, 2, kR, kU, true>(W, sc, xs, r0, a.H, nc, a.dN2, vals, wbytes<WT>(size_t(a.I)));
 }
 
 // ------------------------------------------------------------------ k3: dR1, dSub = s_o W_O dR1
@@ -313,10 +332,9 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
     }
     {   // this block's W_O rows into L2, after the staging loads above (so they do not queue
         // behind this prefetch while the previous kernel still streams its weights)
-        constexpr int ES = 16 / EPC<WT>::v;
         const int lane = threadIdx.x & 31, r = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR + lane;
         if (lane < kR && r < a.qd)
-            prefetch_l2(reinterpret_cast<const char *>(a.w_o) + (size_t(r) * a.H + c0) * ES, size_t(nc) * ES);
+            prefetch_l2(reinterpret_cast<const char *>(a.w_o) + wbytes<WT>(size_t(r) * a.H + c0), wbytes<WT>(size_t(nc)));
     }
     pdl_wait();
     // After the wait: dN2 (one round of loads), the pre-norm coefficients, dR1 over the range.
@@ -355,13 +373,12 @@ __global__ void __launch_bounds__(kThreads) dec_k3(DecodeArgs a) {
         if (blockIdx.x == 0) reinterpret_cast<float4 *>(a.dR1 + c0)[i] = v;
     }
     __syncthreads();
-    constexpr int ES = 16 / EPC<WT>::v;
-    const char *W[1] = {reinterpret_cast<const char *>(a.w_o) + size_t(c0) * ES};
+    const char *W[1] = {reinterpret_cast<const char *>(a.w_o) + wbytes<WT>(size_t(c0))};
     const float sc[1] = {a.s_o};
     const float *xs[1] = {sR};
     const int r0 = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kR;
     float vals[kR] = {};
-    if (r0 < a.qd) warp_rows<WT, 1, kR, kU, true>(W, sc, xs, r0, a.qd, nc, a.dSub, vals, size_t(a.H) * ES);
+    if (r0 < a.qd) warp_rows<WT, 1, kR, kU, true>(W, sc, xs, r0, a.qd, nc, a.dSub, vals, wbytes<WT>(size_t(a.H)));
 }
 
 // ------------------------------------------------------------------ k4: attention, one pass over K and V
@@ -853,7 +870,7 @@ int decode_rows_per_block() { return kWarps * kR; }
 
 bool decode_supported(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     const int G = c.n_heads / c.n_kv_heads;
-    const int E = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 8 : 16);
+    const int E = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 8 : (c.wtype == TLB_W_TERNARY_I8 ? 16 : 64));
     const int hd = c.head_dim;
     const int gmax = hd > 128 ? 8 : 16;   // heads per KV group held in registers by k4
     const size_t sm4 = (size_t(G) * hd + size_t(kAWarps) * G * 2 * hd + size_t(c.n_heads) * hd) * 4;
@@ -866,6 +883,7 @@ int decode_ffn_launch(const DecodeArgs &a, int wtype, cudaStream_t st, bool k1_p
     switch (wtype) {
         case TLB_W_F32: return launch_ffn<TLB_W_F32>(a, st, k1_pdl);
         case TLB_W_BF16: return launch_ffn<TLB_W_BF16>(a, st, k1_pdl);
+        case TLB_W_TERNARY_2B: return launch_ffn<TLB_W_TERNARY_2B>(a, st, k1_pdl);
         default: return launch_ffn<TLB_W_TERNARY_I8>(a, st, k1_pdl);
     }
 }

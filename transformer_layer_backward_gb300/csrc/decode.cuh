@@ -34,8 +34,14 @@ struct DecodeArgs {
 // Weight elements per 16-byte chunk of a row.
 template <int WT>
 struct EPC {
-    static constexpr int v = WT == TLB_W_F32 ? 4 : (WT == TLB_W_BF16 ? 8 : 16);
+    static constexpr int v = WT == TLB_W_F32 ? 4 : (WT == TLB_W_BF16 ? 8 : (WT == TLB_W_TERNARY_I8 ? 16 : 64));
 };
+
+// Bytes of n weights of a row (n a multiple of 4 for the packed ternary type).
+template <int WT>
+__host__ __device__ constexpr size_t wbytes(size_t n) {
+    return n * 16 / EPC<WT>::v;
+}
 
 template <int WT>
 __device__ __forceinline__ float chunk_dot(uint4 w, const float *x) {
@@ -73,9 +79,12 @@ __device__ __forceinline__ int xunit(int u) {
     constexpr int P = EPC<WT>::v / 4;
     if constexpr (P == 1) {
         return u;
-    } else {
+    } else if constexpr (P < 8) {
         const int ch = u / P, k = u % P;
         return ch * P + (k ^ ((ch / (8 / P)) % P));
+    } else {
+        const int ch = u / P, k = u % P;     // a chunk spans the 8 bank groups twice or more
+        return ch * P + (k ^ (ch & 7));
     }
 }
 

@@ -790,6 +790,7 @@ bool persistent_supported(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     const int hd = c.head_dim, G = c.n_heads / c.n_kv_heads;
     const int E = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 8 : 16);
     if (S != 1 || L < 1 || c.rank > 16 || c.n_heads > kPT || (c.flags & TLB_QK_NORM)) return false;
+    if (c.wtype == TLB_W_TERNARY_2B) return false;    // packed weights take the multi-kernel chain
     if (!(hd == 32 || hd == 64 || hd == 128 || hd == 256) || G * (hd / 32) > 16) return false;
     if (c.dim % E || c.ffn_dim % E || c.dim % 4 || c.ffn_dim % 4) return false;
     if (ceil_div(c.dim, std::min(num_sms(), kMaxPersistentBlocks)) + 1 > kMaxBlockRows) return false;

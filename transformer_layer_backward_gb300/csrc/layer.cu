@@ -107,8 +107,12 @@ int validate_cfg(const tlb_layer_cfg *c) {
     TLB_REQUIRE(c->rank >= 1 && c->rank <= 64, TLB_EINVAL, "layer cfg: rank must be in 1..64");
     TLB_REQUIRE(c->act == TLB_ACT_RELU2_MUL || c->act == TLB_ACT_SILU_MUL, TLB_EINVAL,
                 "layer cfg: unknown activation %d", c->act);
-    TLB_REQUIRE(c->wtype == TLB_W_F32 || c->wtype == TLB_W_BF16 || c->wtype == TLB_W_TERNARY_I8, TLB_EINVAL,
-                "layer cfg: unknown weight type %d", c->wtype);
+    TLB_REQUIRE(c->wtype == TLB_W_F32 || c->wtype == TLB_W_BF16 || c->wtype == TLB_W_TERNARY_I8 ||
+                    c->wtype == TLB_W_TERNARY_2B, TLB_EINVAL, "layer cfg: unknown weight type %d", c->wtype);
+    if (c->wtype == TLB_W_TERNARY_2B)   // every weight row (out weights) a whole number of bytes
+        TLB_REQUIRE(c->dim % 4 == 0 && c->ffn_dim % 4 == 0 && (c->n_heads * c->head_dim) % 4 == 0 &&
+                        (c->n_kv_heads * c->head_dim) % 4 == 0,
+                    TLB_EINVAL, "layer cfg: packed ternary weights need dim, ffn_dim, q_dim, kv_dim % 4 == 0");
     return TLB_OK;
 }
 
@@ -457,7 +461,7 @@ void decode_args(const tlb_layer_cfg &c, int64_t L, const tlb_layer_weights *w, 
     // column ranges: more blocks in flight for the two GEMVs with few rows (whole 16-byte
     // weight chunks per range, ranges a multiple of 4 floats), as long as k2 stays one
     // wave of three blocks per SM
-    const int E = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 8 : 16);
+    const int E = c.wtype == TLB_W_F32 ? 4 : (c.wtype == TLB_W_BF16 ? 8 : (c.wtype == TLB_W_TERNARY_I8 ? 16 : 64));
     d.ns2 = 1;
     for (int n : {4, 2})
         if (c.ffn_dim % (n * E) == 0 && (c.ffn_dim / n) % 4 == 0 && int64_t(d.n2) * n <= 3 * num_sms()) {

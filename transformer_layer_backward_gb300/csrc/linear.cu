@@ -21,6 +21,7 @@ struct Elem;
 template <> struct Elem<TLB_W_F32> { static constexpr int size = 4; };
 template <> struct Elem<TLB_W_BF16> { static constexpr int size = 2; };
 template <> struct Elem<TLB_W_TERNARY_I8> { static constexpr int size = 1; };
+template <> struct Elem<TLB_W_TERNARY_2B> { static constexpr int size = 0; };   // four weights per byte
 
 // Dot product of one 16-byte chunk of a weight row with EPC floats of x.
 template <int WT>
@@ -115,13 +116,20 @@ static int launch_gemv(const void *W, const float *x, float *y, int rows, int co
     constexpr int R = 4;
     const size_t row_bytes = size_t(cols) * Elem<WT>::size;
     const size_t smem = size_t(cols) * sizeof(float);
-    if (row_bytes % 16 == 0 && aligned16(W) && smem <= 200 * 1024) {
-        if (smem > 48 * 1024)
-            TLB_CUDA(cudaFuncSetAttribute(gemv_rows_kernel<WT, R>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-        const int grid = int(ceil_div(rows, kGemvWarps * R));
-        gemv_rows_kernel<WT, R><<<grid, kGemvWarps * 32, smem, st>>>(W, x, y, rows, cols, scale, accumulate);
-    } else {
+    // packed ternary rows: the decode chain's streaming kernels serve S = 1 layers; this
+    // standalone product reads them one weight at a time
+    bool chunked = false;
+    if constexpr (Elem<WT>::size > 0) {
+        if (row_bytes % 16 == 0 && aligned16(W) && smem <= 200 * 1024) {
+            if (smem > 48 * 1024)
+                TLB_CUDA(cudaFuncSetAttribute(gemv_rows_kernel<WT, R>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+            const int grid = int(ceil_div(rows, kGemvWarps * R));
+            gemv_rows_kernel<WT, R><<<grid, kGemvWarps * 32, smem, st>>>(W, x, y, rows, cols, scale, accumulate);
+            chunked = true;
+        }
+    }
+    if (!chunked) {
         gemv_rows_generic_kernel<WT><<<unsigned(ceil_div(rows, 8)), 256, 0, st>>>(W, x, y, rows, cols,
                                                                                scale, accumulate);
     }
@@ -204,6 +212,8 @@ int linear_t_launch(int wtype, const void *W, float scale, const float *dY, int6
         switch (wtype) {
             case TLB_W_F32: return launch_gemv<TLB_W_F32>(W, dY, dX, int(in_dim), int(out_dim), scale, acc, st);
             case TLB_W_BF16: return launch_gemv<TLB_W_BF16>(W, dY, dX, int(in_dim), int(out_dim), scale, acc, st);
+            case TLB_W_TERNARY_2B:
+                return launch_gemv<TLB_W_TERNARY_2B>(W, dY, dX, int(in_dim), int(out_dim), scale, acc, st);
             default: return launch_gemv<TLB_W_TERNARY_I8>(W, dY, dX, int(in_dim), int(out_dim), scale, acc, st);
         }
     }
@@ -221,6 +231,9 @@ int linear_t_launch(int wtype, const void *W, float scale, const float *dY, int6
             return launch_gemm_simt<TLB_W_F32>(dY, W, dX, int(S), int(in_dim), int(out_dim), scale, acc, st);
         case TLB_W_BF16:
             return launch_gemm_simt<TLB_W_BF16>(dY, W, dX, int(S), int(in_dim), int(out_dim), scale, acc, st);
+        case TLB_W_TERNARY_2B:
+            return launch_gemm_simt<TLB_W_TERNARY_2B>(dY, W, dX, int(S), int(in_dim), int(out_dim), scale, acc,
+                                                      st);
         default:
             return launch_gemm_simt<TLB_W_TERNARY_I8>(dY, W, dX, int(S), int(in_dim), int(out_dim), scale,
                                                       acc, st);

@@ -816,7 +816,9 @@ __global__ void __launch_bounds__(256) lora_din_kernel(LoraDinArgs a) {
                 for (int row = 0; row < kDinRows; ++row) acc[row] = fmaf(sgh[row * per + t * a.rank + r], av, acc[row]);
             }
         }
-        for (int row = 0; row < nrows; ++row) a.dn1[int64_t(r0 + row) * a.C + c] += acc[row];
+#pragma unroll
+        for (int row = 0; row < kDinRows; ++row)      // constant bound: acc stays in registers
+            if (row < nrows) a.dn1[int64_t(r0 + row) * a.C + c] += acc[row];
     }
 }
 
