@@ -61,8 +61,8 @@ extern "C" {
 #define TLB_W_TERNARY_I8 2     /* int8 in {-1, 0, +1}; the per-tensor float scale multiplies */
 #define TLB_W_TERNARY_2B 3     /* ternary packed four to a byte ([FFN] BitLinear weights): a row of
                                   `out` weights is out / 4 bytes; weight 4k + i of the row sits in
-                                  bits 2i, 2i + 1 of byte k, code 0 = 0, 1 = +1, 2 = -1 (3 is not
-                                  a valid code and reads as 0).  out must be a multiple of 4; the
+                                  bits 2i, 2i + 1 of byte k as code q = w + 1 (0: -1, 1: 0, 2: +1;
+                                  3 is not a valid code).  out must be a multiple of 4; the
                                   per-tensor float scale multiplies.  S = 1 runs the streaming
                                   GEMVs (row lengths multiples of 64 weights), S > 1 the CUDA-core
                                   GEMM */

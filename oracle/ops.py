@@ -22,14 +22,14 @@ def f64(a) -> np.ndarray:
 
 def unpack_ternary2(packed) -> np.ndarray:
     """Ternary weights [in, out] from their packed storage [in, out / 4] (uint8): four
-    2-bit codes per byte along the row, the first weight in the lowest two bits; code 0
-    is 0, 1 is +1, 2 is -1 (the BitLinear weight of [FFN], stored four to a byte).
-    Code 3 is not a ternary value and is refused."""
+    2-bit codes per byte along the row, the first weight in the lowest two bits; a code
+    is the weight plus one (0 is -1, 1 is 0, 2 is +1: the BitLinear weight of [FFN],
+    stored four to a byte).  Code 3 is not a ternary value and is refused."""
     b = np.asarray(packed, dtype=np.uint8)
     codes = np.stack([(b >> (2 * i)) & 3 for i in range(4)], axis=-1)      # [..., out/4, 4]
     if np.any(codes == 3):
         raise ValueError("code 3 in packed ternary weights")
-    value = np.array([0.0, 1.0, -1.0, 0.0])
+    value = np.array([-1.0, 0.0, 1.0])
     return value[codes].reshape(b.shape[:-1] + (b.shape[-1] * 4,))
 
 

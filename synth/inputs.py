@@ -42,11 +42,10 @@ def _u(seed, cfg, layer, name, shape, lo, hi):
 
 def pack_ternary2(w: np.ndarray) -> np.ndarray:
     """Packed storage of a ternary [in, out] int8 matrix (out a multiple of 4): uint8 [in,
-    out / 4], weight 4k + i of a row in bits 2i, 2i + 1 of byte k, code 0 for 0, 1 for +1,
-    2 for -1."""
+    out / 4], weight 4k + i of a row in bits 2i, 2i + 1 of byte k as the code w + 1."""
     w = np.asarray(w)
     assert w.shape[-1] % 4 == 0 and np.all(np.abs(w) <= 1)
-    code = np.where(w > 0, 1, np.where(w < 0, 2, 0)).astype(np.uint8)
+    code = (w.astype(np.int16) + 1).astype(np.uint8)
     c = code.reshape(w.shape[:-1] + (w.shape[-1] // 4, 4))
     return (c[..., 0] | (c[..., 1] << 2) | (c[..., 2] << 4) | (c[..., 3] << 6)).astype(np.uint8)
 

@@ -229,11 +229,11 @@ def test_stack_backward_matches_finite_differences(case):
 
 
 def test_packed_ternary_worked_bytes():
-    """The 2-bit storage read by its definition: byte 0x91 = 10 01 00 01 holds, from the
-    lowest bits up, codes 1, 0, 1, 2 = +1, 0, +1, -1; 0x55 is four +1, 0xAA four -1;
-    code 3 is refused."""
+    """The 2-bit storage read by its definition (code = weight + 1): byte 0x91 = 10 01 00
+    01 holds, from the lowest bits up, codes 1, 0, 1, 2 = 0, -1, 0, +1; 0x55 is four 0,
+    0xAA four +1, 0x00 four -1; code 3 is refused."""
     got = ops.unpack_ternary2(np.array([[0x91, 0x00, 0x55, 0xAA]], dtype=np.uint8))
-    assert got.tolist() == [[1, 0, 1, -1, 0, 0, 0, 0, 1, 1, 1, 1, -1, -1, -1, -1]]
+    assert got.tolist() == [[0, -1, 0, 1, -1, -1, -1, -1, 0, 0, 0, 0, 1, 1, 1, 1]]
     with pytest.raises(ValueError):
         ops.unpack_ternary2(np.array([[0x03]], dtype=np.uint8))
 

@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__
     float *sS = sQ + kT * (HD + 4);                     // [kT][kTP]   dS tile [query][key]
     __shared__ float sDq[kT];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    const int kvh = blockIdx.y, G = a.nh / a.nkv;
+    const int kvh = blockIdx.y, G = a.nh / a.nkv, g = blockIdx.z;   // one head of the group per block
     const int k0 = blockIdx.x * kT;                     // among the S newest keys
     const int q_dim = a.nh * HD;
     constexpr int CPT = HD / 16;
@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__
         for (int c = 0; c < CPT; ++c) acc[r][c] = 0.f;
     const int qt0 = a.causal ? k0 / kT : 0;
     const int nqt = (a.S + kT - 1) / kT;
-    for (int g = 0; g < G; ++g) {
+    {
         const int h = kvh * G + g;
         const float *Ph = a.attn + int64_t(h) * a.S * a.L + a.pos0;
         for (int qt = qt0; qt < nqt; ++qt) {
@@ -480,29 +480,50 @@ __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__
             }
         }
     }
+    // this head's share: dk holds [G][S, kv_dim] partials, added in head order afterwards
+    float *out = dk + int64_t(g) * a.S * a.nkv * HD;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int jj = k0 + 4 * ty + r;
         if (jj >= a.S) continue;
 #pragma unroll
-        for (int c = 0; c < CPT; ++c) dk[int64_t(jj) * a.nkv * HD + kvh * HD + tx * CPT + c] = a.scale * acc[r][c];
+        for (int c = 0; c < CPT; ++c) out[int64_t(jj) * a.nkv * HD + kvh * HD + tx * CPT + c] = a.scale * acc[r][c];
+    }
+}
+
+// dk[e] = sum over the group's heads g (in order) of part[g][e]
+__global__ void attn_dk_sum_kernel(const float *__restrict__ part, float *dk, int64_t n, int G) {
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += int64_t(gridDim.x) * blockDim.x) {
+        float s = part[e];
+        for (int g = 1; g < G; ++g) s += part[int64_t(g) * n + e];
+        dk[e] = s;
     }
 }
 
 template <int HD>
-int launch_dk_tiled(const AttnArgs &a, const float *q, const float *D, float *dk, cudaStream_t st) {
+int launch_dk_tiled(const AttnArgs &a, const float *q, const float *D, float *dk, float *part, cudaStream_t st) {
+    const int G = a.nh / a.nkv;
     const size_t sm = (size_t(2) * HD * kTP + size_t(kT) * (HD + 4) + size_t(kT) * kTP) * 4;
     if (sm > 48 * 1024) TLB_CUDA(cudaFuncSetAttribute(attn_dk_tiled<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)));
-    attn_dk_tiled<HD><<<dim3(unsigned(ceil_div(a.S, kT)), unsigned(a.nkv)), 256, sm, st>>>(a, q, D, dk);
-    return check_launch("attn_dk_tiled");
+    float *dst = G > 1 ? part : dk;
+    attn_dk_tiled<HD><<<dim3(unsigned(ceil_div(a.S, kT)), unsigned(a.nkv), unsigned(G)), 256, sm, st>>>(a, q, D, dst);
+    TLB_TRY(check_launch("attn_dk_tiled"));
+    if (G == 1) return TLB_OK;
+    const int64_t n = int64_t(a.S) * a.nkv * HD;
+    attn_dk_sum_kernel<<<stream_grid(n, 256), 256, 0, st>>>(part, dk, n, G);
+    return check_launch("attn_dk_sum");
 }
 
-int attn_dk_launch(const AttnArgs &a, const float *q, const float *D, float *dk, cudaStream_t st) {
+size_t attn_dk_bytes(int64_t S, int nh, int nkv, int hd) {
+    return nh > nkv ? size_t(nh) * S * hd * 4 : 0;     // per-head partials of the tiled kernel
+}
+
+int attn_dk_launch(const AttnArgs &a, const float *q, const float *D, float *dk, float *part, cudaStream_t st) {
     if (a.S == 0) return TLB_OK;
     if (a.S > 1) {
-        if (a.hd == 128) return launch_dk_tiled<128>(a, q, D, dk, st);
-        if (a.hd == 64) return launch_dk_tiled<64>(a, q, D, dk, st);
-        if (a.hd == 32) return launch_dk_tiled<32>(a, q, D, dk, st);
+        if (a.hd == 128) return launch_dk_tiled<128>(a, q, D, dk, part, st);
+        if (a.hd == 64) return launch_dk_tiled<64>(a, q, D, dk, part, st);
+        if (a.hd == 32) return launch_dk_tiled<32>(a, q, D, dk, part, st);
     }
     const int threads = 128;
     attn_dk_rows_kernel<<<dim3(unsigned(a.S), unsigned(a.nkv)), threads, (size_t(a.hd) + threads) * 4, st>>>(

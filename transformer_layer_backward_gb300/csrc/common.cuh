@@ -181,22 +181,20 @@ __device__ __forceinline__ float weight_at(const void *w, int64_t idx) {
         return float(__ldg(reinterpret_cast<const signed char *>(w) + idx));
     } else {
         const uint32_t b = __ldg(reinterpret_cast<const unsigned char *>(w) + (idx >> 2));
-        const uint32_t c = (b >> (2 * uint32_t(idx & 3))) & 3u;
-        return c == 1u ? 1.f : (c == 2u ? -1.f : 0.f);
+        return float((b >> (2 * uint32_t(idx & 3))) & 3u) - 1.f;     // code q = w + 1
     }
 }
 
-// sum_i w_i x_i over the four 2-bit ternary codes of byte b (lowest bits first; 0: 0,
-// 1: +1, 2: -1, 3: read as 0) and the four floats of x.
-__device__ __forceinline__ float t2_dot4(uint32_t b, float4 x) {
-    const float xs[4] = {x.x, x.y, x.z, x.w};
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t c = (b >> (2 * i)) & 3u;
-        s += c == 1u ? xs[i] : (c == 2u ? -xs[i] : 0.f);
-    }
-    return s;
+// sum_i q_i x_i over the four 2-bit codes q_i of byte b (lowest bits first) and the four
+// floats of x.  Each code becomes an exact float by OR-ing it into the mantissa of 2^23
+// and subtracting 2^23; the ternary dot product is this minus the sum of x (w = q - 1),
+// which the caller forms once for all the rows that share x.
+__device__ __forceinline__ float t2_qdot4(uint32_t b, float4 x) {
+    const float q0 = __uint_as_float(0x4B000000u | (b & 3u)) - 8388608.f;
+    const float q1 = __uint_as_float(0x4B000000u | ((b >> 2) & 3u)) - 8388608.f;
+    const float q2 = __uint_as_float(0x4B000000u | ((b >> 4) & 3u)) - 8388608.f;
+    const float q3 = __uint_as_float(0x4B000000u | ((b >> 6) & 3u)) - 8388608.f;
+    return fmaf(q3, x.w, fmaf(q2, x.z, fmaf(q1, x.y, q0 * x.x)));
 }
 
 // cos and sin of theta = pos * f with f = f_hi + f_lo (a float pair carrying the

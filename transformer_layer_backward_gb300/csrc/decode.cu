@@ -75,24 +75,26 @@ __device__ __forceinline__ void warp_rows(const char *const *W, const float *sca
             const int ch = base + u * 32 + lane;
             if (ch >= nch) break;
             if constexpr (WT == TLB_W_TERNARY_2B) {
-                // 64 packed weights per chunk: byte k of the chunk against float4 unit k
+                // 64 packed weights per chunk: byte k of the chunk against float4 unit k;
+                // sum w x = sum q x - sum x with the codes q = w + 1
 #pragma unroll
                 for (int m = 0; m < NM; ++m) {
-                    float part[R];
+                    float part[R], xsum = 0.f;
 #pragma unroll
                     for (int r = 0; r < R; ++r) part[r] = 0.f;
 #pragma unroll
                     for (int k = 0; k < P; ++k) {
                         const float4 t = reinterpret_cast<const float4 *>(xs[m])[xunit<WT>(ch * P + k)];
+                        xsum += (t.x + t.y) + (t.z + t.w);
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const uint4 &q = w[m][r][u];
                             const uint32_t word = k < 4 ? q.x : (k < 8 ? q.y : (k < 12 ? q.z : q.w));
-                            part[r] += t2_dot4((word >> (8 * (k & 3))) & 0xFFu, t);
+                            part[r] += t2_qdot4(word >> (8 * (k & 3)), t);
                         }
                     }
 #pragma unroll
-                    for (int r = 0; r < R; ++r) acc[r] = fmaf(scale[m], part[r], acc[r]);
+                    for (int r = 0; r < R; ++r) acc[r] = fmaf(scale[m], part[r] - xsum, acc[r]);
                 }
                 continue;
             }

@@ -82,7 +82,9 @@ int attn_core_launch(const AttnArgs &a, float rope_base, cudaStream_t st);
 //   dK[jj, kvh, :] = scale sum_{h in group} sum_i attn[h,i,j] (dCtx[i,h,:] . V[j,kvh,:] - D[h,i]) q[i,h,:]
 // with j = L - S + jj, q [S, q_dim] the cached queries (after RoPE), D from the attention
 // kernels; dk [S, kv_dim] (before RoPE backward).
-int attn_dk_launch(const AttnArgs &a, const float *q, const float *D, float *dk, cudaStream_t st);
+// part: attn_dk_bytes(...) bytes of scratch (per-head partials; may be NULL when that is 0).
+size_t attn_dk_bytes(int64_t S, int nh, int nkv, int hd);
+int attn_dk_launch(const AttnArgs &a, const float *q, const float *D, float *dk, float *part, cudaStream_t st);
 
 // Tensor-core (tf32) attention backward (attn_tc.cu): S > 1, head_dim 64 or 128, L and
 // L - S multiples of 4; attn, dq and dv 16-byte aligned.  scratch: attn_tc_bytes(...) bytes, 256-byte aligned.

@@ -19,7 +19,7 @@ struct LayerWs {
     size_t abf, gbf, ubf, part;               // tensor-core path: bf16 A operands, split-K partials
     size_t atc;                               // tensor-core attention: tf32 operand copies
     size_t dR1, Upart, Wpart, Dpart, gh2, part1, part2, part3, gbar, pp;   // single-token path
-    size_t dk, Dh, dn1, dctx, xbf;            // exact layer-input gradient (TLB_EXACT_DIN)
+    size_t dk, dkpart, Dh, dn1, dctx, xbf;    // exact layer-input gradient (TLB_EXACT_DIN)
     size_t total;
 };
 
@@ -81,6 +81,7 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     }
     if (exact) {
         w.dk = p.take(S * kvd * 4);
+        w.dkpart = p.take(std::max(attn_dk_bytes(S, c.n_heads, c.n_kv_heads, c.head_dim), size_t(256)));
         w.Dh = p.take(int64_t(c.n_heads) * S * 4);
         w.dn1 = p.take(S * H * 4);
         w.dctx = p.take(S * qd * 4);
@@ -90,7 +91,7 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
                          tc_supported(S, H, kvd);
         w.xbf = tcx ? p.take(S * (qd + 2 * kvd) * 2) : 0;
     } else {
-        w.dk = w.Dh = w.dn1 = w.dctx = w.xbf = 0;
+        w.dk = w.dkpart = w.Dh = w.dn1 = w.dctx = w.xbf = 0;
     }
     w.total = p.off;
     return w;
@@ -277,7 +278,7 @@ int exact_din_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const tlb_layer
     const int64_t H = c.dim, qd = int64_t(c.n_heads) * c.head_dim, kvd = int64_t(c.n_kv_heads) * c.head_dim;
     float *dk = ws_at<float>(ws, p.dk);
     const AttnArgs g = attn_args(c, S, L, dctx, a, nullptr, nullptr);
-    TLB_TRY(attn_dk_launch(g, a.q, D, dk, st));
+    TLB_TRY(attn_dk_launch(g, a.q, D, dk, ws_at<float>(ws, p.dkpart), st));
     if (c.flags & TLB_ROPE)
         TLB_TRY(rope_backward_launch(dk, dk, S, c.n_kv_heads, c.head_dim, L - S, c.rope_base, st));
     if (c.flags & TLB_QK_NORM)

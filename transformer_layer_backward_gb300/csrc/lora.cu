@@ -791,12 +791,13 @@ struct LoraDinArgs {
     float *dn1;                  // [S, C], added into
 };
 
-// Block = 16 rows, 256 threads: the rows' gh values of both adapters in shared memory, then
-// dn1[row, c] += sum_t sum_r gh_t[row, r] A_t[r, c], each A value read once per block and
-// used for its 16 rows.
+// Block = 16 rows x 256 columns, one column per thread: the rows' gh values of both
+// adapters in shared memory, then dn1[row, c] += sum_t sum_r gh_t[row, r] A_t[r, c].  A
+// thread loads 16 of its A values at a time before it uses them (loads in flight), and
+// each serves the block's 16 rows.
 __global__ void __launch_bounds__(256) lora_din_kernel(LoraDinArgs a) {
     extern __shared__ float sgh[];                  // [kDinRows][njobs][rank]
-    const int r0 = blockIdx.x * kDinRows;
+    const int r0 = blockIdx.y * kDinRows;
     const int nrows = min(kDinRows, a.S - r0);
     const int per = a.njobs * a.rank;
     for (int e = threadIdx.x; e < kDinRows * per; e += blockDim.x) {
@@ -804,22 +805,29 @@ __global__ void __launch_bounds__(256) lora_din_kernel(LoraDinArgs a) {
         sgh[e] = row < nrows ? (t == 0 ? a.gh[0] : a.gh[1])[int64_t(r0 + row) * a.rank + r] : 0.f;
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < a.C; c += blockDim.x) {
-        float acc[kDinRows];
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= a.C) return;
+    float acc[kDinRows];
 #pragma unroll
-        for (int row = 0; row < kDinRows; ++row) acc[row] = 0.f;
-        for (int t = 0; t < a.njobs; ++t) {
-            const float *A = t == 0 ? a.A[0] : a.A[1];
-            for (int r = 0; r < a.rank; ++r) {
-                const float av = A[int64_t(r) * a.C + c];
+    for (int row = 0; row < kDinRows; ++row) acc[row] = 0.f;
+    for (int t = 0; t < a.njobs; ++t) {
+        const float *A = t == 0 ? a.A[0] : a.A[1];
+        for (int rc = 0; rc < a.rank; rc += 16) {
+            float av[16];
 #pragma unroll
-                for (int row = 0; row < kDinRows; ++row) acc[row] = fmaf(sgh[row * per + t * a.rank + r], av, acc[row]);
+            for (int k = 0; k < 16; ++k) av[k] = rc + k < a.rank ? __ldg(A + int64_t(rc + k) * a.C + c) : 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                if (rc + k >= a.rank) break;
+                const float *g = sgh + t * a.rank + rc + k;
+#pragma unroll
+                for (int row = 0; row < kDinRows; ++row) acc[row] = fmaf(g[row * per], av[k], acc[row]);
             }
         }
-#pragma unroll
-        for (int row = 0; row < kDinRows; ++row)      // constant bound: acc stays in registers
-            if (row < nrows) a.dn1[int64_t(r0 + row) * a.C + c] += acc[row];
     }
+#pragma unroll
+    for (int row = 0; row < kDinRows; ++row)      // constant bound: acc stays in registers
+        if (row < nrows) a.dn1[int64_t(r0 + row) * a.C + c] += acc[row];
 }
 
 }  // namespace
@@ -839,7 +847,8 @@ int lora_din_launch(int64_t S, int in_dim, int rank, const float *const *gh, con
     a.rank = rank;
     a.dn1 = dn1;
     const size_t sm = size_t(kDinRows) * njobs * rank * 4;
-    lora_din_kernel<<<unsigned(ceil_div(S, int64_t(kDinRows))), 256, sm, st>>>(a);
+    lora_din_kernel<<<dim3(unsigned(ceil_div(in_dim, 256)), unsigned(ceil_div(S, int64_t(kDinRows)))), 256, sm,
+                      st>>>(a);
     return check_launch("lora_din");
 }
 
