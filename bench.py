@@ -62,6 +62,9 @@ def parse(argv=None):
     p.add_argument("--workload", default="stack2048", choices=["decode", "seq512", "seq2048", "stack2048", "sweep", "tf32peak"])
     p.add_argument("--qk-norm", action="store_true",
                    help="layers with the per-head QK-norm on q (decode and sequence workloads)")
+    p.add_argument("--recompute-p", action="store_true",
+                   help="sequence workloads: attention weights recomputed from q, K and each row's logsumexp "
+                        "(not read from the cached [nh, S, L] weights)")
     p.add_argument("--wtype", default="ternary", choices=["ternary", "ternary2"],
                    help="decode: int8 ternary weights, or the same values packed four 2-bit codes to a byte")
     p.add_argument("--exact-din", action="store_true",
@@ -211,6 +214,8 @@ def run_reference(args, rank, world):
             cfg = cfg.with_(qk_norm=True)
         if args.exact_din:
             cfg = cfg.with_(exact_din=True)
+        if args.recompute_p:
+            cfg = cfg.with_(recompute_p=True)
         slices = seq_cpu_sample(cfg)
         for k in range(min(args.warmup, 1)):
             seq_cpu_time(slices[k])
@@ -282,6 +287,10 @@ def seq_kernel_flops(cfg, names):
             out.append((2 * 2 * pairs * cfg.head_dim * cfg.n_heads, "tf32"))
         elif nm == "attn_tc_dv":
             out.append((2 * pairs * cfg.head_dim * cfg.n_heads, "tf32"))
+        elif nm == "attn_dq_tiled":       # dAttn, dQ (+ the recomputed scores)
+            out.append(((3 if cfg.recompute_p else 2) * 2 * pairs * cfg.head_dim * cfg.n_heads, "fp32"))
+        elif nm == "attn_dv_tiled":
+            out.append(((2 if cfg.recompute_p else 1) * 2 * pairs * cfg.head_dim * cfg.n_heads, "fp32"))
         elif nm in ("attn_dk_tiled", "attn_dk_tc"):     # dAttn recomputed and dK = dS^T q
             out.append((2 * 2 * pairs * cfg.head_dim * cfg.n_heads, "fp32" if nm == "attn_dk_tiled" else "tf32"))
         else:
@@ -296,6 +305,7 @@ def seq_workload_config(cfg, depth, world):
     return {"workload": name + ": dim 2560, ffn 9728, 32/8 heads x 128, SwiGLU, RoPE, residual, " +
                         ("QK-norm on q, " if cfg.qk_norm else "") +
                         ("exact layer-input gradient, " if cfg.exact_din else "") +
+                        ("attention recomputed from q, K and the logsumexp, " if cfg.recompute_p else "") +
                         "bf16 weights, LoRA r16 Q/V, AdamW+LoRA+",
             "global_batch": world, "seq_len": cfg.seq_len, "layers_per_step": depth,
             "parallelism": "replicas" if world > 1 else "single",
@@ -324,6 +334,8 @@ def seq_main(args, rank, world, local, dist):
         cfg = cfg.with_(qk_norm=True)
     if args.exact_din:
         cfg = cfg.with_(exact_din=True)
+    if args.recompute_p:
+        cfg = cfg.with_(recompute_p=True)
     S, L = cfg.seq_len, cfg.cache_len
     NL = args.layers or (depth if depth > 1 else 2)     # distinct layers (weights, caches, adapters)
     c = tlb.layer_cfg_of(cfg)
@@ -431,17 +443,22 @@ def seq_main(args, rank, world, local, dist):
     pk = peaks()
     bf16_peak = pk["bf16_tflops_sustained"] if pk else 1700.0
     tf32, tf32_src = tf32_peak(bf16_peak)
+    # CUDA-core fp32 kernels: FMA peak from the unit counts (128 fp32 lanes per SM, 2 flops
+    # per FMA) at the maximum SM clock
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    fp32_peak = sms * 128 * 2 * (pk["sm_max_mhz"] if pk else 2070.0) * 1e6 / 1e12
+    peak_of = {"bf16": bf16_peak, "tf32": tf32, "fp32": fp32_peak}
     per_kernel = []
     for nm, t, (f, kind) in zip(names, ktime, fl):
         e = {"kernel": nm, "us": t * 1e3}
         if f:
-            pkk = bf16_peak if kind == "bf16" else tf32
+            pkk = peak_of[kind]
             e.update({"flop": f, "TFLOP/s": f / (t / 1e3) / 1e12, "operands": kind,
                       "frac": f / (t / 1e3) / 1e12 / pkk})
         per_kernel.append(e)
     dom = max((k for k in range(nkern) if fl[k][0]), key=lambda k: ktime[k])
     achieved = fl[dom][0] / (ktime[dom] / 1e3) / 1e12
-    peak = bf16_peak if fl[dom][1] == "bf16" else tf32
+    peak = peak_of[fl[dom][1]]
     # DRAM bytes of the dominant kernel from the committed ncu capture of the S = 2048 layer
     # (per launch; the stack runs the same launches per layer)
     traffic = None
@@ -461,8 +478,9 @@ def seq_main(args, rank, world, local, dist):
     # pinned host memory on a copy stream (the next layer's copy overlapping this layer's
     # kernels), one tlb_layer_backward call per layer from the top of the stack down, and
     # d_in and the gradient sums read back at the end of each step
-    acts = ("x", "gate", "up", "silu_gate", "k", "v", "attn", "lora_q_h", "lora_v_h") + \
-        (("q_raw",) if cfg.qk_norm else ()) + (("q",) if cfg.exact_din else ()) + \
+    acts = ("x", "gate", "up", "silu_gate", "k", "v", "lora_q_h", "lora_v_h") + \
+        (("lse", "q") if cfg.recompute_p else ("attn",)) + (("q_raw",) if cfg.qk_norm else ()) + \
+        (("q",) if cfg.exact_din and not cfg.recompute_p else ()) + \
         (("k_raw",) if cfg.exact_din and cfg.qk_norm else ())
     NP = min(NL, 2)
     pinned = [{k: layers[l]["t"][k].cpu().pin_memory() for k in acts} for l in range(NP)]
@@ -513,11 +531,15 @@ def seq_main(args, rank, world, local, dist):
                             "step": ("one tlb_stack_backward call over %d layers" % depth) if depth > 1 else
                                     "one tlb_layer_backward call"},
                 "layer_tokens_per_s": value * depth,
-                "roofline": {"bound": "tensor", "kernel": names[dom], "achieved": achieved, "peak": peak,
+                "roofline": {"bound": "alu" if fl[dom][1] == "fp32" else "tensor", "kernel": names[dom],
+                             "achieved": achieved, "peak": peak,
                              "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                              "algorithmic_flop": fl[dom][0],
-                             "peak_source": ("MEASURED_PEAKS.json bf16_tflops_sustained (of measured)" if pk else
-                                             "fallback") if fl[dom][1] == "bf16" else tf32_src},
+                             "peak_source": {"bf16": ("MEASURED_PEAKS.json bf16_tflops_sustained (of measured)" if pk
+                                                      else "fallback"),
+                                             "tf32": tf32_src,
+                                             "fp32": "SMs x 128 fp32 lanes x 2 flops x max SM clock (derived)"}[
+                                                 fl[dom][1]]},
                 "step_roofline": step_roofline,
                 "per_kernel": per_kernel, "per_kernel_timing": "graph",
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk}

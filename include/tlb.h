@@ -107,6 +107,14 @@ extern "C" {
                                   Needs w_q, w_k, w_v and acts->q; with PRE_NORM x_in and gamma_attn;
                                   with TLB_QK_NORM k_raw and gamma_k.  Not with TLB_PERSISTENT, and a
                                   single-token stack runs its layers one after another */
+#define TLB_RECOMPUTE_P 1024   /* the attention weights are not read from acts->attn (which may be NULL)
+                                  but recomputed where they are used from the queries and the
+                                  logsumexp of each query row: attn[h,i,j] = exp(attn_scale <q[i,h],
+                                  k[j,kvh]> - lse[h,i]) on the visible keys (flash-style, so that the
+                                  [n_heads, S, L] weights need not be cached; [RS] LayerActivations
+                                  attn_weights is that cache).  Needs acts->q and acts->lse.  Runs the
+                                  CUDA-core attention kernels (fp32) for every S, also with bf16
+                                  weights */
 
 /* Shapes and constants of one layer. q_dim = n_heads*head_dim, kv_dim = n_kv_heads*head_dim. */
 typedef struct {
@@ -171,6 +179,8 @@ typedef struct {
     const float *x_in;       /* layer input before the attention pre-norm [S, dim], with TLB_PRE_NORM */
     const float *q;          /* queries after RoPE (and the QK-norm) [S, q_dim] */
     const float *k_raw;      /* K projection output of the S new rows before the norm [S, kv_dim], with TLB_QK_NORM */
+    /* TLB_RECOMPUTE_P only (NULL otherwise; q above is needed too): */
+    const float *lse;        /* [n_heads, S] logsumexp over the visible keys of attn_scale <q[i,h], k[j,kvh]> */
 } tlb_layer_acts;
 
 /* A LoRA adapter (A [rank, in], B [out, rank]) and its AdamW moments, updated in place.

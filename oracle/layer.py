@@ -42,7 +42,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .ops import (adamw, apply_backward, f64, linear_backward, lora_backward,
+from .ops import (adamw, apply_backward, attention_from_logsumexp, f64, linear_backward, lora_backward,
                   relu2_mul_backward, rmsnorm_backward, rope_backward, score_backward_k,
                   score_backward_q, silu_mul_backward, softmax_backward, unpack_ternary2,
                   value_backward)
@@ -83,7 +83,11 @@ def attn_backward(cfg, d, dR1) -> dict:
     dSub = linear_backward(dR1, W(cfg, d, "w_o"), d["s_o"])
     dCtx = rmsnorm_backward(d["ctx"], d["g_sub_attn"], dSub, cfg.norm_eps) if cfg.sub_norm else dSub
     K, V = kv_heads_first(d["k"], cfg), kv_heads_first(d["v"], cfg)
-    attn = f64(d["attn"])
+    if getattr(cfg, "recompute_p", False):      # the weights from q, K and each row's logsumexp
+        attn = attention_from_logsumexp(f64(d["q"]).reshape(S, nh, hd), K, d["lse"], cfg.attn_scale, cfg.pos0,
+                                        nkv)
+    else:
+        attn = f64(d["attn"])
     group = nh // nkv
     dQ = np.zeros((S, nh, hd))
     dS_all = np.zeros((nh, S, L))

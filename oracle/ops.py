@@ -33,6 +33,22 @@ def unpack_ternary2(packed) -> np.ndarray:
     return value[codes].reshape(b.shape[:-1] + (b.shape[-1] * 4,))
 
 
+def attention_from_logsumexp(q, K, lse, scale: float, pos0: int, n_kv: int) -> np.ndarray:
+    """Attention weights [nh, S, L] recomputed from the queries q [S, nh, hd] (after RoPE),
+    the key cache K [n_kv, L, hd] and each row's logsumexp lse [nh, S]:
+    attn[h, i, j] = exp(scale q_i,h . k_j - lse[h, i]) for j <= pos0 + i, else 0 (the
+    softmax of the forward, given its normaliser; GQA head h reads KV head h // (nh / n_kv))."""
+    q, K, lse = f64(q), f64(K), f64(lse)
+    S, nh, hd = q.shape
+    L = K.shape[1]
+    vis = np.arange(L)[None, :] <= (pos0 + np.arange(S))[:, None]
+    out = np.zeros((nh, S, L))
+    g = nh // n_kv
+    for h in range(nh):
+        out[h] = np.where(vis, np.exp(scale * q[:, h, :] @ K[h // g].T - lse[h][:, None]), 0.0)
+    return out
+
+
 def linear_backward(dy, w, scale: float = 1.0) -> np.ndarray:
     """Input gradient of y = x @ (scale * W) with W stored [in, out]: dX = scale * dY @ W^T.
 

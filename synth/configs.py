@@ -36,6 +36,8 @@ class LayerConfig:
     exact_din: bool = False  # the layer-input gradient also through the Q/K/V projections,
                              # their LoRA paths and the attention pre-norm (the pages stop
                              # at the projection outputs); oracle only
+    recompute_p: bool = False  # attention weights recomputed from q, the K cache and each row's
+                               # logsumexp instead of read from the cached [nh, S, L] weights
     kv_layout: str = "shd"   # "shd": [L, n_kv*hd]   "hsd": [n_kv, L, hd]
     rope_base: float = 10000.0
     norm_eps: float = 1e-6

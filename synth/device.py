@@ -66,12 +66,24 @@ def device_layer(cfg, layer, seed=0):
         t[k] = n(*shape)
     t["silu_gate"] = torch.nn.functional.silu(t["gate"])
     pos0 = L - S
-    attn = torch.empty(cfg.n_heads, S, L, device="cuda")
     mask = torch.arange(L, device="cuda")[None, :] > (pos0 + torch.arange(S, device="cuda"))[:, None]
-    for h in range(cfg.n_heads):
-        logits = n(S, L, std=cfg.attn_logit_std).masked_fill_(mask, float("-inf"))
-        attn[h] = torch.softmax(logits, dim=-1)
-    t["attn"] = attn
+    if getattr(cfg, "recompute_p", False):
+        # queries after RoPE and each row's logsumexp of attn_scale q k^T over its keys; the
+        # weights themselves are not kept (they are recomputed where they are used)
+        t["q"] = n(S, qd)
+        kh = t["k"].view(L, cfg.n_kv_heads, cfg.head_dim)
+        lse = torch.empty(cfg.n_heads, S, device="cuda")
+        g = cfg.n_heads // cfg.n_kv_heads
+        for h in range(cfg.n_heads):
+            z = cfg.attn_scale * t["q"][:, h * cfg.head_dim:(h + 1) * cfg.head_dim] @ kh[:, h // g, :].t()
+            lse[h] = torch.logsumexp(z.masked_fill_(mask, float("-inf")), dim=-1)
+        t["lse"] = lse
+    else:
+        attn = torch.empty(cfg.n_heads, S, L, device="cuda")
+        for h in range(cfg.n_heads):
+            logits = n(S, L, std=cfg.attn_logit_std).masked_fill_(mask, float("-inf"))
+            attn[h] = torch.softmax(logits, dim=-1)
+        t["attn"] = attn
     for k, shape in (("a_q", (r, H)), ("b_q", (qd, r)), ("a_v", (r, H)), ("b_v", (kvd, r))):
         t[k] = n(*shape, std=0.02)
         t["m_" + k] = torch.zeros_like(t[k])
@@ -83,7 +95,8 @@ def device_layer(cfg, layer, seed=0):
         t["g_q"] = torch.rand(cfg.head_dim, device="cuda", generator=g) + 0.5
     if getattr(cfg, "exact_din", False):
         t["x_in"] = n(S, H)
-        t["q"] = n(S, qd)
+        if "q" not in t:
+            t["q"] = n(S, qd)
         if cfg.pre_norm:
             t["g_attn"] = torch.rand(H, device="cuda", generator=g) + 0.5
         if cfg.qk_norm:

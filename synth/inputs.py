@@ -18,6 +18,9 @@ Recipe (distributions follow the workload descriptions):
   * the cached SiLU output is silu(gate) and the cached LoRA activations are
     x @ A^T, both formed in float64 from the values above and then rounded;
   * with the QK-norm, the Q projection before it ~ N(0, 1) and its gain ~ U(0.5, 1.5);
+  * with the attention recomputed: the queries after RoPE ~ N(0, 1) and each row's
+    logsumexp of attn_scale q k^T over its visible keys (the cached weights are then that
+    softmax too);
   * for the exact layer-input gradient: W_Q, W_K, W_V like the other weights, the layer
     input, the cached (rotated) q and, with the QK-norm, the new rows of k before it
     ~ N(0, 1), and the attention pre-norm and k-norm gains ~ U(0.5, 1.5).
@@ -104,7 +107,27 @@ def layer_inputs(cfg: LayerConfig, layer: int = 0, seed: int = 0, with_dout: boo
     kshape = (L, kvd) if cfg.kv_layout == "shd" else (cfg.n_kv_heads, L, cfg.head_dim)
     d["k"] = _n(seed, cfg, layer, "k_cache", kshape).astype(f32)
     d["v"] = _n(seed, cfg, layer, "v_cache", kshape).astype(f32)
-    d["attn"] = attention_rows(seed, cfg, layer)
+    if cfg.recompute_p:
+        # queries after RoPE and the logsumexp of each row's scaled logits over the keys it
+        # sees (the forward's softmax statistics); the cached weights are the same softmax
+        q = _n(seed, cfg, layer, "q_cache", (S, qd)).astype(f32)
+        d["q"] = q
+        kh = (d["k"].reshape(L, cfg.n_kv_heads, cfg.head_dim).transpose(1, 0, 2) if cfg.kv_layout == "shd"
+              else d["k"]).astype(np.float64)
+        qh = q.astype(np.float64).reshape(S, cfg.n_heads, cfg.head_dim)
+        vis = np.arange(L)[None, :] <= (cfg.pos0 + np.arange(S))[:, None]
+        lse = np.zeros((cfg.n_heads, S))
+        attn = np.zeros((cfg.n_heads, S, L))
+        g = cfg.n_heads // cfg.n_kv_heads
+        for h in range(cfg.n_heads):
+            z = np.where(vis, cfg.attn_scale * qh[:, h, :] @ kh[h // g].T, -np.inf)
+            m = z.max(axis=-1, keepdims=True)
+            lse[h] = (m + np.log(np.exp(z - m).sum(axis=-1, keepdims=True)))[:, 0]
+            attn[h] = np.exp(z - lse[h][:, None])
+        d["lse"] = lse.astype(f32)
+        d["attn"] = attn.astype(f32)
+    else:
+        d["attn"] = attention_rows(seed, cfg, layer)
     if cfg.qk_norm:
         d["q_raw"] = _n(seed, cfg, layer, "q_raw", (S, qd)).astype(f32)
         d["g_q"] = _u(seed, cfg, layer, "g_q", (cfg.head_dim,), 0.5, 1.5).astype(f32)
@@ -113,7 +136,8 @@ def layer_inputs(cfg: LayerConfig, layer: int = 0, seed: int = 0, with_dout: boo
         d["w_k"], d["s_k"] = _weight(seed, cfg, layer, "w_k", (H, kvd))
         d["w_v"], d["s_v"] = _weight(seed, cfg, layer, "w_v", (H, kvd))
         d["x_in"] = _n(seed, cfg, layer, "layer_input", (S, H)).astype(f32)
-        d["q"] = _n(seed, cfg, layer, "q_cache", (S, qd)).astype(f32)
+        if "q" not in d:
+            d["q"] = _n(seed, cfg, layer, "q_cache", (S, qd)).astype(f32)
         if cfg.pre_norm:
             d["g_attn"] = _u(seed, cfg, layer, "g_attn", (H,), 0.5, 1.5).astype(f32)
         if cfg.qk_norm:

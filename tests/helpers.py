@@ -58,7 +58,7 @@ def tc_attention_shape(cfg) -> bool:
     128, L and L - S multiples of 4 (16-byte starts of the attention rows)."""
     S, L = cfg.seq_len, cfg.cache_len
     return (cfg.wtype == "bf16" and S > 1 and L % 4 == 0 and (L - S) % 4 == 0 and cfg.head_dim in (64, 128)
-            and cfg.n_heads % cfg.n_kv_heads == 0)
+            and cfg.n_heads % cfg.n_kv_heads == 0 and not cfg.recompute_p)
 
 
 def assert_route(cfg, names):

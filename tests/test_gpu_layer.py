@@ -71,7 +71,20 @@ SEQ512_EXACT = SEQ512.with_(name="seq512_exact", exact_din=True)
 DECODE_T2 = DECODE.with_(name="decode_t2", wtype="ternary2")
 DEC_T2 = DEC_G8.with_(name="dec_t2_g8", wtype="ternary2")
 DEC_T2_EXACT = DEC_T2.with_(name="dec_t2_exact", exact_din=True, pre_norm=True)
-CASES = {c.name: c for c in (DECODE_T2, DEC_T2, DEC_T2_EXACT,
+# attention weights recomputed from q, the K cache and the logsumexp (flash-style): the
+# row kernels (tiny, head_dim 16; a single-token layer), the tiled CUDA-core kernels (bf16
+# layers of head_dim 32, 64 and 128, a cache longer than the sequence), and with the exact
+# input gradient (the key-gradient kernels recompute too)
+TINY_RC = TINY.with_(name="tiny_recompute", recompute_p=True)
+DEC_RC = DEC_F32.with_(name="dec_recompute", recompute_p=True)
+MINI_SEQ_RC = MINI_SEQ.with_(name="mini_seq_recompute", recompute_p=True)
+SEQ_RC = SEQ_HD64.with_(name="seq_recompute", recompute_p=True)
+SEQ_RC_CACHE = SEQ_CACHE.with_(name="seq_recompute_cache", recompute_p=True)
+SEQ_RC_EXACT = SEQ_HD64.with_(name="seq_recompute_exact", recompute_p=True, exact_din=True, seq_len=130,
+                              cache_len=130)
+TINY_RC_EXACT = TINY.with_(name="tiny_recompute_exact", recompute_p=True, exact_din=True, qk_norm=True)
+CASES = {c.name: c for c in (TINY_RC, DEC_RC, MINI_SEQ_RC, SEQ_RC, SEQ_RC_CACHE, SEQ_RC_EXACT, TINY_RC_EXACT,
+                             DECODE_T2, DEC_T2, DEC_T2_EXACT,
                              TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512, DEC_F32, DEC_BF16, DEC_G8, DEC_HD256,
                              SEQ_HD64, SEQ_CACHE, SEQ_MHA, SEQ_ODD, TINY_QK, DEC_QK, SEQ_QK, SEQ_PRENORM,
                              SEQ_NORESID, SEQ_NORMS, TINY_EXACT, TINY_EXACT_QK, DEC_EXACT, DECODE_EXACT,

@@ -257,6 +257,46 @@ def test_packed_ternary_round_trip_and_layer():
         np.testing.assert_array_equal(a[k], b[k])
 
 
+def test_attention_from_logsumexp_is_the_softmax():
+    """Recomputed weights exp(scale q.k - lse) against a softmax formed directly (max
+    shift, exponent, row sum) over the visible keys, with GQA and a cache longer than the
+    sequence: equal, masked keys zero, rows summing to one."""
+    rs = np.random.default_rng(5)
+    S, L, nh, nkv, hd, scale = 3, 7, 4, 2, 5, 0.37
+    q = rs.normal(size=(S, nh, hd))
+    K = rs.normal(size=(nkv, L, hd))
+    pos0 = L - S
+    want = np.zeros((nh, S, L))
+    lse = np.zeros((nh, S))
+    for h in range(nh):
+        for i in range(S):
+            z = np.array([scale * q[i, h] @ K[h // 2, j] for j in range(pos0 + i + 1)])
+            e = np.exp(z - z.max())
+            want[h, i, :pos0 + i + 1] = e / e.sum()
+            lse[h, i] = z.max() + math.log(e.sum())
+    got = ops.attention_from_logsumexp(q, K, lse, scale, pos0, nkv)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(got.sum(axis=-1), 1.0, rtol=0, atol=1e-14)
+
+
+def test_recomputed_attention_layer_is_the_cached_one():
+    """A layer whose attention weights are recomputed from q, K and the logsumexp gives the
+    gradients of the same layer reading those weights from the cache (float64 on both
+    sides), for the sequence and exact-gradient compositions."""
+    from synth import layer_inputs
+    for cfg in (small_cfg(name="rc", recompute_p=True, seq_len=3, cache_len=6),
+                small_cfg(name="rc_exact", recompute_p=True, exact_din=True, qk_norm=True)):
+        d = layer_inputs(cfg)
+        K = Lyr.kv_heads_first(d["k"], cfg)
+        q = d["q"].astype(np.float64).reshape(cfg.seq_len, cfg.n_heads, cfg.head_dim)
+        d2 = dict(d)
+        d2["attn"] = ops.attention_from_logsumexp(q, K, d["lse"], cfg.attn_scale, cfg.pos0, cfg.n_kv_heads)
+        a = Lyr.layer_backward(cfg, d, d["dout"])
+        b = Lyr.layer_backward(cfg.with_(recompute_p=False), d2, d["dout"])
+        for k in ("d_in", "dA_q", "dB_q", "dA_v", "dB_v", "dQpre", "dV"):
+            np.testing.assert_array_equal(a[k], b[k])
+
+
 def test_linear_backward_is_the_adjoint():
     rs = np.random.default_rng(2)
     x, w, dy = rs.normal(size=(5, 7)), rs.normal(size=(7, 3)), rs.normal(size=(5, 3))

@@ -14,7 +14,7 @@ TLB_OK, TLB_EINVAL, TLB_EUNSUPPORTED, TLB_ENONFINITE, TLB_ETIMEOUT, TLB_ECUDA = 
 ACT_RELU2_MUL, ACT_SILU_MUL = 0, 1
 W_F32, W_BF16, W_TERNARY_I8, W_TERNARY_2B = 0, 1, 2, 3
 SUB_NORM, PRE_NORM, RESIDUAL, ROPE, USE_SILU_CACHE, CAUSAL, PERSISTENT, QK_NORM = 1, 2, 4, 8, 16, 32, 64, 128
-CHECK_FINITE, EXACT_DIN = 256, 512
+CHECK_FINITE, EXACT_DIN, RECOMPUTE_P = 256, 512, 1024
 
 vp, i32, i64, f32, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_size_t
 
@@ -40,7 +40,7 @@ class LayerActs(C.Structure):
     _fields_ = [("x", vp), ("gate", vp), ("up", vp), ("silu_gate", vp), ("hidden", vp),
                 ("r1", vp), ("ctx", vp), ("k", vp), ("v", vp), ("kv_stride_head", i64),
                 ("kv_stride_pos", i64), ("attn", vp), ("lora_q_h", vp), ("lora_v_h", vp),
-                ("q_raw", vp), ("x_in", vp), ("q", vp), ("k_raw", vp)]
+                ("q_raw", vp), ("x_in", vp), ("q", vp), ("k_raw", vp), ("lse", vp)]
 
 
 class Lora(C.Structure):

@@ -149,12 +149,13 @@ def layer_cfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, lora_alpha, act
               wtype="f32", sub_norm=False, pre_norm=False, residual=True, rope=True,
               use_silu_cache=False, causal=True, rope_base=10000.0, norm_eps=1e-6,
               attn_scale=None, persistent=False, qk_norm=False, check_finite=False,
-              exact_din=False) -> A.LayerCfg:
+              exact_din=False, recompute_p=False) -> A.LayerCfg:
     flags = ((A.SUB_NORM if sub_norm else 0) | (A.PRE_NORM if pre_norm else 0) |
              (A.RESIDUAL if residual else 0) | (A.ROPE if rope else 0) |
              (A.USE_SILU_CACHE if use_silu_cache else 0) | (A.CAUSAL if causal else 0) |
              (A.PERSISTENT if persistent else 0) | (A.QK_NORM if qk_norm else 0) |
-             (A.CHECK_FINITE if check_finite else 0) | (A.EXACT_DIN if exact_din else 0))
+             (A.CHECK_FINITE if check_finite else 0) | (A.EXACT_DIN if exact_din else 0) |
+             (A.RECOMPUTE_P if recompute_p else 0))
     return A.LayerCfg(dim, ffn_dim, n_heads, n_kv_heads, head_dim, rank, float(lora_alpha),
                       float(rope_base), float(norm_eps),
                       float(1.0 / math.sqrt(head_dim) if attn_scale is None else attn_scale),
@@ -173,7 +174,7 @@ def layer_cfg_of(c, persistent=False, check_finite=False) -> A.LayerCfg:
                      use_silu_cache=(c.act == "silu_mul" and c.use_silu_cache), causal=True,
                      rope_base=c.rope_base, norm_eps=c.norm_eps, attn_scale=c.attn_scale,
                      persistent=persistent, qk_norm=c.qk_norm, check_finite=check_finite,
-                     exact_din=getattr(c, "exact_din", False))
+                     exact_din=getattr(c, "exact_din", False), recompute_p=getattr(c, "recompute_p", False))
 
 
 def adamw_cfg_of(c) -> A.AdamwCfg:
@@ -230,7 +231,7 @@ def layer_acts(cfg: A.LayerCfg, t: dict, kv_layout: str, L: int):
     g = lambda k: _ptr(t.get(k), name=k)
     return A.LayerActs(g("x"), g("gate"), g("up"), g("silu_gate"), g("hidden"), g("r1"),
                        g("ctx"), g("k"), g("v"), sh, sp, g("attn"), g("lora_q_h"), g("lora_v_h"),
-                       g("q_raw"), g("x_in"), g("q"), g("k_raw"))
+                       g("q_raw"), g("x_in"), g("q"), g("k_raw"), g("lse"))
 
 
 def lora(t: dict, tag: str, grads: dict | None = None):

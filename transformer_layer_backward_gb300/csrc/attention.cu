@@ -17,27 +17,44 @@
 
 namespace tlb {
 
+constexpr int kT = 64;          // tile edge
+constexpr int kTP = kT + 4;     // padded row of a transposed tile (float4-aligned, 4-way store conflicts)
+
 __global__ void attn_rows_kernel(AttnArgs a, RopeFreqs fr) {
     extern __shared__ float4 smem4[];
     __shared__ float red[32];
     float *sS = reinterpret_cast<float *>(smem4);
     float *sd = sS + a.L;
     float *sq = sd + a.hd;
+    float *sqr = sq + a.hd;                      // recompute: the query row, then P[0 .. L)
+    float *sP = sqr + a.hd;
     const int i = blockIdx.x, h = blockIdx.y;
     const int kvh = h / (a.nh / a.nkv);
     const int q_dim = a.nh * a.hd;
     const int jmax = a.causal ? min(a.L, a.pos0 + i + 1) : a.L;
-    for (int d = threadIdx.x; d < a.hd; d += blockDim.x) sd[d] = a.dctx[int64_t(i) * q_dim + h * a.hd + d];
+    const bool rc = a.lse != nullptr;
+    for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
+        sd[d] = a.dctx[int64_t(i) * q_dim + h * a.hd + d];
+        if (rc) sqr[d] = a.q[int64_t(i) * q_dim + h * a.hd + d];
+    }
     __syncthreads();
     const float *Vh = a.v + int64_t(kvh) * a.sh;
     const float *Kh = a.k + int64_t(kvh) * a.sh;
+    const float lse = rc ? a.lse[int64_t(h) * a.S + i] : 0.f;
     for (int j = threadIdx.x; j < jmax; j += blockDim.x) {
         const float *vr = Vh + int64_t(j) * a.sp;
         float acc = 0.f;
         for (int d = 0; d < a.hd; ++d) acc = fmaf(sd[d], vr[d], acc);
         sS[j] = acc;
+        if (rc) {
+            const float *kr = Kh + int64_t(j) * a.sp;
+            float s = 0.f;
+            for (int d = 0; d < a.hd; ++d) s = fmaf(sqr[d], kr[d], s);
+            sP[j] = expf(a.scale * s - lse);
+        }
     }
-    const float *P = a.attn + (int64_t(h) * a.S + i) * a.L;
+    __syncthreads();
+    const float *P = rc ? sP : a.attn + (int64_t(h) * a.S + i) * a.L;
     float part = 0.f;
     for (int j = threadIdx.x; j < jmax; j += blockDim.x) part += P[j] * sS[j];
     const float D = block_sum(part, red);
@@ -83,6 +100,96 @@ __global__ void attn_dv_kernel(AttnArgs a) {
     }
 }
 
+// Recomputed attention: one block per (newest key jj, KV head), the P values of up to
+// blockDim (head, query) pairs at a time formed one pair per thread (scale q . k - lse),
+// then every thread adds their share of the pairs' dCtx rows into its head_dim columns.
+__global__ void attn_dv_rc_kernel(AttnArgs a) {
+    extern __shared__ float4 smem4[];
+    float *sK = reinterpret_cast<float *>(smem4);      // [hd] K row of the key
+    float *sPp = sK + a.hd;                            // [blockDim] P of the current pairs
+    const int jj = blockIdx.x, kvh = blockIdx.y, G = a.nh / a.nkv;
+    const int j = a.pos0 + jj, q_dim = a.nh * a.hd;
+    const int i0 = a.causal ? jj : 0;
+    const int nq = a.S - i0, npairs = G * nq;
+    const float *Kj = a.k + int64_t(kvh) * a.sh + int64_t(j) * a.sp;
+    for (int d = threadIdx.x; d < a.hd; d += blockDim.x) sK[d] = Kj[d];
+    constexpr int kMaxCols = 2;                        // head_dim <= 256, blockDim 128
+    float acc[kMaxCols] = {0.f, 0.f};
+    __syncthreads();
+    for (int p0 = 0; p0 < npairs; p0 += blockDim.x) {
+        const int pp = p0 + threadIdx.x;
+        float P = 0.f;
+        if (pp < npairs) {
+            const int h = kvh * G + pp / nq, i = i0 + pp % nq;
+            const float *qr = a.q + int64_t(i) * q_dim + h * a.hd;
+            float t = 0.f;
+            for (int d = 0; d < a.hd; ++d) t = fmaf(qr[d], sK[d], t);
+            P = expf(a.scale * t - a.lse[int64_t(h) * a.S + i]);
+        }
+        sPp[threadIdx.x] = P;
+        __syncthreads();
+        const int n = min(int(blockDim.x), npairs - p0);
+        for (int t = 0; t < n; ++t) {
+            const int pt = p0 + t;
+            const int h = kvh * G + pt / nq, i = i0 + pt % nq;
+            const float *dc = a.dctx + int64_t(i) * q_dim + h * a.hd;
+#pragma unroll
+            for (int k = 0; k < kMaxCols; ++k) {
+                const int d = threadIdx.x + k * blockDim.x;
+                if (d < a.hd) acc[k] = fmaf(sPp[t], dc[d], acc[k]);
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxCols; ++k) {
+        const int d = threadIdx.x + k * blockDim.x;
+        if (d < a.hd) a.dv[int64_t(jj) * a.nkv * a.hd + kvh * a.hd + d] = acc[k];
+    }
+}
+
+// Recomputed attention in the tiled kernels: the 4 x 4 micro-tile of P at query rows
+// 4 ty + r and keys 4 tx + c from transposed q and K tiles in shared memory.
+template <int HD>
+__device__ __forceinline__ void p_tile(const float *sQt, const float *sKt, const float (&lse)[4], float scale,
+                                       int q0, int j0, const AttnArgs &a, int tx, int ty, float (&pv)[4][4]) {
+    float s[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s[r][c] = 0.f;
+#pragma unroll 4
+    for (int d = 0; d < HD; ++d) {
+        const float4 qv = *reinterpret_cast<const float4 *>(sQt + d * kTP + 4 * ty);
+        const float4 kv = *reinterpret_cast<const float4 *>(sKt + d * kTP + 4 * tx);
+        const float qr[4] = {qv.x, qv.y, qv.z, qv.w}, kc[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s[r][c] = fmaf(qr[r], kc[c], s[r][c]);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = q0 + 4 * ty + r;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int j = j0 + 4 * tx + c;          // cache position
+            const bool vis = i < a.S && j < a.L && (!a.causal || j <= a.pos0 + i);
+            pv[r][c] = vis ? expf(scale * s[r][c] - lse[r]) : 0.f;
+        }
+    }
+}
+
+// [HD][kTP] transposed tile of rows r0 .. r0 + kT of src (row stride ld, head offset
+// already applied), zero past nrow.
+template <int HD>
+__device__ __forceinline__ void load_t(float *dst, const float *src, int64_t ld, int r0, int nrow, int tid) {
+    for (int e = tid; e < kT * HD; e += 256) {
+        const int i = e / HD, d = e % HD;
+        dst[d * kTP + i] = (r0 + i < nrow) ? src[int64_t(r0 + i) * ld + d] : 0.f;
+    }
+}
+
 // ------------------------------------------------------------------ tiled kernels
 
 // Tiled fp32 attention backward (64 x 64 tiles, 256 threads, 4 x 4 register tiles).
@@ -92,16 +199,16 @@ __global__ void attn_dv_kernel(AttnArgs a) {
 //   attn_dv_tiled: block = (64 of the S newest keys, KV head): dV = sum_group P^T dCtx.
 // With TLB_CAUSAL, key tiles past the last visible key of a query tile are skipped and the
 // masked entries inside a diagonal tile are read as zero, as in the per-row kernels.
-constexpr int kT = 64;          // tile edge
-constexpr int kTP = kT + 4;     // padded row of a transposed tile (float4-aligned, 4-way store conflicts)
 
-template <int HD>
+template <int HD, bool RC>
 __global__ void __launch_bounds__(256) attn_dq_tiled(AttnArgs a, RopeFreqs fr) {
     extern __shared__ float4 sm4[];
     float *sCt = reinterpret_cast<float *>(sm4);        // [HD][kTP]   dCtx tile, transposed
     float *sVt = sCt + HD * kTP;                        // [HD][kTP]   V tile, transposed
     float *sK = sVt + HD * kTP;                         // [kT][HD+4]  K tile
     float *sSt = sK + kT * (HD + 4);                    // [kT][kTP]   dS tile, transposed
+    float *sQt = sSt + kT * kTP;                        // RC: [HD][kTP] q tile, transposed
+    float *sKt = sQt + HD * kTP;                        // RC: [HD][kTP] K tile, transposed
     __shared__ float sD[kT];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int h = blockIdx.y, kvh = h / (a.nh / a.nkv);
@@ -116,7 +223,15 @@ __global__ void __launch_bounds__(256) attn_dq_tiled(AttnArgs a, RopeFreqs fr) {
         const int i = e / HD, d = e % HD;
         sCt[d * kTP + i] = (q0 + i < a.S) ? a.dctx[int64_t(q0 + i) * q_dim + h * HD + d] : 0.f;
     }
+    float lse[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (RC) {
+        load_t<HD>(sQt, a.q + h * HD, q_dim, q0, a.S, tid);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            lse[r] = q0 + 4 * ty + r < a.S ? a.lse[int64_t(h) * a.S + q0 + 4 * ty + r] : 0.f;
+    }
     auto load_vt = [&](int j0) {
+        if constexpr (RC) load_t<HD>(sKt, Kh, a.sp, j0, a.L, tid);
         for (int e = tid; e < kT * HD; e += 256) {
             const int j = e / HD, d = e % HD;
             sVt[d * kTP + j] = (j0 + j < a.L) ? Vh[int64_t(j0 + j) * a.sp + d] : 0.f;
@@ -140,6 +255,10 @@ __global__ void __launch_bounds__(256) attn_dq_tiled(AttnArgs a, RopeFreqs fr) {
         }
     };
     auto load_p = [&](int j0, float (&pv)[4][4]) {
+        if constexpr (RC) {
+            p_tile<HD>(sQt, sKt, lse, a.scale, q0, j0, a, tx, ty, pv);
+            return;
+        }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int i = q0 + 4 * ty + r;
@@ -243,11 +362,13 @@ __global__ void __launch_bounds__(256) attn_dq_tiled(AttnArgs a, RopeFreqs fr) {
     }
 }
 
-template <int HD>
+template <int HD, bool RC>
 __global__ void __launch_bounds__(256) attn_dv_tiled(AttnArgs a) {
     extern __shared__ float4 sm4[];
     float *sP = reinterpret_cast<float *>(sm4);         // [kT][kTP]   P tile [query][key]
     float *sC = sP + kT * kTP;                          // [kT][HD+4]  dCtx tile
+    float *sQt = sC + kT * (HD + 4);                    // RC: [HD][kTP] q tile, transposed
+    float *sKt = sQt + HD * kTP;                        // RC: [HD][kTP] K tile, transposed
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int kvh = blockIdx.y, G = a.nh / a.nkv;
     const int k0 = blockIdx.x * kT;                     // among the S newest keys
@@ -261,16 +382,32 @@ __global__ void __launch_bounds__(256) attn_dv_tiled(AttnArgs a) {
     // query i sees key pos0 + jj iff i >= jj: query tiles from the one holding row k0
     const int qt0 = a.causal ? k0 / kT : 0;
     const int nqt = (a.S + kT - 1) / kT;
+    if constexpr (RC) load_t<HD>(sKt, a.k + int64_t(kvh) * a.sh, a.sp, a.pos0 + k0, a.pos0 + a.S, tid);
     for (int g = 0; g < G; ++g) {
         const int h = kvh * G + g;
         const float *Ph = a.attn + int64_t(h) * a.S * a.L + a.pos0;
         for (int qt = qt0; qt < nqt; ++qt) {
             const int q0 = qt * kT;
             __syncthreads();
-            for (int e = tid; e < kT * kT; e += 256) {
-                const int i = e / kT, j = e % kT;
-                const bool vis = q0 + i < a.S && k0 + j < a.S && (!a.causal || q0 + i >= k0 + j);
-                sP[i * kTP + j] = vis ? Ph[int64_t(q0 + i) * a.L + k0 + j] : 0.f;
+            if constexpr (RC) {
+                load_t<HD>(sQt, a.q + h * HD, q_dim, q0, a.S, tid);
+                __syncthreads();
+                float lse[4], pv[4][4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    lse[r] = q0 + 4 * ty + r < a.S ? a.lse[int64_t(h) * a.S + q0 + 4 * ty + r] : 0.f;
+                p_tile<HD>(sQt, sKt, lse, a.scale, q0, a.pos0 + k0, a, tx, ty, pv);
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)    // keys past the S newest read as 0
+                        sP[(4 * ty + r) * kTP + 4 * tx + c] = k0 + 4 * tx + c < a.S ? pv[r][c] : 0.f;
+            } else {
+                for (int e = tid; e < kT * kT; e += 256) {
+                    const int i = e / kT, j = e % kT;
+                    const bool vis = q0 + i < a.S && k0 + j < a.S && (!a.causal || q0 + i >= k0 + j);
+                    sP[i * kTP + j] = vis ? Ph[int64_t(q0 + i) * a.L + k0 + j] : 0.f;
+                }
             }
             for (int e = tid; e < kT * HD; e += 256) {
                 const int i = e / HD, d = e % HD;
@@ -304,16 +441,24 @@ __global__ void __launch_bounds__(256) attn_dv_tiled(AttnArgs a) {
     }
 }
 
+template <int HD, bool RC>
+int launch_tiled_rc(const AttnArgs &a, const RopeFreqs &fr, cudaStream_t st) {
+    const size_t rc = RC ? size_t(2) * HD * kTP : 0;     // transposed q and K tiles
+    const size_t smq = (size_t(2) * HD * kTP + size_t(kT) * (HD + 4) + size_t(kT) * kTP + rc) * 4;
+    const size_t smv = (size_t(kT) * kTP + size_t(kT) * (HD + 4) + rc) * 4;
+    if (smq > 48 * 1024)
+        TLB_CUDA(cudaFuncSetAttribute(attn_dq_tiled<HD, RC>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smq)));
+    if (smv > 48 * 1024)
+        TLB_CUDA(cudaFuncSetAttribute(attn_dv_tiled<HD, RC>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smv)));
+    attn_dq_tiled<HD, RC><<<dim3(unsigned(ceil_div(a.S, kT)), unsigned(a.nh)), 256, smq, st>>>(a, fr);
+    TLB_TRY(check_launch("attn_dq_tiled"));
+    attn_dv_tiled<HD, RC><<<dim3(unsigned(ceil_div(a.S, kT)), unsigned(a.nkv)), 256, smv, st>>>(a);
+    return check_launch("attn_dv_tiled");
+}
+
 template <int HD>
 int launch_tiled(const AttnArgs &a, const RopeFreqs &fr, cudaStream_t st) {
-    const size_t smq = (size_t(2) * HD * kTP + size_t(kT) * (HD + 4) + size_t(kT) * kTP) * 4;
-    const size_t smv = (size_t(kT) * kTP + size_t(kT) * (HD + 4)) * 4;
-    if (smq > 48 * 1024) TLB_CUDA(cudaFuncSetAttribute(attn_dq_tiled<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smq)));
-    if (smv > 48 * 1024) TLB_CUDA(cudaFuncSetAttribute(attn_dv_tiled<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smv)));
-    attn_dq_tiled<HD><<<dim3(unsigned(ceil_div(a.S, kT)), unsigned(a.nh)), 256, smq, st>>>(a, fr);
-    TLB_TRY(check_launch("attn_dq_tiled"));
-    attn_dv_tiled<HD><<<dim3(unsigned(ceil_div(a.S, kT)), unsigned(a.nkv)), 256, smv, st>>>(a);
-    return check_launch("attn_dv_tiled");
+    return a.lse != nullptr ? launch_tiled_rc<HD, true>(a, fr, st) : launch_tiled_rc<HD, false>(a, fr, st);
 }
 
 int attn_core_launch(const AttnArgs &a, float rope_base, cudaStream_t st) {
@@ -325,13 +470,17 @@ int attn_core_launch(const AttnArgs &a, float rope_base, cudaStream_t st) {
         if (a.hd == 64) return launch_tiled<64>(a, fr, st);
         if (a.hd == 32) return launch_tiled<32>(a, fr, st);
     }
-    const size_t smem = (size_t(a.L) + 2 * size_t(a.hd)) * sizeof(float);
+    const size_t smem = (size_t(a.L) + 2 * size_t(a.hd) + (a.lse != nullptr ? size_t(a.L) + a.hd : 0)) * sizeof(float);
     TLB_REQUIRE(smem <= 200 * 1024, TLB_EUNSUPPORTED, "attn_backward: cache length %d too long", a.L);
     if (smem > 48 * 1024)
         TLB_CUDA(cudaFuncSetAttribute(attn_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       int(smem)));
     attn_rows_kernel<<<dim3(a.S, a.nh), 128, smem, st>>>(a, fr);
     TLB_TRY(check_launch("attn_rows"));
+    if (a.lse != nullptr) {
+        attn_dv_rc_kernel<<<dim3(a.S, a.nkv), 128, (size_t(a.hd) + 128) * 4, st>>>(a);
+        return check_launch("attn_dv_rc");
+    }
     attn_dv_kernel<<<dim3(a.S, a.nkv), a.hd < 128 ? a.hd : 128, 0, st>>>(a);
     return check_launch("attn_dv");
 }
@@ -352,7 +501,13 @@ __global__ void attn_dk_rows_kernel(AttnArgs a, const float *__restrict__ q, con
     const int i0 = a.causal ? jj : 0;                   // query i sees key pos0 + jj iff i >= jj
     const int nq = a.S - i0, npairs = G * nq;
     const float *Vj = a.v + int64_t(kvh) * a.sh + int64_t(j) * a.sp;
-    for (int d = threadIdx.x; d < a.hd; d += blockDim.x) sV[d] = Vj[d];
+    const float *Kj = a.k + int64_t(kvh) * a.sh + int64_t(j) * a.sp;
+    float *sK = sDs + blockDim.x;                      // recompute: [hd] K row of the key
+    const bool rc = a.lse != nullptr;
+    for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
+        sV[d] = Vj[d];
+        if (rc) sK[d] = Kj[d];
+    }
     constexpr int kMaxCols = 2;                         // head_dim <= 256, blockDim >= 128
     float acc[kMaxCols] = {0.f, 0.f};
     __syncthreads();
@@ -361,7 +516,15 @@ __global__ void attn_dk_rows_kernel(AttnArgs a, const float *__restrict__ q, con
         float ds = 0.f;
         if (pp < npairs) {
             const int h = kvh * G + pp / nq, i = i0 + pp % nq;
-            const float P = a.attn[(int64_t(h) * a.S + i) * a.L + j];
+            float P;
+            if (rc) {
+                const float *qr = q + int64_t(i) * q_dim + h * a.hd;
+                float t = 0.f;
+                for (int d = 0; d < a.hd; ++d) t = fmaf(qr[d], sK[d], t);
+                P = expf(a.scale * t - a.lse[int64_t(h) * a.S + i]);
+            } else {
+                P = a.attn[(int64_t(h) * a.S + i) * a.L + j];
+            }
             const float *dc = a.dctx + int64_t(i) * q_dim + h * a.hd;
             float t = 0.f;
             for (int d = 0; d < a.hd; ++d) t = fmaf(dc[d], sV[d], t);
@@ -394,7 +557,7 @@ __global__ void attn_dk_rows_kernel(AttnArgs a, const float *__restrict__ q, con
 // head of the group and query tile: T = dCtx V^T on the tile (4 x 4 per thread, from
 // transposed tiles so that each step is two 16-byte shared loads), dS = P (T - D) in
 // shared memory, then dK += dS^T q (4 keys x HD/16 columns per thread).
-template <int HD>
+template <int HD, bool RC>
 __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__restrict__ q,
                                                      const float *__restrict__ Dv, float *dk) {
     extern __shared__ float4 sm4[];
@@ -402,6 +565,8 @@ __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__
     float *sCt = sVt + HD * kTP;                        // [HD][kTP]   dCtx tile, transposed
     float *sQ = sCt + HD * kTP;                         // [kT][HD+4]  q tile [query][d]
     float *sS = sQ + kT * (HD + 4);                     // [kT][kTP]   dS tile [query][key]
+    float *sQt = sS + kT * kTP;                         // RC: [HD][kTP] q tile, transposed
+    float *sKt = sQt + HD * kTP;                        // RC: [HD][kTP] K rows of the key tile, transposed
     __shared__ float sDq[kT];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int kvh = blockIdx.y, G = a.nh / a.nkv, g = blockIdx.z;   // one head of the group per block
@@ -420,6 +585,7 @@ __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__
         for (int c = 0; c < CPT; ++c) acc[r][c] = 0.f;
     const int qt0 = a.causal ? k0 / kT : 0;
     const int nqt = (a.S + kT - 1) / kT;
+    if constexpr (RC) load_t<HD>(sKt, a.k + int64_t(kvh) * a.sh, a.sp, a.pos0 + k0, a.pos0 + a.S, tid);
     {
         const int h = kvh * G + g;
         const float *Ph = a.attn + int64_t(h) * a.S * a.L + a.pos0;
@@ -433,7 +599,16 @@ __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__
                 sQ[i * (HD + 4) + d] = in ? q[int64_t(q0 + i) * q_dim + h * HD + d] : 0.f;
             }
             if (tid < kT) sDq[tid] = q0 + tid < a.S ? Dv[int64_t(h) * a.S + q0 + tid] : 0.f;
+            if constexpr (RC) load_t<HD>(sQt, q + h * HD, q_dim, q0, a.S, tid);
             __syncthreads();
+            float pv[4][4];
+            if constexpr (RC) {
+                float lse[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    lse[r] = q0 + 4 * ty + r < a.S ? a.lse[int64_t(h) * a.S + q0 + 4 * ty + r] : 0.f;
+                p_tile<HD>(sQt, sKt, lse, a.scale, q0, a.pos0 + k0, a, tx, ty, pv);
+            }
             // T[i][j] for query rows 4 ty + r and keys 4 tx + c
             float t[4][4];
 #pragma unroll
@@ -457,7 +632,9 @@ __global__ void __launch_bounds__(256) attn_dk_tiled(AttnArgs a, const float *__
                 for (int c = 0; c < 4; ++c) {
                     const int jk = k0 + 4 * tx + c;
                     const bool vis = i < a.S && jk < a.S && (!a.causal || i >= jk);
-                    const float P = vis ? Ph[int64_t(i) * a.L + jk] : 0.f;
+                    float P;
+                    if constexpr (RC) P = jk < a.S ? pv[r][c] : 0.f;
+                    else P = vis ? Ph[int64_t(i) * a.L + jk] : 0.f;
                     sS[(4 * ty + r) * kTP + 4 * tx + c] = P * (t[r][c] - sDq[4 * ty + r]);
                 }
             }
@@ -500,14 +677,23 @@ __global__ void attn_dk_sum_kernel(const float *__restrict__ part, float *dk, in
     }
 }
 
+template <int HD, bool RC>
+int launch_dk_tiled_rc(const AttnArgs &a, const float *q, const float *D, float *dst, cudaStream_t st) {
+    const int G = a.nh / a.nkv;
+    const size_t sm = (size_t(RC ? 4 : 2) * HD * kTP + size_t(kT) * (HD + 4) + size_t(kT) * kTP) * 4;
+    if (sm > 48 * 1024)
+        TLB_CUDA(cudaFuncSetAttribute(attn_dk_tiled<HD, RC>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)));
+    attn_dk_tiled<HD, RC><<<dim3(unsigned(ceil_div(a.S, kT)), unsigned(a.nkv), unsigned(G)), 256, sm, st>>>(a, q, D,
+                                                                                                          dst);
+    return check_launch("attn_dk_tiled");
+}
+
 template <int HD>
 int launch_dk_tiled(const AttnArgs &a, const float *q, const float *D, float *dk, float *part, cudaStream_t st) {
     const int G = a.nh / a.nkv;
-    const size_t sm = (size_t(2) * HD * kTP + size_t(kT) * (HD + 4) + size_t(kT) * kTP) * 4;
-    if (sm > 48 * 1024) TLB_CUDA(cudaFuncSetAttribute(attn_dk_tiled<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)));
     float *dst = G > 1 ? part : dk;
-    attn_dk_tiled<HD><<<dim3(unsigned(ceil_div(a.S, kT)), unsigned(a.nkv), unsigned(G)), 256, sm, st>>>(a, q, D, dst);
-    TLB_TRY(check_launch("attn_dk_tiled"));
+    if (a.lse != nullptr) TLB_TRY((launch_dk_tiled_rc<HD, true>(a, q, D, dst, st)));
+    else TLB_TRY((launch_dk_tiled_rc<HD, false>(a, q, D, dst, st)));
     if (G == 1) return TLB_OK;
     const int64_t n = int64_t(a.S) * a.nkv * HD;
     attn_dk_sum_kernel<<<stream_grid(n, 256), 256, 0, st>>>(part, dk, n, G);
@@ -526,7 +712,7 @@ int attn_dk_launch(const AttnArgs &a, const float *q, const float *D, float *dk,
         if (a.hd == 32) return launch_dk_tiled<32>(a, q, D, dk, part, st);
     }
     const int threads = 128;
-    attn_dk_rows_kernel<<<dim3(unsigned(a.S), unsigned(a.nkv)), threads, (size_t(a.hd) + threads) * 4, st>>>(
+    attn_dk_rows_kernel<<<dim3(unsigned(a.S), unsigned(a.nkv)), threads, (size_t(2 * a.hd) + threads) * 4, st>>>(
         a, q, D, dk);
     return check_launch("attn_dk_rows");
 }

@@ -75,6 +75,10 @@ struct AttnArgs {
     int S, L, nh, nkv, hd, pos0, causal, rope;
     float scale;
     float *D = nullptr;      // [nh, S] (optional): D[h, i] = sum_j attn[h,i,j] dAttn[h,i,j]
+    // Recomputed attention (lse != NULL; attn unused): attn[h,i,j] = exp(scale <q[i,h,:],
+    // k[j,kvh,:]> - lse[h,i]) on the visible keys, q [S, q_dim] the queries after RoPE.
+    const float *q = nullptr;
+    const float *lse = nullptr;   // [nh, S] logsumexp of each query row's scaled logits
 };
 int attn_core_launch(const AttnArgs &a, float rope_base, cudaStream_t st);
 // Key gradient of the S newest cache rows (the keys of the call's own tokens), for the

@@ -33,7 +33,8 @@ bool tc_route(const tlb_layer_cfg &c, int64_t S) {
 // With bf16 weights the sequence attention contractions run on tcgen05 too (tf32
 // operands); fp32 and ternary layers keep the fp32 CUDA-core kernels.
 bool attn_tc_route(const tlb_layer_cfg &c, int64_t S, int64_t L) {
-    return c.wtype == TLB_W_BF16 && attn_tc_supported(S, L, c.n_heads, c.n_kv_heads, c.head_dim);
+    return c.wtype == TLB_W_BF16 && !(c.flags & TLB_RECOMPUTE_P) &&
+           attn_tc_supported(S, L, c.n_heads, c.n_kv_heads, c.head_dim);
 }
 
 LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
@@ -219,6 +220,8 @@ AttnArgs attn_args(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dc
     g.rope = (c.flags & TLB_ROPE) ? 1 : 0;
     g.scale = c.attn_scale;
     g.D = nullptr;
+    g.q = a.q;
+    g.lse = (c.flags & TLB_RECOMPUTE_P) ? a.lse : nullptr;
     return g;
 }
 
@@ -350,7 +353,11 @@ int check_acts_attn(const tlb_layer_cfg &c, int64_t S, int64_t L, const tlb_laye
     TLB_REQUIRE(w && a, TLB_EINVAL, "weights / activations struct is NULL");
     TLB_REQUIRE(L >= S && S >= 0, TLB_EINVAL, "need 0 <= S <= L (S=%lld, L=%lld)", (long long)S, (long long)L);
     TLB_REQUIRE(L < (int64_t(1) << 24), TLB_EUNSUPPORTED, "cache length >= 2^24");
-    TLB_REQUIRE(w->w_o.w && a->k && a->v && a->attn, TLB_EINVAL, "W_O / K / V / attn pointer is NULL");
+    TLB_REQUIRE(w->w_o.w && a->k && a->v, TLB_EINVAL, "W_O / K / V pointer is NULL");
+    if (c.flags & TLB_RECOMPUTE_P)
+        TLB_REQUIRE(a->q && a->lse, TLB_EINVAL, "RECOMPUTE_P needs q and lse");
+    else
+        TLB_REQUIRE(a->attn, TLB_EINVAL, "attn pointer is NULL");
     TLB_REQUIRE(a->kv_stride_pos >= c.head_dim && a->kv_stride_head >= c.head_dim, TLB_EINVAL,
                 "K/V strides smaller than head_dim");
     if (c.flags & TLB_SUB_NORM)
@@ -375,7 +382,8 @@ int check_adam(const tlb_adamw_cfg *a) {
 // The single-token kernels read every vector with 16-byte loads.
 bool decode_route(const tlb_layer_cfg &c, int64_t S, int64_t L, const tlb_layer_weights *w,
                   const tlb_layer_acts *acts, const float *d_hidden) {
-    if (!decode_supported(c, S, L)) return false;
+    // the single-token kernels read the cached attention row
+    if (!decode_supported(c, S, L) || (c.flags & TLB_RECOMPUTE_P)) return false;
     for (const void *ptr : {(const void *)w->w_down.w, (const void *)w->w_gate.w, (const void *)w->w_up.w,
                             (const void *)w->w_o.w, (const void *)w->gamma_sub_ffn, (const void *)w->gamma_ffn,
                             (const void *)w->gamma_sub_attn, (const void *)acts->gate, (const void *)acts->up,
