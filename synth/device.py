@@ -73,9 +73,9 @@ def device_layer(cfg, layer, seed=0):
         t["q"] = n(S, qd)
         kh = t["k"].view(L, cfg.n_kv_heads, cfg.head_dim)
         lse = torch.empty(cfg.n_heads, S, device="cuda")
-        g = cfg.n_heads // cfg.n_kv_heads
+        grp = cfg.n_heads // cfg.n_kv_heads
         for h in range(cfg.n_heads):
-            z = cfg.attn_scale * t["q"][:, h * cfg.head_dim:(h + 1) * cfg.head_dim] @ kh[:, h // g, :].t()
+            z = cfg.attn_scale * t["q"][:, h * cfg.head_dim:(h + 1) * cfg.head_dim] @ kh[:, h // grp, :].t()
             lse[h] = torch.logsumexp(z.masked_fill_(mask, float("-inf")), dim=-1)
         t["lse"] = lse
     else:
