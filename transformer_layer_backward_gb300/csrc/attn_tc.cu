@@ -647,6 +647,257 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_tc_dv_kernel(const __gri
     }
 }
 
+// ------------------------------------------------------------------ dK (exact input gradient)
+
+// Key gradient of the S newest keys for the exact layer-input gradient: per head h and
+// tile of 128 keys, over 32-query items w (causal: from the first item that sees key k0),
+//   T^T_w = V_tile dCtx_w^T          tcgen05.mma, both operands in shared memory (V once)
+//   dS^T  = P^T (.) (T^T - D_w)       writer warps, tf32 into tensor memory
+//   dK   += dS^T q_w                  tcgen05.mma, A from tensor memory, q^T tile as B
+// then scale dK (per-head partials added in head order when the group has several heads).
+// A ring slot holds one item's P tile (4 boxes of 32 keys), tf32 dCtx rows and q^T tile,
+// filled by one transaction and freed by ten arrivals: the eight writer warps once they
+// have read P, and the commits of the item's two MMAs.  T^T_w+2 may take T^T_w's buffer as
+// soon as the writers have read it; dS^T_w+2 waits for the dK MMA of item w.
+template <int HD>
+struct DkLayout {
+    static constexpr int NB = HD / 32;                       // 128-byte atoms along head_dim
+    static constexpr int V_BYTES = kVK * HD * 4;             // V tile [128 keys][HD], NB atoms
+    static constexpr int P_BYTES = kVQ * kVK * 4;            // P item [32 queries][128 keys], 4 boxes
+    static constexpr int C_BYTES = kVQ * HD * 4;             // dCtx rows [32 queries][HD], NB atoms
+    static constexpr int Q_BYTES = HD * kVQ * 4;             // q^T [HD][32 queries], one atom
+    static constexpr int SLOT = P_BYTES + C_BYTES + Q_BYTES;
+    static constexpr int NS = 3;
+    static constexpr int S0 = V_BYTES, TOTAL = V_BYTES + NS * SLOT;
+    __host__ __device__ static constexpr int P(int s) { return S0 + s * SLOT; }
+    __host__ __device__ static constexpr int C(int s) { return S0 + s * SLOT + P_BYTES; }
+    __host__ __device__ static constexpr int Q(int s) { return S0 + s * SLOT + P_BYTES + C_BYTES; }
+    // tensor memory: dK [128 keys][HD], then T^T and dS^T double buffers [128 keys][32]
+    static constexpr uint32_t TT = HD, TS = HD + 2 * kVQ;
+    static constexpr uint32_t COLS = (HD + 4 * kVQ) <= 256 ? 256 : 512;
+};
+
+struct AttnTcDkParams {
+    CUtensorMap v;              // Vr  {hd, L, nkv},   box {32, 128, 1}
+    CUtensorMap pv;             // attn {L, S, nh},    box {32, 32, 1}
+    CUtensorMap dcr;            // dCR {hd, nh, S},    box {32, 1, 32}  (tf32 dCtx rows)
+    CUtensorMap qt;             // QT  {S, hd, nh},    box {32, hd, 1}  (tf32 q, transposed)
+    const float *D;             // [nh, S]
+    float *dk;                  // [S, nkv * hd], or per-head partials [nh / nkv][S, nkv * hd]
+    int S, L, nh, nkv, pos0, causal;
+    float scale;
+    uint32_t *status;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __grid_constant__ AttnTcDkParams p) {
+    using Ly = DkLayout<HD>;
+    constexpr int NS = Ly::NS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    __shared__ uint64_t vfull, full[NS], sfree[NS], tfull[2], tfree[2], afull[2], afree[2], dfull;
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_abort, s_issued, s_used;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x, G = p.nh / p.nkv, kvh = h / G, g = h % G;
+    const int k0 = int(gridDim.y - 1 - blockIdx.y) * kVK;    // among the S newest keys (heaviest first)
+    const int t0 = p.causal ? k0 / kVQ : 0;                   // first query item that sees key k0
+    const int nw = (p.S + kVQ - 1) / kVQ - t0;
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        s_issued = s_used = 0;
+        mbar_init(&vfull, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&sfree[s], kEpiWarps + 2);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tfree[b], kEpiWarps);
+            mbar_init(&afull[b], kEpiWarps);
+            mbar_init(&afree[b], 1);
+        }
+        mbar_init(&dfull, 1);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, Ly::COLS);
+        tmem_relinquish();
+    }
+    fence_mbar_init();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tD = tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer: V once, then NS items ahead
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&vfull, Ly::V_BYTES);
+            for (int b = 0; b < Ly::NB; ++b)
+                tma_load_3d(sm + b * (kVK * 128), &p.v, b * 32, p.pos0 + k0, kvh, &vfull);
+            for (int w = 0; w < nw; ++w) {
+                const int s = w % NS, qa = (t0 + w) * kVQ;
+                if (w >= NS && !mbar_wait(&sfree[s], (w / NS - 1) & 1, p.status, 40u)) { s_abort = 1; break; }
+                mbar_arrive_expect_tx(&full[s], Ly::SLOT);
+                for (int b = 0; b < kVK / 32; ++b)
+                    tma_load_3d(sm + Ly::P(s) + b * (kVQ * 128), &p.pv, p.pos0 + k0 + b * 32, qa, h, &full[s]);
+                for (int b = 0; b < Ly::NB; ++b)
+                    tma_load_3d(sm + Ly::C(s) + b * (kVQ * 128), &p.dcr, b * 32, h, qa, &full[s]);
+                tma_load_3d(sm + Ly::Q(s), &p.qt, qa, 0, h, &full[s]);
+                s_issued = w + 1;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_t = idesc_tf32(kVK, kVQ), id_k = idesc_tf32(kVK, HD);
+            auto mma_t = [&](int w) -> bool {              // T^T[w % 2] = V dCtx_w^T
+                const int s = w % NS;
+                if (!mbar_wait(&full[s], (w / NS) & 1, p.status, 41u)) return false;
+                s_used = w + 1;
+                tc_fence_after();
+#pragma unroll
+                for (int kb = 0; kb < Ly::NB; ++kb)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_tf32(tD + Ly::TT + uint32_t((w & 1) * kVQ), sw128_desc(sm + kb * (kVK * 128)) + 2 * k,
+                                 sw128_desc(sm + Ly::C(s) + kb * (kVQ * 128)) + 2 * k, id_t, (kb | k) ? 1u : 0u);
+                mma_commit(&sfree[s]);
+                mma_commit(&tfull[w & 1]);
+                return true;
+            };
+            bool ok = mbar_wait(&vfull, 0, p.status, 42u);
+            tc_fence_after();
+            ok = ok && (nw < 1 || mma_t(0)) && (nw < 2 || mma_t(1));
+            for (int w = 0; ok && w < nw; ++w) {
+                const int s = w % NS;
+                if (!mbar_wait(&afull[w & 1], (w >> 1) & 1, p.status, 43u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t qd = sw128_desc(sm + Ly::Q(s));
+#pragma unroll
+                for (int k = 0; k < kVQ / 8; ++k)
+                    mma_tf32_ts(tD, tD + Ly::TS + uint32_t((w & 1) * kVQ + 8 * k), qd + 2 * k, id_k,
+                                (w > 0 || k > 0) ? 1u : 0u);
+                mma_commit(&sfree[s]);
+                mma_commit(&afree[w & 1]);
+                // T^T_w+2 takes T^T_w's buffer: the writers read it before they filled dS^T_w
+                if (w + 2 < nw) {
+                    if (!mbar_wait(&tfree[w & 1], (w >> 1) & 1, p.status, 44u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (!(ok = mma_t(w + 2))) break;
+                }
+            }
+            if (!ok) s_abort = 1;
+            mma_commit(&dfull);
+            mbar_wait(&dfull, 0, nullptr, 0u);
+        }
+    } else {
+        // ------------------------------------------------ dS^T writers, then the dK epilogue:
+        // one key row (tensor-memory lane) and half of an item's queries per thread
+        constexpr int HQ = kVQ / 2;
+        const int quarter = warp & 3, hf = (warp - 2) >> 2;
+        const int r = quarter * 32 + lane, jj = k0 + r;        // key row of this thread
+        const bool key_ok = jj < p.S;
+        const int box = r >> 5, col = r & 31;
+        const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+        bool ok = true;
+        for (int w = 0; w < nw; ++w) {
+            const int s = w % NS, qa = (t0 + w) * kVQ + hf * HQ;
+            if (!mbar_wait(&full[s], (w / NS) & 1, p.status, 45u) ||
+                !mbar_wait(&tfull[w & 1], (w >> 1) & 1, p.status, 46u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t t[HQ];
+            tmem_ld16(tD + Ly::TT + uint32_t((w & 1) * kVQ + hf * HQ) + lane_off, t);
+            const uint8_t *ps = sm + Ly::P(s) + box * (kVQ * 128) + (col & 3) * 4;
+            float pv[HQ], dv[HQ];
+#pragma unroll
+            for (int qq = 0; qq < HQ; ++qq) {
+                pv[qq] = *reinterpret_cast<const float *>(ps + sw128_off(hf * HQ + qq, col >> 2));
+                dv[qq] = qa + qq < p.S ? __ldg(p.D + int64_t(h) * p.S + qa + qq) : 0.f;
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&tfree[w & 1]);                     // T^T_w read
+                mbar_arrive(&sfree[s]);                         // P read
+            }
+            uint32_t ds[HQ];
+#pragma unroll
+            for (int qq = 0; qq < HQ; ++qq) {
+                const bool vis = key_ok && qa + qq < p.S && (!p.causal || qa + qq >= jj);
+                ds[qq] = to_tf32(vis ? pv[qq] * (__uint_as_float(t[qq]) - dv[qq]) : 0.f);
+            }
+            if (w >= 2 && !mbar_wait(&afree[w & 1], ((w - 2) >> 1) & 1, p.status, 47u)) { ok = false; break; }
+            tc_fence_after();
+            tmem_st16(tD + Ly::TS + uint32_t((w & 1) * kVQ + hf * HQ) + lane_off, ds);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[w & 1]);
+        }
+        if (ok && mbar_wait(&dfull, 0, p.status, 48u)) {
+            tc_fence_after();
+            // every copy into the ring has been consumed: each warp turns its 32 x 32 blocks
+            // in the first slot so that the stores coalesce
+            float *blk = reinterpret_cast<float *>(sm + Ly::P(0)) + (warp - 2) * 32 * 33;
+            const int64_t kvd = int64_t(p.nkv) * HD;
+            float *out = p.dk + (G > 1 ? int64_t(g) * p.S * kvd : 0) + kvh * HD;
+            const int c4 = (lane & 7) * 4, rl = lane >> 3;
+#pragma unroll 1
+            for (int c = hf * (HD / 2); c < (hf + 1) * (HD / 2); c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tD + uint32_t(c) + lane_off, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 32; ++q) blk[lane * 33 + q] = p.scale * __uint_as_float(v[q]);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int rr = 4 * k + rl, key = k0 + quarter * 32 + rr;
+                    const float *a = blk + rr * 33 + c4;
+                    if (key < p.S)
+                        *reinterpret_cast<float4 *>(out + int64_t(key) * kvd + c + c4) =
+                            make_float4(a[0], a[1], a[2], a[3]);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok) s_abort = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (s_abort && threadIdx.x == 0) {
+        // the copies issued but not yet consumed (at most NS of them, and V)
+        mbar_wait(&vfull, 0, nullptr, 0u);
+        for (int w = max(s_used, s_issued - NS); w < s_issued; ++w) mbar_wait(&full[w % NS], (w / NS) & 1, nullptr, 0u);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tD, Ly::COLS);
+    }
+}
+
+// dst = tf32 (round to nearest) copy of src, n floats (n % 4 == 0, 16-byte aligned)
+__global__ void tf32_copy_kernel(const float4 *__restrict__ src, float4 *__restrict__ dst, int64_t n4) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
+        const float4 x = src[i];
+        dst[i] = make_float4(__uint_as_float(to_tf32(x.x)), __uint_as_float(to_tf32(x.y)), __uint_as_float(to_tf32(x.z)),
+                             __uint_as_float(to_tf32(x.w)));
+    }
+}
+
 // dV[jj, c] = sum over the group's heads g (in order) of part[g][jj, c]
 __global__ void attn_tc_dv_sum_kernel(const float4 *__restrict__ part, float4 *__restrict__ dv, int64_t n4, int G) {
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -772,6 +1023,74 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     return check_launch("attn_tc_dv_sum");
 }
 
+template <int HD>
+int launch_attn_tc_dk(const AttnArgs &a, const float *q, const float *D, float *dk, void *scratch, void *extra,
+                      uint32_t *status, cudaStream_t st) {
+    const TcAttnWs w = tc_attn_layout(a.S, a.L, a.nh, a.nkv, HD);
+    char *base = static_cast<char *>(scratch);
+    const float *Vr = reinterpret_cast<const float *>(base + w.Vr);     // left by the attention prep
+    float *part = reinterpret_cast<float *>(base + w.part);
+    const int64_t qd = int64_t(a.nh) * HD;
+    float *dCR = static_cast<float *>(extra);                            // [S, qd] tf32 dCtx
+    float *QT = dCR + ((a.S * qd + 63) & ~int64_t(63));                  // [qd, S4] tf32 q, transposed
+    const int64_t n4 = a.S * qd / 4;
+    tf32_copy_kernel<<<stream_grid(n4, 256), 256, 0, st>>>(reinterpret_cast<const float4 *>(a.dctx),
+                                                           reinterpret_cast<float4 *>(dCR), n4);
+    TLB_TRY(check_launch("tf32_copy"));
+    AttnArgs aq = a;               // the prep's first job transposes its dctx rows: give it q
+    aq.dctx = q;
+    const int nt_q = int(ceil_div(a.S, kPrepT)) * int(qd / kPrepT);
+    attn_tc_prep_kernel<<<unsigned(nt_q), 256, 0, st>>>(aq, QT, nullptr, nullptr, int(w.S4), int(w.L4), nt_q, 0, 0);
+    TLB_TRY(check_launch("attn_tc_prep_q"));
+
+    AttnTcDkParams p;
+    memset(&p, 0, sizeof(p));
+    {
+        const uint64_t d[3] = {uint64_t(HD), uint64_t(a.L), uint64_t(a.nkv)};
+        const uint64_t s[2] = {uint64_t(HD) * 4, uint64_t(a.L) * HD * 4};
+        const uint32_t b[3] = {32, uint32_t(kVK), 1};
+        TLB_TRY(make_map_f32_3d(&p.v, Vr, d, s, b));
+    }
+    {
+        const uint64_t d[3] = {uint64_t(a.L), uint64_t(a.S), uint64_t(a.nh)};
+        const uint64_t s[2] = {uint64_t(a.L) * 4, uint64_t(a.S) * a.L * 4};
+        const uint32_t b[3] = {32, uint32_t(kVQ), 1};
+        TLB_TRY(make_map_f32_3d(&p.pv, a.attn, d, s, b));
+    }
+    {
+        const uint64_t d[3] = {uint64_t(HD), uint64_t(a.nh), uint64_t(a.S)};
+        const uint64_t s[2] = {uint64_t(HD) * 4, uint64_t(qd) * 4};
+        const uint32_t b[3] = {32, 1, uint32_t(kVQ)};
+        TLB_TRY(make_map_f32_3d(&p.dcr, dCR, d, s, b));
+    }
+    {
+        const uint64_t d[3] = {uint64_t(a.S), uint64_t(HD), uint64_t(a.nh)};
+        const uint64_t s[2] = {uint64_t(w.S4) * 4, uint64_t(w.S4) * HD * 4};
+        const uint32_t b[3] = {32, uint32_t(HD), 1};
+        TLB_TRY(make_map_f32_3d(&p.qt, QT, d, s, b));
+    }
+    const int G = a.nh / a.nkv;
+    p.D = D;
+    p.dk = G > 1 ? part : dk;
+    p.S = a.S;
+    p.L = a.L;
+    p.nh = a.nh;
+    p.nkv = a.nkv;
+    p.pos0 = a.pos0;
+    p.causal = a.causal;
+    p.scale = a.scale;
+    p.status = status;
+    const int sm = DkLayout<HD>::TOTAL + 1024;
+    TLB_CUDA(cudaFuncSetAttribute(attn_tc_dk_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm));
+    attn_tc_dk_kernel<HD><<<dim3(unsigned(a.nh), unsigned(ceil_div(a.S, kVK))), kAttnThreads, sm, st>>>(p);
+    TLB_TRY(check_launch("attn_tc_dk"));
+    if (G == 1) return TLB_OK;
+    const int64_t m4 = int64_t(a.S) * a.nkv * HD / 4;
+    attn_tc_dv_sum_kernel<<<stream_grid(m4, 256), 256, 0, st>>>(reinterpret_cast<const float4 *>(part),
+                                                                reinterpret_cast<float4 *>(dk), m4, G);
+    return check_launch("attn_tc_dk_sum");
+}
+
 }  // namespace
 
 bool attn_tc_supported(int64_t S, int64_t L, int nh, int nkv, int hd) {
@@ -782,6 +1101,21 @@ bool attn_tc_supported(int64_t S, int64_t L, int nh, int nkv, int hd) {
 
 size_t attn_tc_bytes(int64_t S, int64_t L, int nh, int nkv, int hd) {
     return tc_attn_layout(S, L, nh, nkv, hd).total;
+}
+
+size_t attn_tc_dk_bytes(int64_t S, int nh, int hd) {
+    const int64_t qd = int64_t(nh) * hd, S4 = (S + 3) & ~int64_t(3);
+    return size_t((S * qd + 63) & ~int64_t(63)) * 4 + size_t(qd) * S4 * 4;
+}
+
+int attn_tc_dk_launch(const AttnArgs &a, const float *q, const float *D, float *dk, void *scratch, void *extra,
+                      uint32_t *status, cudaStream_t st) {
+    if (a.S == 0) return TLB_OK;
+    TLB_REQUIRE(attn_tc_supported(a.S, a.L, a.nh, a.nkv, a.hd), TLB_EUNSUPPORTED, "key gradient (tcgen05): shape");
+    TLB_REQUIRE(aligned16(q) && aligned16(dk) && aligned16(a.dctx) && aligned16(extra), TLB_EUNSUPPORTED,
+                "key gradient (tcgen05): q / dk / dctx / scratch not 16-byte aligned");
+    return a.hd == 128 ? launch_attn_tc_dk<128>(a, q, D, dk, scratch, extra, status, st)
+                       : launch_attn_tc_dk<64>(a, q, D, dk, scratch, extra, status, st);
 }
 
 int attn_tc_launch(const AttnArgs &a, float rope_base, void *scratch, uint32_t *status, cudaStream_t st) {

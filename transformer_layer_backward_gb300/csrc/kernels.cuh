@@ -95,6 +95,12 @@ int attn_dk_launch(const AttnArgs &a, const float *q, const float *D, float *dk,
 bool attn_tc_supported(int64_t S, int64_t L, int nh, int nkv, int hd);
 size_t attn_tc_bytes(int64_t S, int64_t L, int nh, int nkv, int hd);
 int attn_tc_launch(const AttnArgs &a, float rope_base, void *scratch, uint32_t *status, cudaStream_t st);
+// Key gradient of the S newest keys on tcgen05 (the exact input gradient), after
+// attn_tc_launch on the same scratch (its tf32 V copy and per-head partial buffer are
+// reused); extra: attn_tc_dk_bytes(...) bytes, 16-byte aligned.  dk as attn_dk_launch.
+size_t attn_tc_dk_bytes(int64_t S, int nh, int hd);
+int attn_tc_dk_launch(const AttnArgs &a, const float *q, const float *D, float *dk, void *scratch, void *extra,
+                      uint32_t *status, cudaStream_t st);
 
 // LoRA gradients + AdamW of one adapter (lora.cu); gh: [S, rank] scratch.
 int lora_launch(int64_t S, int out_dim, int in_dim, int rank, float alpha, const float *G, const float *h,

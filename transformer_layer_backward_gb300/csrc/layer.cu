@@ -19,7 +19,7 @@ struct LayerWs {
     size_t abf, gbf, ubf, part;               // tensor-core path: bf16 A operands, split-K partials
     size_t atc;                               // tensor-core attention: tf32 operand copies
     size_t dR1, Upart, Wpart, Dpart, gh2, part1, part2, part3, gbar, pp;   // single-token path
-    size_t dk, dkpart, Dh, dn1, dctx, xbf;    // exact layer-input gradient (TLB_EXACT_DIN)
+    size_t dk, dkpart, Dh, dn1, dctx, xbf, dkx;   // exact layer-input gradient (TLB_EXACT_DIN)
     size_t total;
 };
 
@@ -91,8 +91,10 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
         const bool tcx = tc_route(c, S) && qd % 8 == 0 && kvd % 8 == 0 && tc_supported(S, H, qd) &&
                          tc_supported(S, H, kvd);
         w.xbf = tcx ? p.take(S * (qd + 2 * kvd) * 2) : 0;
+        // the tcgen05 key gradient: tf32 copies of dCtx and of q transposed
+        w.dkx = attn_tc_route(c, S, L) ? p.take(attn_tc_dk_bytes(S, c.n_heads, c.head_dim)) : 0;
     } else {
-        w.dk = w.dkpart = w.Dh = w.dn1 = w.dctx = w.xbf = 0;
+        w.dk = w.dkpart = w.Dh = w.dn1 = w.dctx = w.xbf = w.dkx = 0;
     }
     w.total = p.off;
     return w;
@@ -281,7 +283,11 @@ int exact_din_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const tlb_layer
     const int64_t H = c.dim, qd = int64_t(c.n_heads) * c.head_dim, kvd = int64_t(c.n_kv_heads) * c.head_dim;
     float *dk = ws_at<float>(ws, p.dk);
     const AttnArgs g = attn_args(c, S, L, dctx, a, nullptr, nullptr);
-    TLB_TRY(attn_dk_launch(g, a.q, D, dk, ws_at<float>(ws, p.dkpart), st));
+    if (p.dkx != 0 && aligned16(a.attn) && aligned16(a.q))   // the attention ran on tcgen05 too
+        TLB_TRY(attn_tc_dk_launch(g, a.q, D, dk, ws_at<void>(ws, p.atc), ws_at<void>(ws, p.dkx),
+                                  ws_at<uint32_t>(ws, 0), st));
+    else
+        TLB_TRY(attn_dk_launch(g, a.q, D, dk, ws_at<float>(ws, p.dkpart), st));
     if (c.flags & TLB_ROPE)
         TLB_TRY(rope_backward_launch(dk, dk, S, c.n_kv_heads, c.head_dim, L - S, c.rope_base, st));
     if (c.flags & TLB_QK_NORM)
