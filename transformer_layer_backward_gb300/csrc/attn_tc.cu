@@ -710,12 +710,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __gri
         mbar_init(&vfull, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&sfree[s], kEpiWarps + 2);
+            mbar_init(&sfree[s], kEpiWarps / 2 + 2);    // the item's writer group and its two MMAs
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tfree[b], kEpiWarps);
-            mbar_init(&afull[b], kEpiWarps);
+            mbar_init(&tfree[b], kEpiWarps / 2);
+            mbar_init(&afull[b], kEpiWarps / 2);
             mbar_init(&afree[b], 1);
         }
         mbar_init(&dfull, 1);
@@ -800,31 +800,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __gri
         }
     } else {
         // ------------------------------------------------ dS^T writers, then the dK epilogue:
-        // one key row (tensor-memory lane) and half of an item's queries per thread
-        constexpr int HQ = kVQ / 2;
+        // the two groups of four warps take alternate items (group hf the items w = hf mod 2
+        // and with them T^T / dS^T buffer hf), one key row (tensor-memory lane) and all 32
+        // queries of the item per thread; the D values of the group's next item are loaded
+        // while the current one is formed
         const int quarter = warp & 3, hf = (warp - 2) >> 2;
         const int r = quarter * 32 + lane, jj = k0 + r;        // key row of this thread
         const bool key_ok = jj < p.S;
         const int box = r >> 5, col = r & 31;
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+        const float *Dh = p.D + int64_t(h) * p.S;
+        auto load_d = [&](int w, float (&dv)[kVQ]) {
+            const int qa = (t0 + w) * kVQ;
+#pragma unroll
+            for (int qq = 0; qq < kVQ; ++qq) dv[qq] = (w < nw && qa + qq < p.S) ? __ldg(Dh + qa + qq) : 0.f;
+        };
+        float dv[kVQ], dvn[kVQ];
+        load_d(hf, dv);
         bool ok = true;
-        for (int w = 0; w < nw; ++w) {
-            const int s = w % NS, qa = (t0 + w) * kVQ + hf * HQ;
+        for (int w = hf; w < nw; w += 2) {
+            const int s = w % NS, qa = (t0 + w) * kVQ;
             if (!mbar_wait(&full[s], (w / NS) & 1, p.status, 45u) ||
                 !mbar_wait(&tfull[w & 1], (w >> 1) & 1, p.status, 46u)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t t[HQ];
-            tmem_ld16(tD + Ly::TT + uint32_t((w & 1) * kVQ + hf * HQ) + lane_off, t);
+            uint32_t t[kVQ];
+            tmem_ld32(tD + Ly::TT + uint32_t((w & 1) * kVQ) + lane_off, t);
             const uint8_t *ps = sm + Ly::P(s) + box * (kVQ * 128) + (col & 3) * 4;
-            float pv[HQ], dv[HQ];
+            float pv[kVQ];
 #pragma unroll
-            for (int qq = 0; qq < HQ; ++qq) {
-                pv[qq] = *reinterpret_cast<const float *>(ps + sw128_off(hf * HQ + qq, col >> 2));
-                dv[qq] = qa + qq < p.S ? __ldg(p.D + int64_t(h) * p.S + qa + qq) : 0.f;
-            }
+            for (int qq = 0; qq < kVQ; ++qq) pv[qq] = *reinterpret_cast<const float *>(ps + sw128_off(qq, col >> 2));
+            load_d(w + 2, dvn);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -832,19 +840,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __gri
                 mbar_arrive(&tfree[w & 1]);                     // T^T_w read
                 mbar_arrive(&sfree[s]);                         // P read
             }
-            uint32_t ds[HQ];
+            uint32_t ds[kVQ];
 #pragma unroll
-            for (int qq = 0; qq < HQ; ++qq) {
+            for (int qq = 0; qq < kVQ; ++qq) {
                 const bool vis = key_ok && qa + qq < p.S && (!p.causal || qa + qq >= jj);
                 ds[qq] = to_tf32(vis ? pv[qq] * (__uint_as_float(t[qq]) - dv[qq]) : 0.f);
             }
             if (w >= 2 && !mbar_wait(&afree[w & 1], ((w - 2) >> 1) & 1, p.status, 47u)) { ok = false; break; }
             tc_fence_after();
-            tmem_st16(tD + Ly::TS + uint32_t((w & 1) * kVQ + hf * HQ) + lane_off, ds);
+            tmem_st32(tD + Ly::TS + uint32_t((w & 1) * kVQ) + lane_off, ds);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&afull[w & 1]);
+#pragma unroll
+            for (int qq = 0; qq < kVQ; ++qq) dv[qq] = dvn[qq];
         }
         if (ok && mbar_wait(&dfull, 0, p.status, 48u)) {
             tc_fence_after();
