@@ -666,12 +666,12 @@ struct DkLayout {
     static constexpr int P_BYTES = kVQ * kVK * 4;            // P item [32 queries][128 keys], 4 boxes
     static constexpr int C_BYTES = kVQ * HD * 4;             // dCtx rows [32 queries][HD], NB atoms
     static constexpr int Q_BYTES = HD * kVQ * 4;             // q^T [HD][32 queries], one atom
-    static constexpr int SLOT = P_BYTES + C_BYTES + Q_BYTES;
-    static constexpr int NS = 3;
-    static constexpr int S0 = V_BYTES, TOTAL = V_BYTES + NS * SLOT;
-    __host__ __device__ static constexpr int P(int s) { return S0 + s * SLOT; }
-    __host__ __device__ static constexpr int C(int s) { return S0 + s * SLOT + P_BYTES; }
-    __host__ __device__ static constexpr int Q(int s) { return S0 + s * SLOT + P_BYTES + C_BYTES; }
+    static constexpr int SA = P_BYTES + C_BYTES;             // ring A slot: P and dCtx rows
+    static constexpr int NS = 3;                             // slots of each ring
+    static constexpr int A0 = V_BYTES, B0 = V_BYTES + NS * SA, TOTAL = B0 + NS * Q_BYTES;
+    __host__ __device__ static constexpr int P(int s) { return A0 + s * SA; }
+    __host__ __device__ static constexpr int C(int s) { return A0 + s * SA + P_BYTES; }
+    __host__ __device__ static constexpr int Q(int s) { return B0 + s * Q_BYTES; }
     // tensor memory: dK [128 keys][HD], then T^T and dS^T double buffers [128 keys][32]
     static constexpr uint32_t TT = HD, TS = HD + 2 * kVQ;
     static constexpr uint32_t COLS = (HD + 4 * kVQ) <= 256 ? 256 : 512;
@@ -689,15 +689,27 @@ struct AttnTcDkParams {
     uint32_t *status;
 };
 
+// Key gradient of the S newest keys for the exact layer-input gradient: per head h and
+// tile of 128 keys, over 32-query items w (causal: from the first item that sees key k0),
+//   T^T_w = V_tile dCtx_w^T          tcgen05.mma, both operands in shared memory (V once)
+//   dS^T  = P^T (.) (T^T - D_w)       writer warps, tf32 into tensor memory
+//   dK   += dS^T q_w                  tcgen05.mma, A from tensor memory, q^T tile as B
+// then scale dK (per-head partials added in head order when the group has several heads).
+// Two rings, each filled by its own producer lane: A holds an item's P tile (4 boxes of
+// 32 keys) and tf32 dCtx rows, freed once the writers have read P and T^T_w is formed; B
+// holds its q^T tile, freed by the dK MMA.  The two writer groups take alternate items.
+// T^T_w+2 may take T^T_w's buffer as soon as the writers have read it; dS^T_w+2 waits for
+// the dK MMA of item w.
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __grid_constant__ AttnTcDkParams p) {
     using Ly = DkLayout<HD>;
     constexpr int NS = Ly::NS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    __shared__ uint64_t vfull, full[NS], sfree[NS], tfull[2], tfree[2], afull[2], afree[2], dfull;
+    __shared__ uint64_t vfull, afullr[NS], afreer[NS], bfull[NS], bfree[NS], tfull[2], tfree[2], afull[2], afree[2],
+        dfull;
     __shared__ uint32_t tmem_base;
-    __shared__ int s_abort, s_issued, s_used;
+    __shared__ int s_abort, s_a_issued, s_a_used, s_b_issued, s_b_used;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.x, G = p.nh / p.nkv, kvh = h / G, g = h % G;
     const int k0 = int(gridDim.y - 1 - blockIdx.y) * kVK;    // among the S newest keys (heaviest first)
@@ -706,11 +718,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __gri
 
     if (threadIdx.x == 0) {
         s_abort = 0;
-        s_issued = s_used = 0;
+        s_a_issued = s_a_used = s_b_issued = s_b_used = 0;
         mbar_init(&vfull, 1);
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&sfree[s], kEpiWarps / 2 + 2);    // the item's writer group and its two MMAs
+            mbar_init(&afullr[s], 1);
+            mbar_init(&afreer[s], kEpiWarps / 2 + 1);   // the item's writer group and its T^T MMA
+            mbar_init(&bfull[s], 1);
+            mbar_init(&bfree[s], 1);                    // its dK MMA
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -731,21 +745,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __gri
     const uint32_t tD = tmem_base;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer: V once, then NS items ahead
+        // ------------------------------------------------ TMA producers: lane 0 V and ring A,
+        // lane 1 ring B, NS items ahead each
         if (lane == 0) {
             mbar_arrive_expect_tx(&vfull, Ly::V_BYTES);
             for (int b = 0; b < Ly::NB; ++b)
                 tma_load_3d(sm + b * (kVK * 128), &p.v, b * 32, p.pos0 + k0, kvh, &vfull);
             for (int w = 0; w < nw; ++w) {
                 const int s = w % NS, qa = (t0 + w) * kVQ;
-                if (w >= NS && !mbar_wait(&sfree[s], (w / NS - 1) & 1, p.status, 40u)) { s_abort = 1; break; }
-                mbar_arrive_expect_tx(&full[s], Ly::SLOT);
+                if (w >= NS && !mbar_wait(&afreer[s], (w / NS - 1) & 1, p.status, 40u)) { s_abort = 1; break; }
+                mbar_arrive_expect_tx(&afullr[s], Ly::SA);
                 for (int b = 0; b < kVK / 32; ++b)
-                    tma_load_3d(sm + Ly::P(s) + b * (kVQ * 128), &p.pv, p.pos0 + k0 + b * 32, qa, h, &full[s]);
+                    tma_load_3d(sm + Ly::P(s) + b * (kVQ * 128), &p.pv, p.pos0 + k0 + b * 32, qa, h, &afullr[s]);
                 for (int b = 0; b < Ly::NB; ++b)
-                    tma_load_3d(sm + Ly::C(s) + b * (kVQ * 128), &p.dcr, b * 32, h, qa, &full[s]);
-                tma_load_3d(sm + Ly::Q(s), &p.qt, qa, 0, h, &full[s]);
-                s_issued = w + 1;
+                    tma_load_3d(sm + Ly::C(s) + b * (kVQ * 128), &p.dcr, b * 32, h, qa, &afullr[s]);
+                s_a_issued = w + 1;
+            }
+        } else if (lane == 1) {
+            for (int w = 0; w < nw; ++w) {
+                const int s = w % NS, qa = (t0 + w) * kVQ;
+                if (w >= NS && !mbar_wait(&bfree[s], (w / NS - 1) & 1, p.status, 49u)) { s_abort = 1; break; }
+                mbar_arrive_expect_tx(&bfull[s], Ly::Q_BYTES);
+                tma_load_3d(sm + Ly::Q(s), &p.qt, qa, 0, h, &bfull[s]);
+                s_b_issued = w + 1;
             }
         }
     } else if (warp == 1) {
@@ -754,8 +776,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __gri
             constexpr uint32_t id_t = idesc_tf32(kVK, kVQ), id_k = idesc_tf32(kVK, HD);
             auto mma_t = [&](int w) -> bool {              // T^T[w % 2] = V dCtx_w^T
                 const int s = w % NS;
-                if (!mbar_wait(&full[s], (w / NS) & 1, p.status, 41u)) return false;
-                s_used = w + 1;
+                if (!mbar_wait(&afullr[s], (w / NS) & 1, p.status, 41u)) return false;
+                s_a_used = w + 1;
                 tc_fence_after();
 #pragma unroll
                 for (int kb = 0; kb < Ly::NB; ++kb)
@@ -763,7 +785,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __gri
                     for (int k = 0; k < 4; ++k)
                         mma_tf32(tD + Ly::TT + uint32_t((w & 1) * kVQ), sw128_desc(sm + kb * (kVK * 128)) + 2 * k,
                                  sw128_desc(sm + Ly::C(s) + kb * (kVQ * 128)) + 2 * k, id_t, (kb | k) ? 1u : 0u);
-                mma_commit(&sfree[s]);
+                mma_commit(&afreer[s]);
                 mma_commit(&tfull[w & 1]);
                 return true;
             };
@@ -772,17 +794,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __gri
             ok = ok && (nw < 1 || mma_t(0)) && (nw < 2 || mma_t(1));
             for (int w = 0; ok && w < nw; ++w) {
                 const int s = w % NS;
-                if (!mbar_wait(&afull[w & 1], (w >> 1) & 1, p.status, 43u)) {
+                if (!mbar_wait(&afull[w & 1], (w >> 1) & 1, p.status, 43u) ||
+                    !mbar_wait(&bfull[s], (w / NS) & 1, p.status, 50u)) {
                     ok = false;
                     break;
                 }
+                s_b_used = w + 1;
                 tc_fence_after();
                 const uint64_t qd = sw128_desc(sm + Ly::Q(s));
 #pragma unroll
                 for (int k = 0; k < kVQ / 8; ++k)
                     mma_tf32_ts(tD, tD + Ly::TS + uint32_t((w & 1) * kVQ + 8 * k), qd + 2 * k, id_k,
                                 (w > 0 || k > 0) ? 1u : 0u);
-                mma_commit(&sfree[s]);
+                mma_commit(&bfree[s]);
                 mma_commit(&afree[w & 1]);
                 // T^T_w+2 takes T^T_w's buffer: the writers read it before they filled dS^T_w
                 if (w + 2 < nw) {
@@ -820,7 +844,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __gri
         bool ok = true;
         for (int w = hf; w < nw; w += 2) {
             const int s = w % NS, qa = (t0 + w) * kVQ;
-            if (!mbar_wait(&full[s], (w / NS) & 1, p.status, 45u) ||
+            if (!mbar_wait(&afullr[s], (w / NS) & 1, p.status, 45u) ||
                 !mbar_wait(&tfull[w & 1], (w >> 1) & 1, p.status, 46u)) {
                 ok = false;
                 break;
@@ -838,7 +862,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __gri
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&tfree[w & 1]);                     // T^T_w read
-                mbar_arrive(&sfree[s]);                         // P read
+                mbar_arrive(&afreer[s]);                        // P read
             }
             uint32_t ds[kVQ];
 #pragma unroll
@@ -858,8 +882,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __gri
         }
         if (ok && mbar_wait(&dfull, 0, p.status, 48u)) {
             tc_fence_after();
-            // every copy into the ring has been consumed: each warp turns its 32 x 32 blocks
-            // in the first slot so that the stores coalesce
+            // every copy into the rings has been consumed: each warp turns its 32 x 32 blocks
+            // in ring A so that the stores coalesce
             float *blk = reinterpret_cast<float *>(sm + Ly::P(0)) + (warp - 2) * 32 * 33;
             const int64_t kvd = int64_t(p.nkv) * HD;
             float *out = p.dk + (G > 1 ? int64_t(g) * p.S * kvd : 0) + kvh * HD;
@@ -888,9 +912,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dk_kernel(const __gri
     tc_fence_before();
     __syncthreads();
     if (s_abort && threadIdx.x == 0) {
-        // the copies issued but not yet consumed (at most NS of them, and V)
+        // the copies issued but not yet consumed (at most NS per ring, and V)
         mbar_wait(&vfull, 0, nullptr, 0u);
-        for (int w = max(s_used, s_issued - NS); w < s_issued; ++w) mbar_wait(&full[w % NS], (w / NS) & 1, nullptr, 0u);
+        for (int w = max(s_a_used, s_a_issued - NS); w < s_a_issued; ++w)
+            mbar_wait(&afullr[w % NS], (w / NS) & 1, nullptr, 0u);
+        for (int w = max(s_b_used, s_b_issued - NS); w < s_b_issued; ++w)
+            mbar_wait(&bfull[w % NS], (w / NS) & 1, nullptr, 0u);
     }
     __syncthreads();
     if (warp == 1) {
