@@ -74,3 +74,7 @@ def assert_route(cfg, names):
             assert k in names, ("%s did not run" % k, names)
         for k in ("attn_dq_tiled", "attn_rows"):
             assert k not in names, ("CUDA-core attention ran", names)
+        if cfg.rank == 16:       # the adapters' passes run on the tensor cores beside it
+            for k in ("lora_tc_gpass", "lora_tc_xpass"):
+                assert k in names, ("%s did not run" % k, names)
+            assert "lora_gpass" not in names, ("CUDA-core LoRA pass ran", names)

@@ -120,12 +120,30 @@ size_t lora_seq_bytes(int64_t S, int out_dim, int in_dim, int rank);
 // adapters of gh A, gh [S, rank] = s G B and A [rank, in_dim] both from before the update.
 int lora_din_launch(int64_t S, int in_dim, int rank, const float *const *gh, const float *const *A, int njobs,
                     float *dn1, cudaStream_t st);
+// The same passes on the tensor cores (lora_tc.cu, kind::tf32, rank 16): per adapter
+// G [S, out_dim], h [S, 16], B [out_dim, 16] (before its update), gh [S, 16] (written
+// between the passes) and the partial sums part_gh [n_ot][S][16], part_b [chunks][out][16],
+// part_a [chunks][16][in_dim] of the CUDA-core passes, over chunks of 128-token tiles.
+struct LoraTcJob {
+    const float *G, *h, *b, *gh;
+    float *part_gh, *part_b, *part_a;
+    int out_dim;
+};
+bool lora_tc_supported(int64_t S, int in_dim, int rank, const float *x, const LoraTcJob *jobs, int njobs);
+// Chunks of 128-token tiles for a pass over n_ct column tiles (about one CTA per SM).
+int lora_tc_chunks(int64_t S, int n_ct, int &tiles_per_chunk);
+int lora_tc_gpass_launch(int64_t S, const LoraTcJob *jobs, int njobs, int tiles_per_chunk, uint32_t *status,
+                         cudaStream_t st);
+int lora_tc_xpass_launch(int64_t S, int in_dim, const float *x, const LoraTcJob *jobs, int njobs,
+                         int tiles_per_chunk, uint32_t *status, cudaStream_t st);
+// tc (optional): run the passes on the tensor cores when lora_tc_supported holds, with
+// bounded waits that run out recorded in this status block.
 // status (optional): a status block whose step gate (kStatusGate) is 1 skips the AdamW
 // steps (the gradients are still written and summed).
 // din (optional): dn1 of the exact input gradient; gh A of every adapter is added into it
 // between the gh sums and AdamW.
 int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x, const LoraJob *jobs, int njobs,
                     const tlb_adamw_cfg &adam, double *sumsq, cudaStream_t st, const uint32_t *status = nullptr,
-                    float *din = nullptr);
+                    float *din = nullptr, uint32_t *tc = nullptr);
 
 }  // namespace tlb

@@ -614,8 +614,10 @@ static int layer_backward_impl(const tlb_layer_cfg *cfg, int64_t S, int64_t L, c
         TLB_TRY(exact_din_impl(c, S, L, *w, *acts, dqpre, dv, ws_at<float>(ws, p.dSub), Dh, d_hidden, ws, p, st));
     const LoraJob jobs[2] = {{dqpre, acts->lora_q_h, qd, *lora_q, ws_at<void>(ws, p.lora_q)},
                              {dv, acts->lora_v_h, kvd, *lora_v, ws_at<void>(ws, p.lora_v)}};
+    // on the tensor cores where the attention backward ran there (the same tf32 class)
     TLB_TRY(lora_seq_launch(S, c.dim, c.rank, c.lora_alpha, acts->x, jobs, 2, *adam, sumsq, st,
-                            chk ? status : nullptr, exact ? exact_dst(c, d_hidden, ws, p) : nullptr));
+                            chk ? status : nullptr, exact ? exact_dst(c, d_hidden, ws, p) : nullptr,
+                            attn_tc_route(c, S, L) ? status : nullptr));
     return exact ? exact_din_finish(c, S, *w, *acts, d_hidden, ws, p, st) : TLB_OK;
 }
 

@@ -650,7 +650,34 @@ SideBytes side_bytes(int64_t S, int out_dim, int in_dim, int rank) {
 
 template <int RB>
 int lora_seq_run(LoraSeqArgs a, int n_ot_total, const AdamCoef &ka, const AdamCoef &kb, double *sumsq,
-                 cudaStream_t st, float *din) {
+                 cudaStream_t st, float *din, uint32_t *tc) {
+    if constexpr (RB == 16) {
+        // the tensor-core passes, with partial sums over chunks of 128-token tiles
+        LoraTcJob tj[2] = {};
+        for (int sd = 0; sd < a.nside; ++sd) {
+            const LoraSide &p = a.side[sd];
+            tj[sd] = LoraTcJob{p.G, p.h, p.l.b, p.gh, p.part_gh, p.part_b, p.part_a, p.O};
+        }
+        if (tc != nullptr && lora_tc_supported(a.S, a.C, a.rank, a.x, tj, a.nside)) {
+            int tpc = 0;
+            a.nrc_b = lora_tc_chunks(a.S, n_ot_total, tpc);
+            TLB_TRY(lora_tc_gpass_launch(a.S, tj, a.nside, tpc, tc, st));
+            const int64_t ngh = int64_t(a.nside) * a.S * a.rank;
+            lora_gh_sum_kernel<<<unsigned(ceil_div(ngh, int64_t(256))), 256, 0, st>>>(a);
+            TLB_TRY(check_launch("lora_gh_sum"));
+            if (din != nullptr) {
+                const float *gh[2] = {a.side[0].gh, a.side[1].gh};
+                const float *A[2] = {a.side[0].l.a, a.side[1].l.a};
+                TLB_TRY(lora_din_launch(a.S, a.C, a.rank, gh, A, a.nside, din, st));
+            }
+            a.nrc_a = lora_tc_chunks(a.S, int(ceil_div(a.C, kLO)), tpc);
+            TLB_TRY(lora_tc_xpass_launch(a.S, a.C, a.x, tj, a.nside, tpc, tc, st));
+            int64_t np = 0;
+            for (int sd = 0; sd < a.nside; ++sd) np += int64_t(a.rank) * (a.C + a.side[sd].O);
+            lora_seq_adamw_kernel<<<unsigned(ceil_div(np, int64_t(256))), 256, 0, st>>>(a, ka, kb, sumsq);
+            return check_launch("lora_seq_adamw");
+        }
+    }
     // chunks of row tiles per block: at most two blocks per SM in each pass (one wave)
     const int target = 2 * num_sms();
     a.nrc_b = int(std::min<int64_t>(a.n_rt, std::max<int64_t>(1, target / n_ot_total)));
@@ -728,7 +755,7 @@ size_t lora_seq_bytes(int64_t S, int out_dim, int in_dim, int rank) {
 
 int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x, const LoraJob *jobs, int njobs,
                     const tlb_adamw_cfg &adam, double *sumsq, cudaStream_t st, const uint32_t *status,
-                    float *din) {
+                    float *din, uint32_t *tc) {
     if (S == 0 || njobs == 0) return TLB_OK;
     TLB_REQUIRE(njobs <= 2, TLB_EINVAL, "lora: at most two adapters per call");
     TLB_REQUIRE(rank >= 1 && rank <= 64, TLB_EINVAL, "lora: rank must be in 1..64");
@@ -770,11 +797,11 @@ int lora_seq_launch(int64_t S, int in_dim, int rank, float alpha, const float *x
     }
     const AdamCoef kb = adam_coef(adam, adam.lr_b_mult);
     const AdamCoef ka = adam_coef(adam, 1.0f);
-    if (rank <= 4) return lora_seq_run<4>(a, blk, ka, kb, sumsq, st, din);
-    if (rank <= 8) return lora_seq_run<8>(a, blk, ka, kb, sumsq, st, din);
-    if (rank <= 16) return lora_seq_run<16>(a, blk, ka, kb, sumsq, st, din);
-    if (rank <= 32) return lora_seq_run<32>(a, blk, ka, kb, sumsq, st, din);
-    return lora_seq_run<64>(a, blk, ka, kb, sumsq, st, din);
+    if (rank <= 4) return lora_seq_run<4>(a, blk, ka, kb, sumsq, st, din, tc);
+    if (rank <= 8) return lora_seq_run<8>(a, blk, ka, kb, sumsq, st, din, tc);
+    if (rank <= 16) return lora_seq_run<16>(a, blk, ka, kb, sumsq, st, din, tc);
+    if (rank <= 32) return lora_seq_run<32>(a, blk, ka, kb, sumsq, st, din, tc);
+    return lora_seq_run<64>(a, blk, ka, kb, sumsq, st, din, tc);
 }
 
 
