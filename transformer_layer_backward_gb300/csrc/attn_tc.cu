@@ -60,7 +60,7 @@ struct AttnTcParams {
     float scale;
     uint32_t *status;
     float *D;                   // [nh, S] row sums D (optional)
-    RopeFreqs fr;
+    const float2 *rt;           // [S][hd / 2] (cos, sin) of the RoPE angles of positions pos0 + i
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -86,10 +86,26 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int ch) { return uint32_t(r
 // K and V rows allow 16-byte loads (else those two load one float at a time).
 constexpr int kPrepT = 64;
 __global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dCT, float *Kt, float *Vr,
-                                                           int S4, int L4, int nt_dc, int nt_kv, int vec_kv) {
+                                                           int S4, int L4, int nt_dc, int nt_kv, int vec_kv,
+                                                           const __grid_constant__ RopeFreqs fr, float2 *rt) {
     __shared__ float tile[kPrepT][kPrepT + 1];
     const int qd = a.nh * a.hd, kvd = a.nkv * a.hd;
     int t = blockIdx.x;
+    if (t >= nt_dc + 2 * nt_kv) {
+        // the RoPE table: (cos, sin) of (pos0 + i) f_d for the S new positions, the angles
+        // every head's dQ epilogue rotates by
+        const int hh = a.hd / 2;
+        const int64_t e0 = int64_t(t - nt_dc - 2 * nt_kv) * 1024, n = int64_t(a.S) * hh;
+        for (int k = 0; k < 4; ++k) {
+            const int64_t e = e0 + threadIdx.x + 256 * k;
+            if (e >= n) break;
+            const int i = int(e / hh), d = int(e % hh);
+            float c, sn;
+            rope_cos_sin(float(a.pos0 + i), fr.hi[d], fr.lo[d], c, sn);
+            rt[e] = make_float2(c, sn);
+        }
+        return;
+    }
     int job, rows, cols;
     if (t < nt_dc) {
         job = 0;
@@ -285,18 +301,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
                 s_k_used = j + 1;
                 tc_fence_after();
                 const uint32_t te = tmem + Ly::TT + uint32_t((j & 1) * kQK);    // E_j, where T_j was
+                // U_j first and its commit, then W_j: the wait for U_j below (before T_j+2 may
+                // take E_j's buffer) overlaps W_j in the tensor pipe instead of draining it
+#pragma unroll
+                for (int a = 0; a < Ly::NA; ++a) {
+                    const uint64_t kd = sw128_desc(sm + Ly::KT(s) + a * Ly::KT_ATOM);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_tf32_ts(tmem + Ly::TU, te + uint32_t(32 * a + 8 * k), kd + 2 * k, id2,
+                                    (j > 0 || a > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(&afree[j & 1]);
 #pragma unroll
                 for (int a = 0; a < Ly::NA; ++a) {
                     const uint64_t kd = sw128_desc(sm + Ly::KT(s) + a * Ly::KT_ATOM);
                     const uint64_t pd = sw128_desc(sm + Ly::P(s) + a * Ly::P_ATOM);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t acc = (j > 0 || a > 0 || k > 0) ? 1u : 0u;
-                        mma_tf32_ts(tmem + Ly::TU, te + uint32_t(32 * a + 8 * k), kd + 2 * k, id2, acc);
-                        mma_tf32(tmem + Ly::TW, pd + 2 * k, kd + 2 * k, id2, acc);
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        mma_tf32(tmem + Ly::TW, pd + 2 * k, kd + 2 * k, id2, (j > 0 || a > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit(&afree[j & 1]);
                 mma_commit(&kfree[s]);
                 // T_j+2 overwrites E_j: issue it once U_j has read E_j
                 if (j + 2 < nt) {
@@ -321,18 +344,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
         const int jlast = p.causal ? p.pos0 + i : p.L - 1;      // last visible key
         {   // this row's half of dCtx_h, rounded to tf32, into tensor memory: the A operand of T
-            const float *src = p.dctx + int64_t(row_ok ? i : 0) * (p.nh * HD) + h * HD + hf * (HD / 2);
+            const float4 *src = reinterpret_cast<const float4 *>(p.dctx + int64_t(row_ok ? i : 0) * (p.nh * HD) +
+                                                                 h * HD + hf * (HD / 2));
+            float4 x[HD / 8];                    // every load in flight before the first store
+#pragma unroll
+            for (int k = 0; k < HD / 8; ++k) x[k] = row_ok ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < HD / 2; c += 16) {
                 uint32_t v[16];
 #pragma unroll
                 for (int t = 0; t < 16; t += 4) {
-                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (row_ok) x = *reinterpret_cast<const float4 *>(src + c + t);
-                    v[t] = to_tf32(x.x);
-                    v[t + 1] = to_tf32(x.y);
-                    v[t + 2] = to_tf32(x.z);
-                    v[t + 3] = to_tf32(x.w);
+                    const float4 y = x[(c + t) / 4];
+                    v[t] = to_tf32(y.x);
+                    v[t + 1] = to_tf32(y.y);
+                    v[t + 2] = to_tf32(y.z);
+                    v[t + 3] = to_tf32(y.w);
                 }
                 tmem_st16(tmem + Ly::TDC + uint32_t(hf * (HD / 2) + c) + lane_off, v);
             }
@@ -412,13 +438,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
             tc_fence_after();
             constexpr int half = HD / 2, q4 = HD / 4;
             float *out0 = p.dq + h * HD;
-            const float pos = float(p.pos0 + i);
+            const float4 *rt4 = reinterpret_cast<const float4 *>(p.rt + int64_t(row_ok ? i : 0) * half);
             // the rings are idle (every copy consumed, every MMA done): each warp turns its
             // 32-row blocks there so that the stores coalesce
             float *blk = reinterpret_cast<float *>(sm) + (warp - 2) * 32 * 33;
             const int c4 = (lane & 7) * 4, rl = lane >> 3;
 #pragma unroll 1
             for (int c = hf * q4; c < (hf + 1) * q4; c += 16) {      // pairs (c, c + HD / 2)
+                float4 cs[8];                    // (cos, sin) of columns c .. c + 15, two per load
+                if (p.rope) {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) cs[t] = rt4[c / 2 + t];
+                }
                 uint32_t u1[16], u2[16], w1[16], w2[16];
                 tmem_ld16(tmem + Ly::TU + uint32_t(c) + lane_off, u1);
                 tmem_ld16(tmem + Ly::TU + uint32_t(c + half) + lane_off, u2);
@@ -431,9 +462,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
                     float a1 = p.scale * (__uint_as_float(u1[t]) - D * __uint_as_float(w1[t]));
                     float a2 = p.scale * (__uint_as_float(u2[t]) - D * __uint_as_float(w2[t]));
                     if (p.rope) {
-                        float cs, sn;
-                        rope_cos_sin(pos, p.fr.hi[c + t], p.fr.lo[c + t], cs, sn);
-                        const float b1 = a1 * cs + a2 * sn, b2 = -a1 * sn + a2 * cs;
+                        const float4 q = cs[t / 2];
+                        const float co = (t & 1) ? q.z : q.x, sn = (t & 1) ? q.w : q.y;
+                        const float b1 = a1 * co + a2 * sn, b2 = -a1 * sn + a2 * co;
                         a1 = b1;
                         a2 = b2;
                     }
@@ -972,7 +1003,7 @@ int make_map_f32_3d(CUtensorMap *m, const void *base, const uint64_t dims[3], co
 }
 
 struct TcAttnWs {
-    size_t dCT, Kt, Vr, part, total;
+    size_t dCT, Kt, Vr, part, rt, total;
     int64_t S4, L4;
 };
 
@@ -985,7 +1016,8 @@ TcAttnWs tc_attn_layout(int64_t S, int64_t L, int nh, int nkv, int hd) {
     w.Kt = w.dCT + r256(size_t(nh) * hd * w.S4 * 4);
     w.Vr = w.Kt + r256(size_t(nkv) * hd * w.L4 * 4);
     w.part = w.Vr + r256(size_t(nkv) * L * hd * 4);
-    w.total = w.part + (nh > nkv ? r256(size_t(nh) * S * hd * 4) : 0);   // per-head dV sums
+    w.rt = w.part + (nh > nkv ? r256(size_t(nh) * S * hd * 4) : 0);      // per-head dV sums
+    w.total = w.rt + r256(size_t(S) * (hd / 2) * 8);                      // RoPE table
     return w;
 }
 
@@ -998,8 +1030,10 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     const int nt_dc = int(ceil_div(a.S, kPrepT)) * (a.nh * HD / kPrepT);
     const int nt_kv = int(ceil_div(a.L, kPrepT)) * (a.nkv * HD / kPrepT);
     const int vec_kv = aligned16(a.k) && aligned16(a.v) && a.sh % 4 == 0 && a.sp % 4 == 0;
-    attn_tc_prep_kernel<<<unsigned(nt_dc + 2 * nt_kv), 256, 0, st>>>(a, dCT, Kt, Vr, int(w.S4), int(w.L4), nt_dc,
-                                                                    nt_kv, vec_kv);
+    float2 *rt = reinterpret_cast<float2 *>(base + w.rt);
+    const int nt_rt = a.rope ? int(ceil_div(int64_t(a.S) * (HD / 2), int64_t(1024))) : 0;
+    attn_tc_prep_kernel<<<unsigned(nt_dc + 2 * nt_kv + nt_rt), 256, 0, st>>>(a, dCT, Kt, Vr, int(w.S4), int(w.L4),
+                                                                            nt_dc, nt_kv, vec_kv, fr, rt);
     TLB_TRY(check_launch("attn_tc_prep"));
 
     AttnTcParams p;
@@ -1044,7 +1078,7 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     p.scale = a.scale;
     p.status = status;
     p.D = a.D;
-    p.fr = fr;
+    p.rt = rt;
 
     const int smq = DqLayout<HD>::TOTAL + 1024, smv = DvLayout<HD>::TOTAL + 1024;
     TLB_CUDA(cudaFuncSetAttribute(attn_tc_dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smq));
@@ -1077,7 +1111,9 @@ int launch_attn_tc_dk(const AttnArgs &a, const float *q, const float *D, float *
     AttnArgs aq = a;               // the prep's first job transposes its dctx rows: give it q
     aq.dctx = q;
     const int nt_q = int(ceil_div(a.S, kPrepT)) * int(qd / kPrepT);
-    attn_tc_prep_kernel<<<unsigned(nt_q), 256, 0, st>>>(aq, QT, nullptr, nullptr, int(w.S4), int(w.L4), nt_q, 0, 0);
+    const RopeFreqs no_rope{};
+    attn_tc_prep_kernel<<<unsigned(nt_q), 256, 0, st>>>(aq, QT, nullptr, nullptr, int(w.S4), int(w.L4), nt_q, 0, 0,
+                                                        no_rope, nullptr);
     TLB_TRY(check_launch("attn_tc_prep_q"));
 
     AttnTcDkParams p;
