@@ -61,6 +61,12 @@ def tc_attention_shape(cfg) -> bool:
             and cfg.n_heads % cfg.n_kv_heads == 0 and not cfg.recompute_p)
 
 
+def tc_recompute_shape(cfg) -> bool:
+    """The recomputed attention (flash-style) runs on tcgen05 on the same shapes, without
+    the exact input gradient (whose key gradient then recomputes on CUDA cores)."""
+    return (tc_attention_shape(cfg.with_(recompute_p=False)) and cfg.recompute_p and not cfg.exact_din)
+
+
 def assert_route(cfg, names):
     """bf16 layers with S > 1 must run their weight products on the tcgen05 GEMM and, where
     the shape allows, their attention on the tcgen05 kernels: a silent fall-back to the
@@ -68,6 +74,10 @@ def assert_route(cfg, names):
     if cfg.wtype != "bf16" or cfg.seq_len <= 1:
         return
     assert "tcgen05 gemm" in names, ("tcgen05 GEMM did not run", names)
+    if tc_recompute_shape(cfg):
+        for k in ("attn_tc_dv_rc", "attn_tc_dsum", "attn_tc_dq_rc"):
+            assert k in names, ("%s did not run" % k, names)
+        assert "attn_dq_tiled" not in names, ("CUDA-core attention ran", names)
     assert "gemm_nt_simt" not in names, ("CUDA-core GEMM ran on a bf16 sequence layer", names)
     if tc_attention_shape(cfg):
         for k in ("attn_tc_dq", "attn_tc_dv"):

@@ -21,10 +21,12 @@ pytestmark = pytest.mark.gpu
 LAYER = STACK2048.with_(name="layer2048", n_layers=1)
 
 
-@pytest.mark.parametrize("exact", [False, True], ids=["truncated", "exact_din"])
-def test_full_size_layer_against_oracle(lib, exact):
+@pytest.mark.parametrize("mode", ["truncated", "exact_din", "recompute"])
+def test_full_size_layer_against_oracle(lib, mode):
     import torch
-    cfg = LAYER.with_(name="layer2048_exact", exact_din=True) if exact else LAYER
+    exact = mode == "exact_din"
+    cfg = {"truncated": LAYER, "exact_din": LAYER.with_(name="layer2048_exact", exact_din=True),
+           "recompute": LAYER.with_(name="layer2048_recompute", recompute_p=True)}[mode]
     d = layer_inputs(cfg, layer=0, seed=0)
     ref = OL.layer_backward(cfg, d, d["dout"])
     t = to_dev(d, cfg.wtype)
@@ -45,7 +47,7 @@ def test_full_size_layer_against_oracle(lib, exact):
     rel = {"d_in": check("d_in", host(dh), ref["d_in"], BF16_REL_L2, None)[0]}
     for k in ("dA_q", "dB_q", "dA_v", "dB_v"):
         rel[k] = check(k, host(grads[k]), ref[k], BF16_REL_L2, None)[0]
-    print("full-size layer%s: relative L2" % (" (exact d_in)" if exact else ""), {k: "%.2e" % v for k, v in rel.items()})
+    print("full-size layer (%s): relative L2" % mode, {k: "%.2e" % v for k, v in rel.items()})
     s = ss.cpu().numpy()
     assert abs(s[0] - ref["sumsq_a"]) <= 2 * BF16_REL_L2 * ref["sumsq_a"]
     assert abs(s[1] - ref["sumsq_b"]) <= 2 * BF16_REL_L2 * ref["sumsq_b"]

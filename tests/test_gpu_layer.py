@@ -83,12 +83,14 @@ SEQ_RC_CACHE = SEQ_CACHE.with_(name="seq_recompute_cache", recompute_p=True)
 SEQ_RC_EXACT = SEQ_HD64.with_(name="seq_recompute_exact", recompute_p=True, exact_din=True, seq_len=130,
                               cache_len=130)
 TINY_RC_EXACT = TINY.with_(name="tiny_recompute_exact", recompute_p=True, exact_din=True, qk_norm=True)
+# the flash-style tcgen05 kernels: head_dim 128 over three ragged 128-query / 128-key tiles
+SEQ_RC_LONG = SEQ_CACHE.with_(name="seq_recompute_long", recompute_p=True, seq_len=300, cache_len=300)
 # rank-16 adapters beside the tensor-core attention take the tcgen05 LoRA passes: three
 # 128-token tiles with a ragged last one, and a V side of 1.5 column tiles (3 KV heads)
 SEQ_LORA16 = SEQ_HD64.with_(name="seq_lora16", rank=16, lora_alpha=32.0, seq_len=300, cache_len=300)
 SEQ_LORA16_KV3 = SEQ_HD64.with_(name="seq_lora16_kv3", n_heads=6, n_kv_heads=3, rank=16, lora_alpha=32.0,
                                 seq_len=170, cache_len=170, adam_state="warm", step=6)
-CASES = {c.name: c for c in (SEQ_LORA16, SEQ_LORA16_KV3, TINY_RC, DEC_RC, MINI_SEQ_RC, SEQ_RC, SEQ_RC_CACHE, SEQ_RC_EXACT, TINY_RC_EXACT,
+CASES = {c.name: c for c in (SEQ_LORA16, SEQ_LORA16_KV3, SEQ_RC_LONG, TINY_RC, DEC_RC, MINI_SEQ_RC, SEQ_RC, SEQ_RC_CACHE, SEQ_RC_EXACT, TINY_RC_EXACT,
                              DECODE_T2, DEC_T2, DEC_T2_EXACT,
                              TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512, DEC_F32, DEC_BF16, DEC_G8, DEC_HD256,
                              SEQ_HD64, SEQ_CACHE, SEQ_MHA, SEQ_ODD, TINY_QK, DEC_QK, SEQ_QK, SEQ_PRENORM,

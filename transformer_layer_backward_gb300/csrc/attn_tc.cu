@@ -87,15 +87,17 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int ch) { return uint32_t(r
 constexpr int kPrepT = 64;
 __global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dCT, float *Kt, float *Vr,
                                                            int S4, int L4, int nt_dc, int nt_kv, int vec_kv,
-                                                           const __grid_constant__ RopeFreqs fr, float2 *rt) {
+                                                           const __grid_constant__ RopeFreqs fr, float2 *rt,
+                                                           float *Kr) {
     __shared__ float tile[kPrepT][kPrepT + 1];
     const int qd = a.nh * a.hd, kvd = a.nkv * a.hd;
+    const int nkvj = Kr != nullptr ? 3 : 2;        // K^T, V rows, and the K rows when recomputing
     int t = blockIdx.x;
-    if (t >= nt_dc + 2 * nt_kv) {
+    if (t >= nt_dc + nkvj * nt_kv) {
         // the RoPE table: (cos, sin) of (pos0 + i) f_d for the S new positions, the angles
         // every head's dQ epilogue rotates by
         const int hh = a.hd / 2;
-        const int64_t e0 = int64_t(t - nt_dc - 2 * nt_kv) * 1024, n = int64_t(a.S) * hh;
+        const int64_t e0 = int64_t(t - nt_dc - nkvj * nt_kv) * 1024, n = int64_t(a.S) * hh;
         for (int k = 0; k < 4; ++k) {
             const int64_t e = e0 + threadIdx.x + 256 * k;
             if (e >= n) break;
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dC
         cols = qd;
     } else {
         t -= nt_dc;
-        job = t / nt_kv + 1;                       // 1: K, 2: V
+        job = t / nt_kv + 1;                       // 1: K^T, 2: V rows, 3: K rows
         t %= nt_kv;
         rows = a.L;
         cols = kvd;
@@ -131,7 +133,7 @@ __global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dC
                 x = *reinterpret_cast<const float4 *>(a.dctx + int64_t(r) * qd + c);
             } else {
                 const int kvh = c / a.hd, d = c % a.hd;
-                const float *src = (job == 1 ? a.k : a.v) + int64_t(kvh) * a.sh + int64_t(r) * a.sp + d;
+                const float *src = (job == 2 ? a.v : a.k) + int64_t(kvh) * a.sh + int64_t(r) * a.sp + d;
                 if (vec_kv) x = *reinterpret_cast<const float4 *>(src);
                 else x = make_float4(src[0], src[1], src[2], src[3]);
             }
@@ -139,13 +141,14 @@ __global__ void __launch_bounds__(256) attn_tc_prep_kernel(AttnArgs a, float *dC
         v[k] = make_float4(__uint_as_float(to_tf32(x.x)), __uint_as_float(to_tf32(x.y)),
                            __uint_as_float(to_tf32(x.z)), __uint_as_float(to_tf32(x.w)));
     }
-    if (job == 2) {
+    if (job >= 2) {
+        float *rows_out = job == 2 ? Vr : Kr;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int e = tid + 256 * k, rr = e >> 4, c = c0 + 4 * (e & 15), r = r0 + rr;
             if (r < rows) {
                 const int hh = c / a.hd, d = c % a.hd;
-                *reinterpret_cast<float4 *>(Vr + (int64_t(hh) * a.L + r) * a.hd + d) = v[k];
+                *reinterpret_cast<float4 *>(rows_out + (int64_t(hh) * a.L + r) * a.hd + d) = v[k];
             }
         }
         return;
@@ -983,6 +986,596 @@ __global__ void attn_tc_dv_sum_kernel(const float4 *__restrict__ part, float4 *_
     }
 }
 
+// ------------------------------------------------------------------ recomputed attention
+
+// The flash-style path: the attention weights are recomputed from q, the K cache and each
+// query row's logsumexp instead of read from a materialised [nh, S, L] tensor.  After the
+// prep (which also writes the tf32 K rows Kr):
+//   dV kernel, per (head, tile of 128 cache keys), over 32-query items w:
+//     S^T = K_tile q_w^T and T^T = V_tile dCtx_w^T            tcgen05.mma
+//     P^T = exp(scale S^T - lse), masked, tf32, over S^T        writer warps
+//     D_part[key tile, quarter][h, q] = sum over the quarter's 32 keys of P^T (.) T^T
+//     dV += P^T dCtx_w                                          tcgen05.mma, A from tensor memory
+//   D sum: D[h, i] = the partials of the visible key tiles in (tile, quarter) order, the
+//     softmax-backward row sum sum_j P_ij dAttn_ij;
+//   dQ kernel, per (head, tile of 128 queries), over 32-key tiles j:
+//     S_j = q K_j^T and T_j = dCtx V_j^T                        tcgen05.mma
+//     E_j = exp(scale S_j - lse) (T_j - D), masked, tf32, over T_j
+//     dQ += E_j K_j                                             tcgen05.mma, A from tensor memory
+//   then scale and RoPE backward as for the materialised path.
+constexpr int kRK = 32;         // keys per recomputed-dQ tile
+constexpr int kRBuf = 3;        // S / T buffer sets in tensor memory (an MMA set ahead of the wait)
+
+struct AttnTcRcParams {
+    CUtensorMap kr128, vr128;   // Kr, Vr {hd, L, nkv}, box {32, 128, 1}  dV: A of S^T, T^T (once)
+    CUtensorMap qrow, crow;     // q, dCtx {hd, nh, S}, box {32, 1, 32}   dV: B of S^T, T^T
+    CUtensorMap dct;            // dCT {S, hd, nh}, box {32, hd, 1}       dV: B of dV
+    CUtensorMap kr32, vr32;     // Kr, Vr {hd, L, nkv}, box {32, 32, 1}   dQ: B of S, T
+    CUtensorMap kt;             // Kt {L, hd, nkv}, box {32, hd, 1}       dQ: B of dQ
+    const float *q, *dctx, *lse;
+    float *Dpart, *D;           // [nkt * 4][nh][S], [nh][S]
+    float *dq, *dv;             // dv: [S, nkv * hd], or per-head partials [nh / nkv][S, nkv * hd]
+    const float2 *rt;           // RoPE table (rope only)
+    int S, L, nh, nkv, pos0, causal, rope, nkt;
+    float scale;
+    uint32_t *status;
+};
+
+template <int HD>
+struct DvRcLayout {
+    static constexpr int NB = HD / 32;
+    static constexpr int KV_BYTES = kVK * HD * 4;     // K or V rows [128 keys][HD]: NB atoms
+    static constexpr int QI_BYTES = kVQ * HD * 4;     // q or dCtx rows [32][HD]: NB atoms
+    static constexpr int CT_BYTES = HD * kVQ * 4;     // dCtx^T [HD][32]: one atom
+    // ring A: an item's q and dCtx rows (freed once S^T and T^T are formed); ring B: its
+    // dCtx^T (freed by its dV MMA)
+    static constexpr int SA = 2 * QI_BYTES, NS = 2;
+    static constexpr int K0 = 0, V0 = KV_BYTES, A0 = 2 * KV_BYTES, B0 = A0 + NS * SA, TOTAL = B0 + NS * CT_BYTES;
+    __host__ __device__ static constexpr int Q(int s) { return A0 + s * SA; }
+    __host__ __device__ static constexpr int C(int s) { return A0 + s * SA + QI_BYTES; }
+    __host__ __device__ static constexpr int CT(int s) { return B0 + s * CT_BYTES; }
+    // tensor memory: dV [128 keys][HD], then kRBuf sets of S^T (P^T written over it) and T^T
+    static constexpr uint32_t TS = HD, TT = HD + kRBuf * kVQ;
+    static constexpr uint32_t COLS = (HD + 2 * kRBuf * kVQ) <= 256 ? 256 : 512;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_rc_kernel(const __grid_constant__ AttnTcRcParams p) {
+    using Ly = DvRcLayout<HD>;
+    constexpr int NB = Ly::NB, NS = Ly::NS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    // kvfull: the K and V tiles; afull/afree, bfull/bfree: rings A and B; sfull: S^T and T^T of
+    // an item formed; pfull: its P^T written; tfree: its dV MMA done (the buffer set is free)
+    __shared__ uint64_t kvfull, afull[NS], afree[NS], bfull[NS], bfree[NS], sfull[kRBuf], pfull[kRBuf],
+        tfree[kRBuf], dfull;
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_abort, s_a_issued, s_a_used, s_b_issued, s_b_used;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x, G = p.nh / p.nkv, kvh = h / G, g = h % G;
+    const int k0 = int(blockIdx.y) * kVK;                           // cache keys k0 .. k0 + 127
+    const int t0 = (p.causal ? max(0, k0 - p.pos0) : 0) / kVQ;      // first item that sees key k0
+    const int nw = (p.S + kVQ - 1) / kVQ - t0;
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        s_a_issued = s_a_used = s_b_issued = s_b_used = 0;
+        mbar_init(&kvfull, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&afull[s], 1);
+            mbar_init(&afree[s], 1);
+            mbar_init(&bfull[s], 1);
+            mbar_init(&bfree[s], 1);
+        }
+        for (int b = 0; b < kRBuf; ++b) {
+            mbar_init(&sfull[b], 1);
+            mbar_init(&pfull[b], kEpiWarps);
+            mbar_init(&tfree[b], 1);
+        }
+        mbar_init(&dfull, 1);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, Ly::COLS);
+        tmem_relinquish();
+    }
+    fence_mbar_init();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tD = tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producers: lane 0 the K and V
+        // tiles and ring A, lane 1 ring B
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&kvfull, 2 * Ly::KV_BYTES);
+            for (int b = 0; b < NB; ++b) {
+                tma_load_3d(sm + Ly::K0 + b * (kVK * 128), &p.kr128, b * 32, k0, kvh, &kvfull);
+                tma_load_3d(sm + Ly::V0 + b * (kVK * 128), &p.vr128, b * 32, k0, kvh, &kvfull);
+            }
+            for (int w = 0; w < nw; ++w) {
+                const int s = w % NS, qa = (t0 + w) * kVQ;
+                if (w >= NS && !mbar_wait(&afree[s], (w / NS - 1) & 1, p.status, 40u)) {
+                    s_abort = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&afull[s], Ly::SA);
+                for (int b = 0; b < NB; ++b) {
+                    tma_load_3d(sm + Ly::Q(s) + b * (kVQ * 128), &p.qrow, b * 32, h, qa, &afull[s]);
+                    tma_load_3d(sm + Ly::C(s) + b * (kVQ * 128), &p.crow, b * 32, h, qa, &afull[s]);
+                }
+                s_a_issued = w + 1;
+            }
+        } else if (lane == 1) {
+            for (int w = 0; w < nw; ++w) {
+                const int s = w % NS, qa = (t0 + w) * kVQ;
+                if (w >= NS && !mbar_wait(&bfree[s], (w / NS - 1) & 1, p.status, 41u)) {
+                    s_abort = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bfull[s], Ly::CT_BYTES);
+                tma_load_3d(sm + Ly::CT(s), &p.dct, qa, 0, h, &bfull[s]);
+                s_b_issued = w + 1;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_tf32(kVK, kVQ), idV = idesc_tf32(kVK, HD);
+            auto issue = [&](int w) -> bool {      // S^T_w and T^T_w into buffer set w % kRBuf
+                const int s = w % NS, b = w % kRBuf;
+                if (!mbar_wait(&afull[s], (w / NS) & 1, p.status, 42u)) return false;
+                if (w >= kRBuf && !mbar_wait(&tfree[b], (w / kRBuf - 1) & 1, p.status, 43u)) return false;
+                s_a_used = w + 1;
+                tc_fence_after();
+#pragma unroll
+                for (int kb = 0; kb < NB; ++kb)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t acc = (kb | k) ? 1u : 0u;
+                        mma_tf32(tD + Ly::TS + uint32_t(b * kVQ), sw128_desc(sm + Ly::K0 + kb * (kVK * 128)) + 2 * k,
+                                 sw128_desc(sm + Ly::Q(s) + kb * (kVQ * 128)) + 2 * k, idS, acc);
+                        mma_tf32(tD + Ly::TT + uint32_t(b * kVQ), sw128_desc(sm + Ly::V0 + kb * (kVK * 128)) + 2 * k,
+                                 sw128_desc(sm + Ly::C(s) + kb * (kVQ * 128)) + 2 * k, idS, acc);
+                    }
+                mma_commit(&afree[s]);
+                mma_commit(&sfull[b]);
+                return true;
+            };
+            bool ok = mbar_wait(&kvfull, 0, p.status, 44u);
+            tc_fence_after();
+            ok = ok && issue(0) && (nw < 2 || issue(1));
+            for (int w = 0; ok && w < nw; ++w) {
+                const int s = w % NS, b = w % kRBuf;
+                if (!mbar_wait(&pfull[b], (w / kRBuf) & 1, p.status, 45u) ||
+                    !mbar_wait(&bfull[s], (w / NS) & 1, p.status, 46u)) {
+                    ok = false;
+                    break;
+                }
+                s_b_used = w + 1;
+                tc_fence_after();
+                const uint64_t bd = sw128_desc(sm + Ly::CT(s));
+#pragma unroll
+                for (int k = 0; k < kVQ / 8; ++k)
+                    mma_tf32_ts(tD, tD + Ly::TS + uint32_t(b * kVQ + 8 * k), bd + 2 * k, idV, (w > 0 || k > 0) ? 1u : 0u);
+                mma_commit(&bfree[s]);
+                mma_commit(&tfree[b]);
+                // S^T / T^T of item w + 2 take the buffer set of item w - 1, whose dV MMA was
+                // issued one item ago: the wait overlaps dV_w in the tensor pipe
+                if (w + 2 < nw && !(ok = issue(w + 2))) break;
+            }
+            if (!ok) s_abort = 1;
+            mma_commit(&dfull);
+            mbar_wait(&dfull, 0, nullptr, 0u);
+        }
+    } else {
+        // ------------------------------------------------ writers: one key row and half of the
+        // item's queries per thread; then the dV epilogue
+        const int quarter = warp & 3, hf = (warp - 2) >> 2;
+        const int r = quarter * 32 + lane, key = k0 + r;
+        const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+        const float *lse_h = p.lse + int64_t(h) * p.S;
+        float *dpart = p.Dpart + (int64_t(int(blockIdx.y) * 4 + quarter) * p.nh + h) * p.S;
+        // the query of the item's half whose sum over this warp's keys this lane ends with
+        const int b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1, b1 = (lane >> 1) & 1;
+        const int cq = 8 * b4 + 4 * b3 + 2 * b2 + b1;
+        bool ok = true;
+        for (int w = 0; w < nw; ++w) {
+            const int b = w % kRBuf, qa = (t0 + w) * kVQ + hf * 16;
+            float l[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) l[c] = qa + c < p.S ? __ldg(lse_h + qa + c) : 0.f;
+            if (!mbar_wait(&sfull[b], (w / kRBuf) & 1, p.status, 47u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[16], tv[16];
+            tmem_ld16(tD + Ly::TS + uint32_t(b * kVQ + hf * 16) + lane_off, sv);
+            tmem_ld16(tD + Ly::TT + uint32_t(b * kVQ + hf * 16) + lane_off, tv);
+            tmem_wait_ld();
+            float e[16];
+            uint32_t pt[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const int qi = qa + c;
+                const bool vis = qi < p.S && key < p.L && (!p.causal || key <= p.pos0 + qi);
+                const float pv = vis ? expf(p.scale * __uint_as_float(sv[c]) - l[c]) : 0.f;
+                e[c] = pv * __uint_as_float(tv[c]);
+                pt[c] = to_tf32(pv);
+            }
+            tmem_st16(tD + Ly::TS + uint32_t(b * kVQ + hf * 16) + lane_off, pt);     // P^T over S^T
+            // sum of e over the warp's 32 keys by halving exchanges: each level keeps half of
+            // the queries and adds the partner's values of that half
+            float v8[8], v4[4], v2[2];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float send = b4 ? e[i] : e[8 + i];
+                v8[i] = (b4 ? e[8 + i] : e[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float send = b3 ? v8[i] : v8[4 + i];
+                v4[i] = (b3 ? v8[4 + i] : v8[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float send = b2 ? v4[i] : v4[2 + i];
+                v2[i] = (b2 ? v4[2 + i] : v4[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
+            }
+            float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
+            v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+            if ((lane & 1) == 0 && qa + cq < p.S) dpart[qa + cq] = v1;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pfull[b]);
+        }
+        if (ok && mbar_wait(&dfull, 0, p.status, 48u)) {
+            tc_fence_after();
+            // the rings are idle (every copy consumed, every MMA done): each warp turns its
+            // 32 x 32 blocks there so that the stores coalesce; only the S newest keys have dV
+            float *blk = reinterpret_cast<float *>(sm) + (warp - 2) * 32 * 33;
+            const int64_t kvd = int64_t(p.nkv) * HD;
+            float *out = p.dv + (G > 1 ? int64_t(g) * p.S * kvd : 0) + kvh * HD;
+            const int c4 = (lane & 7) * 4, rl = lane >> 3, first = p.L - p.S;
+#pragma unroll 1
+            for (int c = hf * (HD / 2); c < (hf + 1) * (HD / 2); c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tD + uint32_t(c) + lane_off, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int t = 0; t < 32; ++t) blk[lane * 33 + t] = __uint_as_float(v[t]);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int rr = 4 * k + rl, kk = k0 + quarter * 32 + rr;
+                    const float *a = blk + rr * 33 + c4;
+                    if (kk >= first && kk < p.L)
+                        *reinterpret_cast<float4 *>(out + int64_t(kk - first) * kvd + c + c4) =
+                            make_float4(a[0], a[1], a[2], a[3]);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok) s_abort = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (s_abort && threadIdx.x == 0) {
+        mbar_wait(&kvfull, 0, nullptr, 0u);
+        for (int w = max(s_a_used, s_a_issued - NS); w < s_a_issued; ++w)
+            mbar_wait(&afull[w % NS], (w / NS) & 1, nullptr, 0u);
+        for (int w = max(s_b_used, s_b_issued - NS); w < s_b_issued; ++w)
+            mbar_wait(&bfull[w % NS], (w / NS) & 1, nullptr, 0u);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tD, Ly::COLS);
+    }
+}
+
+// D[h, i] = the partial row sums of the key tiles that row i sees, in (tile, quarter) order.
+__global__ void attn_tc_dsum_kernel(const float *__restrict__ Dpart, float *__restrict__ D, int S, int nh, int nkt,
+                                    int pos0, int causal) {
+    const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (e >= int64_t(nh) * S) return;
+    const int h = int(e / S), i = int(e % S);
+    const int lim = causal ? min(nkt, (pos0 + i) / kVK + 1) : nkt;      // tiles with first key <= pos0 + i
+    const int64_t stride = int64_t(nh) * S;
+    const float *src = Dpart + int64_t(h) * S + i;
+    float acc = 0.f;
+    for (int t0 = 0; t0 < lim; t0 += 4) {          // sixteen loads in flight, then the sum in order
+        float v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = t0 + k / 4 < lim ? __ldg(src + int64_t(t0 * 4 + k) * stride) : 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc += v[k];
+    }
+    D[e] = acc;
+}
+
+template <int HD>
+struct DqRcLayout {
+    static constexpr int NB = HD / 32;
+    static constexpr int Q_BYTES = kQM * HD * 4;      // q tile [128 rows][HD]: NB atoms (A of S)
+    static constexpr int R_BYTES = kRK * HD * 4;      // K or V rows [32 keys][HD]: NB atoms
+    static constexpr int KT_BYTES = HD * kRK * 4;     // K^T [HD][32 keys]: one atom
+    // ring A: a tile's K and V rows (freed once S and T are formed); ring B: its K^T (freed
+    // by its dQ MMA)
+    static constexpr int SA = 2 * R_BYTES, NS = 3;
+    static constexpr int A0 = Q_BYTES, B0 = A0 + NS * SA, TOTAL = B0 + NS * KT_BYTES;
+    __host__ __device__ static constexpr int KR(int s) { return A0 + s * SA; }
+    __host__ __device__ static constexpr int VR(int s) { return A0 + s * SA + R_BYTES; }
+    __host__ __device__ static constexpr int KT(int s) { return B0 + s * KT_BYTES; }
+    // tensor memory: dCtx (A of T), dQ, kRBuf sets of S and T (E written over T), [128][32] each
+    static constexpr uint32_t TDC = 0, TQD = HD, TS = 2 * HD, TT = 2 * HD + kRBuf * kRK;
+    static constexpr uint32_t COLS = (2 * HD + 2 * kRBuf * kRK) <= 256 ? 256 : 512;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_rc_kernel(const __grid_constant__ AttnTcRcParams p) {
+    using Ly = DqRcLayout<HD>;
+    constexpr int NB = Ly::NB, NS = Ly::NS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    // afull/afree, bfull/bfree: rings A and B; qready: q in shared memory and dCtx in tensor
+    // memory; sfull: S_j and T_j formed; efull: E_j written; tfree: dQ_j done
+    __shared__ uint64_t afull[NS], afree[NS], bfull[NS], bfree[NS], qready, sfull[kRBuf], efull[kRBuf],
+        tfree[kRBuf], dfull;
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_abort, s_a_issued, s_a_used, s_b_issued, s_b_used;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x, kvh = h / (p.nh / p.nkv);
+    const int q0 = int(gridDim.y - 1 - blockIdx.y) * kQM;      // longest tiles first
+    const int kend = p.causal ? min(p.L, p.pos0 + q0 + kQM) : p.L;
+    const int nt = (kend + kRK - 1) / kRK;
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        s_a_issued = s_a_used = s_b_issued = s_b_used = 0;
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&afull[s], 1);
+            mbar_init(&afree[s], 1);
+            mbar_init(&bfull[s], 1);
+            mbar_init(&bfree[s], 1);
+        }
+        mbar_init(&qready, kEpiWarps);
+        for (int b = 0; b < kRBuf; ++b) {
+            mbar_init(&sfull[b], 1);
+            mbar_init(&efull[b], kEpiWarps / 2);    // the four warps of the group that forms E_j
+            mbar_init(&tfree[b], 1);
+        }
+        mbar_init(&dfull, 1);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, Ly::COLS);
+        tmem_relinquish();
+    }
+    fence_mbar_init();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producers: lane 0 ring A, lane 1 ring B
+        if (lane == 0) {
+            for (int j = 0; j < nt; ++j) {
+                const int s = j % NS, k0 = j * kRK;
+                if (j >= NS && !mbar_wait(&afree[s], (j / NS - 1) & 1, p.status, 50u)) {
+                    s_abort = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&afull[s], Ly::SA);
+                for (int b = 0; b < NB; ++b) {
+                    tma_load_3d(sm + Ly::KR(s) + b * (kRK * 128), &p.kr32, b * 32, k0, kvh, &afull[s]);
+                    tma_load_3d(sm + Ly::VR(s) + b * (kRK * 128), &p.vr32, b * 32, k0, kvh, &afull[s]);
+                }
+                s_a_issued = j + 1;
+            }
+        } else if (lane == 1) {
+            for (int j = 0; j < nt; ++j) {
+                const int s = j % NS;
+                if (j >= NS && !mbar_wait(&bfree[s], (j / NS - 1) & 1, p.status, 51u)) {
+                    s_abort = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bfull[s], Ly::KT_BYTES);
+                tma_load_3d(sm + Ly::KT(s), &p.kt, j * kRK, 0, kvh, &bfull[s]);
+                s_b_issued = j + 1;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_tf32(kQM, kRK), idQ = idesc_tf32(kQM, HD);
+            auto issue = [&](int j) -> bool {      // S_j and T_j into buffer set j % kRBuf
+                const int s = j % NS, b = j % kRBuf;
+                if (!mbar_wait(&afull[s], (j / NS) & 1, p.status, 52u)) return false;
+                if (j >= kRBuf && !mbar_wait(&tfree[b], (j / kRBuf - 1) & 1, p.status, 53u)) return false;
+                s_a_used = j + 1;
+                tc_fence_after();
+#pragma unroll
+                for (int kb = 0; kb < NB; ++kb)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t acc = (kb | k) ? 1u : 0u;
+                        mma_tf32(tm + Ly::TS + uint32_t(b * kRK), sw128_desc(sm + kb * (kQM * 128)) + 2 * k,
+                                 sw128_desc(sm + Ly::KR(s) + kb * (kRK * 128)) + 2 * k, idS, acc);
+                        mma_tf32_ts(tm + Ly::TT + uint32_t(b * kRK), tm + Ly::TDC + uint32_t(kb * 32 + k * 8),
+                                    sw128_desc(sm + Ly::VR(s) + kb * (kRK * 128)) + 2 * k, idS, acc);
+                    }
+                mma_commit(&afree[s]);
+                mma_commit(&sfull[b]);
+                return true;
+            };
+            bool ok = mbar_wait(&qready, 0, p.status, 54u);
+            tc_fence_after();
+            ok = ok && issue(0) && (nt < 2 || issue(1));
+            for (int j = 0; ok && j < nt; ++j) {
+                const int s = j % NS, b = j % kRBuf;
+                if (!mbar_wait(&efull[b], (j / kRBuf) & 1, p.status, 55u) ||
+                    !mbar_wait(&bfull[s], (j / NS) & 1, p.status, 56u)) {
+                    ok = false;
+                    break;
+                }
+                s_b_used = j + 1;
+                tc_fence_after();
+                const uint64_t kd = sw128_desc(sm + Ly::KT(s));
+#pragma unroll
+                for (int k = 0; k < kRK / 8; ++k)
+                    mma_tf32_ts(tm + Ly::TQD, tm + Ly::TT + uint32_t(b * kRK + 8 * k), kd + 2 * k, idQ,
+                                (j > 0 || k > 0) ? 1u : 0u);
+                mma_commit(&bfree[s]);
+                mma_commit(&tfree[b]);
+                // S_j+2 / T_j+2 take the buffer set of tile j - 1, whose dQ MMA was issued one
+                // tile ago: the wait overlaps dQ_j in the tensor pipe
+                if (j + 2 < nt && !(ok = issue(j + 2))) break;
+            }
+            if (!ok) s_abort = 1;
+            mma_commit(&dfull);
+            mbar_wait(&dfull, 0, nullptr, 0u);
+        }
+    } else {
+        // ------------------------------------------------ writers: two groups of four warps
+        // (one per TMEM lane quarter), one query row per thread
+        const int quarter = warp & 3, hf = (warp - 2) >> 2;
+        const int r = quarter * 32 + lane, i = q0 + r;
+        const bool row_ok = i < p.S;
+        const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+        const int jlast = p.causal ? p.pos0 + i : p.L - 1;      // last visible key
+        {   // this row's half of q (tf32) into the q tile (the A operand of S, 128-byte
+            // swizzled atoms of 32 columns) and of dCtx (tf32) into tensor memory (A of T)
+            const int64_t ro = int64_t(row_ok ? i : 0) * (p.nh * HD) + h * HD + hf * (HD / 2);
+            const float4 *qs = reinterpret_cast<const float4 *>(p.q + ro);
+            const float4 *cs = reinterpret_cast<const float4 *>(p.dctx + ro);
+            float4 xq[HD / 8], xc[HD / 8];
+#pragma unroll
+            for (int k = 0; k < HD / 8; ++k) {
+                xq[k] = row_ok ? qs[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+                xc[k] = row_ok ? cs[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < HD / 8; ++k) {
+                const int col = hf * (HD / 2) + 4 * k;          // column of the row
+                st_shared_v4(sm + (col >> 5) * (kQM * 128) + sw128_off(r, (col & 31) >> 2), to_tf32(xq[k].x),
+                             to_tf32(xq[k].y), to_tf32(xq[k].z), to_tf32(xq[k].w));
+            }
+#pragma unroll
+            for (int c = 0; c < HD / 2; c += 16) {
+                uint32_t v[16];
+#pragma unroll
+                for (int t = 0; t < 16; t += 4) {
+                    const float4 y = xc[(c + t) / 4];
+                    v[t] = to_tf32(y.x);
+                    v[t + 1] = to_tf32(y.y);
+                    v[t + 2] = to_tf32(y.z);
+                    v[t + 3] = to_tf32(y.w);
+                }
+                tmem_st16(tm + Ly::TDC + uint32_t(hf * (HD / 2) + c) + lane_off, v);
+            }
+            tmem_wait_st();
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&qready);
+        }
+        const float lse_i = row_ok ? __ldg(p.lse + int64_t(h) * p.S + i) : 0.f;
+        const float D_i = row_ok ? __ldg(p.D + int64_t(h) * p.S + i) : 0.f;
+        // Key tiles alternate between the two groups of four warps
+        bool ok = true;
+        for (int j = hf; j < nt; j += 2) {
+            const int b = j % kRBuf, ka = j * kRK;
+            if (!mbar_wait(&sfull[b], (j / kRBuf) & 1, p.status, 57u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[32], tv[32];
+            tmem_ld32(tm + Ly::TS + uint32_t(b * kRK) + lane_off, sv);
+            tmem_ld32(tm + Ly::TT + uint32_t(b * kRK) + lane_off, tv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const bool vis = row_ok && ka + c <= jlast;
+                const float pv = vis ? expf(p.scale * __uint_as_float(sv[c]) - lse_i) : 0.f;
+                tv[c] = to_tf32(pv * (__uint_as_float(tv[c]) - D_i));
+            }
+            tmem_st32(tm + Ly::TT + uint32_t(b * kRK) + lane_off, tv);       // E_j over T_j
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&efull[b]);
+        }
+        if (ok && mbar_wait(&dfull, 0, p.status, 58u)) {
+            tc_fence_after();
+            constexpr int half = HD / 2, q4 = HD / 4;
+            float *out0 = p.dq + h * HD;
+            const float4 *rt4 = reinterpret_cast<const float4 *>(p.rt + int64_t(row_ok ? i : 0) * half);
+            float *blk = reinterpret_cast<float *>(sm) + (warp - 2) * 32 * 33;
+            const int c4 = (lane & 7) * 4, rl = lane >> 3;
+#pragma unroll 1
+            for (int c = hf * q4; c < (hf + 1) * q4; c += 16) {      // pairs (c, c + HD / 2)
+                float4 cs[8];
+                if (p.rope) {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) cs[t] = rt4[c / 2 + t];
+                }
+                uint32_t u1[16], u2[16];
+                tmem_ld16(tm + Ly::TQD + uint32_t(c) + lane_off, u1);
+                tmem_ld16(tm + Ly::TQD + uint32_t(c + half) + lane_off, u2);
+                tmem_wait_ld();
+                float y1[16], y2[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    float a1 = p.scale * __uint_as_float(u1[t]), a2 = p.scale * __uint_as_float(u2[t]);
+                    if (p.rope) {
+                        const float4 qv = cs[t / 2];
+                        const float co = (t & 1) ? qv.z : qv.x, sn = (t & 1) ? qv.w : qv.y;
+                        const float b1 = a1 * co + a2 * sn, b2 = -a1 * sn + a2 * co;
+                        a1 = b1;
+                        a2 = b2;
+                    }
+                    y1[t] = a1;
+                    y2[t] = a2;
+                }
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    blk[lane * 33 + t] = y1[t];
+                    blk[lane * 33 + 16 + t] = y2[t];
+                }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int rr = 4 * k + rl, ii = q0 + quarter * 32 + rr;
+                    const float *a = blk + rr * 33 + c4;
+                    if (ii < p.S)
+                        *reinterpret_cast<float4 *>(out0 + int64_t(ii) * (p.nh * HD) +
+                                                    (c4 < 16 ? c + c4 : c + half + c4 - 16)) =
+                            make_float4(a[0], a[1], a[2], a[3]);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok) s_abort = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (s_abort && threadIdx.x == 0) {
+        for (int j = max(s_a_used, s_a_issued - NS); j < s_a_issued; ++j)
+            mbar_wait(&afull[j % NS], (j / NS) & 1, nullptr, 0u);
+        for (int j = max(s_b_used, s_b_issued - NS); j < s_b_issued; ++j)
+            mbar_wait(&bfull[j % NS], (j / NS) & 1, nullptr, 0u);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tm, Ly::COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 // fp32 3-D tensor map, 128-byte swizzle, zero fill out of range.  dims / box innermost
@@ -1003,11 +1596,12 @@ int make_map_f32_3d(CUtensorMap *m, const void *base, const uint64_t dims[3], co
 }
 
 struct TcAttnWs {
-    size_t dCT, Kt, Vr, part, rt, total;
+    size_t dCT, Kt, Vr, part, rt, Kr, Dpart, Dd, total;
     int64_t S4, L4;
 };
 
-TcAttnWs tc_attn_layout(int64_t S, int64_t L, int nh, int nkv, int hd) {
+// rc: the recomputed-attention path, which adds the K rows and the row-sum partials.
+TcAttnWs tc_attn_layout(int64_t S, int64_t L, int nh, int nkv, int hd, bool rc = false) {
     auto r256 = [](size_t b) { return (b + 255) & ~size_t(255); };
     TcAttnWs w;
     w.S4 = (S + 3) & ~int64_t(3);
@@ -1017,7 +1611,11 @@ TcAttnWs tc_attn_layout(int64_t S, int64_t L, int nh, int nkv, int hd) {
     w.Vr = w.Kt + r256(size_t(nkv) * hd * w.L4 * 4);
     w.part = w.Vr + r256(size_t(nkv) * L * hd * 4);
     w.rt = w.part + (nh > nkv ? r256(size_t(nh) * S * hd * 4) : 0);      // per-head dV sums
-    w.total = w.rt + r256(size_t(S) * (hd / 2) * 8);                      // RoPE table
+    w.Kr = w.rt + r256(size_t(S) * (hd / 2) * 8);                         // RoPE table
+    const int64_t nkt = (L + kVK - 1) / kVK;
+    w.Dpart = w.Kr + (rc ? r256(size_t(nkv) * L * hd * 4) : 0);
+    w.Dd = w.Dpart + (rc ? r256(size_t(nkt) * 4 * nh * S * 4) : 0);
+    w.total = w.Dd + (rc ? r256(size_t(nh) * S * 4) : 0);
     return w;
 }
 
@@ -1033,7 +1631,7 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     float2 *rt = reinterpret_cast<float2 *>(base + w.rt);
     const int nt_rt = a.rope ? int(ceil_div(int64_t(a.S) * (HD / 2), int64_t(1024))) : 0;
     attn_tc_prep_kernel<<<unsigned(nt_dc + 2 * nt_kv + nt_rt), 256, 0, st>>>(a, dCT, Kt, Vr, int(w.S4), int(w.L4),
-                                                                            nt_dc, nt_kv, vec_kv, fr, rt);
+                                                                            nt_dc, nt_kv, vec_kv, fr, rt, nullptr);
     TLB_TRY(check_launch("attn_tc_prep"));
 
     AttnTcParams p;
@@ -1113,7 +1711,7 @@ int launch_attn_tc_dk(const AttnArgs &a, const float *q, const float *D, float *
     const int nt_q = int(ceil_div(a.S, kPrepT)) * int(qd / kPrepT);
     const RopeFreqs no_rope{};
     attn_tc_prep_kernel<<<unsigned(nt_q), 256, 0, st>>>(aq, QT, nullptr, nullptr, int(w.S4), int(w.L4), nt_q, 0, 0,
-                                                        no_rope, nullptr);
+                                                        no_rope, nullptr, nullptr);
     TLB_TRY(check_launch("attn_tc_prep_q"));
 
     AttnTcDkParams p;
@@ -1164,6 +1762,92 @@ int launch_attn_tc_dk(const AttnArgs &a, const float *q, const float *D, float *
     return check_launch("attn_tc_dk_sum");
 }
 
+// The recomputed-attention path (attention weights from q, K and lse).
+template <int HD>
+int launch_attn_tc_rc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32_t *status, cudaStream_t st) {
+    const TcAttnWs w = tc_attn_layout(a.S, a.L, a.nh, a.nkv, HD, true);
+    char *base = static_cast<char *>(scratch);
+    float *dCT = reinterpret_cast<float *>(base + w.dCT);
+    float *Kt = reinterpret_cast<float *>(base + w.Kt), *Vr = reinterpret_cast<float *>(base + w.Vr);
+    float *Kr = reinterpret_cast<float *>(base + w.Kr);
+    float2 *rt = reinterpret_cast<float2 *>(base + w.rt);
+    const int nt_dc = int(ceil_div(a.S, kPrepT)) * (a.nh * HD / kPrepT);
+    const int nt_kv = int(ceil_div(a.L, kPrepT)) * (a.nkv * HD / kPrepT);
+    const int nt_rt = a.rope ? int(ceil_div(int64_t(a.S) * (HD / 2), int64_t(1024))) : 0;
+    const int vec_kv = aligned16(a.k) && aligned16(a.v) && a.sh % 4 == 0 && a.sp % 4 == 0;
+    attn_tc_prep_kernel<<<unsigned(nt_dc + 3 * nt_kv + nt_rt), 256, 0, st>>>(a, dCT, Kt, Vr, int(w.S4), int(w.L4),
+                                                                            nt_dc, nt_kv, vec_kv, fr, rt, Kr);
+    TLB_TRY(check_launch("attn_tc_prep"));
+
+    AttnTcRcParams p;
+    memset(&p, 0, sizeof(p));
+    {
+        const uint64_t d[3] = {uint64_t(HD), uint64_t(a.L), uint64_t(a.nkv)};
+        const uint64_t s[2] = {uint64_t(HD) * 4, uint64_t(a.L) * HD * 4};
+        const uint32_t b128[3] = {32, uint32_t(kVK), 1}, b32[3] = {32, uint32_t(kRK), 1};
+        TLB_TRY(make_map_f32_3d(&p.kr128, Kr, d, s, b128));
+        TLB_TRY(make_map_f32_3d(&p.vr128, Vr, d, s, b128));
+        TLB_TRY(make_map_f32_3d(&p.kr32, Kr, d, s, b32));
+        TLB_TRY(make_map_f32_3d(&p.vr32, Vr, d, s, b32));
+    }
+    {
+        const uint64_t d[3] = {uint64_t(HD), uint64_t(a.nh), uint64_t(a.S)};
+        const uint64_t s[2] = {uint64_t(HD) * 4, uint64_t(a.nh) * HD * 4};
+        const uint32_t b[3] = {32, 1, uint32_t(kVQ)};
+        TLB_TRY(make_map_f32_3d(&p.qrow, a.q, d, s, b));
+        TLB_TRY(make_map_f32_3d(&p.crow, a.dctx, d, s, b));
+    }
+    {
+        const uint64_t d[3] = {uint64_t(a.S), uint64_t(HD), uint64_t(a.nh)};
+        const uint64_t s[2] = {uint64_t(w.S4) * 4, uint64_t(w.S4) * HD * 4};
+        const uint32_t b[3] = {32, uint32_t(HD), 1};
+        TLB_TRY(make_map_f32_3d(&p.dct, dCT, d, s, b));
+    }
+    {
+        const uint64_t d[3] = {uint64_t(a.L), uint64_t(HD), uint64_t(a.nkv)};
+        const uint64_t s[2] = {uint64_t(w.L4) * 4, uint64_t(w.L4) * HD * 4};
+        const uint32_t b[3] = {32, uint32_t(HD), 1};
+        TLB_TRY(make_map_f32_3d(&p.kt, Kt, d, s, b));
+    }
+    const int G = a.nh / a.nkv;
+    float *part = reinterpret_cast<float *>(base + w.part);
+    p.q = a.q;
+    p.dctx = a.dctx;
+    p.lse = a.lse;
+    p.Dpart = reinterpret_cast<float *>(base + w.Dpart);
+    p.D = a.D != nullptr ? a.D : reinterpret_cast<float *>(base + w.Dd);
+    p.dq = a.dq;
+    p.dv = G > 1 ? part : a.dv;
+    p.rt = rt;
+    p.S = a.S;
+    p.L = a.L;
+    p.nh = a.nh;
+    p.nkv = a.nkv;
+    p.pos0 = a.pos0;
+    p.causal = a.causal;
+    p.rope = a.rope;
+    p.nkt = int(ceil_div(int64_t(a.L), int64_t(kVK)));
+    p.scale = a.scale;
+    p.status = status;
+
+    const int smv = DvRcLayout<HD>::TOTAL + 1024, smq = DqRcLayout<HD>::TOTAL + 1024;
+    TLB_CUDA(cudaFuncSetAttribute(attn_tc_dv_rc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smv));
+    TLB_CUDA(cudaFuncSetAttribute(attn_tc_dq_rc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smq));
+    attn_tc_dv_rc_kernel<HD><<<dim3(unsigned(a.nh), unsigned(p.nkt)), kAttnThreads, smv, st>>>(p);
+    TLB_TRY(check_launch("attn_tc_dv_rc"));
+    const int64_t nd = int64_t(a.nh) * a.S;
+    attn_tc_dsum_kernel<<<unsigned(ceil_div(nd, int64_t(256))), 256, 0, st>>>(p.Dpart, p.D, a.S, a.nh, p.nkt, a.pos0,
+                                                                            a.causal);
+    TLB_TRY(check_launch("attn_tc_dsum"));
+    attn_tc_dq_rc_kernel<HD><<<dim3(unsigned(a.nh), unsigned(ceil_div(a.S, kQM))), kAttnThreads, smq, st>>>(p);
+    TLB_TRY(check_launch("attn_tc_dq_rc"));
+    if (G == 1) return TLB_OK;
+    const int64_t n4 = int64_t(a.S) * a.nkv * HD / 4;
+    attn_tc_dv_sum_kernel<<<stream_grid(n4, 256), 256, 0, st>>>(reinterpret_cast<const float4 *>(part),
+                                                                reinterpret_cast<float4 *>(a.dv), n4, G);
+    return check_launch("attn_tc_dv_sum");
+}
+
 }  // namespace
 
 bool attn_tc_supported(int64_t S, int64_t L, int nh, int nkv, int hd) {
@@ -1195,11 +1879,19 @@ int attn_tc_launch(const AttnArgs &a, float rope_base, void *scratch, uint32_t *
     if (a.S == 0) return TLB_OK;
     TLB_REQUIRE(attn_tc_supported(a.S, a.L, a.nh, a.nkv, a.hd), TLB_EUNSUPPORTED, "attention (tcgen05): shape");
     TLB_REQUIRE((reinterpret_cast<uintptr_t>(scratch) & 255u) == 0, TLB_EINVAL, "attention (tcgen05): scratch alignment");
-    TLB_REQUIRE(aligned16(a.attn) && aligned16(a.dq) && aligned16(a.dv) && aligned16(a.dctx), TLB_EUNSUPPORTED,
-                "attention (tcgen05): attn / dq / dv not 16-byte aligned");
+    const bool rc = a.lse != nullptr;
+    TLB_REQUIRE((rc ? aligned16(a.q) : aligned16(a.attn)) && aligned16(a.dq) && aligned16(a.dv) && aligned16(a.dctx),
+                TLB_EUNSUPPORTED, "attention (tcgen05): attn or q / dq / dv / dctx not 16-byte aligned");
     RopeFreqs fr;
     rope_freqs(fr, a.hd, rope_base);
+    if (rc)
+        return a.hd == 128 ? launch_attn_tc_rc<128>(a, fr, scratch, status, st)
+                           : launch_attn_tc_rc<64>(a, fr, scratch, status, st);
     return a.hd == 128 ? launch_attn_tc<128>(a, fr, scratch, status, st) : launch_attn_tc<64>(a, fr, scratch, status, st);
+}
+
+size_t attn_tc_rc_bytes(int64_t S, int64_t L, int nh, int nkv, int hd) {
+    return tc_attn_layout(S, L, nh, nkv, hd, true).total;
 }
 
 }  // namespace tlb

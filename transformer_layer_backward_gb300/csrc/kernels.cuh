@@ -94,7 +94,10 @@ int attn_dk_launch(const AttnArgs &a, const float *q, const float *D, float *dk,
 // L - S multiples of 4; attn, dq and dv 16-byte aligned.  scratch: attn_tc_bytes(...) bytes, 256-byte aligned.
 bool attn_tc_supported(int64_t S, int64_t L, int nh, int nkv, int hd);
 size_t attn_tc_bytes(int64_t S, int64_t L, int nh, int nkv, int hd);
+// With a.lse set (recomputed attention) the same entry runs the flash-style kernels (q 16-byte
+// aligned instead of attn; attn unused); scratch: attn_tc_rc_bytes(...) bytes.
 int attn_tc_launch(const AttnArgs &a, float rope_base, void *scratch, uint32_t *status, cudaStream_t st);
+size_t attn_tc_rc_bytes(int64_t S, int64_t L, int nh, int nkv, int hd);
 // Key gradient of the S newest keys on tcgen05 (the exact input gradient), after
 // attn_tc_launch on the same scratch (its tf32 V copy and per-head partial buffer are
 // reused); extra: attn_tc_dk_bytes(...) bytes, 16-byte aligned.  dk as attn_dk_launch.

@@ -37,6 +37,14 @@ bool attn_tc_route(const tlb_layer_cfg &c, int64_t S, int64_t L) {
            attn_tc_supported(S, L, c.n_heads, c.n_kv_heads, c.head_dim);
 }
 
+// The recomputed attention (TLB_RECOMPUTE_P) runs its flash-style tcgen05 kernels on the
+// same layers; with the exact input gradient it keeps the CUDA-core kernels, whose key
+// gradient recomputes too.
+bool attn_tc_rc_route(const tlb_layer_cfg &c, int64_t S, int64_t L) {
+    return c.wtype == TLB_W_BF16 && (c.flags & TLB_RECOMPUTE_P) && !(c.flags & TLB_EXACT_DIN) &&
+           attn_tc_supported(S, L, c.n_heads, c.n_kv_heads, c.head_dim);
+}
+
 LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     WsPlan p;
     LayerWs w;
@@ -55,7 +63,9 @@ LayerWs plan(const tlb_layer_cfg &c, int64_t S, int64_t L) {
     } else {
         w.abf = w.gbf = w.ubf = w.part = 0;
     }
-    w.atc = attn_tc_route(c, S, L) ? p.take(attn_tc_bytes(S, L, c.n_heads, c.n_kv_heads, c.head_dim)) : 0;
+    w.atc = attn_tc_route(c, S, L)      ? p.take(attn_tc_bytes(S, L, c.n_heads, c.n_kv_heads, c.head_dim))
+            : attn_tc_rc_route(c, S, L) ? p.take(attn_tc_rc_bytes(S, L, c.n_heads, c.n_kv_heads, c.head_dim))
+                                        : 0;
     w.dF = p.take(S * I * 4);
     w.dG = p.take(S * I * 4);
     w.dU = p.take(S * I * 4);
@@ -249,7 +259,8 @@ int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, co
         TLB_TRY(rmsnorm_backward_launch(a.ctx, w.gamma_sub_attn, dSub, dSub, S, qd, c.norm_eps, 0, st));
     AttnArgs g = attn_args(c, S, L, dSub, a, d_qpre, d_v);
     g.D = D;
-    if (attn_tc_route(c, S, L) && aligned16(d_qpre) && aligned16(d_v) && aligned16(a.attn))
+    if ((attn_tc_route(c, S, L) && aligned16(d_qpre) && aligned16(d_v) && aligned16(a.attn)) ||
+        (attn_tc_rc_route(c, S, L) && aligned16(d_qpre) && aligned16(d_v) && aligned16(a.q)))
         TLB_TRY(attn_tc_launch(g, c.rope_base, ws_at<void>(ws, p.atc), ws_at<uint32_t>(ws, 0), st));
     else
         TLB_TRY(attn_core_launch(g, c.rope_base, st));
@@ -617,7 +628,7 @@ static int layer_backward_impl(const tlb_layer_cfg *cfg, int64_t S, int64_t L, c
     // on the tensor cores where the attention backward ran there (the same tf32 class)
     TLB_TRY(lora_seq_launch(S, c.dim, c.rank, c.lora_alpha, acts->x, jobs, 2, *adam, sumsq, st,
                             chk ? status : nullptr, exact ? exact_dst(c, d_hidden, ws, p) : nullptr,
-                            attn_tc_route(c, S, L) ? status : nullptr));
+                            (attn_tc_route(c, S, L) || attn_tc_rc_route(c, S, L)) ? status : nullptr));
     return exact ? exact_din_finish(c, S, *w, *acts, d_hidden, ws, p, st) : TLB_OK;
 }
 
