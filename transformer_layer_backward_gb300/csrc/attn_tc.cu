@@ -72,6 +72,16 @@ __device__ __forceinline__ void st_shared_v4(uint8_t *p, uint32_t a, uint32_t b,
                  : "memory");
 }
 
+// 2^x by the special-function unit (relative error near 2^-22; results below the normal
+// range flush to zero).  The recomputed attention weights go through it as
+// exp(scale s - lse) = 2^(scale log2(e) s - lse log2(e)), then to tf32 (2^-11).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
 // Byte offset of 16-byte chunk `ch` (0..7) of row r in a K-major 128-byte-swizzled box.
 __device__ __forceinline__ uint32_t sw128_off(int r, int ch) { return uint32_t(r) * 128u + (uint32_t(ch ^ (r & 7)) << 4); }
 
@@ -1004,7 +1014,7 @@ __global__ void attn_tc_dv_sum_kernel(const float4 *__restrict__ part, float4 *_
 //     dQ += E_j K_j                                             tcgen05.mma, A from tensor memory
 //   then scale and RoPE backward as for the materialised path.
 constexpr int kRK = 32;         // keys per recomputed-dQ tile
-constexpr int kRBuf = 3;        // S / T buffer sets in tensor memory (an MMA set ahead of the wait)
+constexpr int kRBuf = 4;        // S / T buffer sets in tensor memory: the MMA thread keeps three ahead
 
 struct AttnTcRcParams {
     CUtensorMap kr128, vr128;   // Kr, Vr {hd, L, nkv}, box {32, 128, 1}  dV: A of S^T, T^T (once)
@@ -1043,6 +1053,7 @@ template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_rc_kernel(const __grid_constant__ AttnTcRcParams p) {
     using Ly = DvRcLayout<HD>;
     constexpr int NB = Ly::NB, NS = Ly::NS;
+    static_assert(HD + 2 * kRBuf * kVQ <= 512, "tensor memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     // kvfull: the K and V tiles; afull/afree, bfull/bfree: rings A and B; sfull: S^T and T^T of
@@ -1144,7 +1155,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_rc_kernel(const __
             };
             bool ok = mbar_wait(&kvfull, 0, p.status, 44u);
             tc_fence_after();
-            ok = ok && issue(0) && (nw < 2 || issue(1));
+            for (int w = 0; ok && w < min(nw, kRBuf - 1); ++w) ok = issue(w);
             for (int w = 0; ok && w < nw; ++w) {
                 const int s = w % NS, b = w % kRBuf;
                 if (!mbar_wait(&pfull[b], (w / kRBuf) & 1, p.status, 45u) ||
@@ -1160,9 +1171,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_rc_kernel(const __
                     mma_tf32_ts(tD, tD + Ly::TS + uint32_t(b * kVQ + 8 * k), bd + 2 * k, idV, (w > 0 || k > 0) ? 1u : 0u);
                 mma_commit(&bfree[s]);
                 mma_commit(&tfree[b]);
-                // S^T / T^T of item w + 2 take the buffer set of item w - 1, whose dV MMA was
+                // S^T / T^T of item w + 3 take the buffer set of item w - 1, whose dV MMA was
                 // issued one item ago: the wait overlaps dV_w in the tensor pipe
-                if (w + 2 < nw && !(ok = issue(w + 2))) break;
+                if (w + kRBuf - 1 < nw && !(ok = issue(w + kRBuf - 1))) break;
             }
             if (!ok) s_abort = 1;
             mma_commit(&dfull);
@@ -1175,6 +1186,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_rc_kernel(const __
         const int r = quarter * 32 + lane, key = k0 + r;
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
         const float *lse_h = p.lse + int64_t(h) * p.S;
+        const float sl2 = p.scale * kLog2e;
         float *dpart = p.Dpart + (int64_t(int(blockIdx.y) * 4 + quarter) * p.nh + h) * p.S;
         // the query of the item's half whose sum over this warp's keys this lane ends with
         const int b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1, b1 = (lane >> 1) & 1;
@@ -1182,9 +1194,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_rc_kernel(const __
         bool ok = true;
         for (int w = 0; w < nw; ++w) {
             const int b = w % kRBuf, qa = (t0 + w) * kVQ + hf * 16;
-            float l[16];
+            float l[16];                                     // lse log2(e) of the half's queries
 #pragma unroll
-            for (int c = 0; c < 16; ++c) l[c] = qa + c < p.S ? __ldg(lse_h + qa + c) : 0.f;
+            for (int c = 0; c < 16; ++c) l[c] = qa + c < p.S ? __ldg(lse_h + qa + c) * kLog2e : 0.f;
             if (!mbar_wait(&sfull[b], (w / kRBuf) & 1, p.status, 47u)) {
                 ok = false;
                 break;
@@ -1200,7 +1212,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dv_rc_kernel(const __
             for (int c = 0; c < 16; ++c) {
                 const int qi = qa + c;
                 const bool vis = qi < p.S && key < p.L && (!p.causal || key <= p.pos0 + qi);
-                const float pv = vis ? expf(p.scale * __uint_as_float(sv[c]) - l[c]) : 0.f;
+                const float pv = vis ? ex2_approx(fmaf(sl2, __uint_as_float(sv[c]), -l[c])) : 0.f;
                 e[c] = pv * __uint_as_float(tv[c]);
                 pt[c] = to_tf32(pv);
             }
@@ -1318,6 +1330,7 @@ template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_rc_kernel(const __grid_constant__ AttnTcRcParams p) {
     using Ly = DqRcLayout<HD>;
     constexpr int NB = Ly::NB, NS = Ly::NS;
+    static_assert(2 * HD + 2 * kRBuf * kRK <= 512, "tensor memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     // afull/afree, bfull/bfree: rings A and B; qready: q in shared memory and dCtx in tensor
@@ -1413,7 +1426,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_rc_kernel(const __
             };
             bool ok = mbar_wait(&qready, 0, p.status, 54u);
             tc_fence_after();
-            ok = ok && issue(0) && (nt < 2 || issue(1));
+            for (int j = 0; ok && j < min(nt, kRBuf - 1); ++j) ok = issue(j);
             for (int j = 0; ok && j < nt; ++j) {
                 const int s = j % NS, b = j % kRBuf;
                 if (!mbar_wait(&efull[b], (j / kRBuf) & 1, p.status, 55u) ||
@@ -1430,9 +1443,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_rc_kernel(const __
                                 (j > 0 || k > 0) ? 1u : 0u);
                 mma_commit(&bfree[s]);
                 mma_commit(&tfree[b]);
-                // S_j+2 / T_j+2 take the buffer set of tile j - 1, whose dQ MMA was issued one
+                // S_j+3 / T_j+3 take the buffer set of tile j - 1, whose dQ MMA was issued one
                 // tile ago: the wait overlaps dQ_j in the tensor pipe
-                if (j + 2 < nt && !(ok = issue(j + 2))) break;
+                if (j + kRBuf - 1 < nt && !(ok = issue(j + kRBuf - 1))) break;
             }
             if (!ok) s_abort = 1;
             mma_commit(&dfull);
@@ -1482,7 +1495,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_rc_kernel(const __
             __syncwarp();
             if (lane == 0) mbar_arrive(&qready);
         }
-        const float lse_i = row_ok ? __ldg(p.lse + int64_t(h) * p.S + i) : 0.f;
+        const float lse_i = row_ok ? __ldg(p.lse + int64_t(h) * p.S + i) * kLog2e : 0.f;   // in log2 units
+        const float sl2 = p.scale * kLog2e;
         const float D_i = row_ok ? __ldg(p.D + int64_t(h) * p.S + i) : 0.f;
         // Key tiles alternate between the two groups of four warps
         bool ok = true;
@@ -1500,7 +1514,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_rc_kernel(const __
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 const bool vis = row_ok && ka + c <= jlast;
-                const float pv = vis ? expf(p.scale * __uint_as_float(sv[c]) - lse_i) : 0.f;
+                const float pv = vis ? ex2_approx(fmaf(sl2, __uint_as_float(sv[c]), -lse_i)) : 0.f;
                 tv[c] = to_tf32(pv * (__uint_as_float(tv[c]) - D_i));
             }
             tmem_st32(tm + Ly::TT + uint32_t(b * kRK) + lane_off, tv);       // E_j over T_j
