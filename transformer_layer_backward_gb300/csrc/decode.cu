@@ -301,6 +301,135 @@ __global__ void __launch_bounds__(kThreads) dec_k2(DecodeArgs a) {
     if (r0 < a.H) warp_rows<WT, 2, kR, kU, true>(W, sc, xs, r0, a.H, nc, a.dN2, vals, wbytes<WT>(size_t(a.I)));
 }
 
+// Column-stationary form of k2 (int8, bf16 and fp32 weights): each thread owns one
+// 16-byte chunk of columns of both W_gate and W_up (E = 16 / 8 / 4 columns), forms its own
+// dG and dU for those columns in registers (no shared-memory vector), and streams the
+// block's rows kRowBatch at a time, double-buffered: a batch's two 16-byte loads per row
+// are issued before the previous batch is dotted, and the first batch goes out before the
+// wait on k1.  Each row's sum over the block's columns is reduced across the warp by
+// halving exchanges, then across the warps in shared memory, and added into dN2 (the
+// column blocks of a row meet there).
+constexpr int kRowBatch = 4;
+
+template <int WT, int ACT>
+__global__ void __launch_bounds__(256, 2) dec_k2c(DecodeArgs a) {
+    constexpr int E = EPC<WT>::v;
+    extern __shared__ float red2[];            // [warps][rows of the block]
+    __shared__ float2 red[32];
+    const int nch = a.I / E;                   // 16-byte chunks per row
+    const int ch = int(blockIdx.y) * blockDim.x + threadIdx.x;
+    const bool col_ok = ch < nch;
+    const int rows = a.H, r0 = int(int64_t(blockIdx.x) * rows / gridDim.x);
+    const int r1 = int(int64_t(blockIdx.x + 1) * rows / gridDim.x), nr = r1 - r0;
+    const size_t rb = wbytes<WT>(size_t(a.I));
+    const char *wg = static_cast<const char *>(a.w_gate), *wu = static_cast<const char *>(a.w_up);
+    {   // this block's rows of both matrices, over its column range, into L2 before the wait
+        const int c0 = int(blockIdx.y) * blockDim.x, c1 = min(nch, c0 + int(blockDim.x));
+        for (int k = threadIdx.x; k < 2 * nr; k += blockDim.x) {
+            const char *base = (k & 1 ? wu : wg) + size_t(r0 + (k >> 1)) * rb + size_t(c0) * 16;
+            prefetch_l2(base, size_t(c1 - c0) * 16);
+        }
+    }
+    const char *pg = wg + size_t(ch) * 16, *pu = wu + size_t(ch) * 16;
+    uint4 qg[2][kRowBatch], qu[2][kRowBatch];
+    auto load = [&](int buf, int rr) {
+#pragma unroll
+        for (int k = 0; k < kRowBatch; ++k) {
+            const bool ok = col_ok && rr + k < nr;
+            const size_t off = size_t(r0 + rr + k) * rb;
+            qg[buf][k] = ok ? ld_stream_u4(pg + off) : make_uint4(0, 0, 0, 0);
+            qu[buf][k] = ok ? ld_stream_u4(pu + off) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    load(0, 0);                                // the weights depend on nothing before this kernel
+    pdl_trigger();
+    pdl_wait();
+    float rinv = 1.f, c = 0.f;
+    const bool sub = a.flags & TLB_SUB_NORM;
+    if (sub) rms_coef2(sum_partials(a.part1, a.n1, red), a.I, a.eps, rinv, c);
+    const bool cache = (ACT == TLB_ACT_SILU_MUL) && (a.flags & TLB_USE_SILU_CACHE);
+    // dh (sub-norm backward) and the gated-activation backward of this thread's E columns
+    float xg[E], xu[E];
+    {
+        constexpr int F = E / 4;
+        const int j0 = col_ok ? ch * E : 0;
+        float4 df[F], hd[F], gm[F], ga[F], uu[F], sl[F];
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int f = 0; f < F; ++f) {
+            const int j = j0 + 4 * f;
+            df[f] = col_ok ? *reinterpret_cast<const float4 *>(a.dF + j) : z;
+            hd[f] = col_ok && sub ? *reinterpret_cast<const float4 *>(a.hidden + j) : z;
+            gm[f] = col_ok && sub ? *reinterpret_cast<const float4 *>(a.g_sub_ffn + j) : z;
+            ga[f] = col_ok ? *reinterpret_cast<const float4 *>(a.gate + j) : z;
+            uu[f] = col_ok ? *reinterpret_cast<const float4 *>(a.up + j) : z;
+            sl[f] = col_ok && cache ? *reinterpret_cast<const float4 *>(a.silu_gate + j) : z;
+        }
+#pragma unroll
+        for (int f = 0; f < F; ++f) {
+            const float dfv[4] = {df[f].x, df[f].y, df[f].z, df[f].w};
+            const float hdv[4] = {hd[f].x, hd[f].y, hd[f].z, hd[f].w};
+            const float gmv[4] = {gm[f].x, gm[f].y, gm[f].z, gm[f].w};
+            const float gav[4] = {ga[f].x, ga[f].y, ga[f].z, ga[f].w};
+            const float uuv[4] = {uu[f].x, uu[f].y, uu[f].z, uu[f].w};
+            const float slv[4] = {sl[f].x, sl[f].y, sl[f].z, sl[f].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float dh = sub ? rinv * (dfv[e] * gmv[e] - hdv[e] * c) : dfv[e];
+                const float g = gav[e], u = uuv[e];
+                float og, ou;
+                if constexpr (ACT == TLB_ACT_RELU2_MUL) {
+                    const float r = fmaxf(g, 0.f);
+                    og = dh * u * 2.f * r;
+                    ou = dh * r * r;
+                } else {
+                    const float sig = 1.f / (1.f + expf(-g));
+                    const float y = g * sig;
+                    og = dh * u * (sig * (1.f + g - y));
+                    ou = dh * (cache ? slv[e] : y);
+                }
+                xg[4 * f + e] = col_ok ? og : 0.f;
+                xu[4 * f + e] = col_ok ? ou : 0.f;
+            }
+        }
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1;
+    const int krow = 2 * b4 + b3;              // the batch row whose warp sum this lane ends with
+    static_assert(kRowBatch == 4, "two halving levels");
+    auto process = [&](int buf, int rr) {
+        float v[kRowBatch];
+#pragma unroll
+        for (int k = 0; k < kRowBatch; ++k)
+            v[k] = fmaf(a.s_gate, chunk_dot<WT>(qg[buf][k], xg), a.s_up * chunk_dot<WT>(qu[buf][k], xu));
+        // sum over the warp's lanes: each level keeps half of the rows and adds the partner's
+        float v2[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float send = b4 ? v[i] : v[2 + i];
+            v2[i] = (b4 ? v[2 + i] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+        float v1 = (b3 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b3 ? v2[0] : v2[1], 8);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 4);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+        if ((lane & 7) == 0 && rr + krow < nr) red2[warp * nr + rr + krow] = v1;
+    };
+    // two batches per pass, so that the buffer of each load and dot is a constant
+    for (int rr = 0; rr < nr; rr += 2 * kRowBatch) {
+        if (rr + kRowBatch < nr) load(1, rr + kRowBatch);          // next batch in flight
+        process(0, rr);
+        if (rr + 2 * kRowBatch < nr) load(0, rr + 2 * kRowBatch);
+        if (rr + kRowBatch < nr) process(1, rr + kRowBatch);
+    }
+    __syncthreads();
+    for (int r = threadIdx.x; r < nr; r += blockDim.x) {
+        float s = 0.f;
+        for (int w = 0; w < nwarps; ++w) s += red2[w * nr + r];
+        atomicAdd(a.dN2 + r0 + r, s);
+    }
+}
+
 // ------------------------------------------------------------------ k3: dR1, dSub = s_o W_O dR1
 
 template <int WT>
@@ -836,10 +965,22 @@ template <int WT>
 int launch_ffn(const DecodeArgs &a, cudaStream_t st, bool k1_pdl) {
     TLB_CUDA(launch(dec_k1<WT>, dim3(unsigned(a.n1)), size_t(a.H) * 4, st, k1_pdl, a));
     TLB_TRY(check_launch("decode k1"));
-    const size_t sm2 = size_t(2) * (a.I / a.ns2) * 4;
-    const dim3 g2(unsigned(a.n2), unsigned(a.ns2));
-    if (a.act == TLB_ACT_RELU2_MUL) TLB_CUDA(launch(dec_k2<WT, TLB_ACT_RELU2_MUL>, g2, sm2, st, true, a));
-    else TLB_CUDA(launch(dec_k2<WT, TLB_ACT_SILU_MUL>, g2, sm2, st, true, a));
+    if constexpr (WT != TLB_W_TERNARY_2B) {
+        // column-stationary k2: column blocks of at most 256 chunks (a whole number of warps),
+        // about two blocks per SM in all
+        const int nch = a.I / EPC<WT>::v, ncb = (nch + 255) / 256;
+        const int bs = ((nch + ncb - 1) / ncb + 31) / 32 * 32;
+        const int nrb = std::max(1, std::min(a.H, 2 * num_sms() / ncb));
+        const size_t smc = size_t(bs / 32) * ceil_div(a.H, nrb) * 4;
+        const dim3 gc{unsigned(nrb), unsigned(ncb)};
+        if (a.act == TLB_ACT_RELU2_MUL) TLB_CUDA(launch_b(dec_k2c<WT, TLB_ACT_RELU2_MUL>, gc, bs, smc, st, true, a));
+        else TLB_CUDA(launch_b(dec_k2c<WT, TLB_ACT_SILU_MUL>, gc, bs, smc, st, true, a));
+    } else {
+        const size_t sm2 = size_t(2) * (a.I / a.ns2) * 4;
+        const dim3 g2(unsigned(a.n2), unsigned(a.ns2));
+        if (a.act == TLB_ACT_RELU2_MUL) TLB_CUDA(launch(dec_k2<WT, TLB_ACT_RELU2_MUL>, g2, sm2, st, true, a));
+        else TLB_CUDA(launch(dec_k2<WT, TLB_ACT_SILU_MUL>, g2, sm2, st, true, a));
+    }
     TLB_TRY(check_launch("decode k2"));
     TLB_CUDA(launch(dec_k3<WT>, dim3(unsigned(a.n3), unsigned(a.ns3)), (size_t(4) * (a.H / a.ns3) + a.H) * 4, st,
                     true, a));
