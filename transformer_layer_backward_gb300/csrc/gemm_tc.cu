@@ -61,8 +61,8 @@ struct TcParams {
     float *partial;                      // [ctas][2][kBM * BN] fp32 partial tiles
     // epilogue: mode 0 writes out (+)= alpha acc; mode 1 treats alpha acc as dh and writes
     // the gated-activation backward dG, dU in bf16 ([FFN] ReLU^2 x Mul / [RS] SwiGLU)
-    int mode, act, act_cache;
-    const float *gate, *up, *silu;       // [M, N] fp32 (mode 1)
+    int mode, act;
+    const float *gate, *up;              // [M, N] fp32 (mode 1); silu(gate) is recomputed
     uint2 *dg, *du;                      // [M, N] bf16, four per uint2 (mode 1)
     // schedule over the flattened (tile, k block) iterations, tiles numbered m fastest:
     // CTA c first runs the whole tiles [c dp, (c + 1) dp), then the stream-K share
@@ -107,12 +107,6 @@ __device__ __forceinline__ void emit4(const TcParams &p, int row, int col, float
         act_bwd_elem<TLB_ACT_RELU2_MUL, false>(g.y, u.y, 0.f, d.y, og.y, ou.y);
         act_bwd_elem<TLB_ACT_RELU2_MUL, false>(g.z, u.z, 0.f, d.z, og.z, ou.z);
         act_bwd_elem<TLB_ACT_RELU2_MUL, false>(g.w, u.w, 0.f, d.w, og.w, ou.w);
-    } else if (p.act_cache) {
-        const float4 sv = ld_stream(reinterpret_cast<const float4 *>(p.silu + e));
-        act_bwd_elem<TLB_ACT_SILU_MUL, true>(g.x, u.x, sv.x, d.x, og.x, ou.x);
-        act_bwd_elem<TLB_ACT_SILU_MUL, true>(g.y, u.y, sv.y, d.y, og.y, ou.y);
-        act_bwd_elem<TLB_ACT_SILU_MUL, true>(g.z, u.z, sv.z, d.z, og.z, ou.z);
-        act_bwd_elem<TLB_ACT_SILU_MUL, true>(g.w, u.w, sv.w, d.w, og.w, ou.w);
     } else {
         act_bwd_elem<TLB_ACT_SILU_MUL, false>(g.x, u.x, 0.f, d.x, og.x, ou.x);
         act_bwd_elem<TLB_ACT_SILU_MUL, false>(g.y, u.y, 0.f, d.y, og.y, ou.y);
@@ -125,11 +119,13 @@ __device__ __forceinline__ void emit4(const TcParams &p, int row, int col, float
 
 // Activation epilogue of one 32 x 32 block (rows rbase.., columns col0..) held in shared
 // memory [32][33]: lanes are 8 column quads x 4 rows; every load of the block is issued
-// before the first store, so the memory latency is paid once per block.
-template <int ACT, bool CACHE>
+// before the first store, so the memory latency is paid once per block.  The SwiGLU form
+// recomputes silu(gate) from the gate it loads anyway: a cached copy would add a third to
+// the loads this epilogue is bound by.
+template <int ACT>
 __device__ __forceinline__ void act_block_t(const TcParams &p, int rbase, int col0, const float *blk, int lane) {
     const int c4 = (lane & 7) * 4, rl = lane >> 3;
-    float4 g[8], u[8], sv[8];
+    float4 g[8], u[8];
     bool ok[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -138,8 +134,6 @@ __device__ __forceinline__ void act_block_t(const TcParams &p, int rbase, int co
         const int64_t e = ok[k] ? int64_t(rbase + r) * p.N + col0 + c4 : 0;
         g[k] = ld_stream(reinterpret_cast<const float4 *>(p.gate + e));
         u[k] = ld_stream(reinterpret_cast<const float4 *>(p.up + e));
-        if constexpr (CACHE) sv[k] = ld_stream(reinterpret_cast<const float4 *>(p.silu + e));
-        else sv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -147,10 +141,10 @@ __device__ __forceinline__ void act_block_t(const TcParams &p, int rbase, int co
         if (!ok[k]) continue;
         const float *a = blk + r * 33 + c4;
         float4 og, ou;
-        act_bwd_elem<ACT, CACHE>(g[k].x, u[k].x, sv[k].x, p.alpha * a[0], og.x, ou.x);
-        act_bwd_elem<ACT, CACHE>(g[k].y, u[k].y, sv[k].y, p.alpha * a[1], og.y, ou.y);
-        act_bwd_elem<ACT, CACHE>(g[k].z, u[k].z, sv[k].z, p.alpha * a[2], og.z, ou.z);
-        act_bwd_elem<ACT, CACHE>(g[k].w, u[k].w, sv[k].w, p.alpha * a[3], og.w, ou.w);
+        act_bwd_elem<ACT, false>(g[k].x, u[k].x, 0.f, p.alpha * a[0], og.x, ou.x);
+        act_bwd_elem<ACT, false>(g[k].y, u[k].y, 0.f, p.alpha * a[1], og.y, ou.y);
+        act_bwd_elem<ACT, false>(g[k].z, u[k].z, 0.f, p.alpha * a[2], og.z, ou.z);
+        act_bwd_elem<ACT, false>(g[k].w, u[k].w, 0.f, p.alpha * a[3], og.w, ou.w);
         const int64_t e = int64_t(rbase + r) * p.N + col0 + c4;
         p.dg[e / 4] = pack_bf16x4(og.x, og.y, og.z, og.w);
         p.du[e / 4] = pack_bf16x4(ou.x, ou.y, ou.z, ou.w);
@@ -158,9 +152,8 @@ __device__ __forceinline__ void act_block_t(const TcParams &p, int rbase, int co
 }
 
 __device__ __forceinline__ void act_block(const TcParams &p, int rbase, int col0, const float *blk, int lane) {
-    if (p.act == TLB_ACT_RELU2_MUL) act_block_t<TLB_ACT_RELU2_MUL, false>(p, rbase, col0, blk, lane);
-    else if (p.act_cache) act_block_t<TLB_ACT_SILU_MUL, true>(p, rbase, col0, blk, lane);
-    else act_block_t<TLB_ACT_SILU_MUL, false>(p, rbase, col0, blk, lane);
+    if (p.act == TLB_ACT_RELU2_MUL) act_block_t<TLB_ACT_RELU2_MUL>(p, rbase, col0, blk, lane);
+    else act_block_t<TLB_ACT_SILU_MUL>(p, rbase, col0, blk, lane);
 }
 
 // Plain epilogue of a warp's 32 x 32 block staged in shared memory (blk[r * 33 + c], before
@@ -339,6 +332,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
             }
             tc_fence_after();
             const int half = (warp - 2) >> 2;     // this warp's half of the tile's columns
+            float *blk = ep + (warp - 2) * 32 * 33;
             for (int j = half * (BN / 64); j < (half + 1) * (BN / 64); ++j) {
                 uint32_t v[32];
                 tmem_ld32(tmem + uint32_t(b * BN) + (uint32_t(q * 32) << 16) + uint32_t(j * 32), v);
@@ -346,7 +340,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                 const int col0 = n0 + j * 32;
                 // the warp's 32 x 32 block (one row per lane) goes through shared memory so
                 // that lanes run along columns and every global access is coalesced
-                float *blk = ep + (warp - 2) * 32 * 33;
 #pragma unroll
                 for (int t = 0; t < 32; ++t) blk[lane * 33 + t] = __uint_as_float(v[t]);
                 __syncwarp();
@@ -564,9 +557,8 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
     const TcPlan pl = tc_plan(M, N, K);
     TLB_REQUIRE(partial != nullptr, TLB_EINVAL, "tcgen05 GEMM: needs a partial-tile buffer");
     if (act != nullptr) {
-        const bool cache = act->act == TLB_ACT_SILU_MUL && act->silu_gate != nullptr;
         TLB_REQUIRE(!accumulate && N % 4 == 0 && aligned16(act->gate) && aligned16(act->up) &&
-                        aligned16(act->dgate) && aligned16(act->dup) && (!cache || aligned16(act->silu_gate)),
+                        aligned16(act->dgate) && aligned16(act->dup),
                     TLB_EUNSUPPORTED, "tcgen05 GEMM: activation epilogue operands");
     } else {
         TLB_REQUIRE(aligned16(out) && (out_bf16 == nullptr || aligned16(out_bf16)), TLB_EUNSUPPORTED,
@@ -593,10 +585,8 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
     if (act != nullptr) {
         p.mode = 1;
         p.act = act->act;
-        p.act_cache = (act->act == TLB_ACT_SILU_MUL && act->silu_gate != nullptr) ? 1 : 0;
         p.gate = act->gate;
         p.up = act->up;
-        p.silu = act->silu_gate;
         p.dg = static_cast<uint2 *>(act->dgate);
         p.du = static_cast<uint2 *>(act->dup);
     }

@@ -53,7 +53,7 @@ int tc_convert_bf16(const float *x, void *y, int64_t n, cudaStream_t st);
 // writes dG, dU in bf16 (the A operands of the [W_gate | W_up]^T product) instead of out.
 struct TcActEpilogue {
     int act;                              // TLB_ACT_*
-    const float *gate, *up, *silu_gate;   // [M, N] fp32; silu_gate may be NULL (recomputed)
+    const float *gate, *up;               // [M, N] fp32; silu(gate) is recomputed
     void *dgate, *dup;                    // [M, N] bf16
 };
 // out_bf16 (optional, no activation epilogue): [M, N] bf16 copy of every value stored to out.

@@ -168,7 +168,7 @@ int ffn_impl(const tlb_layer_cfg &c, int64_t S, const float *d_out, const tlb_la
             // the activation backward runs in the product's epilogue: dF never reaches memory.
             // The epilogue is bound by its loads, so it recomputes silu(gate) from the gate
             // value it reads rather than loading the cache (a third of its reads)
-            const TcActEpilogue ae{c.act, a.gate, a.up, nullptr, gbf, ubf};
+            const TcActEpilogue ae{c.act, a.gate, a.up, gbf, ubf};
             TLB_TRY(tc_gemm(&down, 1, S, I, w.w_down.scale, nullptr, false, part, status, st, &ae));
         }
         const TcOperand gu[2] = {{gbf, w.w_gate.w, I}, {ubf, w.w_up.w, I}};
