@@ -119,7 +119,8 @@ def test_adamw(lib, n, step):
 @pytest.mark.parametrize("wtype", ["f32", "bf16", "ternary", "ternary2"])
 @pytest.mark.parametrize("S,in_dim,out_dim", [(1, 640, 2560), (1, 37, 50), (3, 100, 64), (130, 96, 272),
                                               (1, 6912, 2560), (256, 768, 1024), (130, 272, 4096),
-                                              (77, 640, 2560), (512, 2560, 9728), (512, 9728, 2560)])
+                                              (77, 640, 2560), (512, 2560, 9728), (512, 9728, 2560),
+                                              (300, 600, 1024), (2048, 2560, 9728)])
 @pytest.mark.parametrize("accumulate", [False, True])
 def test_linear_backward(lib, wtype, S, in_dim, out_dim, accumulate):
     import torch

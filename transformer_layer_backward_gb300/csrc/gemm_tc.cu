@@ -19,6 +19,16 @@
 //               lanes run along columns; scale, optional accumulate into C, coalesced fp32
 //               (and optional bf16) stores, then release the accumulator, so one segment's
 //               epilogue overlaps the next one's MMAs
+// Paired form (BN = 256, clusters of two CTAs on one TPC, cta_group::2): the pair owns a
+// 256 x 256 super-tile; each CTA loads its own 128 rows of A and its half (128 rows) of B
+// into its own ring, the even CTA issues tcgen05.mma.cta_group::2 (M = 256, N = 256), which
+// takes A and B halves from both CTAs' shared memory and leaves rows 0..127 in the even
+// CTA's tensor memory and rows 128..255 in the odd one's.  Per CTA and k block that is
+// 32 KB staged instead of 48 KB for the same 128 x 256 x 64 of work, which relieves the
+// shared-memory traffic (TMA writes + MMA reads) that bounds the single-CTA form.  Both
+// CTAs' copies count on the even CTA's full barrier; its commits free the stage and hand
+// over the accumulators in both CTAs (multicast); both CTAs' epilogue warps release an
+// accumulator on the even CTA's barrier.
 // K may come from two segments (A0.B0^T + A1.B1^T, e.g. [dG | dU] . [W_gate | W_up]^T).
 // Work is balanced stream-K style: the (tile, k block) iterations are split evenly over
 // the CTAs; a tile done by one CTA is written by it, a tile shared by several is summed
@@ -43,7 +53,11 @@ namespace tlb {
 namespace {
 
 constexpr int kBM = 128, kBK = 64;       // tile rows, k block (64 bf16 = 128 bytes)
-constexpr int kStages = 4;
+constexpr int kStages = 4;               // ring depth, single-CTA form (48 KB stages)
+constexpr int kStagesPair = 6;           // paired form (32 KB stages)
+template <bool PAIR> constexpr int stages_of() { return PAIR ? kStagesPair : kStages; }
+// k-block time of the paired form relative to the single-CTA 128 x 256 form (planner)
+constexpr double kPairRate = 0.75;
 constexpr int kThreadsTC = 320;          // 10 warps: producer, MMA, 8 epilogue warps
 constexpr int kEpiWarpsTC = 8;           // two per TMEM lane quarter, each half of the columns
 constexpr int kMaxSeg = 3;               // K segments of one product
@@ -66,7 +80,8 @@ struct TcParams {
     uint2 *dg, *du;                      // [M, N] bf16, four per uint2 (mode 1)
     // schedule over the flattened (tile, k block) iterations, tiles numbered m fastest:
     // CTA c first runs the whole tiles [c dp, (c + 1) dp), then the stream-K share
-    // [sk_base + sk_work c / ctas, sk_base + sk_work (c + 1) / ctas) of the rest
+    // [sk_base + sk_work c / ctas, sk_base + sk_work (c + 1) / ctas) of the rest.  In the
+    // paired form a tile is a 256-row super-tile and c a CTA pair (ctas pairs).
     int dp;                              // whole tiles per CTA
     int ctas;
     int64_t sk_base, sk_work;
@@ -75,7 +90,8 @@ struct TcParams {
 
 constexpr int kMaxFix = 256;
 // Tiles shared by several CTAs (stream-K part): tile t is the sum of the partial tiles of
-// CTAs c0..c1, CTA c0's in slot s0 (1 when c0 began in an earlier tile), the others in slot 0.
+// CTAs c0..c1, CTA c0's in slot s0 (1 when c0 began in an earlier tile), the others in slot 0
+// (paired form: super-tile t, pairs c0..c1, half h of it from CTA 2 c + h).
 struct TcFixup {
     int n;
     int4 e[kMaxFix];                     // {tile, c0, c1, s0}
@@ -199,28 +215,35 @@ __device__ __forceinline__ void partial_block(float *o, int ld, const float *blk
     }
 }
 
-template <int BN>
+template <int M, int BN>
 __device__ __forceinline__ uint32_t idesc_bf16() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-    constexpr int A_BYTES = kBM * kBK * 2, B_BYTES = BN * kBK * 2, STAGE = A_BYTES + B_BYTES;
+    static_assert(!PAIR || BN == 256, "the paired form runs 256 x 256 super-tiles");
+    constexpr int TM = PAIR ? 2 * kBM : kBM;                 // rows of a scheduled tile
+    constexpr int BH = PAIR ? BN / 2 : BN;                   // rows of B this CTA stages
+    constexpr int A_BYTES = kBM * kBK * 2, B_BYTES = BH * kBK * 2, STAGE = A_BYTES + B_BYTES;
+    constexpr int kStages = stages_of<PAIR>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t full[kStages], empty[kStages], accfull[2], accempty[2], done;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort, s_issued, s_consumed;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = PAIR ? int(cluster_rank()) : 0;        // this CTA's half of a super-tile
+    const int cl = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
+    const bool leader = rank == 0;                           // issues the MMAs
 
-    // this CTA's iterations: the whole tiles [c dp, (c + 1) dp), then its stream-K range;
-    // cut at tile boundaries into segments
-    const int tiles_m = (p.M + kBM - 1) / kBM;
+    // this CTA's (pair's) iterations: the whole tiles [c dp, (c + 1) dp), then its stream-K
+    // range; cut at tile boundaries into segments
+    const int tiles_m = (p.M + TM - 1) / TM;
     const int KB = p.kb[0] + (p.nseg > 1 ? p.kb[1] : 0) + (p.nseg > 2 ? p.kb[2] : 0);
-    const int64_t a0 = int64_t(blockIdx.x) * p.dp * KB, a1 = a0 + int64_t(p.dp) * KB;
-    const int64_t b0 = p.sk_base + sk_start(p.sk_work, p.ctas, blockIdx.x);
-    const int64_t b1 = p.sk_base + sk_start(p.sk_work, p.ctas, blockIdx.x + 1);
+    const int64_t a0 = int64_t(cl) * p.dp * KB, a1 = a0 + int64_t(p.dp) * KB;
+    const int64_t b0 = p.sk_base + sk_start(p.sk_work, p.ctas, cl);
+    const int64_t b1 = p.sk_base + sk_start(p.sk_work, p.ctas, cl + 1);
     const int64_t g0 = a0, g1 = a1 + (b1 - b0);               // local iteration count g1 - g0
     auto to_global = [&](int64_t g) { return g < a1 ? g : b0 + (g - a1); };
     // segment starting at local iteration g: tile, rows, columns, k blocks [kb0, kb1)
@@ -229,7 +252,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
         const int64_t t = gg / KB;
         kb0 = int(gg - t * KB);
         kb1 = int(std::min<int64_t>(KB, end - t * KB));
-        m0 = int(t % tiles_m) * kBM;
+        m0 = int(t % tiles_m) * TM + rank * kBM;             // this CTA's rows
         n0 = int(t / tiles_m) * BN;
     };
 
@@ -242,17 +265,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accfull[b], 1);
-            mbar_init(&accempty[b], kEpiWarpsTC);
+            mbar_init(&accempty[b], (PAIR ? 2 : 1) * kEpiWarpsTC);   // paired: both CTAs' warps
         }
         mbar_init(&done, 1);
     }
     if (warp == 1) {
-        tmem_alloc(&tmem_base, 2 * BN);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(&tmem_base, 2 * BN);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&tmem_base, 2 * BN);
+            tmem_relinquish();
+        }
     }
     fence_mbar_init();
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();              // the peer's barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = tmem_base;
 
@@ -274,9 +303,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                     const int seg = kb < p.kb[0] ? 0 : (kb < p.kb[0] + p.kb[1] ? 1 : 2);
                     const int kx = (kb - (seg > 0 ? p.kb[0] : 0) - (seg > 1 ? p.kb[1] : 0)) * kBK;
                     uint8_t *sa = smem + s * STAGE;
-                    mbar_arrive_expect_tx(&full[s], STAGE);
-                    tma_load_2d(sa, &p.a[seg], kx, m0, &full[s]);
-                    tma_load_2d(sa + A_BYTES, &p.b[seg], kx, n0, &full[s]);
+                    if constexpr (PAIR) {
+                        // both CTAs' copies count on the even CTA's full barrier
+                        if (leader) mbar_arrive_expect_tx(&full[s], 2 * STAGE);
+                        const uint32_t fb = cluster_addr(&full[s], 0);
+                        tma_load_2d_pair(sa, &p.a[seg], kx, m0, fb);
+                        tma_load_2d_pair(sa + A_BYTES, &p.b[seg], kx, n0 + rank * BH, fb);
+                    } else {
+                        mbar_arrive_expect_tx(&full[s], STAGE);
+                        tma_load_2d(sa, &p.a[seg], kx, m0, &full[s]);
+                        tma_load_2d(sa + A_BYTES, &p.b[seg], kx, n0, &full[s]);
+                    }
                     s_issued = g + 1;
                 }
             }
@@ -284,8 +321,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer, accumulators alternate
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16<BN>();
+        if (lane == 0 && leader) {
+            const uint32_t idesc = idesc_bf16<TM, BN>();
             int g = 0, i = 0;
             bool ok = true;
             for (int64_t gs = g0; ok && gs < g1; ++i) {
@@ -303,15 +340,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                     const uint8_t *sa = smem + s * STAGE;
                     const uint64_t ad = sw128_desc(sa), bd = sw128_desc(sa + A_BYTES);
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)   // 16 bf16 = 32 bytes = 2 descriptor units
-                        mma_bf16(acc, ad + 2 * k, bd + 2 * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-                    mma_commit(&empty[s]);
+                    for (int k = 0; k < kBK / 16; ++k) {  // 16 bf16 = 32 bytes = 2 descriptor units
+                        if constexpr (PAIR)
+                            mma_bf16_pair(acc, ad + 2 * k, bd + 2 * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        else
+                            mma_bf16(acc, ad + 2 * k, bd + 2 * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                    }
+                    if constexpr (PAIR) mma_commit_pair(&empty[s], 3);   // frees the stage in both CTAs
+                    else mma_commit(&empty[s]);
                     s_consumed = g + 1;
                 }
-                if (ok) mma_commit(&accfull[b]);      // this unit's MMAs done -> epilogue
+                if (ok) {                             // this unit's MMAs done -> epilogue
+                    if constexpr (PAIR) mma_commit_pair(&accfull[b], 3);
+                    else mma_commit(&accfull[b]);
+                }
             }
             if (!ok) s_abort = 1;
-            mma_commit(&done);                        // fires once every MMA issued above is complete
+            // fires once every MMA issued above is complete
+            if constexpr (PAIR) mma_commit_pair(&done, 1);
+            else mma_commit(&done);
             mbar_wait(&done, 0, nullptr, 0u);
         }
     } else {
@@ -345,7 +392,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                 __syncwarp();
                 if (!whole)         // partial tile of this CTA, tile-local [kBM][BN]
                     partial_block(p.partial + ((int64_t(blockIdx.x) * 2 + slot) * kBM + q * 32) * BN + j * 32, BN,
-                                  blk, lane);
+                                  blk, lane);   // paired: blockIdx.x = 2 pair + half
                 else if (p.mode == 1)
                     act_block(p, m0 + q * 32, col0, blk, lane);
                 else
@@ -354,7 +401,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&accempty[b]);
+            if (lane == 0) {
+                if constexpr (PAIR) mbar_arrive_cluster(cluster_addr(&accempty[b], 0));
+                else mbar_arrive(&accempty[b]);
+            }
         }
     }
     // wind down: the MMA thread waited for its final commit, so no MMA is in flight;
@@ -362,30 +412,37 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
     // consumed, so nothing lands in shared memory after exit
     tc_fence_before();
     __syncthreads();
-    if (s_abort && threadIdx.x == 0) {
+    if (s_abort && threadIdx.x == 0 && leader) {
         for (int g = s_consumed; g < s_issued; ++g) mbar_wait(&full[g % kStages], (g / kStages) & 1, nullptr, 0u);
     }
     __syncthreads();
+    // paired: neither CTA leaves or frees its tensor memory while the other's copies,
+    // commits or arrivals may still reach it
+    if constexpr (PAIR) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 2 * BN);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem, 2 * BN);
+        else tmem_dealloc(tmem, 2 * BN);
     }
 }
 
 // Stream-K fixup: a tile shared by CTAs c0..c1 is the sum, in CTA order, of their partial
 // tiles; out (+)= alpha * sum.  Block (entry, y) does rows [y kBM / gridDim.y, ...) of it.
-template <int BN>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(256) tc_fixup_kernel(const __grid_constant__ TcParams p,
                                                        const __grid_constant__ TcFixup f) {
+    constexpr int TM = PAIR ? 2 * kBM : kBM;
     const int4 en = f.e[blockIdx.x];
-    const int tiles_m = (p.M + kBM - 1) / kBM;
-    const int m0 = (en.x % tiles_m) * kBM, n0 = (en.x / tiles_m) * BN;
-    const int rows = kBM / gridDim.y, r0 = blockIdx.y * rows;
+    const int tiles_m = (p.M + TM - 1) / TM;
+    const int m0 = (en.x % tiles_m) * TM, n0 = (en.x / tiles_m) * BN;
+    const int rows = TM / gridDim.y, r0 = blockIdx.y * rows;
     for (int e = threadIdx.x; e < rows * (BN / 4); e += blockDim.x) {
         const int r = r0 + e / (BN / 4), c4 = (e % (BN / 4)) * 4;
+        const int h = r / kBM, lr = r % kBM;               // half of a super-tile, row in it
         auto part = [&](int c) {
             const int slot = c == en.y ? en.w : 0;
-            return *reinterpret_cast<const float4 *>(p.partial + ((int64_t(c) * 2 + slot) * kBM + r) * BN + c4);
+            const int64_t cta = PAIR ? 2 * int64_t(c) + h : c;
+            return *reinterpret_cast<const float4 *>(p.partial + ((cta * 2 + slot) * kBM + lr) * BN + c4);
         };
         // CTA order, four partial tiles' loads in flight at a time
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -443,12 +500,30 @@ int make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int b
     return TLB_OK;
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 int launch_tc(const TcParams &p, cudaStream_t st) {
-    constexpr int smem = kStages * (kBM * kBK * 2 + BN * kBK * 2) + kEpiWarpsTC * 32 * 33 * 4 + 1024;
-    auto k = tc_gemm_kernel<BN>;
+    constexpr int smem = stages_of<PAIR>() * (kBM * kBK * 2 + (PAIR ? BN / 2 : BN) * kBK * 2) +
+                         kEpiWarpsTC * 32 * 33 * 4 + 1024;
+    static_assert(smem <= 227 * 1024 - 256, "shared memory of one CTA");
+    auto k = tc_gemm_kernel<BN, PAIR>;
     TLB_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    k<<<p.ctas, kThreadsTC, smem, st>>>(p);
+    if constexpr (PAIR) {                             // clusters of two CTAs, one pair per TPC
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(2 * p.ctas));
+        cfg.blockDim = dim3(kThreadsTC);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        TLB_CUDA(cudaLaunchKernelEx(&cfg, k, p));
+    } else {
+        k<<<p.ctas, kThreadsTC, smem, st>>>(p);
+    }
     TLB_TRY(check_launch("tcgen05 gemm"));
     // tiles of the stream-K part that more than one CTA touched
     const int64_t KB = p.kb[0] + (p.nseg > 1 ? p.kb[1] : 0) + (p.nseg > 2 ? p.kb[2] : 0);
@@ -466,15 +541,16 @@ int launch_tc(const TcParams &p, cudaStream_t st) {
         }
     }
     if (f.n == 0) return TLB_OK;
-    tc_fixup_kernel<BN><<<dim3(unsigned(f.n), 32), 256, 0, st>>>(p, f);
+    tc_fixup_kernel<BN, PAIR><<<dim3(unsigned(f.n), PAIR ? 64 : 32), 256, 0, st>>>(p, f);
     return check_launch("tcgen05 gemm fixup");
 }
 
 }  // namespace
 
 TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
-    // 128 x 256 or 128 x 128 tiles on persistent CTAs.  Candidates: `dp` whole tiles per
-    // CTA, the remaining tiles shared stream-K style by the `ctas` CTAs.
+    // 256 x 256 super-tiles on persistent CTA pairs, or 128 x 256 / 128 x 128 tiles on
+    // persistent CTAs.  Candidates: `dp` whole tiles per CTA (pair), the remaining tiles
+    // shared stream-K style by the `ctas` CTAs (pairs).
     // Cost: the busiest CTA's k blocks (one 128 x BN x 64 MMA block each, at the rate
     // these kernels reach: 128-wide tiles about 1.4 times slower per flop), plus 8 us
     // per stream-K segment of the busiest CTA (each ends in a TMEM drain into a partial
@@ -490,16 +566,23 @@ TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    TcPlan best{N > 128 ? 256 : 128, 1, 0, 0};
+    TcPlan best{N > 128 ? 256 : 128, 1, 0, 0, 0};
     double best_cost = 1e300;
-    for (int bn : {256, 128}) {
+    for (int form = 0; form < 3; ++form) {
+        // 0: paired 256 x 256 super-tiles, 1: single 128 x 256, 2: single 128 x 128
+        const bool pair = form == 0;
+        const int bn = form == 2 ? 128 : 256;
         if (bn == 256 && N <= 128) continue;
-        const int64_t tiles = ceil_div(N, bn) * ceil_div(M, kBM), KB = ceil_div(K, kBK);
-        // s per k block; 128-wide tiles fetch A twice as often per flop
-        const double t_kb = 2.0 * kBM * bn * kBK / (1.3e15 / nsm) * (bn == 128 ? 1.4 : 1.0);
-        const double tile_io = 2.0 * kBM * bn * 4 / 6.0e12;                // s per partial tile written + read
+        if (pair && (M <= kBM || nsm < 2)) continue;
+        const int64_t tm = pair ? 2 * kBM : kBM;
+        const int units = pair ? nsm / 2 : nsm;
+        const int64_t tiles = ceil_div(N, bn) * ceil_div(M, tm), KB = ceil_div(K, kBK);
+        // s per k block of a CTA's 128 x bn share; 128-wide tiles stage A twice as often per
+        // flop, the paired form stages half of B
+        const double t_kb = 2.0 * kBM * bn * kBK / (1.3e15 / nsm) * (bn == 128 ? 1.4 : pair ? kPairRate : 1.0);
+        const double tile_io = (pair ? 2.0 : 1.0) * 2.0 * kBM * bn * 4 / 6.0e12;   // s per partial tile written + read
         auto consider = [&](int64_t ctas, int64_t dp) {
-            if (ctas < 1 || ctas > nsm || dp < 0 || dp * ctas > tiles) return;
+            if (ctas < 1 || ctas > units || dp < 0 || dp * ctas > tiles) return;
             const int64_t skw = (tiles - dp * ctas) * KB;
             int64_t shared = 0;
             for (int64_t c = 1; c < ctas && skw > 0; ++c)
@@ -513,12 +596,12 @@ TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
                                 (shared > 0 ? 2.0 * shared * tile_io + 3e-6 : 0.0);
             if (cost < best_cost) {
                 best_cost = cost;
-                best = TcPlan{bn, int(ctas), int(dp), int(shared)};
+                best = TcPlan{bn, int(ctas), int(dp), int(shared), pair ? 1 : 0};
             }
         };
-        std::vector<int64_t> cand = {nsm};
-        for (int64_t s = 1; s <= 8; ++s) cand.push_back(std::min<int64_t>(tiles * s, nsm));
-        for (int64_t d = 1; d <= 8; ++d) cand.push_back(std::max<int64_t>(1, std::min<int64_t>(nsm, ceil_div(tiles, d))));
+        std::vector<int64_t> cand = {units};
+        for (int64_t s = 1; s <= 8; ++s) cand.push_back(std::min<int64_t>(tiles * s, units));
+        for (int64_t d = 1; d <= 8; ++d) cand.push_back(std::max<int64_t>(1, std::min<int64_t>(units, ceil_div(tiles, d))));
         for (int64_t ctas : cand) {
             consider(ctas, tiles / ctas);
             consider(ctas, tiles / ctas - 1);
@@ -533,7 +616,7 @@ TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
 size_t tc_partial_bytes(int64_t M, int64_t N, int64_t K) {
     // sized for two partial tiles per CTA whatever the split of K into segments
     const TcPlan pl = tc_plan(M, N, K);
-    return size_t(pl.ctas) * 2 * kBM * pl.bn * 4;
+    return size_t(pl.ctas) * (pl.pair ? 2 : 1) * 2 * kBM * pl.bn * 4;
 }
 
 int tc_convert_bf16(const float *x, void *y, int64_t n, cudaStream_t st) {
@@ -571,7 +654,7 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
         TLB_REQUIRE(aligned16(seg[i].a) && aligned16(seg[i].b) && seg[i].K % 8 == 0, TLB_EUNSUPPORTED,
                     "tcgen05 GEMM: operand alignment");
         TLB_TRY(make_map(&p.a[i], seg[i].a, M, seg[i].K, kBM));
-        TLB_TRY(make_map(&p.b[i], seg[i].b, N, seg[i].K, pl.bn));
+        TLB_TRY(make_map(&p.b[i], seg[i].b, N, seg[i].K, pl.pair ? pl.bn / 2 : pl.bn));
         p.kb[i] = int(ceil_div(seg[i].K, kBK));
     }
     p.nseg = nseg;
@@ -590,13 +673,14 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
         p.dg = static_cast<uint2 *>(act->dgate);
         p.du = static_cast<uint2 *>(act->dup);
     }
-    const int64_t KB = p.kb[0] + (nseg > 1 ? p.kb[1] : 0) + (nseg > 2 ? p.kb[2] : 0), tiles = ceil_div(N, pl.bn) * ceil_div(M, kBM);
+    const int64_t KB = p.kb[0] + (nseg > 1 ? p.kb[1] : 0) + (nseg > 2 ? p.kb[2] : 0), tiles = ceil_div(N, pl.bn) * ceil_div(M, pl.pair ? 2 * kBM : kBM);
     p.ctas = pl.ctas;
     p.dp = pl.dp;
     p.sk_base = int64_t(pl.dp) * pl.ctas * KB;
     p.sk_work = (tiles - int64_t(pl.dp) * pl.ctas) * KB;
     p.status = status;
-    return pl.bn == 256 ? launch_tc<256>(p, st) : launch_tc<128>(p, st);
+    if (pl.pair) return launch_tc<256, true>(p, st);
+    return pl.bn == 256 ? launch_tc<256, false>(p, st) : launch_tc<128, false>(p, st);
 }
 
 }  // namespace tlb

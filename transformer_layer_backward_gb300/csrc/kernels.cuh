@@ -41,9 +41,10 @@ struct TcOperand {
     int64_t K;
 };
 struct TcPlan {
-    int bn, ctas;    // tile width, persistent CTAs
+    int bn, ctas;    // tile width, persistent CTAs (CTA pairs when paired)
     int dp;          // whole tiles per CTA before the stream-K part
     int shared;      // CTA boundaries that fall inside a stream-K tile (0: no fixup)
+    int pair;        // 1: clusters of two CTAs on 256 x 256 super-tiles (cta_group::2 MMA)
 };
 TcPlan tc_plan(int64_t M, int64_t N, int64_t K);
 bool tc_supported(int64_t M, int64_t N, int64_t K);
