@@ -243,6 +243,23 @@ __device__ __forceinline__ void act_bwd_elem(float g, float u, float s, float dh
     }
 }
 
+// The same for results rounded to bf16 (the tensor-core W_down^T epilogue): the exponential
+// and the reciprocal are the fast hardware approximations, whose relative error (~1e-6) is
+// far below the 2^-9 of the bf16 rounding that follows.
+template <int ACT>
+__device__ __forceinline__ void act_bwd_elem_bf16(float g, float u, float dh, float &dg, float &du) {
+    if constexpr (ACT == TLB_ACT_RELU2_MUL) {
+        const float r = fmaxf(g, 0.f);
+        dg = dh * u * 2.f * r;
+        du = dh * r * r;
+    } else {
+        const float sig = __fdividef(1.f, 1.f + __expf(-g));
+        const float y = g * sig;
+        dg = dh * u * (sig * (1.f + g - y));
+        du = dh * y;
+    }
+}
+
 // bf16 outputs (the A operands of the [W_gate | W_up]^T tensor-core GEMM)
 __device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
     const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);

@@ -54,7 +54,7 @@ namespace {
 
 constexpr int kBM = 128, kBK = 64;       // tile rows, k block (64 bf16 = 128 bytes)
 constexpr int kStages = 4;               // ring depth, single-CTA form (48 KB stages)
-constexpr int kStagesPair = 6;           // paired form (32 KB stages)
+constexpr int kStagesPair = 5;           // paired form (32 KB stages; a sixth slows the W_down^T epilogue)
 template <bool PAIR> constexpr int stages_of() { return PAIR ? kStagesPair : kStages; }
 // k-block time of the paired form relative to the single-CTA 128 x 256 form (planner)
 constexpr double kPairRate = 0.75;
@@ -119,15 +119,15 @@ __device__ __forceinline__ void emit4(const TcParams &p, int row, int col, float
     const float4 u = ld_stream(reinterpret_cast<const float4 *>(p.up + e));
     float4 og, ou;
     if (p.act == TLB_ACT_RELU2_MUL) {
-        act_bwd_elem<TLB_ACT_RELU2_MUL, false>(g.x, u.x, 0.f, d.x, og.x, ou.x);
-        act_bwd_elem<TLB_ACT_RELU2_MUL, false>(g.y, u.y, 0.f, d.y, og.y, ou.y);
-        act_bwd_elem<TLB_ACT_RELU2_MUL, false>(g.z, u.z, 0.f, d.z, og.z, ou.z);
-        act_bwd_elem<TLB_ACT_RELU2_MUL, false>(g.w, u.w, 0.f, d.w, og.w, ou.w);
+        act_bwd_elem_bf16<TLB_ACT_RELU2_MUL>(g.x, u.x, d.x, og.x, ou.x);
+        act_bwd_elem_bf16<TLB_ACT_RELU2_MUL>(g.y, u.y, d.y, og.y, ou.y);
+        act_bwd_elem_bf16<TLB_ACT_RELU2_MUL>(g.z, u.z, d.z, og.z, ou.z);
+        act_bwd_elem_bf16<TLB_ACT_RELU2_MUL>(g.w, u.w, d.w, og.w, ou.w);
     } else {
-        act_bwd_elem<TLB_ACT_SILU_MUL, false>(g.x, u.x, 0.f, d.x, og.x, ou.x);
-        act_bwd_elem<TLB_ACT_SILU_MUL, false>(g.y, u.y, 0.f, d.y, og.y, ou.y);
-        act_bwd_elem<TLB_ACT_SILU_MUL, false>(g.z, u.z, 0.f, d.z, og.z, ou.z);
-        act_bwd_elem<TLB_ACT_SILU_MUL, false>(g.w, u.w, 0.f, d.w, og.w, ou.w);
+        act_bwd_elem_bf16<TLB_ACT_SILU_MUL>(g.x, u.x, d.x, og.x, ou.x);
+        act_bwd_elem_bf16<TLB_ACT_SILU_MUL>(g.y, u.y, d.y, og.y, ou.y);
+        act_bwd_elem_bf16<TLB_ACT_SILU_MUL>(g.z, u.z, d.z, og.z, ou.z);
+        act_bwd_elem_bf16<TLB_ACT_SILU_MUL>(g.w, u.w, d.w, og.w, ou.w);
     }
     p.dg[e / 4] = pack_bf16x4(og.x, og.y, og.z, og.w);
     p.du[e / 4] = pack_bf16x4(ou.x, ou.y, ou.z, ou.w);
@@ -157,10 +157,10 @@ __device__ __forceinline__ void act_block_t(const TcParams &p, int rbase, int co
         if (!ok[k]) continue;
         const float *a = blk + r * 33 + c4;
         float4 og, ou;
-        act_bwd_elem<ACT, false>(g[k].x, u[k].x, 0.f, p.alpha * a[0], og.x, ou.x);
-        act_bwd_elem<ACT, false>(g[k].y, u[k].y, 0.f, p.alpha * a[1], og.y, ou.y);
-        act_bwd_elem<ACT, false>(g[k].z, u[k].z, 0.f, p.alpha * a[2], og.z, ou.z);
-        act_bwd_elem<ACT, false>(g[k].w, u[k].w, 0.f, p.alpha * a[3], og.w, ou.w);
+        act_bwd_elem_bf16<ACT>(g[k].x, u[k].x, p.alpha * a[0], og.x, ou.x);
+        act_bwd_elem_bf16<ACT>(g[k].y, u[k].y, p.alpha * a[1], og.y, ou.y);
+        act_bwd_elem_bf16<ACT>(g[k].z, u[k].z, p.alpha * a[2], og.z, ou.z);
+        act_bwd_elem_bf16<ACT>(g[k].w, u[k].w, p.alpha * a[3], og.w, ou.w);
         const int64_t e = int64_t(rbase + r) * p.N + col0 + c4;
         p.dg[e / 4] = pack_bf16x4(og.x, og.y, og.z, og.w);
         p.du[e / 4] = pack_bf16x4(ou.x, ou.y, ou.z, ou.w);
