@@ -444,21 +444,19 @@ __global__ void __launch_bounds__(256) tc_fixup_kernel(const __grid_constant__ T
             const int64_t cta = PAIR ? 2 * int64_t(c) + h : c;
             return *reinterpret_cast<const float4 *>(p.partial + ((cta * 2 + slot) * kBM + lr) * BN + c4);
         };
-        // CTA order, four partial tiles' loads in flight at a time
+        // CTA order, up to eight partial tiles' loads in flight at a time
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        int c = en.y;
-        for (; c + 3 <= en.z; c += 4) {
-            float4 v[4];
+        for (int c = en.y; c <= en.z; c += 8) {
+            const int n = min(8, en.z - c + 1);
+            float4 v[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = part(c + u);
+            for (int u = 0; u < 8; ++u)
+                if (u < n) v[u] = part(c + u);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
-            }
-        }
-        for (; c <= en.z; ++c) {
-            const float4 v = part(c);
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            for (int u = 0; u < 8; ++u)
+                if (u < n) {
+                    acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
+                }
         }
         const int row = m0 + r, col = n0 + c4;
         if (row >= p.M || col >= p.N) continue;
