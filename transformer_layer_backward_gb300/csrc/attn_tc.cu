@@ -1639,7 +1639,7 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     char *base = static_cast<char *>(scratch);
     float *dCT = reinterpret_cast<float *>(base + w.dCT);
     float *Kt = reinterpret_cast<float *>(base + w.Kt), *Vr = reinterpret_cast<float *>(base + w.Vr);
-    const int nt_dc = int(ceil_div(a.S, kPrepT)) * (a.nh * HD / kPrepT);
+    const int nt_dc = a.dct_ready ? 0 : int(ceil_div(a.S, kPrepT)) * (a.nh * HD / kPrepT);   // dCtx^T tiles
     const int nt_kv = int(ceil_div(a.L, kPrepT)) * (a.nkv * HD / kPrepT);
     const int vec_kv = aligned16(a.k) && aligned16(a.v) && a.sh % 4 == 0 && a.sp % 4 == 0;
     float2 *rt = reinterpret_cast<float2 *>(base + w.rt);
@@ -1785,7 +1785,7 @@ int launch_attn_tc_rc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uin
     float *Kt = reinterpret_cast<float *>(base + w.Kt), *Vr = reinterpret_cast<float *>(base + w.Vr);
     float *Kr = reinterpret_cast<float *>(base + w.Kr);
     float2 *rt = reinterpret_cast<float2 *>(base + w.rt);
-    const int nt_dc = int(ceil_div(a.S, kPrepT)) * (a.nh * HD / kPrepT);
+    const int nt_dc = a.dct_ready ? 0 : int(ceil_div(a.S, kPrepT)) * (a.nh * HD / kPrepT);   // dCtx^T tiles
     const int nt_kv = int(ceil_div(a.L, kPrepT)) * (a.nkv * HD / kPrepT);
     const int nt_rt = a.rope ? int(ceil_div(int64_t(a.S) * (HD / 2), int64_t(1024))) : 0;
     const int vec_kv = aligned16(a.k) && aligned16(a.v) && a.sh % 4 == 0 && a.sp % 4 == 0;

@@ -71,6 +71,8 @@ struct TcParams {
     float alpha;
     float *out;                          // [M, N] fp32
     uint2 *obf;                          // mode 0: [M, N] bf16 copy of out (four per uint2), or null
+    float *out_t;                        // mode 0, not accumulating: tf32 copy, transposed (ld_t), or null
+    int64_t ld_t;
     int accumulate;
     float *partial;                      // [ctas][2][kBM * BN] fp32 partial tiles
     // epilogue: mode 0 writes out (+)= alpha acc; mode 1 treats alpha acc as dh and writes
@@ -113,6 +115,13 @@ __device__ __forceinline__ void emit4(const TcParams &p, int row, int col, float
         }
         *reinterpret_cast<float4 *>(p.out + e) = y;
         if (p.obf != nullptr) p.obf[e / 4] = pack_bf16x4(y.x, y.y, y.z, y.w);
+        if (p.out_t != nullptr) {
+            float *t = p.out_t + int64_t(col) * p.ld_t + row;
+            t[0] = __uint_as_float(to_tf32(y.x));
+            t[p.ld_t] = __uint_as_float(to_tf32(y.y));
+            t[2 * p.ld_t] = __uint_as_float(to_tf32(y.z));
+            t[3 * p.ld_t] = __uint_as_float(to_tf32(y.w));
+        }
         return;
     }
     const float4 g = ld_stream(reinterpret_cast<const float4 *>(p.gate + e));
@@ -200,6 +209,24 @@ __device__ __forceinline__ void out_block(const TcParams &p, int rbase, int col0
             const int64_t e = int64_t(rbase + r) * p.N + col0 + c4;
             *reinterpret_cast<float4 *>(p.out + e) = y;
             if (p.obf != nullptr) p.obf[e / 4] = pack_bf16x4(y.x, y.y, y.z, y.w);
+        }
+    }
+    if (p.out_t != nullptr) {
+        // the tf32 transposed copy (never accumulating: the value is alpha acc, as stored
+        // above): four columns per step, eight lanes per column, four rows per lane, so each
+        // column's 32 rows go out as 128 contiguous bytes.  Rows past M up to ld_t (a multiple
+        // of 4) are padding of the copy.
+        const int r4 = (lane & 7) * 4;
+        if (rbase + r4 < p.M) {
+#pragma unroll
+            for (int cg = 0; cg < 8; ++cg) {
+                const int c = cg * 4 + (lane >> 3);
+                if (col0 + c >= p.N) continue;
+                const float *a = blk + r4 * 33 + c;
+                *reinterpret_cast<float4 *>(p.out_t + int64_t(col0 + c) * p.ld_t + rbase + r4) =
+                    make_float4(__uint_as_float(to_tf32(p.alpha * a[0])), __uint_as_float(to_tf32(p.alpha * a[33])),
+                                __uint_as_float(to_tf32(p.alpha * a[66])), __uint_as_float(to_tf32(p.alpha * a[99])));
+            }
         }
     }
 }
@@ -631,7 +658,8 @@ bool tc_supported(int64_t M, int64_t N, int64_t K) {
 }
 
 int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, float *out, bool accumulate,
-            float *partial, uint32_t *status, cudaStream_t st, const TcActEpilogue *act, void *out_bf16) {
+            float *partial, uint32_t *status, cudaStream_t st, const TcActEpilogue *act, void *out_bf16,
+            float *out_t, int64_t ld_t) {
     TLB_REQUIRE(nseg >= 1 && nseg <= kMaxSeg, TLB_EINVAL, "tcgen05 GEMM: 1 to 3 K segments");
     int64_t K = 0;
     for (int i = 0; i < nseg; ++i) K += seg[i].K;
@@ -646,6 +674,9 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
                     "tcgen05 GEMM: output alignment");
     }
     TLB_REQUIRE(act == nullptr || out_bf16 == nullptr, TLB_EINVAL, "tcgen05 GEMM: bf16 copy of an activation epilogue");
+    TLB_REQUIRE(out_t == nullptr || (act == nullptr && !accumulate && ld_t >= M && ld_t % 4 == 0 && aligned16(out_t)),
+                TLB_EINVAL, "tcgen05 GEMM: transposed copy needs the plain, non-accumulating epilogue, ld_t >= M, "
+                            "ld_t %% 4 == 0 and 16-byte alignment");
     TcParams p;
     memset(&p, 0, sizeof(p));
     for (int i = 0; i < nseg; ++i) {
@@ -661,6 +692,8 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
     p.alpha = alpha;
     p.out = out;
     p.obf = static_cast<uint2 *>(out_bf16);
+    p.out_t = out_t;
+    p.ld_t = ld_t;
     p.accumulate = accumulate ? 1 : 0;
     p.partial = partial;
     if (act != nullptr) {

@@ -58,9 +58,11 @@ struct TcActEpilogue {
     void *dgate, *dup;                    // [M, N] bf16
 };
 // out_bf16 (optional, no activation epilogue): [M, N] bf16 copy of every value stored to out.
+// out_t (optional, no activation epilogue, not accumulating): tf32-rounded transposed copy,
+// out_t[c * ld_t + r] = tf32(out[r, c]) (the tensor-core attention's dCtx^T operand).
 int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, float *out, bool accumulate,
             float *partial, uint32_t *status, cudaStream_t st, const TcActEpilogue *act = nullptr,
-            void *out_bf16 = nullptr);
+            void *out_bf16 = nullptr, float *out_t = nullptr, int64_t ld_t = 0);
 // gated-activation backward writing bf16 dG, dU (rowwise.cu)
 int act_backward_bf16_launch(int act, const float *gate, const float *up, const float *silu_gate, const float *dh,
                              void *dgate, void *dup, int64_t n, cudaStream_t st);
@@ -80,6 +82,9 @@ struct AttnArgs {
     // k[j,kvh,:]> - lse[h,i]) on the visible keys, q [S, q_dim] the queries after RoPE.
     const float *q = nullptr;
     const float *lse = nullptr;   // [nh, S] logsumexp of each query row's scaled logits
+    // tensor-core kernels: the scratch already holds the tf32 dCtx^T ([q_dim][S rounded up to
+    // 4], at its start) that the O-projection product wrote beside dctx
+    int dct_ready = 0;
 };
 int attn_core_launch(const AttnArgs &a, float rope_base, cudaStream_t st);
 // Key gradient of the S newest cache rows (the keys of the call's own tokens), for the

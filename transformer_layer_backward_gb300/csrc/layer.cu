@@ -245,12 +245,18 @@ int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, co
     const LayerWs p = plan(c, S, L);
     const int64_t qd = int64_t(c.n_heads) * c.head_dim;
     float *dSub = ws_at<float>(ws, p.dSub);
+    const bool tc_attn = (attn_tc_route(c, S, L) && aligned16(d_qpre) && aligned16(d_v) && aligned16(a.attn)) ||
+                         (attn_tc_rc_route(c, S, L) && aligned16(d_qpre) && aligned16(d_v) && aligned16(a.q));
+    // without the sub-norm dSub is dCtx, and the product also writes the attention kernels'
+    // tf32 dCtx^T (the start of their scratch, rows of S rounded up to 4)
+    const bool dct = tc_attn && tc_route(c, S) && !(c.flags & TLB_SUB_NORM);
     // dSub = dR1 W_O^T
     if (tc_route(c, S)) {
         void *abf = ws_at<void>(ws, p.abf);
         if (!abf_dr1) TLB_TRY(tc_convert_bf16(dR1, abf, S * c.dim, st));
         const TcOperand o{abf, w.w_o.w, c.dim};
-        TLB_TRY(tc_gemm(&o, 1, S, qd, w.w_o.scale, dSub, false, ws_at<float>(ws, p.part), ws_at<uint32_t>(ws, 0), st));
+        TLB_TRY(tc_gemm(&o, 1, S, qd, w.w_o.scale, dSub, false, ws_at<float>(ws, p.part), ws_at<uint32_t>(ws, 0), st,
+                        nullptr, nullptr, dct ? ws_at<float>(ws, p.atc) : nullptr, (S + 3) & ~int64_t(3)));
     } else {
         TLB_TRY(linear_t_launch(c.wtype, w.w_o.w, w.w_o.scale, dR1, S, c.dim, qd, dSub, false, st));
     }
@@ -259,8 +265,8 @@ int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, co
         TLB_TRY(rmsnorm_backward_launch(a.ctx, w.gamma_sub_attn, dSub, dSub, S, qd, c.norm_eps, 0, st));
     AttnArgs g = attn_args(c, S, L, dSub, a, d_qpre, d_v);
     g.D = D;
-    if ((attn_tc_route(c, S, L) && aligned16(d_qpre) && aligned16(d_v) && aligned16(a.attn)) ||
-        (attn_tc_rc_route(c, S, L) && aligned16(d_qpre) && aligned16(d_v) && aligned16(a.q)))
+    g.dct_ready = dct ? 1 : 0;
+    if (tc_attn)
         TLB_TRY(attn_tc_launch(g, c.rope_base, ws_at<void>(ws, p.atc), ws_at<uint32_t>(ws, 0), st));
     else
         TLB_TRY(attn_core_launch(g, c.rope_base, st));
