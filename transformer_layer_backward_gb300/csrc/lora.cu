@@ -415,15 +415,34 @@ __global__ void __launch_bounds__(256) lora_gpass16_kernel(LoraSeqArgs a) {
 }
 
 // sum_{k < n} p[k * stride] in index order, eight loads in flight at a time.
+// sum of p[k stride], k = 0 .. n - 1, in index order, sixteen loads in flight at a time
+// (the tail batch included)
+__device__ __forceinline__ float ordered_sum16(const float *p, int n, int64_t stride) {
+    float acc = 0.f;
+    for (int k = 0; k < n; k += 16) {
+        const int m = min(16, n - k);
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j < m) v[j] = p[int64_t(k + j) * stride];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j < m) acc += v[j];
+    }
+    return acc;
+}
+
+// the same sum, B loads in flight at a time
+template <int B>
 __device__ __forceinline__ float ordered_sum(const float *p, int n, int64_t stride) {
     float acc = 0.f;
     int k = 0;
-    for (; k + 8 <= n; k += 8) {
-        float v[8];
+    for (; k + B <= n; k += B) {
+        float v[B];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = p[int64_t(k + j) * stride];
+        for (int j = 0; j < B; ++j) v[j] = p[int64_t(k + j) * stride];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc += v[j];
+        for (int j = 0; j < B; ++j) acc += v[j];
     }
     for (; k < n; ++k) acc += p[int64_t(k) * stride];
     return acc;
@@ -439,7 +458,7 @@ __global__ void __launch_bounds__(256) lora_gh_sum_kernel(LoraSeqArgs a) {
     }
     if (side >= a.nside || e >= n) return;
     const LoraSide &p = a.side[side];
-    p.gh[e] = p.s * ordered_sum(p.part_gh + e, p.n_ot, n);
+    p.gh[e] = p.s * ordered_sum16(p.part_gh + e, p.n_ot, n);
 }
 
 // Block (column tile of x, chunk of row tiles): one pass over its x tiles, staged two
@@ -595,12 +614,19 @@ __global__ void __launch_bounds__(256) lora_seq_adamw_kernel(LoraSeqArgs a, Adam
         const LoraSide &p = a.side[sd];
         const int64_t nA = int64_t(a.rank) * a.C, nB = int64_t(p.O) * a.rank;
         if (e < 0) break;
+        // the parameter and its moments are loaded before the partial sums, so that both
+        // rounds of loads are in flight together
         if (e < nA) {
-            const float g = ordered_sum(p.part_a + e, a.nrc_a, nA);
+            float w = 0.f, m = 0.f, v = 0.f;
+            if (step) {
+                w = p.l.a[e];
+                m = p.l.m_a[e];
+                v = p.l.v_a[e];
+            }
+            const float g = ordered_sum<8>(p.part_a + e, a.nrc_a, nA);
             if (p.l.grad_a) p.l.grad_a[e] = g;
             if (step) {
-                float m = p.l.m_a[e], v = p.l.v_a[e];
-                p.l.a[e] = adam_elem(p.l.a[e], g, m, v, ka);
+                p.l.a[e] = adam_elem(w, g, m, v, ka);
                 p.l.m_a[e] = m;
                 p.l.v_a[e] = v;
             }
@@ -608,11 +634,16 @@ __global__ void __launch_bounds__(256) lora_seq_adamw_kernel(LoraSeqArgs a, Adam
             e = -1;
         } else if (e < nA + nB) {
             const int64_t f = e - nA;
-            const float g = p.s * ordered_sum(p.part_b + f, a.nrc_b, nB);
+            float w = 0.f, m = 0.f, v = 0.f;
+            if (step) {
+                w = p.l.b[f];
+                m = p.l.m_b[f];
+                v = p.l.v_b[f];
+            }
+            const float g = p.s * ordered_sum<8>(p.part_b + f, a.nrc_b, nB);
             if (p.l.grad_b) p.l.grad_b[f] = g;
             if (step) {
-                float m = p.l.m_b[f], v = p.l.v_b[f];
-                p.l.b[f] = adam_elem(p.l.b[f], g, m, v, kb);
+                p.l.b[f] = adam_elem(w, g, m, v, kb);
                 p.l.m_b[f] = m;
                 p.l.v_b[f] = v;
             }
