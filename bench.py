@@ -60,7 +60,7 @@ def parse(argv=None):
                    help="decode: also time the layer inside a stack of this many layers (0: skip)")
     p.add_argument("--cases", default=None,
                    help="sweep: run only the cases whose 'kernel shape' label matches this regex")
-    p.add_argument("--workload", default="stack2048", choices=["decode", "seq512", "seq2048", "stack2048", "sweep", "tf32peak"])
+    p.add_argument("--workload", default="stack2048", choices=["decode", "seq512", "seq2048", "stack2048", "sweep", "tf32peak", "h2dpeak"])
     p.add_argument("--qk-norm", action="store_true",
                    help="layers with the per-head QK-norm on q (decode and sequence workloads)")
     p.add_argument("--recompute-p", action="store_true",
@@ -517,7 +517,9 @@ def seq_main(args, rank, world, local, dist):
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
     e2e = {"value": n_e2e * S * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "steps": n_e2e}
+           "steps": n_e2e, "h2d_gbs": h2d * n_e2e / e2e_s / 1e9,
+           "note": "copy-bound: the host link moves about 210 GB/s host to device on this machine "
+                   "(bench.py --workload h2dpeak, profiles/h2d_link.md)"}
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
@@ -852,6 +854,42 @@ def tf32peak_main(args, local):
                       "gpu": torch.cuda.get_device_name(local), "torch": torch.__version__, "clocks": clk}), flush=True)
 
 
+def h2dpeak_main(args, local):
+    """Host -> device bandwidth of this machine's link, the ceiling of every e2e figure: 1 GiB
+    from pinned host memory into device memory, split over 1, 2 and 4 copy streams, best of 4
+    each, CUDA events around the copies."""
+    import torch
+    torch.cuda.set_device(local)
+    n = 1 << 28                                   # floats: 1 GiB
+    h = torch.empty(n, pin_memory=True)
+    h.fill_(1.0)
+    d = torch.empty(n, device="cuda")
+    main = torch.cuda.current_stream()
+    out = {}
+    for ns in (1, 2, 4):
+        streams = [torch.cuda.Stream() for _ in range(ns)]
+        chunk = n // ns
+        best = 1e30
+        for _ in range(4):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            for k, st in enumerate(streams):
+                st.wait_event(e0)
+                with torch.cuda.stream(st):
+                    d[k * chunk:(k + 1) * chunk].copy_(h[k * chunk:(k + 1) * chunk], non_blocking=True)
+            for st in streams:
+                main.wait_stream(st)
+            e1.record(main)
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        out["%d stream%s" % (ns, "" if ns == 1 else "s")] = n * 4 / (best / 1e3) / 1e9
+    print(json.dumps({"h2d_gbs": max(out.values()), "by_streams": out,
+                      "how": "torch copy_ of 1 GiB from pinned host memory, non_blocking, split over the copy "
+                             "streams, best of 4, CUDA events", "gpu": torch.cuda.get_device_name(local),
+                      "torch": torch.__version__}), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -869,6 +907,9 @@ def main():
             dist.destroy_process_group()
         return
 
+    if args.workload == "h2dpeak":
+        h2dpeak_main(args, local)
+        return
     if args.workload == "tf32peak":
         tf32peak_main(args, local)
         return
