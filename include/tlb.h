@@ -333,9 +333,11 @@ int tlb_lora_grad_adamw(int64_t S, int32_t out_dim, int32_t in_dim, int32_t rank
  * [S, rank] rows gh, is a fixed 65536-float (256 KiB) array inside the library that
  * every GPU loading the library keeps until the process exits.
  *   - S * rank must not exceed 65536; larger calls fail with TLB_EINVAL.
- *   - It allocates and frees nothing.  The first call on each device looks up the
- *     array's device address with that device current; make that first call before
- *     any stream capture.
+ *   - It allocates and frees nothing.  Each call outside a stream capture looks up the
+ *     array's device address with its device current (so a device reset, which loads
+ *     the library's device code again, leaves no stale address); a call inside a capture
+ *     uses the address of the last call outside one.  So make one call on each device
+ *     before any stream capture, and again after a device reset.
  *   - All calls share the one array and it keeps the last call's contents (every call
  *     overwrites the rows it uses before reading them): calls that overlap on the GPU,
  *     on different streams, race and give wrong results.  Serialise them. */

@@ -30,14 +30,18 @@ std::mutex g_mu;
 float *g_gh_ptr[kMaxDevices] = {nullptr};
 
 // Device address of g_noalloc_gh on the current device.  In host code the array's
-// name is only a host-side stand-in, so the address is asked of the runtime once
-// per device, with that device current.
-int gh_address(float **out) {
+// name is only a host-side stand-in, so the address is asked of the runtime, with the
+// device current.  Outside a stream capture it is asked on every call, so that a device
+// reset (which loads the module again, possibly elsewhere) never leaves a stale address;
+// inside a capture the address of the last call outside one is used.
+int gh_address(cudaStream_t st, float **out) {
     int dev = 0;
     TLB_CUDA(cudaGetDevice(&dev));
     TLB_REQUIRE(dev >= 0 && dev < kMaxDevices, TLB_EUNSUPPORTED, "lora_grad_adamw_noalloc: device %d", dev);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    TLB_CUDA(cudaStreamIsCapturing(st, &cs));
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_gh_ptr[dev] == nullptr) {
+    if (cs == cudaStreamCaptureStatusNone || g_gh_ptr[dev] == nullptr) {
         void *p = nullptr;
         TLB_CUDA(cudaGetSymbolAddress(&p, g_noalloc_gh));
         g_gh_ptr[dev] = static_cast<float *>(p);
@@ -66,7 +70,7 @@ extern "C" int tlb_lora_grad_adamw_noalloc(int64_t S, int32_t out_dim, int32_t i
     TLB_REQUIRE(S == 0 || (G && h && x), TLB_EINVAL, "lora_grad_adamw_noalloc: NULL input");
     if (S == 0) return TLB_OK;
     float *gh = nullptr;
-    TLB_TRY(gh_address(&gh));
+    TLB_TRY(gh_address(as_stream(stream), &gh));
     // gh is written in full by the first kernel before anything reads it, so the
     // array needs no clearing between calls.
     return lora_launch(S, out_dim, in_dim, rank, alpha, G, h, x, *lora, *adam, sumsq, gh, as_stream(stream));
