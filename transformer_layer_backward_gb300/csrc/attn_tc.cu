@@ -1529,20 +1529,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_rc_kernel(const __
             __syncwarp();
             if (lane == 0) mbar_arrive(&efull[b]);
         }
+        constexpr int half = HD / 2, q4 = HD / 4, nck = q4 / 16;
+        // this row's (cos, sin) of its group's columns, loaded while the last MMAs run
+        float4 cs_all[nck][8];
+        {
+            const float4 *rt4 = reinterpret_cast<const float4 *>(p.rt + int64_t(row_ok ? i : 0) * half);
+#pragma unroll
+            for (int ck = 0; ck < nck; ++ck)
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    cs_all[ck][t] = p.rope ? rt4[(hf * q4 + 16 * ck) / 2 + t] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         if (ok && mbar_wait(&dfull, 0, p.status, 58u)) {
             tc_fence_after();
-            constexpr int half = HD / 2, q4 = HD / 4;
             float *out0 = p.dq + h * HD;
-            const float4 *rt4 = reinterpret_cast<const float4 *>(p.rt + int64_t(row_ok ? i : 0) * half);
             float *blk = reinterpret_cast<float *>(sm) + (warp - 2) * 32 * 33;
             const int c4 = (lane & 7) * 4, rl = lane >> 3;
-#pragma unroll 1
-            for (int c = hf * q4; c < (hf + 1) * q4; c += 16) {      // pairs (c, c + HD / 2)
-                float4 cs[8];
-                if (p.rope) {
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) cs[t] = rt4[c / 2 + t];
-                }
+            for (int ck = 0; ck < nck; ++ck) {                        // pairs (c, c + HD / 2)
+                const int c = hf * q4 + 16 * ck;
+                const float4 *cs = cs_all[ck];
                 uint32_t u1[16], u2[16];
                 tmem_ld16(tm + Ly::TQD + uint32_t(c) + lane_off, u1);
                 tmem_ld16(tm + Ly::TQD + uint32_t(c + half) + lane_off, u2);
