@@ -17,8 +17,9 @@
 //   warps 2..9  epilogue: tcgen05.ld 32x32b.x32 (two warps per 32 TMEM lanes = rows, each
 //               half of the columns); each 32 x 32 block turns in shared memory so that
 //               lanes run along columns; scale, optional accumulate into C, coalesced fp32
-//               (and optional bf16) stores, then release the accumulator, so one segment's
-//               epilogue overlaps the next one's MMAs
+//               stores (and an optional bf16 copy, or a tf32 transposed copy for the
+//               attention), then release the accumulator, so one segment's epilogue
+//               overlaps the next one's MMAs
 // Paired form (BN = 256, clusters of two CTAs on one TPC, cta_group::2): the pair owns a
 // 256 x 256 super-tile; each CTA loads its own 128 rows of A and its half (128 rows) of B
 // into its own ring, the even CTA issues tcgen05.mma.cta_group::2 (M = 256, N = 256), which
