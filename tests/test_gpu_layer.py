@@ -90,7 +90,10 @@ SEQ_RC_LONG = SEQ_CACHE.with_(name="seq_recompute_long", recompute_p=True, seq_l
 SEQ_LORA16 = SEQ_HD64.with_(name="seq_lora16", rank=16, lora_alpha=32.0, seq_len=300, cache_len=300)
 SEQ_LORA16_KV3 = SEQ_HD64.with_(name="seq_lora16_kv3", n_heads=6, n_kv_heads=3, rank=16, lora_alpha=32.0,
                                 seq_len=170, cache_len=170, adam_state="warm", step=6)
-CASES = {c.name: c for c in (SEQ_LORA16, SEQ_LORA16_KV3, SEQ_RC_LONG, TINY_RC, DEC_RC, MINI_SEQ_RC, SEQ_RC, SEQ_RC_CACHE, SEQ_RC_EXACT, TINY_RC_EXACT,
+# a wide hidden size with few query columns: the O-projection product [128, 512] x K 4096
+# runs stream-K with shared tiles, so the fixup writes the attention's tf32 dCtx^T copy
+SEQ_WIDE = SEQ_HD64.with_(name="seq_wide_wo_streamk", dim=4096, ffn_dim=1024, seq_len=128, cache_len=160)
+CASES = {c.name: c for c in (SEQ_WIDE, SEQ_LORA16, SEQ_LORA16_KV3, SEQ_RC_LONG, TINY_RC, DEC_RC, MINI_SEQ_RC, SEQ_RC, SEQ_RC_CACHE, SEQ_RC_EXACT, TINY_RC_EXACT,
                              DECODE_T2, DEC_T2, DEC_T2_EXACT,
                              TINY, TINY_WARM, DECODE, MINI_SEQ, SEQ512, DEC_F32, DEC_BF16, DEC_G8, DEC_HD256,
                              SEQ_HD64, SEQ_CACHE, SEQ_MHA, SEQ_ODD, TINY_QK, DEC_QK, SEQ_QK, SEQ_PRENORM,
@@ -211,7 +214,10 @@ def test_layer_backward(lib, case, persistent):
     lib.layer_backward(c, cfg.seq_len, cfg.cache_len, lib.layer_weights(c, t),
                        lib.layer_acts(c, t, cfg.kv_layout, cfg.cache_len), lib.lora(L, "q", grads),
                        lib.lora(L, "v", grads), adam, dh, ss, ws)
-    assert_route(cfg, lib.launch_names(n0))
+    names = lib.launch_names(n0)
+    assert_route(cfg, names)
+    if cfg is SEQ_WIDE:
+        assert "tcgen05 gemm fixup" in names, ("the stream-K fixup did not run", names)
     lib.workspace_status(ws)
     rl, ma = tol(cfg)
     rel = check("d_in", host(dh), ref["d_in"], rl, ma)[0]
