@@ -53,7 +53,9 @@ struct AttnTcParams {
     CUtensorMap dct;            // dCT  {S, hd, nh},  box {32, hd, 1}
     CUtensorMap pq;             // attn {L, S, nh},   box {32, 128, 1}   (dQ: 128 queries x 32 keys)
     CUtensorMap pv;             // attn {L, S, nh},   box {32, 32, 1}    (dV: 32 queries x 32 keys)
-    const float *dctx;          // dCtx [S, nh * hd]
+    const float *dctx;          // dCtx [S, nh * hd], or null: the dQ kernel reads dcT instead
+    const float *dcT;           // the tf32 dCtx^T [nh * hd][ld_ct] in the scratch
+    int ld_ct;
     float *dq;                  // [S, nh * hd]
     float *dv;                  // [S, nkv * hd], or per-head partial sums [nh / nkv][S, nkv * hd]
     int S, L, nh, nkv, pos0, causal, rope;
@@ -357,11 +359,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_dq_kernel(const __gri
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
         const int jlast = p.causal ? p.pos0 + i : p.L - 1;      // last visible key
         {   // this row's half of dCtx_h, rounded to tf32, into tensor memory: the A operand of T
-            const float4 *src = reinterpret_cast<const float4 *>(p.dctx + int64_t(row_ok ? i : 0) * (p.nh * HD) +
-                                                                 h * HD + hf * (HD / 2));
             float4 x[HD / 8];                    // every load in flight before the first store
+            if (p.dctx != nullptr) {
+                const float4 *src = reinterpret_cast<const float4 *>(p.dctx + int64_t(row_ok ? i : 0) * (p.nh * HD) +
+                                                                     h * HD + hf * (HD / 2));
 #pragma unroll
-            for (int k = 0; k < HD / 8; ++k) x[k] = row_ok ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k = 0; k < HD / 8; ++k) x[k] = row_ok ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+                // from the tf32 dCtx^T (already rounded; rounding again changes nothing): for
+                // each column the warp's lanes read 32 consecutive rows, 128 contiguous bytes
+                const float *src = p.dcT + int64_t(h * HD + hf * (HD / 2)) * p.ld_ct + (row_ok ? i : 0);
+#pragma unroll
+                for (int k = 0; k < HD / 8; ++k) {
+                    const float *c4 = src + int64_t(4 * k) * p.ld_ct;
+                    x[k] = row_ok ? make_float4(c4[0], c4[p.ld_ct], c4[2 * p.ld_ct], c4[3 * p.ld_ct])
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
 #pragma unroll
             for (int c = 0; c < HD / 2; c += 16) {
                 uint32_t v[16];
@@ -1690,6 +1704,8 @@ int launch_attn_tc(const AttnArgs &a, const RopeFreqs &fr, void *scratch, uint32
     const int G = a.nh / a.nkv;
     float *part = reinterpret_cast<float *>(base + w.part);
     p.dctx = a.dctx;
+    p.dcT = dCT;
+    p.ld_ct = int(w.S4);
     p.dq = a.dq;
     p.dv = G > 1 ? part : a.dv;
     p.S = a.S;
@@ -1908,6 +1924,8 @@ int attn_tc_launch(const AttnArgs &a, float rope_base, void *scratch, uint32_t *
     const bool rc = a.lse != nullptr;
     TLB_REQUIRE((rc ? aligned16(a.q) : aligned16(a.attn)) && aligned16(a.dq) && aligned16(a.dv) && aligned16(a.dctx),
                 TLB_EUNSUPPORTED, "attention (tcgen05): attn or q / dq / dv / dctx not 16-byte aligned");
+    TLB_REQUIRE(a.dctx != nullptr || (a.dct_ready && !rc), TLB_EINVAL,
+                "attention (tcgen05): no dctx needs the stored weights and a ready dCtx^T");
     RopeFreqs fr;
     rope_freqs(fr, a.hd, rope_base);
     if (rc)

@@ -114,7 +114,7 @@ __device__ __forceinline__ void emit4(const TcParams &p, int row, int col, float
             const float4 c = *reinterpret_cast<const float4 *>(p.out + e);
             y.x += c.x; y.y += c.y; y.z += c.z; y.w += c.w;
         }
-        *reinterpret_cast<float4 *>(p.out + e) = y;
+        if (p.out != nullptr) *reinterpret_cast<float4 *>(p.out + e) = y;
         if (p.obf != nullptr) p.obf[e / 4] = pack_bf16x4(y.x, y.y, y.z, y.w);
         if (p.out_t != nullptr) {
             float *t = p.out_t + int64_t(col) * p.ld_t + row;
@@ -189,7 +189,7 @@ __device__ __forceinline__ void out_block(const TcParams &p, int rbase, int col0
     const int c4 = (lane & 7) * 4, rl = lane >> 3;
     const bool col_ok = col0 + c4 < p.N;                  // N % 4 == 0: the quad is whole
 #pragma unroll 1
-    for (int k0 = 0; k0 < 8; k0 += 4) {                   // four loads of C in flight
+    for (int k0 = 0; k0 < 8 && p.out != nullptr; k0 += 4) {   // four loads of C in flight
         float4 c[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -673,6 +673,8 @@ int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, f
     } else {
         TLB_REQUIRE(aligned16(out) && (out_bf16 == nullptr || aligned16(out_bf16)), TLB_EUNSUPPORTED,
                     "tcgen05 GEMM: output alignment");
+        TLB_REQUIRE(out != nullptr || (out_t != nullptr && out_bf16 == nullptr), TLB_EINVAL,
+                    "tcgen05 GEMM: no output (out may be null only beside the transposed copy)");
     }
     TLB_REQUIRE(act == nullptr || out_bf16 == nullptr, TLB_EINVAL, "tcgen05 GEMM: bf16 copy of an activation epilogue");
     TLB_REQUIRE(out_t == nullptr || (act == nullptr && !accumulate && ld_t >= M && ld_t % 4 == 0 && aligned16(out_t)),

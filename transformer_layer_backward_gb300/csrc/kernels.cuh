@@ -59,7 +59,8 @@ struct TcActEpilogue {
 };
 // out_bf16 (optional, no activation epilogue): [M, N] bf16 copy of every value stored to out.
 // out_t (optional, no activation epilogue, not accumulating): tf32-rounded transposed copy,
-// out_t[c * ld_t + r] = tf32(out[r, c]) (the tensor-core attention's dCtx^T operand).
+// out_t[c * ld_t + r] = tf32(out[r, c]) (the tensor-core attention's dCtx^T operand); with
+// out_t, out may be null (only the copy is written).
 int tc_gemm(const TcOperand *seg, int nseg, int64_t M, int64_t N, float alpha, float *out, bool accumulate,
             float *partial, uint32_t *status, cudaStream_t st, const TcActEpilogue *act = nullptr,
             void *out_bf16 = nullptr, float *out_t = nullptr, int64_t ld_t = 0);
@@ -83,7 +84,8 @@ struct AttnArgs {
     const float *q = nullptr;
     const float *lse = nullptr;   // [nh, S] logsumexp of each query row's scaled logits
     // tensor-core kernels: the scratch already holds the tf32 dCtx^T ([q_dim][S rounded up to
-    // 4], at its start) that the O-projection product wrote beside dctx
+    // 4], at its start) that the O-projection product wrote (beside dctx; with dct_ready and
+    // the stored weights, dctx may be null and the kernels read only the transposed copy)
     int dct_ready = 0;
 };
 int attn_core_launch(const AttnArgs &a, float rope_base, cudaStream_t st);

@@ -250,13 +250,17 @@ int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, co
     // without the sub-norm dSub is dCtx, and the product also writes the attention kernels'
     // tf32 dCtx^T (the start of their scratch, rows of S rounded up to 4)
     const bool dct = tc_attn && tc_route(c, S) && !(c.flags & TLB_SUB_NORM);
+    // and on the stored-weight path without the exact input gradient nothing else reads dCtx
+    // by rows: the product writes only the transposed copy
+    const bool dct_only = dct && !(c.flags & TLB_RECOMPUTE_P) && !(c.flags & TLB_EXACT_DIN);
     // dSub = dR1 W_O^T
     if (tc_route(c, S)) {
         void *abf = ws_at<void>(ws, p.abf);
         if (!abf_dr1) TLB_TRY(tc_convert_bf16(dR1, abf, S * c.dim, st));
         const TcOperand o{abf, w.w_o.w, c.dim};
-        TLB_TRY(tc_gemm(&o, 1, S, qd, w.w_o.scale, dSub, false, ws_at<float>(ws, p.part), ws_at<uint32_t>(ws, 0), st,
-                        nullptr, nullptr, dct ? ws_at<float>(ws, p.atc) : nullptr, (S + 3) & ~int64_t(3)));
+        TLB_TRY(tc_gemm(&o, 1, S, qd, w.w_o.scale, dct_only ? nullptr : dSub, false, ws_at<float>(ws, p.part),
+                        ws_at<uint32_t>(ws, 0), st, nullptr, nullptr, dct ? ws_at<float>(ws, p.atc) : nullptr,
+                        (S + 3) & ~int64_t(3)));
     } else {
         TLB_TRY(linear_t_launch(c.wtype, w.w_o.w, w.w_o.scale, dR1, S, c.dim, qd, dSub, false, st));
     }
@@ -266,6 +270,7 @@ int attn_impl(const tlb_layer_cfg &c, int64_t S, int64_t L, const float *dR1, co
     AttnArgs g = attn_args(c, S, L, dSub, a, d_qpre, d_v);
     g.D = D;
     g.dct_ready = dct ? 1 : 0;
+    if (dct_only) g.dctx = nullptr;
     if (tc_attn)
         TLB_TRY(attn_tc_launch(g, c.rope_base, ws_at<void>(ws, p.atc), ws_at<uint32_t>(ws, 0), st));
     else
