@@ -1001,15 +1001,38 @@ __global__ void tf32_copy_kernel(const float4 *__restrict__ src, float4 *__restr
 
 // dV[jj, c] = sum over the group's heads g (in order) of part[g][jj, c]
 __global__ void attn_tc_dv_sum_kernel(const float4 *__restrict__ part, float4 *__restrict__ dv, int64_t n4, int G) {
+    constexpr int kMaxG = 8;                              // heads per KV head summed from registers
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n4; e += 2 * stride) {
-        const bool two = e + stride < n4;                 // two elements' loads in flight
-        float4 s0 = part[e], s1 = two ? part[e + stride] : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int g = 1; g < G; ++g) {
-            const float4 t0 = part[int64_t(g) * n4 + e];
-            const float4 t1 = two ? part[int64_t(g) * n4 + e + stride] : make_float4(0.f, 0.f, 0.f, 0.f);
-            s0.x += t0.x; s0.y += t0.y; s0.z += t0.z; s0.w += t0.w;
-            s1.x += t1.x; s1.y += t1.y; s1.z += t1.z; s1.w += t1.w;
+        const bool two = e + stride < n4;                 // two elements per thread
+        float4 s0, s1;
+        if (G <= kMaxG) {
+            // every head's partial of both elements in flight at once, then the sums in
+            // head order (the order the general loop below adds them in)
+            float4 t0[kMaxG], t1[kMaxG];
+#pragma unroll
+            for (int g = 0; g < kMaxG; ++g) {
+                t0[g] = g < G ? part[int64_t(g) * n4 + e] : z;
+                t1[g] = g < G && two ? part[int64_t(g) * n4 + e + stride] : z;
+            }
+            s0 = t0[0];
+            s1 = t1[0];
+#pragma unroll
+            for (int g = 1; g < kMaxG; ++g) {
+                if (g >= G) break;
+                s0.x += t0[g].x; s0.y += t0[g].y; s0.z += t0[g].z; s0.w += t0[g].w;
+                s1.x += t1[g].x; s1.y += t1[g].y; s1.z += t1[g].z; s1.w += t1[g].w;
+            }
+        } else {
+            s0 = part[e];
+            s1 = two ? part[e + stride] : z;
+            for (int g = 1; g < G; ++g) {
+                const float4 t0 = part[int64_t(g) * n4 + e];
+                const float4 t1 = two ? part[int64_t(g) * n4 + e + stride] : z;
+                s0.x += t0.x; s0.y += t0.y; s0.z += t0.z; s0.w += t0.w;
+                s1.x += t1.x; s1.y += t1.y; s1.z += t1.z; s1.w += t1.w;
+            }
         }
         dv[e] = s0;
         if (two) dv[e + stride] = s1;
