@@ -444,8 +444,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
         for (int g = s_consumed; g < s_issued; ++g) mbar_wait(&full[g % kStages], (g / kStages) & 1, nullptr, 0u);
     }
     __syncthreads();
-    // paired: neither CTA leaves or frees its tensor memory while the other's copies,
-    // commits or arrivals may still reach it
+    // paired: neither CTA leaves or frees its tensor memory while the other's commits or
+    // arrivals may still reach it.  (After an abort, which a wait that ran out has already
+    // reported, the bounded wait above covers the even CTA's own copies; the odd CTA's count
+    // on the even CTA's barrier and are not awaited separately.)
     if constexpr (PAIR) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
