@@ -1170,6 +1170,10 @@ def main():
                              "algorithmic_bytes": kern[dom][1],
                              "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else "fallback"},
                 "per_kernel": per_kernel, "per_kernel_timing": ktiming,
+                "per_kernel_note": "events recorded between the kernels serialise the programmatic launches, so "
+                                   "each kernel's time here includes the wait for its predecessor and its first "
+                                   "round of loads (about its time alone); in the live chain k2 spans about 11 us "
+                                   "(per-block globaltimer timeline, profiles/decode_kernels.md)",
                 "step_roofline": {"bytes_per_step": step_bytes, "achieved": step_bytes / (ms_max / args.steps / 1e3) / 1e9,
                                   "peak": hbm, "unit": "GB/s",
                                   "frac": step_bytes / (ms_max / args.steps / 1e3) / 1e9 / hbm},
