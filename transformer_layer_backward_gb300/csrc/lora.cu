@@ -414,7 +414,6 @@ __global__ void __launch_bounds__(256) lora_gpass16_kernel(LoraSeqArgs a) {
     }
 }
 
-// sum_{k < n} p[k * stride] in index order, eight loads in flight at a time.
 // sum of p[k stride], k = 0 .. n - 1, in index order, sixteen loads in flight at a time
 // (the tail batch included)
 __device__ __forceinline__ float ordered_sum16(const float *p, int n, int64_t stride) {
