@@ -347,9 +347,10 @@ int tlb_lora_grad_adamw_noalloc(int64_t S, int32_t out_dim, int32_t in_dim, int3
 
 /* One whole layer: FFN backward, attention backward, LoRA Q/V gradients and AdamW.
  * d_hidden [S, dim] in/out: dOut on entry, the gradient for the layer below on return
- * ([RS] grad_hidden): dR1, or with TLB_EXACT_DIN the exact gradient of the layer input.  sumsq (device double[2]) += {sum dA^2, sum dB^2} over both
- * adapters; the page's gradient norm over a stack is sqrt(sumsq[0]).  lora_q: A [r, dim],
- * B [q_dim, r]; lora_v: A [r, dim], B [kv_dim, r]. */
+ * ([RS] grad_hidden): dR1, or with TLB_EXACT_DIN the exact gradient of the layer input.
+ * sumsq (device double[2]) += {sum dA^2, sum dB^2} over both adapters; the page's
+ * gradient norm over a stack is sqrt(sumsq[0]).  lora_q: A [r, dim], B [q_dim, r];
+ * lora_v: A [r, dim], B [kv_dim, r]. */
 int tlb_layer_backward(const tlb_layer_cfg *cfg, int64_t S, int64_t L,
                        const tlb_layer_weights *w, const tlb_layer_acts *acts,
                        const tlb_lora *lora_q, const tlb_lora *lora_v,
