@@ -163,6 +163,38 @@ def test_attn_backward(lib, case):
     check("dV", host(dv), r2["dV"], rl, ma)
 
 
+# The cached weights carry the causal mask as zeros ([ATT] "Softmax Backward" reads them as
+# given), so the attention without the causal flag must give the same gradients.  The
+# tensor-core kernels then take every key tile of the cache for every query tile (no tile
+# is masked in place; a last tile past L is zero-filled by the copy): S = L = 512, a ragged
+# S = L = 200, and a cache longer than the sequence (L = 300, S = 96).
+@pytest.mark.parametrize("name", ["seq512", "seq_hd64", "seq_cache"])
+def test_attn_backward_without_causal_flag(lib, name):
+    import torch
+    from transformer_layer_backward_gb300 import _abi
+    cfg = CASES[name]
+    d = layer_inputs(cfg, layer=0, seed=0)
+    t = to_dev(d, cfg.wtype)
+    c = cfg_to_abi(lib, cfg)
+    c.flags &= ~_abi.CAUSAL
+    ws = lib.workspace(c, cfg.seq_len, cfg.cache_len)
+    w = lib.layer_weights(c, t)
+    a = lib.layer_acts(c, t, cfg.kv_layout, cfg.cache_len)
+    dr1_h = np.random.default_rng(11).standard_normal((cfg.seq_len, cfg.dim)).astype(np.float32)
+    dr1 = torch.from_numpy(dr1_h).cuda()
+    dq = torch.empty(cfg.seq_len, cfg.q_dim, device="cuda")
+    dv = torch.empty(cfg.seq_len, cfg.kv_dim, device="cuda")
+    n0 = lib.launch_count()
+    lib.attn_backward(c, cfg.seq_len, cfg.cache_len, dr1, w, a, dq, dv, ws)
+    names = lib.launch_names(n0)
+    for k in ("attn_tc_dq", "attn_tc_dv"):
+        assert k in names, ("%s did not run" % k, names)
+    r2 = OL.attn_backward(cfg, dict(d), dr1_h)
+    rl, ma = tol(cfg)
+    check("dQpre", host(dq), r2["dQpre"], rl, ma)
+    check("dV", host(dv), r2["dV"], rl, ma)
+
+
 def test_lora_grad_adamw(lib, case):
     import torch
     cfg, d, ref = case
