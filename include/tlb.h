@@ -265,8 +265,12 @@ int tlb_rope_backward(const float *dy, float *dx, int64_t rows, int32_t n_heads,
  *   dX[S, in_dim] (+)= scale * dY[S, out_dim] . W[in_dim, out_dim]^T
  * W in storage type wtype (TLB_W_*); accumulate = 1 adds into dX.  S = 1 runs a GEMV;
  * S > 1 a GEMM: for bf16 weights on the tcgen05 tensor cores (dY rounded to bf16, fp32
- * accumulation), otherwise on CUDA cores in fp32.  ws: zero-filled workspace of at least
- * tlb_linear_workspace_bytes() bytes (bf16 copy of dY and split-K partials). */
+ * accumulation), otherwise on CUDA cores in fp32.  The tensor-core GEMM needs out_dim % 8
+ * == 0, in_dim % 4 == 0, dY, W and dX 16-byte aligned and ws_bytes >=
+ * tlb_linear_workspace_bytes(); a bf16 call that misses one of these runs the CUDA-core
+ * GEMM instead (same result within bf16 rounding; tlb_launch_name shows which ran).
+ * ws: zero-filled workspace of at least tlb_linear_workspace_bytes() bytes (bf16 copy of
+ * dY and split-K partials). */
 size_t tlb_linear_workspace_bytes(int32_t wtype, int64_t S, int64_t out_dim, int64_t in_dim);
 int tlb_linear_backward(int32_t wtype, const void *W, float scale, const float *dY, int64_t S,
                         int64_t out_dim, int64_t in_dim, float *dX, int32_t accumulate, void *ws,
