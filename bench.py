@@ -557,7 +557,7 @@ def seq_layer_flops(cfg):
     pairs = S * (L - S) + S * (S + 1) // 2
     gemm = 2 * S * I * H + 2 * S * H * 2 * I + 2 * S * qd * H
     attn = 3 * 2 * pairs * cfg.head_dim * cfg.n_heads
-    lora = sum(3 * 2 * S * od * r for od in (qd, kvd)) + 2 * 2 * S * r * H
+    lora = sum(2 * 2 * S * od * r for od in (qd, kvd)) + 2 * 2 * S * r * H   # dB, gh per adapter; dA
     if cfg.exact_din:       # dK = dS^T q, the [dQpre | dK | dV] W^T product, the LoRA A paths
         gemm += 2 * S * H * (qd + 2 * kvd)
         attn += 2 * pairs * cfg.head_dim * cfg.n_heads
