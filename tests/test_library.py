@@ -136,3 +136,95 @@ def test_qk_norm_needs_its_inputs(lib):
     acts.q_raw = fake
     assert lib.tlb_layer_backward(*args) == A.TLB_EINVAL
     assert b"workspace" in lib.tlb_last_error()
+
+
+def test_linear_backward_host_side_errors(lib):
+    """tlb_linear_backward refuses unknown weight types, packed-ternary rows that are not
+    whole bytes, negative sizes, NULL operands and a short workspace before any device work."""
+    from transformer_layer_backward_gb300 import _abi as A
+    fake = C.c_void_p(256)                       # never dereferenced: the checks fail first
+
+    def call(wtype, S, out_dim, in_dim, W=fake, dY=fake, dX=fake, ws=None, ws_bytes=0):
+        return lib.tlb_linear_backward(wtype, W, 1.0, dY, S, out_dim, in_dim, dX, 0, ws, ws_bytes, None)
+
+    assert call(9, 4, 8, 8) == A.TLB_EINVAL
+    assert b"unknown weight type" in lib.tlb_last_error()
+    assert call(A.W_TERNARY_2B, 4, 6, 8) == A.TLB_EINVAL                   # rows of 6 two-bit codes
+    assert b"out_dim % 4" in lib.tlb_last_error()
+    assert call(A.W_F32, -1, 8, 8) == A.TLB_EINVAL
+    assert b"negative" in lib.tlb_last_error()
+    assert call(A.W_F32, 0, 8, 8, W=None, dY=None, dX=None) == A.TLB_OK    # no rows: a no-op
+    assert call(A.W_F32, 4, 8, 8, W=None) == A.TLB_EINVAL
+    assert b"null pointer" in lib.tlb_last_error()
+    assert lib.tlb_linear_workspace_bytes(A.W_F32, -1, 8, 8) == 0
+    need = lib.tlb_linear_workspace_bytes(A.W_BF16, 256, 512, 256)
+    assert need > lib.tlb_linear_workspace_bytes(A.W_F32, 256, 512, 256)   # bf16 copy of dY and partials
+    assert call(A.W_BF16, 256, 512, 256, ws=fake, ws_bytes=need - 1) == A.TLB_EINVAL
+    assert b"workspace" in lib.tlb_last_error()
+
+
+def test_lora_grad_adamw_host_side_errors(lib):
+    from transformer_layer_backward_gb300 import _abi as A
+    fake = C.c_void_p(256)
+    good = A.Lora(fake, fake, fake, fake, fake, fake, None, None)
+    adam = A.AdamwCfg(1e-4, 0.9, 0.999, 1e-8, 0.0, 16.0, 1)
+
+    def call(S, out_dim, in_dim, rank, lora=good, G=fake):
+        return lib.tlb_lora_grad_adamw(S, out_dim, in_dim, rank, 2.0 * rank, G, fake, fake, C.byref(lora),
+                                       C.byref(adam), None, None, 0, None)
+
+    assert call(8, 0, 16, 4) == A.TLB_EINVAL
+    assert b"bad sizes" in lib.tlb_last_error()
+    for rank in (0, 65):
+        assert call(8, 16, 16, rank) == A.TLB_EINVAL
+        assert b"rank" in lib.tlb_last_error()
+    assert call(8, 16, 16, 4, lora=A.Lora(fake, None, fake, fake, fake, fake, None, None)) == A.TLB_EINVAL
+    assert b"NULL pointer" in lib.tlb_last_error()
+    assert call(8, 16, 16, 4, G=None) == A.TLB_EINVAL
+    assert b"NULL input" in lib.tlb_last_error()
+    assert call(0, 16, 16, 4, G=None) == A.TLB_OK          # no tokens: no gradient and no step
+    assert call(8, 16, 16, 4) == A.TLB_EINVAL
+    assert b"workspace" in lib.tlb_last_error()
+
+
+def test_attention_inputs_of_each_mode_are_checked(lib):
+    """The exact input gradient, the recomputed attention and the cache bounds refuse
+    missing inputs before any device work; with them the call reaches the workspace check."""
+    from transformer_layer_backward_gb300 import _abi as A
+    fake = C.c_void_p(256)
+    adam = A.AdamwCfg(1e-4, 0.9, 0.999, 1e-8, 0.0, 16.0, 1)
+    lq = A.Lora(fake, fake, fake, fake, fake, fake, None, None)
+
+    def layer(flags, S=8, L=8, **fields):
+        cfg = A.LayerCfg(64, 256, 4, 2, 16, 4, 8.0, 1e4, 1e-6, 0.25, 0, 0, A.CAUSAL | flags)
+        w = A.LayerWeights(A.Weight(fake, 1.0), A.Weight(fake, 1.0), A.Weight(fake, 1.0), A.Weight(fake, 1.0))
+        acts = A.LayerActs(fake, fake, fake, None, None, None, None, fake, fake, 16, 32, fake, fake, fake)
+        for k, v in fields.items():
+            setattr(w if hasattr(w, k) and k.startswith(("w_", "gamma")) else acts, k, v)
+        return lib.tlb_layer_backward(C.byref(cfg), S, L, C.byref(w), C.byref(acts), C.byref(lq), C.byref(lq),
+                                      C.byref(adam), fake, fake, None, 0, None)
+
+    wqkv = dict(w_q=A.Weight(fake, 1.0), w_k=A.Weight(fake, 1.0), w_v=A.Weight(fake, 1.0))
+    assert layer(A.EXACT_DIN) == A.TLB_EINVAL
+    assert b"EXACT_DIN needs w_q, w_k and w_v" in lib.tlb_last_error()
+    assert layer(A.EXACT_DIN, **wqkv) == A.TLB_EINVAL
+    assert b"EXACT_DIN needs q" in lib.tlb_last_error()
+    assert layer(A.EXACT_DIN, q=fake, **wqkv) == A.TLB_EINVAL
+    assert b"workspace" in lib.tlb_last_error()
+    assert layer(A.EXACT_DIN | A.PRE_NORM, q=fake, r1=fake, gamma_ffn=fake, **wqkv) == A.TLB_EINVAL
+    assert b"EXACT_DIN with PRE_NORM needs x_in and gamma_attn" in lib.tlb_last_error()
+    assert layer(A.EXACT_DIN | A.QK_NORM, q=fake, q_raw=fake, gamma_q=fake, **wqkv) == A.TLB_EINVAL
+    assert b"EXACT_DIN with QK_NORM needs k_raw and gamma_k" in lib.tlb_last_error()
+
+    assert layer(A.RECOMPUTE_P, attn=None) == A.TLB_EINVAL
+    assert b"RECOMPUTE_P needs q and lse" in lib.tlb_last_error()
+    assert layer(A.RECOMPUTE_P, attn=None, q=fake, lse=fake) == A.TLB_EINVAL
+    assert b"workspace" in lib.tlb_last_error()
+    assert layer(0, attn=None) == A.TLB_EINVAL
+    assert b"attn pointer is NULL" in lib.tlb_last_error()
+
+    assert layer(0, S=9, L=8) == A.TLB_EINVAL
+    assert b"need 0 <= S <= L" in lib.tlb_last_error()
+    assert layer(0, S=1, L=1 << 24) == A.TLB_EUNSUPPORTED
+    assert layer(0, kv_stride_pos=8) == A.TLB_EINVAL
+    assert b"strides smaller than head_dim" in lib.tlb_last_error()
