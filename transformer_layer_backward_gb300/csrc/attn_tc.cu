@@ -4,6 +4,9 @@
 //
 //   attn_tc_prep  tf32-rounded copies laid out for TMA (32 x 32 tile transposes):
 //                   dCT [nh][hd][S4]   Kt [nkv][hd][L4]   Vr [nkv][L][hd]
+//                 and the RoPE (cos, sin) table of the S new positions.  dCT is skipped
+//                 when the O-projection product has written it from its epilogue; the
+//                 dQ kernel then loads its dCtx rows from dCT too.
 //   attn_tc_dq    CTA = (head h, 128 queries), 10 warps: TMA producer, MMA issuer, and
 //                 8 epilogue warps in two groups that take alternate key tiles (one query
 //                 row = one TMEM lane per thread).  dCtx_h sits in tensor memory as the A
