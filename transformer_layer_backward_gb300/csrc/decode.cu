@@ -4,9 +4,11 @@
 // from HBM once; the small vectors between the steps stay in L2.
 //
 //   k1  dF   = s_d W_down dOut                                   GEMV over I rows
-//   k2  dG, dU from dF (sub-norm RMSNorm backward + gated activation backward,
-//       recomputed per block in shared memory), then
+//   k2  dG, dU from dF (sub-norm RMSNorm backward + gated activation backward), then
 //       dN2  = s_g W_gate dG + s_u W_up dU                        GEMV over H rows
+//       (int8, bf16 and fp32 weights: column-stationary, each thread's dG, dU values in
+//       registers and the rows streamed past them; packed 2-bit weights: dG, dU
+//       recomputed per block into a shared-memory vector)
 //   k3  dR1  = dOut + RMSNorm_bwd(r1, g_ffn, dN2) (per block, shared memory), then
 //       dSub = s_o W_O dR1                                        GEMV over q_dim rows
 //   k4  per (KV head, key chunk), one pass over K and V: dCtx of the group's heads

@@ -16,6 +16,9 @@
 //       x pass   one read of each x tile gives the dA partials of every adapter;
 //       AdamW    sums the token-tile partials of dA and dB, applies the update.
 //     Every sum runs in a fixed order: the result does not depend on scheduling.
+//     Rank-16 adapters of a layer whose attention ran on the tensor cores take the
+//     tcgen05 G and x passes of lora_tc.cu over 128-token tiles instead; they write the
+//     same partial-sum layouts, so the gh sum and the AdamW kernel serve both.
 #include <algorithm>
 
 #include <mutex>
