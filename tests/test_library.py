@@ -228,3 +228,16 @@ def test_attention_inputs_of_each_mode_are_checked(lib):
     assert layer(0, S=1, L=1 << 24) == A.TLB_EUNSUPPORTED
     assert layer(0, kv_stride_pos=8) == A.TLB_EINVAL
     assert b"strides smaller than head_dim" in lib.tlb_last_error()
+
+
+def test_no_host_fallback_on_the_product_path(monkeypatch):
+    """The binding never computes on the host: CPU tensors are refused before any library
+    call, and a missing library is an error, not a fallback."""
+    import torch
+    from transformer_layer_backward_gb300 import _abi, api
+    x = torch.zeros(2, 4)
+    with pytest.raises(ValueError, match="CUDA"):
+        api.softmax_backward(x, x)
+    monkeypatch.setattr(_abi, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        _abi.load(os.path.join(ROOT, "no_such_dir", "libtlb.so"))
