@@ -299,6 +299,41 @@ def seq_kernel_flops(cfg, names):
     return out
 
 
+def seq_kernel_bytes(cfg, names):
+    """Algorithmic HBM bytes of the tensor-core attention kernels of one sequence layer,
+    by launch order (0 for the other kernels): what each must read and write once.  dQ
+    reads the weights of the visible (query, key) pairs, dCtx, K and V and writes dQpre;
+    dV reads the weights and dCtx and writes dV.  Both are bound by these bytes rather than
+    by their tf32 flops."""
+    S, L, qd, kvd = cfg.seq_len, cfg.cache_len, cfg.q_dim, cfg.kv_dim
+    pairs = S * (L - S) + S * (S + 1) // 2
+    P = 4 * cfg.n_heads * pairs
+    out = []
+    for nm in names:
+        if nm == "attn_tc_dq":
+            out.append(P + 4 * (S * qd + 2 * L * kvd + S * qd))
+        elif nm == "attn_tc_dv":
+            out.append(P + 4 * (S * qd + S * kvd))
+        else:
+            out.append(0)
+    return out
+
+
+def kernel_entries(names, ktime_ms, flops, nbytes, peak_of, hbm_gbs):
+    """The bench line's per-kernel entries: live time, and where known the algorithmic
+    flops against the peak of the operand type and the algorithmic bytes against HBM."""
+    out = []
+    for nm, t, (f, kind), b in zip(names, ktime_ms, flops, nbytes):
+        e = {"kernel": nm, "us": t * 1e3}
+        if f:
+            e.update({"flop": f, "TFLOP/s": f / (t / 1e3) / 1e12, "operands": kind,
+                      "frac": f / (t / 1e3) / 1e12 / peak_of[kind]})
+        if b:
+            e.update({"bytes": b, "GB/s": b / (t / 1e3) / 1e9, "hbm_frac": b / (t / 1e3) / 1e9 / hbm_gbs})
+        out.append(e)
+    return out
+
+
 def seq_workload_config(cfg, depth, world):
     """The config dict of a sequence workload: the same for both arms."""
     name = ("%d-layer stack backward, S = L = %d" % (depth, cfg.seq_len) if depth > 1 else
@@ -449,14 +484,8 @@ def seq_main(args, rank, world, local, dist):
     sms = torch.cuda.get_device_properties(local).multi_processor_count
     fp32_peak = sms * 128 * 2 * (pk["sm_max_mhz"] if pk else 2070.0) * 1e6 / 1e12
     peak_of = {"bf16": bf16_peak, "tf32": tf32, "fp32": fp32_peak}
-    per_kernel = []
-    for nm, t, (f, kind) in zip(names, ktime, fl):
-        e = {"kernel": nm, "us": t * 1e3}
-        if f:
-            pkk = peak_of[kind]
-            e.update({"flop": f, "TFLOP/s": f / (t / 1e3) / 1e12, "operands": kind,
-                      "frac": f / (t / 1e3) / 1e12 / pkk})
-        per_kernel.append(e)
+    per_kernel = kernel_entries(names, ktime, fl, seq_kernel_bytes(cfg, names[:nkern]), peak_of,
+                                pk["hbm_gbs"] if pk else 6800.0)
     dom = max((k for k in range(nkern) if fl[k][0]), key=lambda k: ktime[k])
     achieved = fl[dom][0] / (ktime[dom] / 1e3) / 1e12
     peak = peak_of[fl[dom][1]]

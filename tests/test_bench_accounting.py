@@ -67,3 +67,37 @@ def test_stack_step_is_36_layers():
                                           3 * 2 * (S * (S + 1) // 2) * cfg.head_dim * cfg.n_heads +
                                           2 * 2 * S * cfg.rank * (cfg.q_dim + cfg.kv_dim) +
                                           2 * 2 * S * cfg.rank * cfg.dim)
+
+
+def test_attention_kernel_bytes():
+    cfg = SMALL
+    S, L, qd, kvd = cfg.seq_len, cfg.cache_len, cfg.q_dim, cfg.kv_dim
+    weights = 4 * cfg.n_heads * visible_pairs(S, L)
+    got = bench.seq_kernel_bytes(cfg, ["tcgen05 gemm", "attn_tc_prep", "attn_tc_dq", "attn_tc_dv", "lora_tc_gpass"])
+    assert got == [0, 0, weights + 4 * (S * qd + L * kvd + L * kvd + S * qd), weights + 4 * (S * qd + S * kvd), 0]
+
+
+def test_per_kernel_entries_of_a_layer_line():
+    # the kernels of one S = L = 2048 layer call and live times of the same order as the
+    # bench line's; the weight products carry flops, the attention kernels flops and bytes
+    cfg = STACK2048.with_(n_layers=1)
+    names = ["to_bf16", "tcgen05 gemm", "tcgen05 gemm", "tcgen05 gemm fixup", "tcgen05 gemm", "attn_tc_prep",
+             "attn_tc_dq", "attn_tc_dv", "attn_tc_dv_sum", "lora_tc_gpass", "lora_gh_sum", "lora_tc_xpass",
+             "lora_seq_adamw"]
+    ms = [0.0082, 0.0891, 0.1219, 0.0096, 0.0399, 0.0146, 0.1184, 0.0654, 0.0102, 0.0194, 0.0070, 0.0141, 0.0090]
+    peak_of = {"bf16": 1750.0, "tf32": 921.0, "fp32": 80.0}
+    fl = bench.seq_kernel_flops(cfg, names)
+    kb = bench.seq_kernel_bytes(cfg, names)
+    e = bench.kernel_entries(names, ms, fl, kb, peak_of, 6702.2)
+    assert [x["kernel"] for x in e] == names
+    assert [x.get("operands") for x in e] == [None, "bf16", "bf16", None, "bf16", None, "tf32", "tf32", None,
+                                              None, None, None, None]
+    gate_up = e[2]
+    assert gate_up["flop"] == 2 * 2048 * 2560 * 2 * 9728
+    assert gate_up["frac"] == pytest.approx(gate_up["flop"] / 0.1219e-3 / 1e12 / 1750.0)
+    dq, dv = e[6], e[7]
+    assert dq["bytes"] == 4 * 32 * (2048 * 2049 // 2) + 4 * (2 * 2048 * 4096 + 2 * 2048 * 1024)
+    assert dq["hbm_frac"] == pytest.approx(dq["bytes"] / 0.1184e-3 / 1e9 / 6702.2)
+    assert 0.4 < dq["hbm_frac"] < 0.5 and 0.3 < dq["frac"] < 0.35      # bound by its bytes, not its flops
+    assert dv["bytes"] == 4 * 32 * (2048 * 2049 // 2) + 4 * (2048 * 4096 + 2048 * 1024)
+    assert "bytes" not in e[1] and "flop" not in e[0]
